@@ -1,0 +1,258 @@
+/*
+ * fp64 CPU oracle for the selective state-space scan.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or calls
+ * this file: only the tests, the package's smoke check and the benchmark's CPU
+ * baseline leg do.  It shares no code, header, table or constant with the CUDA
+ * library; the two meet only at the seeded input generator.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [Mamba-2 explainer] "Mamba-2：把状态空间模型和 Attention 统一到一个数学框架里"
+ *       section 背景问题: discrete recurrence h_t = Abar h_{t-1} + Bbar x_t, y_t = C h_t
+ *       section 核心思路 / 第一步: Delta_t = softplus(Linear(x_t)); Abar obtained from Delta
+ *       section 第二步: unrolled form y = (L o M) x with a lower-triangular M
+ *       section 关键技术点 1: semiseparable M, low-rank off-diagonal blocks
+ *   [SSM engineering article] "引言：Attention的天花板 ... State Space Model：序列建模的另一条路"
+ *       section 基本原理: y(t) = C h(t) + D x(t)
+ *   [Mamba paper digest] "论文解读：Mamba — 线性时间的序列建模革命"
+ *       section 五 Mamba块架构: SSM output multiplied by SiLU of the z branch
+ *   [Mamba / hybrid overview] "基础知识：Mamba 与混合 SSM 架构"
+ *       section 2 从 SSM 到 Selective SSM: h_t = A_t h_{t-1} + B_t x_t, y_t = C_t h_t
+ *
+ * Readings taken where the pages are silent (each is listed in the design notes):
+ *   - discretisation: Abar = exp(Delta * A) and Bbar = Delta * B (exponential decay,
+ *     Euler input term); the pages only say that Abar comes from Delta;
+ *   - initial state zero unless an initial state is passed;
+ *   - y_t reads the state after the update (so M[t,t] = C_t . Delta_t B_t);
+ *   - softplus(v) = ln(1 + e^v), evaluated as max(v,0) + log1p(exp(-|v|)), with the
+ *     optional dt_bias added before the softplus;
+ *   - out = (C.h + D x) * SiLU(z) with SiLU(z) = z / (1 + e^-z);
+ *   - B and C are shared by groups: channel group g = head / (nheads / ngroups).
+ *
+ * Layouts (row-major, token-major, all float64 here):
+ *   x, z, out      (batch, seqlen, nheads, headdim)   -- DIAG: headdim == 1
+ *   dt             (batch, seqlen, nheads)
+ *   A              DIAG: (nheads, dstate)             SSD: (nheads,)
+ *   B, C           (batch, seqlen, ngroups, dstate)
+ *   D, dt_bias     (nheads,)                          nullable
+ *   initial_state, final_state (batch, nheads, headdim, dstate), nullable
+ *
+ * Parity status: pinned (brute-force semiseparable matrix, closed-form LTI responses,
+ * masked linear attention at A = 0, hand-worked golden values, invariants).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_MODE_DIAG 0
+#define ORACLE_MODE_SSD 1
+
+/* softplus(v) = ln(1 + e^v), overflow-free form. */
+static double oracle_softplus(double v) { return fmax(v, 0.0) + log1p(exp(-fabs(v))); }
+
+/* SiLU(z) = z * sigmoid(z). */
+static double oracle_silu(double z) { return z / (1.0 + exp(-z)); }
+
+typedef struct {
+    int mode;
+    int64_t batch, seqlen, nheads, headdim, dstate, ngroups;
+    const double *x, *dt, *A, *B, *C, *D, *z, *dt_bias, *initial_state;
+    double *out, *final_state;
+} oracle_problem;
+
+static int oracle_check(const oracle_problem* p) {
+    if (!p->x || !p->dt || !p->A || !p->B || !p->C || !p->out) return 1;
+    if (p->batch < 0 || p->seqlen < 0 || p->nheads <= 0 || p->headdim <= 0 || p->dstate <= 0 ||
+        p->ngroups <= 0)
+        return 2;
+    if (p->nheads % p->ngroups != 0) return 2;
+    if (p->mode == ORACLE_MODE_DIAG && p->headdim != 1) return 2;
+    if (p->mode != ORACLE_MODE_DIAG && p->mode != ORACLE_MODE_SSD) return 2;
+    return 0;
+}
+
+/* Decay coefficient A for channel head h and state index n. */
+static double oracle_acoef(const oracle_problem* p, int64_t h, int64_t n) {
+    return p->mode == ORACLE_MODE_DIAG ? p->A[h * p->dstate + n] : p->A[h];
+}
+
+/* Plain sequential recurrence for one channel (b, h, q); q indexes headdim. */
+static void oracle_channel_sequential(const oracle_problem* p, int64_t b, int64_t h, int64_t q,
+                                      double* state) {
+    const int64_t T = p->seqlen, H = p->nheads, P = p->headdim, N = p->dstate, G = p->ngroups;
+    const int64_t g = h / (H / G);
+    const int64_t sidx = ((b * H + h) * P + q) * N;
+    for (int64_t n = 0; n < N; ++n) state[n] = p->initial_state ? p->initial_state[sidx + n] : 0.0;
+    for (int64_t t = 0; t < T; ++t) {
+        const int64_t bt = b * T + t;
+        const double v = p->dt[bt * H + h] + (p->dt_bias ? p->dt_bias[h] : 0.0);
+        const double delta = oracle_softplus(v);
+        const int64_t xi = (bt * H + h) * P + q;
+        const double xv = p->x[xi];
+        const double* Bt = p->B + (bt * G + g) * N;
+        const double* Ct = p->C + (bt * G + g) * N;
+        double y = 0.0;
+        for (int64_t n = 0; n < N; ++n) {
+            const double abar = exp(delta * oracle_acoef(p, h, n));
+            state[n] = abar * state[n] + delta * Bt[n] * xv;
+            y += Ct[n] * state[n];
+        }
+        if (p->D) y += p->D[h] * xv;
+        if (p->z) y *= oracle_silu(p->z[xi]);
+        p->out[xi] = y;
+    }
+    if (p->final_state)
+        for (int64_t n = 0; n < N; ++n) p->final_state[sidx + n] = state[n];
+}
+
+/*
+ * Chunked evaluation of the same operator, following the semiseparable block
+ * structure ([Mamba-2 explainer] 第二步 and 关键技术点 1): inside a chunk of Q steps
+ * the diagonal block is summed directly,
+ *     y_t += sum_{s<=t} C_t[n] exp(A_n (S_t - S_s)) B_s[n] Delta_s x_s,
+ * with S the in-chunk inclusive cumulative sum of Delta, and the off-diagonal
+ * blocks enter through the state carried across the chunk boundary,
+ *     y_t += C_t[n] exp(A_n S_t) h_prev[n],
+ *     h_next[n] = exp(A_n S_last) h_prev[n] + sum_s exp(A_n (S_last - S_s)) B_s[n] Delta_s x_s.
+ * A different summation order from the sequential recurrence, used to pin that
+ * the result does not depend on the chunk length.
+ */
+static void oracle_channel_chunked(const oracle_problem* p, int64_t b, int64_t h, int64_t q,
+                                   int64_t Q, double* state, double* scratch) {
+    const int64_t T = p->seqlen, H = p->nheads, P = p->headdim, N = p->dstate, G = p->ngroups;
+    const int64_t g = h / (H / G);
+    const int64_t sidx = ((b * H + h) * P + q) * N;
+    double* delta = scratch;     /* Q */
+    double* cum = scratch + Q;   /* Q */
+    double* hnext = scratch + 2 * Q; /* N */
+    for (int64_t n = 0; n < N; ++n) state[n] = p->initial_state ? p->initial_state[sidx + n] : 0.0;
+    for (int64_t c0 = 0; c0 < T; c0 += Q) {
+        const int64_t len = (T - c0 < Q) ? (T - c0) : Q;
+        double run = 0.0;
+        for (int64_t i = 0; i < len; ++i) {
+            const int64_t bt = b * T + c0 + i;
+            delta[i] = oracle_softplus(p->dt[bt * H + h] + (p->dt_bias ? p->dt_bias[h] : 0.0));
+            run += delta[i];
+            cum[i] = run;
+        }
+        for (int64_t i = 0; i < len; ++i) {
+            const int64_t bt = b * T + c0 + i;
+            const double* Ct = p->C + (bt * G + g) * N;
+            double y = 0.0;
+            for (int64_t n = 0; n < N; ++n) {
+                const double an = oracle_acoef(p, h, n);
+                double acc = exp(an * cum[i]) * state[n];
+                for (int64_t s = 0; s <= i; ++s) {
+                    const int64_t bs = b * T + c0 + s;
+                    const double* Bs = p->B + (bs * G + g) * N;
+                    const double xs = p->x[(bs * H + h) * P + q];
+                    acc += exp(an * (cum[i] - cum[s])) * Bs[n] * delta[s] * xs;
+                }
+                y += Ct[n] * acc;
+            }
+            const int64_t xi = (bt * H + h) * P + q;
+            if (p->D) y += p->D[h] * p->x[xi];
+            if (p->z) y *= oracle_silu(p->z[xi]);
+            p->out[xi] = y;
+        }
+        for (int64_t n = 0; n < N; ++n) {
+            const double an = oracle_acoef(p, h, n);
+            double acc = exp(an * cum[len - 1]) * state[n];
+            for (int64_t s = 0; s < len; ++s) {
+                const int64_t bs = b * T + c0 + s;
+                const double* Bs = p->B + (bs * G + g) * N;
+                const double xs = p->x[(bs * H + h) * P + q];
+                acc += exp(an * (cum[len - 1] - cum[s])) * Bs[n] * delta[s] * xs;
+            }
+            hnext[n] = acc;
+        }
+        for (int64_t n = 0; n < N; ++n) state[n] = hnext[n];
+    }
+    if (p->final_state)
+        for (int64_t n = 0; n < N; ++n) p->final_state[sidx + n] = state[n];
+}
+
+static int oracle_run(const oracle_problem* p, int64_t chunk, const int64_t* sel, int64_t nsel,
+                      int nthreads) {
+    int rc = oracle_check(p);
+    if (rc) return rc;
+    const int64_t H = p->nheads, P = p->headdim, N = p->dstate;
+    const int64_t nchan = p->batch * H * P;
+    const int64_t count = sel ? nsel : nchan;
+    if (sel)
+        for (int64_t i = 0; i < nsel; ++i)
+            if (sel[i] < 0 || sel[i] >= nchan) return 2;
+    const int64_t Q = chunk > 0 ? chunk : 1;
+    int failed = 0;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel
+#endif
+    {
+        double* state = (double*)malloc(sizeof(double) * (size_t)(N + 2 * Q + N));
+        if (!state) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            failed = 1;
+        }
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int64_t i = 0; i < count; ++i) {
+            if (!state) continue;
+            const int64_t ch = sel ? sel[i] : i;
+            const int64_t b = ch / (H * P), h = (ch / P) % H, q = ch % P;
+            if (chunk > 0)
+                oracle_channel_chunked(p, b, h, q, Q, state, state + N);
+            else
+                oracle_channel_sequential(p, b, h, q, state);
+        }
+        free(state);
+    }
+    return failed ? 6 : 0;
+}
+
+/*
+ * Exported entry points (called through ctypes by the tests and the benchmark's
+ * CPU leg).  Return 0 on success, 1 for a missing required pointer, 2 for a bad
+ * shape or selection, 6 when a per-thread buffer cannot be allocated.
+ *
+ * sel / nsel: optional list of flat channel indices b*H*P + h*P + q to evaluate;
+ * outputs of channels not listed are left untouched.  nthreads <= 0 keeps the
+ * OpenMP default.
+ */
+int oracle_scan(int mode, int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
+                int64_t dstate, int64_t ngroups, const double* x, const double* dt,
+                const double* A, const double* B, const double* C, const double* D,
+                const double* z, const double* dt_bias, const double* initial_state,
+                double* out, double* final_state, const int64_t* sel, int64_t nsel,
+                int nthreads) {
+    oracle_problem p = {mode, batch, seqlen, nheads, headdim, dstate, ngroups, x, dt, A, B, C,
+                        D, z, dt_bias, initial_state, out, final_state};
+    return oracle_run(&p, 0, sel, nsel, nthreads);
+}
+
+int oracle_scan_chunked(int mode, int64_t batch, int64_t seqlen, int64_t nheads,
+                        int64_t headdim, int64_t dstate, int64_t ngroups, int64_t chunk,
+                        const double* x, const double* dt, const double* A, const double* B,
+                        const double* C, const double* D, const double* z,
+                        const double* dt_bias, const double* initial_state, double* out,
+                        double* final_state, const int64_t* sel, int64_t nsel, int nthreads) {
+    if (chunk <= 0) return 2;
+    oracle_problem p = {mode, batch, seqlen, nheads, headdim, dstate, ngroups, x, dt, A, B, C,
+                        D, z, dt_bias, initial_state, out, final_state};
+    return oracle_run(&p, chunk, sel, nsel, nthreads);
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
