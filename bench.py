@@ -1,0 +1,400 @@
+#!/usr/bin/env python3
+"""Benchmark of the B300 selective-scan library.
+
+One step = one ``ssm_scan_fwd`` call (the whole hot path: softplus discretisation,
+decay and input terms, the scan, skip term, gate, store) over one batch of the
+workload's synthetic inputs, which are resident in HBM before timing starts.  L2
+is flushed (a 256 MB write) before every timed step; each step is bracketed by CUDA
+events on the stream the library launches on.
+
+Prints ONE JSON line (rank 0).  Under torchrun every rank runs the same workload
+on its own GPU with no collective on the data path (weak scaling); ``value`` is the
+total token-channels of all ranks divided by the slowest rank's time.
+
+``--impl reference`` times the fp64 CPU oracle instead (host cores, rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "SSM scan Gtoken·ch/s and % of HBM / tensor roofline, 1 B300, vs CPU oracle"
+UNIT = "Gtoken·ch/s"
+L2_FLUSH_BYTES = 256 << 20
+
+DESCRIPTIONS = {
+    "c0": "Mamba-1 selective scan (diagonal A), fp32, batch 1 x L 256 x d_inner 64, N 16, D=1",
+    "c1": "Mamba-1 block scan (diagonal A), bf16 in / fp32 state, batch 8 x L 1024 x d_inner 512, "
+          "N 16, dt_bias, D, SiLU(z) gate",
+    "c2": "Mamba-1 scan at 3B-layer width, bf16 in / fp32 state, batch 4 x L 8192 x d_inner 5120, "
+          "N 16, dt_bias, D, SiLU(z) gate, final_state",
+    "c3": "Mamba-2 SSD scan (scalar A per head), bf16, batch 4 x L 8192, 64 heads x 64, N 128, "
+          "1 group, chunk 256, D",
+    "c4": "Mamba-2 SSD long sequence, bf16, batch 1 x L 131072, 32 heads x 64, N 256, 1 group, "
+          "chunk 256, D, final_state",
+}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="c1", choices=sorted(DESCRIPTIONS))
+    ap.add_argument("--chunk", type=int, default=None, help="override the workload's chunk")
+    ap.add_argument("--quick", action="store_true",
+                    help="skip the clock soak, CPU baseline and end-to-end legs (profiling runs)")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle baseline sample")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------- helpers
+
+def algorithmic_bytes(w) -> int:
+    """Bytes the method must move: inputs, outputs, parameters, final state."""
+    E = 2 if w.dtype == "bf16" else 4
+    b, T, H, P, N, G = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups
+    per_tok_ch = (2 + (1 if w.gate else 0)) * E + E  # x, z?, out  (+dt below)
+    nbytes = b * T * H * P * per_tok_ch
+    nbytes += b * T * H * E                      # dt: per channel (diag) or per head (ssd)
+    nbytes += 2 * b * T * G * N * E              # B, C
+    nbytes += (H * N if w.mode == "diag" else H) * 4   # A
+    nbytes += H * 4 * ((1 if w.d_skip != "none" else 0) + (1 if w.dt_bias else 0))
+    if w.final_state:
+        nbytes += b * H * P * N * 4
+    return int(nbytes)
+
+
+def algorithmic_flops(w) -> float:
+    """Tensor-core FLOPs of the SSD chunk form (dense tiles, causal half of Q x Q terms)."""
+    if w.mode != "ssd":
+        return 0.0
+    Q = w.chunk or 256
+    nchunks = math.ceil(w.seqlen / Q)
+    per_chunk_group = Q * Q * w.dstate               # causal half of 2 Q^2 N (C B^T)
+    per_chunk_head = Q * Q * w.headdim + 2 * Q * w.headdim * w.dstate * 2
+    return float(w.batch * nchunks * (w.ngroups * per_chunk_group + w.nheads * per_chunk_head))
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason sampling in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.strip().split(",") for r in self.file.read().splitlines() if r.strip()]
+        self.file.close()
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        return dist, world, rank, local
+    return None, 1, 0, local
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, value: float) -> float:
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------- CPU oracle
+
+def oracle_sample(w, inp, seconds: float, max_reps: int = 1000):
+    """Time the oracle on whole channels of the workload until ``seconds`` pass.
+    Returns (token-channels processed, elapsed seconds, threads, description)."""
+    import oracle
+    nch = w.batch * w.d_inner
+    per_channel = w.seqlen
+    # pick a channel block sized to ~1 s per call
+    t0 = time.perf_counter()
+    probe = np.arange(min(nch, 64))
+    oracle.scan(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
+                inp["dt_bias"], select=probe)
+    dt_probe = max(time.perf_counter() - t0, 1e-4)
+    per_call = int(min(nch, max(64, probe.size * 1.0 / dt_probe)))
+    done, elapsed, reps = 0, 0.0, 0
+    rng = np.random.default_rng(0)
+    while elapsed < seconds and reps < max_reps:
+        sel = np.sort(rng.choice(nch, per_call, replace=False)) if per_call < nch else np.arange(nch)
+        t0 = time.perf_counter()
+        oracle.scan(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
+                    inp["dt_bias"], select=sel)
+        elapsed += time.perf_counter() - t0
+        done += sel.size * per_channel
+        reps += 1
+    desc = (f"{reps} oracle calls of {per_call} whole channels (of {nch}) x L {w.seqlen}, "
+            f"fp64, OpenMP over channels")
+    return done, elapsed, oracle.max_threads(), desc
+
+
+# ---------------------------------------------------------------------------- arms
+
+def host_inputs(w):
+    from selective_state_space_143_b300.inputs import make_inputs
+    return make_inputs(w)
+
+
+def run_reference(args, w):
+    dist, world, rank, _ = dist_setup()
+    if rank != 0:
+        barrier(dist)
+        return 0
+    inp = host_inputs(w)
+    import oracle
+    nch = w.batch * w.d_inner
+    # per step: a bounded sample of whole channels (about 1 s of CPU work)
+    done_probe, el_probe, threads, _ = oracle_sample(w, inp, seconds=0.5, max_reps=1)
+    per_sec = done_probe / el_probe / w.seqlen  # channels per second
+    per_step = int(max(1, min(nch, per_sec * 1.0)))
+    rng = np.random.default_rng(1)
+    times, units = [], 0
+    for i in range(args.warmup + args.steps):
+        sel = np.sort(rng.choice(nch, per_step, replace=False))
+        t0 = time.perf_counter()
+        oracle.scan(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
+                    inp["dt_bias"], select=sel)
+        el = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(el)
+            units += per_step * w.seqlen
+    total = sum(times)
+    value = units / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{w.name}: {DESCRIPTIONS[w.name]}",
+                   "sample_per_step": f"{per_step} of {nch} whole channels"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{per_step} whole channels x L {w.seqlen} per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    barrier(dist)
+    return 0
+
+
+def run_ours(args, w):
+    import selective_state_space_143_b300 as ssm
+    dist, world, rank, local = dist_setup()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (there is no CPU path)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    chunk = w.chunk if args.chunk is None else args.chunk
+    inp = host_inputs(w)
+    d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+    out = torch.empty_like(d["x"])
+    st_shape = (w.batch, w.nheads, w.dstate) if w.mode == "diag" else (w.batch, w.nheads, w.headdim, w.dstate)
+    fs = torch.empty(st_shape, device=dev, dtype=torch.float32) if w.final_state else None
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        ssm.scan_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["z"], d["dt_bias"],
+                     out=out, final_state=fs, chunk=chunk, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    if not args.quick:
+        clocks.start()
+        # keep the GPU busy for about a second so that the clock samples see load
+        t_end = time.perf_counter() + 1.0
+        while time.perf_counter() < t_end:
+            for _ in range(50):
+                step()
+            torch.cuda.synchronize()
+
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    barrier(dist)
+    torch.cuda.synchronize()
+    n0 = ssm.launch_count()
+    for i in range(K):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    launches = ssm.launch_count() - n0
+    barrier(dist)
+    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms_step = max_over_ranks(dist, sum(ms) / K)
+    clk = clocks.stop() if not args.quick else {"sm_mhz": None, "sm_max_mhz": None,
+                                               "reasons": ["not sampled (--quick)"]}
+
+    units = w.token_channels * world
+    value = units / (ms_step * 1e-3) / 1e9
+
+    # ---- roofline of the call (all its kernels) against the measured peaks
+    peaks, peak_kind = measured_peaks()
+    nbytes = algorithmic_bytes(w)
+    hbm_gbs = nbytes / (ms_step * 1e-3) / 1e9
+    roof = {"bound": "hbm", "achieved": hbm_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": hbm_gbs / peaks["hbm_gbs"], "traffic": None,
+            "kernel": "ssm_scan_fwd (all kernels of one call)",
+            "algorithmic_bytes_per_launch": nbytes, "peak_source": peak_kind}
+    if w.mode == "ssd":
+        fl = algorithmic_flops(w)
+        roof["tensor_tflops"] = fl / (ms_step * 1e-3) / 1e12
+        roof["tensor_frac"] = roof["tensor_tflops"] / peaks["bf16_tflops"]
+
+    # ---- end to end through the public API from pinned host buffers
+    e2e = None
+    cpu = None
+    if not args.quick:
+        host = {k: (None if v is None else v.pin_memory()) for k, v in inp.items()}
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        fs_h = torch.empty(st_shape, dtype=torch.float32).pin_memory() if fs is not None else None
+        h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+        d2h = out_h.numel() * out_h.element_size() + (fs_h.numel() * 4 if fs_h is not None else 0)
+
+        def e2e_step():
+            dd = {k: (None if v is None else v.to(dev, non_blocking=True)) for k, v in host.items()}
+            o = ssm.scan_fwd(dd["x"], dd["dt"], dd["A"], dd["B"], dd["C"], dd["D"], dd["z"],
+                             dd["dt_bias"], final_state=None if fs is None else torch.empty_like(fs),
+                             chunk=chunk, stream=stream)
+            if fs is not None:
+                o, f = o
+                fs_h.copy_(f, non_blocking=True)
+            out_h.copy_(o, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        barrier(dist)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(K):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1) / K)
+        e2e = {"value": units / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+        if rank == 0:
+            done, el, threads, desc = oracle_sample(w, inp, args.cpu_seconds)
+            cpu = {"value": done / el / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
+                   "sample": desc, "seconds": el}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": f"{w.name}: {DESCRIPTIONS[w.name]}",
+                       "l2": "flushed before every timed step (256 MB write)",
+                       "chunk": chunk, "parallelism": f"replicas x{world} (independent batches)"},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
+            "gpu_launches": int(launches),
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    from selective_state_space_143_b300.inputs import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,133 @@
+/*
+ * ssm_scan.h -- C ABI of the B300 selective state-space scan library (libssmscan.so).
+ *
+ * The operation (cited by web-page title and section):
+ *   "Mamba-2：把状态空间模型和 Attention 统一到一个数学框架里", 背景问题 / 第一步:
+ *       h_t = Abar_t h_{t-1} + Bbar_t x_t,  y_t = C_t h_t,  Delta_t = softplus(.),
+ *       Abar from Delta (selective, input-dependent parameters);
+ *   "引言：Attention的天花板" (SSM engineering article), 基本原理: y = C h + D x;
+ *   "论文解读：Mamba — 线性时间的序列建模革命", 五 Mamba块架构: y * SiLU(z);
+ *   "Mamba-2 ..." explainer, 第二步 / 关键技术点 1-3: with A scalar per head the same
+ *       operator is y = (L o M) x with a semiseparable M, evaluated in chunks by
+ *       matrix multiplications (the SSD form).
+ * Discretisation: Abar = exp(Delta * A), Bbar = Delta * B, with
+ *   Delta = softplus(dt + dt_bias) = ln(1 + exp(dt + dt_bias)).
+ * Per channel c (SSD: c = (head h, p), A_c = A_h, Delta_c = Delta_h), group g:
+ *   h_t[n] = exp(Delta_t A[c,n]) h_{t-1}[n] + Delta_t B_t[g,n] x_t[c]
+ *   out_t[c] = (sum_n C_t[g,n] h_t[n] + D[c] x_t[c]) * SiLU(z_t[c])
+ * with h_{-1} = 0, D and the gate optional.  final_state = h_{T-1}.
+ *
+ * Layouts: row-major, contiguous, token-major (channels innermost).
+ *   mode DIAG (Mamba-1, A per channel and state):
+ *     x, z, out : (batch, seqlen, nheads)        nheads = d_inner, headdim must be 1
+ *     dt        : (batch, seqlen, nheads)
+ *     A         : (nheads, dstate) fp32
+ *     D, dt_bias: (nheads,) fp32
+ *     final_state: (batch, nheads, dstate) fp32
+ *   mode SSD (Mamba-2, scalar A per head):
+ *     x, z, out : (batch, seqlen, nheads, headdim)
+ *     dt        : (batch, seqlen, nheads)
+ *     A, D, dt_bias: (nheads,) fp32
+ *     final_state: (batch, nheads, headdim, dstate) fp32
+ *   both: B, C : (batch, seqlen, ngroups, dstate); head h reads group h / (nheads/ngroups).
+ *   x, dt, B, C, z and out share the element type `dtype` (fp32 or bf16; bf16 output
+ *   is rounded to nearest even).  State and accumulation are fp32.
+ *
+ * Ownership: every pointer is device memory owned by the caller; the library keeps
+ * no reference after the call returns.  Calls are asynchronous on `stream`; results
+ * are valid after the caller synchronises with it.  Kernel faults surface at that
+ * synchronisation, not in the return value.
+ *
+ * Errors: every argument is checked on the host before any work is queued; on an
+ * error nothing is launched and the status says why (see ssm_strerror).  There is
+ * no CPU fallback: without a usable CUDA device the call returns SSM_ERR_CUDA.
+ */
+#ifndef SSM_SCAN_H
+#define SSM_SCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SSM_OK = 0,
+    SSM_ERR_NULL = 1,        /* a required pointer is NULL                          */
+    SSM_ERR_SHAPE = 2,       /* a size is out of range or inconsistent              */
+    SSM_ERR_DTYPE = 3,       /* unknown mode or dtype                                */
+    SSM_ERR_ALIGN = 4,       /* a pointer or a row is not 16-byte aligned            */
+    SSM_ERR_UNSUPPORTED = 5, /* valid but unsupported (dstate too large, flags != 0) */
+    SSM_ERR_ALLOC = 6,       /* workspace allocation failed or workspace too small   */
+    SSM_ERR_CUDA = 7,        /* a CUDA call failed (launch error, no device)         */
+    SSM_ERR_TIMEOUT = 8      /* reserved: a bounded device-side wait ran out         */
+} ssm_status;
+
+typedef enum { SSM_MODE_DIAG = 0, SSM_MODE_SSD = 1 } ssm_mode;
+typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
+
+typedef struct ssm_shape {
+    int32_t mode;     /* ssm_mode                                                        */
+    int32_t dtype;    /* ssm_dtype of x, dt, B, C, z, out                                */
+    int64_t batch;    /* >= 0                                                            */
+    int64_t seqlen;   /* >= 0                                                            */
+    int64_t nheads;   /* DIAG: d_inner; SSD: heads; >= 1                                 */
+    int64_t headdim;  /* DIAG: 1; SSD: channels per head, 1..256                         */
+    int64_t dstate;   /* N: DIAG 1..64; SSD 1..256                                       */
+    int64_t ngroups;  /* >= 1, divides nheads                                            */
+    int64_t chunk;    /* 0 = default.  DIAG: time-segment length (multiple of 64) used to
+                         split the sequence across thread blocks; SSD: chunk length Q
+                         (multiple of 16, <= 256).  Results agree within rounding for any
+                         valid value.                                                    */
+    uint32_t flags;   /* reserved, must be 0                                             */
+} ssm_shape;
+
+/* A cudaStream_t passed as an opaque handle (NULL = the legacy default stream). */
+typedef struct CUstream_st* ssm_stream_t;
+
+/*
+ * Forward scan.  x, dt, A, B, C and out are required; D, z, dt_bias and final_state
+ * may be NULL (no skip term, no gate, no bias, no final state written).
+ * Alignment: every non-NULL pointer 16-byte aligned, and the innermost row of x/z/out
+ * (DIAG: nheads elements; SSD: nheads*headdim elements) and of B/C (ngroups*dstate)
+ * a multiple of 16 bytes.
+ * Workspace: when the chosen schedule needs device scratch (see
+ * ssm_scan_workspace_size) this call takes it from the stream-ordered allocator
+ * (cudaMallocAsync / cudaFreeAsync on `stream`); SSM_ERR_ALLOC if that fails.
+ * Returns an ssm_status.
+ */
+int ssm_scan_fwd(const void* x, const void* dt, const float* A, const void* B, const void* C,
+                 const float* D, const void* z, const float* dt_bias, void* out,
+                 float* final_state, const ssm_shape* shape, ssm_stream_t stream);
+
+/* Bytes of device scratch the call needs for `shape` (0 when none; (size_t)-1 when the
+ * shape is invalid).  Depends only on the shape. */
+size_t ssm_scan_workspace_size(const ssm_shape* shape);
+
+/*
+ * As ssm_scan_fwd, with caller-provided scratch: `workspace` (device, 256-byte aligned)
+ * of at least ssm_scan_workspace_size(shape) bytes; it may be NULL when that size is 0.
+ * The workspace must not be used by anything else until the call's work on `stream`
+ * has finished.  SSM_ERR_ALLOC if it is too small.
+ */
+int ssm_scan_fwd_ws(const void* x, const void* dt, const float* A, const void* B, const void* C,
+                    const float* D, const void* z, const float* dt_bias, void* out,
+                    float* final_state, const ssm_shape* shape, void* workspace,
+                    size_t workspace_bytes, ssm_stream_t stream);
+
+/* Static, NUL-terminated description of a status code (never NULL). */
+const char* ssm_strerror(int status);
+
+/* Number of kernels this library has launched in the calling process so far.  Used to
+ * count launches inside a timed region.  Thread-safe. */
+uint64_t ssm_kernel_launch_count(void);
+
+/* Library ABI version: (major << 16) | minor. */
+int ssm_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSM_SCAN_H */

@@ -1,1 +1,143 @@
-"""B300-native selective state-space scan (Mamba-1 diagonal form and Mamba-2 SSD form)."""
+"""B300-native selective state-space scan (Mamba-1 diagonal form and Mamba-2 SSD form).
+
+Python binding of libssmscan.so.  Every step of the scan runs in the library's CUDA
+kernels; this module only checks tensor metadata and passes device pointers and the
+current CUDA stream through the C ABI (include/ssm_scan.h).  PyTorch provides device
+memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import SsmError, ssm_shape
+
+__all__ = ["scan_fwd", "workspace_size", "make_shape", "launch_count", "SsmError", "ssm_shape"]
+
+_DTYPES = {torch.float32: _lib.SSM_F32, torch.bfloat16: _lib.SSM_BF16}
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def make_shape(x: torch.Tensor, A: torch.Tensor, B: torch.Tensor, chunk: int = 0) -> ssm_shape:
+    """Build the ``ssm_shape`` descriptor from tensor shapes.
+
+    DIAG (Mamba-1): x (b, T, D), A (D, N).  SSD (Mamba-2): x (b, T, H, P), A (H,).
+    B: (b, T, N) or (b, T, G, N).
+    """
+    if x.dtype not in _DTYPES:
+        raise TypeError(f"x must be float32 or bfloat16, got {x.dtype}")
+    s = ssm_shape()
+    s.dtype = _DTYPES[x.dtype]
+    if A.dim() == 2:
+        if x.dim() != 3:
+            raise ValueError("diagonal mode: x must be (batch, seqlen, d_inner)")
+        s.mode = _lib.SSM_MODE_DIAG
+        s.batch, s.seqlen, s.nheads = x.shape
+        s.headdim = 1
+    elif A.dim() == 1:
+        if x.dim() != 4:
+            raise ValueError("SSD mode: x must be (batch, seqlen, nheads, headdim)")
+        s.mode = _lib.SSM_MODE_SSD
+        s.batch, s.seqlen, s.nheads, s.headdim = x.shape
+    else:
+        raise ValueError("A must be 2-D (d_inner, dstate) or 1-D (nheads,)")
+    if B.dim() == 3:
+        s.ngroups, s.dstate = 1, B.shape[2]
+    elif B.dim() == 4:
+        s.ngroups, s.dstate = B.shape[2], B.shape[3]
+    else:
+        raise ValueError("B must be (batch, seqlen, dstate) or (batch, seqlen, ngroups, dstate)")
+    s.chunk = int(chunk)
+    s.flags = 0
+    return s
+
+
+def _check(name, t, shape, dtype, device):
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def workspace_size(x, A, B, chunk: int = 0) -> int:
+    """Device scratch bytes ``scan_fwd`` needs for these shapes (0 when none)."""
+    s = make_shape(x, A, B, chunk)
+    n = _lib.load().ssm_scan_workspace_size(ctypes.byref(s))
+    if n == ctypes.c_size_t(-1).value:
+        raise SsmError(_lib.SSM_ERR_SHAPE, "ssm_scan_workspace_size")
+    return int(n)
+
+
+def scan_fwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, *, out=None, final_state=None,
+             return_final_state: bool = False, chunk: int = 0, workspace=None, stream=None):
+    """Selective scan forward on the GPU.
+
+    out_t = (C_t . h_t + D x_t) * SiLU(z_t),  h_t = exp(Delta_t A) h_{t-1} + Delta_t B_t x_t,
+    Delta_t = softplus(dt_t + dt_bias).  Shapes as in ``make_shape``; dt is (b, T, D) for
+    the diagonal mode and (b, T, H) for SSD; D and dt_bias are (D,) / (H,) float32.
+
+    Returns ``out``, or ``(out, final_state)`` when ``return_final_state`` is set or a
+    ``final_state`` tensor is passed.  Runs asynchronously on ``stream`` (default: the
+    current torch stream).  ``workspace``: optional uint8 CUDA tensor of at least
+    ``workspace_size`` bytes; otherwise the library draws scratch from the stream-ordered
+    allocator.
+    """
+    s = make_shape(x, A, B, chunk)
+    dev = x.device
+    if dev.type != "cuda":
+        raise ValueError("scan_fwd runs on CUDA tensors only")
+    b, T, H, P, N, G = s.batch, s.seqlen, s.nheads, s.headdim, s.dstate, s.ngroups
+    diag = s.mode == _lib.SSM_MODE_DIAG
+    _check("x", x, x.shape, x.dtype, dev)
+    _check("dt", dt, (b, T, H), x.dtype, dev)
+    _check("A", A, (H, N) if diag else (H,), torch.float32, dev)
+    _check("B", B, B.shape, x.dtype, dev)
+    _check("C", C, B.shape, x.dtype, dev)
+    _check("D", D, (H,), torch.float32, dev)
+    _check("z", z, x.shape, x.dtype, dev)
+    _check("dt_bias", dt_bias, (H,), torch.float32, dev)
+    if out is None:
+        out = torch.empty_like(x)
+    _check("out", out, x.shape, x.dtype, dev)
+    want_state = return_final_state or final_state is not None
+    st_shape = (b, H, N) if diag else (b, H, P, N)
+    if want_state and final_state is None:
+        final_state = torch.empty(st_shape, device=dev, dtype=torch.float32)
+    _check("final_state", final_state, st_shape, torch.float32, dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    handle = ctypes.c_void_p(stream.cuda_stream)
+    lib = _lib.load()
+    with torch.cuda.device(dev):
+        if workspace is None:
+            rc = lib.ssm_scan_fwd(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                                  _ptr(dt_bias), _ptr(out), _ptr(final_state), ctypes.byref(s),
+                                  handle)
+        else:
+            if workspace.device != dev:
+                raise ValueError("workspace must be on x's device")
+            rc = lib.ssm_scan_fwd_ws(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                     _ptr(z), _ptr(dt_bias), _ptr(out), _ptr(final_state),
+                                     ctypes.byref(s), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), handle)
+    if rc != _lib.SSM_OK:
+        raise SsmError(rc, "ssm_scan_fwd")
+    return (out, final_state) if want_state else out
+
+
+def launch_count() -> int:
+    """Kernels launched by libssmscan.so in this process so far."""
+    return _lib.launch_count()

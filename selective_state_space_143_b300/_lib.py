@@ -1,0 +1,96 @@
+"""ctypes view of libssmscan.so (the C ABI declared in include/ssm_scan.h).
+
+Argument marshalling only: no arithmetic of the scan happens in Python.  The
+library must be present (or buildable with nvcc); there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+SSM_OK = 0
+SSM_ERR_NULL = 1
+SSM_ERR_SHAPE = 2
+SSM_ERR_DTYPE = 3
+SSM_ERR_ALIGN = 4
+SSM_ERR_UNSUPPORTED = 5
+SSM_ERR_ALLOC = 6
+SSM_ERR_CUDA = 7
+SSM_ERR_TIMEOUT = 8
+
+SSM_MODE_DIAG = 0
+SSM_MODE_SSD = 1
+SSM_F32 = 0
+SSM_BF16 = 1
+
+# Every function declared in include/ssm_scan.h.
+EXPORTED = ("ssm_scan_fwd", "ssm_scan_fwd_ws", "ssm_scan_workspace_size", "ssm_strerror",
+            "ssm_kernel_launch_count", "ssm_abi_version")
+
+
+class ssm_shape(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int32), ("dtype", ctypes.c_int32), ("batch", ctypes.c_int64),
+                ("seqlen", ctypes.c_int64), ("nheads", ctypes.c_int64), ("headdim", ctypes.c_int64),
+                ("dstate", ctypes.c_int64), ("ngroups", ctypes.c_int64), ("chunk", ctypes.c_int64),
+                ("flags", ctypes.c_uint32)]
+
+
+class SsmError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {strerror(status)} (status {status})")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def path() -> str:
+    return _build.OUT
+
+
+def load() -> ctypes.CDLL:
+    """Load (building first if the sources are newer) and declare the C ABI."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not _build.up_to_date():
+            try:
+                _build.build()
+            except Exception as exc:  # no nvcc or a compile error: fail loudly
+                if not os.path.exists(_build.OUT):
+                    raise RuntimeError(
+                        "libssmscan.so is missing and could not be built "
+                        f"({exc}); run `python -m selective_state_space_143_b300.build`") from exc
+        lib = ctypes.CDLL(_build.OUT)
+        vp = ctypes.c_void_p
+        fp = ctypes.POINTER(ctypes.c_float)
+        sp = ctypes.POINTER(ssm_shape)
+        lib.ssm_scan_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sp, vp]
+        lib.ssm_scan_fwd.restype = ctypes.c_int
+        lib.ssm_scan_fwd_ws.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sp, vp,
+                                        ctypes.c_size_t, vp]
+        lib.ssm_scan_fwd_ws.restype = ctypes.c_int
+        lib.ssm_scan_workspace_size.argtypes = [sp]
+        lib.ssm_scan_workspace_size.restype = ctypes.c_size_t
+        lib.ssm_strerror.argtypes = [ctypes.c_int]
+        lib.ssm_strerror.restype = ctypes.c_char_p
+        lib.ssm_kernel_launch_count.argtypes = []
+        lib.ssm_kernel_launch_count.restype = ctypes.c_uint64
+        lib.ssm_abi_version.argtypes = []
+        lib.ssm_abi_version.restype = ctypes.c_int
+        del fp
+        _lib = lib
+        return lib
+
+
+def strerror(status: int) -> str:
+    return load().ssm_strerror(int(status)).decode()
+
+
+def launch_count() -> int:
+    return int(load().ssm_kernel_launch_count())

@@ -1,0 +1,378 @@
+// Mamba-2 / SSD selective scan: scalar A per head, evaluated chunk by chunk.
+//
+// With A scalar per head the scan operator is y = (L o M) x with a semiseparable M
+// ("Mamba-2：把状态空间模型和 Attention 统一到一个数学框架里", 第二步 and
+// 关键技术点 1-3).  Its diagonal blocks (one chunk of Q steps) are dense and are
+// computed directly; its off-diagonal blocks are low rank and pass through the state
+// carried between chunks.  With s_t the in-chunk inclusive cumulative sum of
+// Delta_t * A_h:
+//   Y_diag[t, :] = sum_{s<=t} exp(s_t - s_s) (C_t . B_s) Delta_s x_s[:]
+//   S_c          = sum_s exp(s_last - s_s) Delta_s x_s[:] B_s^T           (P x N)
+//   h_c          = exp(s_last) h_{c-1} + S_c                             (chunk carry)
+//   Y_off[t, :]  = exp(s_t) h_{c-1} C_t
+//   out          = (Y_diag + Y_off + D x) * SiLU(z)
+//
+// This file holds the CUDA-core implementation, three kernels:
+//   ssd_chunk_state  : Delta, cumulative decay sums and the local chunk states S_c
+//   ssd_state_pass   : sequential carry over chunks, h_{c-1} stored per chunk, final state
+//   ssd_chunk_scan   : Y_diag + Y_off + skip + gate for each chunk
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "ssm_device.cuh"
+#include "ssm_internal.h"
+
+namespace ssm {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kTile = 64;   // P-tile, N-tile and row tile
+constexpr int kSub = 32;    // inner time sub-tile
+
+struct SsdArgs {
+    const char* x;
+    const char* dt;
+    const char* z;
+    const char* B;
+    const char* C;
+    const float* A;
+    const float* D;
+    const float* dt_bias;
+    const float* init;  // (b, H, P, N) or null
+    char* out;
+    float* final_state;
+    float* dl;      // (b, H, nchunks, Q) Delta
+    float* cum;     // (b, H, nchunks, Q) inclusive cumsum of Delta*A_h within the chunk
+    float* states;  // (b, nchunks, H, P, N)
+    int64_t T, H, P, N, G, Q, nchunks;
+};
+
+template <typename T>
+__device__ __forceinline__ float ld(const char* base, int64_t idx) {
+    return to_f32<T>(reinterpret_cast<const T*>(base)[idx]);
+}
+
+// Delta and the inclusive cumulative sum of Delta * A_h over one chunk, into smem.
+template <typename T>
+__device__ void chunk_delta_cumsum(const SsdArgs& a, int64_t b, int64_t h, int64_t c,
+                                   float* s_dl, float* s_cum, float* s_warp) {
+    const int tid = threadIdx.x;
+    const int64_t t0 = c * a.Q;
+    const int len = (int)min(a.Q, a.T - t0);
+    float dA = 0.0f;
+    if (tid < len) {
+        const float v = ld<T>(a.dt, (b * a.T + t0 + tid) * a.H + h) + (a.dt_bias ? a.dt_bias[h] : 0.0f);
+        const float de = softplus(v);
+        s_dl[tid] = de;
+        dA = de * a.A[h];
+    } else if (tid < a.Q) {
+        s_dl[tid] = 0.0f;
+    }
+    // block inclusive scan of dA (blockDim == 256 >= Q)
+    const int lane = tid & 31, warp = tid >> 5;
+    float v = dA;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
+    }
+    if (lane == 31) s_warp[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        float w = lane < kThreads / 32 ? s_warp[lane] : 0.0f;
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            const float u = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += u;
+        }
+        if (lane < kThreads / 32) s_warp[lane] = w;
+    }
+    __syncthreads();
+    if (warp > 0) v += s_warp[warp - 1];
+    if (tid < a.Q) s_cum[tid] = v;  // rows past the end repeat the last sum
+    __syncthreads();
+}
+
+// grid: (nchunks, H * nP * nN, b)
+template <typename T>
+__global__ void __launch_bounds__(kThreads) ssd_chunk_state(const SsdArgs a) {
+    __shared__ float s_dl[256], s_cum[256], s_warp[8], s_w[kSub];
+    __shared__ float s_x[kSub][kTile + 1];
+    __shared__ float s_b[kSub][kTile + 1];
+    const int64_t c = blockIdx.x, b = blockIdx.z;
+    const int nP = (int)((a.P + kTile - 1) / kTile), nN = (int)((a.N + kTile - 1) / kTile);
+    const int64_t h = blockIdx.y / (nP * nN);
+    const int pt = (blockIdx.y / nN) % nP, nt = blockIdx.y % nN;
+    const int64_t g = h / (a.H / a.G);
+    chunk_delta_cumsum<T>(a, b, h, c, s_dl, s_cum, s_warp);
+    const int tid = threadIdx.x;
+    const int64_t t0 = c * a.Q;
+    const int len = (int)min(a.Q, a.T - t0);
+    if (pt == 0 && nt == 0 && tid < a.Q) {
+        const int64_t o = ((b * a.H + h) * a.nchunks + c) * a.Q + tid;
+        a.dl[o] = s_dl[tid];
+        a.cum[o] = s_cum[tid];
+    }
+    const float last = s_cum[len - 1];
+    const int pi = (tid / 16) * 4, nj = (tid % 16) * 4;
+    float acc[4][4] = {};
+    for (int s0 = 0; s0 < len; s0 += kSub) {
+        __syncthreads();
+        for (int i = tid; i < kSub * kTile; i += kThreads) {
+            const int r = i / kTile, q = i % kTile;
+            const int64_t t = t0 + s0 + r;
+            const int64_t p = (int64_t)pt * kTile + q, n = (int64_t)nt * kTile + q;
+            const bool rok = s0 + r < len;
+            s_x[r][q] = (rok && p < a.P) ? ld<T>(a.x, ((b * a.T + t) * a.H + h) * a.P + p) : 0.0f;
+            s_b[r][q] = (rok && n < a.N) ? ld<T>(a.B, ((b * a.T + t) * a.G + g) * a.N + n) : 0.0f;
+        }
+        if (tid < kSub) {
+            const int s = s0 + tid;
+            s_w[tid] = s < len ? __expf(last - s_cum[s]) * s_dl[s] : 0.0f;
+        }
+        __syncthreads();
+        for (int r = 0; r < kSub; ++r) {
+            const float w = s_w[r];
+            float xv[4], bv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) xv[i] = s_x[r][pi + i] * w;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) bv[j] = s_b[r][nj + j];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(xv[i], bv[j], acc[i][j]);
+        }
+    }
+    float* S = a.states + (((b * a.nchunks + c) * a.H + h) * a.P) * a.N;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int64_t p = (int64_t)pt * kTile + pi + i, n = (int64_t)nt * kTile + nj + j;
+            if (p < a.P && n < a.N) S[p * a.N + n] = acc[i][j];
+        }
+}
+
+// grid: (ceil(P*N / 256), H, b).  In place: states[c] <- state entering chunk c.
+__global__ void __launch_bounds__(kThreads) ssd_state_pass(const SsdArgs a) {
+    const int64_t idx = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int64_t h = blockIdx.y, b = blockIdx.z;
+    if (idx >= a.P * a.N) return;
+    float st = a.init ? a.init[((b * a.H + h) * a.P) * a.N + idx] : 0.0f;
+    for (int64_t c = 0; c < a.nchunks; ++c) {
+        const int len = (int)min(a.Q, a.T - c * a.Q);
+        const float decay = __expf(a.cum[((b * a.H + h) * a.nchunks + c) * a.Q + len - 1]);
+        float* S = a.states + (((b * a.nchunks + c) * a.H + h) * a.P) * a.N + idx;
+        const float local = *S;
+        *S = st;
+        st = fmaf(decay, st, local);
+    }
+    if (a.final_state) a.final_state[((b * a.H + h) * a.P) * a.N + idx] = st;
+}
+
+// grid: (nchunks, H * nP, b * nTq); output tile of 64 rows x 64 head channels.
+template <typename T, bool GATE>
+__global__ void __launch_bounds__(kThreads) ssd_chunk_scan(const SsdArgs a) {
+    extern __shared__ __align__(16) float dsm[];
+    const int nP = (int)((a.P + kTile - 1) / kTile);
+    const int nTq = (int)((a.Q + kTile - 1) / kTile);
+    const int64_t c = blockIdx.x;
+    const int64_t h = blockIdx.y / nP;
+    const int pt = blockIdx.y % nP;
+    const int64_t b = blockIdx.z / nTq;
+    const int tq = blockIdx.z % nTq;
+    const int64_t g = h / (a.H / a.G);
+    const int tid = threadIdx.x;
+    const int64_t t0 = c * a.Q;
+    const int len = (int)min(a.Q, a.T - t0);
+    const int r0 = tq * kTile;  // first row of this tile inside the chunk
+    if (r0 >= len) return;
+    const int Nn = (int)a.N;
+    // smem: cum[Q] dl[Q] | C tile [64][N+1] | B sub [32][N+1] | x sub [32][65] | G [64][33]
+    float* s_cum = dsm;
+    float* s_dl = s_cum + a.Q;
+    float* s_c = s_dl + a.Q;
+    float* s_b = s_c + kTile * (Nn + 1);
+    float* s_x = s_b + kSub * (Nn + 1);
+    float* s_g = s_x + kSub * (kTile + 1);
+    for (int i = tid; i < a.Q; i += kThreads) {
+        const int64_t o = ((b * a.H + h) * a.nchunks + c) * a.Q + i;
+        s_cum[i] = a.cum[o];
+        s_dl[i] = a.dl[o];
+    }
+    for (int i = tid; i < kTile * Nn; i += kThreads) {
+        const int r = i / Nn, n = i % Nn;
+        s_c[r * (Nn + 1) + n] = (r0 + r < len) ? ld<T>(a.C, ((b * a.T + t0 + r0 + r) * a.G + g) * a.N + n) : 0.0f;
+    }
+    __syncthreads();
+    const int ti = (tid / 16) * 4, pj = (tid % 16) * 4;
+    float acc[4][4] = {};
+    const int s_end = min(len, r0 + kTile);
+    for (int s0 = 0; s0 < s_end; s0 += kSub) {
+        __syncthreads();
+        for (int i = tid; i < kSub * Nn; i += kThreads) {
+            const int r = i / Nn, n = i % Nn;
+            s_b[r * (Nn + 1) + n] = (s0 + r < len) ? ld<T>(a.B, ((b * a.T + t0 + s0 + r) * a.G + g) * a.N + n) : 0.0f;
+        }
+        for (int i = tid; i < kSub * kTile; i += kThreads) {
+            const int r = i / kTile, q = i % kTile;
+            const int64_t p = (int64_t)pt * kTile + q;
+            s_x[r * (kTile + 1) + q] = (s0 + r < len && p < a.P) ? ld<T>(a.x, ((b * a.T + t0 + s0 + r) * a.H + h) * a.P + p) : 0.0f;
+        }
+        __syncthreads();
+        // G'[t][s] = (s <= t) (C_t . B_s) exp(cum_t - cum_s) Delta_s for the 64 x 32 block
+        for (int i = tid; i < kTile * kSub; i += kThreads) {
+            const int r = i / kSub, s = i % kSub;
+            const int tt = r0 + r, ss = s0 + s;
+            float v = 0.0f;
+            if (ss <= tt && tt < len && ss < len) {
+                const float* cr = s_c + r * (Nn + 1);
+                const float* br = s_b + s * (Nn + 1);
+                float dot = 0.0f;
+                for (int n = 0; n < Nn; ++n) dot = fmaf(cr[n], br[n], dot);
+                v = dot * __expf(s_cum[tt] - s_cum[ss]) * s_dl[ss];
+            }
+            s_g[r * (kSub + 1) + s] = v;
+        }
+        __syncthreads();
+        for (int s = 0; s < kSub; ++s) {
+            float gv[4], xv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) gv[i] = s_g[(ti + i) * (kSub + 1) + s];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) xv[j] = s_x[s * (kTile + 1) + pj + j];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(gv[i], xv[j], acc[i][j]);
+        }
+    }
+    // Y_off = exp(cum_t) * sum_n C_t[n] hin[p][n]
+    const float* hin = a.states + (((b * a.nchunks + c) * a.H + h) * a.P) * a.N;
+    float off[4][4] = {};
+    for (int n0 = 0; n0 < Nn; n0 += kSub) {
+        __syncthreads();
+        // reuse s_x as hin sub-tile [32 n][65 p]
+        for (int i = tid; i < kSub * kTile; i += kThreads) {
+            const int nn = i / kTile, q = i % kTile;
+            const int64_t p = (int64_t)pt * kTile + q;
+            s_x[nn * (kTile + 1) + q] = (n0 + nn < Nn && p < a.P) ? hin[p * a.N + n0 + nn] : 0.0f;
+        }
+        __syncthreads();
+        const int nlim = min(kSub, Nn - n0);
+        for (int nn = 0; nn < nlim; ++nn) {
+            float cv[4], hv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) cv[i] = s_c[(ti + i) * (Nn + 1) + n0 + nn];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) hv[j] = s_x[nn * (kTile + 1) + pj + j];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) off[i][j] = fmaf(cv[i], hv[j], off[i][j]);
+        }
+    }
+    const float Dh = a.D ? a.D[h] : 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int tt = r0 + ti + i;
+        if (tt >= len) continue;
+        const float e = __expf(s_cum[tt]);
+        const int64_t row = ((b * a.T + t0 + tt) * a.H + h) * a.P;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int64_t p = (int64_t)pt * kTile + pj + j;
+            if (p >= a.P) continue;
+            const float xv = ld<T>(a.x, row + p);
+            float y = acc[i][j] + e * off[i][j] + Dh * xv;
+            if (GATE) y *= silu(ld<T>(a.z, row + p));
+            reinterpret_cast<T*>(a.out)[row + p] = from_f32<T>(y);
+        }
+    }
+}
+
+struct SsdPlan {
+    int64_t Q, nchunks;
+    size_t dl_off, cum_off, st_off, total;
+};
+
+SsdPlan ssd_plan(const ScanArgs& a) {
+    SsdPlan p;
+    p.Q = a.chunk > 0 ? a.chunk : 256;
+    p.nchunks = (a.seqlen + p.Q - 1) / p.Q;
+    const size_t vec = (size_t)a.batch * a.nheads * p.nchunks * p.Q * sizeof(float);
+    const size_t st = (size_t)a.batch * p.nchunks * a.nheads * a.headdim * a.dstate * sizeof(float);
+    p.dl_off = 0;
+    p.cum_off = align_up(vec, 256);
+    p.st_off = p.cum_off + align_up(vec, 256);
+    p.total = p.st_off + align_up(st, 256);
+    return p;
+}
+
+template <typename T>
+cudaError_t ssd_launch_typed(const ScanArgs& a, void* ws, cudaStream_t stream) {
+    const SsdPlan pl = ssd_plan(a);
+    SsdArgs s;
+    s.x = (const char*)a.x;
+    s.dt = (const char*)a.dt;
+    s.z = (const char*)a.z;
+    s.B = (const char*)a.B;
+    s.C = (const char*)a.C;
+    s.A = a.A;
+    s.D = a.D;
+    s.dt_bias = a.dt_bias;
+    s.init = a.initial_state;
+    s.out = (char*)a.out;
+    s.final_state = a.final_state;
+    s.dl = (float*)((char*)ws + pl.dl_off);
+    s.cum = (float*)((char*)ws + pl.cum_off);
+    s.states = (float*)((char*)ws + pl.st_off);
+    s.T = a.seqlen;
+    s.H = a.nheads;
+    s.P = a.headdim;
+    s.N = a.dstate;
+    s.G = a.ngroups;
+    s.Q = pl.Q;
+    s.nchunks = pl.nchunks;
+    const unsigned nP = (unsigned)((a.headdim + kTile - 1) / kTile);
+    const unsigned nN = (unsigned)((a.dstate + kTile - 1) / kTile);
+    const unsigned nTq = (unsigned)((pl.Q + kTile - 1) / kTile);
+    if (pl.nchunks > 0) {
+        ssd_chunk_state<T><<<dim3((unsigned)pl.nchunks, (unsigned)a.nheads * nP * nN, (unsigned)a.batch), kThreads, 0, stream>>>(s);
+        note_launches(1);
+    }
+    ssd_state_pass<<<dim3((unsigned)((a.headdim * a.dstate + kThreads - 1) / kThreads), (unsigned)a.nheads, (unsigned)a.batch), kThreads, 0, stream>>>(s);
+    note_launches(1);
+    if (pl.nchunks > 0) {
+        const size_t smem = sizeof(float) * (2 * pl.Q + kTile * (a.dstate + 1) + kSub * (a.dstate + 1) +
+                                             kSub * (kTile + 1) + kTile * (kSub + 1));
+        const dim3 grid((unsigned)pl.nchunks, (unsigned)a.nheads * nP, (unsigned)a.batch * nTq);
+        if (a.z) {
+            cudaFuncSetAttribute(ssd_chunk_scan<T, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            ssd_chunk_scan<T, true><<<grid, kThreads, smem, stream>>>(s);
+        } else {
+            cudaFuncSetAttribute(ssd_chunk_scan<T, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            ssd_chunk_scan<T, false><<<grid, kThreads, smem, stream>>>(s);
+        }
+        note_launches(1);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t ssd_workspace_bytes(const ScanArgs& a) {
+    if (a.batch == 0) return 0;
+    return ssd_plan(a).total;
+}
+
+cudaError_t ssd_launch(const ScanArgs& a, void* ws, cudaStream_t stream) {
+    if (a.batch == 0) return cudaSuccess;
+    if (a.dtype == 1) return ssd_launch_typed<__nv_bfloat16>(a, ws, stream);
+    return ssd_launch_typed<float>(a, ws, stream);
+}
+
+}  // namespace ssm

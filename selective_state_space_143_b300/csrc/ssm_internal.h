@@ -1,0 +1,40 @@
+// Internal interface between the C-ABI entry points and the kernel launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace ssm {
+
+// Everything a launcher needs, already validated by the entry point.
+struct ScanArgs {
+    const void* x;
+    const void* dt;
+    const float* A;
+    const void* B;
+    const void* C;
+    const float* D;
+    const void* z;
+    const float* dt_bias;
+    const float* initial_state;  // nullable: state entering t = 0 (zero when NULL)
+    void* out;
+    float* final_state;
+    int64_t batch, seqlen, nheads, headdim, dstate, ngroups, chunk;
+    int dtype;  // 0 fp32, 1 bf16
+};
+
+// Counts kernel launches made by this library (thread-safe).
+void note_launches(int n);
+
+// Diagonal (Mamba-1) path.
+size_t diag_workspace_bytes(const ScanArgs& a);
+cudaError_t diag_launch(const ScanArgs& a, void* ws, cudaStream_t stream);
+
+// SSD (Mamba-2) path.
+size_t ssd_workspace_bytes(const ScanArgs& a);
+cudaError_t ssd_launch(const ScanArgs& a, void* ws, cudaStream_t stream);
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace ssm

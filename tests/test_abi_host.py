@@ -1,0 +1,139 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports every
+function include/ssm_scan.h declares, and rejects bad arguments with the documented
+status before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import selective_state_space_143_b300 as ssm
+from selective_state_space_143_b300 import _lib
+from selective_state_space_143_b300.inputs import WORKLOADS
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "ssm_scan.h")
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(ssm_[a-z_0-9]+)\s*\(",
+                                 text, flags=re.M)))
+
+
+def test_header_declares_expected_functions():
+    assert declared_functions() == sorted(_lib.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = _lib.load()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_strerror_and_version():
+    for st in range(0, 9):
+        assert _lib.strerror(st)
+    assert "unknown" in _lib.strerror(99)
+    assert _lib.load().ssm_abi_version() >> 16 == 1
+
+
+def _shape(**kw):
+    s = _lib.ssm_shape()
+    base = dict(mode=0, dtype=1, batch=2, seqlen=64, nheads=64, headdim=1, dstate=16, ngroups=1,
+                chunk=0, flags=0)
+    base.update(kw)
+    for k, v in base.items():
+        setattr(s, k, v)
+    return s
+
+
+def _ws(s):
+    return _lib.load().ssm_scan_workspace_size(ctypes.byref(s))
+
+
+BAD = ctypes.c_size_t(-1).value
+
+
+@pytest.mark.parametrize("kw,valid", [
+    (dict(), True),
+    (dict(mode=7), False), (dict(dtype=5), False), (dict(flags=1), False),
+    (dict(batch=-1), False), (dict(nheads=0), False), (dict(ngroups=3), False),
+    (dict(headdim=2), False),                   # diagonal mode needs headdim 1
+    (dict(dstate=72), False),                   # diagonal N limit 64
+    (dict(dstate=12), False),                   # bf16 B/C rows must be 16-byte multiples
+    (dict(nheads=60), False),                   # bf16 channel rows must be 16-byte multiples
+    (dict(chunk=48), False),                    # diagonal segment length multiple of 32
+    (dict(mode=1, headdim=64, nheads=8, dstate=128, chunk=256), True),
+    (dict(mode=1, headdim=64, nheads=8, dstate=300), False),
+    (dict(mode=1, headdim=64, nheads=8, dstate=128, chunk=100), False),
+    (dict(mode=1, headdim=64, nheads=8, dstate=128, chunk=512), False),
+])
+def test_workspace_query_validates_shape(kw, valid):
+    n = _ws(_shape(**kw))
+    assert (n != BAD) == valid
+
+
+def test_workspace_sizes_of_workloads():
+    for name, w in WORKLOADS.items():
+        s = _shape(mode=0 if w.mode == "diag" else 1, dtype=1 if w.dtype == "bf16" else 0,
+                   batch=w.batch, seqlen=w.seqlen, nheads=w.nheads, headdim=w.headdim,
+                   dstate=w.dstate, ngroups=w.ngroups, chunk=w.chunk)
+        n = _ws(s)
+        assert n != BAD, name
+        if w.mode == "ssd":
+            assert n > 0
+
+
+def _call(s, x=1 << 12, dt=2 << 12, A=3 << 12, B=4 << 12, C=5 << 12, out=6 << 12, **opt):
+    lib = _lib.load()
+    vp = ctypes.c_void_p
+    return lib.ssm_scan_fwd(vp(x), vp(dt), vp(A), vp(B), vp(C), vp(opt.get("D")), vp(opt.get("z")),
+                            vp(opt.get("dt_bias")), vp(out), vp(opt.get("fs")),
+                            ctypes.byref(s) if s is not None else None, None)
+
+
+def test_argument_errors_are_reported_before_any_launch():
+    s = _shape()
+    assert _call(None) == _lib.SSM_ERR_NULL
+    assert _call(s, x=0) == _lib.SSM_ERR_NULL
+    assert _call(s, out=0) == _lib.SSM_ERR_NULL
+    assert _call(s, dt=(2 << 12) + 8) == _lib.SSM_ERR_ALIGN
+    assert _call(s, z=(7 << 12) + 2) == _lib.SSM_ERR_ALIGN
+    assert _call(_shape(dtype=9)) == _lib.SSM_ERR_DTYPE
+    assert _call(_shape(flags=2)) == _lib.SSM_ERR_UNSUPPORTED
+    assert _call(_shape(nheads=12, ngroups=5)) == _lib.SSM_ERR_SHAPE
+    assert _call(_shape(mode=1, nheads=8, headdim=64, dstate=512)) == _lib.SSM_ERR_UNSUPPORTED
+
+
+def test_workspace_entry_rejects_small_or_misaligned_workspace():
+    lib = _lib.load()
+    s = _shape(mode=1, nheads=8, headdim=64, dstate=128, chunk=64, seqlen=256)
+    need = _ws(s)
+    assert need > 0
+    vp = ctypes.c_void_p
+    args = [vp(1 << 12), vp(2 << 12), vp(3 << 12), vp(4 << 12), vp(5 << 12), None, None, None,
+            vp(6 << 12), None, ctypes.byref(s)]
+    assert lib.ssm_scan_fwd_ws(*args, None, 0, None) == _lib.SSM_ERR_ALLOC
+    assert lib.ssm_scan_fwd_ws(*args, vp(1 << 20), need - 1, None) == _lib.SSM_ERR_ALLOC
+    assert lib.ssm_scan_fwd_ws(*args, vp((1 << 20) + 16), need, None) == _lib.SSM_ERR_ALIGN
+
+
+def test_binding_shape_descriptor():
+    x = torch.zeros(2, 10, 4, 8, dtype=torch.bfloat16)
+    A = torch.zeros(4)
+    B = torch.zeros(2, 10, 2, 16, dtype=torch.bfloat16)
+    s = ssm.make_shape(x, A, B, chunk=64)
+    assert (s.mode, s.dtype, s.batch, s.seqlen, s.nheads, s.headdim, s.dstate, s.ngroups,
+            s.chunk) == (1, 1, 2, 10, 4, 8, 16, 2, 64)
+    x3 = torch.zeros(1, 5, 32)
+    s3 = ssm.make_shape(x3, torch.zeros(32, 8), torch.zeros(1, 5, 8))
+    assert (s3.mode, s3.dtype, s3.nheads, s3.headdim, s3.dstate, s3.ngroups) == (0, 0, 32, 1, 8, 1)
+
+
+def test_binding_refuses_cpu_tensors():
+    x = torch.zeros(1, 4, 8)
+    with pytest.raises(ValueError):
+        ssm.scan_fwd(x, x, torch.zeros(8, 4), torch.zeros(1, 4, 4), torch.zeros(1, 4, 4))
