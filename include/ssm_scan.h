@@ -76,7 +76,7 @@ typedef struct ssm_shape {
     int64_t headdim;  /* DIAG: 1; SSD: channels per head, 1..256                         */
     int64_t dstate;   /* N: DIAG 1..64; SSD 1..256                                       */
     int64_t ngroups;  /* >= 1, divides nheads                                            */
-    int64_t chunk;    /* 0 = default.  DIAG: time-segment length (multiple of 64) used to
+    int64_t chunk;    /* 0 = default.  DIAG: time-segment length (multiple of 32) used to
                          split the sequence across thread blocks; SSD: chunk length Q
                          (multiple of 16, <= 256).  Results agree within rounding for any
                          valid value.                                                    */
@@ -87,8 +87,10 @@ typedef struct ssm_shape {
 typedef struct CUstream_st* ssm_stream_t;
 
 /*
- * Forward scan.  x, dt, A, B, C and out are required; D, z, dt_bias and final_state
- * may be NULL (no skip term, no gate, no bias, no final state written).
+ * Forward scan.  x, dt, A, B, C and out are required (x, dt, B, C, out may be NULL
+ * when batch or seqlen is 0, since they then hold no elements); D, z, dt_bias and
+ * final_state may be NULL (no skip term, no gate, no bias, no final state written).
+ * With seqlen 0 and batch > 0 the final state is written as zeros.
  * Alignment: every non-NULL pointer 16-byte aligned, and the innermost row of x/z/out
  * (DIAG: nheads elements; SSD: nheads*headdim elements) and of B/C (ngroups*dstate)
  * a multiple of 16 bytes.

@@ -8,17 +8,23 @@
 //   y_t     = (sum_n C_t[n] h_t[n] + D x_t) * SiLU(z_t)
 //
 // Design (B300):
-//  * The expanded state (b, T, d_inner, N) never leaves registers: each thread owns
-//    NPT = NK / LPC state entries of one channel, LPC lanes cover one channel.
-//  * Inputs are token-major (channels innermost).  A block owns CPB channels of one
-//    group and walks time in tiles of 32 steps.  Each tile of x, dt, z, B, C is staged
-//    into shared memory by 16-byte cp.async copies in a 3-deep pipeline, so HBM reads
-//    are coalesced rows and overlap the arithmetic of the previous tiles.
-//  * Per tile: (A) every thread computes softplus and Delta*x for a few (t, c) pairs and
-//    converts B, C to fp32 (per-(t,c) work done once, not once per state entry);
-//    (B) the scan: exp via ex2.approx, packed fp32x2 multiply/FMA for the decay, the
-//    input term, the state update and the C.h partial sum; (C) the partial sums over the
-//    LPC lanes are combined, D*x and the SiLU gate applied, and bf16/fp32 pairs stored.
+//  * The expanded state (b, T, d_inner, N) never leaves registers: a quad of 4 lanes
+//    owns one channel, each lane NPT = N/4 state entries.
+//  * Inputs are token-major (channels innermost).  A 64-thread block owns 16 channels
+//    of one group and walks time in tiles of 32 steps; each tile of x, dt, z, B, C is
+//    staged into shared memory by 16-byte cp.async copies in a 3-deep pipeline, so HBM
+//    reads are coalesced rows that overlap the arithmetic of earlier tiles.
+//  * Rows are taken in groups of 4: lane q of a quad evaluates softplus(dt + dt_bias)
+//    and Delta*x for row q of the group and the quad exchanges them by shuffles; each
+//    lane then advances its state entries over the 4 rows (ex2.approx for the decay,
+//    packed fp32x2 multiply/FMA for the decay argument, the input term, the update and
+//    the C.h partial sum); a transposed quad reduction leaves the full C.h of row q in
+//    lane q, which applies D*x and the SiLU gate and stores.  Every per-(t, c)
+//    operation runs once, spread over the quad.
+//  * B300's SFU runs ex2 at 32/clk/SM (lg2, rcp at 16) and packed fp32x2 FMA gives no
+//    extra lane throughput over scalar FMA (128 lane-ops/clk/SM), so the scan is bound
+//    by the SFU and FMA pipes (one exp and four FP32 operations per state entry and
+//    step), above the HBM time of its 8 bytes per token-channel.
 //  * Time parallelism when there are few channels: the sequence is cut into segments.
 //    A state-only pass computes each segment's local end state (from zero) and its
 //    sum of Delta; the output pass folds those summaries into the segment's initial
@@ -29,6 +35,8 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
+#include <cstdlib>
 
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
@@ -36,30 +44,31 @@
 namespace ssm {
 namespace {
 
-constexpr int kThreads = 128;
 constexpr int kTT = 32;      // time steps per tile
-constexpr int kStages = 3;   // cp.async pipeline depth
+constexpr int kStages = 2;   // cp.async double buffer
 
-template <typename T, int NK, int LPC>
+// LPC lanes per channel, WARPS warps per block.
+template <typename T, int NK, int LPC, int WARPS>
 struct DiagCfg {
-    static constexpr int NPT = NK / LPC;      // state entries per thread
-    static constexpr int CPB = kThreads / LPC;  // channels per block
+    static constexpr int NT = 32 * WARPS;       // threads per block
+    static constexpr int CPB = NT / LPC;        // channels per block
+    static constexpr int NPT = NK / LPC;        // state entries per thread
+    static constexpr int P2 = CPB / 2;          // channel pairs per block
     static constexpr int kElem = (int)sizeof(T);
-    static constexpr int kRowBytes = CPB * kElem;         // one time row of the x/dt/z tile
+    static constexpr int kRowBytes = CPB * kElem;  // one time row of the x/dt/z tile
     static constexpr int kRowChunks = kRowBytes / 16;
     static constexpr int kXBytes = kTT * kRowBytes;
     static constexpr int kBCRowBytes = NK * kElem;
     static constexpr int kBCRowChunks = kBCRowBytes / 16;
     static constexpr int kBCBytes = kTT * kBCRowBytes;
     static constexpr int kStageBytes = 3 * kXBytes + 2 * kBCBytes;
-    // working buffers
-    static constexpr int kDuBytes = kTT * CPB * 8;        // float2 (Delta, Delta*x)
-    static constexpr int kBfBytes = kTT * NK * 4;         // fp32 B (and C)
-    static constexpr int kYpBytes = kTT * CPB * LPC * 4;  // partial C.h per lane
-    static constexpr int kSmemBytes = kStages * kStageBytes + kDuBytes + 2 * kBfBytes + kYpBytes;
-    static_assert(NK % LPC == 0 && NPT % 4 == 0, "NPT must be a multiple of 4");
+    static constexpr int kBfBytes = kTT * NK * 4;      // fp32 copy of B (and of C)
+    static constexpr int kDuBytes = kTT * CPB * 8;     // (Delta, Delta*x) per (t, c)
+    static constexpr int kYsBytes = kTT * CPB * LPC * 4;  // partial C.h per lane
+    static constexpr int kSmemBytes = kStages * kStageBytes + 2 * kBfBytes + kDuBytes + kYsBytes;
+    static_assert(NPT % 4 == 0, "state entries are processed in groups of 4");
     static_assert(kRowBytes % 16 == 0 && kBCRowBytes % 16 == 0, "16-byte rows");
-    static_assert((CPB / 2) * kTT % kThreads == 0, "pair mapping");
+    static_assert(NT % P2 == 0, "pair mapping");
 };
 
 struct DiagKernelArgs {
@@ -93,13 +102,13 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 template <typename T>
-__device__ __forceinline__ float2 load_pair(const char* p);
+__device__ __forceinline__ float2 load_pair(const unsigned char* p);
 template <>
-__device__ __forceinline__ float2 load_pair<float>(const char* p) {
+__device__ __forceinline__ float2 load_pair<float>(const unsigned char* p) {
     return *reinterpret_cast<const float2*>(p);
 }
 template <>
-__device__ __forceinline__ float2 load_pair<__nv_bfloat16>(const char* p) {
+__device__ __forceinline__ float2 load_pair<__nv_bfloat16>(const unsigned char* p) {
     return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
 }
 
@@ -116,16 +125,25 @@ __device__ __forceinline__ void store_pair<__nv_bfloat16>(char* p, float2 v) {
 
 // STATE_ONLY: compute each segment's local end state from zero (segments 0..nseg-2).
 // Otherwise: full output pass over every segment with the folded initial state.
-template <typename T, int NK, int LPC, bool STATE_ONLY, bool GATE>
-__global__ void __launch_bounds__(kThreads) diag_scan_kernel(const DiagKernelArgs a) {
-    using Cfg = DiagCfg<T, NK, LPC>;
-    constexpr int NPT = Cfg::NPT, CPB = Cfg::CPB, E = Cfg::kElem;
+//
+// Per tile of 32 steps:
+//   A) per (t, channel pair): softplus(dt + dt_bias) and Delta*x, packed fp32x2, into
+//      shared memory; B and C converted to fp32;
+//   B) per lane: NPT state entries of one channel advanced over the tile's rows, partial
+//      C.h sums into shared memory;
+//   C) per (t, channel pair): sum of the LPC partials, D*x, SiLU gate, store.
+template <typename T, int NK, int LPC, int WARPS, bool STATE_ONLY, bool GATE>
+__global__ void __launch_bounds__(32 * WARPS) diag_scan_kernel(const DiagKernelArgs a) {
+    using Cfg = DiagCfg<T, NK, LPC, WARPS>;
+    constexpr int NT = Cfg::NT, CPB = Cfg::CPB, NPT = Cfg::NPT, P2 = Cfg::P2, E = Cfg::kElem;
+    constexpr int RS = NT / P2;  // rows per sweep of the pair roles
+    constexpr bool PRECISE = sizeof(T) == 4;
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* stage0 = smem;
-    float2* du = reinterpret_cast<float2*>(smem + kStages * Cfg::kStageBytes);
-    float* Bf = reinterpret_cast<float*>(smem + kStages * Cfg::kStageBytes + Cfg::kDuBytes);
+    float* Bf = reinterpret_cast<float*>(smem + kStages * Cfg::kStageBytes);
     float* Cf = Bf + kTT * NK;
-    float* yp = Cf + kTT * NK;
+    float2* du = reinterpret_cast<float2*>(Cf + kTT * NK);
+    float* ys = reinterpret_cast<float*>(du + kTT * CPB);
 
     const int tid = threadIdx.x;
     const int group = blockIdx.x / a.tiles_per_group;
@@ -137,11 +155,21 @@ __global__ void __launch_bounds__(kThreads) diag_scan_kernel(const DiagKernelArg
     const int64_t t_end = min(a.T, t_begin + a.seg_len);
     const int ntiles = (int)((t_end - t_begin + kTT - 1) / kTT);
 
-    // scan-phase role: channel cc within the block, lane group g over the state index
+    // scan role: channel cc, lane g of LPC
     const int cc = tid / LPC;
     const int g = tid % LPC;
     const int64_t c = c_begin + cc;
     const bool c_ok = c < c_end;
+
+    // pair role (phases A and C): channels 2*pp, 2*pp+1, rows r0, r0 + RS, ...
+    const int pp = tid % P2;
+    const int r0 = tid / P2;
+    const int64_t cA = c_begin + 2 * pp;
+    const bool pair_ok = cA < c_end;  // group runs are whole 16-byte chunks: even
+    const float2 bias2 = (pair_ok && a.dt_bias) ? make_float2(a.dt_bias[cA], a.dt_bias[cA + 1])
+                                                : make_float2(0.0f, 0.0f);
+    const float2 d2 = (pair_ok && a.D) ? make_float2(a.D[cA], a.D[cA + 1]) : make_float2(0.0f, 0.0f);
+    float2 dsum2 = make_float2(0.0f, 0.0f);  // sum of Delta (state-only pass)
 
     float A2[NPT];
     float h[NPT];
@@ -159,8 +187,7 @@ __global__ void __launch_bounds__(kThreads) diag_scan_kernel(const DiagKernelArg
             const int n = g * NPT + j;
             if (c_ok && n < a.N && a.init) h[j] = a.init[(b * a.dim + c) * a.N + n];
         }
-        for (int s = 0; s < seg; ++s) {
-            if (!c_ok) break;
+        for (int s = 0; s < seg && c_ok; ++s) {
             const float dsum = a.seg_dsum[((int64_t)s * gridDim.z + b) * a.dim + c];
             const float* Hs = a.seg_h + (((int64_t)s * gridDim.z + b) * a.dim + c) * a.N;
 #pragma unroll
@@ -170,19 +197,6 @@ __global__ void __launch_bounds__(kThreads) diag_scan_kernel(const DiagKernelArg
             }
         }
     }
-
-    // pair role for phases A and C: channels (2*cp, 2*cp+1) of the tile, rows r0 + k*RS
-    constexpr int PAIRS = CPB / 2;
-    constexpr int RS = kThreads / PAIRS;  // rows handled per sweep
-    const int cp = tid % PAIRS;
-    const int r0 = tid / PAIRS;
-    const int64_t cA = c_begin + 2 * cp;
-    const bool pair_ok = cA < c_end;  // cpg is even (16-byte rows), so both or neither
-    const float bias0 = (pair_ok && a.dt_bias) ? a.dt_bias[cA] : 0.0f;
-    const float bias1 = (pair_ok && a.dt_bias) ? a.dt_bias[cA + 1] : 0.0f;
-    const float d0 = (pair_ok && a.D) ? a.D[cA] : 0.0f;
-    const float d1 = (pair_ok && a.D) ? a.D[cA + 1] : 0.0f;
-    float dsum0 = 0.0f, dsum1 = 0.0f;  // running sum of Delta (state-only pass)
 
     const int64_t row_stride = a.dim * E;     // bytes between consecutive time rows
     const int64_t bc_stride = a.G * a.N * E;  // bytes between consecutive B/C rows
@@ -194,7 +208,7 @@ __global__ void __launch_bounds__(kThreads) diag_scan_kernel(const DiagKernelArg
             unsigned char* st = stage0 + (k % kStages) * Cfg::kStageBytes;
             const int64_t t0 = t_begin + (int64_t)k * kTT;
             const int rows = (int)min((int64_t)kTT, t_end - t0);
-            for (int i = tid; i < kTT * Cfg::kRowChunks; i += kThreads) {
+            for (int i = tid; i < kTT * Cfg::kRowChunks; i += NT) {
                 const int r = i / Cfg::kRowChunks, q = i % Cfg::kRowChunks;
                 const int64_t ch = c_begin + q * (16 / E);
                 const bool ok = r < rows && ch < c_end;
@@ -204,7 +218,7 @@ __global__ void __launch_bounds__(kThreads) diag_scan_kernel(const DiagKernelArg
                 if (GATE && !STATE_ONLY)
                     cp_async16(st + 2 * Cfg::kXBytes + r * Cfg::kRowBytes + q * 16, a.z + off, ok);
             }
-            for (int i = tid; i < kTT * Cfg::kBCRowChunks; i += kThreads) {
+            for (int i = tid; i < kTT * Cfg::kBCRowChunks; i += NT) {
                 const int r = i / Cfg::kBCRowChunks, q = i % Cfg::kBCRowChunks;
                 const bool ok = r < rows && q * (16 / E) < a.N;
                 const int64_t off = ok ? ((b * a.T + t0 + r) * bc_stride + q * 16) : 0;
@@ -216,102 +230,115 @@ __global__ void __launch_bounds__(kThreads) diag_scan_kernel(const DiagKernelArg
         cp_async_commit();
     };
 
-#pragma unroll
-    for (int k = 0; k < kStages - 1; ++k) issue_tile(k);
-
+    issue_tile(0);
     for (int k = 0; k < ntiles; ++k) {
-        cp_async_wait<kStages - 2>();
-        __syncthreads();
-        issue_tile(k + kStages - 1);
+        cp_async_wait<0>();
+        __syncthreads();  // tile k visible; every thread is done with tile k-1
+        issue_tile(k + 1);
         const unsigned char* st = stage0 + (k % kStages) * Cfg::kStageBytes;
         const int64_t t0 = t_begin + (int64_t)k * kTT;
         const int rows = (int)min((int64_t)kTT, t_end - t0);
 
-        // ---- phase A: Delta and Delta*x per (t, c); B, C to fp32
+        // ---- A: Delta and Delta*x per (t, channel pair); B, C to fp32
 #pragma unroll
         for (int kk = 0; kk < kTT / RS; ++kk) {
             const int r = r0 + kk * RS;
-            const float2 dtv = load_pair<T>((const char*)st + Cfg::kXBytes + r * Cfg::kRowBytes + 2 * cp * E);
-            const float2 xv = load_pair<T>((const char*)st + r * Cfg::kRowBytes + 2 * cp * E);
-            const float de0 = softplus(dtv.x + bias0);
-            const float de1 = softplus(dtv.y + bias1);
-            float4 v;
-            v.x = de0;
-            v.y = de0 * xv.x;
-            v.z = de1;
-            v.w = de1 * xv.y;
-            *reinterpret_cast<float4*>(&du[r * CPB + 2 * cp]) = v;
-            if (STATE_ONLY && r < rows) {
-                dsum0 += de0;
-                dsum1 += de1;
-            }
+            const float2 dtv = load_pair<T>(st + Cfg::kXBytes + r * Cfg::kRowBytes + 2 * pp * E);
+            const float2 xv = load_pair<T>(st + r * Cfg::kRowBytes + 2 * pp * E);
+            float2 de = softplus2_t<PRECISE>(__fadd2_rn(dtv, bias2));
+            if (r >= rows) de = make_float2(0.0f, 0.0f);  // no-op rows: Delta = 0 keeps h
+            const float2 u = __fmul2_rn(de, xv);
+            *reinterpret_cast<float4*>(&du[r * CPB + 2 * pp]) = make_float4(de.x, u.x, de.y, u.y);
+            if (STATE_ONLY) dsum2 = __fadd2_rn(dsum2, de);
         }
-        for (int i = tid; i < kTT * NK / 2; i += kThreads) {
-            const float2 bv = load_pair<T>((const char*)st + 3 * Cfg::kXBytes + i * 2 * E);
-            *reinterpret_cast<float2*>(&Bf[2 * i]) = bv;
-            if (!STATE_ONLY) {
-                const float2 cv = load_pair<T>((const char*)st + 3 * Cfg::kXBytes + Cfg::kBCBytes + i * 2 * E);
-                *reinterpret_cast<float2*>(&Cf[2 * i]) = cv;
-            }
+        for (int i = tid; i < kTT * NK / 2; i += NT) {
+            *reinterpret_cast<float2*>(&Bf[2 * i]) = load_pair<T>(st + 3 * Cfg::kXBytes + i * 2 * E);
+            if (!STATE_ONLY)
+                *reinterpret_cast<float2*>(&Cf[2 * i]) =
+                    load_pair<T>(st + 3 * Cfg::kXBytes + Cfg::kBCBytes + i * 2 * E);
         }
         __syncthreads();
 
-        // ---- phase B: the recurrence over this tile's rows
-        for (int r = 0; r < rows; ++r) {
-            const float2 dv = du[r * CPB + cc];
-            const float2 dd = make_float2(dv.x, dv.x);
-            const float2 uu = make_float2(dv.y, dv.y);
-            float2 y2 = make_float2(0.0f, 0.0f);
+        // ---- B: the recurrence over the tile's rows, 4 rows at a time.  The decays and
+        // input terms of the 4 rows do not depend on h, so they are formed first (32
+        // independent exponentials per lane for NPT = 8), then the dependent updates run.
+        // Rows past the tile's end have Delta = 0 and x*Delta = 0, so they leave h as is.
+        for (int rb = 0; rb < rows; rb += 4) {
+            float av[4][NPT], ub[4][NPT];
 #pragma unroll
-            for (int j = 0; j < NPT; j += 4) {
-                const float4 bq = *reinterpret_cast<const float4*>(&Bf[r * NK + g * NPT + j]);
-                const float2 dA0 = __fmul2_rn(dd, make_float2(A2[j], A2[j + 1]));
-                const float2 dA1 = __fmul2_rn(dd, make_float2(A2[j + 2], A2[j + 3]));
-                const float2 a0 = make_float2(ex2(dA0.x), ex2(dA0.y));
-                const float2 a1 = make_float2(ex2(dA1.x), ex2(dA1.y));
-                const float2 ub0 = __fmul2_rn(uu, make_float2(bq.x, bq.y));
-                const float2 ub1 = __fmul2_rn(uu, make_float2(bq.z, bq.w));
-                const float2 h0 = __ffma2_rn(a0, make_float2(h[j], h[j + 1]), ub0);
-                const float2 h1 = __ffma2_rn(a1, make_float2(h[j + 2], h[j + 3]), ub1);
-                h[j] = h0.x;
-                h[j + 1] = h0.y;
-                h[j + 2] = h1.x;
-                h[j + 3] = h1.y;
-                if (!STATE_ONLY) {
-                    const float4 cq = *reinterpret_cast<const float4*>(&Cf[r * NK + g * NPT + j]);
-                    y2 = __ffma2_rn(make_float2(cq.x, cq.y), h0, y2);
-                    y2 = __ffma2_rn(make_float2(cq.z, cq.w), h1, y2);
+            for (int i = 0; i < 4; ++i) {
+                const float2 dv = du[(rb + i) * CPB + cc];
+                const float2 dd = make_float2(dv.x, dv.x);
+                const float2 uu = make_float2(dv.y, dv.y);
+#pragma unroll
+                for (int j = 0; j < NPT; j += 4) {
+                    const float4 bq = *reinterpret_cast<const float4*>(&Bf[(rb + i) * NK + g * NPT + j]);
+                    const float2 dA0 = __fmul2_rn(dd, make_float2(A2[j], A2[j + 1]));
+                    const float2 dA1 = __fmul2_rn(dd, make_float2(A2[j + 2], A2[j + 3]));
+                    av[i][j] = ex2(dA0.x);
+                    av[i][j + 1] = ex2(dA0.y);
+                    av[i][j + 2] = ex2(dA1.x);
+                    av[i][j + 3] = ex2(dA1.y);
+                    const float2 u0 = __fmul2_rn(uu, make_float2(bq.x, bq.y));
+                    const float2 u1 = __fmul2_rn(uu, make_float2(bq.z, bq.w));
+                    ub[i][j] = u0.x;
+                    ub[i][j + 1] = u0.y;
+                    ub[i][j + 2] = u1.x;
+                    ub[i][j + 3] = u1.y;
                 }
             }
-            if (!STATE_ONLY) yp[(r * CPB + cc) * LPC + g] = y2.x + y2.y;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float2 ya = make_float2(0.0f, 0.0f), yb = make_float2(0.0f, 0.0f);
+#pragma unroll
+                for (int j = 0; j < NPT; j += 4) {
+                    const float2 h0 = __ffma2_rn(make_float2(av[i][j], av[i][j + 1]), make_float2(h[j], h[j + 1]),
+                                                 make_float2(ub[i][j], ub[i][j + 1]));
+                    const float2 h1 = __ffma2_rn(make_float2(av[i][j + 2], av[i][j + 3]),
+                                                 make_float2(h[j + 2], h[j + 3]),
+                                                 make_float2(ub[i][j + 2], ub[i][j + 3]));
+                    h[j] = h0.x;
+                    h[j + 1] = h0.y;
+                    h[j + 2] = h1.x;
+                    h[j + 3] = h1.y;
+                    if (!STATE_ONLY) {
+                        const float4 cq = *reinterpret_cast<const float4*>(&Cf[(rb + i) * NK + g * NPT + j]);
+                        ya = __ffma2_rn(make_float2(cq.x, cq.y), h0, ya);
+                        yb = __ffma2_rn(make_float2(cq.z, cq.w), h1, yb);
+                    }
+                }
+                if (!STATE_ONLY) {
+                    const float2 ys2 = __fadd2_rn(ya, yb);
+                    ys[((rb + i) * CPB + cc) * LPC + g] = ys2.x + ys2.y;
+                }
+            }
         }
 
         if (!STATE_ONLY) {
             __syncthreads();
-            // ---- phase C: combine the LPC partial sums, skip term, gate, store
+            // ---- C: combine the LPC partial sums, skip term, gate, store
 #pragma unroll
             for (int kk = 0; kk < kTT / RS; ++kk) {
                 const int r = r0 + kk * RS;
                 if (r >= rows || !pair_ok) continue;
-                float y0 = 0.0f, y1 = 0.0f;
+                float2 y = make_float2(0.0f, 0.0f);
+                if (LPC == 1) {
+                    y = *reinterpret_cast<const float2*>(&ys[r * CPB + 2 * pp]);
+                } else {
 #pragma unroll
-                for (int q = 0; q < LPC; ++q) {
-                    y0 += yp[(r * CPB + 2 * cp) * LPC + q];
-                    y1 += yp[(r * CPB + 2 * cp + 1) * LPC + q];
+                    for (int q = 0; q < LPC; q += 2) {
+                        const float2 p0 = *reinterpret_cast<const float2*>(&ys[(r * CPB + 2 * pp) * LPC + q]);
+                        const float2 p1 = *reinterpret_cast<const float2*>(&ys[(r * CPB + 2 * pp + 1) * LPC + q]);
+                        y = __fadd2_rn(y, make_float2(p0.x + p0.y, p1.x + p1.y));
+                    }
                 }
-                const float2 xv = load_pair<T>((const char*)st + r * Cfg::kRowBytes + 2 * cp * E);
-                y0 = fmaf(d0, xv.x, y0);
-                y1 = fmaf(d1, xv.y, y1);
-                if (GATE) {
-                    const float2 zv = load_pair<T>((const char*)st + 2 * Cfg::kXBytes + r * Cfg::kRowBytes + 2 * cp * E);
-                    y0 *= silu(zv.x);
-                    y1 *= silu(zv.y);
-                }
-                store_pair<T>(a.out + (b * a.T + t0 + r) * row_stride + cA * E, make_float2(y0, y1));
+                const float2 xv = load_pair<T>(st + r * Cfg::kRowBytes + 2 * pp * E);
+                y = __ffma2_rn(d2, xv, y);
+                if (GATE) y = __fmul2_rn(y, silu2_t<PRECISE>(load_pair<T>(st + 2 * Cfg::kXBytes + r * Cfg::kRowBytes + 2 * pp * E)));
+                store_pair<T>(a.out + (b * a.T + t0 + r) * row_stride + cA * E, y);
             }
         }
     }
-    cp_async_wait<0>();
 
     if (STATE_ONLY) {
         // local end state and Delta sum of this segment
@@ -323,18 +350,20 @@ __global__ void __launch_bounds__(kThreads) diag_scan_kernel(const DiagKernelArg
                 if (n < a.N) Hs[n] = h[j];
             }
         }
-        // Delta sums: the pair role accumulated rows r0, r0+RS, ...; reduce over the RS
-        // threads that share a pair (they are tid = cp + PAIRS * k)
+        // the RS threads of a pair each summed a subset of rows
         __syncthreads();
-        float* red = yp;  // reuse: RS x CPB floats
-        red[r0 * CPB + 2 * cp] = dsum0;
-        red[r0 * CPB + 2 * cp + 1] = dsum1;
+        float2* red = du;  // reuse: RS x P2 partial sums
+        red[r0 * P2 + pp] = dsum2;
         __syncthreads();
-        if (tid < CPB) {
-            float s = 0.0f;
-            for (int k = 0; k < RS; ++k) s += red[k * CPB + tid];
-            const int64_t cc2 = c_begin + tid;
-            if (cc2 < c_end) a.seg_dsum[((int64_t)seg * gridDim.z + b) * a.dim + cc2] = s;
+        if (tid < P2) {
+            float2 s = make_float2(0.0f, 0.0f);
+            for (int k = 0; k < RS; ++k) s = __fadd2_rn(s, red[k * P2 + tid]);
+            const int64_t c0 = c_begin + 2 * tid;
+            if (c0 < c_end) {
+                float* dst = a.seg_dsum + ((int64_t)seg * gridDim.z + b) * a.dim + c0;
+                dst[0] = s.x;
+                dst[1] = s.y;
+            }
         }
     } else if (a.final_state && seg == a.nseg - 1 && c_ok) {
 #pragma unroll
@@ -350,6 +379,8 @@ __global__ void __launch_bounds__(kThreads) diag_scan_kernel(const DiagKernelArg
 struct Plan {
     int NK;
     int LPC;
+    int warps;
+    int cpb;
     int64_t seg_len;
     int nseg;
     int tiles_per_group;
@@ -363,25 +394,37 @@ int pick_nk(int64_t N) {
     return 64;
 }
 
+// State entries per lane: 8 by default (the best instruction count per element on
+// B300 for the configurations measured); SSM_DIAG_NPT=4 selects 4 (tuning knob).
+int pick_npt() {
+    static const int v = [] {
+        const char* e = getenv("SSM_DIAG_NPT");
+        return (e && atoi(e) == 4) ? 4 : 8;
+    }();
+    return v;
+}
+
 Plan make_plan(const ScanArgs& a) {
     Plan p;
     p.NK = pick_nk(a.dstate);
-    p.LPC = p.NK == 8 ? 2 : 4;  // 4 state entries per lane (2 lanes/ch for N <= 8)
-    const int cpb = kThreads / p.LPC;
+    p.LPC = std::max(1, p.NK / pick_npt());
+    p.cpb = p.LPC == 1 ? 32 : 16;
+    p.warps = p.cpb * p.LPC / 32;
     const int64_t cpg = a.nheads / a.ngroups;
-    p.tiles_per_group = (int)((cpg + cpb - 1) / cpb);
+    p.tiles_per_group = (int)((cpg + p.cpb - 1) / p.cpb);
     p.blocks_x = (int)(a.ngroups * p.tiles_per_group);
-    const int64_t units = (int64_t)p.blocks_x * a.batch;
-    // Aim for >= 4 resident blocks on each of the B300's 148 SMs; split time only when
-    // channels are scarce.  (A fixed count keeps the plan, and so the workspace size, a
-    // function of the shape alone.)
-    const int sms = 148;
-    const int64_t target = (int64_t)sms * 4;
+    const int64_t warps = (int64_t)p.blocks_x * a.batch * p.warps;
+    // Split time only when the channels give fewer than 2 warps per SM sub-partition
+    // (148 SMs x 4); then aim for 4.  The plan, and so the workspace size, is a
+    // function of the shape alone.
+    const int64_t smsp = 148 * 4;
     int64_t seg_len;
     if (a.chunk > 0) {
         seg_len = a.chunk;
+    } else if (warps >= 2 * smsp || warps == 0) {
+        seg_len = a.seqlen;
     } else {
-        int64_t nseg = units > 0 ? (target + units - 1) / units : 1;
+        int64_t nseg = (4 * smsp + warps - 1) / warps;
         nseg = std::max<int64_t>(1, std::min<int64_t>(nseg, a.seqlen / 128));
         seg_len = (a.seqlen + nseg - 1) / nseg;
     }
@@ -393,11 +436,21 @@ Plan make_plan(const ScanArgs& a) {
 
 template <typename T, int NK, int LPC, bool STATE_ONLY, bool GATE>
 cudaError_t launch_one(const DiagKernelArgs& ka, dim3 grid, cudaStream_t stream) {
-    using Cfg = DiagCfg<T, NK, LPC>;
-    auto kern = diag_scan_kernel<T, NK, LPC, STATE_ONLY, GATE>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+    constexpr int WARPS = (LPC == 1 ? 32 : 16) * LPC / 32;
+    using Cfg = DiagCfg<T, NK, LPC, WARPS>;
+    auto kern = diag_scan_kernel<T, NK, LPC, WARPS, STATE_ONLY, GATE>;
+    // the shared-memory attribute is set once per instantiation and device
+    static std::atomic<uint64_t> attr_done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, Cfg::kSmemBytes, stream>>>(ka);
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(attr_done.load(std::memory_order_relaxed) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_done.fetch_or(bit, std::memory_order_relaxed);
+    }
+    kern<<<grid, Cfg::NT, Cfg::kSmemBytes, stream>>>(ka);
     note_launches(1);
     return cudaGetLastError();
 }
@@ -442,10 +495,10 @@ cudaError_t launch_typed(const ScanArgs& a, const Plan& p, void* ws, cudaStream_
 template <typename T>
 cudaError_t launch_dtype(const ScanArgs& a, const Plan& p, void* ws, cudaStream_t stream) {
     switch (p.NK) {
-        case 8: return launch_typed<T, 8, 2>(a, p, ws, stream);
-        case 16: return launch_typed<T, 16, 4>(a, p, ws, stream);
-        case 32: return launch_typed<T, 32, 4>(a, p, ws, stream);
-        default: return launch_typed<T, 64, 4>(a, p, ws, stream);
+        case 8: return p.LPC == 1 ? launch_typed<T, 8, 1>(a, p, ws, stream) : launch_typed<T, 8, 2>(a, p, ws, stream);
+        case 16: return p.LPC == 2 ? launch_typed<T, 16, 2>(a, p, ws, stream) : launch_typed<T, 16, 4>(a, p, ws, stream);
+        case 32: return p.LPC == 4 ? launch_typed<T, 32, 4>(a, p, ws, stream) : launch_typed<T, 32, 8>(a, p, ws, stream);
+        default: return p.LPC == 8 ? launch_typed<T, 64, 8>(a, p, ws, stream) : launch_typed<T, 64, 16>(a, p, ws, stream);
     }
 }
 

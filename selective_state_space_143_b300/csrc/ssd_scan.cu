@@ -20,8 +20,10 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdlib>
 
 #include "ssm_device.cuh"
+#include "ssd_tc.h"
 #include "ssm_internal.h"
 
 namespace ssm {
@@ -54,6 +56,12 @@ __device__ __forceinline__ float ld(const char* base, int64_t idx) {
     return to_f32<T>(reinterpret_cast<const T*>(base)[idx]);
 }
 
+// e^x: CUDA's accurate expf for fp32 inputs, the fast intrinsic for 16-bit inputs.
+template <typename T>
+__device__ __forceinline__ float exp_t(float x) {
+    return sizeof(T) == 4 ? expf(x) : __expf(x);
+}
+
 // Delta and the inclusive cumulative sum of Delta * A_h over one chunk, into smem.
 template <typename T>
 __device__ void chunk_delta_cumsum(const SsdArgs& a, int64_t b, int64_t h, int64_t c,
@@ -64,7 +72,7 @@ __device__ void chunk_delta_cumsum(const SsdArgs& a, int64_t b, int64_t h, int64
     float dA = 0.0f;
     if (tid < len) {
         const float v = ld<T>(a.dt, (b * a.T + t0 + tid) * a.H + h) + (a.dt_bias ? a.dt_bias[h] : 0.0f);
-        const float de = softplus(v);
+        const float de = softplus_t<sizeof(T) == 4>(v);
         s_dl[tid] = de;
         dA = de * a.A[h];
     } else if (tid < a.Q) {
@@ -130,7 +138,7 @@ __global__ void __launch_bounds__(kThreads) ssd_chunk_state(const SsdArgs a) {
         }
         if (tid < kSub) {
             const int s = s0 + tid;
-            s_w[tid] = s < len ? __expf(last - s_cum[s]) * s_dl[s] : 0.0f;
+            s_w[tid] = s < len ? exp_t<T>(last - s_cum[s]) * s_dl[s] : 0.0f;
         }
         __syncthreads();
         for (int r = 0; r < kSub; ++r) {
@@ -164,7 +172,7 @@ __global__ void __launch_bounds__(kThreads) ssd_state_pass(const SsdArgs a) {
     float st = a.init ? a.init[((b * a.H + h) * a.P) * a.N + idx] : 0.0f;
     for (int64_t c = 0; c < a.nchunks; ++c) {
         const int len = (int)min(a.Q, a.T - c * a.Q);
-        const float decay = __expf(a.cum[((b * a.H + h) * a.nchunks + c) * a.Q + len - 1]);
+        const float decay = expf(a.cum[((b * a.H + h) * a.nchunks + c) * a.Q + len - 1]);
         float* S = a.states + (((b * a.nchunks + c) * a.H + h) * a.P) * a.N + idx;
         const float local = *S;
         *S = st;
@@ -233,7 +241,7 @@ __global__ void __launch_bounds__(kThreads) ssd_chunk_scan(const SsdArgs a) {
                 const float* br = s_b + s * (Nn + 1);
                 float dot = 0.0f;
                 for (int n = 0; n < Nn; ++n) dot = fmaf(cr[n], br[n], dot);
-                v = dot * __expf(s_cum[tt] - s_cum[ss]) * s_dl[ss];
+                v = dot * exp_t<T>(s_cum[tt] - s_cum[ss]) * s_dl[ss];
             }
             s_g[r * (kSub + 1) + s] = v;
         }
@@ -280,7 +288,7 @@ __global__ void __launch_bounds__(kThreads) ssd_chunk_scan(const SsdArgs a) {
     for (int i = 0; i < 4; ++i) {
         const int tt = r0 + ti + i;
         if (tt >= len) continue;
-        const float e = __expf(s_cum[tt]);
+        const float e = exp_t<T>(s_cum[tt]);
         const int64_t row = ((b * a.T + t0 + tt) * a.H + h) * a.P;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -288,15 +296,25 @@ __global__ void __launch_bounds__(kThreads) ssd_chunk_scan(const SsdArgs a) {
             if (p >= a.P) continue;
             const float xv = ld<T>(a.x, row + p);
             float y = acc[i][j] + e * off[i][j] + Dh * xv;
-            if (GATE) y *= silu(ld<T>(a.z, row + p));
+            if (GATE) y *= silu_t<sizeof(T) == 4>(ld<T>(a.z, row + p));
             reinterpret_cast<T*>(a.out)[row + p] = from_f32<T>(y);
         }
     }
 }
 
+// SSM_SSD_CUDA_CORES=1 keeps every shape on the CUDA-core kernels (a cross-check of the
+// tensor-core kernels; both compute the same chunk algebra).
+bool force_cuda_cores() {
+    static const bool v = [] {
+        const char* e = getenv("SSM_SSD_CUDA_CORES");
+        return e && e[0] == '1';
+    }();
+    return v;
+}
+
 struct SsdPlan {
     int64_t Q, nchunks;
-    size_t dl_off, cum_off, st_off, total;
+    size_t dl_off, cum_off, st_off, status_off, total;
 };
 
 SsdPlan ssd_plan(const ScanArgs& a) {
@@ -308,7 +326,8 @@ SsdPlan ssd_plan(const ScanArgs& a) {
     p.dl_off = 0;
     p.cum_off = align_up(vec, 256);
     p.st_off = p.cum_off + align_up(vec, 256);
-    p.total = p.st_off + align_up(st, 256);
+    p.status_off = p.st_off + align_up(st, 256);
+    p.total = p.status_off + 256;
     return p;
 }
 
@@ -340,6 +359,35 @@ cudaError_t ssd_launch_typed(const ScanArgs& a, void* ws, cudaStream_t stream) {
     const unsigned nP = (unsigned)((a.headdim + kTile - 1) / kTile);
     const unsigned nN = (unsigned)((a.dstate + kTile - 1) / kTile);
     const unsigned nTq = (unsigned)((pl.Q + kTile - 1) / kTile);
+    if (pl.nchunks > 0 && ssd_tc_supported(a, pl.Q) && !force_cuda_cores()) {
+        SsdTcArgs t;
+        t.x = (const __nv_bfloat16*)a.x;
+        t.dt = (const __nv_bfloat16*)a.dt;
+        t.z = (const __nv_bfloat16*)a.z;
+        t.B = (const __nv_bfloat16*)a.B;
+        t.C = (const __nv_bfloat16*)a.C;
+        t.A = a.A;
+        t.D = a.D;
+        t.dt_bias = a.dt_bias;
+        t.out = (__nv_bfloat16*)a.out;
+        t.dl = s.dl;
+        t.cum = s.cum;
+        t.states = s.states;
+        t.status = (int*)((char*)ws + pl.status_off);
+        t.T = a.seqlen;
+        t.H = a.nheads;
+        t.N = a.dstate;
+        t.G = a.ngroups;
+        t.Q = pl.Q;
+        t.nchunks = pl.nchunks;
+        cudaError_t e = ssd_tc_chunk_state(t, a.batch, stream);
+        if (e != cudaSuccess) return e;
+        ssd_state_pass<<<dim3((unsigned)((a.headdim * a.dstate + kThreads - 1) / kThreads), (unsigned)a.nheads, (unsigned)a.batch), kThreads, 0, stream>>>(s);
+        note_launches(1);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        return ssd_tc_chunk_scan(t, a.batch, a.z != nullptr, stream);
+    }
     if (pl.nchunks > 0) {
         ssd_chunk_state<T><<<dim3((unsigned)pl.nchunks, (unsigned)a.nheads * nP * nN, (unsigned)a.batch), kThreads, 0, stream>>>(s);
         note_launches(1);

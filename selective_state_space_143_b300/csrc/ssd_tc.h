@@ -1,0 +1,39 @@
+// Tensor-core (tcgen05) SSD chunk kernels: arguments and launchers.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ssm_internal.h"
+
+namespace ssm {
+
+struct SsdTcArgs {
+    const __nv_bfloat16* x;
+    const __nv_bfloat16* dt;
+    const __nv_bfloat16* z;
+    const __nv_bfloat16* B;
+    const __nv_bfloat16* C;
+    const float* A;
+    const float* D;
+    const float* dt_bias;
+    __nv_bfloat16* out;
+    float* dl;      // (b, H, nchunks, Q) Delta
+    float* cum;     // (b, H, nchunks, Q) inclusive cumsum of Delta*A_h within the chunk
+    float* states;  // (b, nchunks, H, P, N): S_c, then (after the carry pass) h_{c-1}
+    int* status;    // device status word (set to SSM_ERR_TIMEOUT if a bounded wait ran out)
+    int64_t T, H, N, G, Q, nchunks;
+};
+
+// True when the shape is one the tensor-core kernels take (bf16, headdim 64,
+// dstate in {32, 64, 128, 256}, chunk 128 or 256, even heads per group).
+bool ssd_tc_supported(const ScanArgs& a, int64_t Q);
+
+// S_c for every (chunk, head) into states; also writes dl and cum.
+cudaError_t ssd_tc_chunk_state(const SsdTcArgs& s, int64_t batch, cudaStream_t stream);
+
+// out for every chunk, reading h_{c-1} from states (after the carry pass).
+cudaError_t ssd_tc_chunk_scan(const SsdTcArgs& s, int64_t batch, bool gate, cudaStream_t stream);
+
+}  // namespace ssm

@@ -59,7 +59,9 @@ int check_args(const void* x, const void* dt, const float* A, const void* B, con
                const float* final_state, const ssm_shape* s) {
     const int rc = check_shape(s);
     if (rc != SSM_OK) return rc;
-    if (!x || !dt || !A || !B || !C || !out) return SSM_ERR_NULL;
+    // x, dt, B, C and out may be NULL only when they hold no elements
+    const bool empty = s->batch == 0 || s->seqlen == 0;
+    if (!A || (!empty && (!x || !dt || !B || !C || !out))) return SSM_ERR_NULL;
     const void* ptrs[] = {x, dt, A, B, C, D, z, dt_bias, out, final_state};
     for (const void* p : ptrs)
         if (!aligned16(p)) return SSM_ERR_ALIGN;

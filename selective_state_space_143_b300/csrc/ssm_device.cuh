@@ -41,6 +41,57 @@ __device__ __forceinline__ float silu(float z) {
     return __fdividef(z, 1.0f + ex2(-z * kLog2e));
 }
 
+// Accurate variants (CUDA's log1pf / expf / IEEE division) for fp32 inputs, where the
+// tolerance is tighter than the approximate instructions allow.
+__device__ __forceinline__ float softplus_precise(float v) {
+    return fmaxf(v, 0.0f) + log1pf(expf(-fabsf(v)));
+}
+__device__ __forceinline__ float silu_precise(float z) { return z / (1.0f + expf(-z)); }
+
+// Fast path for 16-bit inputs, accurate path for fp32 inputs.
+template <bool PRECISE>
+__device__ __forceinline__ float softplus_t(float v) {
+    return PRECISE ? softplus_precise(v) : softplus(v);
+}
+template <bool PRECISE>
+__device__ __forceinline__ float silu_t(float z) {
+    return PRECISE ? silu_precise(z) : silu(z);
+}
+
+// softplus of two values with packed fp32x2 arithmetic where it applies.
+__device__ __forceinline__ float2 softplus2(float2 v) {
+    const float e0 = ex2(-fabsf(v.x) * kLog2e), e1 = ex2(-fabsf(v.y) * kLog2e);
+    const float2 e = make_float2(e0, e1);
+    // e (1 - e (1/2 - e (1/3 - e/4)))
+    float2 p = __ffma2_rn(e, make_float2(-0.25f, -0.25f), make_float2(0.33333334f, 0.33333334f));
+    p = __ffma2_rn(e, make_float2(-p.x, -p.y), make_float2(0.5f, 0.5f));
+    p = __ffma2_rn(e, make_float2(-p.x, -p.y), make_float2(1.0f, 1.0f));
+    p = __fmul2_rn(e, p);
+    const float2 one_e = __fadd2_rn(e, make_float2(1.0f, 1.0f));
+    const float l0 = lg2(one_e.x) * kLn2, l1 = lg2(one_e.y) * kLn2;
+    const float r0 = e0 < 0.015625f ? p.x : l0;
+    const float r1 = e1 < 0.015625f ? p.y : l1;
+    return __fadd2_rn(make_float2(fmaxf(v.x, 0.0f), fmaxf(v.y, 0.0f)), make_float2(r0, r1));
+}
+
+// SiLU of two values.
+__device__ __forceinline__ float2 silu2(float2 z) {
+    const float2 m = __fmul2_rn(z, make_float2(-kLog2e, -kLog2e));
+    const float2 d = __fadd2_rn(make_float2(ex2(m.x), ex2(m.y)), make_float2(1.0f, 1.0f));
+    return make_float2(__fdividef(z.x, d.x), __fdividef(z.y, d.y));
+}
+
+template <bool PRECISE>
+__device__ __forceinline__ float2 softplus2_t(float2 v) {
+    if (PRECISE) return make_float2(softplus_precise(v.x), softplus_precise(v.y));
+    return softplus2(v);
+}
+template <bool PRECISE>
+__device__ __forceinline__ float2 silu2_t(float2 z) {
+    if (PRECISE) return make_float2(silu_precise(z.x), silu_precise(z.y));
+    return silu2(z);
+}
+
 template <typename T>
 __device__ __forceinline__ float to_f32(T v);
 template <>
