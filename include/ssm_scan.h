@@ -118,6 +118,28 @@ int ssm_scan_fwd_ws(const void* x, const void* dt, const float* A, const void* B
                     float* final_state, const ssm_shape* shape, void* workspace,
                     size_t workspace_bytes, ssm_stream_t stream);
 
+/*
+ * As ssm_scan_fwd, but the call allocates no device memory.  (This entry point has
+ * no counterpart in the papers: it is a deployment variant of the same scan.)
+ * It is for callers that must not allocate during a scan -- for example an
+ * application that reserves all device memory up front for its own allocator, or a
+ * latency-critical loop where an allocation could synchronise the device or fail
+ * under memory pressure.  Inputs and outputs are passed as for ssm_scan_fwd.
+ * Scratch: a fixed 64 MiB device array inside the library, held by every GPU that
+ * uses it until the process exits.  Shapes whose scratch
+ * (ssm_scan_workspace_size) exceeds 64 MiB are rejected with SSM_ERR_ALLOC before
+ * anything is queued; shapes that need no scratch always run.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before any
+ * stream capture.  Every call shares the one array per device, so calls that can
+ * overlap on the GPU (different streams, or host threads without ordering) race on
+ * it; order them on one stream.  Nothing in the array needs clearing between calls.
+ */
+int ssm_scan_fwd_noalloc(const void* x, const void* dt, const float* A, const void* B,
+                         const void* C, const float* D, const void* z, const float* dt_bias,
+                         void* out, float* final_state, const ssm_shape* shape,
+                         ssm_stream_t stream);
+
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char* ssm_strerror(int status);
 

@@ -27,8 +27,8 @@ SSM_F32 = 0
 SSM_BF16 = 1
 
 # Every function declared in include/ssm_scan.h.
-EXPORTED = ("ssm_scan_fwd", "ssm_scan_fwd_ws", "ssm_scan_workspace_size", "ssm_strerror",
-            "ssm_kernel_launch_count", "ssm_abi_version")
+EXPORTED = ("ssm_scan_fwd", "ssm_scan_fwd_ws", "ssm_scan_workspace_size", "ssm_scan_fwd_noalloc",
+            "ssm_strerror", "ssm_kernel_launch_count", "ssm_abi_version")
 
 
 class ssm_shape(ctypes.Structure):
@@ -75,6 +75,8 @@ def load() -> ctypes.CDLL:
         lib.ssm_scan_fwd_ws.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sp, vp,
                                         ctypes.c_size_t, vp]
         lib.ssm_scan_fwd_ws.restype = ctypes.c_int
+        lib.ssm_scan_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sp, vp]
+        lib.ssm_scan_fwd_noalloc.restype = ctypes.c_int
         lib.ssm_scan_workspace_size.argtypes = [sp]
         lib.ssm_scan_workspace_size.restype = ctypes.c_size_t
         lib.ssm_strerror.argtypes = [ctypes.c_int]
