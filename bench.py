@@ -70,7 +70,7 @@ def algorithmic_bytes(w) -> int:
     """Bytes the method must move: inputs, outputs, parameters, final state."""
     E = 2 if w.dtype == "bf16" else 4
     b, T, H, P, N, G = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups
-    per_tok_ch = (2 + (1 if w.gate else 0)) * E + E  # x, z?, out  (+dt below)
+    per_tok_ch = (2 + (1 if w.gate else 0)) * E  # x, out, z (dt below)
     nbytes = b * T * H * P * per_tok_ch
     nbytes += b * T * H * E                      # dt: per channel (diag) or per head (ssd)
     nbytes += 2 * b * T * G * N * E              # B, C
@@ -332,6 +332,16 @@ def run_ours(args, w):
         fl = algorithmic_flops(w)
         roof["tensor_tflops"] = fl / (ms_step * 1e-3) / 1e12
         roof["tensor_frac"] = roof["tensor_tflops"] / peaks["bf16_tflops"]
+    else:
+        # The diagonal scan needs one exponential per state entry and step; B300's SFU
+        # retires 32 ex2 per clock per SM (measured), so its ceiling is
+        # 148 x 32 x SM clock.
+        sm_mhz = float(peaks.get("sm_max_mhz", 2032.0))
+        sfu_peak = 148 * 32 * sm_mhz * 1e6
+        exps = float(w.token_channels * w.dstate)
+        roof["sfu"] = {"achieved": exps / (ms_step * 1e-3), "peak": sfu_peak, "unit": "exp/s",
+                       "frac": exps / (ms_step * 1e-3) / sfu_peak,
+                       "note": "one ex2 per state entry and step; peak = 148 SMs x 32/clk x max SM clock"}
 
     # ---- end to end through the public API from pinned host buffers
     e2e = None

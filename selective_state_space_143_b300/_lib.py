@@ -49,7 +49,9 @@ _lib = None
 
 
 def path() -> str:
-    return _build.OUT
+    """The library this process loads: SSM_LIB_PATH if set (another build of the same
+    sources, e.g. with different compile-time options), else the in-tree build."""
+    return os.environ.get("SSM_LIB_PATH") or _build.OUT
 
 
 def load() -> ctypes.CDLL:
@@ -58,7 +60,7 @@ def load() -> ctypes.CDLL:
     with _lock:
         if _lib is not None:
             return _lib
-        if not _build.up_to_date():
+        if path() == _build.OUT and not _build.up_to_date():
             try:
                 _build.build()
             except Exception as exc:  # no nvcc or a compile error: fail loudly
@@ -66,7 +68,7 @@ def load() -> ctypes.CDLL:
                     raise RuntimeError(
                         "libssmscan.so is missing and could not be built "
                         f"({exc}); run `python -m selective_state_space_143_b300.build`") from exc
-        lib = ctypes.CDLL(_build.OUT)
+        lib = ctypes.CDLL(path())
         vp = ctypes.c_void_p
         fp = ctypes.POINTER(ctypes.c_float)
         sp = ctypes.POINTER(ssm_shape)

@@ -45,6 +45,10 @@ namespace ssm {
 namespace {
 
 constexpr int kTT = 32;      // time steps per tile
+#ifndef SSM_DIAG_ROWS
+#define SSM_DIAG_ROWS 4
+#endif
+constexpr int kRB = SSM_DIAG_ROWS;  // rows whose decays are formed together
 constexpr int kStages = 2;   // cp.async double buffer
 
 // LPC lanes per channel, WARPS warps per block.
@@ -171,29 +175,37 @@ __global__ void __launch_bounds__(32 * WARPS) diag_scan_kernel(const DiagKernelA
     const float2 d2 = (pair_ok && a.D) ? make_float2(a.D[cA], a.D[cA + 1]) : make_float2(0.0f, 0.0f);
     float2 dsum2 = make_float2(0.0f, 0.0f);  // sum of Delta (state-only pass)
 
-    float A2[NPT];
-    float h[NPT];
+    // state entries and decay rates (times log2 e) in fp32 pairs, as the packed
+    // fp32x2 instructions take them
+    float2 A2[NPT / 2];
+    float2 h[NPT / 2];
 #pragma unroll
-    for (int j = 0; j < NPT; ++j) {
-        const int n = g * NPT + j;
-        A2[j] = (c_ok && n < a.N) ? a.A[c * a.N + n] * kLog2e : 0.0f;
-        h[j] = 0.0f;
+    for (int k = 0; k < NPT / 2; ++k) {
+        const int n = g * NPT + 2 * k;
+        A2[k].x = (c_ok && n < a.N) ? a.A[c * a.N + n] * kLog2e : 0.0f;
+        A2[k].y = (c_ok && n + 1 < a.N) ? a.A[c * a.N + n + 1] * kLog2e : 0.0f;
+        h[k] = make_float2(0.0f, 0.0f);
     }
     if (!STATE_ONLY) {
         // state entering this segment: the initial state decayed through the earlier
         // segments plus their local end states
+        if (c_ok && a.init) {
+            const float* hi = a.init + (b * a.dim + c) * a.N;
 #pragma unroll
-        for (int j = 0; j < NPT; ++j) {
-            const int n = g * NPT + j;
-            if (c_ok && n < a.N && a.init) h[j] = a.init[(b * a.dim + c) * a.N + n];
+            for (int k = 0; k < NPT / 2; ++k) {
+                const int n = g * NPT + 2 * k;
+                if (n < a.N) h[k].x = hi[n];
+                if (n + 1 < a.N) h[k].y = hi[n + 1];
+            }
         }
         for (int s = 0; s < seg && c_ok; ++s) {
             const float dsum = a.seg_dsum[((int64_t)s * gridDim.z + b) * a.dim + c];
             const float* Hs = a.seg_h + (((int64_t)s * gridDim.z + b) * a.dim + c) * a.N;
 #pragma unroll
-            for (int j = 0; j < NPT; ++j) {
-                const int n = g * NPT + j;
-                if (n < a.N) h[j] = ex2(A2[j] * dsum) * h[j] + Hs[n];
+            for (int k = 0; k < NPT / 2; ++k) {
+                const int n = g * NPT + 2 * k;
+                if (n < a.N) h[k].x = ex2(A2[k].x * dsum) * h[k].x + Hs[n];
+                if (n + 1 < a.N) h[k].y = ex2(A2[k].y * dsum) * h[k].y + Hs[n + 1];
             }
         }
     }
@@ -259,52 +271,39 @@ __global__ void __launch_bounds__(32 * WARPS) diag_scan_kernel(const DiagKernelA
         }
         __syncthreads();
 
-        // ---- B: the recurrence over the tile's rows, 4 rows at a time.  The decays and
-        // input terms of the 4 rows do not depend on h, so they are formed first (32
-        // independent exponentials per lane for NPT = 8), then the dependent updates run.
+        // ---- B: the recurrence over the tile's rows, kRB rows at a time.  The decays
+        // and input terms of those rows do not depend on h, so they are formed first
+        // (kRB * NPT independent exponentials per lane), then the dependent updates run.
         // Rows past the tile's end have Delta = 0 and x*Delta = 0, so they leave h as is.
-        for (int rb = 0; rb < rows; rb += 4) {
-            float av[4][NPT], ub[4][NPT];
+        for (int rb = 0; rb < rows; rb += kRB) {
+            float2 av[kRB][NPT / 2], ub[kRB][NPT / 2];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < kRB; ++i) {
                 const float2 dv = du[(rb + i) * CPB + cc];
                 const float2 dd = make_float2(dv.x, dv.x);
                 const float2 uu = make_float2(dv.y, dv.y);
 #pragma unroll
-                for (int j = 0; j < NPT; j += 4) {
-                    const float4 bq = *reinterpret_cast<const float4*>(&Bf[(rb + i) * NK + g * NPT + j]);
-                    const float2 dA0 = __fmul2_rn(dd, make_float2(A2[j], A2[j + 1]));
-                    const float2 dA1 = __fmul2_rn(dd, make_float2(A2[j + 2], A2[j + 3]));
-                    av[i][j] = ex2(dA0.x);
-                    av[i][j + 1] = ex2(dA0.y);
-                    av[i][j + 2] = ex2(dA1.x);
-                    av[i][j + 3] = ex2(dA1.y);
-                    const float2 u0 = __fmul2_rn(uu, make_float2(bq.x, bq.y));
-                    const float2 u1 = __fmul2_rn(uu, make_float2(bq.z, bq.w));
-                    ub[i][j] = u0.x;
-                    ub[i][j + 1] = u0.y;
-                    ub[i][j + 2] = u1.x;
-                    ub[i][j + 3] = u1.y;
+                for (int k = 0; k < NPT / 2; k += 2) {
+                    const float4 bq = *reinterpret_cast<const float4*>(&Bf[(rb + i) * NK + g * NPT + 2 * k]);
+                    const float2 dA0 = __fmul2_rn(dd, A2[k]);
+                    const float2 dA1 = __fmul2_rn(dd, A2[k + 1]);
+                    av[i][k] = make_float2(ex2(dA0.x), ex2(dA0.y));
+                    av[i][k + 1] = make_float2(ex2(dA1.x), ex2(dA1.y));
+                    ub[i][k] = __fmul2_rn(uu, make_float2(bq.x, bq.y));
+                    ub[i][k + 1] = __fmul2_rn(uu, make_float2(bq.z, bq.w));
                 }
             }
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < kRB; ++i) {
                 float2 ya = make_float2(0.0f, 0.0f), yb = make_float2(0.0f, 0.0f);
 #pragma unroll
-                for (int j = 0; j < NPT; j += 4) {
-                    const float2 h0 = __ffma2_rn(make_float2(av[i][j], av[i][j + 1]), make_float2(h[j], h[j + 1]),
-                                                 make_float2(ub[i][j], ub[i][j + 1]));
-                    const float2 h1 = __ffma2_rn(make_float2(av[i][j + 2], av[i][j + 3]),
-                                                 make_float2(h[j + 2], h[j + 3]),
-                                                 make_float2(ub[i][j + 2], ub[i][j + 3]));
-                    h[j] = h0.x;
-                    h[j + 1] = h0.y;
-                    h[j + 2] = h1.x;
-                    h[j + 3] = h1.y;
+                for (int k = 0; k < NPT / 2; k += 2) {
+                    h[k] = __ffma2_rn(av[i][k], h[k], ub[i][k]);
+                    h[k + 1] = __ffma2_rn(av[i][k + 1], h[k + 1], ub[i][k + 1]);
                     if (!STATE_ONLY) {
-                        const float4 cq = *reinterpret_cast<const float4*>(&Cf[(rb + i) * NK + g * NPT + j]);
-                        ya = __ffma2_rn(make_float2(cq.x, cq.y), h0, ya);
-                        yb = __ffma2_rn(make_float2(cq.z, cq.w), h1, yb);
+                        const float4 cq = *reinterpret_cast<const float4*>(&Cf[(rb + i) * NK + g * NPT + 2 * k]);
+                        ya = __ffma2_rn(make_float2(cq.x, cq.y), h[k], ya);
+                        yb = __ffma2_rn(make_float2(cq.z, cq.w), h[k + 1], yb);
                     }
                 }
                 if (!STATE_ONLY) {
@@ -345,9 +344,10 @@ __global__ void __launch_bounds__(32 * WARPS) diag_scan_kernel(const DiagKernelA
         if (c_ok) {
             float* Hs = a.seg_h + (((int64_t)seg * gridDim.z + b) * a.dim + c) * a.N;
 #pragma unroll
-            for (int j = 0; j < NPT; ++j) {
-                const int n = g * NPT + j;
-                if (n < a.N) Hs[n] = h[j];
+            for (int k = 0; k < NPT / 2; ++k) {
+                const int n = g * NPT + 2 * k;
+                if (n < a.N) Hs[n] = h[k].x;
+                if (n + 1 < a.N) Hs[n + 1] = h[k].y;
             }
         }
         // the RS threads of a pair each summed a subset of rows
@@ -366,10 +366,12 @@ __global__ void __launch_bounds__(32 * WARPS) diag_scan_kernel(const DiagKernelA
             }
         }
     } else if (a.final_state && seg == a.nseg - 1 && c_ok) {
+        float* fs = a.final_state + (b * a.dim + c) * a.N;
 #pragma unroll
-        for (int j = 0; j < NPT; ++j) {
-            const int n = g * NPT + j;
-            if (n < a.N) a.final_state[(b * a.dim + c) * a.N + n] = h[j];
+        for (int k = 0; k < NPT / 2; ++k) {
+            const int n = g * NPT + 2 * k;
+            if (n < a.N) fs[n] = h[k].x;
+            if (n + 1 < a.N) fs[n + 1] = h[k].y;
         }
     }
 }

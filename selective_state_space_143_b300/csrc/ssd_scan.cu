@@ -164,21 +164,46 @@ __global__ void __launch_bounds__(kThreads) ssd_chunk_state(const SsdArgs a) {
         }
 }
 
-// grid: (ceil(P*N / 256), H, b).  In place: states[c] <- state entering chunk c.
+// grid: (ceil(P*N / 4 / 256), H, b).  In place: states[c] <- state entering chunk c,
+// h_c = exp(s_last,c) h_{c-1} + S_c.  Each thread carries 4 consecutive state entries;
+// the loads of S_c do not depend on the carry, so 8 chunks are fetched ahead.
+constexpr int kPassAhead = 8;
+
 __global__ void __launch_bounds__(kThreads) ssd_state_pass(const SsdArgs a) {
-    const int64_t idx = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int64_t i4 = (int64_t)blockIdx.x * kThreads + threadIdx.x;  // float4 index
     const int64_t h = blockIdx.y, b = blockIdx.z;
-    if (idx >= a.P * a.N) return;
-    float st = a.init ? a.init[((b * a.H + h) * a.P) * a.N + idx] : 0.0f;
-    for (int64_t c = 0; c < a.nchunks; ++c) {
-        const int len = (int)min(a.Q, a.T - c * a.Q);
-        const float decay = expf(a.cum[((b * a.H + h) * a.nchunks + c) * a.Q + len - 1]);
-        float* S = a.states + (((b * a.nchunks + c) * a.H + h) * a.P) * a.N + idx;
-        const float local = *S;
-        *S = st;
-        st = fmaf(decay, st, local);
+    const int64_t PN = a.P * a.N;
+    if (i4 * 4 >= PN) return;
+    float4 st = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (a.init) st = *reinterpret_cast<const float4*>(a.init + (b * a.H + h) * PN + i4 * 4);
+    const int64_t cstride = a.H * PN;  // floats between consecutive chunks of one head
+    float* base = a.states + (b * a.nchunks * a.H + h) * PN + i4 * 4;
+    const float* cum = a.cum + (b * a.H + h) * a.nchunks * a.Q;
+    for (int64_t c0 = 0; c0 < a.nchunks; c0 += kPassAhead) {
+        float4 S[kPassAhead];
+        float dec[kPassAhead];
+#pragma unroll
+        for (int j = 0; j < kPassAhead; ++j) {
+            const int64_t c = c0 + j;
+            if (c < a.nchunks) {
+                S[j] = *reinterpret_cast<const float4*>(base + c * cstride);
+                const int len = (int)min(a.Q, a.T - c * a.Q);
+                dec[j] = expf(cum[c * a.Q + len - 1]);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kPassAhead; ++j) {
+            const int64_t c = c0 + j;
+            if (c < a.nchunks) {
+                *reinterpret_cast<float4*>(base + c * cstride) = st;
+                st.x = fmaf(dec[j], st.x, S[j].x);
+                st.y = fmaf(dec[j], st.y, S[j].y);
+                st.z = fmaf(dec[j], st.z, S[j].z);
+                st.w = fmaf(dec[j], st.w, S[j].w);
+            }
+        }
     }
-    if (a.final_state) a.final_state[((b * a.H + h) * a.P) * a.N + idx] = st;
+    if (a.final_state) *reinterpret_cast<float4*>(a.final_state + (b * a.H + h) * PN + i4 * 4) = st;
 }
 
 // grid: (nchunks, H * nP, b * nTq); output tile of 64 rows x 64 head channels.
@@ -382,7 +407,7 @@ cudaError_t ssd_launch_typed(const ScanArgs& a, void* ws, cudaStream_t stream) {
         t.nchunks = pl.nchunks;
         cudaError_t e = ssd_tc_chunk_state(t, a.batch, stream);
         if (e != cudaSuccess) return e;
-        ssd_state_pass<<<dim3((unsigned)((a.headdim * a.dstate + kThreads - 1) / kThreads), (unsigned)a.nheads, (unsigned)a.batch), kThreads, 0, stream>>>(s);
+        ssd_state_pass<<<dim3((unsigned)((a.headdim * a.dstate / 4 + kThreads - 1) / kThreads), (unsigned)a.nheads, (unsigned)a.batch), kThreads, 0, stream>>>(s);
         note_launches(1);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
@@ -392,7 +417,7 @@ cudaError_t ssd_launch_typed(const ScanArgs& a, void* ws, cudaStream_t stream) {
         ssd_chunk_state<T><<<dim3((unsigned)pl.nchunks, (unsigned)a.nheads * nP * nN, (unsigned)a.batch), kThreads, 0, stream>>>(s);
         note_launches(1);
     }
-    ssd_state_pass<<<dim3((unsigned)((a.headdim * a.dstate + kThreads - 1) / kThreads), (unsigned)a.nheads, (unsigned)a.batch), kThreads, 0, stream>>>(s);
+    ssd_state_pass<<<dim3((unsigned)((a.headdim * a.dstate / 4 + kThreads - 1) / kThreads), (unsigned)a.nheads, (unsigned)a.batch), kThreads, 0, stream>>>(s);
     note_launches(1);
     if (pl.nchunks > 0) {
         const size_t smem = sizeof(float) * (2 * pl.Q + kTile * (a.dstate + 1) + kSub * (a.dstate + 1) +

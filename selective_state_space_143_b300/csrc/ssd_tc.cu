@@ -32,7 +32,7 @@ namespace ssm {
 namespace {
 
 constexpr int kP = 64;         // headdim handled here
-constexpr int kThreads = 128;  // 4 warps: TMEM lanes 0..127
+constexpr int kThreads = 256;  // 8 warps: warp w reads TMEM lanes 32*(w%4).., column half w/4
 constexpr int kStatusTimeout = 8;
 
 __device__ __forceinline__ void cp_async16(uint32_t saddr, const void* gmem, bool valid) {
@@ -48,7 +48,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-// Inclusive prefix sum of v over the block (128 threads, one value each); s_warp: 4 floats.
+// Inclusive prefix sum of v over the block (one value per thread); s_warp: one float per warp.
 __device__ __forceinline__ float block_incl_scan(float v, float* s_warp) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -64,29 +64,32 @@ __device__ __forceinline__ float block_incl_scan(float v, float* s_warp) {
     return v + add;
 }
 
-// Delta_s and the inclusive cumulative sum of Delta_s A_h for s in [0, len) of chunk c,
-// for s < Q (two values per thread: s = 2*tid, 2*tid + 1).  Rows past len get Delta 0.
+// Delta_s and the inclusive cumulative sum of Delta_s A_h for s in [0, Q) of chunk c
+// (one row per thread; Q <= 256).  Rows past len get Delta 0.
 __device__ void delta_cumsum(const SsdTcArgs& a, int64_t b, int64_t h, int64_t c, int len,
                              float* s_dl, float* s_cum, float* s_warp) {
-    const int tid = threadIdx.x;
-    const float Ah = a.A[h];
-    const float bias = a.dt_bias ? a.dt_bias[h] : 0.0f;
-    float d0 = 0.0f, d1 = 0.0f;
-    const int s0 = 2 * tid;
-    if (s0 < a.Q) {
-        const int64_t base = (b * a.T + c * a.Q + s0) * a.H + h;
-        if (s0 < len) d0 = softplus(__bfloat162float(a.dt[base]) + bias);
-        if (s0 + 1 < len) d1 = softplus(__bfloat162float(a.dt[base + a.H]) + bias);
-    }
-    const float pair = d0 * Ah + d1 * Ah;
-    const float incl = block_incl_scan(pair, s_warp);
-    if (s0 < a.Q) {
-        s_dl[s0] = d0;
-        s_dl[s0 + 1] = d1;
-        s_cum[s0 + 1] = incl;
-        s_cum[s0] = incl - d1 * Ah;
+    const int s = threadIdx.x;
+    float d = 0.0f;
+    if (s < len) d = softplus(__bfloat162float(a.dt[(b * a.T + c * a.Q + s) * a.H + h]) + (a.dt_bias ? a.dt_bias[h] : 0.0f));
+    const float incl = block_incl_scan(d * a.A[h], s_warp);
+    if (s < a.Q) {
+        s_dl[s] = d;
+        s_cum[s] = incl;
     }
     __syncthreads();
+}
+
+// Tile fill orders that keep 16-byte shared-memory stores free of bank conflicts: the
+// row index inside a core matrix (8 rows x 16 bytes, contiguous) runs fastest.
+// K-major tile, KC chunks of 8 elements per row: i -> (row, chunk).
+__device__ __forceinline__ void kmajor_item(int i, int KC, int& row, int& kc) {
+    row = (i / (8 * KC)) * 8 + (i & 7);
+    kc = (i >> 3) % KC;
+}
+// MN-major tile, MC chunks of 8 elements along M/N: i -> (k, chunk).
+__device__ __forceinline__ void mnmajor_item(int i, int MC, int& k, int& mc) {
+    k = (i / (8 * MC)) * 8 + (i & 7);
+    mc = (i >> 3) % MC;
 }
 
 __device__ __forceinline__ void report_timeout(int* status) {
@@ -116,7 +119,7 @@ template <int N>
 __global__ void __launch_bounds__(kThreads) ssd_state_tc(const SsdTcArgs a) {
     constexpr int NB = N < 128 ? N : 128;
     extern __shared__ __align__(1024) unsigned char smem[];
-    __shared__ float s_dl[2][256], s_cum[2][256], s_w[2][256], s_warp[4];
+    __shared__ float s_dl[2][256], s_cum[2][256], s_w[2][256], s_warp[8];
     __shared__ uint32_t s_tmem;
     __shared__ __align__(8) uint64_t s_mbar;
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -131,7 +134,9 @@ __global__ void __launch_bounds__(kThreads) ssd_state_tc(const SsdTcArgs a) {
     auto load_B = [&](int nb) {
         const uint32_t base = tc::smem_u32(sB);
         for (int i = tid; i < Q * (NB / 8); i += kThreads) {
-            const int s = i / (NB / 8), n0 = (i % (NB / 8)) * 8;
+            int s, nc;
+            mnmajor_item(i, NB / 8, s, nc);
+            const int n0 = nc * 8;
             const bool ok = s < len;
             const __nv_bfloat16* src = a.B + (ok ? (((b * a.T + c * a.Q + s) * a.G + g) * a.N + nb * NB + n0) : 0);
             cp_async16(base + tc::off_mnmajor(n0, s, NB), src, ok);
@@ -153,8 +158,11 @@ __global__ void __launch_bounds__(kThreads) ssd_state_tc(const SsdTcArgs a) {
     // Xd = w_s x_s for both heads, split hi/lo, MN-major (8 consecutive p at one s)
     {
         const uint32_t bh = tc::smem_u32(sXh), bl = tc::smem_u32(sXl);
+#pragma unroll 4
         for (int i = tid; i < Q * 16; i += kThreads) {
-            const int s = i / 16, m0 = (i % 16) * 8;  // m = head_local * 64 + p
+            int s, mc;
+            mnmajor_item(i, 16, s, mc);
+            const int m0 = mc * 8;  // m = head_local * 64 + p
             const int hl = m0 / kP, p0 = m0 % kP;
             uint32_t hi[4] = {0, 0, 0, 0}, lo[4] = {0, 0, 0, 0};
             if (s < len) {
@@ -211,13 +219,16 @@ __global__ void __launch_bounds__(kThreads) ssd_state_tc(const SsdTcArgs a) {
     ok = tc::mbar_wait(&s_mbar, phase) && ok;
     tc::fence_after_sync();
     if (ok) {
-        // row m = lane: (head h0 + m/64, p = m%64) -> states[b, c, h, p, :]
-        const int m = warp * 32 + (tid & 31);
+        // row m = lane: (head h0 + m/64, p = m%64) -> states[b, c, h, p, :]; warps 4-7 take
+        // the upper half of the columns
+        const int q = warp & 3;
+        const int m = q * 32 + (tid & 31);
         float* dst = a.states + (((b * a.nchunks + c) * a.H + h0 + m / kP) * kP + (m % kP)) * a.N;
+        constexpr int NH = N / 2 < 16 ? 16 : N / 2;
 #pragma unroll 1
-        for (int n0 = 0; n0 < N; n0 += 16) {
+        for (int n0 = (warp >> 2) * NH; n0 < N && n0 < ((warp >> 2) + 1) * NH; n0 += 16) {
             float v[16];
-            tc::tmem_ld16(tc::taddr(tmem, warp * 32, n0), v);
+            tc::tmem_ld16(tc::taddr(tmem, q * 32, n0), v);
 #pragma unroll
             for (int j = 0; j < 16; j += 4) *reinterpret_cast<float4*>(dst + n0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
         }
@@ -266,14 +277,18 @@ __global__ void __launch_bounds__(kThreads) ssd_scan_tc(const SsdTcArgs a, int h
     {
         const uint32_t cb = tc::smem_u32(sC), bb = tc::smem_u32(sB);
         for (int i = tid; i < 128 * (N / 8); i += kThreads) {
-            const int r = i / (N / 8), n0 = (i % (N / 8)) * 8;
+            int r, nc;
+            kmajor_item(i, N / 8, r, nc);
+            const int n0 = nc * 8;
             const int s = t0 + r;
             const bool ok = s < len;
             const __nv_bfloat16* src = a.C + (ok ? (((b * a.T + c * a.Q + s) * a.G + g) * a.N + n0) : 0);
             cp_async16(cb + tc::off_kmajor(r, n0, N), src, ok);
         }
         for (int i = tid; i < SW * (N / 8); i += kThreads) {
-            const int s = i / (N / 8), n0 = (i % (N / 8)) * 8;
+            int s, nc;
+            kmajor_item(i, N / 8, s, nc);
+            const int n0 = nc * 8;
             const bool ok = s < len;
             const __nv_bfloat16* src = a.B + (ok ? (((b * a.T + c * a.Q + s) * a.G + g) * a.N + n0) : 0);
             cp_async16(bb + tc::off_kmajor(s, n0, N), src, ok);
@@ -306,11 +321,13 @@ __global__ void __launch_bounds__(kThreads) ssd_scan_tc(const SsdTcArgs a, int h
     phase ^= 1;
     tc::fence_after_sync();
 
-    const int r = warp * 32 + (tid & 31);  // my row (TMEM lane) within the half
+    const int q = warp & 3;                  // TMEM lane quarter of this warp
+    const int chalf = warp >> 2;             // warps 4-7 take the upper half of the columns
+    const int r = q * 32 + (tid & 31);       // my row (TMEM lane) within the half
     const int t = t0 + r;                    // row within the chunk
     const bool row_ok = t < len;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const int t_warp_max = t0 + warp * 32 + 31;  // tcgen05.ld is warp-collective
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    const int t_warp_max = t0 + q * 32 + 31;  // tcgen05.ld is warp-collective
 
     for (int hi = 0; hi < heads_per_cta && ok; ++hi) {
         const int64_t h = hbeg + hi;
@@ -325,7 +342,9 @@ __global__ void __launch_bounds__(kThreads) ssd_scan_tc(const SsdTcArgs a, int h
         {
             const uint32_t xb = tc::smem_u32(sXh);
             for (int i = tid; i < SW * 8; i += kThreads) {
-                const int s = i / 8, p0 = (i % 8) * 8;
+                int s, pc;
+                mnmajor_item(i, 8, s, pc);
+                const int p0 = pc * 8;
                 const bool okr = s < len;
                 const __nv_bfloat16* src = a.x + (okr ? (((b * a.T + c * a.Q + s) * a.H + h) * kP + p0) : 0);
                 cp_async16(xb + tc::off_mnmajor(p0, s, kP), src, okr);
@@ -335,8 +354,11 @@ __global__ void __launch_bounds__(kThreads) ssd_scan_tc(const SsdTcArgs a, int h
         {
             const uint32_t hb = tc::smem_u32(sHh), lb = tc::smem_u32(sHl);
             const float* hs = a.states + ((b * a.nchunks + c) * a.H + h) * (int64_t)kP * a.N;
+#pragma unroll 2
             for (int i = tid; i < kP * (N / 8); i += kThreads) {
-                const int p = i / (N / 8), n0 = (i % (N / 8)) * 8;
+                int p, nc;
+                kmajor_item(i, N / 8, p, nc);
+                const int n0 = nc * 8;
                 const float4 v0 = *reinterpret_cast<const float4*>(hs + (int64_t)p * a.N + n0);
                 const float4 v1 = *reinterpret_cast<const float4*>(hs + (int64_t)p * a.N + n0 + 4);
                 uint32_t qh[4], ql[4];
@@ -362,7 +384,7 @@ __global__ void __launch_bounds__(kThreads) ssd_scan_tc(const SsdTcArgs a, int h
             // M'[t, s] = G[t, s] exp(cum_t - cum_s) Delta_s for s <= t, hi/lo, K-major
             {
                 const uint32_t mh = tc::smem_u32(sMh), ml = tc::smem_u32(sMl);
-                for (int s0 = 128 * kp; s0 < 128 * kp + 128; s0 += 16) {
+                for (int s0 = 128 * kp + 64 * chalf; s0 < 128 * kp + 64 * chalf + 64; s0 += 16) {
                     uint32_t ph[8], pl[8];
                     if (s0 <= t_warp_max) {
                         float gv[16];
@@ -419,7 +441,7 @@ __global__ void __launch_bounds__(kThreads) ssd_scan_tc(const SsdTcArgs a, int h
             const float Dh = a.D ? a.D[h] : 0.0f;
             const int64_t row = ((b * a.T + c * a.Q + t) * a.H + h) * kP;
 #pragma unroll 1
-            for (int p0 = 0; p0 < kP; p0 += 16) {
+            for (int p0 = 32 * chalf; p0 < 32 * chalf + 32; p0 += 16) {
                 float yd[16], yo[16];
                 tc::tmem_ld16(tYd + lane_base + (uint32_t)p0, yd);
                 tc::tmem_ld16(tYo + lane_base + (uint32_t)p0, yo);
