@@ -44,12 +44,9 @@
 namespace ssm {
 namespace {
 
-constexpr int kTT = 32;      // time steps per tile
-#ifndef SSM_DIAG_ROWS
-#define SSM_DIAG_ROWS 4
-#endif
-constexpr int kRB = SSM_DIAG_ROWS;  // rows whose decays are formed together
-constexpr int kStages = 2;   // cp.async double buffer
+constexpr int kTT = 16;      // time steps per tile
+constexpr int kStages = 4;   // cp.async ring: tiles k-1 (epilogue), k+1 (prep), k+2, k+3 (loads)
+constexpr int kRB = 4;       // rows whose decays are formed together
 
 // LPC lanes per channel, WARPS warps per block.
 template <typename T, int NK, int LPC, int WARPS>
@@ -66,13 +63,19 @@ struct DiagCfg {
     static constexpr int kBCRowChunks = kBCRowBytes / 16;
     static constexpr int kBCBytes = kTT * kBCRowBytes;
     static constexpr int kStageBytes = 3 * kXBytes + 2 * kBCBytes;
-    static constexpr int kBfBytes = kTT * NK * 4;      // fp32 copy of B (and of C)
-    static constexpr int kDuBytes = kTT * CPB * 8;     // (Delta, Delta*x) per (t, c)
-    static constexpr int kYsBytes = kTT * CPB * LPC * 4;  // partial C.h per lane
-    static constexpr int kSmemBytes = kStages * kStageBytes + 2 * kBfBytes + kDuBytes + kYsBytes;
+    static constexpr int kBfFloats = kTT * NK;         // fp32 B (and C) of one tile
+    static constexpr int kDuFloat2 = kTT * CPB;        // (Delta, Delta*x) of one tile
+    static constexpr int kYsFloats = kTT * CPB * LPC;  // partial C.h of one tile
+    // two buffers (tile parity) of each derived array
+    static constexpr int kSmemBytes = kStages * kStageBytes + 2 * (2 * kBfFloats * 4 + kDuFloat2 * 8 + kYsFloats * 4);
+    static constexpr int RS = NT / P2;                 // rows per sweep of the pair roles
+    static constexpr int kPairItems = kTT / RS;        // pair items per thread per tile
+    static constexpr int kBCItems = kTT * NK / 2 / NT; // B/C pair conversions per thread per tile
+    static constexpr int kBatches = kTT / kRB;
     static_assert(NPT % 4 == 0, "state entries are processed in groups of 4");
     static_assert(kRowBytes % 16 == 0 && kBCRowBytes % 16 == 0, "16-byte rows");
-    static_assert(NT % P2 == 0, "pair mapping");
+    static_assert(NT % P2 == 0 && kTT % RS == 0, "pair mapping");
+    static_assert(kTT * NK / 2 % NT == 0, "B/C conversion mapping");
 };
 
 struct DiagKernelArgs {
@@ -127,27 +130,44 @@ __device__ __forceinline__ void store_pair<__nv_bfloat16>(char* p, float2 v) {
     *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(v.x, v.y);
 }
 
+// softplus / SiLU of a channel pair: accurate library functions for fp32 inputs; for
+// 16-bit inputs one SFU exponential each, the rest on the FMA pipe.
+template <bool PRECISE>
+__device__ __forceinline__ float2 softplus_pair(float2 v) {
+    if (PRECISE) return make_float2(softplus_precise(v.x), softplus_precise(v.y));
+    return softplus2_fma(v);
+}
+template <bool PRECISE>
+__device__ __forceinline__ float2 silu_pair(float2 z) {
+    if (PRECISE) return make_float2(silu_precise(z.x), silu_precise(z.y));
+    return silu2_fma(z);
+}
+
 // STATE_ONLY: compute each segment's local end state from zero (segments 0..nseg-2).
 // Otherwise: full output pass over every segment with the folded initial state.
 //
-// Per tile of 32 steps:
-//   A) per (t, channel pair): softplus(dt + dt_bias) and Delta*x, packed fp32x2, into
-//      shared memory; B and C converted to fp32;
-//   B) per lane: NPT state entries of one channel advanced over the tile's rows, partial
-//      C.h sums into shared memory;
-//   C) per (t, channel pair): sum of the LPC partials, D*x, SiLU gate, store.
+// Software pipeline over tiles of 16 steps.  Iteration k of the tile loop, in one
+// fused loop body over groups of 4 rows:
+//   scan(k):      the recurrence of tile k's rows (state entries of one channel per lane,
+//                 decays of 4 rows formed before the dependent updates), partial C.h
+//                 sums to shared memory;
+//   prep(k+1):    softplus(dt + dt_bias) and Delta*x of tile k+1 per channel pair, B and C
+//                 of tile k+1 to fp32;
+//   finish(k-1):  the LPC partial sums of tile k-1 per channel pair, D*x, SiLU gate, store.
+// Interleaving the per-(t, c) work (SFU-latency chains) with the scan keeps the SFU and
+// FMA pipes busy at the low occupancy these channel counts give.
 template <typename T, int NK, int LPC, int WARPS, bool STATE_ONLY, bool GATE>
 __global__ void __launch_bounds__(32 * WARPS) diag_scan_kernel(const DiagKernelArgs a) {
     using Cfg = DiagCfg<T, NK, LPC, WARPS>;
     constexpr int NT = Cfg::NT, CPB = Cfg::CPB, NPT = Cfg::NPT, P2 = Cfg::P2, E = Cfg::kElem;
-    constexpr int RS = NT / P2;  // rows per sweep of the pair roles
+    constexpr int RS = Cfg::RS;
     constexpr bool PRECISE = sizeof(T) == 4;
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* stage0 = smem;
-    float* Bf = reinterpret_cast<float*>(smem + kStages * Cfg::kStageBytes);
-    float* Cf = Bf + kTT * NK;
-    float2* du = reinterpret_cast<float2*>(Cf + kTT * NK);
-    float* ys = reinterpret_cast<float*>(du + kTT * CPB);
+    float* Bf0 = reinterpret_cast<float*>(smem + kStages * Cfg::kStageBytes);  // [2][kBfFloats]
+    float* Cf0 = Bf0 + 2 * Cfg::kBfFloats;                                   // [2][kBfFloats]
+    float2* du0 = reinterpret_cast<float2*>(Cf0 + 2 * Cfg::kBfFloats);        // [2][kDuFloat2]
+    float* ys0 = reinterpret_cast<float*>(du0 + 2 * Cfg::kDuFloat2);          // [2][kYsFloats]
 
     const int tid = threadIdx.x;
     const int group = blockIdx.x / a.tiles_per_group;
@@ -165,7 +185,7 @@ __global__ void __launch_bounds__(32 * WARPS) diag_scan_kernel(const DiagKernelA
     const int64_t c = c_begin + cc;
     const bool c_ok = c < c_end;
 
-    // pair role (phases A and C): channels 2*pp, 2*pp+1, rows r0, r0 + RS, ...
+    // pair role (prep and finish): channels 2*pp, 2*pp+1; rows r0, r0 + RS, ...
     const int pp = tid % P2;
     const int r0 = tid / P2;
     const int64_t cA = c_begin + 2 * pp;
@@ -215,11 +235,14 @@ __global__ void __launch_bounds__(32 * WARPS) diag_scan_kernel(const DiagKernelA
     const char* bc_off_B = a.B + (int64_t)group * a.N * E;
     const char* bc_off_C = a.C + (int64_t)group * a.N * E;
 
+    auto tile_rows = [&](int k) { return (int)min((int64_t)kTT, t_end - (t_begin + (int64_t)k * kTT)); };
+    auto stage = [&](int k) { return stage0 + (k % kStages) * Cfg::kStageBytes; };
+
     auto issue_tile = [&](int k) {
         if (k < ntiles) {
-            unsigned char* st = stage0 + (k % kStages) * Cfg::kStageBytes;
+            unsigned char* st = stage(k);
             const int64_t t0 = t_begin + (int64_t)k * kTT;
-            const int rows = (int)min((int64_t)kTT, t_end - t0);
+            const int rows = tile_rows(k);
             for (int i = tid; i < kTT * Cfg::kRowChunks; i += NT) {
                 const int r = i / Cfg::kRowChunks, q = i % Cfg::kRowChunks;
                 const int64_t ch = c_begin + q * (16 / E);
@@ -242,40 +265,90 @@ __global__ void __launch_bounds__(32 * WARPS) diag_scan_kernel(const DiagKernelA
         cp_async_commit();
     };
 
-    issue_tile(0);
-    for (int k = 0; k < ntiles; ++k) {
-        cp_async_wait<0>();
-        __syncthreads();  // tile k visible; every thread is done with tile k-1
-        issue_tile(k + 1);
-        const unsigned char* st = stage0 + (k % kStages) * Cfg::kStageBytes;
-        const int64_t t0 = t_begin + (int64_t)k * kTT;
-        const int rows = (int)min((int64_t)kTT, t_end - t0);
-
-        // ---- A: Delta and Delta*x per (t, channel pair); B, C to fp32
+    // prep item it (0..kPairItems-1) of tile k: one (row, channel pair)
+    auto prep_item = [&](int k, int it) {
+        const unsigned char* st = stage(k);
+        float2* du = du0 + (k & 1) * Cfg::kDuFloat2;
+        const int r = r0 + it * RS;
+        const float2 dtv = load_pair<T>(st + Cfg::kXBytes + r * Cfg::kRowBytes + 2 * pp * E);
+        const float2 xv = load_pair<T>(st + r * Cfg::kRowBytes + 2 * pp * E);
+        float2 de = softplus_pair<PRECISE>(__fadd2_rn(dtv, bias2));
+        if (r >= tile_rows(k)) de = make_float2(0.0f, 0.0f);  // no-op rows: Delta = 0 keeps h
+        const float2 u = __fmul2_rn(de, xv);
+        *reinterpret_cast<float4*>(&du[r * CPB + 2 * pp]) = make_float4(de.x, u.x, de.y, u.y);
+        if (STATE_ONLY) dsum2 = __fadd2_rn(dsum2, de);
+    };
+    // B/C conversion item it of tile k
+    auto conv_item = [&](int k, int it) {
+        const unsigned char* st = stage(k);
+        const int i = tid + it * NT;
+        float* Bf = Bf0 + (k & 1) * Cfg::kBfFloats;
+        *reinterpret_cast<float2*>(&Bf[2 * i]) = load_pair<T>(st + 3 * Cfg::kXBytes + i * 2 * E);
+        if (!STATE_ONLY) {
+            float* Cf = Cf0 + (k & 1) * Cfg::kBfFloats;
+            *reinterpret_cast<float2*>(&Cf[2 * i]) = load_pair<T>(st + 3 * Cfg::kXBytes + Cfg::kBCBytes + i * 2 * E);
+        }
+    };
+    // finish item it of tile k: combine partial sums, skip term, gate, store
+    auto finish_item = [&](int k, int it) {
+        const int r = r0 + it * RS;
+        if (r >= tile_rows(k) || !pair_ok) return;
+        const unsigned char* st = stage(k);
+        const float* ys = ys0 + (k & 1) * Cfg::kYsFloats;
+        float2 y = make_float2(0.0f, 0.0f);
+        if (LPC == 1) {
+            y = *reinterpret_cast<const float2*>(&ys[r * CPB + 2 * pp]);
+        } else {
 #pragma unroll
-        for (int kk = 0; kk < kTT / RS; ++kk) {
-            const int r = r0 + kk * RS;
-            const float2 dtv = load_pair<T>(st + Cfg::kXBytes + r * Cfg::kRowBytes + 2 * pp * E);
-            const float2 xv = load_pair<T>(st + r * Cfg::kRowBytes + 2 * pp * E);
-            float2 de = softplus2_t<PRECISE>(__fadd2_rn(dtv, bias2));
-            if (r >= rows) de = make_float2(0.0f, 0.0f);  // no-op rows: Delta = 0 keeps h
-            const float2 u = __fmul2_rn(de, xv);
-            *reinterpret_cast<float4*>(&du[r * CPB + 2 * pp]) = make_float4(de.x, u.x, de.y, u.y);
-            if (STATE_ONLY) dsum2 = __fadd2_rn(dsum2, de);
+            for (int q = 0; q < LPC; q += 2) {
+                const float2 p0 = *reinterpret_cast<const float2*>(&ys[(r * CPB + 2 * pp) * LPC + q]);
+                const float2 p1 = *reinterpret_cast<const float2*>(&ys[(r * CPB + 2 * pp + 1) * LPC + q]);
+                y = __fadd2_rn(y, make_float2(p0.x + p0.y, p1.x + p1.y));
+            }
         }
-        for (int i = tid; i < kTT * NK / 2; i += NT) {
-            *reinterpret_cast<float2*>(&Bf[2 * i]) = load_pair<T>(st + 3 * Cfg::kXBytes + i * 2 * E);
-            if (!STATE_ONLY)
-                *reinterpret_cast<float2*>(&Cf[2 * i]) =
-                    load_pair<T>(st + 3 * Cfg::kXBytes + Cfg::kBCBytes + i * 2 * E);
-        }
-        __syncthreads();
+        const float2 xv = load_pair<T>(st + r * Cfg::kRowBytes + 2 * pp * E);
+        y = __ffma2_rn(d2, xv, y);
+        if (GATE) y = __fmul2_rn(y, silu_pair<PRECISE>(load_pair<T>(st + 2 * Cfg::kXBytes + r * Cfg::kRowBytes + 2 * pp * E)));
+        const int64_t t = t_begin + (int64_t)k * kTT + r;
+        store_pair<T>(a.out + (b * a.T + t) * row_stride + cA * E, y);
+    };
 
-        // ---- B: the recurrence over the tile's rows, kRB rows at a time.  The decays
-        // and input terms of those rows do not depend on h, so they are formed first
-        // (kRB * NPT independent exponentials per lane), then the dependent updates run.
-        // Rows past the tile's end have Delta = 0 and x*Delta = 0, so they leave h as is.
-        for (int rb = 0; rb < rows; rb += kRB) {
+    // prologue: tiles 0..2 in flight, tile 0 prepared
+    issue_tile(0);
+    issue_tile(1);
+    issue_tile(2);
+    if (ntiles > 0) {
+        cp_async_wait<2>();
+        __syncthreads();
+#pragma unroll
+        for (int it = 0; it < Cfg::kPairItems; ++it) prep_item(0, it);
+#pragma unroll
+        for (int it = 0; it < Cfg::kBCItems; ++it) conv_item(0, it);
+    }
+
+    for (int k = 0; k < ntiles; ++k) {
+        cp_async_wait<1>();  // tile k+1 landed (tile k+2 may still be in flight)
+        __syncthreads();     // ... and visible; tile k's derived data visible
+        const bool next = k + 1 < ntiles;
+        const bool prev = !STATE_ONLY && k > 0;
+        const float2* du = du0 + (k & 1) * Cfg::kDuFloat2;
+        const float* Bf = Bf0 + (k & 1) * Cfg::kBfFloats;
+        const float* Cf = Cf0 + (k & 1) * Cfg::kBfFloats;
+        float* ys = ys0 + (k & 1) * Cfg::kYsFloats;
+        const int rows = tile_rows(k);
+#pragma unroll
+        for (int bt = 0; bt < Cfg::kBatches; ++bt) {
+            const int rb = bt * kRB;
+            // per-(t, c) work of the neighbouring tiles, interleaved with this batch
+            if (next) {
+                for (int it = bt; it < Cfg::kPairItems; it += Cfg::kBatches) prep_item(k + 1, it);
+                for (int it = bt; it < Cfg::kBCItems; it += Cfg::kBatches) conv_item(k + 1, it);
+            }
+            if (prev)
+                for (int it = bt; it < Cfg::kPairItems; it += Cfg::kBatches) finish_item(k - 1, it);
+            if (rb >= rows) continue;
+            // decays and input terms of kRB rows first, then the dependent updates;
+            // rows past the tile's end have Delta = 0 and x*Delta = 0 and leave h as is
             float2 av[kRB][NPT / 2], ub[kRB][NPT / 2];
 #pragma unroll
             for (int i = 0; i < kRB; ++i) {
@@ -283,27 +356,27 @@ __global__ void __launch_bounds__(32 * WARPS) diag_scan_kernel(const DiagKernelA
                 const float2 dd = make_float2(dv.x, dv.x);
                 const float2 uu = make_float2(dv.y, dv.y);
 #pragma unroll
-                for (int k = 0; k < NPT / 2; k += 2) {
-                    const float4 bq = *reinterpret_cast<const float4*>(&Bf[(rb + i) * NK + g * NPT + 2 * k]);
-                    const float2 dA0 = __fmul2_rn(dd, A2[k]);
-                    const float2 dA1 = __fmul2_rn(dd, A2[k + 1]);
-                    av[i][k] = make_float2(ex2(dA0.x), ex2(dA0.y));
-                    av[i][k + 1] = make_float2(ex2(dA1.x), ex2(dA1.y));
-                    ub[i][k] = __fmul2_rn(uu, make_float2(bq.x, bq.y));
-                    ub[i][k + 1] = __fmul2_rn(uu, make_float2(bq.z, bq.w));
+                for (int kk = 0; kk < NPT / 2; kk += 2) {
+                    const float4 bq = *reinterpret_cast<const float4*>(&Bf[(rb + i) * NK + g * NPT + 2 * kk]);
+                    const float2 dA0 = __fmul2_rn(dd, A2[kk]);
+                    const float2 dA1 = __fmul2_rn(dd, A2[kk + 1]);
+                    av[i][kk] = make_float2(ex2(dA0.x), ex2(dA0.y));
+                    av[i][kk + 1] = make_float2(ex2(dA1.x), ex2(dA1.y));
+                    ub[i][kk] = __fmul2_rn(uu, make_float2(bq.x, bq.y));
+                    ub[i][kk + 1] = __fmul2_rn(uu, make_float2(bq.z, bq.w));
                 }
             }
 #pragma unroll
             for (int i = 0; i < kRB; ++i) {
                 float2 ya = make_float2(0.0f, 0.0f), yb = make_float2(0.0f, 0.0f);
 #pragma unroll
-                for (int k = 0; k < NPT / 2; k += 2) {
-                    h[k] = __ffma2_rn(av[i][k], h[k], ub[i][k]);
-                    h[k + 1] = __ffma2_rn(av[i][k + 1], h[k + 1], ub[i][k + 1]);
+                for (int kk = 0; kk < NPT / 2; kk += 2) {
+                    h[kk] = __ffma2_rn(av[i][kk], h[kk], ub[i][kk]);
+                    h[kk + 1] = __ffma2_rn(av[i][kk + 1], h[kk + 1], ub[i][kk + 1]);
                     if (!STATE_ONLY) {
-                        const float4 cq = *reinterpret_cast<const float4*>(&Cf[(rb + i) * NK + g * NPT + 2 * k]);
-                        ya = __ffma2_rn(make_float2(cq.x, cq.y), h[k], ya);
-                        yb = __ffma2_rn(make_float2(cq.z, cq.w), h[k + 1], yb);
+                        const float4 cq = *reinterpret_cast<const float4*>(&Cf[(rb + i) * NK + g * NPT + 2 * kk]);
+                        ya = __ffma2_rn(make_float2(cq.x, cq.y), h[kk], ya);
+                        yb = __ffma2_rn(make_float2(cq.z, cq.w), h[kk + 1], yb);
                     }
                 }
                 if (!STATE_ONLY) {
@@ -312,32 +385,15 @@ __global__ void __launch_bounds__(32 * WARPS) diag_scan_kernel(const DiagKernelA
                 }
             }
         }
-
-        if (!STATE_ONLY) {
-            __syncthreads();
-            // ---- C: combine the LPC partial sums, skip term, gate, store
-#pragma unroll
-            for (int kk = 0; kk < kTT / RS; ++kk) {
-                const int r = r0 + kk * RS;
-                if (r >= rows || !pair_ok) continue;
-                float2 y = make_float2(0.0f, 0.0f);
-                if (LPC == 1) {
-                    y = *reinterpret_cast<const float2*>(&ys[r * CPB + 2 * pp]);
-                } else {
-#pragma unroll
-                    for (int q = 0; q < LPC; q += 2) {
-                        const float2 p0 = *reinterpret_cast<const float2*>(&ys[(r * CPB + 2 * pp) * LPC + q]);
-                        const float2 p1 = *reinterpret_cast<const float2*>(&ys[(r * CPB + 2 * pp + 1) * LPC + q]);
-                        y = __fadd2_rn(y, make_float2(p0.x + p0.y, p1.x + p1.y));
-                    }
-                }
-                const float2 xv = load_pair<T>(st + r * Cfg::kRowBytes + 2 * pp * E);
-                y = __ffma2_rn(d2, xv, y);
-                if (GATE) y = __fmul2_rn(y, silu2_t<PRECISE>(load_pair<T>(st + 2 * Cfg::kXBytes + r * Cfg::kRowBytes + 2 * pp * E)));
-                store_pair<T>(a.out + (b * a.T + t0 + r) * row_stride + cA * E, y);
-            }
-        }
+        __syncthreads();      // every thread is done with stage k-1 before it is reloaded
+        issue_tile(k + 3);    // into the stage of tile k-1
     }
+    if (!STATE_ONLY && ntiles > 0) {
+        __syncthreads();
+#pragma unroll
+        for (int it = 0; it < Cfg::kPairItems; ++it) finish_item(ntiles - 1, it);
+    }
+    cp_async_wait<0>();
 
     if (STATE_ONLY) {
         // local end state and Delta sum of this segment
@@ -352,7 +408,7 @@ __global__ void __launch_bounds__(32 * WARPS) diag_scan_kernel(const DiagKernelA
         }
         // the RS threads of a pair each summed a subset of rows
         __syncthreads();
-        float2* red = du;  // reuse: RS x P2 partial sums
+        float2* red = du0;  // reuse: RS x P2 partial sums
         red[r0 * P2 + pp] = dsum2;
         __syncthreads();
         if (tid < P2) {
@@ -396,37 +452,42 @@ int pick_nk(int64_t N) {
     return 64;
 }
 
-// State entries per lane: 8 by default (the best instruction count per element on
-// B300 for the configurations measured); SSM_DIAG_NPT=4 selects 4 (tuning knob).
-int pick_npt() {
+// State entries per lane: SSM_DIAG_NPT (4 or 8) when set (tuning knob), else 8 when
+// the channels alone fill the GPU and 4 when the sequence has to be split.
+int npt_override() {
     static const int v = [] {
         const char* e = getenv("SSM_DIAG_NPT");
-        return (e && atoi(e) == 4) ? 4 : 8;
+        return e ? atoi(e) : 0;
     }();
-    return v;
+    return v == 4 || v == 8 ? v : 0;
 }
 
 Plan make_plan(const ScanArgs& a) {
     Plan p;
     p.NK = pick_nk(a.dstate);
-    p.LPC = std::max(1, p.NK / pick_npt());
-    p.cpb = p.LPC == 1 ? 32 : 16;
-    p.warps = p.cpb * p.LPC / 32;
-    const int64_t cpg = a.nheads / a.ngroups;
-    p.tiles_per_group = (int)((cpg + p.cpb - 1) / p.cpb);
-    p.blocks_x = (int)(a.ngroups * p.tiles_per_group);
-    const int64_t warps = (int64_t)p.blocks_x * a.batch * p.warps;
-    // Split time only when the channels give fewer than 2 warps per SM sub-partition
-    // (148 SMs x 4); then aim for 4.  The plan, and so the workspace size, is a
-    // function of the shape alone.
-    const int64_t smsp = 148 * 4;
+    const int64_t smsp = 148 * 4;  // B300 SM sub-partitions
+    auto fill = [&](int npt) {
+        p.LPC = std::max(1, std::min(8, p.NK / npt));
+        p.cpb = p.LPC == 1 ? 32 : 16;
+        p.warps = p.cpb * p.LPC / 32;
+        const int64_t cpg = a.nheads / a.ngroups;
+        p.tiles_per_group = (int)((cpg + p.cpb - 1) / p.cpb);
+        p.blocks_x = (int)(a.ngroups * p.tiles_per_group);
+        return (int64_t)p.blocks_x * a.batch * p.warps;
+    };
+    // Measured on B300: 8 state entries per lane is fastest when the channels give at
+    // least 2 warps per sub-partition; below that, 4 per lane plus time segments of
+    // about 3 warps per sub-partition (segment folding costs a state-only pass).
+    int64_t warps = fill(npt_override() ? npt_override() : 8);
+    const bool split = a.chunk == 0 && warps > 0 && warps < 2 * smsp;
+    if (split && !npt_override()) warps = fill(4);
     int64_t seg_len;
     if (a.chunk > 0) {
         seg_len = a.chunk;
-    } else if (warps >= 2 * smsp || warps == 0) {
+    } else if (!split) {
         seg_len = a.seqlen;
     } else {
-        int64_t nseg = (4 * smsp + warps - 1) / warps;
+        int64_t nseg = (3 * smsp + warps - 1) / warps;
         nseg = std::max<int64_t>(1, std::min<int64_t>(nseg, a.seqlen / 128));
         seg_len = (a.seqlen + nseg - 1) / nseg;
     }
@@ -500,7 +561,7 @@ cudaError_t launch_dtype(const ScanArgs& a, const Plan& p, void* ws, cudaStream_
         case 8: return p.LPC == 1 ? launch_typed<T, 8, 1>(a, p, ws, stream) : launch_typed<T, 8, 2>(a, p, ws, stream);
         case 16: return p.LPC == 2 ? launch_typed<T, 16, 2>(a, p, ws, stream) : launch_typed<T, 16, 4>(a, p, ws, stream);
         case 32: return p.LPC == 4 ? launch_typed<T, 32, 4>(a, p, ws, stream) : launch_typed<T, 32, 8>(a, p, ws, stream);
-        default: return p.LPC == 8 ? launch_typed<T, 64, 8>(a, p, ws, stream) : launch_typed<T, 64, 16>(a, p, ws, stream);
+        default: return launch_typed<T, 64, 8>(a, p, ws, stream);
     }
 }
 

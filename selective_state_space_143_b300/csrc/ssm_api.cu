@@ -5,7 +5,7 @@
 #include <atomic>
 #include <cstdint>
 
-#include "../../include/ssm_scan.h"
+#include "ssm_scan.h"
 #include "ssm_internal.h"
 
 namespace ssm {

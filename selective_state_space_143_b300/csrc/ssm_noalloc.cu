@@ -10,7 +10,7 @@
 
 #include <mutex>
 
-#include "../../include/ssm_scan.h"
+#include "ssm_scan.h"
 #include "ssm_internal.h"
 
 namespace ssm {
