@@ -155,27 +155,37 @@ __global__ void __launch_bounds__(kThreads) ssd_state_tc(const SsdTcArgs a) {
         }
     }
     __syncthreads();
-    // Xd = w_s x_s for both heads, split hi/lo, MN-major (8 consecutive p at one s)
+    // Xd = w_s x_s for both heads, split hi/lo, MN-major (8 consecutive p at one s).
+    // Raw x is staged into the lo tile by cp.async (all chunks in flight at once), then
+    // each thread rewrites its own chunks: hi into the hi tile, lo in place.
     {
         const uint32_t bh = tc::smem_u32(sXh), bl = tc::smem_u32(sXl);
-#pragma unroll 4
         for (int i = tid; i < Q * 16; i += kThreads) {
             int s, mc;
             mnmajor_item(i, 16, s, mc);
             const int m0 = mc * 8;  // m = head_local * 64 + p
             const int hl = m0 / kP, p0 = m0 % kP;
-            uint32_t hi[4] = {0, 0, 0, 0}, lo[4] = {0, 0, 0, 0};
-            if (s < len) {
-                const uint4 raw = *reinterpret_cast<const uint4*>(a.x + ((b * a.T + c * a.Q + s) * a.H + h0 + hl) * kP + p0);
-                const float w = s_w[hl][s];
-                const __nv_bfloat162* r2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float2 f = __bfloat1622float2(r2[k]);
-                    split2(f.x * w, f.y * w, hi[k], lo[k]);
-                }
-            }
+            const bool ok = s < len;
+            const __nv_bfloat16* src = a.x + (ok ? ((b * a.T + c * a.Q + s) * a.H + h0 + hl) * kP + p0 : 0);
+            cp_async16(bl + tc::off_mnmajor(m0, s, 128), src, ok);
+        }
+        cp_async_commit_wait_all();
+        __syncthreads();
+        for (int i = tid; i < Q * 16; i += kThreads) {
+            int s, mc;
+            mnmajor_item(i, 16, s, mc);
+            const int m0 = mc * 8;
+            const int hl = m0 / kP;
             const uint32_t off = tc::off_mnmajor(m0, s, 128);
+            const uint4 raw = *reinterpret_cast<const uint4*>(sXl + off);
+            const float w = s_w[hl][s];
+            const __nv_bfloat162* r2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float2 f = __bfloat1622float2(r2[k]);
+                split2(f.x * w, f.y * w, hi[k], lo[k]);
+            }
             st_shared_v4(bh + off, hi[0], hi[1], hi[2], hi[3]);
             st_shared_v4(bl + off, lo[0], lo[1], lo[2], lo[3]);
         }
@@ -207,12 +217,14 @@ __global__ void __launch_bounds__(kThreads) ssd_state_tc(const SsdTcArgs a) {
         // D[(head, p), nb*NB + n] = sum_s (Xd_hi + Xd_lo)[s, (head, p)] B[s, nb*NB + n]
         if (tid == 0) {
             constexpr uint32_t idesc = tc::idesc_bf16(128, NB, 1, 1);
-            const uint32_t xh = tc::smem_u32(sXh), xl = tc::smem_u32(sXl), ba = tc::smem_u32(sB);
+            const uint64_t dxh = tc::desc_mnmajor(tc::smem_u32(sXh), 128, 0);
+            const uint64_t dxl = tc::desc_mnmajor(tc::smem_u32(sXl), 128, 0);
+            const uint64_t db = tc::desc_mnmajor(tc::smem_u32(sB), NB, 0);
             const uint32_t d = tmem + (uint32_t)(nb * NB);
             for (int ks = 0; ks < Q / 16; ++ks)
-                tc::mma_bf16(d, tc::desc_mnmajor(xh, 128, ks), tc::desc_mnmajor(ba, NB, ks), idesc, ks > 0);
+                tc::mma_bf16(d, dxh + ks * tc::kstep_mnmajor(128), db + ks * tc::kstep_mnmajor(NB), idesc, ks > 0);
             for (int ks = 0; ks < Q / 16; ++ks)
-                tc::mma_bf16(d, tc::desc_mnmajor(xl, 128, ks), tc::desc_mnmajor(ba, NB, ks), idesc, 1);
+                tc::mma_bf16(d, dxl + ks * tc::kstep_mnmajor(128), db + ks * tc::kstep_mnmajor(NB), idesc, 1);
             tc::mma_commit(&s_mbar);
         }
     }
@@ -240,17 +252,37 @@ __global__ void __launch_bounds__(kThreads) ssd_state_tc(const SsdTcArgs a) {
     if (warp == 0) tc::tmem_dealloc(tmem, kCols);
 }
 
-// grid (nchunks * Q/128, H / HG, b); 128 threads.  Rows [128*rh, 128*rh + 128) of chunk c.
-// dynamic smem: C rows (128 x N, K-major) | region:
-//   phase 1: B rows [0, SW) (K-major)
-//   phase 2: M' hi | M' lo (128 x 128 each, one 128-column K-part at a time) | x_h (SW x 64)
-//            | h hi | h lo (64 x N each)
+// Columns of M' built per K-part (two K-part buffers alternate).
+template <int N>
+struct ScanTcCfg {
+    static constexpr int KPC = N > 128 ? 32 : 64;
+    static constexpr size_t kC = (size_t)128 * N * 2;            // C rows, resident
+    static constexpr size_t kPhase1 = (size_t)256 * N * 2;       // B rows [0, SW)
+    static constexpr size_t kMPart = (size_t)128 * KPC * 2;      // one M' K-part, hi or lo
+    static constexpr size_t kX = (size_t)256 * kP * 2;           // one x_h tile
+    static constexpr size_t kH = (size_t)kP * N * 2;             // one h tile, hi or lo
+    static constexpr size_t kPhase2 = 4 * kMPart + 2 * kX + 2 * kH;
+    static constexpr size_t kSmem = kC + (kPhase1 > kPhase2 ? kPhase1 : kPhase2);
+};
+
+// grid (nchunks * Q/128, H / HG, b); 256 threads.  Rows [128*rh, 128*rh + 128) of chunk c,
+// heads [HG*blockIdx.y, +HG).
+// Per head h, pipelined over the CTA's heads:
+//   commit   : prefetched inputs of h to shared memory (x_h into its parity buffer, h_{c-1}
+//              split hi/lo), inputs of h+1 fetched into registers;
+//   K-parts  : M' columns built into alternating buffers while the tensor core runs the
+//              previous part's MMAs (Y_diag += M'_hi X + M'_lo X; Y_off with part 0);
+//   finish   : the epilogue of head h-1, from its own TMEM accumulators, right after
+//              head h's first MMAs are issued.
 template <int N, bool GATE>
 __global__ void __launch_bounds__(kThreads) ssd_scan_tc(const SsdTcArgs a, int heads_per_cta) {
+    using Cfg = ScanTcCfg<N>;
+    constexpr int KPC = Cfg::KPC;
     extern __shared__ __align__(1024) unsigned char smem[];
-    __shared__ float s_dl[256], s_cum[256];
+    __shared__ float s_cum[256];
+    __shared__ __align__(16) float s_beta[256];
     __shared__ uint32_t s_tmem;
-    __shared__ __align__(8) uint64_t s_mbar;
+    __shared__ __align__(8) uint64_t s_mbar[3];  // [0], [1]: MMA commits by parity; [2]: G
     const int tid = threadIdx.x, warp = tid >> 5;
     const int Q = (int)a.Q;
     const int halves = Q / 128;
@@ -261,42 +293,40 @@ __global__ void __launch_bounds__(kThreads) ssd_scan_tc(const SsdTcArgs a, int h
     const int t0 = 128 * rh;
     if (t0 >= len) return;  // no valid rows in this half (uniform)
     const int SW = t0 + 128;  // columns s of G needed by this half (causal)
+    const int nparts = SW / KPC;
     const int64_t hbeg = (int64_t)blockIdx.y * heads_per_cta;
     const int64_t g = hbeg / (a.H / a.G);
 
-    unsigned char* sC = smem;                        // K-major: M = t (128), K = n
-    unsigned char* region = smem + 128 * N * 2;
-    unsigned char* sB = region;                      // K-major: N_mma = s (SW), K = n
-    unsigned char* sMh = region;                     // K-major: M = t, K = 128 columns of s
-    unsigned char* sMl = region + 128 * 128 * 2;
-    unsigned char* sXh = region + 128 * 128 * 4;     // MN-major: K = s (SW), N_mma = p (64)
-    unsigned char* sHh = sXh + 256 * kP * 2;         // K-major: N_mma = p (64), K = n
-    unsigned char* sHl = sHh + kP * N * 2;
+    unsigned char* sC = smem;                            // K-major: M = t (128), K = n
+    unsigned char* region = smem + Cfg::kC;
+    unsigned char* sB = region;                          // phase 1, K-major: N_mma = s, K = n
+    unsigned char* sM = region;                          // [2 parts][hi, lo], K-major: M = t, K = KPC
+    unsigned char* sX = region + 4 * Cfg::kMPart;        // [2], MN-major: K = s, N_mma = p
+    unsigned char* sHh = sX + 2 * Cfg::kX;               // K-major: N_mma = p, K = n
+    unsigned char* sHl = sHh + Cfg::kH;
 
     // phase 1 loads: C rows of this half and B rows [0, SW)
     {
         const uint32_t cb = tc::smem_u32(sC), bb = tc::smem_u32(sB);
         for (int i = tid; i < 128 * (N / 8); i += kThreads) {
-            int r, nc;
-            kmajor_item(i, N / 8, r, nc);
-            const int n0 = nc * 8;
-            const int s = t0 + r;
+            int rr, nc;
+            kmajor_item(i, N / 8, rr, nc);
+            const int s = t0 + rr;
             const bool ok = s < len;
-            const __nv_bfloat16* src = a.C + (ok ? (((b * a.T + c * a.Q + s) * a.G + g) * a.N + n0) : 0);
-            cp_async16(cb + tc::off_kmajor(r, n0, N), src, ok);
+            const __nv_bfloat16* src = a.C + (ok ? (((b * a.T + c * a.Q + s) * a.G + g) * a.N + nc * 8) : 0);
+            cp_async16(cb + tc::off_kmajor(rr, nc * 8, N), src, ok);
         }
         for (int i = tid; i < SW * (N / 8); i += kThreads) {
             int s, nc;
             kmajor_item(i, N / 8, s, nc);
-            const int n0 = nc * 8;
             const bool ok = s < len;
-            const __nv_bfloat16* src = a.B + (ok ? (((b * a.T + c * a.Q + s) * a.G + g) * a.N + n0) : 0);
-            cp_async16(bb + tc::off_kmajor(s, n0, N), src, ok);
+            const __nv_bfloat16* src = a.B + (ok ? (((b * a.T + c * a.Q + s) * a.G + g) * a.N + nc * 8) : 0);
+            cp_async16(bb + tc::off_kmajor(s, nc * 8, N), src, ok);
         }
     }
     if (warp == 0) tc::tmem_alloc(&s_tmem, 512);
     if (tid == 0) {
-        tc::mbar_init(&s_mbar, 1);
+        for (int i = 0; i < 3; ++i) tc::mbar_init(&s_mbar[i], 1);
         tc::mbar_fence_init();
     }
     cp_async_commit_wait_all();
@@ -305,20 +335,19 @@ __global__ void __launch_bounds__(kThreads) ssd_scan_tc(const SsdTcArgs a, int h
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = s_tmem;
-    const uint32_t tG = tmem, tYd = tmem + 256, tYo = tmem + 320;
-    uint32_t phase = 0;
+    const uint32_t tG = tmem;
     bool ok = true;
 
     // G = C_rows B^T (raw bf16 operands: exact products, fp32 accumulation)
     if (tid == 0) {
         const uint32_t idesc = tc::idesc_bf16(128, SW, 0, 0);
-        const uint32_t ca = tc::smem_u32(sC), ba = tc::smem_u32(sB);
+        const uint64_t da = tc::desc_kmajor(tc::smem_u32(sC), N, 0), db = tc::desc_kmajor(tc::smem_u32(sB), N, 0);
+#pragma unroll
         for (int ks = 0; ks < N / 16; ++ks)
-            tc::mma_bf16(tG, tc::desc_kmajor(ca, N, ks), tc::desc_kmajor(ba, N, ks), idesc, ks > 0);
-        tc::mma_commit(&s_mbar);
+            tc::mma_bf16(tG, da + ks * tc::kstep_kmajor(), db + ks * tc::kstep_kmajor(), idesc, ks > 0);
+        tc::mma_commit(&s_mbar[2]);
     }
-    ok = tc::mbar_wait(&s_mbar, phase);
-    phase ^= 1;
+    ok = tc::mbar_wait(&s_mbar[2], 0);
     tc::fence_after_sync();
 
     const int q = warp & 3;                  // TMEM lane quarter of this warp
@@ -328,151 +357,234 @@ __global__ void __launch_bounds__(kThreads) ssd_scan_tc(const SsdTcArgs a, int h
     const bool row_ok = t < len;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     const int t_warp_max = t0 + q * 32 + 31;  // tcgen05.ld is warp-collective
+    const int cols_per_warp = KPC / 2;       // columns of a K-part built by one warp
 
+    // MMA commits are numbered; commit n arrives on s_mbar[n & 1], phase (n >> 1) & 1.
+    uint32_t ncommit = 0;
+    auto wait_commit = [&](uint32_t n) {
+        ok = tc::mbar_wait(&s_mbar[n & 1], (n >> 1) & 1) && ok;
+        tc::fence_after_sync();
+    };
+
+    // next head's inputs in registers (see commit below)
+    constexpr int XCH = 256 * (kP / 8) / kThreads;  // x_h chunks per thread (SW <= 256)
+    constexpr int HCH = kP * (N / 8) / kThreads;    // 8-float groups of h per thread
+    float pf_dl = 0.0f, pf_cum = 0.0f;
+    uint4 pf_x[XCH];
+    float4 pf_h[HCH][2];
+    auto prefetch = [&](int64_t hn) {
+        if (tid < Q) {
+            const int64_t o = ((b * a.H + hn) * a.nchunks + c) * a.Q + tid;
+            pf_dl = a.dl[o];
+            pf_cum = a.cum[o];
+        }
+#pragma unroll
+        for (int j = 0; j < XCH; ++j) {
+            const int i = tid + j * kThreads;
+            int s, pc;
+            mnmajor_item(i, kP / 8, s, pc);
+            pf_x[j] = make_uint4(0, 0, 0, 0);
+            if (i < SW * (kP / 8) && s < len)
+                pf_x[j] = *reinterpret_cast<const uint4*>(a.x + ((b * a.T + c * a.Q + s) * a.H + hn) * kP + pc * 8);
+        }
+        const float* hs = a.states + ((b * a.nchunks + c) * a.H + hn) * (int64_t)kP * a.N;
+#pragma unroll
+        for (int j = 0; j < HCH; ++j) {
+            int p, nc;
+            kmajor_item(tid + j * kThreads, N / 8, p, nc);
+            pf_h[j][0] = *reinterpret_cast<const float4*>(hs + (int64_t)p * a.N + nc * 8);
+            pf_h[j][1] = *reinterpret_cast<const float4*>(hs + (int64_t)p * a.N + nc * 8 + 4);
+        }
+    };
+    // prefetched inputs -> shared memory: cumsum and beta_s = log2(Delta_s) - cum_s log2(e)
+    // (so that exp(cum_t - cum_s) Delta_s = 2^(cum_t log2(e) + beta_s)); x_h MN-major into
+    // buffer xb; h split hi/lo K-major
+    auto commit = [&](int xbuf) {
+        if (tid < Q) {
+            s_cum[tid] = pf_cum;
+            s_beta[tid] = (pf_dl > 0.0f ? lg2(pf_dl) : -INFINITY) - pf_cum * kLog2e;
+        }
+        const uint32_t xb = tc::smem_u32(sX + xbuf * Cfg::kX);
+#pragma unroll
+        for (int j = 0; j < XCH; ++j) {
+            const int i = tid + j * kThreads;
+            int s, pc;
+            mnmajor_item(i, kP / 8, s, pc);
+            if (i < SW * (kP / 8)) st_shared_v4(xb + tc::off_mnmajor(pc * 8, s, kP), pf_x[j].x, pf_x[j].y, pf_x[j].z, pf_x[j].w);
+        }
+        const uint32_t hb = tc::smem_u32(sHh), lb = tc::smem_u32(sHl);
+#pragma unroll
+        for (int j = 0; j < HCH; ++j) {
+            int p, nc;
+            kmajor_item(tid + j * kThreads, N / 8, p, nc);
+            uint32_t qh[4], ql[4];
+            split2(pf_h[j][0].x, pf_h[j][0].y, qh[0], ql[0]);
+            split2(pf_h[j][0].z, pf_h[j][0].w, qh[1], ql[1]);
+            split2(pf_h[j][1].x, pf_h[j][1].y, qh[2], ql[2]);
+            split2(pf_h[j][1].z, pf_h[j][1].w, qh[3], ql[3]);
+            const uint32_t off = tc::off_kmajor(p, nc * 8, N);
+            st_shared_v4(hb + off, qh[0], qh[1], qh[2], qh[3]);
+            st_shared_v4(lb + off, ql[0], ql[1], ql[2], ql[3]);
+        }
+    };
+    // epilogue of head hh from accumulator set acc: y = Y_diag + exp(cum_t) Y_off + D x, gate
+    auto finish = [&](int64_t hh, int acc, float alpha_h) {
+        const unsigned char* xs = sX + acc * Cfg::kX;  // x_h of head hh (buffer parity = acc)
+        const uint32_t tYd = tmem + 256 + 128 * acc, tYo = tYd + 64;
+        const float et = ex2(alpha_h);
+        const float Dh = a.D ? a.D[hh] : 0.0f;
+        const int64_t row = ((b * a.T + c * a.Q + t) * a.H + hh) * kP;
+#pragma unroll 1
+        for (int p0 = 32 * chalf; p0 < 32 * chalf + 32; p0 += 16) {
+            float yd[16], yo[16];
+            tc::tmem_ld16(tYd + lane_base + (uint32_t)p0, yd);
+            tc::tmem_ld16(tYo + lane_base + (uint32_t)p0, yo);
+            if (row_ok) {
+                uint32_t pk[8];
+#pragma unroll
+                for (int j = 0; j < 16; j += 8) {
+                    const uint4 xr = *reinterpret_cast<const uint4*>(xs + tc::off_mnmajor(p0 + j, t, kP));
+                    const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&xr);
+                    uint4 zr = make_uint4(0, 0, 0, 0);
+                    if (GATE) zr = *reinterpret_cast<const uint4*>(a.z + row + p0 + j);
+                    const __nv_bfloat162* z2 = reinterpret_cast<const __nv_bfloat162*>(&zr);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float2 xv = __bfloat1622float2(x2[k]);
+                        float y0 = fmaf(et, yo[j + 2 * k], yd[j + 2 * k]) + Dh * xv.x;
+                        float y1 = fmaf(et, yo[j + 2 * k + 1], yd[j + 2 * k + 1]) + Dh * xv.y;
+                        if (GATE) {
+                            const float2 zv = __bfloat1622float2(z2[k]);
+                            y0 *= silu(zv.x);
+                            y1 *= silu(zv.y);
+                        }
+                        pk[j / 2 + k] = pack_bf16x2(y0, y1);
+                    }
+                }
+                uint4* dst = reinterpret_cast<uint4*>(a.out + row + p0);
+                dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            }
+        }
+    };
+
+    if (ok) prefetch(hbeg);
+    uint32_t last_commit_prev = 0;  // the previous head's last commit
+    float alpha_prev = 0.0f;
     for (int hi = 0; hi < heads_per_cta && ok; ++hi) {
         const int64_t h = hbeg + hi;
-        __syncthreads();  // every thread is done with the previous head's epilogue
-        for (int s = tid; s < Q; s += kThreads) {
-            const int64_t o = ((b * a.H + h) * a.nchunks + c) * a.Q + s;
-            s_dl[s] = a.dl[o];
-            s_cum[s] = a.cum[o];
-        }
+        // h_{c-1} tiles are single-buffered: the previous head's MMAs must be done reading
+        // them.  (Only the latest commit is waited on here: an mbarrier parity wait is
+        // exact only while its barrier is at most one phase past the awaited commit.)
+        if (hi > 0) wait_commit(last_commit_prev);
+        __syncthreads();  // ... and every thread is past the previous head's M' builds
+        commit(hi & 1);
+        if (hi + 1 < heads_per_cta) prefetch(h + 1);
+        tc::fence_async_smem();
         __syncthreads();
-        // x_h rows [0, SW): raw bf16, MN-major (8 consecutive p at one s)
-        {
-            const uint32_t xb = tc::smem_u32(sXh);
-            for (int i = tid; i < SW * 8; i += kThreads) {
-                int s, pc;
-                mnmajor_item(i, 8, s, pc);
-                const int p0 = pc * 8;
-                const bool okr = s < len;
-                const __nv_bfloat16* src = a.x + (okr ? (((b * a.T + c * a.Q + s) * a.H + h) * kP + p0) : 0);
-                cp_async16(xb + tc::off_mnmajor(p0, s, kP), src, okr);
-            }
-        }
-        // h_{c-1} of this head: fp32 -> bf16 hi/lo, K-major (8 consecutive n at one p)
-        {
-            const uint32_t hb = tc::smem_u32(sHh), lb = tc::smem_u32(sHl);
-            const float* hs = a.states + ((b * a.nchunks + c) * a.H + h) * (int64_t)kP * a.N;
-#pragma unroll 2
-            for (int i = tid; i < kP * (N / 8); i += kThreads) {
-                int p, nc;
-                kmajor_item(i, N / 8, p, nc);
-                const int n0 = nc * 8;
-                const float4 v0 = *reinterpret_cast<const float4*>(hs + (int64_t)p * a.N + n0);
-                const float4 v1 = *reinterpret_cast<const float4*>(hs + (int64_t)p * a.N + n0 + 4);
-                uint32_t qh[4], ql[4];
-                split2(v0.x, v0.y, qh[0], ql[0]);
-                split2(v0.z, v0.w, qh[1], ql[1]);
-                split2(v1.x, v1.y, qh[2], ql[2]);
-                split2(v1.z, v1.w, qh[3], ql[3]);
-                const uint32_t off = tc::off_kmajor(p, n0, N);
-                st_shared_v4(hb + off, qh[0], qh[1], qh[2], qh[3]);
-                st_shared_v4(lb + off, ql[0], ql[1], ql[2], ql[3]);
-            }
-        }
-        const float cum_t = s_cum[min(t, Q - 1)];
-        // Y_diag accumulates over K-parts of 128 columns of s; Y_off goes with part 0
-        for (int kp = 0; kp < SW / 128; ++kp) {
-            if (kp > 0) {
-                // the previous part's MMAs must be done with the M' buffers
-                ok = tc::mbar_wait(&s_mbar, phase) && ok;
-                phase ^= 1;
-                tc::fence_after_sync();
-                __syncthreads();
-            }
-            // M'[t, s] = G[t, s] exp(cum_t - cum_s) Delta_s for s <= t, hi/lo, K-major
+        const float alpha = s_cum[min(t, Q - 1)] * kLog2e;
+        for (int kp = 0; kp < nparts; ++kp) {
+            // this K-part's buffer was last used by commit ncommit - 2
+            if (ncommit >= 2) wait_commit(ncommit - 2);
+            // M'[t, s] = G[t, s] 2^(alpha_t + beta_s) for s <= t, hi/lo, K-major.  This warp
+            // builds cols_per_warp columns in blocks of 16; the TMEM load of block j + 1 is
+            // in flight while block j is computed.
             {
-                const uint32_t mh = tc::smem_u32(sMh), ml = tc::smem_u32(sMl);
-                for (int s0 = 128 * kp + 64 * chalf; s0 < 128 * kp + 64 * chalf + 64; s0 += 16) {
+                unsigned char* part = sM + (ncommit & 1) * 2 * Cfg::kMPart;
+                const uint32_t mh = tc::smem_u32(part), ml = tc::smem_u32(part + Cfg::kMPart);
+                const int s_lo = KPC * kp + cols_per_warp * chalf;
+                constexpr int NBLK = KPC / 2 / 16;
+                int nvalid = 0;  // blocks with some s <= t for this warp (warp-uniform)
+#pragma unroll
+                for (int blk = 0; blk < NBLK; ++blk) nvalid += (s_lo + 16 * blk <= t_warp_max) ? 1 : 0;
+                uint32_t cur[16], nxt[16];
+                if (nvalid > 0) {
+                    tc::tmem_ld16_async(tG + lane_base + (uint32_t)s_lo, cur);
+                    tc::tmem_wait_ld();
+                }
+#pragma unroll
+                for (int blk = 0; blk < NBLK; ++blk) {
+                    const int s0 = s_lo + 16 * blk;
                     uint32_t ph[8], pl[8];
-                    if (s0 <= t_warp_max) {
-                        float gv[16];
-                        tc::tmem_ld16(tG + lane_base + (uint32_t)s0, gv);
+                    if (blk < nvalid) {
+                        if (blk + 1 < nvalid) tc::tmem_ld16_async(tG + lane_base + (uint32_t)(s0 + 16), nxt);
+                        const bool full = s0 + 15 <= t0 + q * 32;  // no masked column in this warp
+                        float bt[16];
+#pragma unroll
+                        for (int j = 0; j < 16; j += 4) *reinterpret_cast<float4*>(&bt[j]) = *reinterpret_cast<const float4*>(&s_beta[s0 + j]);
 #pragma unroll
                         for (int j = 0; j < 16; j += 2) {
-                            const int s = s0 + j;
-                            const float v0 = s <= t ? gv[j] * __expf(cum_t - s_cum[s]) * s_dl[s] : 0.0f;
-                            const float v1 = s + 1 <= t ? gv[j + 1] * __expf(cum_t - s_cum[s + 1]) * s_dl[s + 1] : 0.0f;
+                            float v0 = ex2(alpha + bt[j]) * __uint_as_float(cur[j]);
+                            float v1 = ex2(alpha + bt[j + 1]) * __uint_as_float(cur[j + 1]);
+                            if (!full) {
+                                v0 = s0 + j <= t ? v0 : 0.0f;
+                                v1 = s0 + j + 1 <= t ? v1 : 0.0f;
+                            }
                             split2(v0, v1, ph[j / 2], pl[j / 2]);
+                        }
+                        if (blk + 1 < nvalid) {
+                            tc::tmem_wait_ld();
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) cur[j] = nxt[j];
                         }
                     } else {
 #pragma unroll
                         for (int j = 0; j < 8; ++j) ph[j] = pl[j] = 0u;
                     }
-                    const int sl = s0 - 128 * kp;
-                    st_shared_v4(mh + tc::off_kmajor(r, sl, 128), ph[0], ph[1], ph[2], ph[3]);
-                    st_shared_v4(mh + tc::off_kmajor(r, sl + 8, 128), ph[4], ph[5], ph[6], ph[7]);
-                    st_shared_v4(ml + tc::off_kmajor(r, sl, 128), pl[0], pl[1], pl[2], pl[3]);
-                    st_shared_v4(ml + tc::off_kmajor(r, sl + 8, 128), pl[4], pl[5], pl[6], pl[7]);
+                    const int sl = s0 - KPC * kp;
+                    st_shared_v4(mh + tc::off_kmajor(r, sl, KPC), ph[0], ph[1], ph[2], ph[3]);
+                    st_shared_v4(mh + tc::off_kmajor(r, sl + 8, KPC), ph[4], ph[5], ph[6], ph[7]);
+                    st_shared_v4(ml + tc::off_kmajor(r, sl, KPC), pl[0], pl[1], pl[2], pl[3]);
+                    st_shared_v4(ml + tc::off_kmajor(r, sl + 8, KPC), pl[4], pl[5], pl[6], pl[7]);
                 }
             }
-            cp_async_commit_wait_all();
             tc::fence_async_smem();
             tc::fence_before_sync();
             __syncthreads();
             tc::fence_after_sync();
             if (tid == 0) {
-                const uint32_t mh = tc::smem_u32(sMh), ml = tc::smem_u32(sMl), xa = tc::smem_u32(sXh);
+                unsigned char* part = sM + (ncommit & 1) * 2 * Cfg::kMPart;
+                const uint32_t tYd = tmem + 256 + 128 * (hi & 1), tYo = tYd + 64;
                 constexpr uint32_t id_diag = tc::idesc_bf16(128, kP, 0, 1);
-                for (int ks = 0; ks < 8; ++ks)
-                    tc::mma_bf16(tYd, tc::desc_kmajor(mh, 128, ks), tc::desc_mnmajor(xa, kP, 8 * kp + ks), id_diag,
+                const uint64_t dmh = tc::desc_kmajor(tc::smem_u32(part), KPC, 0);
+                const uint64_t dml = tc::desc_kmajor(tc::smem_u32(part + Cfg::kMPart), KPC, 0);
+                // x_h descriptor at this part's first k-step
+                const uint64_t dx = tc::desc_mnmajor(tc::smem_u32(sX + (hi & 1) * Cfg::kX), kP, KPC / 16 * kp);
+#pragma unroll
+                for (int ks = 0; ks < KPC / 16; ++ks)
+                    tc::mma_bf16(tYd, dmh + ks * tc::kstep_kmajor(), dx + ks * tc::kstep_mnmajor(kP), id_diag,
                                  (kp > 0 || ks > 0) ? 1u : 0u);
-                for (int ks = 0; ks < 8; ++ks)
-                    tc::mma_bf16(tYd, tc::desc_kmajor(ml, 128, ks), tc::desc_mnmajor(xa, kP, 8 * kp + ks), id_diag, 1);
+#pragma unroll
+                for (int ks = 0; ks < KPC / 16; ++ks)
+                    tc::mma_bf16(tYd, dml + ks * tc::kstep_kmajor(), dx + ks * tc::kstep_mnmajor(kP), id_diag, 1);
                 if (kp == 0) {
-                    const uint32_t ca = tc::smem_u32(sC), hh = tc::smem_u32(sHh), hl = tc::smem_u32(sHl);
                     constexpr uint32_t id_off = tc::idesc_bf16(128, kP, 0, 0);
+                    const uint64_t dc = tc::desc_kmajor(tc::smem_u32(sC), N, 0);
+                    const uint64_t dhh = tc::desc_kmajor(tc::smem_u32(sHh), N, 0);
+                    const uint64_t dhl = tc::desc_kmajor(tc::smem_u32(sHl), N, 0);
+#pragma unroll
                     for (int ks = 0; ks < N / 16; ++ks)
-                        tc::mma_bf16(tYo, tc::desc_kmajor(ca, N, ks), tc::desc_kmajor(hh, N, ks), id_off, ks > 0);
+                        tc::mma_bf16(tYo, dc + ks * tc::kstep_kmajor(), dhh + ks * tc::kstep_kmajor(), id_off, ks > 0);
+#pragma unroll
                     for (int ks = 0; ks < N / 16; ++ks)
-                        tc::mma_bf16(tYo, tc::desc_kmajor(ca, N, ks), tc::desc_kmajor(hl, N, ks), id_off, 1);
+                        tc::mma_bf16(tYo, dc + ks * tc::kstep_kmajor(), dhl + ks * tc::kstep_kmajor(), id_off, 1);
                 }
-                tc::mma_commit(&s_mbar);
+                tc::mma_commit(&s_mbar[ncommit & 1]);
+            }
+            ++ncommit;
+            // the previous head's epilogue, once this head's first MMAs are queued
+            if (kp == 0 && hi > 0) {
+                wait_commit(last_commit_prev);
+                finish(h - 1, (hi - 1) & 1, alpha_prev);
+                tc::fence_before_sync();
             }
         }
-        ok = tc::mbar_wait(&s_mbar, phase) && ok;
-        phase ^= 1;
-        tc::fence_after_sync();
-        if (!ok) break;
-        // epilogue: y = Y_diag + exp(cum_t) Y_off + D x, gate, store 64 bf16
-        {
-            const float et = __expf(cum_t);
-            const float Dh = a.D ? a.D[h] : 0.0f;
-            const int64_t row = ((b * a.T + c * a.Q + t) * a.H + h) * kP;
-#pragma unroll 1
-            for (int p0 = 32 * chalf; p0 < 32 * chalf + 32; p0 += 16) {
-                float yd[16], yo[16];
-                tc::tmem_ld16(tYd + lane_base + (uint32_t)p0, yd);
-                tc::tmem_ld16(tYo + lane_base + (uint32_t)p0, yo);
-                if (row_ok) {
-                    uint32_t pk[8];
-#pragma unroll
-                    for (int j = 0; j < 16; j += 8) {
-                        const uint4 xr = *reinterpret_cast<const uint4*>(sXh + tc::off_mnmajor(p0 + j, t, kP));
-                        const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&xr);
-                        uint4 zr = make_uint4(0, 0, 0, 0);
-                        if (GATE) zr = *reinterpret_cast<const uint4*>(a.z + row + p0 + j);
-                        const __nv_bfloat162* z2 = reinterpret_cast<const __nv_bfloat162*>(&zr);
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const float2 xv = __bfloat1622float2(x2[k]);
-                            float y0 = fmaf(et, yo[j + 2 * k], yd[j + 2 * k]) + Dh * xv.x;
-                            float y1 = fmaf(et, yo[j + 2 * k + 1], yd[j + 2 * k + 1]) + Dh * xv.y;
-                            if (GATE) {
-                                const float2 zv = __bfloat1622float2(z2[k]);
-                                y0 *= silu(zv.x);
-                                y1 *= silu(zv.y);
-                            }
-                            pk[j / 2 + k] = pack_bf16x2(y0, y1);
-                        }
-                    }
-                    uint4* dst = reinterpret_cast<uint4*>(a.out + row + p0);
-                    dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-                }
-            }
-        }
+        last_commit_prev = ncommit - 1;
+        alpha_prev = alpha;
+    }
+    if (ok && heads_per_cta > 0) {
+        wait_commit(last_commit_prev);
+        finish(hbeg + heads_per_cta - 1, (heads_per_cta - 1) & 1, alpha_prev);
     }
     if (!ok && tid == 0) report_timeout(a.status);
     tc::fence_before_sync();
@@ -504,10 +616,8 @@ cudaError_t launch_state(const SsdTcArgs& s, int64_t batch, cudaStream_t stream)
 
 template <int N, bool GATE>
 cudaError_t launch_scan(const SsdTcArgs& s, int64_t batch, cudaStream_t stream) {
-    const size_t phase1 = (size_t)256 * N * 2;  // B rows (up to 256)
-    const size_t phase2 = (size_t)128 * 128 * 4 + (size_t)256 * kP * 2 + (size_t)kP * N * 4;
     // at least 116 KB so that one CTA (holding all 512 TMEM columns) runs per SM
-    const size_t smem = std::max<size_t>((size_t)128 * N * 2 + std::max(phase1, phase2), 116 * 1024);
+    const size_t smem = std::max<size_t>(ScanTcCfg<N>::kSmem, 116 * 1024);
     auto kern = ssd_scan_tc<N, GATE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

@@ -63,6 +63,11 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t base, int MN, int ks) 
     return make_desc(base + (uint32_t)ks * 2u * kstride, kstride, 128u);
 }
 
+// Descriptor advance per k-step (16 elements of K), in units of the 16-byte address
+// field: K-major tiles move 256 bytes, MN-major tiles two core matrices along K.
+__host__ __device__ constexpr uint64_t kstep_kmajor() { return 256u >> 4; }
+__host__ __device__ constexpr uint64_t kstep_mnmajor(int MN) { return (uint64_t)(2 * (MN >> 3) * 128) >> 4; }
+
 // ---- tensor memory (one full warp executes these)
 __device__ __forceinline__ void tmem_alloc(uint32_t* smem_dst, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(smem_dst)),
@@ -138,6 +143,16 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+
+// Issue a load of 16 columns without waiting; complete with tmem_wait_ld().
+__device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // TMEM address of (lane, column).
 __device__ __forceinline__ uint32_t taddr(uint32_t base, uint32_t lane, uint32_t col) {
