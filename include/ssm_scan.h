@@ -30,6 +30,8 @@
  *     A, D, dt_bias: (nheads,) fp32
  *     final_state: (batch, nheads, headdim, dstate) fp32
  *   both: B, C : (batch, seqlen, ngroups, dstate); head h reads group h / (nheads/ngroups).
+ *   SSD also needs headdim * dstate to be a multiple of 4 (the state moves in 16-byte
+ *   pieces).
  *   x, dt, B, C, z and out share the element type `dtype` (fp32 or bf16; bf16 output
  *   is rounded to nearest even).  State and accumulation are fp32.
  *
@@ -139,6 +141,47 @@ int ssm_scan_fwd_noalloc(const void* x, const void* dt, const float* A, const vo
                          const void* C, const float* D, const void* z, const float* dt_bias,
                          void* out, float* final_state, const ssm_shape* shape,
                          ssm_stream_t stream);
+
+/*
+ * Forward scan that starts from a given state instead of zero: h_{-1} = initial_state.
+ * Together with final_state this lets a long sequence be scanned in pieces, each call
+ * resuming where the previous one stopped (the recurrent form needs only the previous
+ * state: "Mamba-2：把状态空间模型和 Attention 统一到一个数学框架里", 背景问题; the
+ * streaming example of "引言：Attention的天花板" passes the state between calls).
+ * Arguments as ssm_scan_fwd, plus:
+ *   initial_state: NULL (start from zero) or device fp32 of the final_state layout
+ *     (DIAG (batch, nheads, dstate); SSD (batch, nheads, headdim, dstate)), 16-byte
+ *     aligned.  It must not overlap final_state (SSM_ERR_SHAPE): with the sequence split
+ *     across thread blocks, some blocks read it after others have written the final
+ *     state.  With seqlen 0 the final state is a copy of the initial state.
+ *   workspace, workspace_bytes: both NULL/0 to draw scratch from the stream-ordered
+ *     allocator as ssm_scan_fwd does; otherwise caller scratch as for ssm_scan_fwd_ws.
+ */
+int ssm_scan_fwd_state(const void* x, const void* dt, const float* A, const void* B, const void* C,
+                       const float* D, const void* z, const float* dt_bias,
+                       const float* initial_state, void* out, float* final_state,
+                       const ssm_shape* shape, void* workspace, size_t workspace_bytes,
+                       ssm_stream_t stream);
+
+/*
+ * One token of recurrent decoding for a batch of sequences, the state carried in place:
+ *   Delta = softplus(dt + dt_bias); h <- exp(Delta A) h + Delta B x;
+ *   out = (C . h + D x) * SiLU(z)
+ * (the recurrent form of "Mamba-2：把状态空间模型和 Attention 统一到一个数学框架里",
+ * 背景问题: constant memory per generated token).  The result equals ssm_scan_fwd_state
+ * over a sequence of length 1 with initial_state = state, final_state = state.
+ *   shape: as for the scan with seqlen == 1 (SSM_ERR_SHAPE otherwise); chunk is not used
+ *     beyond the scan's checks; dstate must be a multiple of 4 (SSM_ERR_ALIGN).
+ *   x, z, out: (batch, nheads, headdim) (DIAG: headdim 1); dt: (batch, nheads);
+ *   B, C: (batch, ngroups, dstate); A, D, dt_bias as for the scan.
+ *   state: device fp32, (batch, nheads, headdim, dstate) (DIAG: (batch, nheads, dstate)),
+ *     read and overwritten with the new state.  It must not overlap out (SSM_ERR_SHAPE).
+ * Needs no scratch and allocates nothing.  Calls on one stream apply in order, so a
+ * loop of calls is a decode of one token per call.
+ */
+int ssm_step(const void* x, const void* dt, const float* A, const void* B, const void* C,
+             const float* D, const void* z, const float* dt_bias, float* state, void* out,
+             const ssm_shape* shape, ssm_stream_t stream);
 
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char* ssm_strerror(int status);

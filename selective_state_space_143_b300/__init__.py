@@ -14,7 +14,8 @@ import torch
 from . import _lib
 from ._lib import SsmError, ssm_shape
 
-__all__ = ["scan_fwd", "workspace_size", "make_shape", "launch_count", "SsmError", "ssm_shape"]
+__all__ = ["scan_fwd", "step", "workspace_size", "make_shape", "launch_count", "SsmError",
+           "ssm_shape"]
 
 _DTYPES = {torch.float32: _lib.SSM_F32, torch.bfloat16: _lib.SSM_BF16}
 
@@ -82,7 +83,8 @@ def workspace_size(x, A, B, chunk: int = 0) -> int:
 
 
 def scan_fwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, *, out=None, final_state=None,
-             return_final_state: bool = False, chunk: int = 0, workspace=None, stream=None):
+             return_final_state: bool = False, chunk: int = 0, workspace=None, stream=None,
+             initial_state=None):
     """Selective scan forward on the GPU.
 
     out_t = (C_t . h_t + D x_t) * SiLU(z_t),  h_t = exp(Delta_t A) h_{t-1} + Delta_t B_t x_t,
@@ -93,7 +95,8 @@ def scan_fwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, *, out=None, final_st
     ``final_state`` tensor is passed.  Runs asynchronously on ``stream`` (default: the
     current torch stream).  ``workspace``: optional uint8 CUDA tensor of at least
     ``workspace_size`` bytes; otherwise the library draws scratch from the stream-ordered
-    allocator.
+    allocator.  ``initial_state``: optional float32 state entering t = 0 (the layout of
+    ``final_state``; must not share memory with it), for resuming a split sequence.
     """
     s = make_shape(x, A, B, chunk)
     dev = x.device
@@ -117,18 +120,25 @@ def scan_fwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, *, out=None, final_st
     if want_state and final_state is None:
         final_state = torch.empty(st_shape, device=dev, dtype=torch.float32)
     _check("final_state", final_state, st_shape, torch.float32, dev)
+    _check("initial_state", initial_state, st_shape, torch.float32, dev)
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     handle = ctypes.c_void_p(stream.cuda_stream)
     lib = _lib.load()
     with torch.cuda.device(dev):
-        if workspace is None:
+        if workspace is not None and workspace.device != dev:
+            raise ValueError("workspace must be on x's device")
+        if initial_state is not None:
+            ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+            rc = lib.ssm_scan_fwd_state(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                        _ptr(z), _ptr(dt_bias), _ptr(initial_state), _ptr(out),
+                                        _ptr(final_state), ctypes.byref(s), _ptr(workspace),
+                                        ws_bytes, handle)
+        elif workspace is None:
             rc = lib.ssm_scan_fwd(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
                                   _ptr(dt_bias), _ptr(out), _ptr(final_state), ctypes.byref(s),
                                   handle)
         else:
-            if workspace.device != dev:
-                raise ValueError("workspace must be on x's device")
             rc = lib.ssm_scan_fwd_ws(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
                                      _ptr(z), _ptr(dt_bias), _ptr(out), _ptr(final_state),
                                      ctypes.byref(s), _ptr(workspace),
@@ -136,6 +146,66 @@ def scan_fwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, *, out=None, final_st
     if rc != _lib.SSM_OK:
         raise SsmError(rc, "ssm_scan_fwd")
     return (out, final_state) if want_state else out
+
+
+def step(x, dt, A, B, C, D=None, z=None, dt_bias=None, *, state, out=None, stream=None):
+    """One token of recurrent decoding; ``state`` (float32) is updated in place.
+
+    DIAG: x, z (b, D), dt (b, D), A (D, N), B, C (b, N) or (b, G, N), state (b, D, N).
+    SSD: x, z (b, H, P), dt (b, H), A (H,), B, C (b, N) or (b, G, N), state (b, H, P, N).
+    Returns ``out`` (shaped like x).  Equivalent to ``scan_fwd`` over one token with
+    ``initial_state=state`` and the final state written back to ``state``.
+    """
+    dev = x.device
+    if dev.type != "cuda":
+        raise ValueError("step runs on CUDA tensors only")
+    if x.dtype not in _DTYPES:
+        raise TypeError(f"x must be float32 or bfloat16, got {x.dtype}")
+    s = ssm_shape()
+    s.dtype = _DTYPES[x.dtype]
+    s.seqlen = 1
+    if A.dim() == 2:
+        if x.dim() != 2:
+            raise ValueError("diagonal mode: x must be (batch, d_inner)")
+        s.mode = _lib.SSM_MODE_DIAG
+        (s.batch, s.nheads), s.headdim = x.shape, 1
+    elif A.dim() == 1:
+        if x.dim() != 3:
+            raise ValueError("SSD mode: x must be (batch, nheads, headdim)")
+        s.mode = _lib.SSM_MODE_SSD
+        s.batch, s.nheads, s.headdim = x.shape
+    else:
+        raise ValueError("A must be 2-D (d_inner, dstate) or 1-D (nheads,)")
+    if B.dim() == 2:
+        s.ngroups, s.dstate = 1, B.shape[1]
+    elif B.dim() == 3:
+        s.ngroups, s.dstate = B.shape[1], B.shape[2]
+    else:
+        raise ValueError("B must be (batch, dstate) or (batch, ngroups, dstate)")
+    s.chunk, s.flags = 0, 0
+    b, H, P, N = s.batch, s.nheads, s.headdim, s.dstate
+    diag = s.mode == _lib.SSM_MODE_DIAG
+    _check("x", x, x.shape, x.dtype, dev)
+    _check("dt", dt, (b, H), x.dtype, dev)
+    _check("A", A, (H, N) if diag else (H,), torch.float32, dev)
+    _check("B", B, B.shape, x.dtype, dev)
+    _check("C", C, B.shape, x.dtype, dev)
+    _check("D", D, (H,), torch.float32, dev)
+    _check("z", z, x.shape, x.dtype, dev)
+    _check("dt_bias", dt_bias, (H,), torch.float32, dev)
+    _check("state", state, (b, H, N) if diag else (b, H, P, N), torch.float32, dev)
+    if out is None:
+        out = torch.empty_like(x)
+    _check("out", out, x.shape, x.dtype, dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        rc = _lib.load().ssm_step(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                                  _ptr(dt_bias), _ptr(state), _ptr(out), ctypes.byref(s),
+                                  ctypes.c_void_p(stream.cuda_stream))
+    if rc != _lib.SSM_OK:
+        raise SsmError(rc, "ssm_step")
+    return out
 
 
 def launch_count() -> int:

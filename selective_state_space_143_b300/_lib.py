@@ -28,7 +28,8 @@ SSM_BF16 = 1
 
 # Every function declared in include/ssm_scan.h.
 EXPORTED = ("ssm_scan_fwd", "ssm_scan_fwd_ws", "ssm_scan_workspace_size", "ssm_scan_fwd_noalloc",
-            "ssm_strerror", "ssm_kernel_launch_count", "ssm_abi_version")
+            "ssm_scan_fwd_state", "ssm_step", "ssm_strerror", "ssm_kernel_launch_count",
+            "ssm_abi_version")
 
 
 class ssm_shape(ctypes.Structure):
@@ -79,6 +80,11 @@ def load() -> ctypes.CDLL:
         lib.ssm_scan_fwd_ws.restype = ctypes.c_int
         lib.ssm_scan_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sp, vp]
         lib.ssm_scan_fwd_noalloc.restype = ctypes.c_int
+        lib.ssm_scan_fwd_state.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sp, vp,
+                                           ctypes.c_size_t, vp]
+        lib.ssm_scan_fwd_state.restype = ctypes.c_int
+        lib.ssm_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sp, vp]
+        lib.ssm_step.restype = ctypes.c_int
         lib.ssm_scan_workspace_size.argtypes = [sp]
         lib.ssm_scan_workspace_size.restype = ctypes.c_size_t
         lib.ssm_strerror.argtypes = [ctypes.c_int]

@@ -48,6 +48,8 @@ int check_shape(const ssm_shape* s) {
         if (s->chunk != 0 && (s->chunk % 16 != 0 || s->chunk > 256)) return SSM_ERR_SHAPE;
         if ((s->nheads * s->headdim * E) % 16 != 0) return SSM_ERR_ALIGN;
         if ((s->ngroups * s->dstate * E) % 16 != 0) return SSM_ERR_ALIGN;
+        // the state of one head moves in 16-byte pieces
+        if ((s->headdim * s->dstate) % 4 != 0) return SSM_ERR_ALIGN;
         if (s->nheads * ((s->headdim + 63) / 64) * ((s->dstate + 63) / 64) > kMaxGridYZ)
             return SSM_ERR_UNSUPPORTED;
     }
@@ -56,16 +58,27 @@ int check_shape(const ssm_shape* s) {
 
 int check_args(const void* x, const void* dt, const float* A, const void* B, const void* C,
                const float* D, const void* z, const float* dt_bias, const void* out,
-               const float* final_state, const ssm_shape* s) {
+               const float* final_state, const ssm_shape* s, const float* initial_state = nullptr) {
     const int rc = check_shape(s);
     if (rc != SSM_OK) return rc;
     // x, dt, B, C and out may be NULL only when they hold no elements
     const bool empty = s->batch == 0 || s->seqlen == 0;
     if (!A || (!empty && (!x || !dt || !B || !C || !out))) return SSM_ERR_NULL;
-    const void* ptrs[] = {x, dt, A, B, C, D, z, dt_bias, out, final_state};
+    const void* ptrs[] = {x, dt, A, B, C, D, z, dt_bias, out, final_state, initial_state};
     for (const void* p : ptrs)
         if (!aligned16(p)) return SSM_ERR_ALIGN;
     return SSM_OK;
+}
+
+// Bytes of the fp32 state of all sequences: (batch, nheads, headdim, dstate).
+size_t state_bytes(const ssm_shape* s) {
+    return (size_t)s->batch * s->nheads * s->headdim * s->dstate * sizeof(float);
+}
+
+bool overlaps(const void* p, size_t pn, const void* q, size_t qn) {
+    if (!p || !q || pn == 0 || qn == 0) return false;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(q);
+    return a < b + qn && b < a + pn;
 }
 
 ScanArgs make_args(const void* x, const void* dt, const float* A, const void* B, const void* C,
@@ -104,6 +117,31 @@ int run(const ScanArgs& a, int mode, void* ws, cudaStream_t stream) {
     return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
+// Caller-provided scratch.
+int run_with(const ScanArgs& a, int mode, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    const size_t need = workspace_for(a, mode);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return SSM_ERR_ALLOC;
+    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SSM_ERR_ALIGN;
+    return run(a, mode, workspace, stream);
+}
+
+// Scratch from the stream-ordered allocator, freed on the same stream.
+int run_allocating(const ScanArgs& a, int mode, cudaStream_t st) {
+    const size_t need = workspace_for(a, mode);
+    void* ws = nullptr;
+    if (need > 0 && a.batch > 0) {
+        if (cudaMallocAsync(&ws, need, st) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return SSM_ERR_ALLOC;
+        }
+    }
+    const int r = run(a, mode, ws, st);
+    if (ws) {
+        if (cudaFreeAsync(ws, st) != cudaSuccess && r == SSM_OK) return SSM_ERR_CUDA;
+    }
+    return r;
+}
+
 }  // namespace
 }  // namespace ssm
 
@@ -111,7 +149,7 @@ using namespace ssm;
 
 extern "C" {
 
-int ssm_abi_version(void) { return (1 << 16) | 0; }
+int ssm_abi_version(void) { return (1 << 16) | 1; }
 
 uint64_t ssm_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
@@ -144,10 +182,7 @@ int ssm_scan_fwd_ws(const void* x, const void* dt, const float* A, const void* B
     const int rc = check_args(x, dt, A, B, C, D, z, dt_bias, out, final_state, shape);
     if (rc != SSM_OK) return rc;
     const ScanArgs a = make_args(x, dt, A, B, C, D, z, dt_bias, out, final_state, shape);
-    const size_t need = workspace_for(a, shape->mode);
-    if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return SSM_ERR_ALLOC;
-    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SSM_ERR_ALIGN;
-    return run(a, shape->mode, workspace, (cudaStream_t)stream);
+    return run_with(a, shape->mode, workspace, workspace_bytes, (cudaStream_t)stream);
 }
 
 int ssm_scan_fwd(const void* x, const void* dt, const float* A, const void* B, const void* C,
@@ -156,20 +191,42 @@ int ssm_scan_fwd(const void* x, const void* dt, const float* A, const void* B, c
     const int rc = check_args(x, dt, A, B, C, D, z, dt_bias, out, final_state, shape);
     if (rc != SSM_OK) return rc;
     const ScanArgs a = make_args(x, dt, A, B, C, D, z, dt_bias, out, final_state, shape);
-    const size_t need = workspace_for(a, shape->mode);
-    void* ws = nullptr;
-    cudaStream_t st = (cudaStream_t)stream;
-    if (need > 0 && a.batch > 0) {
-        if (cudaMallocAsync(&ws, need, st) != cudaSuccess) {
-            (void)cudaGetLastError();
-            return SSM_ERR_ALLOC;
-        }
-    }
-    const int r = run(a, shape->mode, ws, st);
-    if (ws) {
-        if (cudaFreeAsync(ws, st) != cudaSuccess && r == SSM_OK) return SSM_ERR_CUDA;
-    }
-    return r;
+    return run_allocating(a, shape->mode, (cudaStream_t)stream);
+}
+
+int ssm_scan_fwd_state(const void* x, const void* dt, const float* A, const void* B, const void* C,
+                       const float* D, const void* z, const float* dt_bias,
+                       const float* initial_state, void* out, float* final_state,
+                       const ssm_shape* shape, void* workspace, size_t workspace_bytes,
+                       ssm_stream_t stream) {
+    const int rc = check_args(x, dt, A, B, C, D, z, dt_bias, out, final_state, shape, initial_state);
+    if (rc != SSM_OK) return rc;
+    // the initial state is read by blocks that may start after the final state is written
+    if (overlaps(initial_state, state_bytes(shape), final_state, state_bytes(shape))) return SSM_ERR_SHAPE;
+    ScanArgs a = make_args(x, dt, A, B, C, D, z, dt_bias, out, final_state, shape);
+    a.initial_state = initial_state;
+    if (workspace == nullptr && workspace_bytes == 0) return run_allocating(a, shape->mode, (cudaStream_t)stream);
+    return run_with(a, shape->mode, workspace, workspace_bytes, (cudaStream_t)stream);
+}
+
+int ssm_step(const void* x, const void* dt, const float* A, const void* B, const void* C,
+             const float* D, const void* z, const float* dt_bias, float* state, void* out,
+             const ssm_shape* shape, ssm_stream_t stream) {
+    const int rc = check_shape(shape);
+    if (rc != SSM_OK) return rc;
+    if (shape->seqlen != 1) return SSM_ERR_SHAPE;
+    if (shape->dstate % 4 != 0) return SSM_ERR_ALIGN;  // state rows move in 16-byte pieces
+    if (shape->batch * shape->nheads * shape->headdim > (int64_t(1) << 36)) return SSM_ERR_UNSUPPORTED;
+    if (!A || (shape->batch > 0 && (!x || !dt || !B || !C || !out || !state))) return SSM_ERR_NULL;
+    const void* ptrs[] = {x, dt, A, B, C, D, z, dt_bias, out, state};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return SSM_ERR_ALIGN;
+    const size_t out_bytes = (size_t)shape->batch * shape->nheads * shape->headdim * elem_size(shape->dtype);
+    if (overlaps(state, state_bytes(shape), out, out_bytes)) return SSM_ERR_SHAPE;
+    if (shape->batch == 0) return SSM_OK;
+    const ScanArgs a = make_args(x, dt, A, B, C, D, z, dt_bias, out, nullptr, shape);
+    const cudaError_t e = step_launch(a, shape->mode == SSM_MODE_DIAG, state, (cudaStream_t)stream);
+    return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
 }  // extern "C"

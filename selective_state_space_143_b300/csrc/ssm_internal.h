@@ -35,6 +35,10 @@ cudaError_t diag_launch(const ScanArgs& a, void* ws, cudaStream_t stream);
 size_t ssd_workspace_bytes(const ScanArgs& a);
 cudaError_t ssd_launch(const ScanArgs& a, void* ws, cudaStream_t stream);
 
+// Single-token step: the state (batch, nheads, headdim, dstate) is updated in place and
+// out (batch, nheads, headdim) written; diag_a selects A of shape (nheads, dstate).
+cudaError_t step_launch(const ScanArgs& a, bool diag_a, float* state, cudaStream_t stream);
+
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 }  // namespace ssm

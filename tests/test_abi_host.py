@@ -70,6 +70,8 @@ BAD = ctypes.c_size_t(-1).value
     (dict(mode=1, headdim=64, nheads=8, dstate=300), False),
     (dict(mode=1, headdim=64, nheads=8, dstate=128, chunk=100), False),
     (dict(mode=1, headdim=64, nheads=8, dstate=128, chunk=512), False),
+    (dict(mode=1, dtype=0, headdim=3, nheads=4, dstate=1, ngroups=4), False),  # P*N % 4
+    (dict(mode=1, dtype=0, headdim=4, nheads=4, dstate=1, ngroups=4), True),
 ])
 def test_workspace_query_validates_shape(kw, valid):
     n = _ws(_shape(**kw))
@@ -137,3 +139,55 @@ def test_binding_refuses_cpu_tensors():
     x = torch.zeros(1, 4, 8)
     with pytest.raises(ValueError):
         ssm.scan_fwd(x, x, torch.zeros(8, 4), torch.zeros(1, 4, 4), torch.zeros(1, 4, 4))
+
+
+def _step(s, x=1 << 12, dt=2 << 12, A=3 << 12, B=4 << 12, C=5 << 12, state=6 << 12,
+          out=7 << 12, **opt):
+    lib = _lib.load()
+    vp = ctypes.c_void_p
+    return lib.ssm_step(vp(x), vp(dt), vp(A), vp(B), vp(C), vp(opt.get("D")), vp(opt.get("z")),
+                        vp(opt.get("dt_bias")), vp(state), vp(out),
+                        ctypes.byref(s) if s is not None else None, None)
+
+
+def test_step_argument_errors():
+    one = dict(seqlen=1)
+    assert _step(None) == _lib.SSM_ERR_NULL
+    assert _step(_shape(seqlen=2)) == _lib.SSM_ERR_SHAPE            # one token per call
+    assert _step(_shape(**one), state=0) == _lib.SSM_ERR_NULL
+    assert _step(_shape(**one), x=0) == _lib.SSM_ERR_NULL
+    assert _step(_shape(**one), state=(6 << 12) + 4) == _lib.SSM_ERR_ALIGN
+    assert _step(_shape(mode=1, nheads=8, headdim=8, dstate=2, ngroups=8, dtype=1, seqlen=1)) \
+        == _lib.SSM_ERR_ALIGN                                      # dstate % 4
+    # out inside the state: the in-place update would overwrite it
+    assert _step(_shape(**one), out=(6 << 12) + 256) == _lib.SSM_ERR_SHAPE
+    # nothing to do
+    assert _step(_shape(batch=0, seqlen=1), x=0, dt=0, B=0, C=0, state=0, out=0) == _lib.SSM_OK
+
+
+def test_scan_with_initial_state_argument_errors():
+    lib = _lib.load()
+    vp = ctypes.c_void_p
+    s = _shape()
+
+    def call(init, fs, ws=None, nbytes=0):
+        return lib.ssm_scan_fwd_state(vp(1 << 12), vp(2 << 12), vp(3 << 12), vp(4 << 12),
+                                      vp(5 << 12), None, None, None, vp(init), vp(6 << 12),
+                                      vp(fs), ctypes.byref(s), vp(ws), nbytes, None)
+
+    assert call((8 << 12) + 4, None) == _lib.SSM_ERR_ALIGN
+    st_bytes = 2 * 64 * 16 * 4
+    assert call(8 << 20, (8 << 20) + st_bytes - 16) == _lib.SSM_ERR_SHAPE  # overlap
+    s2 = _shape(mode=1, nheads=8, headdim=64, dstate=128, chunk=64, seqlen=256)
+    need = _ws(s2)
+    assert lib.ssm_scan_fwd_state(vp(1 << 12), vp(2 << 12), vp(3 << 12), vp(4 << 12),
+                                  vp(5 << 12), None, None, None, vp(8 << 20), vp(6 << 12), None,
+                                  ctypes.byref(s2), vp(1 << 20), need - 1, None) \
+        == _lib.SSM_ERR_ALLOC
+
+
+def test_step_binding_refuses_cpu_tensors():
+    x = torch.zeros(1, 8)
+    with pytest.raises(ValueError):
+        ssm.step(x, x, torch.zeros(8, 4), torch.zeros(1, 4), torch.zeros(1, 4),
+                 state=torch.zeros(1, 8, 4))
