@@ -62,11 +62,16 @@ class OracleLib:
             dp, dp, ip, i64, ctypes.c_int]
         lib.oracle_scan_chunked.restype = ctypes.c_int
         lib.oracle_max_threads.restype = ctypes.c_int
+        lib.oracle_conv_silu.argtypes = [i64] * 4 + [dp] * 6
+        lib.oracle_conv_silu.restype = ctypes.c_int
         self.lib = lib
         self.path = path
 
     def scan(self, *args, **kw):
         return _scan(self.lib, *args, **kw)
+
+    def conv_silu(self, *args, **kw):
+        return _conv_silu(self.lib, *args, **kw)
 
 
 def _load():
@@ -75,6 +80,47 @@ def _load():
         if _default is None:
             _default = OracleLib(build())
     return _default.lib
+
+
+def conv_silu(*args, **kw):
+    """Run the oracle's convolution + SiLU; see ``_conv_silu``."""
+    return _conv_silu(_load(), *args, **kw)
+
+
+def _conv_silu(lib, x, w, bias=None, x_prev=None):
+    """Causal depthwise convolution + SiLU ahead of the scan (fp64).
+
+    x: (b, T, H) or (b, T, H, P); w: (channels, K) with channels = H*P; bias: (channels,);
+    x_prev: (b, K-1, channels) inputs before t = 0 (None: zeros).
+    Returns ``(x_conv, x_last)``: x_conv shaped like x, x_last (b, K-1, channels) the
+    K-1 inputs that precede the end of the sequence.
+    """
+    x, w, bias, x_prev = (_f64(v) for v in (x, w, bias, x_prev))
+    b, T = x.shape[0], x.shape[1]
+    ch = int(np.prod(x.shape[2:]))
+    if w.ndim != 2 or w.shape[0] != ch:
+        raise ValueError("conv weight must be (channels, width)")
+    K = w.shape[1]
+    if bias is not None and bias.shape != (ch,):
+        raise ValueError("conv bias must be (channels,)")
+    if x_prev is not None and x_prev.size != b * (K - 1) * ch:
+        raise ValueError("x_prev must be (batch, width-1, channels)")
+    xc = np.empty(x.shape, dtype=np.float64)
+    x_last = np.empty((b, K - 1, ch), dtype=np.float64)
+    rc = lib.oracle_conv_silu(b, T, ch, K, _ptr(x), _ptr(w), _ptr(bias), _ptr(x_prev),
+                                  _ptr(xc), _ptr(x_last))
+    if rc != 0:
+        raise RuntimeError(f"oracle returned status {rc}")
+    return xc, x_last
+
+
+def scan_conv(x, dt, A, B, C, D=None, z=None, dt_bias=None, *, conv_w, conv_b=None,
+              x_prev=None, **kw):
+    """The scan with the convolution + SiLU ahead of it: ``conv_silu`` then ``scan`` on
+    the convolved input.  Returns ``(out, final_state, x_last)``."""
+    xc, x_last = conv_silu(x, conv_w, conv_b, x_prev)
+    out, fs = scan(xc, dt, A, B, C, D, z, dt_bias, **kw)
+    return out, fs, x_last
 
 
 def max_threads() -> int:

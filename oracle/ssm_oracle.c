@@ -18,6 +18,10 @@
  *       section 五 Mamba块架构: SSM output multiplied by SiLU of the z branch
  *   [Mamba / hybrid overview] "基础知识：Mamba 与混合 SSM 架构"
  *       section 2 从 SSM 到 Selective SSM: h_t = A_t h_{t-1} + B_t x_t, y_t = C_t h_t
+ *       section 3 Mamba block 里发生了什么: a depthwise convolution adds local context
+ *       before the selective scan
+ *   [Mamba paper digest] section 五 Mamba块架构: the x branch runs Conv1d, then SiLU,
+ *       then the selective SSM; [SSM engineering article] 工程实践: kernel width d_conv = 4
  *
  * Readings taken where the pages are silent (each is listed in the design notes):
  *   - discretisation: Abar = exp(Delta * A) and Bbar = Delta * B (exponential decay,
@@ -28,6 +32,10 @@
  *     optional dt_bias added before the softplus;
  *   - out = (C.h + D x) * SiLU(z) with SiLU(z) = z / (1 + e^-z);
  *   - B and C are shared by groups: channel group g = head / (nheads / ngroups).
+ *   - the convolution ahead of the scan (oracle_conv_silu) is causal and depthwise,
+ *     x'_t = SiLU(bias + sum_k w[k] x_{t-K+1+k}), so w[K-1] weights the current input;
+ *     inputs before t = 0 come from the previous call (x_prev) or are zero.  The scan
+ *     then reads x' wherever it reads x, the skip term included.
  *
  * Layouts (row-major, token-major, all float64 here):
  *   x, z, out      (batch, seqlen, nheads, headdim)   -- DIAG: headdim == 1
@@ -247,6 +255,54 @@ int oracle_scan_chunked(int mode, int64_t batch, int64_t seqlen, int64_t nheads,
     oracle_problem p = {mode, batch, seqlen, nheads, headdim, dstate, ngroups, x, dt, A, B, C,
                         D, z, dt_bias, initial_state, out, final_state};
     return oracle_run(&p, chunk, sel, nsel, nthreads);
+}
+
+/*
+ * Causal depthwise convolution followed by SiLU, per batch b, time t and channel c
+ * (channels = nheads * headdim, innermost):
+ *   x'[b,t,c] = SiLU( bias[c] + sum_{k=0..K-1} w[c,k] * x[b, t-K+1+k, c] )
+ * where x at a time s < 0 is x_prev[b, K-1+s, c] (NULL: zero).  x_last, if given,
+ * receives the K-1 inputs that precede time T: x_last[b, j, c] = x at time T-K+1+j
+ * (taken from x_prev where that time is negative).
+ * Layouts: x, xc (batch, T, channels); w (channels, K); bias (channels,) nullable;
+ * x_prev, x_last (batch, K-1, channels) nullable.
+ */
+int oracle_conv_silu(int64_t batch, int64_t seqlen, int64_t channels, int64_t width,
+                     const double* x, const double* w, const double* bias,
+                     const double* x_prev, double* xc, double* x_last) {
+    if (!x || !w || !xc || batch < 0 || seqlen < 0 || channels <= 0 || width < 1) return 2;
+    const int64_t K = width;
+    for (int64_t b = 0; b < batch; ++b) {
+        for (int64_t t = 0; t < seqlen; ++t) {
+            for (int64_t c = 0; c < channels; ++c) {
+                double acc = bias ? bias[c] : 0.0;
+                for (int64_t k = 0; k < K; ++k) {
+                    const int64_t s = t - K + 1 + k;
+                    double v = 0.0;
+                    if (s >= 0)
+                        v = x[(b * seqlen + s) * channels + c];
+                    else if (x_prev)
+                        v = x_prev[(b * (K - 1) + (K - 1 + s)) * channels + c];
+                    acc += w[c * K + k] * v;
+                }
+                xc[(b * seqlen + t) * channels + c] = oracle_silu(acc);
+            }
+        }
+        if (x_last) {
+            for (int64_t j = 0; j < K - 1; ++j) {
+                const int64_t s = seqlen - K + 1 + j;
+                for (int64_t c = 0; c < channels; ++c) {
+                    double v = 0.0;
+                    if (s >= 0)
+                        v = x[(b * seqlen + s) * channels + c];
+                    else if (x_prev)
+                        v = x_prev[(b * (K - 1) + (K - 1 + s)) * channels + c];
+                    x_last[(b * (K - 1) + j) * channels + c] = v;
+                }
+            }
+        }
+    }
+    return 0;
 }
 
 int oracle_max_threads(void) {

@@ -43,6 +43,39 @@ MUTANTS = {
 }
 
 
+CONV_MUTANTS = {
+    "conv_flipped": ("acc += w[c * K + k] * v;", "acc += w[c * K + (K - 1 - k)] * v;"),
+    "conv_drop_bias": ("double acc = bias ? bias[c] : 0.0;", "double acc = 0.0;"),
+    "conv_prev_offset": ("v = x_prev[(b * (K - 1) + (K - 1 + s)) * channels + c];\n"
+                         "                    acc += w[c * K + k] * v;",
+                         "v = x_prev[(b * (K - 1) + (K - 2 + s)) * channels + c];\n"
+                         "                    acc += w[c * K + k] * v;"),
+    "conv_no_silu": ("xc[(b * seqlen + t) * channels + c] = oracle_silu(acc);",
+                     "xc[(b * seqlen + t) * channels + c] = acc;"),
+    "conv_last_off_by_one": ("const int64_t s = seqlen - K + 1 + j;", "const int64_t s = seqlen - K + j;"),
+}
+
+
+def _conv_pins(conv):
+    """The convolution pins against ``conv`` (numpy.convolve per channel, resume)."""
+    failed = []
+    rng = np.random.default_rng(77)
+    x = rng.standard_normal((2, 9, 3))
+    w = rng.standard_normal((3, 4))
+    bias = rng.standard_normal(3)
+    prev = rng.standard_normal((2, 3, 3))
+    xc, last = conv(x, w, bias, prev)
+    for b in range(2):
+        for c in range(3):
+            seq = np.concatenate([prev[b, :, c], x[b, :, c]])
+            pre = np.convolve(seq, w[c, ::-1])[3:12] + bias[c]
+            if not np.allclose(xc[b, :, c], pre / (1 + np.exp(-pre)), rtol=1e-12, atol=1e-14):
+                failed.append("numpy_convolve")
+            if not np.array_equal(last[b, :, c], seq[-3:]):
+                failed.append("last_inputs")
+    return failed
+
+
 def _pins(scan):
     """Run the pins against ``scan``; return the names of those that fail."""
     failed = []
@@ -104,3 +137,15 @@ def test_mutant_is_caught(tmp_path, name):
     old, new = MUTANTS[name]
     lib = _build_variant(tmp_path, name, old, new)
     assert _pins(lib.scan), f"mutant {name} passed every pin"
+
+
+def test_unmutated_conv_passes(tmp_path):
+    lib = _build_variant(tmp_path, "identity_conv", "oracle_silu", "oracle_silu")
+    assert _conv_pins(lib.conv_silu) == []
+
+
+@pytest.mark.parametrize("name", sorted(CONV_MUTANTS))
+def test_conv_mutant_is_caught(tmp_path, name):
+    old, new = CONV_MUTANTS[name]
+    lib = _build_variant(tmp_path, name, old, new)
+    assert _conv_pins(lib.conv_silu), f"mutant {name} passed every pin"

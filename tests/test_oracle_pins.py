@@ -18,6 +18,10 @@ the wrong discretisation) fails at least one of them:
   invariance, SSD == diagonal mode with tied A, and the direction of the
   Delta effect ("Mamba-2 ..." explainer, section 第一步: large Delta updates
   the state quickly, small Delta keeps it).
+* the causal depthwise convolution + SiLU ahead of the scan ("论文解读：Mamba —
+  线性时间的序列建模革命", section 五 Mamba块架构): numpy's own convolution routine
+  on every channel, the identity and pure-delay kernels, and resuming from the
+  previous call's last inputs.
 """
 import math
 import os
@@ -388,3 +392,71 @@ def test_error_measure_leaves_margin_for_exact_fp32(mode):
     y, h = oracle.scan(**arr)
     assert oracle.max_rel_error(y32, y) < 2e-5
     assert oracle.max_rel_error(h32, h) < 2e-5
+
+
+# ---------------------------------------------------------------- convolution ahead of the scan
+
+def _conv_problem(rng, b, T, ch, K):
+    return (rng.standard_normal((b, T, ch)), rng.standard_normal((ch, K)),
+            rng.standard_normal(ch), rng.standard_normal((b, K - 1, ch)))
+
+
+@pytest.mark.parametrize("K", [1, 2, 3, 4])
+def test_conv_matches_numpy_convolution(K):
+    """Every channel against numpy.convolve: the causal correlation
+    sum_k w[k] x[t-K+1+k] is the full convolution with the reversed kernel, cut to
+    the first T outputs; the previous call's inputs are prepended."""
+    rng = np.random.default_rng(40 + K)
+    x, w, bias, x_prev = _conv_problem(rng, 2, 17, 5, K)
+    for prev in (None, x_prev):
+        xc, x_last = oracle.conv_silu(x, w, bias, prev)
+        for b in range(2):
+            for c in range(5):
+                head = np.zeros(K - 1) if prev is None else prev[b, :, c]
+                seq = np.concatenate([head, x[b, :, c]])
+                pre = np.convolve(seq, w[c, ::-1])[K - 1:K - 1 + 17] + bias[c]
+                assert np.allclose(xc[b, :, c], _silu_ref(pre), rtol=1e-13, atol=1e-14)
+                assert np.array_equal(x_last[b, :, c], seq[len(seq) - (K - 1):] if K > 1
+                                      else np.zeros(0))
+
+
+def test_conv_identity_and_delay_kernels():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((1, 9, 4))
+    ident = np.zeros((4, 4))
+    ident[:, 3] = 1.0
+    xc, _ = oracle.conv_silu(x, ident)
+    assert np.allclose(xc, _silu_ref(x), rtol=1e-14, atol=0)
+    delay = np.zeros((4, 4))
+    delay[:, 0] = 1.0
+    xc, _ = oracle.conv_silu(x, delay)
+    assert np.all(xc[:, :3] == 0.0)
+    assert np.allclose(xc[:, 3:], _silu_ref(x[:, :-3]), rtol=1e-14, atol=0)
+
+
+def test_conv_resume_from_last_inputs():
+    """Two calls, the second fed the first one's last inputs, equal one call -- also
+    when the first piece is shorter than the kernel."""
+    rng = np.random.default_rng(8)
+    x, w, bias, x_prev = _conv_problem(rng, 2, 12, 3, 4)
+    whole, last = oracle.conv_silu(x, w, bias, x_prev)
+    for cut in (1, 2, 7):
+        a, la = oracle.conv_silu(x[:, :cut], w, bias, x_prev)
+        bb, lb = oracle.conv_silu(x[:, cut:], w, bias, la)
+        assert np.array_equal(np.concatenate([a, bb], axis=1), whole)
+        assert np.array_equal(lb, last)
+
+
+def test_scan_conv_equals_scan_of_convolved_input():
+    """The skip term reads the convolved input too: with Delta = 0 the output is
+    D * x' * SiLU(z)."""
+    rng = np.random.default_rng(12)
+    arr = _rand_problem(rng, "diag", 1, 10, 3, 1, 2, 1)
+    w = rng.standard_normal((3, 4))
+    cb = rng.standard_normal(3)
+    arr["dt"] = np.full_like(arr["dt"], -1e4)
+    arr["dt_bias"] = None
+    out, fs, _ = oracle.scan_conv(**arr, conv_w=w, conv_b=cb)
+    xc, _ = oracle.conv_silu(arr["x"], w, cb)
+    assert np.allclose(out, arr["D"] * xc * _silu_ref(arr["z"]), rtol=1e-14, atol=1e-15)
+    assert np.all(fs == 0.0)
