@@ -61,6 +61,12 @@ def parse():
                     help="skip the clock soak, CPU baseline and end-to-end legs (profiling runs)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--conv", action="store_true",
+                    help="put the width-4 causal depthwise convolution + SiLU ahead of the scan")
+    ap.add_argument("--decode", action="store_true",
+                    help="time single-token recurrent steps (ssm_step) at the workload's widths")
+    ap.add_argument("--decode-batch", type=int, default=0,
+                    help="sequences decoded per step (0: enough for a 256 MB carried state)")
     return ap.parse_args()
 
 
@@ -184,17 +190,25 @@ def max_over_ranks(dist, value: float) -> float:
 
 # ---------------------------------------------------------------------------- CPU oracle
 
-def oracle_sample(w, inp, seconds: float, max_reps: int = 1000):
+def oracle_sample(w, inp, seconds: float, max_reps: int = 1000, conv=None):
     """Time the oracle on whole channels of the workload until ``seconds`` pass.
-    Returns (token-channels processed, elapsed seconds, threads, description)."""
+    Returns (token-channels processed, elapsed seconds, threads, description).  With
+    ``conv`` (weight, bias) each call also runs the oracle's convolution over the input."""
     import oracle
     nch = w.batch * w.d_inner
     per_channel = w.seqlen
+
+    def run(sel):
+        x = inp["x"]
+        if conv is not None:
+            x, _ = oracle.conv_silu(x, conv["weight"], conv["bias"])
+        oracle.scan(x, inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
+                    inp["dt_bias"], select=sel)
+
     # pick a channel block sized to ~1 s per call
     t0 = time.perf_counter()
     probe = np.arange(min(nch, 64))
-    oracle.scan(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
-                inp["dt_bias"], select=probe)
+    run(probe)
     dt_probe = max(time.perf_counter() - t0, 1e-4)
     per_call = int(min(nch, max(64, probe.size * 1.0 / dt_probe)))
     done, elapsed, reps = 0, 0.0, 0
@@ -202,8 +216,7 @@ def oracle_sample(w, inp, seconds: float, max_reps: int = 1000):
     while elapsed < seconds and reps < max_reps:
         sel = np.sort(rng.choice(nch, per_call, replace=False)) if per_call < nch else np.arange(nch)
         t0 = time.perf_counter()
-        oracle.scan(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
-                    inp["dt_bias"], select=sel)
+        run(sel)
         elapsed += time.perf_counter() - t0
         done += sel.size * per_channel
         reps += 1
@@ -275,10 +288,15 @@ def run_ours(args, w):
     fs = torch.empty(st_shape, device=dev, dtype=torch.float32) if w.final_state else None
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    conv = {}
+    if args.conv:
+        from selective_state_space_143_b300.inputs import conv_params
+        cp = conv_params(w.d_inner, 4, seed=w.seed)
+        conv = dict(conv_weight=cp["weight"].to(dev), conv_bias=cp["bias"].to(dev))
 
     def step():
         ssm.scan_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["z"], d["dt_bias"],
-                     out=out, final_state=fs, chunk=chunk, stream=stream)
+                     out=out, final_state=fs, chunk=chunk, stream=stream, **conv)
 
     for _ in range(max(args.warmup, 3)):
         flush.zero_()
@@ -322,7 +340,7 @@ def run_ours(args, w):
 
     # ---- roofline of the call (all its kernels) against the measured peaks
     peaks, peak_kind = measured_peaks()
-    nbytes = algorithmic_bytes(w)
+    nbytes = algorithmic_bytes(w) + (w.d_inner * 5 * 4 if args.conv else 0)
     hbm_gbs = nbytes / (ms_step * 1e-3) / 1e9
     roof = {"bound": "hbm", "achieved": hbm_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": hbm_gbs / peaks["hbm_gbs"], "traffic": None,
@@ -357,7 +375,7 @@ def run_ours(args, w):
             dd = {k: (None if v is None else v.to(dev, non_blocking=True)) for k, v in host.items()}
             o = ssm.scan_fwd(dd["x"], dd["dt"], dd["A"], dd["B"], dd["C"], dd["D"], dd["z"],
                              dd["dt_bias"], final_state=None if fs is None else torch.empty_like(fs),
-                             chunk=chunk, stream=stream)
+                             chunk=chunk, stream=stream, **conv)
             if fs is not None:
                 o, f = o
                 fs_h.copy_(f, non_blocking=True)
@@ -379,7 +397,8 @@ def run_ours(args, w):
         e2e = {"value": units / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
         if rank == 0:
-            done, el, threads, desc = oracle_sample(w, inp, args.cpu_seconds)
+            done, el, threads, desc = oracle_sample(w, inp, args.cpu_seconds,
+                                                    conv=cp if args.conv else None)
             cpu = {"value": done / el / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
                    "sample": desc, "seconds": el}
 
@@ -388,9 +407,173 @@ def run_ours(args, w):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-            "config": {"workload": f"{w.name}: {DESCRIPTIONS[w.name]}",
+            "config": {"workload": f"{w.name}: {DESCRIPTIONS[w.name]}" +
+                                   (", width-4 causal conv1d + SiLU ahead of the scan" if args.conv else ""),
                        "l2": "flushed before every timed step (256 MB write)",
                        "chunk": chunk, "parallelism": f"replicas x{world} (independent batches)"},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
+            "gpu_launches": int(launches),
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def decode_workload(args, w):
+    """The workload's widths with a serving batch: one token per sequence per step."""
+    per_seq = w.nheads * w.headdim * w.dstate * 4
+    batch = args.decode_batch or max(1, math.ceil((256 << 20) / per_seq))
+    return w.replace(name=w.name, batch=batch, seqlen=1, final_state=False, chunk=0), batch
+
+
+def decode_bytes(w) -> int:
+    """Bytes one decode step must move: the state read and written, the token's inputs
+    and output, the parameters."""
+    E = 2 if w.dtype == "bf16" else 4
+    b, H, P, N, G = w.batch, w.nheads, w.headdim, w.dstate, w.ngroups
+    nbytes = 2 * b * H * P * N * 4
+    nbytes += b * H * P * (2 + (1 if w.gate else 0)) * E + b * H * E + 2 * b * G * N * E
+    nbytes += (H * N if w.mode == "diag" else H) * 4
+    nbytes += H * 4 * ((1 if w.d_skip != "none" else 0) + (1 if w.dt_bias else 0))
+    return int(nbytes)
+
+
+def run_decode(args, w0):
+    """ssm_step over a batch of carried states; each step depends on the previous one."""
+    import selective_state_space_143_b300 as ssm
+    from selective_state_space_143_b300.inputs import make_inputs
+    dist, world, rank, local = dist_setup()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (there is no CPU path)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w, batch = decode_workload(args, w0)
+    ntok = 4  # distinct token inputs, used in turn
+    wt = w.replace(seqlen=ntok)
+    inp = make_inputs(wt)
+    diag = w.mode == "diag"
+
+    def token(t, src):
+        out = {}
+        for k in ("x", "dt", "z"):
+            v = src[k]
+            out[k] = None if v is None else v[:, t].contiguous()
+        for k in ("B", "C"):
+            out[k] = src[k][:, t].contiguous()
+        for k in ("A", "D", "dt_bias"):
+            out[k] = src[k]
+        return out
+
+    toks = [{k: (None if v is None else v.to(dev)) for k, v in token(t, inp).items()}
+            for t in range(ntok)]
+    st_shape = (batch, w.nheads, w.dstate) if diag else (batch, w.nheads, w.headdim, w.dstate)
+    gen = torch.Generator().manual_seed(11)
+    state0 = torch.randn(st_shape, generator=gen)
+    state = state0.to(dev)
+    outs = [torch.empty_like(toks[0]["x"]) for _ in range(ntok)]
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        d = toks[i % ntok]
+        ssm.step(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["z"], d["dt_bias"],
+                 state=state, out=outs[i % ntok], stream=stream)
+
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    if not args.quick:
+        clocks.start()
+        t_end = time.perf_counter() + 1.0
+        while time.perf_counter() < t_end:
+            for i in range(50):
+                step(i)
+            torch.cuda.synchronize()
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    barrier(dist)
+    torch.cuda.synchronize()
+    n0 = ssm.launch_count()
+    torch.cuda._sleep(int(min(2e9, 2e6 + K * 4e5)))
+    for i in range(K):
+        starts[i].record(stream)
+        step(i)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    launches = ssm.launch_count() - n0
+    barrier(dist)
+    ms_step = max_over_ranks(dist, sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / K)
+    clk = clocks.stop() if not args.quick else {"sm_mhz": None, "sm_max_mhz": None,
+                                               "reasons": ["not sampled (--quick)"]}
+    units = batch * w.nheads * w.headdim * world
+    value = units / (ms_step * 1e-3) / 1e9
+    peaks, peak_kind = measured_peaks()
+    nbytes = decode_bytes(w)
+    gbs = nbytes / (ms_step * 1e-3) / 1e9
+    roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": gbs / peaks["hbm_gbs"], "traffic": None, "kernel": "ssm_step_kernel",
+            "algorithmic_bytes_per_launch": nbytes, "peak_source": peak_kind}
+
+    cpu = e2e = None
+    if not args.quick:
+        # end to end: the token's inputs copied in and its output copied out every step
+        host = [{k: (None if v is None else v.pin_memory()) for k, v in token(t, inp).items()
+                 if k not in ("A", "D", "dt_bias")} for t in range(ntok)]
+        out_h = torch.empty(outs[0].shape, dtype=outs[0].dtype).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in host[0].values() if v is not None)
+        d2h = out_h.numel() * out_h.element_size()
+
+        def e2e_step(i):
+            hd = host[i % ntok]
+            dd = {k: (None if v is None else v.to(dev, non_blocking=True)) for k, v in hd.items()}
+            o = ssm.step(dd["x"], dd["dt"], toks[0]["A"], dd["B"], dd["C"], toks[0]["D"],
+                         dd["z"], toks[0]["dt_bias"], state=state, stream=stream)
+            out_h.copy_(o, non_blocking=True)
+
+        for i in range(3):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(K):
+            e2e_step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1) / K)
+        e2e = {"value": units / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+        if rank == 0:
+            import oracle
+            # one-token scans from the carried state over whole sequences until the
+            # sample time is used up
+            t_used, done, reps = 0.0, 0, 0
+            seqs = min(batch, 64)
+            h0 = state0[:seqs].numpy()
+            sub = {k: (None if v is None or k in ("A", "D", "dt_bias") else v[:seqs, :1])
+                   for k, v in inp.items()}
+            while t_used < args.cpu_seconds and reps < 10000:
+                t0 = time.perf_counter()
+                oracle.scan(sub["x"], sub["dt"], inp["A"], sub["B"], sub["C"], inp["D"],
+                            sub["z"], inp["dt_bias"], initial_state=h0)
+                t_used += time.perf_counter() - t0
+                done += seqs * w.nheads * w.headdim
+                reps += 1
+            cpu = {"value": done / t_used / 1e9, "unit": UNIT, "cores": oracle.max_threads(),
+                   "kind": "oracle", "seconds": t_used,
+                   "sample": f"{reps} one-token oracle scans of {seqs} sequences from a carried state"}
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": f"{w0.name}-decode: one token per step for {batch} sequences "
+                                   f"at the widths of {w0.name} ({DESCRIPTIONS[w0.name]})",
+                       "l2": f"carried state {batch * w.nheads * w.headdim * w.dstate * 4 >> 20} MB "
+                             "(larger than L2), not flushed",
+                       "parallelism": f"replicas x{world} (independent batches)"},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
             "gpu_launches": int(launches),
         }
@@ -406,6 +589,8 @@ def main():
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.decode:
+        return run_decode(args, w)
     return run_ours(args, w)
 
 

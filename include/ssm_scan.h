@@ -183,6 +183,58 @@ int ssm_step(const void* x, const void* dt, const float* A, const void* B, const
              const float* D, const void* z, const float* dt_bias, float* state, void* out,
              const ssm_shape* shape, ssm_stream_t stream);
 
+/*
+ * Causal depthwise convolution + SiLU applied to x ahead of the scan: the x branch of the
+ * Mamba block runs Conv1d, then SiLU, then the selective SSM ("论文解读：Mamba — 线性时间的
+ * 序列建模革命", 五 Mamba块架构; "基础知识：Mamba 与混合 SSM 架构", 3 Mamba block 里发生了
+ * 什么: a depthwise convolution adds local context; width d_conv = 4 in the example of
+ * "引言：Attention的天花板", 工程实践).  With channels = nheads * headdim (x's innermost
+ * dimensions) and K = width:
+ *   x'[b,t,c] = SiLU( bias[c] + sum_{k=0..K-1} weight[c,k] * x[b, t-K+1+k, c] )
+ * so weight[c, K-1] multiplies the current input.  x at times before 0 is x_prev (or
+ * zero).  The scan then uses x' wherever it uses x, the skip term D*x' included.
+ */
+typedef struct ssm_conv {
+    const float* weight; /* (channels, width) fp32, required                               */
+    const float* bias;   /* (channels,) fp32, or NULL for none                              */
+    const void* x_prev;  /* (batch, width-1, channels) in the input dtype: the inputs that
+                            precede this call's first token, oldest first; NULL = zeros    */
+    void* x_last;        /* (batch, width-1, channels) in the input dtype, or NULL: receives
+                            the width-1 raw inputs before the end of this call, the x_prev
+                            of a following call                                             */
+    int32_t width;       /* K, 1..4 (SSM_ERR_UNSUPPORTED otherwise)                        */
+} ssm_conv;
+
+/*
+ * Forward scan with the convolution ahead of it; otherwise as ssm_scan_fwd_state
+ * (initial_state nullable; workspace NULL/0 = stream-ordered allocation).
+ * Diagonal mode fuses the convolution into the scan kernels (x is read once).  SSD mode
+ * runs it as a separate pass into scratch that the SSD kernels then read, with x' kept in
+ * fp32 (rounding it to bf16 would exceed the scan's tolerance); the SSD kernels that read
+ * an fp32 x are the CUDA-core ones, slower than the tensor-core kernels used otherwise.
+ * Its scratch is ssm_scan_conv_workspace_size(shape).
+ * All conv pointers 16-byte aligned.  x_last must not overlap x_prev, x or out
+ * (SSM_ERR_SHAPE): thread blocks still reading them may run after it is written.
+ */
+int ssm_scan_fwd_conv(const void* x, const void* dt, const float* A, const void* B, const void* C,
+                      const float* D, const void* z, const float* dt_bias, const ssm_conv* conv,
+                      const float* initial_state, void* out, float* final_state,
+                      const ssm_shape* shape, void* workspace, size_t workspace_bytes,
+                      ssm_stream_t stream);
+
+/* Scratch bytes of ssm_scan_fwd_conv for `shape` ((size_t)-1 when the shape is invalid). */
+size_t ssm_scan_conv_workspace_size(const ssm_shape* shape);
+
+/*
+ * ssm_step with the convolution ahead of it: x' is formed from the width-1 carried inputs
+ * in conv->x_prev and this token's x, and conv->x_last (if non-NULL) receives the carried
+ * inputs shifted by one token.  x_last may be the same pointer as x_prev (the state is then
+ * updated in place) but must not otherwise overlap it, state, out or x (SSM_ERR_SHAPE).
+ */
+int ssm_step_conv(const void* x, const void* dt, const float* A, const void* B, const void* C,
+                  const float* D, const void* z, const float* dt_bias, const ssm_conv* conv,
+                  float* state, void* out, const ssm_shape* shape, ssm_stream_t stream);
+
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char* ssm_strerror(int status);
 

@@ -12,7 +12,7 @@ import ctypes
 import torch
 
 from . import _lib
-from ._lib import SsmError, ssm_shape
+from ._lib import SsmError, ssm_conv, ssm_shape
 
 __all__ = ["scan_fwd", "step", "workspace_size", "make_shape", "launch_count", "SsmError",
            "ssm_shape"]
@@ -82,9 +82,27 @@ def workspace_size(x, A, B, chunk: int = 0) -> int:
     return int(n)
 
 
+def _conv_struct(name, weight, bias, x_prev, x_last, x, b, ch, dev):
+    """Check the convolution tensors and build the ``ssm_conv`` descriptor."""
+    if weight.dim() != 2 or weight.shape[0] != ch:
+        raise ValueError(f"{name}: conv_weight must be ({ch}, width)")
+    K = int(weight.shape[1])
+    _check("conv_weight", weight, (ch, K), torch.float32, dev)
+    _check("conv_bias", bias, (ch,), torch.float32, dev)
+    _check("conv_x_prev", x_prev, (b, K - 1, ch), x.dtype, dev)
+    _check("conv_x_last", x_last, (b, K - 1, ch), x.dtype, dev)
+    c = ssm_conv()
+    c.weight, c.bias = weight.data_ptr(), None if bias is None else bias.data_ptr()
+    c.x_prev = None if x_prev is None else x_prev.data_ptr()
+    c.x_last = None if x_last is None else x_last.data_ptr()
+    c.width = K
+    return c
+
+
 def scan_fwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, *, out=None, final_state=None,
              return_final_state: bool = False, chunk: int = 0, workspace=None, stream=None,
-             initial_state=None):
+             initial_state=None, conv_weight=None, conv_bias=None, conv_x_prev=None,
+             conv_x_last=None):
     """Selective scan forward on the GPU.
 
     out_t = (C_t . h_t + D x_t) * SiLU(z_t),  h_t = exp(Delta_t A) h_{t-1} + Delta_t B_t x_t,
@@ -97,6 +115,11 @@ def scan_fwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, *, out=None, final_st
     ``workspace_size`` bytes; otherwise the library draws scratch from the stream-ordered
     allocator.  ``initial_state``: optional float32 state entering t = 0 (the layout of
     ``final_state``; must not share memory with it), for resuming a split sequence.
+
+    ``conv_weight`` (channels, width) float32 puts the causal depthwise convolution + SiLU
+    ahead of the scan (channels = d_inner, or nheads*headdim); ``conv_bias`` (channels,),
+    ``conv_x_prev`` (b, width-1, channels) the inputs before t = 0, and ``conv_x_last``
+    a tensor of that shape to receive this call's last inputs.
     """
     s = make_shape(x, A, B, chunk)
     dev = x.device
@@ -128,8 +151,15 @@ def scan_fwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, *, out=None, final_st
     with torch.cuda.device(dev):
         if workspace is not None and workspace.device != dev:
             raise ValueError("workspace must be on x's device")
-        if initial_state is not None:
-            ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        if conv_weight is not None:
+            cv = _conv_struct("scan_fwd", conv_weight, conv_bias, conv_x_prev, conv_x_last, x,
+                              b, H * P, dev)
+            rc = lib.ssm_scan_fwd_conv(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                       _ptr(z), _ptr(dt_bias), ctypes.byref(cv),
+                                       _ptr(initial_state), _ptr(out), _ptr(final_state),
+                                       ctypes.byref(s), _ptr(workspace), ws_bytes, handle)
+        elif initial_state is not None:
             rc = lib.ssm_scan_fwd_state(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
                                         _ptr(z), _ptr(dt_bias), _ptr(initial_state), _ptr(out),
                                         _ptr(final_state), ctypes.byref(s), _ptr(workspace),
@@ -148,8 +178,13 @@ def scan_fwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, *, out=None, final_st
     return (out, final_state) if want_state else out
 
 
-def step(x, dt, A, B, C, D=None, z=None, dt_bias=None, *, state, out=None, stream=None):
+def step(x, dt, A, B, C, D=None, z=None, dt_bias=None, *, state, out=None, stream=None,
+         conv_weight=None, conv_bias=None, conv_state=None):
     """One token of recurrent decoding; ``state`` (float32) is updated in place.
+
+    With ``conv_weight`` (channels, width) the convolution + SiLU runs ahead of the scan;
+    ``conv_state`` (b, width-1, channels) in x's dtype holds the previous inputs and is
+    shifted in place (None: zeros, nothing kept).
 
     DIAG: x, z (b, D), dt (b, D), A (D, N), B, C (b, N) or (b, G, N), state (b, D, N).
     SSD: x, z (b, H, P), dt (b, H), A (H,), B, C (b, N) or (b, G, N), state (b, H, P, N).
@@ -200,9 +235,17 @@ def step(x, dt, A, B, C, D=None, z=None, dt_bias=None, *, state, out=None, strea
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     with torch.cuda.device(dev):
-        rc = _lib.load().ssm_step(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
-                                  _ptr(dt_bias), _ptr(state), _ptr(out), ctypes.byref(s),
-                                  ctypes.c_void_p(stream.cuda_stream))
+        if conv_weight is not None:
+            cv = _conv_struct("step", conv_weight, conv_bias, conv_state, conv_state, x, b, H * P,
+                              dev)
+            rc = _lib.load().ssm_step_conv(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                           _ptr(z), _ptr(dt_bias), ctypes.byref(cv), _ptr(state),
+                                           _ptr(out), ctypes.byref(s),
+                                           ctypes.c_void_p(stream.cuda_stream))
+        else:
+            rc = _lib.load().ssm_step(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                      _ptr(z), _ptr(dt_bias), _ptr(state), _ptr(out),
+                                      ctypes.byref(s), ctypes.c_void_p(stream.cuda_stream))
     if rc != _lib.SSM_OK:
         raise SsmError(rc, "ssm_step")
     return out

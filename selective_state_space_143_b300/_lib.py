@@ -28,8 +28,8 @@ SSM_BF16 = 1
 
 # Every function declared in include/ssm_scan.h.
 EXPORTED = ("ssm_scan_fwd", "ssm_scan_fwd_ws", "ssm_scan_workspace_size", "ssm_scan_fwd_noalloc",
-            "ssm_scan_fwd_state", "ssm_step", "ssm_strerror", "ssm_kernel_launch_count",
-            "ssm_abi_version")
+            "ssm_scan_fwd_state", "ssm_step", "ssm_scan_fwd_conv", "ssm_scan_conv_workspace_size",
+            "ssm_step_conv", "ssm_strerror", "ssm_kernel_launch_count", "ssm_abi_version")
 
 
 class ssm_shape(ctypes.Structure):
@@ -37,6 +37,12 @@ class ssm_shape(ctypes.Structure):
                 ("seqlen", ctypes.c_int64), ("nheads", ctypes.c_int64), ("headdim", ctypes.c_int64),
                 ("dstate", ctypes.c_int64), ("ngroups", ctypes.c_int64), ("chunk", ctypes.c_int64),
                 ("flags", ctypes.c_uint32)]
+
+
+class ssm_conv(ctypes.Structure):
+    _fields_ = [("weight", ctypes.c_void_p), ("bias", ctypes.c_void_p),
+                ("x_prev", ctypes.c_void_p), ("x_last", ctypes.c_void_p),
+                ("width", ctypes.c_int32)]
 
 
 class SsmError(RuntimeError):
@@ -85,6 +91,14 @@ def load() -> ctypes.CDLL:
         lib.ssm_scan_fwd_state.restype = ctypes.c_int
         lib.ssm_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sp, vp]
         lib.ssm_step.restype = ctypes.c_int
+        cp = ctypes.POINTER(ssm_conv)
+        lib.ssm_scan_fwd_conv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, cp, vp, vp, vp, sp, vp,
+                                          ctypes.c_size_t, vp]
+        lib.ssm_scan_fwd_conv.restype = ctypes.c_int
+        lib.ssm_scan_conv_workspace_size.argtypes = [sp]
+        lib.ssm_scan_conv_workspace_size.restype = ctypes.c_size_t
+        lib.ssm_step_conv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, cp, vp, vp, sp, vp]
+        lib.ssm_step_conv.restype = ctypes.c_int
         lib.ssm_scan_workspace_size.argtypes = [sp]
         lib.ssm_scan_workspace_size.restype = ctypes.c_size_t
         lib.ssm_strerror.argtypes = [ctypes.c_int]

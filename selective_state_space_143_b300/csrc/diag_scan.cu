@@ -47,9 +47,11 @@ namespace {
 constexpr int kTT = 16;      // time steps per tile
 constexpr int kStages = 4;   // cp.async ring: tiles k-1 (epilogue), k+1 (prep), k+2, k+3 (loads)
 constexpr int kRB = 4;       // rows whose decays are formed together
+constexpr int kConvHalo = 3; // inputs before a tile that the width-4 convolution reads
 
-// LPC lanes per channel, WARPS warps per block.
-template <typename T, int NK, int LPC, int WARPS>
+// LPC lanes per channel, WARPS warps per block; CONV adds the convolved-input ring and
+// the halo of inputs before the segment.
+template <typename T, int NK, int LPC, int WARPS, bool CONV = false>
 struct DiagCfg {
     static constexpr int NT = 32 * WARPS;       // threads per block
     static constexpr int CPB = NT / LPC;        // channels per block
@@ -66,8 +68,12 @@ struct DiagCfg {
     static constexpr int kBfFloats = kTT * NK;         // fp32 B (and C) of one tile
     static constexpr int kDuFloat2 = kTT * CPB;        // (Delta, Delta*x) of one tile
     static constexpr int kYsFloats = kTT * CPB * LPC;  // partial C.h of one tile
-    // two buffers (tile parity) of each derived array
-    static constexpr int kSmemBytes = kStages * kStageBytes + 2 * (2 * kBfFloats * 4 + kDuFloat2 * 8 + kYsFloats * 4);
+    static constexpr int kXsFloats = kTT * CPB;        // convolved x of one tile
+    static constexpr int kHaloFloats = kConvHalo * CPB;  // inputs before the segment
+    // two buffers (tile parity) of each derived array; three for the convolved x, which
+    // is written two tiles ahead of the epilogue that reads it
+    static constexpr int kSmemBytes = kStages * kStageBytes + 2 * (2 * kBfFloats * 4 + kDuFloat2 * 8 + kYsFloats * 4) +
+                                      (CONV ? (3 * kXsFloats + kHaloFloats) * 4 : 0);
     static constexpr int RS = NT / P2;                 // rows per sweep of the pair roles
     static constexpr int kPairItems = kTT / RS;        // pair items per thread per tile
     static constexpr int kBCItems = kTT * NK / 2 / NT; // B/C pair conversions per thread per tile
@@ -88,6 +94,11 @@ struct DiagKernelArgs {
     const float* D;
     const float* dt_bias;
     const float* init;   // initial state (b, dim, N) or null
+    const float* conv_w; // (dim, conv_k) depthwise convolution ahead of the scan, or null
+    const float* conv_b; // (dim,) or null
+    const char* x_prev;  // (b, conv_k-1, dim) inputs before t = 0, or null (zeros)
+    char* x_last;        // (b, conv_k-1, dim) receives the last conv_k-1 inputs, or null
+    int conv_k;          // convolution width 1..4 (CONV kernels only)
     char* out;
     float* final_state;  // (b, dim, N) or null
     float* seg_h;        // (nseg-1, b, dim, N): local end state of each segment but the last
@@ -156,9 +167,15 @@ __device__ __forceinline__ float2 silu_pair(float2 z) {
 //   finish(k-1):  the LPC partial sums of tile k-1 per channel pair, D*x, SiLU gate, store.
 // Interleaving the per-(t, c) work (SFU-latency chains) with the scan keeps the SFU and
 // FMA pipes busy at the low occupancy these channel counts give.
-template <typename T, int NK, int LPC, int WARPS, bool STATE_ONLY, bool GATE>
+//
+// CONV: x is first replaced by x' = SiLU(conv_b + sum_k conv_w[k] x_{t-K+1+k}) (causal
+// depthwise convolution, "论文解读：Mamba — 线性时间的序列建模革命", 五 Mamba块架构),
+// formed in prep from the staged rows of this tile and the three rows before it (the
+// previous tile's stage, or a halo loaded once per segment); the epilogue reads x' for
+// the skip term from a ring of three tile buffers.
+template <typename T, int NK, int LPC, int WARPS, bool STATE_ONLY, bool GATE, bool CONV>
 __global__ void __launch_bounds__(32 * WARPS) diag_scan_kernel(const DiagKernelArgs a) {
-    using Cfg = DiagCfg<T, NK, LPC, WARPS>;
+    using Cfg = DiagCfg<T, NK, LPC, WARPS, CONV>;
     constexpr int NT = Cfg::NT, CPB = Cfg::CPB, NPT = Cfg::NPT, P2 = Cfg::P2, E = Cfg::kElem;
     constexpr int RS = Cfg::RS;
     constexpr bool PRECISE = sizeof(T) == 4;
@@ -168,6 +185,8 @@ __global__ void __launch_bounds__(32 * WARPS) diag_scan_kernel(const DiagKernelA
     float* Cf0 = Bf0 + 2 * Cfg::kBfFloats;                                   // [2][kBfFloats]
     float2* du0 = reinterpret_cast<float2*>(Cf0 + 2 * Cfg::kBfFloats);        // [2][kDuFloat2]
     float* ys0 = reinterpret_cast<float*>(du0 + 2 * Cfg::kDuFloat2);          // [2][kYsFloats]
+    float* xs0 = ys0 + 2 * Cfg::kYsFloats;                                    // [3][kXsFloats] (CONV)
+    float* halo = xs0 + 3 * Cfg::kXsFloats;                                   // [3][CPB] (CONV)
 
     const int tid = threadIdx.x;
     const int group = blockIdx.x / a.tiles_per_group;
@@ -194,6 +213,18 @@ __global__ void __launch_bounds__(32 * WARPS) diag_scan_kernel(const DiagKernelA
                                                 : make_float2(0.0f, 0.0f);
     const float2 d2 = (pair_ok && a.D) ? make_float2(a.D[cA], a.D[cA + 1]) : make_float2(0.0f, 0.0f);
     float2 dsum2 = make_float2(0.0f, 0.0f);  // sum of Delta (state-only pass)
+    // convolution taps of the pair, left-padded to width 4 (tap 3 weights the current row)
+    float2 cw[4];
+    float2 cb2 = make_float2(0.0f, 0.0f);
+    if (CONV) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int kk = k - (4 - a.conv_k);
+            cw[k] = (pair_ok && kk >= 0) ? make_float2(a.conv_w[cA * a.conv_k + kk], a.conv_w[(cA + 1) * a.conv_k + kk])
+                                         : make_float2(0.0f, 0.0f);
+        }
+        if (pair_ok && a.conv_b) cb2 = make_float2(a.conv_b[cA], a.conv_b[cA + 1]);
+    }
 
     // state entries and decay rates (times log2 e) in fp32 pairs, as the packed
     // fp32x2 instructions take them
@@ -265,13 +296,28 @@ __global__ void __launch_bounds__(32 * WARPS) diag_scan_kernel(const DiagKernelA
         cp_async_commit();
     };
 
+    // input pair of row rr of tile k, rr in [-3, kTT): rows before the tile come from the
+    // previous tile's stage or, for the segment's first tile, from the halo
+    auto x_row = [&](int k, int rr) -> float2 {
+        if (rr >= 0) return load_pair<T>(stage(k) + rr * Cfg::kRowBytes + 2 * pp * E);
+        if (k > 0) return load_pair<T>(stage(k - 1) + (kTT + rr) * Cfg::kRowBytes + 2 * pp * E);
+        return *reinterpret_cast<const float2*>(&halo[(kConvHalo + rr) * CPB + 2 * pp]);
+    };
+
     // prep item it (0..kPairItems-1) of tile k: one (row, channel pair)
     auto prep_item = [&](int k, int it) {
         const unsigned char* st = stage(k);
         float2* du = du0 + (k & 1) * Cfg::kDuFloat2;
         const int r = r0 + it * RS;
         const float2 dtv = load_pair<T>(st + Cfg::kXBytes + r * Cfg::kRowBytes + 2 * pp * E);
-        const float2 xv = load_pair<T>(st + r * Cfg::kRowBytes + 2 * pp * E);
+        float2 xv = load_pair<T>(st + r * Cfg::kRowBytes + 2 * pp * E);
+        if (CONV) {
+            float2 acc = __ffma2_rn(cw[3], xv, cb2);
+#pragma unroll
+            for (int j = 1; j <= kConvHalo; ++j) acc = __ffma2_rn(cw[3 - j], x_row(k, r - j), acc);
+            xv = silu_pair<PRECISE>(acc);
+            if (!STATE_ONLY) *reinterpret_cast<float2*>(&xs0[(k % 3) * Cfg::kXsFloats + r * CPB + 2 * pp]) = xv;
+        }
         float2 de = softplus_pair<PRECISE>(__fadd2_rn(dtv, bias2));
         if (r >= tile_rows(k)) de = make_float2(0.0f, 0.0f);  // no-op rows: Delta = 0 keeps h
         const float2 u = __fmul2_rn(de, xv);
@@ -306,7 +352,8 @@ __global__ void __launch_bounds__(32 * WARPS) diag_scan_kernel(const DiagKernelA
                 y = __fadd2_rn(y, make_float2(p0.x + p0.y, p1.x + p1.y));
             }
         }
-        const float2 xv = load_pair<T>(st + r * Cfg::kRowBytes + 2 * pp * E);
+        const float2 xv = CONV ? *reinterpret_cast<const float2*>(&xs0[(k % 3) * Cfg::kXsFloats + r * CPB + 2 * pp])
+                               : load_pair<T>(st + r * Cfg::kRowBytes + 2 * pp * E);
         y = __ffma2_rn(d2, xv, y);
         if (GATE) y = __fmul2_rn(y, silu_pair<PRECISE>(load_pair<T>(st + 2 * Cfg::kXBytes + r * Cfg::kRowBytes + 2 * pp * E)));
         const int64_t t = t_begin + (int64_t)k * kTT + r;
@@ -317,6 +364,25 @@ __global__ void __launch_bounds__(32 * WARPS) diag_scan_kernel(const DiagKernelA
     issue_tile(0);
     issue_tile(1);
     issue_tile(2);
+    if (CONV) {
+        // the three inputs before the segment: earlier rows of x, else the previous
+        // call's last inputs, else zero
+        const T* xg = reinterpret_cast<const T*>(a.x);
+        const T* xp = reinterpret_cast<const T*>(a.x_prev);
+        for (int i = tid; i < kConvHalo * CPB; i += NT) {
+            const int j = i / CPB, cch = i % CPB;
+            const int64_t ch = c_begin + cch;
+            const int64_t s = t_begin - kConvHalo + j;
+            float v = 0.0f;
+            if (ch < c_end) {
+                if (s >= 0)
+                    v = to_f32<T>(xg[(b * a.T + s) * a.dim + ch]);
+                else if (xp && a.conv_k - 1 + s >= 0)
+                    v = to_f32<T>(xp[(b * (a.conv_k - 1) + (a.conv_k - 1 + s)) * a.dim + ch]);
+            }
+            halo[j * CPB + cch] = v;
+        }
+    }
     if (ntiles > 0) {
         cp_async_wait<2>();
         __syncthreads();
@@ -421,7 +487,27 @@ __global__ void __launch_bounds__(32 * WARPS) diag_scan_kernel(const DiagKernelA
                 dst[1] = s.y;
             }
         }
-    } else if (a.final_state && seg == a.nseg - 1 && c_ok) {
+    }
+    if (CONV && !STATE_ONLY && a.x_last && seg == a.nseg - 1) {
+        // the last conv_k-1 inputs (raw) for a following call
+        const T* xg = reinterpret_cast<const T*>(a.x);
+        const T* xp = reinterpret_cast<const T*>(a.x_prev);
+        T* xl = reinterpret_cast<T*>(a.x_last);
+        const int km1 = a.conv_k - 1;
+        for (int i = tid; i < km1 * CPB; i += NT) {
+            const int j = i / CPB, cch = i % CPB;
+            const int64_t ch = c_begin + cch;
+            if (ch >= c_end) continue;
+            const int64_t s = a.T - km1 + j;
+            T v = from_f32<T>(0.0f);
+            if (s >= 0)
+                v = xg[(b * a.T + s) * a.dim + ch];
+            else if (xp)
+                v = xp[(b * km1 + (km1 + s)) * a.dim + ch];
+            xl[(b * km1 + j) * a.dim + ch] = v;
+        }
+    }
+    if (!STATE_ONLY && a.final_state && seg == a.nseg - 1 && c_ok) {
         float* fs = a.final_state + (b * a.dim + c) * a.N;
 #pragma unroll
         for (int k = 0; k < NPT / 2; ++k) {
@@ -497,11 +583,11 @@ Plan make_plan(const ScanArgs& a) {
     return p;
 }
 
-template <typename T, int NK, int LPC, bool STATE_ONLY, bool GATE>
+template <typename T, int NK, int LPC, bool STATE_ONLY, bool GATE, bool CONV>
 cudaError_t launch_one(const DiagKernelArgs& ka, dim3 grid, cudaStream_t stream) {
     constexpr int WARPS = (LPC == 1 ? 32 : 16) * LPC / 32;
-    using Cfg = DiagCfg<T, NK, LPC, WARPS>;
-    auto kern = diag_scan_kernel<T, NK, LPC, WARPS, STATE_ONLY, GATE>;
+    using Cfg = DiagCfg<T, NK, LPC, WARPS, CONV>;
+    auto kern = diag_scan_kernel<T, NK, LPC, WARPS, STATE_ONLY, GATE, CONV>;
     // the shared-memory attribute is set once per instantiation and device
     static std::atomic<uint64_t> attr_done{0};
     int dev = 0;
@@ -518,7 +604,7 @@ cudaError_t launch_one(const DiagKernelArgs& ka, dim3 grid, cudaStream_t stream)
     return cudaGetLastError();
 }
 
-template <typename T, int NK, int LPC>
+template <typename T, int NK, int LPC, bool CONV>
 cudaError_t launch_typed(const ScanArgs& a, const Plan& p, void* ws, cudaStream_t stream) {
     DiagKernelArgs ka;
     ka.x = (const char*)a.x;
@@ -530,6 +616,11 @@ cudaError_t launch_typed(const ScanArgs& a, const Plan& p, void* ws, cudaStream_
     ka.D = a.D;
     ka.dt_bias = a.dt_bias;
     ka.init = a.initial_state;
+    ka.conv_w = a.conv_w;
+    ka.conv_b = a.conv_b;
+    ka.x_prev = (const char*)a.x_prev;
+    ka.x_last = (char*)a.x_last;
+    ka.conv_k = a.conv_k;
     ka.out = (char*)a.out;
     ka.final_state = a.final_state;
     ka.T = a.seqlen;
@@ -547,22 +638,28 @@ cudaError_t launch_typed(const ScanArgs& a, const Plan& p, void* ws, cudaStream_
         ka.seg_h = (float*)ws;
         ka.seg_dsum = (float*)((char*)ws + align_up(hbytes, 256));
         const dim3 g1(p.blocks_x, p.nseg - 1, (unsigned)a.batch);
-        cudaError_t e = launch_one<T, NK, LPC, true, false>(ka, g1, stream);
+        cudaError_t e = CONV ? launch_one<T, NK, LPC, true, false, true>(ka, g1, stream)
+                             : launch_one<T, NK, LPC, true, false, false>(ka, g1, stream);
         if (e != cudaSuccess) return e;
     }
     const dim3 g2(p.blocks_x, p.nseg, (unsigned)a.batch);
-    if (a.z) return launch_one<T, NK, LPC, false, true>(ka, g2, stream);
-    return launch_one<T, NK, LPC, false, false>(ka, g2, stream);
+    if (a.z) return launch_one<T, NK, LPC, false, true, CONV>(ka, g2, stream);
+    return launch_one<T, NK, LPC, false, false, CONV>(ka, g2, stream);
+}
+
+template <typename T, bool CONV>
+cudaError_t launch_conv(const ScanArgs& a, const Plan& p, void* ws, cudaStream_t stream) {
+    switch (p.NK) {
+        case 8: return p.LPC == 1 ? launch_typed<T, 8, 1, CONV>(a, p, ws, stream) : launch_typed<T, 8, 2, CONV>(a, p, ws, stream);
+        case 16: return p.LPC == 2 ? launch_typed<T, 16, 2, CONV>(a, p, ws, stream) : launch_typed<T, 16, 4, CONV>(a, p, ws, stream);
+        case 32: return p.LPC == 4 ? launch_typed<T, 32, 4, CONV>(a, p, ws, stream) : launch_typed<T, 32, 8, CONV>(a, p, ws, stream);
+        default: return launch_typed<T, 64, 8, CONV>(a, p, ws, stream);
+    }
 }
 
 template <typename T>
 cudaError_t launch_dtype(const ScanArgs& a, const Plan& p, void* ws, cudaStream_t stream) {
-    switch (p.NK) {
-        case 8: return p.LPC == 1 ? launch_typed<T, 8, 1>(a, p, ws, stream) : launch_typed<T, 8, 2>(a, p, ws, stream);
-        case 16: return p.LPC == 2 ? launch_typed<T, 16, 2>(a, p, ws, stream) : launch_typed<T, 16, 4>(a, p, ws, stream);
-        case 32: return p.LPC == 4 ? launch_typed<T, 32, 4>(a, p, ws, stream) : launch_typed<T, 32, 8>(a, p, ws, stream);
-        default: return launch_typed<T, 64, 8>(a, p, ws, stream);
-    }
+    return a.conv_k > 0 ? launch_conv<T, true>(a, p, ws, stream) : launch_conv<T, false>(a, p, ws, stream);
 }
 
 }  // namespace

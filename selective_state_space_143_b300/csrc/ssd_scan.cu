@@ -49,11 +49,18 @@ struct SsdArgs {
     float* cum;     // (b, H, nchunks, Q) inclusive cumsum of Delta*A_h within the chunk
     float* states;  // (b, nchunks, H, P, N)
     int64_t T, H, P, N, G, Q, nchunks;
+    int x_f32;      // x is stored as fp32 whatever the dtype (the convolved input)
 };
 
 template <typename T>
 __device__ __forceinline__ float ld(const char* base, int64_t idx) {
     return to_f32<T>(reinterpret_cast<const T*>(base)[idx]);
+}
+
+// an element of x, which is fp32 when it holds the convolved input
+template <typename T>
+__device__ __forceinline__ float ld_x(const SsdArgs& a, int64_t idx) {
+    return a.x_f32 ? reinterpret_cast<const float*>(a.x)[idx] : ld<T>(a.x, idx);
 }
 
 // e^x: CUDA's accurate expf for fp32 inputs, the fast intrinsic for 16-bit inputs.
@@ -133,7 +140,7 @@ __global__ void __launch_bounds__(kThreads) ssd_chunk_state(const SsdArgs a) {
             const int64_t t = t0 + s0 + r;
             const int64_t p = (int64_t)pt * kTile + q, n = (int64_t)nt * kTile + q;
             const bool rok = s0 + r < len;
-            s_x[r][q] = (rok && p < a.P) ? ld<T>(a.x, ((b * a.T + t) * a.H + h) * a.P + p) : 0.0f;
+            s_x[r][q] = (rok && p < a.P) ? ld_x<T>(a, ((b * a.T + t) * a.H + h) * a.P + p) : 0.0f;
             s_b[r][q] = (rok && n < a.N) ? ld<T>(a.B, ((b * a.T + t) * a.G + g) * a.N + n) : 0.0f;
         }
         if (tid < kSub) {
@@ -253,7 +260,7 @@ __global__ void __launch_bounds__(kThreads) ssd_chunk_scan(const SsdArgs a) {
         for (int i = tid; i < kSub * kTile; i += kThreads) {
             const int r = i / kTile, q = i % kTile;
             const int64_t p = (int64_t)pt * kTile + q;
-            s_x[r * (kTile + 1) + q] = (s0 + r < len && p < a.P) ? ld<T>(a.x, ((b * a.T + t0 + s0 + r) * a.H + h) * a.P + p) : 0.0f;
+            s_x[r * (kTile + 1) + q] = (s0 + r < len && p < a.P) ? ld_x<T>(a, ((b * a.T + t0 + s0 + r) * a.H + h) * a.P + p) : 0.0f;
         }
         __syncthreads();
         // G'[t][s] = (s <= t) (C_t . B_s) exp(cum_t - cum_s) Delta_s for the 64 x 32 block
@@ -319,7 +326,7 @@ __global__ void __launch_bounds__(kThreads) ssd_chunk_scan(const SsdArgs a) {
         for (int j = 0; j < 4; ++j) {
             const int64_t p = (int64_t)pt * kTile + pj + j;
             if (p >= a.P) continue;
-            const float xv = ld<T>(a.x, row + p);
+            const float xv = ld_x<T>(a, row + p);
             float y = acc[i][j] + e * off[i][j] + Dh * xv;
             if (GATE) y *= silu_t<sizeof(T) == 4>(ld<T>(a.z, row + p));
             reinterpret_cast<T*>(a.out)[row + p] = from_f32<T>(y);
@@ -381,10 +388,13 @@ cudaError_t ssd_launch_typed(const ScanArgs& a, void* ws, cudaStream_t stream) {
     s.G = a.ngroups;
     s.Q = pl.Q;
     s.nchunks = pl.nchunks;
+    s.x_f32 = a.x_f32;
     const unsigned nP = (unsigned)((a.headdim + kTile - 1) / kTile);
     const unsigned nN = (unsigned)((a.dstate + kTile - 1) / kTile);
     const unsigned nTq = (unsigned)((pl.Q + kTile - 1) / kTile);
-    if (pl.nchunks > 0 && ssd_tc_supported(a, pl.Q) && !force_cuda_cores()) {
+    // The tensor-core kernels take x as an exact bf16 MMA operand; an fp32 x (the
+    // convolved input) runs on the CUDA-core kernels.
+    if (pl.nchunks > 0 && !a.x_f32 && ssd_tc_supported(a, pl.Q) && !force_cuda_cores()) {
         SsdTcArgs t;
         t.x = (const __nv_bfloat16*)a.x;
         t.dt = (const __nv_bfloat16*)a.dt;

@@ -94,6 +94,12 @@ ScanArgs make_args(const void* x, const void* dt, const float* A, const void* B,
     a.z = z;
     a.dt_bias = dt_bias;
     a.initial_state = nullptr;
+    a.conv_w = nullptr;
+    a.conv_b = nullptr;
+    a.x_prev = nullptr;
+    a.x_last = nullptr;
+    a.conv_k = 0;
+    a.x_f32 = 0;
     a.out = out;
     a.final_state = final_state;
     a.batch = s->batch;
@@ -107,14 +113,62 @@ ScanArgs make_args(const void* x, const void* dt, const float* A, const void* B,
     return a;
 }
 
+// Bytes of the convolved input the SSD path keeps in scratch (the diagonal path fuses
+// the convolution and needs none).
+size_t conv_buffer_bytes(const ScanArgs& a, int mode) {
+    if (a.conv_k == 0 || mode != SSM_MODE_SSD || a.batch == 0) return 0;
+    return align_up((size_t)a.batch * a.seqlen * a.nheads * a.headdim * sizeof(float), 256);
+}
+
 size_t workspace_for(const ScanArgs& a, int mode) {
-    return mode == SSM_MODE_DIAG ? diag_workspace_bytes(a) : ssd_workspace_bytes(a);
+    const size_t base = mode == SSM_MODE_DIAG ? diag_workspace_bytes(a) : ssd_workspace_bytes(a);
+    const size_t conv = conv_buffer_bytes(a, mode);
+    return conv ? align_up(base, 256) + conv : base;
 }
 
 int run(const ScanArgs& a, int mode, void* ws, cudaStream_t stream) {
     if (a.batch == 0) return SSM_OK;
-    const cudaError_t e = mode == SSM_MODE_DIAG ? diag_launch(a, ws, stream) : ssd_launch(a, ws, stream);
+    cudaError_t e;
+    if (mode == SSM_MODE_DIAG) {
+        e = diag_launch(a, ws, stream);
+    } else if (a.conv_k > 0) {
+        // convolution pass into scratch, then the SSD kernels on the convolved input
+        void* xc = (char*)ws + align_up(ssd_workspace_bytes(a), 256);
+        e = conv_prepass_launch(a, xc, stream);
+        if (e == cudaSuccess) {
+            ScanArgs b = a;
+            b.x = xc;
+            b.x_f32 = 1;
+            b.conv_k = 0;
+            e = ssd_launch(b, ws, stream);
+        }
+        if (e == cudaSuccess) e = conv_tail_launch(a, stream);
+    } else {
+        e = ssd_launch(a, ws, stream);
+    }
     return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+int check_conv(const ssm_conv* cv) {
+    if (!cv || !cv->weight) return SSM_ERR_NULL;
+    if (cv->width < 1 || cv->width > 4) return SSM_ERR_UNSUPPORTED;
+    const void* ptrs[] = {cv->weight, cv->bias, cv->x_prev, cv->x_last};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return SSM_ERR_ALIGN;
+    return SSM_OK;
+}
+
+void set_conv(ScanArgs& a, const ssm_conv* cv) {
+    a.conv_w = cv->weight;
+    a.conv_b = cv->bias;
+    a.x_prev = cv->x_prev;
+    a.x_last = cv->x_last;
+    a.conv_k = cv->width;
+}
+
+// Bytes of one convolution state (batch, width-1, channels) in the input dtype.
+size_t conv_state_bytes(const ssm_shape* s, int width) {
+    return (size_t)s->batch * (width - 1) * s->nheads * s->headdim * elem_size(s->dtype);
 }
 
 // Caller-provided scratch.
@@ -140,6 +194,37 @@ int run_allocating(const ScanArgs& a, int mode, cudaStream_t st) {
         if (cudaFreeAsync(ws, st) != cudaSuccess && r == SSM_OK) return SSM_ERR_CUDA;
     }
     return r;
+}
+
+int step_common(const void* x, const void* dt, const float* A, const void* B, const void* C,
+                const float* D, const void* z, const float* dt_bias, const ssm_conv* conv,
+                float* state, void* out, const ssm_shape* shape, cudaStream_t stream) {
+    const int rc = check_shape(shape);
+    if (rc != SSM_OK) return rc;
+    if (shape->seqlen != 1) return SSM_ERR_SHAPE;
+    if (shape->dstate % 4 != 0) return SSM_ERR_ALIGN;  // state rows move in 16-byte pieces
+    if (shape->batch * shape->nheads * shape->headdim > (int64_t(1) << 36)) return SSM_ERR_UNSUPPORTED;
+    if (!A || (shape->batch > 0 && (!x || !dt || !B || !C || !out || !state))) return SSM_ERR_NULL;
+    const void* ptrs[] = {x, dt, A, B, C, D, z, dt_bias, out, state};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return SSM_ERR_ALIGN;
+    const size_t out_bytes = (size_t)shape->batch * shape->nheads * shape->headdim * elem_size(shape->dtype);
+    const size_t sb = state_bytes(shape);
+    if (overlaps(state, sb, out, out_bytes)) return SSM_ERR_SHAPE;
+    ScanArgs a = make_args(x, dt, A, B, C, D, z, dt_bias, out, nullptr, shape);
+    if (conv) {
+        // the convolution state may be updated in place (x_last == x_prev), but must not
+        // overlap anything else the step writes or reads
+        const size_t cb = conv_state_bytes(shape, conv->width);
+        if ((conv->x_last != conv->x_prev && overlaps(conv->x_last, cb, conv->x_prev, cb)) ||
+            overlaps(conv->x_last, cb, state, sb) || overlaps(conv->x_last, cb, out, out_bytes) ||
+            overlaps(conv->x_last, cb, x, out_bytes))
+            return SSM_ERR_SHAPE;
+        set_conv(a, conv);
+    }
+    if (shape->batch == 0) return SSM_OK;
+    const cudaError_t e = step_launch(a, shape->mode == SSM_MODE_DIAG, state, stream);
+    return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
 }  // namespace
@@ -209,24 +294,49 @@ int ssm_scan_fwd_state(const void* x, const void* dt, const float* A, const void
     return run_with(a, shape->mode, workspace, workspace_bytes, (cudaStream_t)stream);
 }
 
+size_t ssm_scan_conv_workspace_size(const ssm_shape* shape) {
+    if (check_shape(shape) != SSM_OK) return (size_t)-1;
+    ScanArgs a = make_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                           nullptr, nullptr, shape);
+    a.conv_k = 4;  // any width: the scratch does not depend on it
+    return workspace_for(a, shape->mode);
+}
+
+int ssm_scan_fwd_conv(const void* x, const void* dt, const float* A, const void* B, const void* C,
+                      const float* D, const void* z, const float* dt_bias, const ssm_conv* conv,
+                      const float* initial_state, void* out, float* final_state,
+                      const ssm_shape* shape, void* workspace, size_t workspace_bytes,
+                      ssm_stream_t stream) {
+    int rc = check_args(x, dt, A, B, C, D, z, dt_bias, out, final_state, shape, initial_state);
+    if (rc != SSM_OK) return rc;
+    rc = check_conv(conv);
+    if (rc != SSM_OK) return rc;
+    const size_t sb = state_bytes(shape);
+    const size_t cb = conv_state_bytes(shape, conv->width);
+    const size_t xb = (size_t)shape->batch * shape->seqlen * shape->nheads * shape->headdim * elem_size(shape->dtype);
+    // x_last is written while other thread blocks may still read x, x_prev or out
+    if (overlaps(initial_state, sb, final_state, sb) || overlaps(conv->x_last, cb, conv->x_prev, cb) ||
+        overlaps(conv->x_last, cb, x, xb) || overlaps(conv->x_last, cb, out, xb))
+        return SSM_ERR_SHAPE;
+    ScanArgs a = make_args(x, dt, A, B, C, D, z, dt_bias, out, final_state, shape);
+    a.initial_state = initial_state;
+    set_conv(a, conv);
+    if (workspace == nullptr && workspace_bytes == 0) return run_allocating(a, shape->mode, (cudaStream_t)stream);
+    return run_with(a, shape->mode, workspace, workspace_bytes, (cudaStream_t)stream);
+}
+
+int ssm_step_conv(const void* x, const void* dt, const float* A, const void* B, const void* C,
+                  const float* D, const void* z, const float* dt_bias, const ssm_conv* conv,
+                  float* state, void* out, const ssm_shape* shape, ssm_stream_t stream) {
+    const int rc = check_conv(conv);
+    if (rc != SSM_OK) return rc;
+    return step_common(x, dt, A, B, C, D, z, dt_bias, conv, state, out, shape, (cudaStream_t)stream);
+}
+
 int ssm_step(const void* x, const void* dt, const float* A, const void* B, const void* C,
              const float* D, const void* z, const float* dt_bias, float* state, void* out,
              const ssm_shape* shape, ssm_stream_t stream) {
-    const int rc = check_shape(shape);
-    if (rc != SSM_OK) return rc;
-    if (shape->seqlen != 1) return SSM_ERR_SHAPE;
-    if (shape->dstate % 4 != 0) return SSM_ERR_ALIGN;  // state rows move in 16-byte pieces
-    if (shape->batch * shape->nheads * shape->headdim > (int64_t(1) << 36)) return SSM_ERR_UNSUPPORTED;
-    if (!A || (shape->batch > 0 && (!x || !dt || !B || !C || !out || !state))) return SSM_ERR_NULL;
-    const void* ptrs[] = {x, dt, A, B, C, D, z, dt_bias, out, state};
-    for (const void* p : ptrs)
-        if (!aligned16(p)) return SSM_ERR_ALIGN;
-    const size_t out_bytes = (size_t)shape->batch * shape->nheads * shape->headdim * elem_size(shape->dtype);
-    if (overlaps(state, state_bytes(shape), out, out_bytes)) return SSM_ERR_SHAPE;
-    if (shape->batch == 0) return SSM_OK;
-    const ScanArgs a = make_args(x, dt, A, B, C, D, z, dt_bias, out, nullptr, shape);
-    const cudaError_t e = step_launch(a, shape->mode == SSM_MODE_DIAG, state, (cudaStream_t)stream);
-    return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+    return step_common(x, dt, A, B, C, D, z, dt_bias, nullptr, state, out, shape, (cudaStream_t)stream);
 }
 
 }  // extern "C"

@@ -18,6 +18,14 @@ struct ScanArgs {
     const void* z;
     const float* dt_bias;
     const float* initial_state;  // nullable: state entering t = 0 (zero when NULL)
+    // causal depthwise convolution + SiLU applied to x ahead of the scan (conv_k 0: none)
+    const float* conv_w;         // (channels, conv_k)
+    const float* conv_b;         // (channels,) nullable
+    const void* x_prev;          // (batch, conv_k-1, channels) nullable: inputs before t = 0
+    void* x_last;                // (batch, conv_k-1, channels) nullable: last inputs, written
+    int conv_k;
+    int x_f32;                   // x is stored as fp32 whatever dtype says (SSD after the
+                                 // convolution pass)
     void* out;
     float* final_state;
     int64_t batch, seqlen, nheads, headdim, dstate, ngroups, chunk;
@@ -38,6 +46,12 @@ cudaError_t ssd_launch(const ScanArgs& a, void* ws, cudaStream_t stream);
 // Single-token step: the state (batch, nheads, headdim, dstate) is updated in place and
 // out (batch, nheads, headdim) written; diag_a selects A of shape (nheads, dstate).
 cudaError_t step_launch(const ScanArgs& a, bool diag_a, float* state, cudaStream_t stream);
+
+// Convolution + SiLU of x into xc (same shape, fp32), and the last conv_k-1 inputs into
+// a.x_last; used ahead of the SSD kernels.  x' is kept in fp32: it is an intermediate,
+// and rounding it to bf16 would add an input error the scan's tolerance does not allow.
+cudaError_t conv_prepass_launch(const ScanArgs& a, void* xc, cudaStream_t stream);
+cudaError_t conv_tail_launch(const ScanArgs& a, cudaStream_t stream);
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 

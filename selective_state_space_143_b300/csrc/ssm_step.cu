@@ -7,6 +7,9 @@
 //   Delta = softplus(dt + dt_bias)
 //   h[n]  <- exp(Delta A[c,n]) h[n] + Delta B[n] x        (in place)
 //   out   =  (sum_n C[n] h[n] + D x) * SiLU(z)
+// With a convolution ahead of the scan ("论文解读：Mamba — 线性时间的序列建模革命", 五 Mamba块架构)
+// x is first replaced by x' = SiLU(bias + sum_k w[k] x_{t-K+1+k}), the K-1 earlier
+// inputs coming from the carried convolution state, which is then shifted by one token.
 // The step reads and writes the whole state once, so it is bound by HBM (or L2 when the
 // state fits there).  LPC lanes share one channel's state row, each lane taking 16-byte
 // pieces of it, so a warp's accesses are contiguous; the C.h partial sums are combined
@@ -33,8 +36,13 @@ struct StepArgs {
     const float* dt_bias;
     float* state;
     void* out;
+    const float* conv_w;  // (H*P, conv_k) or null
+    const float* conv_b;  // (H*P,) or null
+    const void* x_prev;   // (batch, conv_k-1, H*P) or null (zeros)
+    void* x_last;         // (batch, conv_k-1, H*P) or null; may equal x_prev
     int64_t batch, H, P, N, G;
     int diag;  // A per (channel, n) when set, one scalar per head otherwise
+    int conv_k;
 };
 
 // Four consecutive elements of a B or C row as fp32 (the row start is 8-byte aligned for
@@ -52,22 +60,36 @@ __device__ __forceinline__ float decay(float de_times_a) {
     return PRECISE ? expf(de_times_a) : ex2(de_times_a * kLog2e);
 }
 
-template <typename T, int LPC>
+template <typename T, int LPC, bool CONV>
 __global__ void __launch_bounds__(kStepThreads) ssm_step_kernel(const StepArgs a) {
     constexpr bool PRECISE = sizeof(T) == 4;
     constexpr int CPB = kStepThreads / LPC;  // channels per block
     const int lane = threadIdx.x % LPC;
     const int64_t ch = (int64_t)blockIdx.x * CPB + threadIdx.x / LPC;  // flat (b, h, p)
-    const bool ok = ch < a.batch * a.H * a.P;
-    float y = 0.0f, xv = 0.0f;
+    const int64_t nc = a.H * a.P;                                       // channels per sequence
+    const bool ok = ch < a.batch * nc;
+    float y = 0.0f, xv = 0.0f, x_raw = 0.0f;
+    float prev[3] = {0.0f, 0.0f, 0.0f};  // convolution state of the channel, oldest first
     int64_t h = 0;
     if (ok) {
-        const int64_t b = ch / (a.H * a.P);
+        const int64_t b = ch / nc;
         h = (ch / a.P) % a.H;
         const int64_t g = h / (a.H / a.G);
         const T* Bs = static_cast<const T*>(a.B) + (b * a.G + g) * a.N;
         const T* Cs = static_cast<const T*>(a.C) + (b * a.G + g) * a.N;
         xv = to_f32<T>(static_cast<const T*>(a.x)[ch]);
+        if (CONV) {
+            const int64_t c = ch % nc;
+            const int km1 = a.conv_k - 1;
+            float acc = a.conv_b ? a.conv_b[c] : 0.0f;
+            for (int j = 0; j < km1; ++j) {
+                prev[j] = a.x_prev ? to_f32<T>(static_cast<const T*>(a.x_prev)[(b * km1 + j) * nc + c]) : 0.0f;
+                acc = fmaf(a.conv_w[c * a.conv_k + j], prev[j], acc);
+            }
+            acc = fmaf(a.conv_w[c * a.conv_k + km1], xv, acc);
+            x_raw = xv;
+            xv = silu_t<PRECISE>(acc);
+        }
         const float v = to_f32<T>(static_cast<const T*>(a.dt)[b * a.H + h]) + (a.dt_bias ? a.dt_bias[h] : 0.0f);
         const float de = softplus_t<PRECISE>(v);
         const float u = de * xv;
@@ -98,7 +120,15 @@ __global__ void __launch_bounds__(kStepThreads) ssm_step_kernel(const StepArgs a
     // every lane of the warp takes part; an LPC group never straddles the ok boundary
 #pragma unroll
     for (int o = LPC / 2; o > 0; o >>= 1) y += __shfl_xor_sync(0xffffffffu, y, o, LPC);
+    if (CONV) __syncwarp();  // every lane has read the old convolution state
     if (!ok || lane != 0) return;
+    if (CONV && a.x_last) {
+        // shift the convolution state by one token (in place when x_last == x_prev)
+        const int64_t b = ch / nc, c = ch % nc;
+        const int km1 = a.conv_k - 1;
+        T* xl = static_cast<T*>(a.x_last) + b * km1 * nc + c;
+        for (int j = 0; j < km1; ++j) xl[j * nc] = from_f32<T>(j + 1 < km1 ? prev[j + 1] : x_raw);
+    }
     if (a.D) y = fmaf(a.D[h], xv, y);
     if (a.z) y *= silu_t<PRECISE>(to_f32<T>(static_cast<const T*>(a.z)[ch]));
     static_cast<T*>(a.out)[ch] = from_f32<T>(y);
@@ -108,7 +138,10 @@ template <typename T, int LPC>
 void launch_lpc(const StepArgs& s, int64_t nch, cudaStream_t stream) {
     constexpr int CPB = kStepThreads / LPC;
     const unsigned blocks = (unsigned)((nch + CPB - 1) / CPB);
-    ssm_step_kernel<T, LPC><<<blocks, kStepThreads, 0, stream>>>(s);
+    if (s.conv_k > 0)
+        ssm_step_kernel<T, LPC, true><<<blocks, kStepThreads, 0, stream>>>(s);
+    else
+        ssm_step_kernel<T, LPC, false><<<blocks, kStepThreads, 0, stream>>>(s);
 }
 
 template <typename T>
@@ -143,6 +176,11 @@ cudaError_t step_launch(const ScanArgs& a, bool diag_a, float* state, cudaStream
     s.N = a.dstate;
     s.G = a.ngroups;
     s.diag = diag_a ? 1 : 0;
+    s.conv_w = a.conv_w;
+    s.conv_b = a.conv_b;
+    s.x_prev = a.x_prev;
+    s.x_last = a.x_last;
+    s.conv_k = a.conv_k;
     const int64_t nch = a.batch * a.nheads * a.headdim;
     if (nch == 0) return cudaSuccess;
     if (a.dtype == 1)

@@ -138,3 +138,24 @@ def random_inputs(mode: str, dtype: str, batch: int, seqlen: int, nheads: int, h
     w = Workload("custom", mode, dtype, batch, seqlen, nheads, headdim if mode == "ssd" else 1,
                  dstate, ngroups=ngroups, gate=gate, dt_bias=dt_bias, d_skip=d_skip, seed=seed)
     return w, make_inputs(w)
+
+
+def conv_params(channels: int, width: int = 4, seed: int = 0, bias: bool = True,
+                batch: int = 0, dtype: str = "bf16") -> dict:
+    """Seeded parameters of the depthwise convolution ahead of the scan.
+
+    weight (channels, width) and bias (channels,) ~ U(-1/sqrt(width), 1/sqrt(width)),
+    PyTorch's default Conv1d initialisation for one input channel per group; with
+    ``batch`` > 0 also ``x_prev`` (batch, width-1, channels) ~ N(0, 1) in ``dtype``, the
+    inputs of an earlier call.  float32 CPU tensors except x_prev.
+    """
+    rng = np.random.Generator(np.random.PCG64(1000 + seed))
+    bound = 1.0 / np.sqrt(width)
+    w = rng.uniform(-bound, bound, (channels, width)).astype(np.float32)
+    b = rng.uniform(-bound, bound, channels).astype(np.float32) if bias else None
+    out = dict(weight=torch.from_numpy(w), bias=None if b is None else torch.from_numpy(b),
+               x_prev=None)
+    if batch > 0:
+        xp = rng.standard_normal((batch, width - 1, channels), dtype=np.float32)
+        out["x_prev"] = _store(xp, torch.bfloat16 if dtype == "bf16" else torch.float32)
+    return out

@@ -191,3 +191,54 @@ def test_step_binding_refuses_cpu_tensors():
     with pytest.raises(ValueError):
         ssm.step(x, x, torch.zeros(8, 4), torch.zeros(1, 4), torch.zeros(1, 4),
                  state=torch.zeros(1, 8, 4))
+
+
+def test_conv_argument_errors():
+    lib = _lib.load()
+    vp = ctypes.c_void_p
+    s = _shape()  # DIAG bf16, batch 2, seqlen 64, 64 channels
+
+    def conv(weight=9 << 20, bias=None, x_prev=None, x_last=None, width=4):
+        c = _lib.ssm_conv()
+        c.weight, c.bias, c.x_prev, c.x_last, c.width = weight, bias, x_prev, x_last, width
+        return c
+
+    def call(c):
+        return lib.ssm_scan_fwd_conv(vp(1 << 12), vp(2 << 12), vp(3 << 12), vp(4 << 12),
+                                     vp(5 << 12), None, None, None,
+                                     None if c is None else ctypes.byref(c), None,
+                                     vp(6 << 20), None, ctypes.byref(s), None, 0, None)
+
+    assert call(None) == _lib.SSM_ERR_NULL
+    assert call(conv(weight=None)) == _lib.SSM_ERR_NULL
+    assert call(conv(width=5)) == _lib.SSM_ERR_UNSUPPORTED
+    assert call(conv(width=0)) == _lib.SSM_ERR_UNSUPPORTED
+    assert call(conv(x_prev=(10 << 20) + 4)) == _lib.SSM_ERR_ALIGN
+    # x_last inside x (x is 2*64*64 bf16 = 16 KB at 4 KB): written while x is read
+    assert call(conv(x_last=(1 << 12) + 256)) == _lib.SSM_ERR_SHAPE
+    # x_last overlapping x_prev
+    assert call(conv(x_prev=10 << 20, x_last=(10 << 20) + 16)) == _lib.SSM_ERR_SHAPE
+    # the SSD path keeps the convolved input in scratch
+    s2 = _shape(mode=1, nheads=8, headdim=64, dstate=128, chunk=64, seqlen=256)
+    plain = _ws(s2)
+    with_conv = lib.ssm_scan_conv_workspace_size(ctypes.byref(s2))
+    assert with_conv >= plain + 2 * 256 * 8 * 64 * 4
+    # the diagonal path fuses it and needs no extra scratch
+    assert lib.ssm_scan_conv_workspace_size(ctypes.byref(s)) == _ws(s)
+
+
+def test_step_conv_state_may_be_updated_in_place():
+    lib = _lib.load()
+    vp = ctypes.c_void_p
+    c = _lib.ssm_conv()
+    c.weight, c.bias, c.width = 9 << 20, None, 4
+    c.x_prev = c.x_last = 10 << 20
+    s = _shape(batch=0, seqlen=1)
+    # nothing to compute, so only the argument checks run
+    assert lib.ssm_step_conv(None, None, vp(3 << 12), None, None, None, None, None,
+                             ctypes.byref(c), None, None, ctypes.byref(s), None) == _lib.SSM_OK
+    c.x_last = (10 << 20) + 16  # partial overlap is refused
+    s = _shape(batch=2, seqlen=1)
+    assert lib.ssm_step_conv(vp(1 << 12), vp(2 << 12), vp(3 << 12), vp(4 << 12), vp(5 << 12),
+                             None, None, None, ctypes.byref(c), vp(6 << 20), vp(7 << 20),
+                             ctypes.byref(s), None) == _lib.SSM_ERR_SHAPE
