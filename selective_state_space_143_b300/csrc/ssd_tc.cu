@@ -5,7 +5,8 @@
 // blocks through the carried state), with the three matrix products of a chunk issued
 // as tcgen05.mma (bf16 operands in shared memory, fp32 accumulators in tensor memory):
 //
-//   ssd_state_tc : S_c^T for two heads at once:  D[(head, p), n] = sum_s Xd[s, (head, p)] B[s, n]
+//   ssd_state_tc : S_c^T for up to 8 heads of a chunk, two at a time:
+//                  D[(head, p), n] = sum_s Xd[s, (head, p)] B[s, n]
 //                  with Xd[s, :] = exp(s_last - s_s) Delta_s x_s  (M = 128, N = dstate, K = Q)
 //   ssd_scan_tc  : per (chunk, 128-row half): G = C_rows B^T once (M = 128, N = rows up to
 //                  the half's end, K = dstate), then per head
@@ -32,7 +33,8 @@ namespace ssm {
 namespace {
 
 constexpr int kP = 64;         // headdim handled here
-constexpr int kThreads = 256;  // 8 warps: warp w reads TMEM lanes 32*(w%4).., column half w/4
+constexpr int kThreads = 256;      // state kernel: 8 warps, TMEM lanes 32*(w%4).., column half w/4
+constexpr int kScanThreads = 512;  // scan kernel: 16 warps, TMEM lanes 32*(w%4).., column quarter w/4
 constexpr int kStatusTimeout = 8;
 
 __device__ __forceinline__ void cp_async16(uint32_t saddr, const void* gmem, bool valid) {
@@ -48,35 +50,57 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-// Inclusive prefix sum of v over the block (one value per thread); s_warp: one float per warp.
-__device__ __forceinline__ float block_incl_scan(float v, float* s_warp) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// For HPC heads [hbeg, hbeg + HPC) of chunk c at once (one row s per thread; Q <= 256):
+// Delta_s, the inclusive cumulative sum cum_s of Delta_s A_h (both to global, for the
+// scan kernel) and the chunk-end weights w[h][s] = exp(cum_last - cum_s) Delta_s.  Rows
+// past len get Delta 0.  s_warp: [8 warps][HPC].
+template <int HPC>
+__device__ void delta_cumsum_heads(const SsdTcArgs& a, int64_t b, int64_t hbeg, int64_t c, int len,
+                                   float (*s_w)[256], float* s_warp) {
+    const int s = threadIdx.x, lane = s & 31, warp = s >> 5;
+    float d[HPC], v[HPC];
+    const int64_t row = (b * a.T + c * a.Q + s) * a.H + hbeg;
+#pragma unroll
+    for (int k = 0; k < HPC; ++k) {
+        d[k] = 0.0f;
+        if (s < len) d[k] = softplus(__bfloat162float(a.dt[row + k]) + (a.dt_bias ? a.dt_bias[hbeg + k] : 0.0f));
+        v[k] = d[k] * a.A[hbeg + k];
+    }
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const float u = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += u;
+#pragma unroll
+        for (int k = 0; k < HPC; ++k) {
+            const float u = __shfl_up_sync(0xffffffffu, v[k], o);
+            if (lane >= o) v[k] += u;
+        }
+    }
+    if (lane == 31) {
+#pragma unroll
+        for (int k = 0; k < HPC; ++k) s_warp[warp * HPC + k] = v[k];
     }
     __syncthreads();
-    if (lane == 31) s_warp[warp] = v;
+#pragma unroll
+    for (int k = 0; k < HPC; ++k)
+        for (int w = 0; w < warp; ++w) v[k] += s_warp[w * HPC + k];
+    // cum_last of every head: row len-1 publishes it through s_w (overwritten below)
+    if (s == len - 1) {
+#pragma unroll
+        for (int k = 0; k < HPC; ++k) s_w[k][255] = v[k];
+    }
     __syncthreads();
-    float add = 0.0f;
-    for (int w = 0; w < warp; ++w) add += s_warp[w];
-    return v + add;
-}
-
-// Delta_s and the inclusive cumulative sum of Delta_s A_h for s in [0, Q) of chunk c
-// (one row per thread; Q <= 256).  Rows past len get Delta 0.
-__device__ void delta_cumsum(const SsdTcArgs& a, int64_t b, int64_t h, int64_t c, int len,
-                             float* s_dl, float* s_cum, float* s_warp) {
-    const int s = threadIdx.x;
-    float d = 0.0f;
-    if (s < len) d = softplus(__bfloat162float(a.dt[(b * a.T + c * a.Q + s) * a.H + h]) + (a.dt_bias ? a.dt_bias[h] : 0.0f));
-    const float incl = block_incl_scan(d * a.A[h], s_warp);
+    float last[HPC];
+#pragma unroll
+    for (int k = 0; k < HPC; ++k) last[k] = s_w[k][255];
+    __syncthreads();
     if (s < a.Q) {
-        s_dl[s] = d;
-        s_cum[s] = incl;
+#pragma unroll
+        for (int k = 0; k < HPC; ++k) {
+            const int64_t o = ((b * a.H + hbeg + k) * a.nchunks + c) * a.Q + s;
+            a.dl[o] = d[k];
+            a.cum[o] = v[k];
+            s_w[k][s] = s < len ? __expf(last[k] - v[k]) * d[k] : 0.0f;
+        }
     }
-    __syncthreads();
 }
 
 // Tile fill orders that keep 16-byte shared-memory stores free of bank conflicts: the
@@ -113,140 +137,182 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
     asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d));
 }
 
-// grid (nchunks, H/2, b); 128 threads.
-// dynamic smem: Xd hi (128 x Q) | Xd lo (128 x Q) | B column block (Q x NB), NB = min(N, 128)
+// State kernel configuration: heads per CTA (a divisor of the heads per group, so that
+// every head of the CTA reads the same B rows) and the K-part of Q taken per step.
 template <int N>
-__global__ void __launch_bounds__(kThreads) ssd_state_tc(const SsdTcArgs a) {
-    constexpr int NB = N < 128 ? N : 128;
+struct StateTcCfg {
+    static constexpr int KS = N > 128 ? 64 : 128;             // rows s per step
+    static constexpr size_t kB = (size_t)256 * N * 2;         // B rows [0, Q), resident
+    static constexpr size_t kXPart = (size_t)128 * KS * 2;    // one Xd part, hi or lo
+    static constexpr size_t kSmem = kB + 4 * kXPart;          // + 2 stages x (hi, lo)
+    static constexpr int kMaxHeads = 8;
+    static constexpr int XCH = 128 * KS / 8 / kThreads;       // 8-element x chunks per thread
+};
+
+// grid (nchunks, H / hpc, b); 256 threads.  S_c^T for hpc heads of chunk c, two heads
+// (128 accumulator rows) per pair:
+//   D[(head, p), n] = sum_s Xd[s, (head, p)] B[s, n],  Xd[s, :] = exp(cum_last - cum_s) Delta_s x_s
+// B (Q x N) is loaded once.  The pairs' K-parts form one pipeline of steps: the raw x of
+// step n+1 is in flight (registers) while step n's weighted, hi/lo-split Xd is written
+// to stage buffer n%2 and the MMAs of step n-1 run; a pair's epilogue (TMEM -> states)
+// runs once the next pair's first MMAs are queued, from alternating accumulators.
+template <int N>
+__global__ void __launch_bounds__(kThreads) ssd_state_tc(const SsdTcArgs a, int hpc) {
+    using Cfg = StateTcCfg<N>;
+    constexpr int KS = Cfg::KS;
     extern __shared__ __align__(1024) unsigned char smem[];
-    __shared__ float s_dl[2][256], s_cum[2][256], s_w[2][256], s_warp[8];
+    __shared__ float s_w[Cfg::kMaxHeads][256], s_warp[8 * Cfg::kMaxHeads];
     __shared__ uint32_t s_tmem;
-    __shared__ __align__(8) uint64_t s_mbar;
+    __shared__ __align__(8) uint64_t s_mbar[2];
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int64_t c = blockIdx.x, h0 = 2 * (int64_t)blockIdx.y, b = blockIdx.z;
+    const int64_t c = blockIdx.x, hbeg = (int64_t)blockIdx.y * hpc, b = blockIdx.z;
     const int Q = (int)a.Q;
     const int len = (int)min((int64_t)Q, a.T - c * a.Q);
-    const int64_t g = h0 / (a.H / a.G);
-    unsigned char* sXh = smem;                         // MN-major A: M = (head, p), K = s
-    unsigned char* sXl = smem + (size_t)Q * 128 * 2;
-    unsigned char* sB = smem + (size_t)Q * 128 * 4;    // MN-major B: K = s, N = NB columns
+    const int64_t g = hbeg / (a.H / a.G);
+    const int nkp = Q / KS;                  // steps per pair
+    const int nsteps = (hpc / 2) * nkp;
+    unsigned char* sB = smem;                // MN-major B operand: N_mma = n, K = s
+    unsigned char* sX = smem + Cfg::kB;      // [stage][hi, lo], MN-major A: M = (head, p), K = s
 
-    auto load_B = [&](int nb) {
-        const uint32_t base = tc::smem_u32(sB);
-        for (int i = tid; i < Q * (NB / 8); i += kThreads) {
+    // B rows of the chunk, once
+    {
+        const uint32_t bb = tc::smem_u32(sB);
+        for (int i = tid; i < Q * (N / 8); i += kThreads) {
             int s, nc;
-            mnmajor_item(i, NB / 8, s, nc);
-            const int n0 = nc * 8;
+            mnmajor_item(i, N / 8, s, nc);
             const bool ok = s < len;
-            const __nv_bfloat16* src = a.B + (ok ? (((b * a.T + c * a.Q + s) * a.G + g) * a.N + nb * NB + n0) : 0);
-            cp_async16(base + tc::off_mnmajor(n0, s, NB), src, ok);
+            const __nv_bfloat16* src = a.B + (ok ? (((b * a.T + c * a.Q + s) * a.G + g) * a.N + nc * 8) : 0);
+            cp_async16(bb + tc::off_mnmajor(nc * 8, s, N), src, ok);
+        }
+        asm volatile("cp.async.commit_group;\n" ::);
+    }
+    constexpr uint32_t kCols = 2 * N < 32 ? 32 : 2 * N;  // two accumulators
+    if (warp == 0) tc::tmem_alloc(&s_tmem, kCols);
+    if (tid == 0) {
+        tc::mbar_init(&s_mbar[0], 1);
+        tc::mbar_init(&s_mbar[1], 1);
+        tc::mbar_fence_init();
+    }
+
+    // raw x of step n in registers: rows s in [kp*KS, +KS) of heads (pair, pair+1); two
+    // register sets, so that steps n+1 and n+2 are in flight while step n is built
+    uint4 pfa[Cfg::XCH], pfb[Cfg::XCH];
+    auto prefetch = [&](int n, uint4 (&pf)[Cfg::XCH]) {
+        const int pair = n / nkp, kp = n % nkp;
+#pragma unroll
+        for (int j = 0; j < Cfg::XCH; ++j) {
+            int sl, mc;
+            mnmajor_item(tid + j * kThreads, 16, sl, mc);
+            const int s = kp * KS + sl, m0 = mc * 8;
+            const int64_t h = hbeg + 2 * pair + m0 / kP;
+            pf[j] = make_uint4(0, 0, 0, 0);
+            if (s < len) pf[j] = *reinterpret_cast<const uint4*>(a.x + ((b * a.T + c * a.Q + s) * a.H + h) * kP + m0 % kP);
         }
     };
-    load_B(0);
-    // Delta, cumulative sums and the chunk-end weights for both heads
-    for (int hl = 0; hl < 2; ++hl) {
-        delta_cumsum(a, b, h0 + hl, c, len, s_dl[hl], s_cum[hl], s_warp);
-        const float last = s_cum[hl][len - 1];
-        for (int s = tid; s < Q; s += kThreads) s_w[hl][s] = s < len ? __expf(last - s_cum[hl][s]) * s_dl[hl][s] : 0.0f;
-        for (int s = tid; s < Q; s += kThreads) {
-            const int64_t o = ((b * a.H + h0 + hl) * a.nchunks + c) * a.Q + s;
-            a.dl[o] = s_dl[hl][s];
-            a.cum[o] = s_cum[hl][s];
-        }
-    }
-    __syncthreads();
-    // Xd = w_s x_s for both heads, split hi/lo, MN-major (8 consecutive p at one s).
-    // Raw x is staged into the lo tile by cp.async (all chunks in flight at once), then
-    // each thread rewrites its own chunks: hi into the hi tile, lo in place.
-    {
-        const uint32_t bh = tc::smem_u32(sXh), bl = tc::smem_u32(sXl);
-        for (int i = tid; i < Q * 16; i += kThreads) {
-            int s, mc;
-            mnmajor_item(i, 16, s, mc);
-            const int m0 = mc * 8;  // m = head_local * 64 + p
-            const int hl = m0 / kP, p0 = m0 % kP;
-            const bool ok = s < len;
-            const __nv_bfloat16* src = a.x + (ok ? ((b * a.T + c * a.Q + s) * a.H + h0 + hl) * kP + p0 : 0);
-            cp_async16(bl + tc::off_mnmajor(m0, s, 128), src, ok);
-        }
-        cp_async_commit_wait_all();
-        __syncthreads();
-        for (int i = tid; i < Q * 16; i += kThreads) {
-            int s, mc;
-            mnmajor_item(i, 16, s, mc);
+    // Xd of step n -> stage n%2, hi/lo
+    auto build = [&](int n, const uint4 (&pf)[Cfg::XCH]) {
+        const int pair = n / nkp, kp = n % nkp;
+        unsigned char* st = sX + (n & 1) * 2 * Cfg::kXPart;
+        const uint32_t bh = tc::smem_u32(st), bl = tc::smem_u32(st + Cfg::kXPart);
+#pragma unroll
+        for (int j = 0; j < Cfg::XCH; ++j) {
+            int sl, mc;
+            mnmajor_item(tid + j * kThreads, 16, sl, mc);
             const int m0 = mc * 8;
-            const int hl = m0 / kP;
-            const uint32_t off = tc::off_mnmajor(m0, s, 128);
-            const uint4 raw = *reinterpret_cast<const uint4*>(sXl + off);
-            const float w = s_w[hl][s];
-            const __nv_bfloat162* r2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+            const float w = s_w[2 * pair + m0 / kP][kp * KS + sl];
+            const __nv_bfloat162* r2 = reinterpret_cast<const __nv_bfloat162*>(&pf[j]);
             uint32_t hi[4], lo[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const float2 f = __bfloat1622float2(r2[k]);
                 split2(f.x * w, f.y * w, hi[k], lo[k]);
             }
+            const uint32_t off = tc::off_mnmajor(m0, sl, 128);
             st_shared_v4(bh + off, hi[0], hi[1], hi[2], hi[3]);
             st_shared_v4(bl + off, lo[0], lo[1], lo[2], lo[3]);
         }
-    }
-    constexpr uint32_t kCols = N < 32 ? 32 : N;
-    if (warp == 0) tc::tmem_alloc(&s_tmem, kCols);
-    if (tid == 0) {
-        tc::mbar_init(&s_mbar, 1);
-        tc::mbar_fence_init();
-    }
-    bool ok = true;
-    uint32_t phase = 0;
-    uint32_t tmem = 0;
-    for (int nb = 0; nb < N / NB; ++nb) {
-        if (nb > 0) {
-            // the previous column block's MMAs must be done with sB before it is reloaded
-            ok = tc::mbar_wait(&s_mbar, phase) && ok;
-            phase ^= 1;
-            tc::fence_after_sync();
-            __syncthreads();
-            load_B(nb);
-        }
-        cp_async_commit_wait_all();
-        tc::fence_async_smem();
-        tc::fence_before_sync();
-        __syncthreads();
-        tc::fence_after_sync();
-        tmem = s_tmem;
-        // D[(head, p), nb*NB + n] = sum_s (Xd_hi + Xd_lo)[s, (head, p)] B[s, nb*NB + n]
-        if (tid == 0) {
-            constexpr uint32_t idesc = tc::idesc_bf16(128, NB, 1, 1);
-            const uint64_t dxh = tc::desc_mnmajor(tc::smem_u32(sXh), 128, 0);
-            const uint64_t dxl = tc::desc_mnmajor(tc::smem_u32(sXl), 128, 0);
-            const uint64_t db = tc::desc_mnmajor(tc::smem_u32(sB), NB, 0);
-            const uint32_t d = tmem + (uint32_t)(nb * NB);
-            for (int ks = 0; ks < Q / 16; ++ks)
-                tc::mma_bf16(d, dxh + ks * tc::kstep_mnmajor(128), db + ks * tc::kstep_mnmajor(NB), idesc, ks > 0);
-            for (int ks = 0; ks < Q / 16; ++ks)
-                tc::mma_bf16(d, dxl + ks * tc::kstep_mnmajor(128), db + ks * tc::kstep_mnmajor(NB), idesc, 1);
-            tc::mma_commit(&s_mbar);
-        }
-    }
-    ok = tc::mbar_wait(&s_mbar, phase) && ok;
-    tc::fence_after_sync();
-    if (ok) {
-        // row m = lane: (head h0 + m/64, p = m%64) -> states[b, c, h, p, :]; warps 4-7 take
-        // the upper half of the columns
+    };
+    // accumulator of pair -> states[b, c, h, p, :]; warp w: lanes 32*(w%4).., column half w/4
+    auto epilogue = [&](uint32_t tmem, int pair) {
         const int q = warp & 3;
         const int m = q * 32 + (tid & 31);
-        float* dst = a.states + (((b * a.nchunks + c) * a.H + h0 + m / kP) * kP + (m % kP)) * a.N;
+        const int64_t h = hbeg + 2 * pair + m / kP;
+        float* dst = a.states + (((b * a.nchunks + c) * a.H + h) * kP + (m % kP)) * a.N;
+        const uint32_t acc = tmem + (uint32_t)((pair & 1) * N);
         constexpr int NH = N / 2 < 16 ? 16 : N / 2;
 #pragma unroll 1
         for (int n0 = (warp >> 2) * NH; n0 < N && n0 < ((warp >> 2) + 1) * NH; n0 += 16) {
             float v[16];
-            tc::tmem_ld16(tc::taddr(tmem, q * 32, n0), v);
+            tc::tmem_ld16(tc::taddr(acc, q * 32, n0), v);
 #pragma unroll
             for (int j = 0; j < 16; j += 4) *reinterpret_cast<float4*>(dst + n0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
         }
-    } else if (tid == 0) {
-        report_timeout(a.status);
+    };
+
+    // steps 0 and 1 in flight during the Delta pass; Delta, cumulative sums (to global,
+    // for the scan kernel) and chunk-end weights of all the CTA's heads in one pass
+    prefetch(0, pfa);
+    if (nsteps > 1) prefetch(1, pfb);
+    if (hpc == 8)
+        delta_cumsum_heads<8>(a, b, hbeg, c, len, s_w, s_warp);
+    else if (hpc == 4)
+        delta_cumsum_heads<4>(a, b, hbeg, c, len, s_w, s_warp);
+    else
+        delta_cumsum_heads<2>(a, b, hbeg, c, len, s_w, s_warp);
+    asm volatile("cp.async.wait_group 0;\n" ::);
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = s_tmem;
+    bool ok = true;
+    // commit n arrives on s_mbar[n & 1], phase (n >> 1) & 1; a wait is only ever on the
+    // latest commit of its barrier
+    auto wait_commit = [&](int n) {
+        ok = tc::mbar_wait(&s_mbar[n & 1], (uint32_t)(n >> 1) & 1u) && ok;
+        tc::fence_after_sync();
+    };
+    auto step = [&](int n, uint4 (&pf)[Cfg::XCH]) {
+        const int pair = n / nkp, kp = n % nkp;
+        if (n >= 2) wait_commit(n - 2);  // stage n%2 free again
+        build(n, pf);
+        if (n + 2 < nsteps) prefetch(n + 2, pf);
+        tc::fence_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+        if (tid == 0) {
+            constexpr uint32_t idesc = tc::idesc_bf16(128, N, 1, 1);
+            unsigned char* st = sX + (n & 1) * 2 * Cfg::kXPart;
+            const uint64_t dxh = tc::desc_mnmajor(tc::smem_u32(st), 128, 0);
+            const uint64_t dxl = tc::desc_mnmajor(tc::smem_u32(st + Cfg::kXPart), 128, 0);
+            const uint64_t db = tc::desc_mnmajor(tc::smem_u32(sB), N, kp * (KS / 16));
+            const uint32_t d = tmem + (uint32_t)((pair & 1) * N);
+#pragma unroll
+            for (int ks = 0; ks < KS / 16; ++ks)
+                tc::mma_bf16(d, dxh + ks * tc::kstep_mnmajor(128), db + ks * tc::kstep_mnmajor(N), idesc,
+                             (kp > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
+            for (int ks = 0; ks < KS / 16; ++ks)
+                tc::mma_bf16(d, dxl + ks * tc::kstep_mnmajor(128), db + ks * tc::kstep_mnmajor(N), idesc, 1u);
+            tc::mma_commit(&s_mbar[n & 1]);
+        }
+        // the previous pair's states, once this pair's first MMAs are queued
+        if (kp == 0 && pair > 0) {
+            wait_commit(n - 1);
+            epilogue(tmem, pair - 1);
+            tc::fence_before_sync();
+        }
+    };
+    for (int n = 0; n < nsteps && ok; n += 2) {
+        step(n, pfa);
+        if (n + 1 < nsteps && ok) step(n + 1, pfb);
     }
+    if (ok && nsteps > 0) {
+        wait_commit(nsteps - 1);
+        epilogue(tmem, hpc / 2 - 1);
+    }
+    if (!ok && tid == 0) report_timeout(a.status);
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, kCols);
@@ -275,7 +341,7 @@ struct ScanTcCfg {
 //   finish   : the epilogue of head h-1, from its own TMEM accumulators, right after
 //              head h's first MMAs are issued.
 template <int N, bool GATE>
-__global__ void __launch_bounds__(kThreads) ssd_scan_tc(const SsdTcArgs a, int heads_per_cta) {
+__global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_tc(const SsdTcArgs a, int heads_per_cta) {
     using Cfg = ScanTcCfg<N>;
     constexpr int KPC = Cfg::KPC;
     extern __shared__ __align__(1024) unsigned char smem[];
@@ -308,7 +374,7 @@ __global__ void __launch_bounds__(kThreads) ssd_scan_tc(const SsdTcArgs a, int h
     // phase 1 loads: C rows of this half and B rows [0, SW)
     {
         const uint32_t cb = tc::smem_u32(sC), bb = tc::smem_u32(sB);
-        for (int i = tid; i < 128 * (N / 8); i += kThreads) {
+        for (int i = tid; i < 128 * (N / 8); i += kScanThreads) {
             int rr, nc;
             kmajor_item(i, N / 8, rr, nc);
             const int s = t0 + rr;
@@ -316,7 +382,7 @@ __global__ void __launch_bounds__(kThreads) ssd_scan_tc(const SsdTcArgs a, int h
             const __nv_bfloat16* src = a.C + (ok ? (((b * a.T + c * a.Q + s) * a.G + g) * a.N + nc * 8) : 0);
             cp_async16(cb + tc::off_kmajor(rr, nc * 8, N), src, ok);
         }
-        for (int i = tid; i < SW * (N / 8); i += kThreads) {
+        for (int i = tid; i < SW * (N / 8); i += kScanThreads) {
             int s, nc;
             kmajor_item(i, N / 8, s, nc);
             const bool ok = s < len;
@@ -351,13 +417,13 @@ __global__ void __launch_bounds__(kThreads) ssd_scan_tc(const SsdTcArgs a, int h
     tc::fence_after_sync();
 
     const int q = warp & 3;                  // TMEM lane quarter of this warp
-    const int chalf = warp >> 2;             // warps 4-7 take the upper half of the columns
+    const int cq = warp >> 2;                // column quarter of this warp
     const int r = q * 32 + (tid & 31);       // my row (TMEM lane) within the half
     const int t = t0 + r;                    // row within the chunk
     const bool row_ok = t < len;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     const int t_warp_max = t0 + q * 32 + 31;  // tcgen05.ld is warp-collective
-    const int cols_per_warp = KPC / 2;       // columns of a K-part built by one warp
+    constexpr int BC = KPC / 4;              // columns of a K-part built by one warp
 
     // MMA commits are numbered; commit n arrives on s_mbar[n & 1], phase (n >> 1) & 1.
     uint32_t ncommit = 0;
@@ -367,8 +433,8 @@ __global__ void __launch_bounds__(kThreads) ssd_scan_tc(const SsdTcArgs a, int h
     };
 
     // next head's inputs in registers (see commit below)
-    constexpr int XCH = 256 * (kP / 8) / kThreads;  // x_h chunks per thread (SW <= 256)
-    constexpr int HCH = kP * (N / 8) / kThreads;    // 8-float groups of h per thread
+    constexpr int XCH = 256 * (kP / 8) / kScanThreads;                   // x_h chunks per thread (SW <= 256)
+    constexpr int HCH = (kP * (N / 8) + kScanThreads - 1) / kScanThreads;  // 8-float groups of h per thread
     float pf_dl = 0.0f, pf_cum = 0.0f;
     uint4 pf_x[XCH];
     float4 pf_h[HCH][2];
@@ -380,7 +446,7 @@ __global__ void __launch_bounds__(kThreads) ssd_scan_tc(const SsdTcArgs a, int h
         }
 #pragma unroll
         for (int j = 0; j < XCH; ++j) {
-            const int i = tid + j * kThreads;
+            const int i = tid + j * kScanThreads;
             int s, pc;
             mnmajor_item(i, kP / 8, s, pc);
             pf_x[j] = make_uint4(0, 0, 0, 0);
@@ -390,8 +456,10 @@ __global__ void __launch_bounds__(kThreads) ssd_scan_tc(const SsdTcArgs a, int h
         const float* hs = a.states + ((b * a.nchunks + c) * a.H + hn) * (int64_t)kP * a.N;
 #pragma unroll
         for (int j = 0; j < HCH; ++j) {
+            const int i = tid + j * kScanThreads;
+            if (i >= kP * (N / 8)) break;
             int p, nc;
-            kmajor_item(tid + j * kThreads, N / 8, p, nc);
+            kmajor_item(i, N / 8, p, nc);
             pf_h[j][0] = *reinterpret_cast<const float4*>(hs + (int64_t)p * a.N + nc * 8);
             pf_h[j][1] = *reinterpret_cast<const float4*>(hs + (int64_t)p * a.N + nc * 8 + 4);
         }
@@ -407,7 +475,7 @@ __global__ void __launch_bounds__(kThreads) ssd_scan_tc(const SsdTcArgs a, int h
         const uint32_t xb = tc::smem_u32(sX + xbuf * Cfg::kX);
 #pragma unroll
         for (int j = 0; j < XCH; ++j) {
-            const int i = tid + j * kThreads;
+            const int i = tid + j * kScanThreads;
             int s, pc;
             mnmajor_item(i, kP / 8, s, pc);
             if (i < SW * (kP / 8)) st_shared_v4(xb + tc::off_mnmajor(pc * 8, s, kP), pf_x[j].x, pf_x[j].y, pf_x[j].z, pf_x[j].w);
@@ -415,8 +483,10 @@ __global__ void __launch_bounds__(kThreads) ssd_scan_tc(const SsdTcArgs a, int h
         const uint32_t hb = tc::smem_u32(sHh), lb = tc::smem_u32(sHl);
 #pragma unroll
         for (int j = 0; j < HCH; ++j) {
+            const int i = tid + j * kScanThreads;
+            if (i >= kP * (N / 8)) break;
             int p, nc;
-            kmajor_item(tid + j * kThreads, N / 8, p, nc);
+            kmajor_item(i, N / 8, p, nc);
             uint32_t qh[4], ql[4];
             split2(pf_h[j][0].x, pf_h[j][0].y, qh[0], ql[0]);
             split2(pf_h[j][0].z, pf_h[j][0].w, qh[1], ql[1]);
@@ -434,8 +504,8 @@ __global__ void __launch_bounds__(kThreads) ssd_scan_tc(const SsdTcArgs a, int h
         const float et = ex2(alpha_h);
         const float Dh = a.D ? a.D[hh] : 0.0f;
         const int64_t row = ((b * a.T + c * a.Q + t) * a.H + hh) * kP;
-#pragma unroll 1
-        for (int p0 = 32 * chalf; p0 < 32 * chalf + 32; p0 += 16) {
+        {
+            const int p0 = 16 * cq;  // this warp's 16 head channels
             float yd[16], yo[16];
             tc::tmem_ld16(tYd + lane_base + (uint32_t)p0, yd);
             tc::tmem_ld16(tYo + lane_base + (uint32_t)p0, yo);
@@ -487,55 +557,39 @@ __global__ void __launch_bounds__(kThreads) ssd_scan_tc(const SsdTcArgs a, int h
             // this K-part's buffer was last used by commit ncommit - 2
             if (ncommit >= 2) wait_commit(ncommit - 2);
             // M'[t, s] = G[t, s] 2^(alpha_t + beta_s) for s <= t, hi/lo, K-major.  This warp
-            // builds cols_per_warp columns in blocks of 16; the TMEM load of block j + 1 is
-            // in flight while block j is computed.
+            // builds BC columns of the part for its 32 rows.
             {
                 unsigned char* part = sM + (ncommit & 1) * 2 * Cfg::kMPart;
                 const uint32_t mh = tc::smem_u32(part), ml = tc::smem_u32(part + Cfg::kMPart);
-                const int s_lo = KPC * kp + cols_per_warp * chalf;
-                constexpr int NBLK = KPC / 2 / 16;
-                int nvalid = 0;  // blocks with some s <= t for this warp (warp-uniform)
+                const int s0 = KPC * kp + BC * cq;
+                uint32_t ph[BC / 2], pl[BC / 2];
+                if (s0 <= t_warp_max) {  // some s <= t for this warp (warp-uniform)
+                    uint32_t gv[BC];
+                    tc::tmem_ld_async(tG + lane_base + (uint32_t)s0, gv);
+                    float bt[BC];
 #pragma unroll
-                for (int blk = 0; blk < NBLK; ++blk) nvalid += (s_lo + 16 * blk <= t_warp_max) ? 1 : 0;
-                uint32_t cur[16], nxt[16];
-                if (nvalid > 0) {
-                    tc::tmem_ld16_async(tG + lane_base + (uint32_t)s_lo, cur);
+                    for (int j = 0; j < BC; j += 4) *reinterpret_cast<float4*>(&bt[j]) = *reinterpret_cast<const float4*>(&s_beta[s0 + j]);
+                    const bool full = s0 + BC - 1 <= t0 + q * 32;  // no masked column in this warp
                     tc::tmem_wait_ld();
-                }
 #pragma unroll
-                for (int blk = 0; blk < NBLK; ++blk) {
-                    const int s0 = s_lo + 16 * blk;
-                    uint32_t ph[8], pl[8];
-                    if (blk < nvalid) {
-                        if (blk + 1 < nvalid) tc::tmem_ld16_async(tG + lane_base + (uint32_t)(s0 + 16), nxt);
-                        const bool full = s0 + 15 <= t0 + q * 32;  // no masked column in this warp
-                        float bt[16];
-#pragma unroll
-                        for (int j = 0; j < 16; j += 4) *reinterpret_cast<float4*>(&bt[j]) = *reinterpret_cast<const float4*>(&s_beta[s0 + j]);
-#pragma unroll
-                        for (int j = 0; j < 16; j += 2) {
-                            float v0 = ex2(alpha + bt[j]) * __uint_as_float(cur[j]);
-                            float v1 = ex2(alpha + bt[j + 1]) * __uint_as_float(cur[j + 1]);
-                            if (!full) {
-                                v0 = s0 + j <= t ? v0 : 0.0f;
-                                v1 = s0 + j + 1 <= t ? v1 : 0.0f;
-                            }
-                            split2(v0, v1, ph[j / 2], pl[j / 2]);
+                    for (int j = 0; j < BC; j += 2) {
+                        float v0 = ex2(alpha + bt[j]) * __uint_as_float(gv[j]);
+                        float v1 = ex2(alpha + bt[j + 1]) * __uint_as_float(gv[j + 1]);
+                        if (!full) {
+                            v0 = s0 + j <= t ? v0 : 0.0f;
+                            v1 = s0 + j + 1 <= t ? v1 : 0.0f;
                         }
-                        if (blk + 1 < nvalid) {
-                            tc::tmem_wait_ld();
-#pragma unroll
-                            for (int j = 0; j < 16; ++j) cur[j] = nxt[j];
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) ph[j] = pl[j] = 0u;
+                        split2(v0, v1, ph[j / 2], pl[j / 2]);
                     }
-                    const int sl = s0 - KPC * kp;
-                    st_shared_v4(mh + tc::off_kmajor(r, sl, KPC), ph[0], ph[1], ph[2], ph[3]);
-                    st_shared_v4(mh + tc::off_kmajor(r, sl + 8, KPC), ph[4], ph[5], ph[6], ph[7]);
-                    st_shared_v4(ml + tc::off_kmajor(r, sl, KPC), pl[0], pl[1], pl[2], pl[3]);
-                    st_shared_v4(ml + tc::off_kmajor(r, sl + 8, KPC), pl[4], pl[5], pl[6], pl[7]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < BC / 2; ++j) ph[j] = pl[j] = 0u;
+                }
+                const int sl = s0 - KPC * kp;
+#pragma unroll
+                for (int j = 0; j < BC / 8; ++j) {
+                    st_shared_v4(mh + tc::off_kmajor(r, sl + 8 * j, KPC), ph[4 * j], ph[4 * j + 1], ph[4 * j + 2], ph[4 * j + 3]);
+                    st_shared_v4(ml + tc::off_kmajor(r, sl + 8 * j, KPC), pl[4 * j], pl[4 * j + 1], pl[4 * j + 2], pl[4 * j + 3]);
                 }
             }
             tc::fence_async_smem();
@@ -603,13 +657,22 @@ bool ssd_tc_supported(const ScanArgs& a, int64_t Q) {
 
 namespace {
 
+// Heads per CTA: the largest of 8, 4, 2 that divides the heads of a group.
+int heads_per_cta(const SsdTcArgs& s, int max_heads) {
+    const int hpg = (int)(s.H / s.G);
+    for (int cand : {8, 4, 2, 1})
+        if (cand <= max_heads && hpg % cand == 0) return cand;
+    return 1;
+}
+
 template <int N>
 cudaError_t launch_state(const SsdTcArgs& s, int64_t batch, cudaStream_t stream) {
-    constexpr int NB = N < 128 ? N : 128;
-    const size_t smem = (size_t)s.Q * 128 * 4 + (size_t)s.Q * NB * 2;
+    using Cfg = StateTcCfg<N>;
+    const size_t smem = Cfg::kSmem;
     cudaError_t e = cudaFuncSetAttribute(ssd_state_tc<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    ssd_state_tc<N><<<dim3((unsigned)s.nchunks, (unsigned)(s.H / 2), (unsigned)batch), kThreads, smem, stream>>>(s);
+    const int hpc = heads_per_cta(s, Cfg::kMaxHeads);  // even: heads per group are even here
+    ssd_state_tc<N><<<dim3((unsigned)s.nchunks, (unsigned)(s.H / hpc), (unsigned)batch), kThreads, smem, stream>>>(s, hpc);
     note_launches(1);
     return cudaGetLastError();
 }
@@ -621,15 +684,9 @@ cudaError_t launch_scan(const SsdTcArgs& s, int64_t batch, cudaStream_t stream) 
     auto kern = ssd_scan_tc<N, GATE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const int hpg = (int)(s.H / s.G);
-    int hpc = 1;  // heads per CTA: G = C B^T is shared by them (a divisor of heads per group)
-    for (int cand : {8, 4, 2, 1})
-        if (hpg % cand == 0) {
-            hpc = cand;
-            break;
-        }
+    const int hpc = heads_per_cta(s, 8);  // G = C B^T is shared by the CTA's heads
     const dim3 grid((unsigned)(s.nchunks * (s.Q / 128)), (unsigned)(s.H / hpc), (unsigned)batch);
-    kern<<<grid, kThreads, smem, stream>>>(s, hpc);
+    kern<<<grid, kScanThreads, smem, stream>>>(s, hpc);
     note_launches(1);
     return cudaGetLastError();
 }
