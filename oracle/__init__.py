@@ -62,6 +62,8 @@ class OracleLib:
             dp, dp, ip, i64, ctypes.c_int]
         lib.oracle_scan_chunked.restype = ctypes.c_int
         lib.oracle_max_threads.restype = ctypes.c_int
+        lib.oracle_scan_bwd.argtypes = [ctypes.c_int] + [i64] * 6 + [dp] * 20
+        lib.oracle_scan_bwd.restype = ctypes.c_int
         lib.oracle_conv_silu.argtypes = [i64] * 4 + [dp] * 6
         lib.oracle_conv_silu.restype = ctypes.c_int
         self.lib = lib
@@ -72,6 +74,9 @@ class OracleLib:
 
     def conv_silu(self, *args, **kw):
         return _conv_silu(self.lib, *args, **kw)
+
+    def scan_bwd(self, *args, **kw):
+        return _scan_bwd(self.lib, *args, **kw)
 
 
 def _load():
@@ -121,6 +126,46 @@ def scan_conv(x, dt, A, B, C, D=None, z=None, dt_bias=None, *, conv_w, conv_b=No
     xc, x_last = conv_silu(x, conv_w, conv_b, x_prev)
     out, fs = scan(xc, dt, A, B, C, D, z, dt_bias, **kw)
     return out, fs, x_last
+
+
+def scan_bwd(*args, **kw):
+    """Run the oracle's backward pass; see ``_scan_bwd``."""
+    return _scan_bwd(_load(), *args, **kw)
+
+
+def _scan_bwd(lib, x, dt, A, B, C, D=None, z=None, dt_bias=None, initial_state=None, *, dout,
+              dfinal=None):
+    """Gradients of the scan (fp64, serial over channels).
+
+    Arguments as ``scan``; ``dout`` has x's shape, ``dfinal`` the final state's.
+    Returns a dict with dx, ddt, dA, dB, dC (always) and dD, dz, ddt_bias, dinit (None
+    where the matching input is None).
+    """
+    x, dt, A, B, C = (_f64(v) for v in (x, dt, A, B, C))
+    D, z, dt_bias, initial_state, dout, dfinal = (
+        _f64(v) for v in (D, z, dt_bias, initial_state, dout, dfinal))
+    mode, b, T, H, P, N, G = _shape(x, dt, A, B)
+    Bs = B.reshape(b, T, G, N)
+    out = {
+        "dx": np.empty(x.shape), "ddt": np.empty(dt.shape), "dA": np.empty(A.shape),
+        "dB": np.empty(Bs.shape), "dC": np.empty(Bs.shape),
+        "dD": None if D is None else np.empty(D.shape),
+        "dz": None if z is None else np.empty(z.shape),
+        "ddt_bias": None if dt_bias is None else np.empty(dt_bias.shape),
+        "dinit": np.empty((b, H, N) if mode == MODE_DIAG else (b, H, P, N)),
+    }
+    if dout.shape != x.shape:
+        raise ValueError("dout must have x's shape")
+    rc = lib.oracle_scan_bwd(mode, b, T, H, P, N, G,
+                             *(_ptr(v) for v in (x, dt, A, Bs, C.reshape(Bs.shape), D, z, dt_bias,
+                                                 initial_state, dout, dfinal)),
+                             *(_ptr(out[k]) for k in ("dx", "ddt", "dA", "dB", "dC", "dD", "dz",
+                                                      "ddt_bias", "dinit")))
+    if rc != 0:
+        raise RuntimeError(f"oracle returned status {rc}")
+    out["dB"] = out["dB"].reshape(B.shape)
+    out["dC"] = out["dC"].reshape(B.shape)
+    return out
 
 
 def max_threads() -> int:

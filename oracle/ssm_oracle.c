@@ -46,7 +46,9 @@
  *   initial_state, final_state (batch, nheads, headdim, dstate), nullable
  *
  * Parity status: pinned (brute-force semiseparable matrix, closed-form LTI responses,
- * masked linear attention at A = 0, hand-worked golden values, invariants).
+ * masked linear attention at A = 0, hand-worked golden values, invariants; the
+ * convolution against numpy's convolution; the backward pass against central finite
+ * differences of the forward).
  */
 #include <math.h>
 #include <stdint.h>
@@ -302,6 +304,124 @@ int oracle_conv_silu(int64_t batch, int64_t seqlen, int64_t channels, int64_t wi
             }
         }
     }
+    return 0;
+}
+
+/*
+ * Backward pass of the scan (reverse-mode derivatives), written from the recurrence;
+ * the pages give none.  With v_t = dt_t + dt_bias, Delta_t = softplus(v_t),
+ * a_t[n] = exp(Delta_t A_n), h_t = a_t h_{t-1} + Delta_t B_t x_t, y_t = C_t.h_t + D x_t,
+ * out_t = y_t SiLU(z_t), and the incoming gradients dout (of out) and dfinal (of the
+ * final state, nullable), per channel from t = T-1 down to 0:
+ *   dy_t     = dout_t SiLU(z_t)                  dz_t += dout_t y_t SiLU'(z_t)
+ *   g_t      = dy_t C_t + a_{t+1} g_{t+1}        (g_T-1 starts from dfinal) = dL/dh_t
+ *   dx_t    += dy_t D + sum_n g_t[n] Delta_t B_t[n]
+ *   dB_t    += g_t Delta_t x_t                   dC_t += dy_t h_t
+ *   dDelta_t = sum_n g_t[n] (B_t[n] x_t + a_t[n] A_n h_{t-1}[n])
+ *   dA_n    += g_t[n] a_t[n] Delta_t h_{t-1}[n]  dD   += dy_t x_t
+ *   ddt_t   += dDelta_t sigmoid(v_t)             ddt_bias += dDelta_t sigmoid(v_t)
+ * and dinit = a_0 g_0.  Parameters shared by channels (B, C by group; A, D, dt and
+ * dt_bias by head in SSD mode) receive the sum over those channels.  Every output is
+ * overwritten (zeroed first).  Each channel keeps its whole state history (T x N).
+ * Layouts as the forward; dA as A; ddt as dt; dinit as initial_state.  dz, dD,
+ * ddt_bias and dinit may be NULL (not computed); z, D, dt_bias, initial_state and
+ * dfinal may be NULL as in the forward.
+ */
+int oracle_scan_bwd(int mode, int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
+                    int64_t dstate, int64_t ngroups, const double* x, const double* dt,
+                    const double* A, const double* B, const double* C, const double* D,
+                    const double* z, const double* dt_bias, const double* initial_state,
+                    const double* dout, const double* dfinal, double* dx, double* ddt, double* dA,
+                    double* dB, double* dC, double* dD, double* dz, double* ddt_bias,
+                    double* dinit) {
+    double dummy = 0.0;
+    oracle_problem p = {mode, batch, seqlen, nheads, headdim, dstate, ngroups, x, dt, A, B, C,
+                        D, z, dt_bias, initial_state, &dummy, NULL};
+    int rc = oracle_check(&p);
+    if (rc) return rc;
+    if (!dout || !dx || !ddt || !dA || !dB || !dC) return 1;
+    const int64_t T = seqlen, H = nheads, P = headdim, N = dstate, G = ngroups;
+    memset(dx, 0, sizeof(double) * (size_t)(batch * T * H * P));
+    memset(ddt, 0, sizeof(double) * (size_t)(batch * T * H));
+    memset(dA, 0, sizeof(double) * (size_t)(mode == ORACLE_MODE_DIAG ? H * N : H));
+    memset(dB, 0, sizeof(double) * (size_t)(batch * T * G * N));
+    memset(dC, 0, sizeof(double) * (size_t)(batch * T * G * N));
+    if (dD) memset(dD, 0, sizeof(double) * (size_t)H);
+    if (dz) memset(dz, 0, sizeof(double) * (size_t)(batch * T * H * P));
+    if (ddt_bias) memset(ddt_bias, 0, sizeof(double) * (size_t)H);
+    double* hist = (double*)malloc(sizeof(double) * (size_t)((T + 1) * N));
+    double* g = (double*)malloc(sizeof(double) * (size_t)N);
+    if (!hist || !g) {
+        free(hist);
+        free(g);
+        return 6;
+    }
+    for (int64_t b = 0; b < batch; ++b)
+        for (int64_t h = 0; h < H; ++h)
+            for (int64_t q = 0; q < P; ++q) {
+                const int64_t grp = h / (H / G);
+                const int64_t sidx = ((b * H + h) * P + q) * N;
+                /* forward, keeping h_{t-1} in hist[t] (hist[0] = initial state) */
+                for (int64_t n = 0; n < N; ++n) hist[n] = initial_state ? initial_state[sidx + n] : 0.0;
+                for (int64_t t = 0; t < T; ++t) {
+                    const int64_t bt = b * T + t;
+                    const double delta = oracle_softplus(dt[bt * H + h] + (dt_bias ? dt_bias[h] : 0.0));
+                    const double xv = x[(bt * H + h) * P + q];
+                    const double* Bt = B + (bt * G + grp) * N;
+                    for (int64_t n = 0; n < N; ++n)
+                        hist[(t + 1) * N + n] = exp(delta * oracle_acoef(&p, h, n)) * hist[t * N + n] + delta * Bt[n] * xv;
+                }
+                /* reverse */
+                for (int64_t n = 0; n < N; ++n) g[n] = dfinal ? dfinal[sidx + n] : 0.0;
+                for (int64_t t = T - 1; t >= 0; --t) {
+                    const int64_t bt = b * T + t;
+                    const int64_t xi = (bt * H + h) * P + q;
+                    const double v = dt[bt * H + h] + (dt_bias ? dt_bias[h] : 0.0);
+                    const double delta = oracle_softplus(v);
+                    const double sig_v = 1.0 / (1.0 + exp(-v));
+                    const double xv = x[xi];
+                    const double* Bt = B + (bt * G + grp) * N;
+                    const double* Ct = C + (bt * G + grp) * N;
+                    const double* hprev = hist + t * N;
+                    const double* hcur = hist + (t + 1) * N;
+                    double y = 0.0;
+                    for (int64_t n = 0; n < N; ++n) y += Ct[n] * hcur[n];
+                    if (D) y += D[h] * xv;
+                    double gate = 1.0;
+                    if (z) {
+                        const double zv = z[xi];
+                        const double sz = 1.0 / (1.0 + exp(-zv));
+                        gate = zv * sz;
+                        if (dz) dz[xi] = dout[xi] * y * sz * (1.0 + zv * (1.0 - sz));
+                    }
+                    const double dy = dout[xi] * gate;
+                    double dxv = D ? dy * D[h] : 0.0;
+                    double ddelta = 0.0;
+                    for (int64_t n = 0; n < N; ++n) {
+                        const double an = oracle_acoef(&p, h, n);
+                        const double abar = exp(delta * an);
+                        g[n] += dy * Ct[n];
+                        dxv += g[n] * delta * Bt[n];
+                        dB[(bt * G + grp) * N + n] += g[n] * delta * xv;
+                        dC[(bt * G + grp) * N + n] += dy * hcur[n];
+                        ddelta += g[n] * (Bt[n] * xv + abar * an * hprev[n]);
+                        const double da = g[n] * abar * delta * hprev[n];
+                        if (mode == ORACLE_MODE_DIAG)
+                            dA[h * N + n] += da;
+                        else
+                            dA[h] += da;
+                        g[n] *= abar; /* now dL/dh_{t-1} */
+                    }
+                    dx[xi] = dxv;
+                    if (dD) dD[h] += dy * xv;
+                    ddt[bt * H + h] += ddelta * sig_v;
+                    if (ddt_bias) ddt_bias[h] += ddelta * sig_v;
+                }
+                if (dinit)
+                    for (int64_t n = 0; n < N; ++n) dinit[sidx + n] = g[n];
+            }
+    free(hist);
+    free(g);
     return 0;
 }
 

@@ -56,6 +56,32 @@ CONV_MUTANTS = {
 }
 
 
+BWD_MUTANTS = {
+    "bwd_no_decay_carry": ("g[n] *= abar; /* now dL/dh_{t-1} */", "/* carry dropped */"),
+    "bwd_dA_uses_h_t": ("const double da = g[n] * abar * delta * hprev[n];",
+                        "const double da = g[n] * abar * delta * hcur[n];"),
+    "bwd_no_softplus_derivative": ("ddt[bt * H + h] += ddelta * sig_v;", "ddt[bt * H + h] += ddelta;"),
+    "bwd_silu_derivative": ("dz[xi] = dout[xi] * y * sz * (1.0 + zv * (1.0 - sz));",
+                            "dz[xi] = dout[xi] * y * sz;"),
+    "bwd_dC_uses_h_prev": ("dC[(bt * G + grp) * N + n] += dy * hcur[n];",
+                           "dC[(bt * G + grp) * N + n] += dy * hprev[n];"),
+    "bwd_dx_no_skip": ("double dxv = D ? dy * D[h] : 0.0;", "double dxv = 0.0;"),
+    "bwd_ddelta_no_decay_term": ("ddelta += g[n] * (Bt[n] * xv + abar * an * hprev[n]);",
+                                 "ddelta += g[n] * (Bt[n] * xv);"),
+    "bwd_gate_ignored": ("const double dy = dout[xi] * gate;", "const double dy = dout[xi];"),
+}
+
+
+def _bwd_pins(lib):
+    """The backward pins (finite differences of this copy's own forward) on two cases."""
+    from test_oracle_bwd_pins import mismatches, problem
+    bad = []
+    for mode, dims in (("diag", (1, 5, 2, 1, 3, 1)), ("ssd", (1, 4, 2, 2, 2, 1))):
+        arr, dout, dfinal = problem(np.random.default_rng(9), mode, *dims)
+        bad += [f"{mode}:{n}" for n in mismatches(oracle.scan, lib.scan_bwd, arr, dout, dfinal)]
+    return bad
+
+
 def _conv_pins(conv):
     """The convolution pins against ``conv`` (numpy.convolve per channel, resume)."""
     failed = []
@@ -149,3 +175,15 @@ def test_conv_mutant_is_caught(tmp_path, name):
     old, new = CONV_MUTANTS[name]
     lib = _build_variant(tmp_path, name, old, new)
     assert _conv_pins(lib.conv_silu), f"mutant {name} passed every pin"
+
+
+def test_unmutated_backward_passes(tmp_path):
+    lib = _build_variant(tmp_path, "identity_bwd", "oracle_silu", "oracle_silu")
+    assert _bwd_pins(lib) == []
+
+
+@pytest.mark.parametrize("name", sorted(BWD_MUTANTS))
+def test_backward_mutant_is_caught(tmp_path, name):
+    old, new = BWD_MUTANTS[name]
+    lib = _build_variant(tmp_path, name, old, new)
+    assert _bwd_pins(lib), f"mutant {name} passed every pin"
