@@ -63,6 +63,8 @@ def parse():
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--conv", action="store_true",
                     help="put the width-4 causal depthwise convolution + SiLU ahead of the scan")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward pass (ssm_scan_bwd, diagonal mode) of the workload")
     ap.add_argument("--decode", action="store_true",
                     help="time single-token recurrent steps (ssm_step) at the workload's widths")
     ap.add_argument("--decode-batch", type=int, default=0,
@@ -583,6 +585,169 @@ def run_decode(args, w0):
     return 0
 
 
+def backward_bytes(w) -> int:
+    """Bytes the backward pass must move: the forward inputs and dout read, every
+    gradient written (fp32)."""
+    E = 2 if w.dtype == "bf16" else 4
+    b, T, H, N, G = w.batch, w.seqlen, w.nheads, w.dstate, w.ngroups
+    nbytes = b * T * H * E * (3 + (1 if w.gate else 0))          # x, dt, dout, z
+    nbytes += 2 * b * T * G * N * E                              # B, C
+    nbytes += b * T * H * 4 * (2 + (1 if w.gate else 0))         # dx, ddt, dz
+    nbytes += 2 * b * T * G * N * 4                              # dB, dC
+    nbytes += 2 * H * N * 4 + 4 * H * 4                          # A, dA, D, dD, dt_bias, ddt_bias
+    nbytes += 2 * b * H * N * 4                                  # dfinal, dinitial_state
+    return int(nbytes)
+
+
+def run_backward(args, w):
+    """ssm_scan_bwd over the workload; one step = one backward call."""
+    import selective_state_space_143_b300 as ssm
+    dist, world, rank, local = dist_setup()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (there is no CPU path)")
+    if w.mode != "diag":
+        raise SystemExit("the backward pass is built for the diagonal mode")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    inp = host_inputs(w)
+    d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+    gen = torch.Generator().manual_seed(w.seed + 100)
+    dout_h = torch.randn(d["x"].shape, generator=gen).to(d["x"].dtype)
+    dfin_h = torch.randn((w.batch, w.nheads, w.dstate), generator=gen)
+    dout, dfin = dout_h.to(dev), dfin_h.to(dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    s = ssm.make_shape(d["x"], d["A"], d["B"])
+    ws = torch.empty(max(1, int(ssm._lib.load().ssm_scan_bwd_workspace_size(ctypes_byref(s)))),
+                     dtype=torch.uint8, device=dev)
+
+    def step():
+        return ssm.scan_bwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["z"], d["dt_bias"],
+                            dout=dout, dfinal_state=dfin, workspace=ws, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    if not args.quick:
+        clocks.start()
+        t_end = time.perf_counter() + 1.0
+        while time.perf_counter() < t_end:
+            for _ in range(10):
+                step()
+            torch.cuda.synchronize()
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    barrier(dist)
+    torch.cuda.synchronize()
+    n0 = ssm.launch_count()
+    torch.cuda._sleep(int(min(2e9, 2e6 + K * 4e5)))
+    for i in range(K):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    launches = ssm.launch_count() - n0
+    barrier(dist)
+    ms_step = max_over_ranks(dist, sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / K)
+    clk = clocks.stop() if not args.quick else {"sm_mhz": None, "sm_max_mhz": None,
+                                               "reasons": ["not sampled (--quick)"]}
+    units = w.token_channels * world
+    value = units / (ms_step * 1e-3) / 1e9
+    peaks, peak_kind = measured_peaks()
+    nbytes = backward_bytes(w)
+    gbs = nbytes / (ms_step * 1e-3) / 1e9
+    roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+            "kernel": "ssm_scan_bwd (zeroing + scan_bwd_kernel)",
+            "algorithmic_bytes_per_launch": nbytes, "peak_source": peak_kind}
+    sm_mhz = float(peaks.get("sm_max_mhz", 2032.0))
+    exps = 3.0 * w.token_channels * w.dstate  # the decay is formed in three sweeps
+    roof["sfu"] = {"achieved": exps / (ms_step * 1e-3), "peak": 148 * 32 * sm_mhz * 1e6,
+                   "unit": "exp/s", "frac": exps / (ms_step * 1e-3) / (148 * 32 * sm_mhz * 1e6),
+                   "note": "three exponentials per state entry and step (forward sweep, "
+                           "recompute, reverse); peak = 148 SMs x 32/clk x max SM clock"}
+    cpu = e2e = None
+    if not args.quick:
+        host = {k: (None if v is None else v.pin_memory()) for k, v in inp.items()}
+        dout_p, dfin_p = dout_h.pin_memory(), dfin_h.pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+        h2d += dout_p.numel() * dout_p.element_size() + dfin_p.numel() * 4
+        outs_h = None
+
+        def e2e_step():
+            nonlocal outs_h
+            dd = {k: (None if v is None else v.to(dev, non_blocking=True)) for k, v in host.items()}
+            g = ssm.scan_bwd(dd["x"], dd["dt"], dd["A"], dd["B"], dd["C"], dd["D"], dd["z"],
+                             dd["dt_bias"], dout=dout_p.to(dev, non_blocking=True),
+                             dfinal_state=dfin_p.to(dev, non_blocking=True), workspace=ws,
+                             stream=stream)
+            if outs_h is None:
+                outs_h = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory()
+                          for k, v in g.items() if v is not None}
+            for k, v in outs_h.items():
+                v.copy_(g[k], non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        d2h = sum(v.numel() * v.element_size() for v in outs_h.values())
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1) / K)
+        e2e = {"value": units / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+        if rank == 0:
+            import oracle
+            # the oracle's backward over the first sequence and a block of channels
+            nch = min(w.nheads, 64)
+            sub = {k: (None if v is None else v) for k, v in inp.items()}
+            cut = lambda t: t[:1, :, :nch].contiguous()
+            sl = dict(x=cut(sub["x"]), dt=cut(sub["dt"]), A=sub["A"][:nch], B=sub["B"][:1],
+                      C=sub["C"][:1], D=None if sub["D"] is None else sub["D"][:nch],
+                      z=None if sub["z"] is None else cut(sub["z"]),
+                      dt_bias=None if sub["dt_bias"] is None else sub["dt_bias"][:nch])
+            t_used, reps = 0.0, 0
+            while t_used < args.cpu_seconds and reps < 1000:
+                t0 = time.perf_counter()
+                oracle.scan_bwd(**sl, dout=dout_h[:1, :, :nch], dfinal=dfin_h[:1, :nch])
+                t_used += time.perf_counter() - t0
+                reps += 1
+            cpu = {"value": reps * w.seqlen * nch / t_used / 1e9, "unit": UNIT, "cores": 1,
+                   "kind": "oracle", "seconds": t_used,
+                   "sample": f"{reps} oracle backward passes over 1 sequence x {nch} channels "
+                             f"x L {w.seqlen} (fp64, one thread)"}
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": f"{w.name}-backward: gradients of every input of "
+                                   f"{DESCRIPTIONS[w.name]}, from dout and dfinal_state",
+                       "l2": "flushed before every timed step (256 MB write)",
+                       "parallelism": f"replicas x{world} (independent batches)"},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
+            "gpu_launches": int(launches),
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def ctypes_byref(s):
+    import ctypes
+    return ctypes.byref(s)
+
+
 def main():
     args = parse()
     from selective_state_space_143_b300.inputs import WORKLOADS
@@ -591,6 +756,8 @@ def main():
         return run_reference(args, w)
     if args.decode:
         return run_decode(args, w)
+    if args.backward:
+        return run_backward(args, w)
     return run_ours(args, w)
 
 

@@ -14,7 +14,7 @@ import torch
 from . import _lib
 from ._lib import SsmError, ssm_conv, ssm_shape
 
-__all__ = ["scan_fwd", "step", "workspace_size", "make_shape", "launch_count", "SsmError",
+__all__ = ["scan_fwd", "scan_bwd", "step", "workspace_size", "make_shape", "launch_count", "SsmError",
            "ssm_shape"]
 
 _DTYPES = {torch.float32: _lib.SSM_F32, torch.bfloat16: _lib.SSM_BF16}
@@ -176,6 +176,52 @@ def scan_fwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, *, out=None, final_st
     if rc != _lib.SSM_OK:
         raise SsmError(rc, "ssm_scan_fwd")
     return (out, final_state) if want_state else out
+
+
+def scan_bwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, *, dout, dfinal_state=None,
+             initial_state=None, workspace=None, stream=None):
+    """Gradients of the diagonal-mode scan (``scan_fwd`` with a 2-D A).
+
+    ``dout`` is the gradient of the output (x's shape and dtype), ``dfinal_state`` that of
+    the final state (float32, optional).  Returns a dict of float32 tensors: dx, ddt, dA,
+    dB, dC (B's shape), and dD, dz, ddt_bias, dinitial_state where the matching input was
+    given (dinitial_state always).
+    """
+    s = make_shape(x, A, B, 0)
+    dev = x.device
+    if dev.type != "cuda":
+        raise ValueError("scan_bwd runs on CUDA tensors only")
+    if s.mode != _lib.SSM_MODE_DIAG:
+        raise SsmError(_lib.SSM_ERR_UNSUPPORTED, "ssm_scan_bwd (diagonal mode only)")
+    b, T, H, N = s.batch, s.seqlen, s.nheads, s.dstate
+    for name, t, shp, dt_ in (("x", x, x.shape, x.dtype), ("dt", dt, (b, T, H), x.dtype),
+                              ("A", A, (H, N), torch.float32), ("B", B, B.shape, x.dtype),
+                              ("C", C, B.shape, x.dtype), ("D", D, (H,), torch.float32),
+                              ("z", z, x.shape, x.dtype), ("dt_bias", dt_bias, (H,), torch.float32),
+                              ("dout", dout, x.shape, x.dtype),
+                              ("dfinal_state", dfinal_state, (b, H, N), torch.float32),
+                              ("initial_state", initial_state, (b, H, N), torch.float32)):
+        _check(name, t, shp, dt_, dev)
+    f32 = dict(device=dev, dtype=torch.float32)
+    g = {"dx": torch.empty(x.shape, **f32), "ddt": torch.empty((b, T, H), **f32),
+         "dA": torch.empty((H, N), **f32), "dB": torch.empty(B.shape, **f32),
+         "dC": torch.empty(B.shape, **f32),
+         "dD": None if D is None else torch.empty((H,), **f32),
+         "dz": None if z is None else torch.empty(x.shape, **f32),
+         "ddt_bias": None if dt_bias is None else torch.empty((H,), **f32),
+         "dinitial_state": torch.empty((b, H, N), **f32)}
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    with torch.cuda.device(dev):
+        rc = _lib.load().ssm_scan_bwd(
+            *(_ptr(t) for t in (x, dt, A, B, C, D, z, dt_bias, initial_state, dout, dfinal_state,
+                                g["dx"], g["ddt"], g["dA"], g["dB"], g["dC"], g["dD"], g["dz"],
+                                g["ddt_bias"], g["dinitial_state"])),
+            ctypes.byref(s), _ptr(workspace), ws_bytes, ctypes.c_void_p(stream.cuda_stream))
+    if rc != _lib.SSM_OK:
+        raise SsmError(rc, "ssm_scan_bwd")
+    return g
 
 
 def step(x, dt, A, B, C, D=None, z=None, dt_bias=None, *, state, out=None, stream=None,

@@ -29,7 +29,8 @@ SSM_BF16 = 1
 # Every function declared in include/ssm_scan.h.
 EXPORTED = ("ssm_scan_fwd", "ssm_scan_fwd_ws", "ssm_scan_workspace_size", "ssm_scan_fwd_noalloc",
             "ssm_scan_fwd_state", "ssm_step", "ssm_scan_fwd_conv", "ssm_scan_conv_workspace_size",
-            "ssm_step_conv", "ssm_strerror", "ssm_kernel_launch_count", "ssm_abi_version")
+            "ssm_step_conv", "ssm_scan_bwd", "ssm_scan_bwd_workspace_size", "ssm_strerror",
+            "ssm_kernel_launch_count", "ssm_abi_version")
 
 
 class ssm_shape(ctypes.Structure):
@@ -99,6 +100,10 @@ def load() -> ctypes.CDLL:
         lib.ssm_scan_conv_workspace_size.restype = ctypes.c_size_t
         lib.ssm_step_conv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, cp, vp, vp, sp, vp]
         lib.ssm_step_conv.restype = ctypes.c_int
+        lib.ssm_scan_bwd.argtypes = [vp] * 20 + [sp, vp, ctypes.c_size_t, vp]
+        lib.ssm_scan_bwd.restype = ctypes.c_int
+        lib.ssm_scan_bwd_workspace_size.argtypes = [sp]
+        lib.ssm_scan_bwd_workspace_size.restype = ctypes.c_size_t
         lib.ssm_scan_workspace_size.argtypes = [sp]
         lib.ssm_scan_workspace_size.restype = ctypes.c_size_t
         lib.ssm_strerror.argtypes = [ctypes.c_int]

@@ -325,6 +325,64 @@ int ssm_scan_fwd_conv(const void* x, const void* dt, const float* A, const void*
     return run_with(a, shape->mode, workspace, workspace_bytes, (cudaStream_t)stream);
 }
 
+size_t ssm_scan_bwd_workspace_size(const ssm_shape* shape) {
+    if (check_shape(shape) != SSM_OK || shape->mode != SSM_MODE_DIAG) return (size_t)-1;
+    const ScanArgs a = make_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                                 nullptr, nullptr, nullptr, shape);
+    return scan_bwd_workspace_bytes(a);
+}
+
+int ssm_scan_bwd(const void* x, const void* dt, const float* A, const void* B, const void* C,
+                 const float* D, const void* z, const float* dt_bias, const float* initial_state,
+                 const void* dout, const float* dfinal_state, float* dx, float* ddt, float* dA,
+                 float* dB, float* dC, float* dD, float* dz, float* ddt_bias,
+                 float* dinitial_state, const ssm_shape* shape, void* workspace,
+                 size_t workspace_bytes, ssm_stream_t stream) {
+    int rc = check_args(x, dt, A, B, C, D, z, dt_bias, dx, nullptr, shape, initial_state);
+    if (rc != SSM_OK) return rc;
+    if (shape->mode != SSM_MODE_DIAG) return SSM_ERR_UNSUPPORTED;
+    const bool empty = shape->batch == 0 || shape->seqlen == 0;
+    if (!dA || (!empty && (!dout || !dx || !ddt || !dB || !dC))) return SSM_ERR_NULL;
+    const void* outs[] = {dout, dfinal_state, dx, ddt, dA, dB, dC, dD, dz, ddt_bias, dinitial_state};
+    for (const void* p : outs)
+        if (!aligned16(p)) return SSM_ERR_ALIGN;
+    ScanBwdArgs s;
+    s.fwd = make_args(x, dt, A, B, C, D, z, dt_bias, nullptr, nullptr, shape);
+    s.fwd.initial_state = initial_state;
+    s.dout = dout;
+    s.dfinal = dfinal_state;
+    s.dx = dx;
+    s.ddt = ddt;
+    s.dA = dA;
+    s.dB = dB;
+    s.dC = dC;
+    s.dD = D ? dD : nullptr;
+    s.dz = z ? dz : nullptr;
+    s.ddt_bias = dt_bias ? ddt_bias : nullptr;
+    s.dinit = dinitial_state;
+    const size_t need = scan_bwd_workspace_bytes(s.fwd);
+    cudaStream_t st = (cudaStream_t)stream;
+    void* ws = workspace;
+    bool owned = false;
+    if (need > 0 && !empty) {
+        if (workspace == nullptr && workspace_bytes == 0) {
+            if (cudaMallocAsync(&ws, need, st) != cudaSuccess) {
+                (void)cudaGetLastError();
+                return SSM_ERR_ALLOC;
+            }
+            owned = true;
+        } else if (workspace == nullptr || workspace_bytes < need) {
+            return SSM_ERR_ALLOC;
+        } else if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) {
+            return SSM_ERR_ALIGN;
+        }
+    }
+    const cudaError_t e = scan_bwd_launch(s, ws, st);
+    int r = e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+    if (owned && cudaFreeAsync(ws, st) != cudaSuccess && r == SSM_OK) r = SSM_ERR_CUDA;
+    return r;
+}
+
 int ssm_step_conv(const void* x, const void* dt, const float* A, const void* B, const void* C,
                   const float* D, const void* z, const float* dt_bias, const ssm_conv* conv,
                   float* state, void* out, const ssm_shape* shape, ssm_stream_t stream) {

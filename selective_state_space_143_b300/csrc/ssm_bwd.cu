@@ -1,0 +1,313 @@
+// Backward pass of the diagonal (Mamba-1) selective scan: gradients of the inputs from
+// the gradient of the output (and optionally of the final state).
+//
+// The pages give the forward recurrence only ("Mamba-2：把状态空间模型和 Attention 统一到
+// 一个数学框架里", 背景问题 / 第一步; training runs it in parallel, "训练时并行化"); the
+// reverse-mode derivatives follow from it.  Per channel c, with v_t = dt_t + dt_bias,
+// Delta_t = softplus(v_t), a_t[n] = exp(Delta_t A[c,n]) and g_t = dL/dh_t:
+//   dy_t   = dout_t SiLU(z_t)                      dz_t = dout_t y_t SiLU'(z_t)
+//   g_t    = dy_t C_t + a_{t+1} g_{t+1}            (g starts from dfinal)
+//   dx_t   = dy_t D + sum_n g_t Delta_t B_t        dB_t += g_t Delta_t x_t,  dC_t += dy_t h_t
+//   dDelta = sum_n g_t (B_t x_t + a_t A h_{t-1})   dA += g_t a_t Delta_t h_{t-1}
+//   ddt_t  = dDelta sigmoid(v_t)                   ddt_bias += ddt_t,  dD += dy_t x_t
+//   dinit  = a_0 g_0
+//
+// Design: LPC lanes of a warp share one channel, each lane R state entries (N up to 64).
+// A forward sweep stores the state entering every segment of kSeg steps (the only
+// scratch); the reverse sweep walks the segments backwards, recomputes the segment's
+// states into registers from its checkpoint and runs the adjoint recurrence over them.
+// Sums over n use shuffles inside the LPC lanes; the dB and dC contributions of the
+// block's channels (one group) are summed in shared memory per segment and added to
+// global memory once per block and step.  All arithmetic is fp32 with CUDA's accurate
+// exp/log1p; every gradient is written in fp32.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "ssm_device.cuh"
+#include "ssm_internal.h"
+
+namespace ssm {
+namespace {
+
+constexpr int kBwdThreads = 256;
+constexpr int kSeg = 16;  // steps per checkpoint segment
+
+template <typename T>
+struct BwdArgs {
+    const T* x;
+    const T* dt;
+    const T* z;
+    const T* B;
+    const T* C;
+    const T* dout;
+    const float* A;
+    const float* D;
+    const float* dt_bias;
+    const float* init;
+    const float* dfinal;
+    float* dx;
+    float* ddt;
+    float* dA;
+    float* dB;
+    float* dC;
+    float* dD;
+    float* dz;
+    float* ddt_bias;
+    float* dinit;
+    float* ckpt;  // (b, nseg, dim, N): state entering each segment
+    int64_t L, dim, N, G, cpg;  // L: sequence length
+    int nseg, tiles_per_group;
+};
+
+__device__ __forceinline__ float sigmoidf_(float v) { return 1.0f / (1.0f + expf(-v)); }
+
+template <int LPC>
+__device__ __forceinline__ float lane_sum(float v) {
+#pragma unroll
+    for (int o = LPC / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o, LPC);
+    return v;
+}
+
+// grid (G * tiles_per_group, 1, batch); LPC lanes x R entries per channel, CPB channels.
+template <typename T, int LPC, int R>
+__global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> a) {
+    constexpr int CPB = kBwdThreads / LPC;
+    constexpr int NP = LPC * R;  // padded state width
+    __shared__ float s_dB[kSeg][NP], s_dC[kSeg][NP];
+    const int tid = threadIdx.x;
+    const int lane = tid % LPC;
+    const int group = blockIdx.x / a.tiles_per_group;
+    const int64_t c_begin = (int64_t)group * a.cpg + (int64_t)(blockIdx.x % a.tiles_per_group) * CPB;
+    const int64_t c_end = (int64_t)(group + 1) * a.cpg;
+    const int64_t c = c_begin + tid / LPC;
+    const bool c_ok = c < c_end;
+    const int64_t b = blockIdx.z;
+    const int64_t L = a.L, dim = a.dim, N = a.N, G = a.G;
+
+    float Ar[R];
+    int nr[R];
+    bool nok[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        nr[r] = lane + r * LPC;
+        nok[r] = c_ok && nr[r] < N;
+        Ar[r] = nok[r] ? a.A[c * N + nr[r]] : 0.0f;
+    }
+    const float bias = (c_ok && a.dt_bias) ? a.dt_bias[c] : 0.0f;
+    const float Dc = (c_ok && a.D) ? a.D[c] : 0.0f;
+
+    auto row = [&](int64_t t) { return (b * L + t) * dim + c; };
+    auto bc = [&](int64_t t) { return (b * L + t) * G * N + (int64_t)group * N; };
+    auto delta_of = [&](int64_t t, float& v) {
+        v = c_ok ? to_f32<T>(a.dt[row(t)]) + bias : 0.0f;
+        return c_ok ? softplus_precise(v) : 0.0f;
+    };
+
+    // forward sweep: checkpoints of the state entering every segment
+    float h[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) h[r] = (nok[r] && a.init) ? a.init[(b * dim + c) * N + nr[r]] : 0.0f;
+    for (int seg = 0; seg < a.nseg; ++seg) {
+        const int64_t t0 = (int64_t)seg * kSeg;
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+            if (nok[r]) a.ckpt[((b * a.nseg + seg) * dim + c) * N + nr[r]] = h[r];
+        const int len = (int)min((int64_t)kSeg, L - t0);
+        for (int j = 0; j < len; ++j) {
+            const int64_t t = t0 + j;
+            float v;
+            const float de = delta_of(t, v);
+            const float u = c_ok ? de * to_f32<T>(a.x[row(t)]) : 0.0f;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const float Bv = nok[r] ? to_f32<T>(a.B[bc(t) + nr[r]]) : 0.0f;
+                h[r] = fmaf(expf(de * Ar[r]), h[r], u * Bv);
+            }
+        }
+    }
+
+    // reverse sweep
+    float g[R], dA_acc[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        g[r] = (nok[r] && a.dfinal) ? a.dfinal[(b * dim + c) * N + nr[r]] : 0.0f;
+        dA_acc[r] = 0.0f;
+    }
+    float dD_acc = 0.0f, dbias_acc = 0.0f;
+    for (int seg = a.nseg - 1; seg >= 0; --seg) {
+        const int64_t t0 = (int64_t)seg * kSeg;
+        const int len = (int)min((int64_t)kSeg, L - t0);
+        for (int i = tid; i < kSeg * NP; i += kBwdThreads) {
+            (&s_dB[0][0])[i] = 0.0f;
+            (&s_dC[0][0])[i] = 0.0f;
+        }
+        // the segment's states h_t (after step t), recomputed from the checkpoint
+        float hs[kSeg][R], h0[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) h0[r] = nok[r] ? a.ckpt[((b * a.nseg + seg) * dim + c) * N + nr[r]] : 0.0f;
+#pragma unroll
+        for (int j = 0; j < kSeg; ++j) {
+            if (j < len) {
+                const int64_t t = t0 + j;
+                float v;
+                const float de = delta_of(t, v);
+                const float u = c_ok ? de * to_f32<T>(a.x[row(t)]) : 0.0f;
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const float Bv = nok[r] ? to_f32<T>(a.B[bc(t) + nr[r]]) : 0.0f;
+                    const float prev = j == 0 ? h0[r] : hs[j - 1][r];
+                    hs[j][r] = fmaf(expf(de * Ar[r]), prev, u * Bv);
+                }
+            }
+        }
+        __syncthreads();  // shared accumulators cleared
+#pragma unroll
+        for (int j = kSeg - 1; j >= 0; --j) {
+            if (j >= len) continue;
+            const int64_t t = t0 + j;
+            float v;
+            const float de = delta_of(t, v);
+            const float xv = c_ok ? to_f32<T>(a.x[row(t)]) : 0.0f;
+            const float dov = c_ok ? to_f32<T>(a.dout[row(t)]) : 0.0f;
+            float Bv[R], Cv[R], av[R];
+            float yp = 0.0f;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                Bv[r] = nok[r] ? to_f32<T>(a.B[bc(t) + nr[r]]) : 0.0f;
+                Cv[r] = nok[r] ? to_f32<T>(a.C[bc(t) + nr[r]]) : 0.0f;
+                av[r] = expf(de * Ar[r]);
+                yp = fmaf(Cv[r], hs[j][r], yp);
+            }
+            const float y = lane_sum<LPC>(yp) + Dc * xv;
+            float gate = 1.0f, dzv = 0.0f;
+            if (a.z) {
+                const float zv = c_ok ? to_f32<T>(a.z[row(t)]) : 0.0f;
+                const float sz = sigmoidf_(zv);
+                gate = zv * sz;
+                dzv = dov * y * sz * (1.0f + zv * (1.0f - sz));
+            }
+            const float dy = dov * gate;
+            float dxp = 0.0f, ddp = 0.0f;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const float hp = j == 0 ? h0[r] : hs[j - 1][r];
+                g[r] = fmaf(dy, Cv[r], g[r]);
+                dxp = fmaf(g[r] * de, Bv[r], dxp);
+                ddp = fmaf(g[r], fmaf(av[r] * Ar[r], hp, Bv[r] * xv), ddp);
+                dA_acc[r] = fmaf(g[r] * av[r] * de, hp, dA_acc[r]);
+                if (nok[r]) {
+                    atomicAdd(&s_dB[j][nr[r]], g[r] * de * xv);
+                    atomicAdd(&s_dC[j][nr[r]], dy * hs[j][r]);
+                }
+                g[r] *= av[r];  // dL/dh_{t-1}
+            }
+            const float dxs = lane_sum<LPC>(dxp);
+            const float dds = lane_sum<LPC>(ddp);
+            if (c_ok && lane == 0) {
+                a.dx[row(t)] = fmaf(dy, Dc, dxs);
+                const float dv = dds * sigmoidf_(v);
+                a.ddt[row(t)] = dv;
+                dbias_acc += dv;
+                dD_acc = fmaf(dy, xv, dD_acc);
+                if (a.z) a.dz[row(t)] = dzv;
+            }
+        }
+        __syncthreads();  // shared accumulators complete
+        for (int i = tid; i < len * NP; i += kBwdThreads) {
+            const int j = i / NP, n = i % NP;
+            if (n < N) {
+                const int64_t o = bc(t0 + j) + n;
+                atomicAdd(&a.dB[o], s_dB[j][n]);
+                atomicAdd(&a.dC[o], s_dC[j][n]);
+            }
+        }
+        __syncthreads();  // read before the next segment clears them
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+        if (nok[r]) {
+            if (a.dinit) a.dinit[(b * dim + c) * N + nr[r]] = g[r];
+            atomicAdd(&a.dA[c * N + nr[r]], dA_acc[r]);
+        }
+    if (c_ok && lane == 0) {
+        if (a.dD) atomicAdd(&a.dD[c], dD_acc);
+        if (a.ddt_bias) atomicAdd(&a.ddt_bias[c], dbias_acc);
+    }
+}
+
+template <typename T, int LPC, int R>
+cudaError_t launch_bwd(const BwdArgs<T>& a, int64_t batch, cudaStream_t stream) {
+    constexpr int CPB = kBwdThreads / LPC;
+    BwdArgs<T> k = a;
+    k.tiles_per_group = (int)((a.cpg + CPB - 1) / CPB);
+    const dim3 grid((unsigned)(a.G * k.tiles_per_group), 1, (unsigned)batch);
+    scan_bwd_kernel<T, LPC, R><<<grid, kBwdThreads, 0, stream>>>(k);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t bwd_typed(const ScanBwdArgs& s, void* ws, cudaStream_t stream) {
+    const ScanArgs& f = s.fwd;
+    BwdArgs<T> a;
+    a.x = (const T*)f.x;
+    a.dt = (const T*)f.dt;
+    a.z = (const T*)f.z;
+    a.B = (const T*)f.B;
+    a.C = (const T*)f.C;
+    a.dout = (const T*)s.dout;
+    a.A = f.A;
+    a.D = f.D;
+    a.dt_bias = f.dt_bias;
+    a.init = f.initial_state;
+    a.dfinal = s.dfinal;
+    a.dx = s.dx;
+    a.ddt = s.ddt;
+    a.dA = s.dA;
+    a.dB = s.dB;
+    a.dC = s.dC;
+    a.dD = s.dD;
+    a.dz = s.dz;
+    a.ddt_bias = s.ddt_bias;
+    a.dinit = s.dinit;
+    a.ckpt = (float*)ws;
+    a.L = f.seqlen;
+    a.dim = f.nheads;
+    a.N = f.dstate;
+    a.G = f.ngroups;
+    a.cpg = f.nheads / f.ngroups;
+    a.nseg = (int)((f.seqlen + kSeg - 1) / kSeg);
+    a.tiles_per_group = 0;
+    // lanes per channel: the state width padded to a power of two, at most a warp
+    if (f.dstate <= 4) return launch_bwd<T, 4, 1>(a, f.batch, stream);
+    if (f.dstate <= 8) return launch_bwd<T, 8, 1>(a, f.batch, stream);
+    if (f.dstate <= 16) return launch_bwd<T, 16, 1>(a, f.batch, stream);
+    if (f.dstate <= 32) return launch_bwd<T, 32, 1>(a, f.batch, stream);
+    return launch_bwd<T, 32, 2>(a, f.batch, stream);
+}
+
+}  // namespace
+
+size_t scan_bwd_workspace_bytes(const ScanArgs& a) {
+    const int64_t nseg = (a.seqlen + kSeg - 1) / kSeg;
+    return align_up((size_t)a.batch * nseg * a.nheads * a.dstate * sizeof(float), 256);
+}
+
+cudaError_t scan_bwd_launch(const ScanBwdArgs& s, void* ws, cudaStream_t stream) {
+    const ScanArgs& f = s.fwd;
+    // accumulated gradients start from zero
+    const size_t acc_bytes[] = {(size_t)f.nheads * f.dstate * 4, (size_t)f.batch * f.seqlen * f.ngroups * f.dstate * 4,
+                                (size_t)f.batch * f.seqlen * f.ngroups * f.dstate * 4, (size_t)f.nheads * 4,
+                                (size_t)f.nheads * 4};
+    float* acc[] = {s.dA, s.dB, s.dC, s.dD, s.ddt_bias};
+    for (int i = 0; i < 5; ++i)
+        if (acc[i] && acc_bytes[i]) {
+            const cudaError_t e = cudaMemsetAsync(acc[i], 0, acc_bytes[i], stream);
+            if (e != cudaSuccess) return e;
+        }
+    if (f.batch == 0) return cudaSuccess;
+    if (f.dtype == 1) return bwd_typed<__nv_bfloat16>(s, ws, stream);
+    return bwd_typed<float>(s, ws, stream);
+}
+
+}  // namespace ssm

@@ -47,6 +47,17 @@ cudaError_t ssd_launch(const ScanArgs& a, void* ws, cudaStream_t stream);
 // out (batch, nheads, headdim) written; diag_a selects A of shape (nheads, dstate).
 cudaError_t step_launch(const ScanArgs& a, bool diag_a, float* state, cudaStream_t stream);
 
+// Backward pass of the diagonal scan: the forward arguments plus the incoming gradients
+// and the gradient outputs (fp32; dA, dB, dC, dD and ddt_bias are zeroed, then summed).
+struct ScanBwdArgs {
+    ScanArgs fwd;
+    const void* dout;
+    const float* dfinal;
+    float *dx, *ddt, *dA, *dB, *dC, *dD, *dz, *ddt_bias, *dinit;
+};
+size_t scan_bwd_workspace_bytes(const ScanArgs& a);
+cudaError_t scan_bwd_launch(const ScanBwdArgs& s, void* ws, cudaStream_t stream);
+
 // Convolution + SiLU of x into xc (same shape, fp32), and the last conv_k-1 inputs into
 // a.x_last; used ahead of the SSD kernels.  x' is kept in fp32: it is an intermediate,
 // and rounding it to bf16 would add an input error the scan's tolerance does not allow.

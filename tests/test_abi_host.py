@@ -242,3 +242,28 @@ def test_step_conv_state_may_be_updated_in_place():
     assert lib.ssm_step_conv(vp(1 << 12), vp(2 << 12), vp(3 << 12), vp(4 << 12), vp(5 << 12),
                              None, None, None, ctypes.byref(c), vp(6 << 20), vp(7 << 20),
                              ctypes.byref(s), None) == _lib.SSM_ERR_SHAPE
+
+
+def test_backward_argument_errors():
+    lib = _lib.load()
+    vp = ctypes.c_void_p
+    s = _shape()
+    ptrs = [vp((i + 1) << 12) for i in range(20)]
+
+    def call(shape, **over):
+        args = list(ptrs)
+        names = ["x", "dt", "A", "B", "C", "D", "z", "dt_bias", "init", "dout", "dfinal", "dx",
+                 "ddt", "dA", "dB", "dC", "dD", "dz", "ddt_bias", "dinit"]
+        for k, v in over.items():
+            args[names.index(k)] = None if v is None else vp(v)
+        return lib.ssm_scan_bwd(*args, ctypes.byref(shape), None, 0, None)
+
+    ssd = _shape(mode=1, nheads=8, headdim=64, dstate=128, chunk=64)
+    assert call(ssd) == _lib.SSM_ERR_UNSUPPORTED
+    assert lib.ssm_scan_bwd_workspace_size(ctypes.byref(ssd)) == BAD
+    assert call(s, dx=None) == _lib.SSM_ERR_NULL
+    assert call(s, dout=None) == _lib.SSM_ERR_NULL
+    assert call(s, dA=None) == _lib.SSM_ERR_NULL
+    assert call(s, dB=(15 << 12) + 8) == _lib.SSM_ERR_ALIGN
+    n = lib.ssm_scan_bwd_workspace_size(ctypes.byref(s))
+    assert n == 2 * (64 // 16) * 64 * 16 * 4   # the state every 16 steps
