@@ -16,10 +16,12 @@
 // A forward sweep stores the state entering every segment of kSeg steps (the only
 // scratch); the reverse sweep walks the segments backwards, recomputes the segment's
 // states into registers from its checkpoint and runs the adjoint recurrence over them.
-// Sums over n use shuffles inside the LPC lanes; the dB and dC contributions of the
-// block's channels (one group) are summed in shared memory per segment and added to
-// global memory once per block and step.  All arithmetic is fp32 with CUDA's accurate
-// exp/log1p; every gradient is written in fp32.
+// The per-step scalars of a channel are computed once per segment, spread over its
+// lanes, and shuffled to the sweeps; sums over n use shuffles inside the LPC lanes; the
+// dB and dC terms of the block's channels (one group) go to shared memory and are summed
+// once per segment, then added to global memory once per block and step.  Arithmetic is
+// fp32 (CUDA's accurate exp/log1p for fp32 inputs, the SFU exp2 for bf16 inputs, as in
+// the forward); every gradient is written in fp32.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -69,17 +71,25 @@ __device__ __forceinline__ float lane_sum(float v) {
 }
 
 // grid (G * tiles_per_group, 1, batch); LPC lanes x R entries per channel, CPB channels.
+// The per-step scalars of a channel (Delta, Delta x, dy, the SiLU' factor, sigmoid(v)) are
+// computed once per segment, spread over the channel's lanes (lane j % LPC holds step j),
+// and fetched with shuffles inside the sequential sweeps.
 template <typename T, int LPC, int R>
 __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> a) {
+    constexpr bool PRECISE = sizeof(T) == 4;
     constexpr int CPB = kBwdThreads / LPC;
-    constexpr int NP = LPC * R;  // padded state width
-    __shared__ float s_dB[kSeg][NP], s_dC[kSeg][NP];
+    constexpr int NP = LPC * R;                    // padded state width
+    constexpr int SPL = (kSeg + LPC - 1) / LPC;    // steps per lane in the per-step pass
+    extern __shared__ float s_acc[];               // [2][kSeg][CPB][NP]: dB and dC terms
+    float* s_dB = s_acc;
+    float* s_dC = s_acc + kSeg * CPB * NP;
     const int tid = threadIdx.x;
     const int lane = tid % LPC;
+    const int cc = tid / LPC;  // channel within the block
     const int group = blockIdx.x / a.tiles_per_group;
     const int64_t c_begin = (int64_t)group * a.cpg + (int64_t)(blockIdx.x % a.tiles_per_group) * CPB;
     const int64_t c_end = (int64_t)(group + 1) * a.cpg;
-    const int64_t c = c_begin + tid / LPC;
+    const int64_t c = c_begin + cc;
     const bool c_ok = c < c_end;
     const int64_t b = blockIdx.z;
     const int64_t L = a.L, dim = a.dim, N = a.N, G = a.G;
@@ -91,17 +101,16 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
     for (int r = 0; r < R; ++r) {
         nr[r] = lane + r * LPC;
         nok[r] = c_ok && nr[r] < N;
-        Ar[r] = nok[r] ? a.A[c * N + nr[r]] : 0.0f;
+        Ar[r] = nok[r] ? a.A[c * N + nr[r]] * (PRECISE ? 1.0f : kLog2e) : 0.0f;
     }
     const float bias = (c_ok && a.dt_bias) ? a.dt_bias[c] : 0.0f;
     const float Dc = (c_ok && a.D) ? a.D[c] : 0.0f;
+    auto decay = [&](float de, int r) { return PRECISE ? expf(de * Ar[r]) : ex2(de * Ar[r]); };
+    auto Aval = [&](int r) { return PRECISE ? Ar[r] : Ar[r] * (1.0f / kLog2e); };
 
     auto row = [&](int64_t t) { return (b * L + t) * dim + c; };
     auto bc = [&](int64_t t) { return (b * L + t) * G * N + (int64_t)group * N; };
-    auto delta_of = [&](int64_t t, float& v) {
-        v = c_ok ? to_f32<T>(a.dt[row(t)]) + bias : 0.0f;
-        return c_ok ? softplus_precise(v) : 0.0f;
-    };
+    auto fetch = [&](const float (&v)[SPL], int j) { return __shfl_sync(0xffffffffu, v[j / LPC], j % LPC, LPC); };
 
     // forward sweep: checkpoints of the state entering every segment
     float h[R];
@@ -113,15 +122,24 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
         for (int r = 0; r < R; ++r)
             if (nok[r]) a.ckpt[((b * a.nseg + seg) * dim + c) * N + nr[r]] = h[r];
         const int len = (int)min((int64_t)kSeg, L - t0);
-        for (int j = 0; j < len; ++j) {
-            const int64_t t = t0 + j;
-            float v;
-            const float de = delta_of(t, v);
-            const float u = c_ok ? de * to_f32<T>(a.x[row(t)]) : 0.0f;
+        float pde[SPL], pu[SPL];
+#pragma unroll
+        for (int k = 0; k < SPL; ++k) {
+            const int j = lane + LPC * k;
+            pde[k] = pu[k] = 0.0f;
+            if (c_ok && j < len) {
+                pde[k] = softplus_t<PRECISE>(to_f32<T>(a.dt[row(t0 + j)]) + bias);
+                pu[k] = pde[k] * to_f32<T>(a.x[row(t0 + j)]);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kSeg; ++j) {
+            if (j >= len) break;
+            const float de = fetch(pde, j), u = fetch(pu, j);
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                const float Bv = nok[r] ? to_f32<T>(a.B[bc(t) + nr[r]]) : 0.0f;
-                h[r] = fmaf(expf(de * Ar[r]), h[r], u * Bv);
+                const float Bv = nok[r] ? to_f32<T>(a.B[bc(t0 + j) + nr[r]]) : 0.0f;
+                h[r] = fmaf(decay(de, r), h[r], u * Bv);
             }
         }
     }
@@ -133,13 +151,33 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
         g[r] = (nok[r] && a.dfinal) ? a.dfinal[(b * dim + c) * N + nr[r]] : 0.0f;
         dA_acc[r] = 0.0f;
     }
-    float dD_acc = 0.0f, dbias_acc = 0.0f;
+    float dD_acc = 0.0f, dbias_acc = 0.0f;  // this lane's steps
     for (int seg = a.nseg - 1; seg >= 0; --seg) {
         const int64_t t0 = (int64_t)seg * kSeg;
         const int len = (int)min((int64_t)kSeg, L - t0);
-        for (int i = tid; i < kSeg * NP; i += kBwdThreads) {
-            (&s_dB[0][0])[i] = 0.0f;
-            (&s_dC[0][0])[i] = 0.0f;
+        // per-step scalars of the segment
+        float pde[SPL], pu[SPL], px[SPL], pdy[SPL], pdz[SPL], psig[SPL];
+#pragma unroll
+        for (int k = 0; k < SPL; ++k) {
+            const int j = lane + LPC * k;
+            pde[k] = pu[k] = px[k] = pdy[k] = pdz[k] = psig[k] = 0.0f;
+            if (c_ok && j < len) {
+                const int64_t t = t0 + j;
+                const float v = to_f32<T>(a.dt[row(t)]) + bias;
+                pde[k] = softplus_t<PRECISE>(v);
+                psig[k] = 1.0f / (1.0f + __expf(-v));
+                px[k] = to_f32<T>(a.x[row(t)]);
+                pu[k] = pde[k] * px[k];
+                const float dov = to_f32<T>(a.dout[row(t)]);
+                if (a.z) {
+                    const float zv = to_f32<T>(a.z[row(t)]);
+                    const float sz = 1.0f / (1.0f + __expf(-zv));
+                    pdy[k] = dov * zv * sz;
+                    pdz[k] = dov * sz * (1.0f + zv * (1.0f - sz));
+                } else {
+                    pdy[k] = dov;
+                }
+            }
         }
         // the segment's states h_t (after step t), recomputed from the checkpoint
         float hs[kSeg][R], h0[R];
@@ -148,81 +186,71 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
 #pragma unroll
         for (int j = 0; j < kSeg; ++j) {
             if (j < len) {
-                const int64_t t = t0 + j;
-                float v;
-                const float de = delta_of(t, v);
-                const float u = c_ok ? de * to_f32<T>(a.x[row(t)]) : 0.0f;
+                const float de = fetch(pde, j), u = fetch(pu, j);
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    const float Bv = nok[r] ? to_f32<T>(a.B[bc(t) + nr[r]]) : 0.0f;
-                    const float prev = j == 0 ? h0[r] : hs[j - 1][r];
-                    hs[j][r] = fmaf(expf(de * Ar[r]), prev, u * Bv);
+                    const float Bv = nok[r] ? to_f32<T>(a.B[bc(t0 + j) + nr[r]]) : 0.0f;
+                    hs[j][r] = fmaf(decay(de, r), j == 0 ? h0[r] : hs[j - 1][r], u * Bv);
                 }
             }
         }
-        __syncthreads();  // shared accumulators cleared
 #pragma unroll
         for (int j = kSeg - 1; j >= 0; --j) {
             if (j >= len) continue;
             const int64_t t = t0 + j;
-            float v;
-            const float de = delta_of(t, v);
-            const float xv = c_ok ? to_f32<T>(a.x[row(t)]) : 0.0f;
-            const float dov = c_ok ? to_f32<T>(a.dout[row(t)]) : 0.0f;
-            float Bv[R], Cv[R], av[R];
-            float yp = 0.0f;
+            const float de = fetch(pde, j), xv = fetch(px, j), dy = fetch(pdy, j);
+            float yp = 0.0f, dxp = 0.0f, ddp = 0.0f;
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                Bv[r] = nok[r] ? to_f32<T>(a.B[bc(t) + nr[r]]) : 0.0f;
-                Cv[r] = nok[r] ? to_f32<T>(a.C[bc(t) + nr[r]]) : 0.0f;
-                av[r] = expf(de * Ar[r]);
-                yp = fmaf(Cv[r], hs[j][r], yp);
-            }
-            const float y = lane_sum<LPC>(yp) + Dc * xv;
-            float gate = 1.0f, dzv = 0.0f;
-            if (a.z) {
-                const float zv = c_ok ? to_f32<T>(a.z[row(t)]) : 0.0f;
-                const float sz = sigmoidf_(zv);
-                gate = zv * sz;
-                dzv = dov * y * sz * (1.0f + zv * (1.0f - sz));
-            }
-            const float dy = dov * gate;
-            float dxp = 0.0f, ddp = 0.0f;
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
+                const float Bv = nok[r] ? to_f32<T>(a.B[bc(t) + nr[r]]) : 0.0f;
+                const float Cv = nok[r] ? to_f32<T>(a.C[bc(t) + nr[r]]) : 0.0f;
+                const float av = decay(de, r);
                 const float hp = j == 0 ? h0[r] : hs[j - 1][r];
-                g[r] = fmaf(dy, Cv[r], g[r]);
-                dxp = fmaf(g[r] * de, Bv[r], dxp);
-                ddp = fmaf(g[r], fmaf(av[r] * Ar[r], hp, Bv[r] * xv), ddp);
-                dA_acc[r] = fmaf(g[r] * av[r] * de, hp, dA_acc[r]);
-                if (nok[r]) {
-                    atomicAdd(&s_dB[j][nr[r]], g[r] * de * xv);
-                    atomicAdd(&s_dC[j][nr[r]], dy * hs[j][r]);
-                }
-                g[r] *= av[r];  // dL/dh_{t-1}
+                yp = fmaf(Cv, hs[j][r], yp);
+                g[r] = fmaf(dy, Cv, g[r]);
+                dxp = fmaf(g[r] * de, Bv, dxp);
+                ddp = fmaf(g[r], fmaf(av * Aval(r), hp, Bv * xv), ddp);
+                dA_acc[r] = fmaf(g[r] * av * de, hp, dA_acc[r]);
+                s_dB[(j * CPB + cc) * NP + r * LPC + lane] = g[r] * de * xv;
+                s_dC[(j * CPB + cc) * NP + r * LPC + lane] = dy * hs[j][r];
+                g[r] *= av;  // dL/dh_{t-1}
             }
-            const float dxs = lane_sum<LPC>(dxp);
-            const float dds = lane_sum<LPC>(ddp);
-            if (c_ok && lane == 0) {
-                a.dx[row(t)] = fmaf(dy, Dc, dxs);
-                const float dv = dds * sigmoidf_(v);
+            // three independent reductions over the channel's lanes
+#pragma unroll
+            for (int o = LPC / 2; o > 0; o >>= 1) {
+                yp += __shfl_xor_sync(0xffffffffu, yp, o, LPC);
+                dxp += __shfl_xor_sync(0xffffffffu, dxp, o, LPC);
+                ddp += __shfl_xor_sync(0xffffffffu, ddp, o, LPC);
+            }
+            if (c_ok && lane == j % LPC) {  // the lane that holds step j's scalars
+                const int k = j / LPC;
+                a.dx[row(t)] = fmaf(dy, Dc, dxp);
+                const float dv = ddp * psig[k];
                 a.ddt[row(t)] = dv;
                 dbias_acc += dv;
                 dD_acc = fmaf(dy, xv, dD_acc);
-                if (a.z) a.dz[row(t)] = dzv;
+                if (a.z) a.dz[row(t)] = pdz[k] * (yp + Dc * xv);
             }
         }
-        __syncthreads();  // shared accumulators complete
+        __syncthreads();  // the segment's dB / dC terms are in shared memory
         for (int i = tid; i < len * NP; i += kBwdThreads) {
             const int j = i / NP, n = i % NP;
             if (n < N) {
+                float sb = 0.0f, sc = 0.0f;
+                const int cmax = (int)min((int64_t)CPB, c_end - c_begin);
+                for (int q = 0; q < cmax; ++q) {
+                    sb += s_dB[(j * CPB + q) * NP + n];
+                    sc += s_dC[(j * CPB + q) * NP + n];
+                }
                 const int64_t o = bc(t0 + j) + n;
-                atomicAdd(&a.dB[o], s_dB[j][n]);
-                atomicAdd(&a.dC[o], s_dC[j][n]);
+                atomicAdd(&a.dB[o], sb);
+                atomicAdd(&a.dC[o], sc);
             }
         }
-        __syncthreads();  // read before the next segment clears them
+        __syncthreads();  // read before the next segment overwrites them
     }
+    dD_acc = lane_sum<LPC>(dD_acc);
+    dbias_acc = lane_sum<LPC>(dbias_acc);
 #pragma unroll
     for (int r = 0; r < R; ++r)
         if (nok[r]) {
@@ -238,10 +266,16 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
 template <typename T, int LPC, int R>
 cudaError_t launch_bwd(const BwdArgs<T>& a, int64_t batch, cudaStream_t stream) {
     constexpr int CPB = kBwdThreads / LPC;
+    constexpr size_t kSmem = sizeof(float) * 2 * kSeg * CPB * LPC * R;
     BwdArgs<T> k = a;
     k.tiles_per_group = (int)((a.cpg + CPB - 1) / CPB);
     const dim3 grid((unsigned)(a.G * k.tiles_per_group), 1, (unsigned)batch);
-    scan_bwd_kernel<T, LPC, R><<<grid, kBwdThreads, 0, stream>>>(k);
+    auto kern = scan_bwd_kernel<T, LPC, R>;
+    if (kSmem > 48 * 1024) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+        if (e != cudaSuccess) return e;
+    }
+    kern<<<grid, kBwdThreads, kSmem, stream>>>(k);
     note_launches(1);
     return cudaGetLastError();
 }
