@@ -432,26 +432,28 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_tc(const SsdTcArgs a
         tc::fence_after_sync();
     };
 
-    // next head's inputs in registers (see commit below)
-    constexpr int XCH = 256 * (kP / 8) / kScanThreads;                   // x_h chunks per thread (SW <= 256)
+    // next head's Delta, cumsum and h_{c-1} in registers (see commit below); its x_h goes
+    // straight to shared memory by cp.async (load_x)
     constexpr int HCH = (kP * (N / 8) + kScanThreads - 1) / kScanThreads;  // 8-float groups of h per thread
     float pf_dl = 0.0f, pf_cum = 0.0f;
-    uint4 pf_x[XCH];
     float4 pf_h[HCH][2];
+    // x_h of head hn -> buffer xbuf (MN-major, rows s < SW; rows past len are zero-filled)
+    auto load_x = [&](int64_t hn, int xbuf) {
+        const uint32_t xb = tc::smem_u32(sX + xbuf * Cfg::kX);
+        for (int i = tid; i < SW * (kP / 8); i += kScanThreads) {
+            int s, pc;
+            mnmajor_item(i, kP / 8, s, pc);
+            const bool okr = s < len;
+            const __nv_bfloat16* src = a.x + (okr ? ((b * a.T + c * a.Q + s) * a.H + hn) * kP + pc * 8 : 0);
+            cp_async16(xb + tc::off_mnmajor(pc * 8, s, kP), src, okr);
+        }
+        asm volatile("cp.async.commit_group;\n" ::);
+    };
     auto prefetch = [&](int64_t hn) {
         if (tid < Q) {
             const int64_t o = ((b * a.H + hn) * a.nchunks + c) * a.Q + tid;
             pf_dl = a.dl[o];
             pf_cum = a.cum[o];
-        }
-#pragma unroll
-        for (int j = 0; j < XCH; ++j) {
-            const int i = tid + j * kScanThreads;
-            int s, pc;
-            mnmajor_item(i, kP / 8, s, pc);
-            pf_x[j] = make_uint4(0, 0, 0, 0);
-            if (i < SW * (kP / 8) && s < len)
-                pf_x[j] = *reinterpret_cast<const uint4*>(a.x + ((b * a.T + c * a.Q + s) * a.H + hn) * kP + pc * 8);
         }
         const float* hs = a.states + ((b * a.nchunks + c) * a.H + hn) * (int64_t)kP * a.N;
 #pragma unroll
@@ -467,19 +469,12 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_tc(const SsdTcArgs a
     // prefetched inputs -> shared memory: cumsum and beta_s = log2(Delta_s) - cum_s log2(e)
     // (so that exp(cum_t - cum_s) Delta_s = 2^(cum_t log2(e) + beta_s)); x_h MN-major into
     // buffer xb; h split hi/lo K-major
-    auto commit = [&](int xbuf) {
+    auto commit = [&]() {
         if (tid < Q) {
             s_cum[tid] = pf_cum;
             s_beta[tid] = (pf_dl > 0.0f ? lg2(pf_dl) : -INFINITY) - pf_cum * kLog2e;
         }
-        const uint32_t xb = tc::smem_u32(sX + xbuf * Cfg::kX);
-#pragma unroll
-        for (int j = 0; j < XCH; ++j) {
-            const int i = tid + j * kScanThreads;
-            int s, pc;
-            mnmajor_item(i, kP / 8, s, pc);
-            if (i < SW * (kP / 8)) st_shared_v4(xb + tc::off_mnmajor(pc * 8, s, kP), pf_x[j].x, pf_x[j].y, pf_x[j].z, pf_x[j].w);
-        }
+        asm volatile("cp.async.wait_group 0;\n" ::);  // this head's x_h (made visible by the sync after)
         const uint32_t hb = tc::smem_u32(sHh), lb = tc::smem_u32(sHl);
 #pragma unroll
         for (int j = 0; j < HCH; ++j) {
@@ -538,7 +533,10 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_tc(const SsdTcArgs a
         }
     };
 
-    if (ok) prefetch(hbeg);
+    if (ok) {
+        prefetch(hbeg);
+        load_x(hbeg, 0);
+    }
     uint32_t last_commit_prev = 0;  // the previous head's last commit
     float alpha_prev = 0.0f;
     for (int hi = 0; hi < heads_per_cta && ok; ++hi) {
@@ -548,7 +546,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_tc(const SsdTcArgs a
         // exact only while its barrier is at most one phase past the awaited commit.)
         if (hi > 0) wait_commit(last_commit_prev);
         __syncthreads();  // ... and every thread is past the previous head's M' builds
-        commit(hi & 1);
+        commit();
         if (hi + 1 < heads_per_cta) prefetch(h + 1);
         tc::fence_async_smem();
         __syncthreads();
@@ -626,11 +624,18 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_tc(const SsdTcArgs a
                 tc::mma_commit(&s_mbar[ncommit & 1]);
             }
             ++ncommit;
-            // the previous head's epilogue, once this head's first MMAs are queued
-            if (kp == 0 && hi > 0) {
-                wait_commit(last_commit_prev);
-                finish(h - 1, (hi - 1) & 1, alpha_prev);
-                tc::fence_before_sync();
+            // the previous head's epilogue, once this head's first MMAs are queued; then the
+            // previous head's x_h buffer takes the next head's x_h
+            if (kp == 0) {
+                if (hi > 0) {
+                    wait_commit(last_commit_prev);
+                    finish(h - 1, (hi - 1) & 1, alpha_prev);
+                    tc::fence_before_sync();
+                }
+                if (hi + 1 < heads_per_cta) {
+                    __syncthreads();  // every thread is done reading the buffer in finish
+                    load_x(h + 1, (hi + 1) & 1);
+                }
             }
         }
         last_commit_prev = ncommit - 1;
