@@ -203,7 +203,8 @@ int step_common(const void* x, const void* dt, const float* A, const void* B, co
     if (rc != SSM_OK) return rc;
     if (shape->seqlen != 1) return SSM_ERR_SHAPE;
     if (shape->dstate % 4 != 0) return SSM_ERR_ALIGN;  // state rows move in 16-byte pieces
-    if (shape->batch * shape->nheads * shape->headdim > (int64_t(1) << 36)) return SSM_ERR_UNSUPPORTED;
+    // one grid row per sequence, 32-bit channel indices within a sequence
+    if (shape->batch > 65535 || shape->nheads * shape->headdim > (int64_t(1) << 30)) return SSM_ERR_UNSUPPORTED;
     if (!A || (shape->batch > 0 && (!x || !dt || !B || !C || !out || !state))) return SSM_ERR_NULL;
     const void* ptrs[] = {x, dt, A, B, C, D, z, dt_bias, out, state};
     for (const void* p : ptrs)

@@ -32,7 +32,7 @@ namespace ssm {
 namespace {
 
 constexpr int kBwdThreads = 256;
-constexpr int kSeg = 16;  // steps per checkpoint segment
+constexpr int kMinSeg = 16;  // shortest checkpoint segment (sizes the scratch)
 
 template <typename T>
 struct BwdArgs {
@@ -70,11 +70,12 @@ __device__ __forceinline__ float lane_sum(float v) {
     return v;
 }
 
-// grid (G * tiles_per_group, 1, batch); LPC lanes x R entries per channel, CPB channels.
+// grid (G * tiles_per_group, 1, batch); LPC lanes x R entries per channel, CPB channels,
+// checkpoints every kSeg steps.
 // The per-step scalars of a channel (Delta, Delta x, dy, the SiLU' factor, sigmoid(v)) are
 // computed once per segment, spread over the channel's lanes (lane j % LPC holds step j),
 // and fetched with shuffles inside the sequential sweeps.
-template <typename T, int LPC, int R>
+template <typename T, int LPC, int R, int kSeg>
 __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> a) {
     constexpr bool PRECISE = sizeof(T) == 4;
     constexpr int CPB = kBwdThreads / LPC;
@@ -263,14 +264,15 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
     }
 }
 
-template <typename T, int LPC, int R>
+template <typename T, int LPC, int R, int kSeg>
 cudaError_t launch_bwd(const BwdArgs<T>& a, int64_t batch, cudaStream_t stream) {
     constexpr int CPB = kBwdThreads / LPC;
     constexpr size_t kSmem = sizeof(float) * 2 * kSeg * CPB * LPC * R;
     BwdArgs<T> k = a;
     k.tiles_per_group = (int)((a.cpg + CPB - 1) / CPB);
+    k.nseg = (int)((a.L + kSeg - 1) / kSeg);
     const dim3 grid((unsigned)(a.G * k.tiles_per_group), 1, (unsigned)batch);
-    auto kern = scan_bwd_kernel<T, LPC, R>;
+    auto kern = scan_bwd_kernel<T, LPC, R, kSeg>;
     if (kSmem > 48 * 1024) {
         const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
         if (e != cudaSuccess) return e;
@@ -310,20 +312,23 @@ cudaError_t bwd_typed(const ScanBwdArgs& s, void* ws, cudaStream_t stream) {
     a.N = f.dstate;
     a.G = f.ngroups;
     a.cpg = f.nheads / f.ngroups;
-    a.nseg = (int)((f.seqlen + kSeg - 1) / kSeg);
+    a.nseg = 0;
     a.tiles_per_group = 0;
-    // lanes per channel: the state width padded to a power of two, at most a warp
-    if (f.dstate <= 4) return launch_bwd<T, 4, 1>(a, f.batch, stream);
-    if (f.dstate <= 8) return launch_bwd<T, 8, 1>(a, f.batch, stream);
-    if (f.dstate <= 16) return launch_bwd<T, 16, 1>(a, f.batch, stream);
-    if (f.dstate <= 32) return launch_bwd<T, 32, 1>(a, f.batch, stream);
-    return launch_bwd<T, 32, 2>(a, f.batch, stream);
+    // lanes per channel: the state width padded to a power of two, at most a warp (four
+    // entries per lane with fewer lanes measured slower on B300: fewer resident warps and
+    // a longer per-step chain outweigh the shorter reductions)
+    const int64_t np = f.dstate <= 4 ? 4 : f.dstate <= 8 ? 8 : f.dstate <= 16 ? 16 : f.dstate <= 32 ? 32 : 64;
+    if (np == 4) return launch_bwd<T, 4, 1, 16>(a, f.batch, stream);
+    if (np == 8) return launch_bwd<T, 8, 1, 16>(a, f.batch, stream);
+    if (np == 16) return launch_bwd<T, 16, 1, 16>(a, f.batch, stream);
+    if (np == 32) return launch_bwd<T, 32, 1, 16>(a, f.batch, stream);
+    return launch_bwd<T, 32, 2, 16>(a, f.batch, stream);
 }
 
 }  // namespace
 
 size_t scan_bwd_workspace_bytes(const ScanArgs& a) {
-    const int64_t nseg = (a.seqlen + kSeg - 1) / kSeg;
+    const int64_t nseg = (a.seqlen + kMinSeg - 1) / kMinSeg;
     return align_up((size_t)a.batch * nseg * a.nheads * a.dstate * sizeof(float), 256);
 }
 

@@ -65,21 +65,22 @@ __global__ void __launch_bounds__(kStepThreads) ssm_step_kernel(const StepArgs a
     constexpr bool PRECISE = sizeof(T) == 4;
     constexpr int CPB = kStepThreads / LPC;  // channels per block
     const int lane = threadIdx.x % LPC;
-    const int64_t ch = (int64_t)blockIdx.x * CPB + threadIdx.x / LPC;  // flat (b, h, p)
-    const int64_t nc = a.H * a.P;                                       // channels per sequence
-    const bool ok = ch < a.batch * nc;
+    const int64_t b = blockIdx.y;                                         // sequence
+    const int nc = (int)(a.H * a.P);                                      // channels per sequence
+    const int cs = blockIdx.x * CPB + threadIdx.x / LPC;                  // channel (h, p)
+    const int64_t ch = b * nc + cs;                                       // flat (b, h, p)
+    const bool ok = cs < nc;
     float y = 0.0f, xv = 0.0f, x_raw = 0.0f;
     float prev[3] = {0.0f, 0.0f, 0.0f};  // convolution state of the channel, oldest first
-    int64_t h = 0;
+    int h = 0;
     if (ok) {
-        const int64_t b = ch / nc;
-        h = (ch / a.P) % a.H;
-        const int64_t g = h / (a.H / a.G);
+        h = a.P == 1 ? cs : cs / (int)a.P;
+        const int g = a.G == 1 ? 0 : h / (int)(a.H / a.G);
         const T* Bs = static_cast<const T*>(a.B) + (b * a.G + g) * a.N;
         const T* Cs = static_cast<const T*>(a.C) + (b * a.G + g) * a.N;
         xv = to_f32<T>(static_cast<const T*>(a.x)[ch]);
         if (CONV) {
-            const int64_t c = ch % nc;
+            const int64_t c = cs;
             const int km1 = a.conv_k - 1;
             float acc = a.conv_b ? a.conv_b[c] : 0.0f;
             for (int j = 0; j < km1; ++j) {
@@ -124,7 +125,7 @@ __global__ void __launch_bounds__(kStepThreads) ssm_step_kernel(const StepArgs a
     if (!ok || lane != 0) return;
     if (CONV && a.x_last) {
         // shift the convolution state by one token (in place when x_last == x_prev)
-        const int64_t b = ch / nc, c = ch % nc;
+        const int64_t c = cs;
         const int km1 = a.conv_k - 1;
         T* xl = static_cast<T*>(a.x_last) + b * km1 * nc + c;
         for (int j = 0; j < km1; ++j) xl[j * nc] = from_f32<T>(j + 1 < km1 ? prev[j + 1] : x_raw);
@@ -137,7 +138,8 @@ __global__ void __launch_bounds__(kStepThreads) ssm_step_kernel(const StepArgs a
 template <typename T, int LPC>
 void launch_lpc(const StepArgs& s, int64_t nch, cudaStream_t stream) {
     constexpr int CPB = kStepThreads / LPC;
-    const unsigned blocks = (unsigned)((nch + CPB - 1) / CPB);
+    (void)nch;
+    const dim3 blocks((unsigned)((s.H * s.P + CPB - 1) / CPB), (unsigned)s.batch);
     if (s.conv_k > 0)
         ssm_step_kernel<T, LPC, true><<<blocks, kStepThreads, 0, stream>>>(s);
     else

@@ -106,3 +106,21 @@ def test_backward_is_repeatable_where_no_atomics():
     b = grads_gpu(inp, dout, dfinal, init)
     for k in ("dx", "ddt", "dz", "dinitial_state"):
         assert np.array_equal(a[k], b[k]), k
+
+
+# shapes whose channels alone fill the GPU (many thread blocks per group, full grids)
+WIDE = [
+    # (dtype, batch, T, D, N)
+    ("bf16", 4, 40, 5120, 16),
+    ("f32", 2, 24, 10240, 8),
+    ("bf16", 2, 20, 1280, 64),
+    ("f32", 4, 17, 9600, 4),        # bf16 rows of 4 entries are not 16-byte multiples
+]
+
+
+@pytest.mark.parametrize("case", WIDE, ids=lambda c: "-".join(map(str, c)))
+def test_backward_many_channels(case):
+    dtype, b, T, D, N = case
+    w, inp = random_inputs("diag", dtype, b, T, D, 1, N, seed=T + N)
+    dout, dfinal, h0 = extras(w, seed=T + 1)
+    compare(w, inp, dout, dfinal, h0)
