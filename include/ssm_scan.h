@@ -270,6 +270,25 @@ int ssm_scan_bwd(const void* x, const void* dt, const float* A, const void* B, c
 /* Scratch bytes of ssm_scan_bwd ((size_t)-1 for an invalid shape or SSD mode). */
 size_t ssm_scan_bwd_workspace_size(const ssm_shape* shape);
 
+/*
+ * Launch timing, for measurement (this has no counterpart in the pages: it instruments
+ * the library's own launches).  While enabled, every kernel the library launches is
+ * bracketed by two CUDA events recorded on the launch's own stream;
+ * ssm_timing_collect waits for the recorded events, fills `out` (up to `max_entries`,
+ * sorted by name) with each kernel's launch count and summed device time in
+ * milliseconds, clears the records and returns the number of distinct kernels (which
+ * may exceed max_entries; out may be NULL), or -SSM_ERR_CUDA if an event failed.
+ * Enabling adds two event records per launch; the library's results do not change.
+ * Process-wide; thread-safe.
+ */
+typedef struct ssm_kernel_time {
+    char name[64];     /* kernel name and role, NUL-terminated */
+    int64_t launches;  /* launches recorded since the last collect */
+    double total_ms;   /* summed event-to-event time of those launches */
+} ssm_kernel_time;
+void ssm_timing_enable(int on);
+int ssm_timing_collect(ssm_kernel_time* out, int max_entries);
+
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char* ssm_strerror(int status);
 

@@ -29,8 +29,8 @@ SSM_BF16 = 1
 # Every function declared in include/ssm_scan.h.
 EXPORTED = ("ssm_scan_fwd", "ssm_scan_fwd_ws", "ssm_scan_workspace_size", "ssm_scan_fwd_noalloc",
             "ssm_scan_fwd_state", "ssm_step", "ssm_scan_fwd_conv", "ssm_scan_conv_workspace_size",
-            "ssm_step_conv", "ssm_scan_bwd", "ssm_scan_bwd_workspace_size", "ssm_strerror",
-            "ssm_kernel_launch_count", "ssm_abi_version")
+            "ssm_step_conv", "ssm_scan_bwd", "ssm_scan_bwd_workspace_size", "ssm_timing_enable",
+            "ssm_timing_collect", "ssm_strerror", "ssm_kernel_launch_count", "ssm_abi_version")
 
 
 class ssm_shape(ctypes.Structure):
@@ -44,6 +44,11 @@ class ssm_conv(ctypes.Structure):
     _fields_ = [("weight", ctypes.c_void_p), ("bias", ctypes.c_void_p),
                 ("x_prev", ctypes.c_void_p), ("x_last", ctypes.c_void_p),
                 ("width", ctypes.c_int32)]
+
+
+class ssm_kernel_time(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 64), ("launches", ctypes.c_int64),
+                ("total_ms", ctypes.c_double)]
 
 
 class SsmError(RuntimeError):
@@ -104,6 +109,10 @@ def load() -> ctypes.CDLL:
         lib.ssm_scan_bwd.restype = ctypes.c_int
         lib.ssm_scan_bwd_workspace_size.argtypes = [sp]
         lib.ssm_scan_bwd_workspace_size.restype = ctypes.c_size_t
+        lib.ssm_timing_enable.argtypes = [ctypes.c_int]
+        lib.ssm_timing_enable.restype = None
+        lib.ssm_timing_collect.argtypes = [ctypes.POINTER(ssm_kernel_time), ctypes.c_int]
+        lib.ssm_timing_collect.restype = ctypes.c_int
         lib.ssm_scan_workspace_size.argtypes = [sp]
         lib.ssm_scan_workspace_size.restype = ctypes.c_size_t
         lib.ssm_strerror.argtypes = [ctypes.c_int]
@@ -123,3 +132,18 @@ def strerror(status: int) -> str:
 
 def launch_count() -> int:
     return int(load().ssm_kernel_launch_count())
+
+
+def timing_enable(on: bool) -> None:
+    """Bracket every library launch with CUDA events on its stream (see ssm_timing_enable)."""
+    load().ssm_timing_enable(1 if on else 0)
+
+
+def timing_collect() -> dict:
+    """{kernel name: (launches, total ms)} since the last collect; clears the records."""
+    buf = (ssm_kernel_time * 64)()  # the library has far fewer distinct kernels
+    n = load().ssm_timing_collect(buf, 64)
+    if n < 0:
+        raise SsmError(-n, "ssm_timing_collect")
+    return {buf[i].name.decode(): (int(buf[i].launches), float(buf[i].total_ms))
+            for i in range(min(n, 64))}

@@ -93,11 +93,12 @@ cudaError_t conv_prepass_launch(const ScanArgs& a, void* xc, cudaStream_t stream
     const int64_t total = c.batch * c.T * c.ch;
     if (total == 0) return cudaSuccess;
     const unsigned blocks = (unsigned)((total + kConvThreads - 1) / kConvThreads);
+    cudaEvent_t t0 = timing_begin(stream);
     if (a.dtype == 1)
         conv_silu_kernel<__nv_bfloat16><<<blocks, kConvThreads, 0, stream>>>(c);
     else
         conv_silu_kernel<float><<<blocks, kConvThreads, 0, stream>>>(c);
-    note_launches(1);
+    note_launch("conv_silu_kernel", stream, t0);
     return cudaGetLastError();
 }
 
@@ -106,11 +107,12 @@ cudaError_t conv_tail_launch(const ScanArgs& a, cudaStream_t stream) {
     const int64_t total = c.batch * (c.K - 1) * c.ch;
     if (!a.x_last || total == 0) return cudaSuccess;
     const unsigned blocks = (unsigned)((total + kConvThreads - 1) / kConvThreads);
+    cudaEvent_t t0 = timing_begin(stream);
     if (a.dtype == 1)
         conv_tail_kernel<__nv_bfloat16><<<blocks, kConvThreads, 0, stream>>>(c);
     else
         conv_tail_kernel<float><<<blocks, kConvThreads, 0, stream>>>(c);
-    note_launches(1);
+    note_launch("conv_tail_kernel", stream, t0);
     return cudaGetLastError();
 }
 

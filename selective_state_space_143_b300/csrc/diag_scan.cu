@@ -599,8 +599,9 @@ cudaError_t launch_one(const DiagKernelArgs& ka, dim3 grid, cudaStream_t stream)
         if (e != cudaSuccess) return e;
         attr_done.fetch_or(bit, std::memory_order_relaxed);
     }
+    cudaEvent_t t0 = timing_begin(stream);
     kern<<<grid, Cfg::NT, Cfg::kSmemBytes, stream>>>(ka);
-    note_launches(1);
+    note_launch(STATE_ONLY ? "diag_scan_kernel (segment state pass)" : "diag_scan_kernel (output pass)", stream, t0);
     return cudaGetLastError();
 }
 

@@ -417,22 +417,28 @@ cudaError_t ssd_launch_typed(const ScanArgs& a, void* ws, cudaStream_t stream) {
         t.nchunks = pl.nchunks;
         cudaError_t e = ssd_tc_chunk_state(t, a.batch, stream);
         if (e != cudaSuccess) return e;
+        cudaEvent_t t0 = timing_begin(stream);
         ssd_state_pass<<<dim3((unsigned)((a.headdim * a.dstate / 4 + kThreads - 1) / kThreads), (unsigned)a.nheads, (unsigned)a.batch), kThreads, 0, stream>>>(s);
-        note_launches(1);
+        note_launch("ssd_state_pass", stream, t0);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         return ssd_tc_chunk_scan(t, a.batch, a.z != nullptr, stream);
     }
     if (pl.nchunks > 0) {
+        cudaEvent_t t0 = timing_begin(stream);
         ssd_chunk_state<T><<<dim3((unsigned)pl.nchunks, (unsigned)a.nheads * nP * nN, (unsigned)a.batch), kThreads, 0, stream>>>(s);
-        note_launches(1);
+        note_launch("ssd_chunk_state", stream, t0);
     }
-    ssd_state_pass<<<dim3((unsigned)((a.headdim * a.dstate / 4 + kThreads - 1) / kThreads), (unsigned)a.nheads, (unsigned)a.batch), kThreads, 0, stream>>>(s);
-    note_launches(1);
+    {
+        cudaEvent_t t0 = timing_begin(stream);
+        ssd_state_pass<<<dim3((unsigned)((a.headdim * a.dstate / 4 + kThreads - 1) / kThreads), (unsigned)a.nheads, (unsigned)a.batch), kThreads, 0, stream>>>(s);
+        note_launch("ssd_state_pass", stream, t0);
+    }
     if (pl.nchunks > 0) {
         const size_t smem = sizeof(float) * (2 * pl.Q + kTile * (a.dstate + 1) + kSub * (a.dstate + 1) +
                                              kSub * (kTile + 1) + kTile * (kSub + 1));
         const dim3 grid((unsigned)pl.nchunks, (unsigned)a.nheads * nP, (unsigned)a.batch * nTq);
+        cudaEvent_t t0 = timing_begin(stream);
         if (a.z) {
             cudaFuncSetAttribute(ssd_chunk_scan<T, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             ssd_chunk_scan<T, true><<<grid, kThreads, smem, stream>>>(s);
@@ -440,7 +446,7 @@ cudaError_t ssd_launch_typed(const ScanArgs& a, void* ws, cudaStream_t stream) {
             cudaFuncSetAttribute(ssd_chunk_scan<T, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             ssd_chunk_scan<T, false><<<grid, kThreads, smem, stream>>>(s);
         }
-        note_launches(1);
+        note_launch("ssd_chunk_scan", stream, t0);
     }
     return cudaGetLastError();
 }

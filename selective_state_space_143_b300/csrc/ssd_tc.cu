@@ -677,8 +677,9 @@ cudaError_t launch_state(const SsdTcArgs& s, int64_t batch, cudaStream_t stream)
     cudaError_t e = cudaFuncSetAttribute(ssd_state_tc<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int hpc = heads_per_cta(s, Cfg::kMaxHeads);  // even: heads per group are even here
+    cudaEvent_t t0 = timing_begin(stream);
     ssd_state_tc<N><<<dim3((unsigned)s.nchunks, (unsigned)(s.H / hpc), (unsigned)batch), kThreads, smem, stream>>>(s, hpc);
-    note_launches(1);
+    note_launch("ssd_state_tc", stream, t0);
     return cudaGetLastError();
 }
 
@@ -691,8 +692,9 @@ cudaError_t launch_scan(const SsdTcArgs& s, int64_t batch, cudaStream_t stream) 
     if (e != cudaSuccess) return e;
     const int hpc = heads_per_cta(s, 8);  // G = C B^T is shared by the CTA's heads
     const dim3 grid((unsigned)(s.nchunks * (s.Q / 128)), (unsigned)(s.H / hpc), (unsigned)batch);
+    cudaEvent_t t0 = timing_begin(stream);
     kern<<<grid, kScanThreads, smem, stream>>>(s, hpc);
-    note_launches(1);
+    note_launch("ssd_scan_tc", stream, t0);
     return cudaGetLastError();
 }
 

@@ -4,6 +4,11 @@
 
 #include <atomic>
 #include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
 
 #include "ssm_scan.h"
 #include "ssm_internal.h"
@@ -12,7 +17,55 @@ namespace ssm {
 
 static std::atomic<uint64_t> g_launches{0};
 
-void note_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+// Launch timing: events recorded around each launch while enabled, summed per kernel
+// name by ssm_timing_collect.
+namespace {
+struct TimedLaunch {
+    const char* name;
+    cudaEvent_t start, end;
+};
+std::atomic<int> g_timing{0};
+std::mutex g_timing_mutex;
+std::vector<TimedLaunch> g_timed;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t take_event() {
+    std::lock_guard<std::mutex> lock(g_timing_mutex);
+    if (!g_event_pool.empty()) {
+        cudaEvent_t e = g_event_pool.back();
+        g_event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    return e;
+}
+}  // namespace
+
+cudaEvent_t timing_begin(cudaStream_t stream) {
+    if (!g_timing.load(std::memory_order_relaxed)) return nullptr;
+    cudaEvent_t e = take_event();
+    if (e && cudaEventRecord(e, stream) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    return e;
+}
+
+void note_launch(const char* name, cudaStream_t stream, cudaEvent_t start) {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (!start) return;
+    cudaEvent_t end = take_event();
+    if (!end || cudaEventRecord(end, stream) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return;
+    }
+    std::lock_guard<std::mutex> lock(g_timing_mutex);
+    g_timed.push_back({name, start, end});
+}
 
 namespace {
 
@@ -238,6 +291,47 @@ extern "C" {
 int ssm_abi_version(void) { return (1 << 16) | 1; }
 
 uint64_t ssm_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+void ssm_timing_enable(int on) { g_timing.store(on ? 1 : 0, std::memory_order_relaxed); }
+
+int ssm_timing_collect(ssm_kernel_time* out, int max_entries) {
+    std::vector<TimedLaunch> recs;
+    {
+        std::lock_guard<std::mutex> lock(g_timing_mutex);
+        recs.swap(g_timed);
+    }
+    std::map<std::string, std::pair<int64_t, double>> agg;
+    int status = 0;
+    for (const TimedLaunch& r : recs) {
+        float ms = 0.0f;
+        if (cudaEventSynchronize(r.end) != cudaSuccess || cudaEventElapsedTime(&ms, r.start, r.end) != cudaSuccess) {
+            (void)cudaGetLastError();
+            status = -SSM_ERR_CUDA;
+        }
+        auto& a = agg[r.name];
+        a.first += 1;
+        a.second += ms;
+    }
+    {
+        std::lock_guard<std::mutex> lock(g_timing_mutex);
+        for (const TimedLaunch& r : recs) {
+            g_event_pool.push_back(r.start);
+            g_event_pool.push_back(r.end);
+        }
+    }
+    if (status < 0) return status;
+    int n = 0;
+    for (const auto& kv : agg) {
+        if (out && n < max_entries) {
+            std::memset(out[n].name, 0, sizeof(out[n].name));
+            std::strncpy(out[n].name, kv.first.c_str(), sizeof(out[n].name) - 1);
+            out[n].launches = kv.second.first;
+            out[n].total_ms = kv.second.second;
+        }
+        ++n;
+    }
+    return n;
+}
 
 const char* ssm_strerror(int status) {
     switch (status) {

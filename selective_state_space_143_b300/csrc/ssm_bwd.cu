@@ -277,8 +277,9 @@ cudaError_t launch_bwd(const BwdArgs<T>& a, int64_t batch, cudaStream_t stream) 
         const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
         if (e != cudaSuccess) return e;
     }
+    cudaEvent_t t0 = timing_begin(stream);
     kern<<<grid, kBwdThreads, kSmem, stream>>>(k);
-    note_launches(1);
+    note_launch("scan_bwd_kernel", stream, t0);
     return cudaGetLastError();
 }
 

@@ -32,8 +32,13 @@ struct ScanArgs {
     int dtype;  // 0 fp32, 1 bf16
 };
 
-// Counts kernel launches made by this library (thread-safe).
-void note_launches(int n);
+// Launch bookkeeping.  Around every kernel launch:
+//   cudaEvent_t t0 = timing_begin(stream);  kernel<<<...>>>(...);  note_launch("name", stream, t0);
+// note_launch counts the launch; when timing is enabled (ssm_timing_enable) timing_begin
+// records an event before the launch and note_launch one after it, on the same stream,
+// for ssm_timing_collect.
+cudaEvent_t timing_begin(cudaStream_t stream);
+void note_launch(const char* name, cudaStream_t stream, cudaEvent_t start);
 
 // Diagonal (Mamba-1) path.
 size_t diag_workspace_bytes(const ScanArgs& a);

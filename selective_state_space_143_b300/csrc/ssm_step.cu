@@ -185,11 +185,12 @@ cudaError_t step_launch(const ScanArgs& a, bool diag_a, float* state, cudaStream
     s.conv_k = a.conv_k;
     const int64_t nch = a.batch * a.nheads * a.headdim;
     if (nch == 0) return cudaSuccess;
+    cudaEvent_t t0 = timing_begin(stream);
     if (a.dtype == 1)
         launch_typed<__nv_bfloat16>(s, nch, stream);
     else
         launch_typed<float>(s, nch, stream);
-    note_launches(1);
+    note_launch("ssm_step_kernel", stream, t0);
     return cudaGetLastError();
 }
 

@@ -267,3 +267,11 @@ def test_backward_argument_errors():
     assert call(s, dB=(15 << 12) + 8) == _lib.SSM_ERR_ALIGN
     n = lib.ssm_scan_bwd_workspace_size(ctypes.byref(s))
     assert n == 2 * (64 // 16) * 64 * 16 * 4   # the state every 16 steps
+
+
+def test_timing_collect_without_launches():
+    lib = _lib.load()
+    lib.ssm_timing_enable(1)
+    assert lib.ssm_timing_collect(None, 0) == 0   # nothing launched, nothing recorded
+    lib.ssm_timing_enable(0)
+    assert _lib.timing_collect() == {}

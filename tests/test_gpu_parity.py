@@ -210,3 +210,25 @@ def test_workspace_entry_matches_allocating_entry():
                        chunk=128, workspace=ws)
     torch.cuda.synchronize()
     assert torch.equal(ref, got)
+
+
+def test_launch_timing_records_every_kernel():
+    """ssm_timing_enable / ssm_timing_collect: one record per launch, named per kernel,
+    the same count as the launch counter, and the results unchanged."""
+    w = WORKLOADS["c1"]
+    inp = make_inputs(w)
+    d = {k: (None if v is None else v.to(DEV)) for k, v in inp.items()}
+    ref = ssm.scan_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["z"], d["dt_bias"])
+    from selective_state_space_143_b300 import _lib
+    _lib.timing_collect()
+    _lib.timing_enable(True)
+    n0 = ssm.launch_count()
+    for _ in range(3):
+        out = ssm.scan_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["z"], d["dt_bias"])
+    torch.cuda.synchronize()
+    _lib.timing_enable(False)
+    kt = _lib.timing_collect()
+    assert sum(v[0] for v in kt.values()) == ssm.launch_count() - n0
+    assert "diag_scan_kernel (output pass)" in kt and kt["diag_scan_kernel (output pass)"][0] == 3
+    assert all(v[1] > 0 for v in kt.values())
+    assert torch.equal(out, ref)
