@@ -100,10 +100,25 @@ def algorithmic_flops(w) -> float:
     return float(w.batch * nchunks * (w.ngroups * per_chunk_group + w.nheads * per_chunk_head))
 
 
+def kernel_times(ssm, K, step, flush=None):
+    """Per-kernel device times from a second pass of K steps with the library's launch
+    events on (kept out of the headline pass: the events add a gap between kernels)."""
+    ssm._lib.timing_collect()
+    ssm._lib.timing_enable(True)
+    for i in range(K):
+        if flush is not None:
+            flush.zero_()
+        step(i)
+    torch.cuda.synchronize()
+    ssm._lib.timing_enable(False)
+    return ssm._lib.timing_collect()
+
+
 def kernel_roofline(kt, nbytes, calls, peak_gbs, peak_kind, whole):
     """Roofline of the dominant kernel from the library's launch timing ``kt``
-    ({name: (launches, total ms)} over the timed steps): the call's algorithmic bytes,
-    all of which that kernel reads or writes, over its average event-timed duration."""
+    ({name: (launches, total ms)} over K steps of the same workload): the call's
+    algorithmic bytes, all of which that kernel reads or writes, over its average
+    event-timed duration."""
     if not kt:
         return whole
     name, (n, ms) = max(kt.items(), key=lambda kv: kv[1][1])
@@ -344,8 +359,6 @@ def run_ours(args, w):
     n0 = ssm.launch_count()
     # Hold the GPU in a spin kernel while the K steps are queued, so that the event
     # pairs time device execution only, not the host's launch rate.
-    ssm._lib.timing_collect()
-    ssm._lib.timing_enable(True)  # events around each of the library's launches
     torch.cuda._sleep(int(min(2e9, 2e6 + K * 4e5)))
     for i in range(K):
         flush.zero_()
@@ -353,9 +366,8 @@ def run_ours(args, w):
         step()
         ends[i].record(stream)
     torch.cuda.synchronize()
-    ssm._lib.timing_enable(False)
-    kt = ssm._lib.timing_collect()
     launches = ssm.launch_count() - n0
+    kt = kernel_times(ssm, K, lambda i: step(), flush)
     barrier(dist)
     ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms_step = max_over_ranks(dist, sum(ms) / K)
@@ -525,17 +537,14 @@ def run_decode(args, w0):
     barrier(dist)
     torch.cuda.synchronize()
     n0 = ssm.launch_count()
-    ssm._lib.timing_collect()
-    ssm._lib.timing_enable(True)
     torch.cuda._sleep(int(min(2e9, 2e6 + K * 4e5)))
     for i in range(K):
         starts[i].record(stream)
         step(i)
         ends[i].record(stream)
     torch.cuda.synchronize()
-    ssm._lib.timing_enable(False)
-    kt = ssm._lib.timing_collect()
     launches = ssm.launch_count() - n0
+    kt = kernel_times(ssm, K, step)
     barrier(dist)
     ms_step = max_over_ranks(dist, sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / K)
     clk = clocks.stop() if not args.quick else {"sm_mhz": None, "sm_max_mhz": None,
@@ -674,8 +683,6 @@ def run_backward(args, w):
     barrier(dist)
     torch.cuda.synchronize()
     n0 = ssm.launch_count()
-    ssm._lib.timing_collect()
-    ssm._lib.timing_enable(True)
     torch.cuda._sleep(int(min(2e9, 2e6 + K * 4e5)))
     for i in range(K):
         flush.zero_()
@@ -683,9 +690,8 @@ def run_backward(args, w):
         step()
         ends[i].record(stream)
     torch.cuda.synchronize()
-    ssm._lib.timing_enable(False)
-    kt = ssm._lib.timing_collect()
     launches = ssm.launch_count() - n0
+    kt = kernel_times(ssm, K, lambda i: step(), flush)
     barrier(dist)
     ms_step = max_over_ranks(dist, sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / K)
     clk = clocks.stop() if not args.quick else {"sm_mhz": None, "sm_max_mhz": None,
