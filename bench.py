@@ -100,6 +100,83 @@ def algorithmic_flops(w) -> float:
     return float(w.batch * nchunks * (w.ngroups * per_chunk_group + w.nheads * per_chunk_head))
 
 
+def _packed(specs, pinned, dev=None):
+    """One contiguous buffer holding tensors of the given {name: (shape, dtype)} at
+    256-byte aligned offsets; returns (buffer, {name: view})."""
+    offs, total = {}, 0
+    for k, (shape, dtype) in specs.items():
+        n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+        offs[k] = (total, n)
+        total += (n + 255) // 256 * 256
+    buf = torch.empty(max(total, 256), dtype=torch.uint8, device=dev)
+    if pinned:
+        buf = buf.pin_memory()
+    views = {k: buf[o:o + n].view(specs[k][1]).view(specs[k][0]) for k, (o, n) in offs.items()}
+    return buf, views
+
+
+def pipelined_e2e(dev, host, run, out_specs, K, dist):
+    """End-to-end steps through the public API: each step copies its inputs from pinned
+    host memory, runs the library call, and copies its outputs back to pinned host memory.
+    The inputs of a step travel as one packed buffer and so do its outputs (one copy each
+    way per step); copy-in, compute and copy-out run on three streams with two buffer
+    sets, so that one step's copies overlap its neighbours' compute (the way a caller
+    streaming batches would drive the library).
+
+    host: {name: CPU tensor or None}; out_specs: {name: (shape, dtype)};
+    run(device_inputs, device_outputs) writes the outputs.  Returns (ms per step, max over
+    ranks; bytes copied in; bytes copied out)."""
+    comp = torch.cuda.current_stream(dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    in_specs = {k: (tuple(v.shape), v.dtype) for k, v in host.items() if v is not None}
+    hbuf, hviews = _packed(in_specs, pinned=True)
+    for k, v in hviews.items():
+        v.copy_(host[k])
+    dins = [_packed(in_specs, pinned=False, dev=dev) for _ in range(2)]
+    douts = [_packed(out_specs, pinned=False, dev=dev) for _ in range(2)]
+    houts = [_packed(out_specs, pinned=True) for _ in range(2)]
+    h_done = [torch.cuda.Event() for _ in range(2)]
+    c_done = [torch.cuda.Event() for _ in range(2)]
+    o_done = [torch.cuda.Event() for _ in range(2)]
+
+    def step(i):
+        sl = i % 2
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(c_done[sl])  # step i-2's compute has read this input set
+            dins[sl][0].copy_(hbuf, non_blocking=True)
+            h_done[sl].record(s_in)
+        comp.wait_event(h_done[sl])
+        if i >= 2:
+            comp.wait_event(o_done[sl])  # step i-2's copy-out has read this output set
+        run({k: dins[sl][1].get(k) for k in host}, douts[sl][1])
+        c_done[sl].record(comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(c_done[sl])
+            houts[sl][0].copy_(douts[sl][0], non_blocking=True)
+            o_done[sl].record(s_out)
+
+    for i in range(4):
+        step(i)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize()
+    e0.record(s_in)
+    for i in range(K):
+        step(i)
+    s_out.wait_stream(comp)
+    e1.record(s_out)
+    torch.cuda.synchronize()
+    return (max_over_ranks(dist, e0.elapsed_time(e1) / K), hbuf.numel(), houts[0][0].numel())
+
+
+E2E_NOTE = ("inputs copied from pinned host memory and outputs read back every step, one "
+            "packed copy each way; copy-in, compute and copy-out on three streams with two "
+            "buffer sets")
+
+
 def kernel_times(ssm, K, step, flush=None):
     """Per-kernel device times from a second pass of K steps with the library's launch
     events on (kept out of the headline pass: the events add a gap between kernels)."""
@@ -406,37 +483,18 @@ def run_ours(args, w):
     e2e = None
     cpu = None
     if not args.quick:
-        host = {k: (None if v is None else v.pin_memory()) for k, v in inp.items()}
-        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        fs_h = torch.empty(st_shape, dtype=torch.float32).pin_memory() if fs is not None else None
-        h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
-        d2h = out_h.numel() * out_h.element_size() + (fs_h.numel() * 4 if fs_h is not None else 0)
+        specs = {"out": (tuple(out.shape), out.dtype)}
+        if fs is not None:
+            specs["final_state"] = (tuple(fs.shape), torch.float32)
 
-        def e2e_step():
-            dd = {k: (None if v is None else v.to(dev, non_blocking=True)) for k, v in host.items()}
-            o = ssm.scan_fwd(dd["x"], dd["dt"], dd["A"], dd["B"], dd["C"], dd["D"], dd["z"],
-                             dd["dt_bias"], final_state=None if fs is None else torch.empty_like(fs),
-                             chunk=chunk, stream=stream, **conv)
-            if fs is not None:
-                o, f = o
-                fs_h.copy_(f, non_blocking=True)
-            out_h.copy_(o, non_blocking=True)
+        def run(dd, oo):
+            ssm.scan_fwd(dd["x"], dd["dt"], dd["A"], dd["B"], dd["C"], dd["D"], dd["z"],
+                         dd["dt_bias"], out=oo["out"], final_state=oo.get("final_state"),
+                         chunk=chunk, stream=torch.cuda.current_stream(dev), **conv)
 
-        for _ in range(3):
-            e2e_step()
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        barrier(dist)
-        torch.cuda.synchronize()
-        e0.record(stream)
-        for _ in range(K):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1) / K)
+        e2e_ms, h2d, d2h = pipelined_e2e(dev, inp, run, specs, K, dist)
         e2e = {"value": units / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": e2e_ms,
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "how": E2E_NOTE}
         if rank == 0:
             done, el, threads, desc = oracle_sample(w, inp, args.cpu_seconds,
                                                     conv=cp if args.conv else None)
@@ -561,32 +619,17 @@ def run_decode(args, w0):
     cpu = e2e = None
     if not args.quick:
         # end to end: the token's inputs copied in and its output copied out every step
-        host = [{k: (None if v is None else v.pin_memory()) for k, v in token(t, inp).items()
-                 if k not in ("A", "D", "dt_bias")} for t in range(ntok)]
-        out_h = torch.empty(outs[0].shape, dtype=outs[0].dtype).pin_memory()
-        h2d = sum(v.numel() * v.element_size() for v in host[0].values() if v is not None)
-        d2h = out_h.numel() * out_h.element_size()
+        host = {k: v for k, v in token(0, inp).items() if k not in ("A", "D", "dt_bias")}
+        specs = {"out": (tuple(outs[0].shape), outs[0].dtype)}
 
-        def e2e_step(i):
-            hd = host[i % ntok]
-            dd = {k: (None if v is None else v.to(dev, non_blocking=True)) for k, v in hd.items()}
-            o = ssm.step(dd["x"], dd["dt"], toks[0]["A"], dd["B"], dd["C"], toks[0]["D"],
-                         dd["z"], toks[0]["dt_bias"], state=state, stream=stream)
-            out_h.copy_(o, non_blocking=True)
+        def run(dd, oo):
+            ssm.step(dd["x"], dd["dt"], toks[0]["A"], dd["B"], dd["C"], toks[0]["D"], dd["z"],
+                     toks[0]["dt_bias"], state=state, out=oo["out"],
+                     stream=torch.cuda.current_stream(dev))
 
-        for i in range(3):
-            e2e_step(i)
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for i in range(K):
-            e2e_step(i)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1) / K)
+        e2e_ms, h2d, d2h = pipelined_e2e(dev, host, run, specs, K, dist)
         e2e = {"value": units / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": e2e_ms,
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "how": E2E_NOTE}
         if rank == 0:
             import oracle
             # one-token scans from the carried state over whole sequences until the
@@ -712,39 +755,27 @@ def run_backward(args, w):
                            "recompute, reverse); peak = 148 SMs x 32/clk x max SM clock"}
     cpu = e2e = None
     if not args.quick:
-        host = {k: (None if v is None else v.pin_memory()) for k, v in inp.items()}
-        dout_p, dfin_p = dout_h.pin_memory(), dfin_h.pin_memory()
-        h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
-        h2d += dout_p.numel() * dout_p.element_size() + dfin_p.numel() * 4
-        outs_h = None
+        host = dict(inp, dout=dout_h, dfinal=dfin_h)
+        xs, f32 = tuple(inp["x"].shape), torch.float32
+        H, N = w.nheads, w.dstate
+        specs = {"dx": (xs, f32), "ddt": (tuple(inp["dt"].shape), f32), "dA": ((H, N), f32),
+                 "dB": (tuple(inp["B"].shape), f32), "dC": (tuple(inp["C"].shape), f32),
+                 "dinitial_state": ((w.batch, H, N), f32)}
+        if inp["D"] is not None:
+            specs["dD"] = ((H,), f32)
+        if inp["z"] is not None:
+            specs["dz"] = (xs, f32)
+        if inp["dt_bias"] is not None:
+            specs["ddt_bias"] = ((H,), f32)
 
-        def e2e_step():
-            nonlocal outs_h
-            dd = {k: (None if v is None else v.to(dev, non_blocking=True)) for k, v in host.items()}
-            g = ssm.scan_bwd(dd["x"], dd["dt"], dd["A"], dd["B"], dd["C"], dd["D"], dd["z"],
-                             dd["dt_bias"], dout=dout_p.to(dev, non_blocking=True),
-                             dfinal_state=dfin_p.to(dev, non_blocking=True), workspace=ws,
-                             stream=stream)
-            if outs_h is None:
-                outs_h = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory()
-                          for k, v in g.items() if v is not None}
-            for k, v in outs_h.items():
-                v.copy_(g[k], non_blocking=True)
+        def run(dd, oo):
+            ssm.scan_bwd(dd["x"], dd["dt"], dd["A"], dd["B"], dd["C"], dd["D"], dd["z"],
+                         dd["dt_bias"], dout=dd["dout"], dfinal_state=dd["dfinal"],
+                         workspace=ws, stream=torch.cuda.current_stream(dev), grads=oo)
 
-        for _ in range(3):
-            e2e_step()
-        torch.cuda.synchronize()
-        d2h = sum(v.numel() * v.element_size() for v in outs_h.values())
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(K):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1) / K)
+        e2e_ms, h2d, d2h = pipelined_e2e(dev, host, run, specs, K, dist)
         e2e = {"value": units / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": e2e_ms,
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "how": E2E_NOTE}
         if rank == 0:
             import oracle
             # the oracle's backward over the first sequence and a block of channels

@@ -179,13 +179,14 @@ def scan_fwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, *, out=None, final_st
 
 
 def scan_bwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, *, dout, dfinal_state=None,
-             initial_state=None, workspace=None, stream=None):
+             initial_state=None, workspace=None, stream=None, grads=None):
     """Gradients of the diagonal-mode scan (``scan_fwd`` with a 2-D A).
 
     ``dout`` is the gradient of the output (x's shape and dtype), ``dfinal_state`` that of
     the final state (float32, optional).  Returns a dict of float32 tensors: dx, ddt, dA,
     dB, dC (B's shape), and dD, dz, ddt_bias, dinitial_state where the matching input was
-    given (dinitial_state always).
+    given (dinitial_state always).  ``grads``: optional dict of preallocated float32
+    tensors with those names and shapes, written in place instead of new ones.
     """
     s = make_shape(x, A, B, 0)
     dev = x.device
@@ -210,6 +211,12 @@ def scan_bwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, *, dout, dfinal_state
          "dz": None if z is None else torch.empty(x.shape, **f32),
          "ddt_bias": None if dt_bias is None else torch.empty((H,), **f32),
          "dinitial_state": torch.empty((b, H, N), **f32)}
+    if grads is not None:
+        for k, v in grads.items():
+            if k not in g or g[k] is None:
+                raise ValueError(f"grads: unexpected {k}")
+            _check(k, v, g[k].shape, torch.float32, dev)
+            g[k] = v
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
