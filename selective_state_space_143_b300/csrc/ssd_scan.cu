@@ -24,6 +24,7 @@
 
 #include "ssm_device.cuh"
 #include "ssd_tc.h"
+#include "tc_util.cuh"
 #include "ssm_internal.h"
 
 namespace ssm {
@@ -211,6 +212,72 @@ __global__ void __launch_bounds__(kThreads) ssd_state_pass(const SsdArgs a) {
         }
     }
     if (a.final_state) *reinterpret_cast<float4*>(a.final_state + (b * a.H + h) * PN + i4 * 4) = st;
+}
+
+// The tensor-core path's carry.  S_c arrives in the split-ready layout of the
+// tensor-core chunk-state kernel: the 8 values of (p, n..n+7) as two float4 at the byte
+// offsets o and o + P*N*2 that their bf16 hi and lo halves take in the scan kernel's
+// K-major h tile.  Each thread owns one such unit: it reads S_c there and writes
+// h_{c-1} back in place as bf16 hi = bf16(h) and lo = bf16(h - hi), so the scan kernel
+// copies the tiles straight into shared memory.  Initial and final states are fp32 in
+// the plain (b, H, P, N) layout.  grid: (ceil(P*N / 8 / 256), H, b).
+constexpr int kPassAheadSplit = 4;
+
+__global__ void __launch_bounds__(kThreads) ssd_state_pass_split(const SsdArgs a) {
+    // units in memory order: unit u sits at byte 16 u of each half, so consecutive
+    // threads touch consecutive 16-byte pieces; u = (core-matrix block) * 8 + (p & 7)
+    const int64_t u = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int64_t h = blockIdx.y, b = blockIdx.z;
+    const int64_t PN = a.P * a.N;
+    if (u * 8 >= PN) return;
+    const int64_t blk = u >> 3, kb = a.N / 8;
+    const int p = (int)((blk / kb) * 8 + (u & 7)), n0 = (int)(blk % kb) * 8;
+    const uint32_t o = (uint32_t)(16 * u);  // == off_kmajor(p, n0, N)
+    const int64_t half = PN * 2;  // bytes of the hi (or lo) tile
+    float st[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) st[k] = a.init ? a.init[(b * a.H + h) * PN + p * a.N + n0 + k] : 0.0f;
+    const int64_t cstride = a.H * PN * 4;  // bytes between consecutive chunks of one head
+    char* base = reinterpret_cast<char*>(a.states + (b * a.nchunks * a.H + h) * PN);
+    const float* cum = a.cum + (b * a.H + h) * a.nchunks * a.Q;
+    for (int64_t c0 = 0; c0 < a.nchunks; c0 += kPassAheadSplit) {
+        float4 S0[kPassAheadSplit], S1[kPassAheadSplit];
+        float dec[kPassAheadSplit];
+#pragma unroll
+        for (int j = 0; j < kPassAheadSplit; ++j) {
+            const int64_t c = c0 + j;
+            if (c < a.nchunks) {
+                S0[j] = *reinterpret_cast<const float4*>(base + c * cstride + o);
+                S1[j] = *reinterpret_cast<const float4*>(base + c * cstride + half + o);
+                const int len = (int)min(a.Q, a.T - c * a.Q);
+                dec[j] = expf(cum[c * a.Q + len - 1]);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kPassAheadSplit; ++j) {
+            const int64_t c = c0 + j;
+            if (c < a.nchunks) {
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const __nv_bfloat162 hv = __floats2bfloat162_rn(st[2 * k], st[2 * k + 1]);
+                    const float2 hf = __bfloat1622float2(hv);
+                    const __nv_bfloat162 lv = __floats2bfloat162_rn(st[2 * k] - hf.x, st[2 * k + 1] - hf.y);
+                    hi[k] = *reinterpret_cast<const uint32_t*>(&hv);
+                    lo[k] = *reinterpret_cast<const uint32_t*>(&lv);
+                }
+                *reinterpret_cast<uint4*>(base + c * cstride + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4*>(base + c * cstride + half + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                const float s[8] = {S0[j].x, S0[j].y, S0[j].z, S0[j].w, S1[j].x, S1[j].y, S1[j].z, S1[j].w};
+#pragma unroll
+                for (int k = 0; k < 8; ++k) st[k] = fmaf(dec[j], st[k], s[k]);
+            }
+        }
+    }
+    if (a.final_state) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) a.final_state[(b * a.H + h) * PN + p * a.N + n0 + k] = st[k];
+    }
 }
 
 // grid: (nchunks, H * nP, b * nTq); output tile of 64 rows x 64 head channels.
@@ -418,8 +485,8 @@ cudaError_t ssd_launch_typed(const ScanArgs& a, void* ws, cudaStream_t stream) {
         cudaError_t e = ssd_tc_chunk_state(t, a.batch, stream);
         if (e != cudaSuccess) return e;
         cudaEvent_t t0 = timing_begin(stream);
-        ssd_state_pass<<<dim3((unsigned)((a.headdim * a.dstate / 4 + kThreads - 1) / kThreads), (unsigned)a.nheads, (unsigned)a.batch), kThreads, 0, stream>>>(s);
-        note_launch("ssd_state_pass", stream, t0);
+        ssd_state_pass_split<<<dim3((unsigned)((a.headdim * a.dstate / 8 + kThreads - 1) / kThreads), (unsigned)a.nheads, (unsigned)a.batch), kThreads, 0, stream>>>(s);
+        note_launch("ssd_state_pass_split", stream, t0);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         return ssd_tc_chunk_scan(t, a.batch, a.z != nullptr, stream);

@@ -232,12 +232,18 @@ __global__ void __launch_bounds__(kThreads) ssd_state_tc(const SsdTcArgs a, int 
             st_shared_v4(bl + off, lo[0], lo[1], lo[2], lo[3]);
         }
     };
-    // accumulator of pair -> states[b, c, h, p, :]; warp w: lanes 32*(w%4).., column half w/4
+    // accumulator of pair -> the (b, c, h) state tile; warp w: lanes 32*(w%4).., column
+    // half w/4.  Split-ready layout: the 8 values of (p, n..n+7) go as two float4 to the
+    // byte offsets that their bf16 hi and lo halves take in the scan kernel's K-major
+    // tile (offset o in the first P*N*2 bytes, and o + P*N*2), so that the carry pass can
+    // convert every unit in place (see ssd_state_pass_split).
     auto epilogue = [&](uint32_t tmem, int pair) {
         const int q = warp & 3;
         const int m = q * 32 + (tid & 31);
         const int64_t h = hbeg + 2 * pair + m / kP;
-        float* dst = a.states + (((b * a.nchunks + c) * a.H + h) * kP + (m % kP)) * a.N;
+        const int p = m % kP;
+        char* tile = reinterpret_cast<char*>(a.states + ((b * a.nchunks + c) * a.H + h) * (int64_t)kP * N);
+        constexpr uint32_t kHalf = (uint32_t)kP * N * 2;
         const uint32_t acc = tmem + (uint32_t)((pair & 1) * N);
         constexpr int NH = N / 2 < 16 ? 16 : N / 2;
 #pragma unroll 1
@@ -245,7 +251,11 @@ __global__ void __launch_bounds__(kThreads) ssd_state_tc(const SsdTcArgs a, int 
             float v[16];
             tc::tmem_ld16(tc::taddr(acc, q * 32, n0), v);
 #pragma unroll
-            for (int j = 0; j < 16; j += 4) *reinterpret_cast<float4*>(dst + n0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            for (int j = 0; j < 16; j += 8) {
+                const uint32_t o = tc::off_kmajor(p, n0 + j, N);
+                *reinterpret_cast<float4*>(tile + o) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                *reinterpret_cast<float4*>(tile + kHalf + o) = make_float4(v[j + 4], v[j + 5], v[j + 6], v[j + 7]);
+            }
         }
     };
 
@@ -327,7 +337,8 @@ struct ScanTcCfg {
     static constexpr size_t kMPart = (size_t)128 * KPC * 2;      // one M' K-part, hi or lo
     static constexpr size_t kX = (size_t)256 * kP * 2;           // one x_h tile
     static constexpr size_t kH = (size_t)kP * N * 2;             // one h tile, hi or lo
-    static constexpr size_t kPhase2 = 4 * kMPart + 2 * kX + 2 * kH;
+    static constexpr int kHBufs = N <= 128 ? 2 : 1;               // (hi, lo) tile sets
+    static constexpr size_t kPhase2 = 4 * kMPart + 2 * kX + kHBufs * 2 * kH;
     static constexpr size_t kSmem = kC + (kPhase1 > kPhase2 ? kPhase1 : kPhase2);
 };
 
@@ -368,8 +379,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_tc(const SsdTcArgs a
     unsigned char* sB = region;                          // phase 1, K-major: N_mma = s, K = n
     unsigned char* sM = region;                          // [2 parts][hi, lo], K-major: M = t, K = KPC
     unsigned char* sX = region + 4 * Cfg::kMPart;        // [2], MN-major: K = s, N_mma = p
-    unsigned char* sHh = sX + 2 * Cfg::kX;               // K-major: N_mma = p, K = n
-    unsigned char* sHl = sHh + Cfg::kH;
+    unsigned char* sH = sX + 2 * Cfg::kX;                // [kHBufs][hi, lo], K-major: N_mma = p, K = n
 
     // phase 1 loads: C rows of this half and B rows [0, SW)
     {
@@ -432,11 +442,18 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_tc(const SsdTcArgs a
         tc::fence_after_sync();
     };
 
-    // next head's Delta, cumsum and h_{c-1} in registers (see commit below); its x_h goes
-    // straight to shared memory by cp.async (load_x)
-    constexpr int HCH = (kP * (N / 8) + kScanThreads - 1) / kScanThreads;  // 8-float groups of h per thread
+    // next head's Delta and cumsum in registers (see commit below); its x_h and its
+    // h_{c-1} tiles go straight to shared memory by cp.async (load_x, load_h)
     float pf_dl = 0.0f, pf_cum = 0.0f;
-    float4 pf_h[HCH][2];
+    // h_{c-1} of head hn (bf16 hi and lo tiles, already in this kernel's K-major layout,
+    // written by the carry pass) -> tile set hbuf
+    auto load_h = [&](int64_t hn, int hbuf) {
+        const unsigned char* src = reinterpret_cast<const unsigned char*>(
+            a.states + ((b * a.nchunks + c) * a.H + hn) * (int64_t)kP * N);
+        const uint32_t dst = tc::smem_u32(sH + hbuf * 2 * Cfg::kH);
+        for (int i = tid; i < (int)(2 * Cfg::kH / 16); i += kScanThreads) cp_async16(dst + 16 * i, src + 16 * i, true);
+        asm volatile("cp.async.commit_group;\n" ::);
+    };
     // x_h of head hn -> buffer xbuf (MN-major, rows s < SW; rows past len are zero-filled)
     auto load_x = [&](int64_t hn, int xbuf) {
         const uint32_t xb = tc::smem_u32(sX + xbuf * Cfg::kX);
@@ -455,16 +472,6 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_tc(const SsdTcArgs a
             pf_dl = a.dl[o];
             pf_cum = a.cum[o];
         }
-        const float* hs = a.states + ((b * a.nchunks + c) * a.H + hn) * (int64_t)kP * a.N;
-#pragma unroll
-        for (int j = 0; j < HCH; ++j) {
-            const int i = tid + j * kScanThreads;
-            if (i >= kP * (N / 8)) break;
-            int p, nc;
-            kmajor_item(i, N / 8, p, nc);
-            pf_h[j][0] = *reinterpret_cast<const float4*>(hs + (int64_t)p * a.N + nc * 8);
-            pf_h[j][1] = *reinterpret_cast<const float4*>(hs + (int64_t)p * a.N + nc * 8 + 4);
-        }
     };
     // prefetched inputs -> shared memory: cumsum and beta_s = log2(Delta_s) - cum_s log2(e)
     // (so that exp(cum_t - cum_s) Delta_s = 2^(cum_t log2(e) + beta_s)); x_h MN-major into
@@ -474,23 +481,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_tc(const SsdTcArgs a
             s_cum[tid] = pf_cum;
             s_beta[tid] = (pf_dl > 0.0f ? lg2(pf_dl) : -INFINITY) - pf_cum * kLog2e;
         }
-        asm volatile("cp.async.wait_group 0;\n" ::);  // this head's x_h (made visible by the sync after)
-        const uint32_t hb = tc::smem_u32(sHh), lb = tc::smem_u32(sHl);
-#pragma unroll
-        for (int j = 0; j < HCH; ++j) {
-            const int i = tid + j * kScanThreads;
-            if (i >= kP * (N / 8)) break;
-            int p, nc;
-            kmajor_item(i, N / 8, p, nc);
-            uint32_t qh[4], ql[4];
-            split2(pf_h[j][0].x, pf_h[j][0].y, qh[0], ql[0]);
-            split2(pf_h[j][0].z, pf_h[j][0].w, qh[1], ql[1]);
-            split2(pf_h[j][1].x, pf_h[j][1].y, qh[2], ql[2]);
-            split2(pf_h[j][1].z, pf_h[j][1].w, qh[3], ql[3]);
-            const uint32_t off = tc::off_kmajor(p, nc * 8, N);
-            st_shared_v4(hb + off, qh[0], qh[1], qh[2], qh[3]);
-            st_shared_v4(lb + off, ql[0], ql[1], ql[2], ql[3]);
-        }
+        asm volatile("cp.async.wait_group 0;\n" ::);  // this head's x_h and h tiles (visible after the sync)
     };
     // epilogue of head hh from accumulator set acc: y = Y_diag + exp(cum_t) Y_off + D x, gate
     auto finish = [&](int64_t hh, int acc, float alpha_h) {
@@ -536,6 +527,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_tc(const SsdTcArgs a
     if (ok) {
         prefetch(hbeg);
         load_x(hbeg, 0);
+        load_h(hbeg, 0);
     }
     uint32_t last_commit_prev = 0;  // the previous head's last commit
     float alpha_prev = 0.0f;
@@ -554,6 +546,9 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_tc(const SsdTcArgs a
         for (int kp = 0; kp < nparts; ++kp) {
             // this K-part's buffer was last used by commit ncommit - 2
             if (ncommit >= 2) wait_commit(ncommit - 2);
+            // one h tile set: part 0's MMAs (the last readers of this head's h tiles) are
+            // done once commit ncommit - 2 has arrived at part 2
+            if (Cfg::kHBufs == 1 && kp == 2 && hi + 1 < heads_per_cta) load_h(h + 1, 0);
             // M'[t, s] = G[t, s] 2^(alpha_t + beta_s) for s <= t, hi/lo, K-major.  This warp
             // builds BC columns of the part for its 32 rows.
             {
@@ -612,8 +607,9 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_tc(const SsdTcArgs a
                 if (kp == 0) {
                     constexpr uint32_t id_off = tc::idesc_bf16(128, kP, 0, 0);
                     const uint64_t dc = tc::desc_kmajor(tc::smem_u32(sC), N, 0);
-                    const uint64_t dhh = tc::desc_kmajor(tc::smem_u32(sHh), N, 0);
-                    const uint64_t dhl = tc::desc_kmajor(tc::smem_u32(sHl), N, 0);
+                    const unsigned char* hset = sH + (Cfg::kHBufs == 2 ? (hi & 1) : 0) * 2 * Cfg::kH;
+                    const uint64_t dhh = tc::desc_kmajor(tc::smem_u32(hset), N, 0);
+                    const uint64_t dhl = tc::desc_kmajor(tc::smem_u32(hset + Cfg::kH), N, 0);
 #pragma unroll
                     for (int ks = 0; ks < N / 16; ++ks)
                         tc::mma_bf16(tYo, dc + ks * tc::kstep_kmajor(), dhh + ks * tc::kstep_kmajor(), id_off, ks > 0);
@@ -635,6 +631,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_tc(const SsdTcArgs a
                 if (hi + 1 < heads_per_cta) {
                     __syncthreads();  // every thread is done reading the buffer in finish
                     load_x(h + 1, (hi + 1) & 1);
+                    // two h tile sets: the previous head's (its MMAs are done) takes the next
+                    if (Cfg::kHBufs == 2) load_h(h + 1, (hi + 1) & 1);
                 }
             }
         }
