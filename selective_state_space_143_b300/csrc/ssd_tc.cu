@@ -533,11 +533,9 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_tc(const SsdTcArgs a
     float alpha_prev = 0.0f;
     for (int hi = 0; hi < heads_per_cta && ok; ++hi) {
         const int64_t h = hbeg + hi;
-        // h_{c-1} tiles are single-buffered: the previous head's MMAs must be done reading
-        // them.  (Only the latest commit is waited on here: an mbarrier parity wait is
-        // exact only while its barrier is at most one phase past the awaited commit.)
-        if (hi > 0) wait_commit(last_commit_prev);
-        __syncthreads();  // ... and every thread is past the previous head's M' builds
+        // every thread is past the previous head's M' builds before s_cum / s_beta change
+        // (the h_{c-1} tiles have their own hand-over: two tile sets, or the copy at part 2)
+        __syncthreads();
         commit();
         if (hi + 1 < heads_per_cta) prefetch(h + 1);
         tc::fence_async_smem();
