@@ -211,3 +211,35 @@ def test_step_matches_one_token_scan_bitwise_state_path():
     for i in range(1, 4):
         assert torch.equal(y2[i], y2[0])
         assert torch.equal(st2[i], st2[0])
+
+
+@pytest.mark.parametrize("mode,dtype,b,H,P,N", [
+    ("diag", "bf16", 2048, 512, 1, 16),   # 64 MB carried state
+    ("diag", "f32", 1400, 512, 1, 24),    # rows of 6 pieces on 4 lanes
+    ("ssd", "bf16", 32, 64, 64, 128),
+])
+def test_step_large_batch(mode, dtype, b, H, P, N):
+    """Decode steps over a carried state of 64 MB or more (serving-size batches), sampled
+    channels against the oracle."""
+    T = 3
+    w, inp = random_inputs(mode, dtype, b, T, H, P, N, seed=N + b)
+    rng = np.random.default_rng(4)
+    shape = (b, H, N) if mode == "diag" else (b, H, P, N)
+    h0 = rng.standard_normal(shape).astype(np.float32)
+    state = torch.from_numpy(h0).to(DEV)
+    ys = []
+    for t in range(T):
+        d = step_tensors(inp, t)
+        ys.append(ssm.step(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["z"], d["dt_bias"],
+                           state=state).float().unsqueeze(1))
+    torch.cuda.synchronize()
+    y = torch.cat(ys, 1).cpu().numpy()
+    nch = b * H * P
+    sel = np.unique(np.concatenate([[0, nch - 1], rng.choice(nch, 200, replace=False)]))
+    ref, ref_fs = oracle.scan(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"],
+                              inp["z"], inp["dt_bias"], initial_state=h0, select=sel)
+    yv = (y.transpose(0, 2, 1) if mode == "diag" else y.transpose(0, 2, 3, 1)).reshape(nch, T)[sel]
+    rv = (ref.transpose(0, 2, 1) if mode == "diag" else ref.transpose(0, 2, 3, 1)).reshape(nch, T)[sel]
+    tol = TOL[dtype]
+    assert oracle.max_rel_error(yv, rv) <= tol
+    assert oracle.max_rel_error(state.cpu().numpy().reshape(nch, N)[sel], ref_fs.reshape(nch, N)[sel]) <= tol
