@@ -119,27 +119,16 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
-// Non-blocking test of `phase` (no suspension of the thread).
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* mbar, uint32_t phase) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(smem_u32(mbar)), "r"(phase));
-    return done != 0;
-}
-
-// Bounded wait for `phase` of `mbar`: polls without suspending (a suspended try_wait
-// sleeps for a whole time slice even when the phase completes just after the first
-// check, which costs far more than the short waits here), and gives up (returns
-// false) after about one second of wall time or 2^26 polls, whichever comes first.
+// Bounded wait for `phase` of `mbar`: try_wait suspends the waiting thread in hardware
+// between checks (so waiting warps take no issue slots from the working ones), and the
+// wait gives up (returns false) after about one second of wall time or 2^24 checks,
+// whichever comes first.
 __device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t phase) {
-    if (mbar_test_wait(mbar, phase)) return true;
+    if (mbar_try_wait(mbar, phase)) return true;
     const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 0; it < (1u << 26); ++it) {
-        if (mbar_test_wait(mbar, phase)) return true;
-        if ((it & 1023u) == 0 && globaltimer_ns() - t0 > 1000000000ull) return false;
+    for (uint32_t it = 0; it < (1u << 24); ++it) {
+        if (mbar_try_wait(mbar, phase)) return true;
+        if ((it & 255u) == 0 && globaltimer_ns() - t0 > 1000000000ull) return false;
     }
     return false;
 }
