@@ -8,19 +8,20 @@
 //   y_t     = (sum_n C_t[n] h_t[n] + D x_t) * SiLU(z_t)
 //
 // Design (B300):
-//  * The expanded state (b, T, d_inner, N) never leaves registers: a quad of 4 lanes
-//    owns one channel, each lane NPT = N/4 state entries.
-//  * Inputs are token-major (channels innermost).  A 64-thread block owns 16 channels
-//    of one group and walks time in tiles of 32 steps; each tile of x, dt, z, B, C is
-//    staged into shared memory by 16-byte cp.async copies in a 3-deep pipeline, so HBM
+//  * The expanded state (b, T, d_inner, N) never leaves registers: LPC lanes own one
+//    channel, each lane NPT = NK/LPC state entries held as fp32 pairs (NPT 4 or 8,
+//    chosen by the host plan from the channel count).
+//  * Inputs are token-major (channels innermost).  A block owns 16 (or 32) channels of
+//    one group and walks time in tiles of 16 steps; each tile of x, dt, z, B, C is
+//    staged into shared memory by 16-byte cp.async copies in a 4-deep ring, so HBM
 //    reads are coalesced rows that overlap the arithmetic of earlier tiles.
-//  * Rows are taken in groups of 4: lane q of a quad evaluates softplus(dt + dt_bias)
-//    and Delta*x for row q of the group and the quad exchanges them by shuffles; each
-//    lane then advances its state entries over the 4 rows (ex2.approx for the decay,
-//    packed fp32x2 multiply/FMA for the decay argument, the input term, the update and
-//    the C.h partial sum); a transposed quad reduction leaves the full C.h of row q in
-//    lane q, which applies D*x and the SiLU gate and stores.  Every per-(t, c)
-//    operation runs once, spread over the quad.
+//  * One software-pipelined loop body per tile k: the recurrence of tile k's rows
+//    (decays of 4 rows formed before their dependent updates: ex2.approx of the decay
+//    argument, packed fp32x2 multiply/FMA for the argument, the input term, the update
+//    and the C.h partial sum), interleaved with the per-(t, c) prep of tile k+1
+//    (softplus(dt + dt_bias) and Delta*x per channel pair, B and C to fp32) and the
+//    epilogue of tile k-1 (the LPC partial sums, D*x, the SiLU gate, the store).  Every
+//    per-(t, c) operation runs once, by one thread of a channel pair.
 //  * B300's SFU runs ex2 at 32/clk/SM (lg2, rcp at 16) and packed fp32x2 FMA gives no
 //    extra lane throughput over scalar FMA (128 lane-ops/clk/SM), so the scan is bound
 //    by the SFU and FMA pipes (one exp and four FP32 operations per state entry and

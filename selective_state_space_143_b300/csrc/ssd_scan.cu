@@ -16,6 +16,8 @@
 //   ssd_chunk_state  : Delta, cumulative decay sums and the local chunk states S_c
 //   ssd_state_pass   : sequential carry over chunks, h_{c-1} stored per chunk, final state
 //   ssd_chunk_scan   : Y_diag + Y_off + skip + gate for each chunk
+// the tensor-core path's carry (ssd_state_pass_split), and the dispatch between the two
+// paths (ssd_tc.cu holds the tensor-core chunk-state and scan kernels).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 

@@ -14,7 +14,9 @@
 //                    Y_diag   = M' X_h                            (M = 128, N = 64, K = s)
 //                    Y_off    = C_rows h_{c-1}^T                  (M = 128, N = 64, K = dstate)
 //                    out      = (Y_diag + exp(s_t) Y_off + D x) SiLU(z)
-// The carry h_c = exp(s_last) h_{c-1} + S_c runs in between (ssd_state_pass).
+// The carry h_c = exp(s_last) h_{c-1} + S_c runs in between (ssd_state_pass_split in
+// ssd_scan.cu): ssd_state_tc stores S_c in a split-ready layout and the carry writes
+// h_{c-1} back as the bf16 hi/lo tiles that ssd_scan_tc copies into shared memory.
 //
 // Shapes taken here: bf16, headdim 64, dstate a multiple of 16 in [32, 256], chunk 128 or
 // 256, an even number of heads per group.  Other shapes use the CUDA-core kernels.

@@ -288,7 +288,7 @@ using namespace ssm;
 
 extern "C" {
 
-int ssm_abi_version(void) { return (1 << 16) | 1; }
+int ssm_abi_version(void) { return (1 << 16) | 2; }
 
 uint64_t ssm_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
