@@ -61,8 +61,6 @@ struct BwdArgs {
     int nseg, tiles_per_group;
 };
 
-__device__ __forceinline__ float sigmoidf_(float v) { return 1.0f / (1.0f + expf(-v)); }
-
 template <int LPC>
 __device__ __forceinline__ float lane_sum(float v) {
 #pragma unroll
