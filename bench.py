@@ -213,6 +213,25 @@ def kernel_roofline(kt, nbytes, calls, peak_gbs, peak_kind, whole):
     return roof
 
 
+# DRAM traffic per launch of the dominant kernel (dram__bytes_read.sum +
+# dram__bytes_write.sum) from an ncu capture of the same bench command, taken with the
+# kernel source as it stands: {(bench mode, workload, kernel name): bytes}.  Anything
+# not listed (no capture of the current kernel) reports null.
+NCU_TRAFFIC = {
+    ("scan", "c1", "diag_scan_kernel (output pass)"): 26_596_352 + 1_536,
+    ("decode", "c1/8192", "ssm_step_kernel"): 294_178_816 + 217_264_384,
+    ("backward", "c1", "scan_bwd_kernel"): 38_175_744 + 19_325_440,
+}
+
+
+def with_traffic(roof, key):
+    t = NCU_TRAFFIC.get(key + (roof.get("kernel"),))
+    roof["traffic"] = t
+    roof["traffic_source"] = ("ncu capture of this command (bytes per launch)" if t is not None
+                              else "no capture of the current kernel")
+    return roof
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -462,6 +481,7 @@ def run_ours(args, w):
              "ms": ms_step, "algorithmic_bytes": nbytes,
              "what": "all kernels of one ssm_scan_fwd call"}
     roof = kernel_roofline(kt, nbytes, K, peaks["hbm_gbs"], peak_kind, whole)
+    roof = with_traffic(roof, ("conv" if args.conv else "scan", w.name))
     if w.mode == "ssd":
         fl = algorithmic_flops(w)
         roof["tensor_tflops"] = fl / (ms_step * 1e-3) / 1e12
@@ -615,6 +635,7 @@ def run_decode(args, w0):
     whole = {"achieved": gbs, "frac": gbs / peaks["hbm_gbs"], "unit": "GB/s", "ms": ms_step,
              "algorithmic_bytes": nbytes, "what": "one ssm_step call"}
     roof = kernel_roofline(kt, nbytes, K, peaks["hbm_gbs"], peak_kind, whole)
+    roof = with_traffic(roof, ("decode", f"{w0.name}/{batch}"))
 
     cpu = e2e = None
     if not args.quick:
@@ -747,6 +768,7 @@ def run_backward(args, w):
     whole = {"achieved": gbs, "frac": gbs / peaks["hbm_gbs"], "unit": "GB/s", "ms": ms_step,
              "algorithmic_bytes": nbytes, "what": "one ssm_scan_bwd call (zeroing + kernel)"}
     roof = kernel_roofline(kt, nbytes, K, peaks["hbm_gbs"], peak_kind, whole)
+    roof = with_traffic(roof, ("backward", w.name))
     sm_mhz = float(peaks.get("sm_max_mhz", 2032.0))
     exps = 3.0 * w.token_channels * w.dstate  # the decay is formed in three sweeps
     roof["sfu"] = {"achieved": exps / (ms_step * 1e-3), "peak": 148 * 32 * sm_mhz * 1e6,

@@ -344,7 +344,7 @@ struct ScanTcCfg {
     static constexpr size_t kSmem = kC + (kPhase1 > kPhase2 ? kPhase1 : kPhase2);
 };
 
-// grid (nchunks * Q/128, H / HG, b); 256 threads.  Rows [128*rh, 128*rh + 128) of chunk c,
+// grid (nchunks * Q/128, H / HG, b); 512 threads.  Rows [128*rh, 128*rh + 128) of chunk c,
 // heads [HG*blockIdx.y, +HG).
 // Per head h, pipelined over the CTA's heads:
 //   commit   : prefetched inputs of h to shared memory (x_h into its parity buffer, h_{c-1}
