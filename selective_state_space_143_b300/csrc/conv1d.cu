@@ -5,12 +5,18 @@
 // "引言：Attention的天花板" article's example):
 //   x'[b,t,c] = SiLU(bias[c] + sum_{k<K} w[c,k] x[b, t-K+1+k, c]),
 // inputs before t = 0 taken from the previous call (x_prev) or zero.  The diagonal scan
-// fuses this into its own input staging; the SSD path runs this pass into fp32 scratch
-// and reads x' from there (the tensor-core SSD kernels take x as an exact bf16 operand,
-// so an fp32 x' runs on the CUDA-core SSD kernels).  One thread per (b, t, channel pair); the K rows a thread reads
-// are shared with its neighbours in time through L1/L2.
+// fuses this into its own input staging; the SSD path runs this pass into scratch.  x'
+// is kept at fp32 precision, either as fp32 (read by the CUDA-core SSD kernels) or as two
+// bf16 planes x_hi = bf16(x'), x_lo = bf16(x' - x_hi) (read by the tensor-core SSD
+// kernels, which multiply both planes against exact bf16 operands).
+//
+// One thread per 16-byte channel vector and 16 consecutive steps: the three inputs before
+// its current step slide through registers, so each input row is read once per thread
+// (plus a three-row halo per 16 steps); a warp's loads and stores are 512-byte rows.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <algorithm>
 
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
@@ -19,6 +25,9 @@ namespace ssm {
 namespace {
 
 constexpr int kConvThreads = 256;
+constexpr int kConvTT = 16;  // steps per thread
+constexpr int kConvVX = 32;  // channel vectors per block
+constexpr int kConvTY = kConvThreads / kConvVX;  // step blocks per block
 
 struct ConvArgs {
     const void* x;
@@ -31,26 +40,99 @@ struct ConvArgs {
     int K;
 };
 
-template <typename T>
-__device__ __forceinline__ float x_at(const ConvArgs& a, int64_t b, int64_t s, int64_t c) {
-    if (s >= 0) return to_f32<T>(static_cast<const T*>(a.x)[(b * a.T + s) * a.ch + c]);
-    const int64_t j = a.K - 1 + s;  // row of x_prev
-    if (a.x_prev && j >= 0) return to_f32<T>(static_cast<const T*>(a.x_prev)[(b * (a.K - 1) + j) * a.ch + c]);
-    return 0.0f;
+// One 16-byte vector of inputs (VW channels from c0) at step s, fp32; rows before t = 0
+// come from x_prev, else zero.
+template <typename T, int VW>
+__device__ __forceinline__ void load_vec(const ConvArgs& a, int64_t b, int64_t s, int64_t c0, float (&v)[VW]) {
+    const T* src = nullptr;
+    if (s >= 0)
+        src = static_cast<const T*>(a.x) + (b * a.T + s) * a.ch + c0;
+    else if (a.x_prev && a.K - 1 + s >= 0)
+        src = static_cast<const T*>(a.x_prev) + (b * (a.K - 1) + (a.K - 1 + s)) * a.ch + c0;
+    if (!src) {
+#pragma unroll
+        for (int j = 0; j < VW; ++j) v[j] = 0.0f;
+        return;
+    }
+    const uint4 r = *reinterpret_cast<const uint4*>(src);
+    if constexpr (sizeof(T) == 2) {
+        const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&r);
+#pragma unroll
+        for (int j = 0; j < VW / 2; ++j) {
+            const float2 f = __bfloat1622float2(p[j]);
+            v[2 * j] = f.x;
+            v[2 * j + 1] = f.y;
+        }
+    } else {
+        const float* p = reinterpret_cast<const float*>(&r);
+#pragma unroll
+        for (int j = 0; j < VW; ++j) v[j] = p[j];
+    }
 }
 
-template <typename T>
+// SPLIT: xc holds the bf16 planes x_hi (first batch*T*ch elements) and x_lo; else fp32.
+template <typename T, bool SPLIT>
 __global__ void __launch_bounds__(kConvThreads) conv_silu_kernel(const ConvArgs a) {
+    constexpr int VW = 16 / (int)sizeof(T);  // channels per thread
     constexpr bool PRECISE = sizeof(T) == 4;
-    const int64_t i = (int64_t)blockIdx.x * kConvThreads + threadIdx.x;  // flat (b, t, c)
-    const int64_t total = a.batch * a.T * a.ch;
-    if (i >= total) return;
-    const int64_t c = i % a.ch;
-    const int64_t t = (i / a.ch) % a.T;
-    const int64_t b = i / (a.ch * a.T);
-    float acc = a.bias ? a.bias[c] : 0.0f;
-    for (int k = 0; k < a.K; ++k) acc = fmaf(a.w[c * a.K + k], x_at<T>(a, b, t - a.K + 1 + k, c), acc);
-    static_cast<float*>(a.xc)[i] = silu_t<PRECISE>(acc);
+    const int64_t c0 = ((int64_t)blockIdx.x * kConvVX + threadIdx.x) * VW;
+    const int64_t b = blockIdx.z;
+    if (c0 >= a.ch) return;
+    // taps left-padded to width 4: tap k weights the input at t - 3 + k
+    float w[4][VW], bias[VW];
+#pragma unroll
+    for (int j = 0; j < VW; ++j) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int kk = k - (4 - a.K);
+            w[k][j] = kk >= 0 ? a.w[(c0 + j) * a.K + kk] : 0.0f;
+        }
+        bias[j] = a.bias ? a.bias[c0 + j] : 0.0f;
+    }
+    const int64_t plane = a.batch * a.T * a.ch;
+    for (int64_t t0 = ((int64_t)blockIdx.y * kConvTY + threadIdx.y) * kConvTT; t0 < a.T;
+         t0 += (int64_t)gridDim.y * kConvTY * kConvTT) {
+        float win[3][VW];  // inputs at t-3, t-2, t-1
+#pragma unroll
+        for (int r = 0; r < 3; ++r) load_vec<T, VW>(a, b, t0 - 3 + r, c0, win[r]);
+        const int tt = (int)min((int64_t)kConvTT, a.T - t0);
+        for (int i = 0; i < tt; ++i) {
+            const int64_t t = t0 + i;
+            float cur[VW], y[VW];
+            load_vec<T, VW>(a, b, t, c0, cur);
+#pragma unroll
+            for (int j = 0; j < VW; ++j) {
+                float acc = fmaf(w[0][j], win[0][j], bias[j]);
+                acc = fmaf(w[1][j], win[1][j], acc);
+                acc = fmaf(w[2][j], win[2][j], acc);
+                acc = fmaf(w[3][j], cur[j], acc);
+                y[j] = silu_t<PRECISE>(acc);
+                win[0][j] = win[1][j];
+                win[1][j] = win[2][j];
+                win[2][j] = cur[j];
+            }
+            const int64_t o = (b * a.T + t) * a.ch + c0;
+            if constexpr (SPLIT) {
+                uint32_t hi[VW / 2], lo[VW / 2];
+#pragma unroll
+                for (int j = 0; j < VW / 2; ++j) {
+                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(y[2 * j], y[2 * j + 1]);
+                    const float2 hf = __bfloat1622float2(h2);
+                    const __nv_bfloat162 l2 = __floats2bfloat162_rn(y[2 * j] - hf.x, y[2 * j + 1] - hf.y);
+                    hi[j] = *reinterpret_cast<const uint32_t*>(&h2);
+                    lo[j] = *reinterpret_cast<const uint32_t*>(&l2);
+                }
+                __nv_bfloat16* xh = static_cast<__nv_bfloat16*>(a.xc);
+                *reinterpret_cast<uint4*>(xh + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4*>(xh + plane + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            } else {
+                float* xf = static_cast<float*>(a.xc) + o;
+#pragma unroll
+                for (int j = 0; j < VW; j += 4)
+                    *reinterpret_cast<float4*>(xf + j) = make_float4(y[j], y[j + 1], y[j + 2], y[j + 3]);
+            }
+        }
+    }
 }
 
 // x_last[b, j, c] = input at time T-K+1+j (raw copy).
@@ -88,16 +170,25 @@ ConvArgs conv_args(const ScanArgs& a, void* xc) {
 
 }  // namespace
 
-cudaError_t conv_prepass_launch(const ScanArgs& a, void* xc, cudaStream_t stream) {
+cudaError_t conv_prepass_launch(const ScanArgs& a, void* xc, bool split, cudaStream_t stream) {
     const ConvArgs c = conv_args(a, xc);
-    const int64_t total = c.batch * c.T * c.ch;
-    if (total == 0) return cudaSuccess;
-    const unsigned blocks = (unsigned)((total + kConvThreads - 1) / kConvThreads);
+    if (c.batch * c.T * c.ch == 0) return cudaSuccess;
+    if (split && a.dtype != 1) return cudaErrorInvalidValue;  // planes are for bf16 inputs
+    const int vw = a.dtype == 1 ? 8 : 4;  // channels per 16-byte vector (ch is a multiple)
+    const int64_t nvec = c.ch / vw;
+    const int64_t tblocks = (c.T + kConvTT * kConvTY - 1) / (kConvTT * kConvTY);
+    const dim3 grid((unsigned)((nvec + kConvVX - 1) / kConvVX), (unsigned)std::min<int64_t>(tblocks, 65535),
+                    (unsigned)c.batch);
+    const dim3 block(kConvVX, kConvTY);
     cudaEvent_t t0 = timing_begin(stream);
-    if (a.dtype == 1)
-        conv_silu_kernel<__nv_bfloat16><<<blocks, kConvThreads, 0, stream>>>(c);
-    else
-        conv_silu_kernel<float><<<blocks, kConvThreads, 0, stream>>>(c);
+    if (a.dtype == 1) {
+        if (split)
+            conv_silu_kernel<__nv_bfloat16, true><<<grid, block, 0, stream>>>(c);
+        else
+            conv_silu_kernel<__nv_bfloat16, false><<<grid, block, 0, stream>>>(c);
+    } else {
+        conv_silu_kernel<float, false><<<grid, block, 0, stream>>>(c);
+    }
     note_launch("conv_silu_kernel", stream, t0);
     return cudaGetLastError();
 }

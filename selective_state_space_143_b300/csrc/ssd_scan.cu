@@ -461,11 +461,15 @@ cudaError_t ssd_launch_typed(const ScanArgs& a, void* ws, cudaStream_t stream) {
     const unsigned nP = (unsigned)((a.headdim + kTile - 1) / kTile);
     const unsigned nN = (unsigned)((a.dstate + kTile - 1) / kTile);
     const unsigned nTq = (unsigned)((pl.Q + kTile - 1) / kTile);
-    // The tensor-core kernels take x as an exact bf16 MMA operand; an fp32 x (the
-    // convolved input) runs on the CUDA-core kernels.
-    if (pl.nchunks > 0 && !a.x_f32 && ssd_tc_supported(a, pl.Q) && !force_cuda_cores()) {
+    // The tensor-core kernels take x as an exact bf16 MMA operand, or as bf16 hi/lo
+    // planes (the convolved input where ssd_conv_split holds); an fp32 x runs on the
+    // CUDA-core kernels.
+    const bool tc = pl.nchunks > 0 && !a.x_f32 && ssd_tc_supported(a, pl.Q) && !force_cuda_cores();
+    if (a.x_lo && !tc) return cudaErrorInvalidValue;  // split planes exist only for the tc kernels
+    if (tc) {
         SsdTcArgs t;
         t.x = (const __nv_bfloat16*)a.x;
+        t.x_lo = (const __nv_bfloat16*)a.x_lo;
         t.dt = (const __nv_bfloat16*)a.dt;
         t.z = (const __nv_bfloat16*)a.z;
         t.B = (const __nv_bfloat16*)a.B;
@@ -521,6 +525,11 @@ cudaError_t ssd_launch_typed(const ScanArgs& a, void* ws, cudaStream_t stream) {
 }
 
 }  // namespace
+
+bool ssd_conv_split(const ScanArgs& a) {
+    const SsdPlan pl = ssd_plan(a);
+    return pl.nchunks > 0 && ssd_tc_supported(a, pl.Q) && !force_cuda_cores();
+}
 
 size_t ssd_workspace_bytes(const ScanArgs& a) {
     if (a.batch == 0) return 0;

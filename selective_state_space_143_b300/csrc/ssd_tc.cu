@@ -35,7 +35,7 @@ namespace ssm {
 namespace {
 
 constexpr int kP = 64;         // headdim handled here
-constexpr int kThreads = 256;      // state kernel: 8 warps, TMEM lanes 32*(w%4).., column half w/4
+constexpr int kThreads = 256;      // state kernel: 8 warps (16 with split x), TMEM lanes 32*(w%4).., column part w/4
 constexpr int kScanThreads = 512;  // scan kernel: 16 warps, TMEM lanes 32*(w%4).., column quarter w/4
 constexpr int kStatusTimeout = 8;
 
@@ -141,14 +141,18 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 
 // State kernel configuration: heads per CTA (a divisor of the heads per group, so that
 // every head of the CTA reads the same B rows) and the K-part of Q taken per step.
-template <int N>
+// XS: x arrives as bf16 hi/lo planes (the convolved input); both planes are prefetched,
+// so the kernel runs 16 warps to keep the per-thread registers of the prefetch the same.
+template <int N, bool XS = false>
 struct StateTcCfg {
+    static constexpr int NT = XS ? 512 : kThreads;            // threads
+    static constexpr int PL = XS ? 2 : 1;                     // x planes
     static constexpr int KS = N > 128 ? 64 : 128;             // rows s per step
     static constexpr size_t kB = (size_t)256 * N * 2;         // B rows [0, Q), resident
     static constexpr size_t kXPart = (size_t)128 * KS * 2;    // one Xd part, hi or lo
     static constexpr size_t kSmem = kB + 4 * kXPart;          // + 2 stages x (hi, lo)
     static constexpr int kMaxHeads = 8;
-    static constexpr int XCH = 128 * KS / 8 / kThreads;       // 8-element x chunks per thread
+    static constexpr int XCH = 128 * KS / 8 / NT;             // 8-element x chunks per thread
 };
 
 // grid (nchunks, H / hpc, b); 256 threads.  S_c^T for hpc heads of chunk c, two heads
@@ -158,12 +162,12 @@ struct StateTcCfg {
 // step n+1 is in flight (registers) while step n's weighted, hi/lo-split Xd is written
 // to stage buffer n%2 and the MMAs of step n-1 run; a pair's epilogue (TMEM -> states)
 // runs once the next pair's first MMAs are queued, from alternating accumulators.
-template <int N>
-__global__ void __launch_bounds__(kThreads) ssd_state_tc(const SsdTcArgs a, int hpc) {
-    using Cfg = StateTcCfg<N>;
-    constexpr int KS = Cfg::KS;
+template <int N, bool XS>
+__global__ void __launch_bounds__(StateTcCfg<N, XS>::NT) ssd_state_tc(const SsdTcArgs a, int hpc) {
+    using Cfg = StateTcCfg<N, XS>;
+    constexpr int KS = Cfg::KS, NT = Cfg::NT, PL = Cfg::PL;
     extern __shared__ __align__(1024) unsigned char smem[];
-    __shared__ float s_w[Cfg::kMaxHeads][256], s_warp[8 * Cfg::kMaxHeads];
+    __shared__ float s_w[Cfg::kMaxHeads][256], s_warp[NT / 32 * Cfg::kMaxHeads];
     __shared__ uint32_t s_tmem;
     __shared__ __align__(8) uint64_t s_mbar[2];
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -179,7 +183,7 @@ __global__ void __launch_bounds__(kThreads) ssd_state_tc(const SsdTcArgs a, int 
     // B rows of the chunk, once
     {
         const uint32_t bb = tc::smem_u32(sB);
-        for (int i = tid; i < Q * (N / 8); i += kThreads) {
+        for (int i = tid; i < Q * (N / 8); i += NT) {
             int s, nc;
             mnmajor_item(i, N / 8, s, nc);
             const bool ok = s < len;
@@ -196,37 +200,48 @@ __global__ void __launch_bounds__(kThreads) ssd_state_tc(const SsdTcArgs a, int 
         tc::mbar_fence_init();
     }
 
-    // raw x of step n in registers: rows s in [kp*KS, +KS) of heads (pair, pair+1); two
-    // register sets, so that steps n+1 and n+2 are in flight while step n is built
-    uint4 pfa[Cfg::XCH], pfb[Cfg::XCH];
-    auto prefetch = [&](int n, uint4 (&pf)[Cfg::XCH]) {
+    // raw x of step n in registers: rows s in [kp*KS, +KS) of heads (pair, pair+1), each
+    // plane; two register sets, so that steps n+1 and n+2 are in flight while step n is
+    // built
+    uint4 pfa[PL][Cfg::XCH], pfb[PL][Cfg::XCH];
+    auto prefetch = [&](int n, uint4 (&pf)[PL][Cfg::XCH]) {
         const int pair = n / nkp, kp = n % nkp;
 #pragma unroll
         for (int j = 0; j < Cfg::XCH; ++j) {
             int sl, mc;
-            mnmajor_item(tid + j * kThreads, 16, sl, mc);
+            mnmajor_item(tid + j * NT, 16, sl, mc);
             const int s = kp * KS + sl, m0 = mc * 8;
             const int64_t h = hbeg + 2 * pair + m0 / kP;
-            pf[j] = make_uint4(0, 0, 0, 0);
-            if (s < len) pf[j] = *reinterpret_cast<const uint4*>(a.x + ((b * a.T + c * a.Q + s) * a.H + h) * kP + m0 % kP);
+            const int64_t o = ((b * a.T + c * a.Q + s) * a.H + h) * kP + m0 % kP;
+#pragma unroll
+            for (int pl = 0; pl < PL; ++pl) {
+                pf[pl][j] = make_uint4(0, 0, 0, 0);
+                if (s < len) pf[pl][j] = *reinterpret_cast<const uint4*>((pl ? a.x_lo : a.x) + o);
+            }
         }
     };
     // Xd of step n -> stage n%2, hi/lo
-    auto build = [&](int n, const uint4 (&pf)[Cfg::XCH]) {
+    auto build = [&](int n, const uint4 (&pf)[PL][Cfg::XCH]) {
         const int pair = n / nkp, kp = n % nkp;
         unsigned char* st = sX + (n & 1) * 2 * Cfg::kXPart;
         const uint32_t bh = tc::smem_u32(st), bl = tc::smem_u32(st + Cfg::kXPart);
 #pragma unroll
         for (int j = 0; j < Cfg::XCH; ++j) {
             int sl, mc;
-            mnmajor_item(tid + j * kThreads, 16, sl, mc);
+            mnmajor_item(tid + j * NT, 16, sl, mc);
             const int m0 = mc * 8;
             const float w = s_w[2 * pair + m0 / kP][kp * KS + sl];
-            const __nv_bfloat162* r2 = reinterpret_cast<const __nv_bfloat162*>(&pf[j]);
+            const __nv_bfloat162* r2 = reinterpret_cast<const __nv_bfloat162*>(&pf[0][j]);
+            const __nv_bfloat162* l2 = reinterpret_cast<const __nv_bfloat162*>(&pf[PL - 1][j]);
             uint32_t hi[4], lo[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const float2 f = __bfloat1622float2(r2[k]);
+                float2 f = __bfloat1622float2(r2[k]);
+                if (XS) {  // x' = x_hi + x_lo
+                    const float2 fl = __bfloat1622float2(l2[k]);
+                    f.x += fl.x;
+                    f.y += fl.y;
+                }
                 split2(f.x * w, f.y * w, hi[k], lo[k]);
             }
             const uint32_t off = tc::off_mnmajor(m0, sl, 128);
@@ -235,7 +250,7 @@ __global__ void __launch_bounds__(kThreads) ssd_state_tc(const SsdTcArgs a, int 
         }
     };
     // accumulator of pair -> the (b, c, h) state tile; warp w: lanes 32*(w%4).., column
-    // half w/4.  Split-ready layout: the 8 values of (p, n..n+7) go as two float4 to the
+    // part w/4 (halves with 8 warps, quarters with 16).  Split-ready layout: the 8 values of (p, n..n+7) go as two float4 to the
     // byte offsets that their bf16 hi and lo halves take in the scan kernel's K-major
     // tile (offset o in the first P*N*2 bytes, and o + P*N*2), so that the carry pass can
     // convert every unit in place (see ssd_state_pass_split).
@@ -247,7 +262,7 @@ __global__ void __launch_bounds__(kThreads) ssd_state_tc(const SsdTcArgs a, int 
         char* tile = reinterpret_cast<char*>(a.states + ((b * a.nchunks + c) * a.H + h) * (int64_t)kP * N);
         constexpr uint32_t kHalf = (uint32_t)kP * N * 2;
         const uint32_t acc = tmem + (uint32_t)((pair & 1) * N);
-        constexpr int NH = N / 2 < 16 ? 16 : N / 2;
+        constexpr int NH = N / (NT / 128) < 16 ? 16 : N / (NT / 128);  // a multiple of 16
 #pragma unroll 1
         for (int n0 = (warp >> 2) * NH; n0 < N && n0 < ((warp >> 2) + 1) * NH; n0 += 16) {
             float v[16];
@@ -284,7 +299,7 @@ __global__ void __launch_bounds__(kThreads) ssd_state_tc(const SsdTcArgs a, int 
         ok = tc::mbar_wait(&s_mbar[n & 1], (uint32_t)(n >> 1) & 1u) && ok;
         tc::fence_after_sync();
     };
-    auto step = [&](int n, uint4 (&pf)[Cfg::XCH]) {
+    auto step = [&](int n, uint4 (&pf)[PL][Cfg::XCH]) {
         const int pair = n / nkp, kp = n % nkp;
         if (n >= 2) wait_commit(n - 2);  // stage n%2 free again
         build(n, pf);
@@ -353,7 +368,11 @@ struct ScanTcCfg {
 //              previous part's MMAs (Y_diag += M'_hi X + M'_lo X; Y_off with part 0);
 //   finish   : the epilogue of head h-1, from its own TMEM accumulators, right after
 //              head h's first MMAs are issued.
-template <int N, bool GATE>
+// XS (x' = x_hi + x_lo, the convolved input): both x buffers hold the current head's
+// planes; Y_diag adds M'_hi X_lo (M'_lo X_lo is below the split's own rounding); the
+// next head's planes are copied in once this head's last MMAs are done, while its first
+// M' part is built; the skip term reads x' from global memory.
+template <int N, bool GATE, bool XS>
 __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_tc(const SsdTcArgs a, int heads_per_cta) {
     using Cfg = ScanTcCfg<N>;
     constexpr int KPC = Cfg::KPC;
@@ -456,14 +475,15 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_tc(const SsdTcArgs a
         for (int i = tid; i < (int)(2 * Cfg::kH / 16); i += kScanThreads) cp_async16(dst + 16 * i, src + 16 * i, true);
         asm volatile("cp.async.commit_group;\n" ::);
     };
-    // x_h of head hn -> buffer xbuf (MN-major, rows s < SW; rows past len are zero-filled)
-    auto load_x = [&](int64_t hn, int xbuf) {
+    // x_h of head hn (plane: x, or x_lo) -> buffer xbuf (MN-major, rows s < SW; rows past
+    // len are zero-filled)
+    auto load_x = [&](const __nv_bfloat16* plane, int64_t hn, int xbuf) {
         const uint32_t xb = tc::smem_u32(sX + xbuf * Cfg::kX);
         for (int i = tid; i < SW * (kP / 8); i += kScanThreads) {
             int s, pc;
             mnmajor_item(i, kP / 8, s, pc);
             const bool okr = s < len;
-            const __nv_bfloat16* src = a.x + (okr ? ((b * a.T + c * a.Q + s) * a.H + hn) * kP + pc * 8 : 0);
+            const __nv_bfloat16* src = plane + (okr ? ((b * a.T + c * a.Q + s) * a.H + hn) * kP + pc * 8 : 0);
             cp_async16(xb + tc::off_mnmajor(pc * 8, s, kP), src, okr);
         }
         asm volatile("cp.async.commit_group;\n" ::);
@@ -483,7 +503,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_tc(const SsdTcArgs a
             s_cum[tid] = pf_cum;
             s_beta[tid] = (pf_dl > 0.0f ? lg2(pf_dl) : -INFINITY) - pf_cum * kLog2e;
         }
-        asm volatile("cp.async.wait_group 0;\n" ::);  // this head's x_h and h tiles (visible after the sync)
+        // this head's x_h and h tiles (visible after the sync); XS waits before its first MMAs
+        if (!XS) asm volatile("cp.async.wait_group 0;\n" ::);
     };
     // epilogue of head hh from accumulator set acc: y = Y_diag + exp(cum_t) Y_off + D x, gate
     auto finish = [&](int64_t hh, int acc, float alpha_h) {
@@ -501,14 +522,26 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_tc(const SsdTcArgs a
                 uint32_t pk[8];
 #pragma unroll
                 for (int j = 0; j < 16; j += 8) {
-                    const uint4 xr = *reinterpret_cast<const uint4*>(xs + tc::off_mnmajor(p0 + j, t, kP));
+                    uint4 xr, xl = make_uint4(0, 0, 0, 0);
+                    if (XS) {
+                        xr = *reinterpret_cast<const uint4*>(a.x + row + p0 + j);
+                        xl = *reinterpret_cast<const uint4*>(a.x_lo + row + p0 + j);
+                    } else {
+                        xr = *reinterpret_cast<const uint4*>(xs + tc::off_mnmajor(p0 + j, t, kP));
+                    }
                     const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&xr);
+                    const __nv_bfloat162* xl2 = reinterpret_cast<const __nv_bfloat162*>(&xl);
                     uint4 zr = make_uint4(0, 0, 0, 0);
                     if (GATE) zr = *reinterpret_cast<const uint4*>(a.z + row + p0 + j);
                     const __nv_bfloat162* z2 = reinterpret_cast<const __nv_bfloat162*>(&zr);
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        const float2 xv = __bfloat1622float2(x2[k]);
+                        float2 xv = __bfloat1622float2(x2[k]);
+                        if (XS) {
+                            const float2 lv = __bfloat1622float2(xl2[k]);
+                            xv.x += lv.x;
+                            xv.y += lv.y;
+                        }
                         float y0 = fmaf(et, yo[j + 2 * k], yd[j + 2 * k]) + Dh * xv.x;
                         float y1 = fmaf(et, yo[j + 2 * k + 1], yd[j + 2 * k + 1]) + Dh * xv.y;
                         if (GATE) {
@@ -528,7 +561,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_tc(const SsdTcArgs a
 
     if (ok) {
         prefetch(hbeg);
-        load_x(hbeg, 0);
+        load_x(a.x, hbeg, 0);
+        if (XS) load_x(a.x_lo, hbeg, 1);
         load_h(hbeg, 0);
     }
     uint32_t last_commit_prev = 0;  // the previous head's last commit
@@ -585,6 +619,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_tc(const SsdTcArgs a
                     st_shared_v4(ml + tc::off_kmajor(r, sl + 8 * j, KPC), pl[4 * j], pl[4 * j + 1], pl[4 * j + 2], pl[4 * j + 3]);
                 }
             }
+            // XS: this head's x planes (copied in while the part was built) before its MMAs
+            if (XS && kp == 0) asm volatile("cp.async.wait_group 0;\n" ::);
             tc::fence_async_smem();
             tc::fence_before_sync();
             __syncthreads();
@@ -595,8 +631,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_tc(const SsdTcArgs a
                 constexpr uint32_t id_diag = tc::idesc_bf16(128, kP, 0, 1);
                 const uint64_t dmh = tc::desc_kmajor(tc::smem_u32(part), KPC, 0);
                 const uint64_t dml = tc::desc_kmajor(tc::smem_u32(part + Cfg::kMPart), KPC, 0);
-                // x_h descriptor at this part's first k-step
-                const uint64_t dx = tc::desc_mnmajor(tc::smem_u32(sX + (hi & 1) * Cfg::kX), kP, KPC / 16 * kp);
+                // x_h descriptor at this part's first k-step (XS: buffer 0 x_hi, 1 x_lo)
+                const uint64_t dx = tc::desc_mnmajor(tc::smem_u32(sX + (XS ? 0 : (hi & 1)) * Cfg::kX), kP, KPC / 16 * kp);
 #pragma unroll
                 for (int ks = 0; ks < KPC / 16; ++ks)
                     tc::mma_bf16(tYd, dmh + ks * tc::kstep_kmajor(), dx + ks * tc::kstep_mnmajor(kP), id_diag,
@@ -604,6 +640,12 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_tc(const SsdTcArgs a
 #pragma unroll
                 for (int ks = 0; ks < KPC / 16; ++ks)
                     tc::mma_bf16(tYd, dml + ks * tc::kstep_kmajor(), dx + ks * tc::kstep_mnmajor(kP), id_diag, 1);
+                if (XS) {
+                    const uint64_t dxl = tc::desc_mnmajor(tc::smem_u32(sX + Cfg::kX), kP, KPC / 16 * kp);
+#pragma unroll
+                    for (int ks = 0; ks < KPC / 16; ++ks)
+                        tc::mma_bf16(tYd, dmh + ks * tc::kstep_kmajor(), dxl + ks * tc::kstep_mnmajor(kP), id_diag, 1);
+                }
                 if (kp == 0) {
                     constexpr uint32_t id_off = tc::idesc_bf16(128, kP, 0, 0);
                     const uint64_t dc = tc::desc_kmajor(tc::smem_u32(sC), N, 0);
@@ -630,10 +672,16 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_tc(const SsdTcArgs a
                 }
                 if (hi + 1 < heads_per_cta) {
                     __syncthreads();  // every thread is done reading the buffer in finish
-                    load_x(h + 1, (hi + 1) & 1);
+                    if (!XS) load_x(a.x, h + 1, (hi + 1) & 1);
                     // two h tile sets: the previous head's (its MMAs are done) takes the next
                     if (Cfg::kHBufs == 2) load_h(h + 1, (hi + 1) & 1);
                 }
+            }
+            // XS: both x buffers are free once this head's last MMAs are done
+            if (XS && kp == nparts - 1 && hi + 1 < heads_per_cta) {
+                wait_commit(ncommit - 1);
+                load_x(a.x, h + 1, 0);
+                load_x(a.x_lo, h + 1, 1);
             }
         }
         last_commit_prev = ncommit - 1;
@@ -668,24 +716,24 @@ int heads_per_cta(const SsdTcArgs& s, int max_heads) {
     return 1;
 }
 
-template <int N>
+template <int N, bool XS>
 cudaError_t launch_state(const SsdTcArgs& s, int64_t batch, cudaStream_t stream) {
-    using Cfg = StateTcCfg<N>;
+    using Cfg = StateTcCfg<N, XS>;
     const size_t smem = Cfg::kSmem;
-    cudaError_t e = cudaFuncSetAttribute(ssd_state_tc<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(ssd_state_tc<N, XS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int hpc = heads_per_cta(s, Cfg::kMaxHeads);  // even: heads per group are even here
     cudaEvent_t t0 = timing_begin(stream);
-    ssd_state_tc<N><<<dim3((unsigned)s.nchunks, (unsigned)(s.H / hpc), (unsigned)batch), kThreads, smem, stream>>>(s, hpc);
+    ssd_state_tc<N, XS><<<dim3((unsigned)s.nchunks, (unsigned)(s.H / hpc), (unsigned)batch), Cfg::NT, smem, stream>>>(s, hpc);
     note_launch("ssd_state_tc", stream, t0);
     return cudaGetLastError();
 }
 
-template <int N, bool GATE>
+template <int N, bool GATE, bool XS>
 cudaError_t launch_scan(const SsdTcArgs& s, int64_t batch, cudaStream_t stream) {
     // at least 116 KB so that one CTA (holding all 512 TMEM columns) runs per SM
     const size_t smem = std::max<size_t>(ScanTcCfg<N>::kSmem, 116 * 1024);
-    auto kern = ssd_scan_tc<N, GATE>;
+    auto kern = ssd_scan_tc<N, GATE, XS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int hpc = heads_per_cta(s, 8);  // G = C B^T is shared by the CTA's heads
@@ -699,20 +747,36 @@ cudaError_t launch_scan(const SsdTcArgs& s, int64_t batch, cudaStream_t stream) 
 }  // namespace
 
 cudaError_t ssd_tc_chunk_state(const SsdTcArgs& s, int64_t batch, cudaStream_t stream) {
+    if (s.x_lo) {
+        switch (s.N) {
+            case 32: return launch_state<32, true>(s, batch, stream);
+            case 64: return launch_state<64, true>(s, batch, stream);
+            case 128: return launch_state<128, true>(s, batch, stream);
+            default: return launch_state<256, true>(s, batch, stream);
+        }
+    }
     switch (s.N) {
-        case 32: return launch_state<32>(s, batch, stream);
-        case 64: return launch_state<64>(s, batch, stream);
-        case 128: return launch_state<128>(s, batch, stream);
-        default: return launch_state<256>(s, batch, stream);
+        case 32: return launch_state<32, false>(s, batch, stream);
+        case 64: return launch_state<64, false>(s, batch, stream);
+        case 128: return launch_state<128, false>(s, batch, stream);
+        default: return launch_state<256, false>(s, batch, stream);
     }
 }
 
 cudaError_t ssd_tc_chunk_scan(const SsdTcArgs& s, int64_t batch, bool gate, cudaStream_t stream) {
+    if (s.x_lo) {
+        switch (s.N) {
+            case 32: return gate ? launch_scan<32, true, true>(s, batch, stream) : launch_scan<32, false, true>(s, batch, stream);
+            case 64: return gate ? launch_scan<64, true, true>(s, batch, stream) : launch_scan<64, false, true>(s, batch, stream);
+            case 128: return gate ? launch_scan<128, true, true>(s, batch, stream) : launch_scan<128, false, true>(s, batch, stream);
+            default: return gate ? launch_scan<256, true, true>(s, batch, stream) : launch_scan<256, false, true>(s, batch, stream);
+        }
+    }
     switch (s.N) {
-        case 32: return gate ? launch_scan<32, true>(s, batch, stream) : launch_scan<32, false>(s, batch, stream);
-        case 64: return gate ? launch_scan<64, true>(s, batch, stream) : launch_scan<64, false>(s, batch, stream);
-        case 128: return gate ? launch_scan<128, true>(s, batch, stream) : launch_scan<128, false>(s, batch, stream);
-        default: return gate ? launch_scan<256, true>(s, batch, stream) : launch_scan<256, false>(s, batch, stream);
+        case 32: return gate ? launch_scan<32, true, false>(s, batch, stream) : launch_scan<32, false, false>(s, batch, stream);
+        case 64: return gate ? launch_scan<64, true, false>(s, batch, stream) : launch_scan<64, false, false>(s, batch, stream);
+        case 128: return gate ? launch_scan<128, true, false>(s, batch, stream) : launch_scan<128, false, false>(s, batch, stream);
+        default: return gate ? launch_scan<256, true, false>(s, batch, stream) : launch_scan<256, false, false>(s, batch, stream);
     }
 }
 

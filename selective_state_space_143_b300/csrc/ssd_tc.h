@@ -10,7 +10,8 @@
 namespace ssm {
 
 struct SsdTcArgs {
-    const __nv_bfloat16* x;
+    const __nv_bfloat16* x;     // x, or x_hi of the split convolved input
+    const __nv_bfloat16* x_lo;  // null, or x_lo: x' = x_hi + x_lo
     const __nv_bfloat16* dt;
     const __nv_bfloat16* z;
     const __nv_bfloat16* B;

@@ -153,6 +153,7 @@ ScanArgs make_args(const void* x, const void* dt, const float* A, const void* B,
     a.x_last = nullptr;
     a.conv_k = 0;
     a.x_f32 = 0;
+    a.x_lo = nullptr;
     a.out = out;
     a.final_state = final_state;
     a.batch = s->batch;
@@ -187,11 +188,15 @@ int run(const ScanArgs& a, int mode, void* ws, cudaStream_t stream) {
     } else if (a.conv_k > 0) {
         // convolution pass into scratch, then the SSD kernels on the convolved input
         void* xc = (char*)ws + align_up(ssd_workspace_bytes(a), 256);
-        e = conv_prepass_launch(a, xc, stream);
+        const bool split = ssd_conv_split(a);
+        e = conv_prepass_launch(a, xc, split, stream);
         if (e == cudaSuccess) {
             ScanArgs b = a;
             b.x = xc;
-            b.x_f32 = 1;
+            if (split)
+                b.x_lo = (const char*)xc + (size_t)a.batch * a.seqlen * a.nheads * a.headdim * 2;
+            else
+                b.x_f32 = 1;
             b.conv_k = 0;
             e = ssd_launch(b, ws, stream);
         }

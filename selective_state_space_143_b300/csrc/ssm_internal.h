@@ -24,8 +24,10 @@ struct ScanArgs {
     const void* x_prev;          // (batch, conv_k-1, channels) nullable: inputs before t = 0
     void* x_last;                // (batch, conv_k-1, channels) nullable: last inputs, written
     int conv_k;
-    int x_f32;                   // x is stored as fp32 whatever dtype says (SSD after the
-                                 // convolution pass)
+    int x_f32;                   // x is stored as fp32 whatever dtype says (the convolved
+                                 // input on the CUDA-core SSD kernels)
+    const void* x_lo;            // nullable: x is bf16 x_hi (at x) + x_lo (here), the
+                                 // convolved input on the tensor-core SSD kernels
     void* out;
     float* final_state;
     int64_t batch, seqlen, nheads, headdim, dstate, ngroups, chunk;
@@ -47,6 +49,9 @@ cudaError_t diag_launch(const ScanArgs& a, void* ws, cudaStream_t stream);
 // SSD (Mamba-2) path.
 size_t ssd_workspace_bytes(const ScanArgs& a);
 cudaError_t ssd_launch(const ScanArgs& a, void* ws, cudaStream_t stream);
+// True when the SSD launcher takes the convolved input of this shape on the tensor-core
+// kernels, i.e. as bf16 hi/lo planes (else as fp32, on the CUDA-core kernels).
+bool ssd_conv_split(const ScanArgs& a);
 
 // Single-token step: the state (batch, nheads, headdim, dstate) is updated in place and
 // out (batch, nheads, headdim) written; diag_a selects A of shape (nheads, dstate).
@@ -63,10 +68,13 @@ struct ScanBwdArgs {
 size_t scan_bwd_workspace_bytes(const ScanArgs& a);
 cudaError_t scan_bwd_launch(const ScanBwdArgs& s, void* ws, cudaStream_t stream);
 
-// Convolution + SiLU of x into xc (same shape, fp32), and the last conv_k-1 inputs into
-// a.x_last; used ahead of the SSD kernels.  x' is kept in fp32: it is an intermediate,
-// and rounding it to bf16 would add an input error the scan's tolerance does not allow.
-cudaError_t conv_prepass_launch(const ScanArgs& a, void* xc, cudaStream_t stream);
+// Convolution + SiLU of x into xc, and the last conv_k-1 inputs into a.x_last; used
+// ahead of the SSD kernels.  x' keeps fp32 precision: it is an intermediate, and
+// rounding it to bf16 would add an input error the scan's tolerance does not allow.  xc
+// holds either fp32 x' (split false) or two bf16 planes of the same total size, x_hi =
+// bf16(x') followed by x_lo = bf16(x' - x_hi) (split true), so that x_hi + x_lo carries
+// 16 significant bits into bf16 tensor-core products.
+cudaError_t conv_prepass_launch(const ScanArgs& a, void* xc, bool split, cudaStream_t stream);
 cudaError_t conv_tail_launch(const ScanArgs& a, cudaStream_t stream);
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }

@@ -1,5 +1,6 @@
 """GPU parity of the causal depthwise convolution + SiLU ahead of the scan: the fused
-diagonal-mode kernels and the SSD path (a convolution pass, then the SSD kernels) against
+diagonal-mode kernels and the SSD path (a convolution pass, then the SSD kernels: the
+tensor-core ones on the split bf16 hi/lo convolved input where the shape allows) against
 the fp64 oracle (convolution, then the sequential scan), the carried last inputs bit for
 bit, and resume / token-by-token decoding with the convolution state carried.
 
@@ -32,6 +33,11 @@ CASES = [
     ("ssd", "f32", 1, 260, 2, 32, 16, 2, 0, 4, True, True),
     ("ssd", "bf16", 2, 300, 4, 64, 128, 2, 128, 4, True, True),
     ("ssd", "bf16", 1, 513, 2, 64, 256, 1, 256, 3, False, False),
+    # tensor-core kernels on the split convolved input, 8 heads per CTA (x planes reloaded
+    # for every head), both 128-row halves, ragged last chunk
+    ("ssd", "bf16", 1, 600, 16, 64, 128, 1, 256, 4, True, True),
+    ("ssd", "bf16", 2, 333, 8, 64, 64, 2, 128, 4, True, False),
+    ("ssd", "bf16", 1, 270, 8, 64, 32, 1, 256, 2, False, True),
 ]
 
 

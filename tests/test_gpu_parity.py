@@ -91,6 +91,8 @@ DIAG_CASES = [
     ("bf16", 2, 700, 64, 16, 1, 64),   # forced time segments
     ("bf16", 1, 1024, 32, 16, 1, 96),
     ("f32", 1, 450, 16, 8, 1, 32),
+    ("f32", 2, 77, 8, 64, 1, 0),       # largest state (N = 64), fp32
+    ("bf16", 4, 1, 16, 16, 2, 0),      # one token per sequence
 ]
 
 
@@ -110,6 +112,9 @@ SSD_CASES = [
     ("bf16", 1, 513, 2, 64, 256, 1, 256),
     ("bf16", 2, 97, 3, 80, 32, 1, 32),
     ("f32", 1, 260, 2, 32, 16, 2, 0),
+    ("bf16", 1, 150, 1, 256, 16, 1, 64),   # largest head dimension (P = 256)
+    ("f32", 1, 70, 2, 16, 256, 1, 32),     # largest state (N = 256), fp32
+    ("bf16", 1, 300, 4, 64, 128, 4, 256),  # one group per head
 ]
 
 
