@@ -96,40 +96,54 @@ __global__ void __launch_bounds__(kConvThreads) conv_silu_kernel(const ConvArgs 
 #pragma unroll
         for (int r = 0; r < 3; ++r) load_vec<T, VW>(a, b, t0 - 3 + r, c0, win[r]);
         const int tt = (int)min((int64_t)kConvTT, a.T - t0);
-        for (int i = 0; i < tt; ++i) {
-            const int64_t t = t0 + i;
-            float cur[VW], y[VW];
-            load_vec<T, VW>(a, b, t, c0, cur);
+        // four rows loaded together, then their four outputs
+        for (int i0 = 0; i0 < tt; i0 += 4) {
+            float cur[4][VW];
 #pragma unroll
-            for (int j = 0; j < VW; ++j) {
-                float acc = fmaf(w[0][j], win[0][j], bias[j]);
-                acc = fmaf(w[1][j], win[1][j], acc);
-                acc = fmaf(w[2][j], win[2][j], acc);
-                acc = fmaf(w[3][j], cur[j], acc);
-                y[j] = silu_t<PRECISE>(acc);
-                win[0][j] = win[1][j];
-                win[1][j] = win[2][j];
-                win[2][j] = cur[j];
-            }
-            const int64_t o = (b * a.T + t) * a.ch + c0;
-            if constexpr (SPLIT) {
-                uint32_t hi[VW / 2], lo[VW / 2];
+            for (int u = 0; u < 4; ++u) {
+                if (i0 + u < tt) {
+                    load_vec<T, VW>(a, b, t0 + i0 + u, c0, cur[u]);
+                } else {
 #pragma unroll
-                for (int j = 0; j < VW / 2; ++j) {
-                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(y[2 * j], y[2 * j + 1]);
-                    const float2 hf = __bfloat1622float2(h2);
-                    const __nv_bfloat162 l2 = __floats2bfloat162_rn(y[2 * j] - hf.x, y[2 * j + 1] - hf.y);
-                    hi[j] = *reinterpret_cast<const uint32_t*>(&h2);
-                    lo[j] = *reinterpret_cast<const uint32_t*>(&l2);
+                    for (int j = 0; j < VW; ++j) cur[u][j] = 0.0f;
                 }
-                __nv_bfloat16* xh = static_cast<__nv_bfloat16*>(a.xc);
-                *reinterpret_cast<uint4*>(xh + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4*>(xh + plane + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-            } else {
-                float* xf = static_cast<float*>(a.xc) + o;
+            }
 #pragma unroll
-                for (int j = 0; j < VW; j += 4)
-                    *reinterpret_cast<float4*>(xf + j) = make_float4(y[j], y[j + 1], y[j + 2], y[j + 3]);
+            for (int u = 0; u < 4; ++u) {
+                if (i0 + u >= tt) break;
+                const int64_t t = t0 + i0 + u;
+                float y[VW];
+#pragma unroll
+                for (int j = 0; j < VW; ++j) {
+                    float acc = fmaf(w[0][j], win[0][j], bias[j]);
+                    acc = fmaf(w[1][j], win[1][j], acc);
+                    acc = fmaf(w[2][j], win[2][j], acc);
+                    acc = fmaf(w[3][j], cur[u][j], acc);
+                    y[j] = silu_t<PRECISE>(acc);
+                    win[0][j] = win[1][j];
+                    win[1][j] = win[2][j];
+                    win[2][j] = cur[u][j];
+                }
+                const int64_t o = (b * a.T + t) * a.ch + c0;
+                if constexpr (SPLIT) {
+                    uint32_t hi[VW / 2], lo[VW / 2];
+#pragma unroll
+                    for (int j = 0; j < VW / 2; ++j) {
+                        const __nv_bfloat162 h2 = __floats2bfloat162_rn(y[2 * j], y[2 * j + 1]);
+                        const float2 hf = __bfloat1622float2(h2);
+                        const __nv_bfloat162 l2 = __floats2bfloat162_rn(y[2 * j] - hf.x, y[2 * j + 1] - hf.y);
+                        hi[j] = *reinterpret_cast<const uint32_t*>(&h2);
+                        lo[j] = *reinterpret_cast<const uint32_t*>(&l2);
+                    }
+                    __nv_bfloat16* xh = static_cast<__nv_bfloat16*>(a.xc);
+                    *reinterpret_cast<uint4*>(xh + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4*>(xh + plane + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                } else {
+                    float* xf = static_cast<float*>(a.xc) + o;
+#pragma unroll
+                    for (int j = 0; j < VW; j += 4)
+                        *reinterpret_cast<float4*>(xf + j) = make_float4(y[j], y[j + 1], y[j + 2], y[j + 3]);
+                }
             }
         }
     }

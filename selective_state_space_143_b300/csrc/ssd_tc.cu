@@ -368,10 +368,12 @@ struct ScanTcCfg {
 //              previous part's MMAs (Y_diag += M'_hi X + M'_lo X; Y_off with part 0);
 //   finish   : the epilogue of head h-1, from its own TMEM accumulators, right after
 //              head h's first MMAs are issued.
-// XS (x' = x_hi + x_lo, the convolved input): both x buffers hold the current head's
-// planes; Y_diag adds M'_hi X_lo (M'_lo X_lo is below the split's own rounding); the
-// next head's planes are copied in once this head's last MMAs are done, while its first
-// M' part is built; the skip term reads x' from global memory.
+// XS (x' = x_hi + x_lo, the convolved input): Y_diag adds M'_hi X_lo (M'_lo X_lo is
+// below the split's own rounding) and the skip term reads x' from global memory.  With
+// 128 rows s (first half) both planes fit in one x buffer and the head pipeline is as
+// above; with 256 rows the two buffers hold the current head's planes and the next
+// head's planes are copied in once this head's last MMAs are done, while its first M'
+// part is built.
 template <int N, bool GATE, bool XS>
 __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_tc(const SsdTcArgs a, int heads_per_cta) {
     using Cfg = ScanTcCfg<N>;
@@ -475,10 +477,15 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_tc(const SsdTcArgs a
         for (int i = tid; i < (int)(2 * Cfg::kH / 16); i += kScanThreads) cp_async16(dst + 16 * i, src + 16 * i, true);
         asm volatile("cp.async.commit_group;\n" ::);
     };
-    // x_h of head hn (plane: x, or x_lo) -> buffer xbuf (MN-major, rows s < SW; rows past
-    // len are zero-filled)
-    auto load_x = [&](const __nv_bfloat16* plane, int64_t hn, int xbuf) {
-        const uint32_t xb = tc::smem_u32(sX + xbuf * Cfg::kX);
+    // XS placement of the planes of head hi: serial (256 rows) x_hi in buffer 0 and x_lo
+    // in buffer 1; else both in buffer hi&1, x_lo after the SW rows of x_hi
+    const bool xser = XS && SW > 128;
+    auto x_hi_tile = [&](int hi_) { return sX + (xser ? 0 : (hi_ & 1)) * Cfg::kX; };
+    auto x_lo_tile = [&](int hi_) { return xser ? sX + Cfg::kX : x_hi_tile(hi_) + (size_t)SW * kP * 2; };
+    // x_h of head hn (plane: x, or x_lo) -> the tile at xt (MN-major, rows s < SW; rows
+    // past len are zero-filled)
+    auto load_x = [&](const __nv_bfloat16* plane, int64_t hn, unsigned char* xt) {
+        const uint32_t xb = tc::smem_u32(xt);
         for (int i = tid; i < SW * (kP / 8); i += kScanThreads) {
             int s, pc;
             mnmajor_item(i, kP / 8, s, pc);
@@ -561,8 +568,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_tc(const SsdTcArgs a
 
     if (ok) {
         prefetch(hbeg);
-        load_x(a.x, hbeg, 0);
-        if (XS) load_x(a.x_lo, hbeg, 1);
+        load_x(a.x, hbeg, x_hi_tile(0));
+        if (XS) load_x(a.x_lo, hbeg, x_lo_tile(0));
         load_h(hbeg, 0);
     }
     uint32_t last_commit_prev = 0;  // the previous head's last commit
@@ -631,8 +638,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_tc(const SsdTcArgs a
                 constexpr uint32_t id_diag = tc::idesc_bf16(128, kP, 0, 1);
                 const uint64_t dmh = tc::desc_kmajor(tc::smem_u32(part), KPC, 0);
                 const uint64_t dml = tc::desc_kmajor(tc::smem_u32(part + Cfg::kMPart), KPC, 0);
-                // x_h descriptor at this part's first k-step (XS: buffer 0 x_hi, 1 x_lo)
-                const uint64_t dx = tc::desc_mnmajor(tc::smem_u32(sX + (XS ? 0 : (hi & 1)) * Cfg::kX), kP, KPC / 16 * kp);
+                // x_h descriptor at this part's first k-step
+                const uint64_t dx = tc::desc_mnmajor(tc::smem_u32(x_hi_tile(hi)), kP, KPC / 16 * kp);
 #pragma unroll
                 for (int ks = 0; ks < KPC / 16; ++ks)
                     tc::mma_bf16(tYd, dmh + ks * tc::kstep_kmajor(), dx + ks * tc::kstep_mnmajor(kP), id_diag,
@@ -641,7 +648,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_tc(const SsdTcArgs a
                 for (int ks = 0; ks < KPC / 16; ++ks)
                     tc::mma_bf16(tYd, dml + ks * tc::kstep_kmajor(), dx + ks * tc::kstep_mnmajor(kP), id_diag, 1);
                 if (XS) {
-                    const uint64_t dxl = tc::desc_mnmajor(tc::smem_u32(sX + Cfg::kX), kP, KPC / 16 * kp);
+                    const uint64_t dxl = tc::desc_mnmajor(tc::smem_u32(x_lo_tile(hi)), kP, KPC / 16 * kp);
 #pragma unroll
                     for (int ks = 0; ks < KPC / 16; ++ks)
                         tc::mma_bf16(tYd, dmh + ks * tc::kstep_kmajor(), dxl + ks * tc::kstep_mnmajor(kP), id_diag, 1);
@@ -672,16 +679,17 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_tc(const SsdTcArgs a
                 }
                 if (hi + 1 < heads_per_cta) {
                     __syncthreads();  // every thread is done reading the buffer in finish
-                    if (!XS) load_x(a.x, h + 1, (hi + 1) & 1);
+                    if (!xser) load_x(a.x, h + 1, x_hi_tile(hi + 1));
+                    if (XS && !xser) load_x(a.x_lo, h + 1, x_lo_tile(hi + 1));
                     // two h tile sets: the previous head's (its MMAs are done) takes the next
                     if (Cfg::kHBufs == 2) load_h(h + 1, (hi + 1) & 1);
                 }
             }
-            // XS: both x buffers are free once this head's last MMAs are done
-            if (XS && kp == nparts - 1 && hi + 1 < heads_per_cta) {
+            // serial XS: both x buffers are free once this head's last MMAs are done
+            if (xser && kp == nparts - 1 && hi + 1 < heads_per_cta) {
                 wait_commit(ncommit - 1);
-                load_x(a.x, h + 1, 0);
-                load_x(a.x_lo, h + 1, 1);
+                load_x(a.x, h + 1, x_hi_tile(hi + 1));
+                load_x(a.x_lo, h + 1, x_lo_tile(hi + 1));
             }
         }
         last_commit_prev = ncommit - 1;
