@@ -694,12 +694,15 @@ def backward_bytes(w) -> int:
     gradient written (fp32)."""
     E = 2 if w.dtype == "bf16" else 4
     b, T, H, N, G = w.batch, w.seqlen, w.nheads, w.dstate, w.ngroups
-    nbytes = b * T * H * E * (3 + (1 if w.gate else 0))          # x, dt, dout, z
+    P = w.headdim if w.mode == "ssd" else 1                      # channels per head
+    na = H if w.mode == "ssd" else H * N                         # entries of A
+    nbytes = b * T * H * P * E * (2 + (1 if w.gate else 0))      # x, dout, z
+    nbytes += b * T * H * (E + 4)                                # dt, ddt
     nbytes += 2 * b * T * G * N * E                              # B, C
-    nbytes += b * T * H * 4 * (2 + (1 if w.gate else 0))         # dx, ddt, dz
+    nbytes += b * T * H * P * 4 * (1 + (1 if w.gate else 0))     # dx, dz
     nbytes += 2 * b * T * G * N * 4                              # dB, dC
-    nbytes += 2 * H * N * 4 + 4 * H * 4                          # A, dA, D, dD, dt_bias, ddt_bias
-    nbytes += 2 * b * H * N * 4                                  # dfinal, dinitial_state
+    nbytes += 2 * na * 4 + 4 * H * 4                             # A, dA, D, dD, dt_bias, ddt_bias
+    nbytes += 2 * b * H * P * N * 4                              # dfinal, dinitial_state
     return int(nbytes)
 
 
@@ -709,15 +712,14 @@ def run_backward(args, w):
     dist, world, rank, local = dist_setup()
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA device (there is no CPU path)")
-    if w.mode != "diag":
-        raise SystemExit("the backward pass is built for the diagonal mode")
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     inp = host_inputs(w)
     d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
     gen = torch.Generator().manual_seed(w.seed + 100)
     dout_h = torch.randn(d["x"].shape, generator=gen).to(d["x"].dtype)
-    dfin_h = torch.randn((w.batch, w.nheads, w.dstate), generator=gen)
+    st_shape = (w.batch, w.nheads) + ((w.headdim,) if w.mode == "ssd" else ()) + (w.dstate,)
+    dfin_h = torch.randn(st_shape, generator=gen)
     dout, dfin = dout_h.to(dev), dfin_h.to(dev)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -780,9 +782,10 @@ def run_backward(args, w):
         host = dict(inp, dout=dout_h, dfinal=dfin_h)
         xs, f32 = tuple(inp["x"].shape), torch.float32
         H, N = w.nheads, w.dstate
-        specs = {"dx": (xs, f32), "ddt": (tuple(inp["dt"].shape), f32), "dA": ((H, N), f32),
+        specs = {"dx": (xs, f32), "ddt": (tuple(inp["dt"].shape), f32),
+                 "dA": (tuple(inp["A"].shape), f32),
                  "dB": (tuple(inp["B"].shape), f32), "dC": (tuple(inp["C"].shape), f32),
-                 "dinitial_state": ((w.batch, H, N), f32)}
+                 "dinitial_state": (st_shape, f32)}
         if inp["D"] is not None:
             specs["dD"] = ((H,), f32)
         if inp["z"] is not None:
@@ -800,8 +803,9 @@ def run_backward(args, w):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "how": E2E_NOTE}
         if rank == 0:
             import oracle
-            # the oracle's backward over the first sequence and a block of channels
-            nch = min(w.nheads, 64)
+            # the oracle's backward over the first sequence and a block of channels (SSD: of
+            # heads)
+            nch = min(w.nheads, 64 if w.mode == "diag" else 2)
             sub = {k: (None if v is None else v) for k, v in inp.items()}
             cut = lambda t: t[:1, :, :nch].contiguous()
             sl = dict(x=cut(sub["x"]), dt=cut(sub["dt"]), A=sub["A"][:nch], B=sub["B"][:1],
@@ -814,10 +818,11 @@ def run_backward(args, w):
                 oracle.scan_bwd(**sl, dout=dout_h[:1, :, :nch], dfinal=dfin_h[:1, :nch])
                 t_used += time.perf_counter() - t0
                 reps += 1
-            cpu = {"value": reps * w.seqlen * nch / t_used / 1e9, "unit": UNIT, "cores": 1,
-                   "kind": "oracle", "seconds": t_used,
-                   "sample": f"{reps} oracle backward passes over 1 sequence x {nch} channels "
-                             f"x L {w.seqlen} (fp64, one thread)"}
+            per_head = w.headdim if w.mode == "ssd" else 1
+            cpu = {"value": reps * w.seqlen * nch * per_head / t_used / 1e9, "unit": UNIT,
+                   "cores": 1, "kind": "oracle", "seconds": t_used,
+                   "sample": f"{reps} oracle backward passes over 1 sequence x {nch * per_head} "
+                             f"channels x L {w.seqlen} (fp64, one thread)"}
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,

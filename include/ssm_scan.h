@@ -236,8 +236,8 @@ int ssm_step_conv(const void* x, const void* dt, const float* A, const void* B, 
                   float* state, void* out, const ssm_shape* shape, ssm_stream_t stream);
 
 /*
- * Backward pass of the diagonal-mode (Mamba-1) scan: the gradients of every input from
- * the gradient of out (and, optionally, of the final state).  The pages give the forward
+ * Backward pass of the scan (both modes): the gradients of every input from the
+ * gradient of out (and, optionally, of the final state).  The pages give the forward
  * recurrence only ("Mamba-2：把状态空间模型和 Attention 统一到一个数学框架里", 背景问题 and
  * 第一步; training runs the recurrence in parallel, "训练时并行化"); the derivatives are
  * taken from it, per channel from the last step to the first, with g_t = dL/dh_t:
@@ -246,19 +246,23 @@ int ssm_step_conv(const void* x, const void* dt, const float* A, const void* B, 
  *   ddt_t = sigmoid(dt_t + dt_bias) sum_n g_t (B_t x_t + exp(Delta_t A) A h_{t-1});
  *   dA += g_t exp(Delta_t A) Delta_t h_{t-1};  dD += dy_t x_t;  ddt_bias += ddt_t;
  *   dz_t = dout_t y_t SiLU'(z_t);  dinitial_state = exp(Delta_0 A) g_0.
- * Mode must be SSM_MODE_DIAG (SSM_ERR_UNSUPPORTED otherwise); shapes and forward
- * arguments as ssm_scan_fwd_state (initial_state nullable).
+ * In SSD mode a channel is (head, p) and A, Delta, D and dt_bias belong to the head
+ * (the same page, 第二步), so their gradients sum over the head's channels (dA also over
+ * n).  Shapes and forward arguments as ssm_scan_fwd_state (initial_state nullable).
  *   dout: the gradient of out, x's layout and dtype (required unless batch or seqlen is 0);
- *   dfinal_state: gradient of the final state, fp32 (batch, nheads, dstate), or NULL (zero).
- * Outputs, all fp32 and in the layout of the matching input: dx, ddt (required), dA, dB, dC
- * (required; dB, dC (batch, seqlen, ngroups, dstate)), dD, dz, ddt_bias, dinitial_state
- * (NULL: not computed; dD, dz and ddt_bias are also skipped when D, z or dt_bias is NULL).
- * dA, dB, dC, dD and ddt_bias are sums over channels and batch: the call zeroes them
- * first.  No output may overlap an input or another output.
- * Scratch: ssm_scan_bwd_workspace_size(shape) bytes (the state every 16 steps); workspace
- * NULL/0 draws it from the stream-ordered allocator, as ssm_scan_fwd does.
- * The sums over channels use floating-point atomics, so dA, dB, dC, dD and ddt_bias may
- * differ between runs in the last bits.
+ *   dfinal_state: gradient of the final state, fp32, the final state's layout
+ *     (DIAG (batch, nheads, dstate); SSD (batch, nheads, headdim, dstate)), or NULL (zero).
+ * Outputs, all fp32 and in the layout of the matching input: dx, ddt (required; SSD
+ * (batch, seqlen, nheads)), dA (required; DIAG (nheads, dstate), SSD (nheads,)), dB, dC
+ * (required; (batch, seqlen, ngroups, dstate)), dD, dz, ddt_bias, dinitial_state (NULL:
+ * not computed; dD, dz and ddt_bias are also skipped when D, z or dt_bias is NULL).
+ * dA, dB, dC, dD and ddt_bias (and, in SSD mode, ddt) are sums over channels and batch:
+ * the call zeroes them first.  No output may overlap an input or another output.
+ * Scratch: ssm_scan_bwd_workspace_size(shape) bytes (the state every 16 steps, every 8
+ * or 4 steps for dstate above 64 or 128); workspace NULL/0 draws it from the
+ * stream-ordered allocator, as ssm_scan_fwd does.
+ * The sums over channels use floating-point atomics, so dA, dB, dC, dD and ddt_bias (and
+ * SSD's ddt) may differ between runs in the last bits.
  */
 int ssm_scan_bwd(const void* x, const void* dt, const float* A, const void* B, const void* C,
                  const float* D, const void* z, const float* dt_bias, const float* initial_state,
@@ -267,7 +271,7 @@ int ssm_scan_bwd(const void* x, const void* dt, const float* A, const void* B, c
                  float* dinitial_state, const ssm_shape* shape, void* workspace,
                  size_t workspace_bytes, ssm_stream_t stream);
 
-/* Scratch bytes of ssm_scan_bwd ((size_t)-1 for an invalid shape or SSD mode). */
+/* Scratch bytes of ssm_scan_bwd ((size_t)-1 for an invalid shape). */
 size_t ssm_scan_bwd_workspace_size(const ssm_shape* shape);
 
 /*

@@ -180,37 +180,39 @@ def scan_fwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, *, out=None, final_st
 
 def scan_bwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, *, dout, dfinal_state=None,
              initial_state=None, workspace=None, stream=None, grads=None):
-    """Gradients of the diagonal-mode scan (``scan_fwd`` with a 2-D A).
+    """Gradients of the scan, diagonal mode (2-D A) or SSD mode (1-D A per head).
 
     ``dout`` is the gradient of the output (x's shape and dtype), ``dfinal_state`` that of
     the final state (float32, optional).  Returns a dict of float32 tensors: dx, ddt, dA,
     dB, dC (B's shape), and dD, dz, ddt_bias, dinitial_state where the matching input was
-    given (dinitial_state always).  ``grads``: optional dict of preallocated float32
+    given (dinitial_state always); each has its input's shape (SSD: ddt (b, T, H), dA
+    (H,), dinitial_state (b, H, P, N)).  ``grads``: optional dict of preallocated float32
     tensors with those names and shapes, written in place instead of new ones.
     """
     s = make_shape(x, A, B, 0)
     dev = x.device
     if dev.type != "cuda":
         raise ValueError("scan_bwd runs on CUDA tensors only")
-    if s.mode != _lib.SSM_MODE_DIAG:
-        raise SsmError(_lib.SSM_ERR_UNSUPPORTED, "ssm_scan_bwd (diagonal mode only)")
-    b, T, H, N = s.batch, s.seqlen, s.nheads, s.dstate
+    ssd = s.mode == _lib.SSM_MODE_SSD
+    b, T, H, P, N = s.batch, s.seqlen, s.nheads, s.headdim, s.dstate
+    st = (b, H, P, N) if ssd else (b, H, N)
+    a_shape = (H,) if ssd else (H, N)
     for name, t, shp, dt_ in (("x", x, x.shape, x.dtype), ("dt", dt, (b, T, H), x.dtype),
-                              ("A", A, (H, N), torch.float32), ("B", B, B.shape, x.dtype),
+                              ("A", A, a_shape, torch.float32), ("B", B, B.shape, x.dtype),
                               ("C", C, B.shape, x.dtype), ("D", D, (H,), torch.float32),
                               ("z", z, x.shape, x.dtype), ("dt_bias", dt_bias, (H,), torch.float32),
                               ("dout", dout, x.shape, x.dtype),
-                              ("dfinal_state", dfinal_state, (b, H, N), torch.float32),
-                              ("initial_state", initial_state, (b, H, N), torch.float32)):
+                              ("dfinal_state", dfinal_state, st, torch.float32),
+                              ("initial_state", initial_state, st, torch.float32)):
         _check(name, t, shp, dt_, dev)
     f32 = dict(device=dev, dtype=torch.float32)
     g = {"dx": torch.empty(x.shape, **f32), "ddt": torch.empty((b, T, H), **f32),
-         "dA": torch.empty((H, N), **f32), "dB": torch.empty(B.shape, **f32),
+         "dA": torch.empty(a_shape, **f32), "dB": torch.empty(B.shape, **f32),
          "dC": torch.empty(B.shape, **f32),
          "dD": None if D is None else torch.empty((H,), **f32),
          "dz": None if z is None else torch.empty(x.shape, **f32),
          "ddt_bias": None if dt_bias is None else torch.empty((H,), **f32),
-         "dinitial_state": torch.empty((b, H, N), **f32)}
+         "dinitial_state": torch.empty(st, **f32)}
     if grads is not None:
         for k, v in grads.items():
             if k not in g or g[k] is None:

@@ -293,7 +293,7 @@ using namespace ssm;
 
 extern "C" {
 
-int ssm_abi_version(void) { return (1 << 16) | 2; }
+int ssm_abi_version(void) { return (1 << 16) | 3; }
 
 uint64_t ssm_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
@@ -426,7 +426,7 @@ int ssm_scan_fwd_conv(const void* x, const void* dt, const float* A, const void*
 }
 
 size_t ssm_scan_bwd_workspace_size(const ssm_shape* shape) {
-    if (check_shape(shape) != SSM_OK || shape->mode != SSM_MODE_DIAG) return (size_t)-1;
+    if (check_shape(shape) != SSM_OK) return (size_t)-1;
     const ScanArgs a = make_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
                                  nullptr, nullptr, nullptr, shape);
     return scan_bwd_workspace_bytes(a);
@@ -440,7 +440,6 @@ int ssm_scan_bwd(const void* x, const void* dt, const float* A, const void* B, c
                  size_t workspace_bytes, ssm_stream_t stream) {
     int rc = check_args(x, dt, A, B, C, D, z, dt_bias, dx, nullptr, shape, initial_state);
     if (rc != SSM_OK) return rc;
-    if (shape->mode != SSM_MODE_DIAG) return SSM_ERR_UNSUPPORTED;
     const bool empty = shape->batch == 0 || shape->seqlen == 0;
     if (!dA || (!empty && (!dout || !dx || !ddt || !dB || !dC))) return SSM_ERR_NULL;
     const void* outs[] = {dout, dfinal_state, dx, ddt, dA, dB, dC, dD, dz, ddt_bias, dinitial_state};
@@ -448,6 +447,7 @@ int ssm_scan_bwd(const void* x, const void* dt, const float* A, const void* B, c
         if (!aligned16(p)) return SSM_ERR_ALIGN;
     ScanBwdArgs s;
     s.fwd = make_args(x, dt, A, B, C, D, z, dt_bias, nullptr, nullptr, shape);
+    s.ssd = shape->mode == SSM_MODE_SSD;
     s.fwd.initial_state = initial_state;
     s.dout = dout;
     s.dfinal = dfinal_state;

@@ -1,5 +1,5 @@
-// Backward pass of the diagonal (Mamba-1) selective scan: gradients of the inputs from
-// the gradient of the output (and optionally of the final state).
+// Backward pass of the selective scan: gradients of the inputs from the gradient of the
+// output (and optionally of the final state), diagonal (Mamba-1) and SSD (Mamba-2) mode.
 //
 // The pages give the forward recurrence only ("Mamba-2：把状态空间模型和 Attention 统一到
 // 一个数学框架里", 背景问题 / 第一步; training runs it in parallel, "训练时并行化"); the
@@ -11,10 +11,14 @@
 //   dDelta = sum_n g_t (B_t x_t + a_t A h_{t-1})   dA += g_t a_t Delta_t h_{t-1}
 //   ddt_t  = dDelta sigmoid(v_t)                   ddt_bias += ddt_t,  dD += dy_t x_t
 //   dinit  = a_0 g_0
+// SSD mode is the same recurrence per channel c = (head, p) with A, Delta, D and dt_bias
+// shared by the head's channels (Mamba-2 explainer, 第二步: a scalar A per head), so
+// dA, ddt, dD and ddt_bias of a head are sums over its channels (and, for dA, over n).
 //
-// Design: LPC lanes of a warp share one channel, each lane R state entries (N up to 64).
-// A forward sweep stores the state entering every segment of kSeg steps (the only
-// scratch); the reverse sweep walks the segments backwards, recomputes the segment's
+// Design: LPC lanes of a warp share one channel, each lane R state entries (N up to 64
+// in diagonal mode, 256 in SSD mode; segments shorten as R grows so that a segment's
+// recomputed states stay in registers).  A forward sweep stores the state entering every
+// segment of kSeg steps (the only scratch); the reverse sweep walks the segments backwards, recomputes the segment's
 // states into registers from its checkpoint and runs the adjoint recurrence over them.
 // The per-step scalars of a channel are computed once per segment, spread over its
 // lanes, and shuffled to the sweeps; sums over n use shuffles inside the LPC lanes; the
@@ -32,7 +36,14 @@ namespace ssm {
 namespace {
 
 constexpr int kBwdThreads = 256;
-constexpr int kMinSeg = 16;  // shortest checkpoint segment (sizes the scratch)
+
+// Lanes per channel and entries per lane for a state width N: the width padded to a
+// power of two, at most a warp (four entries per lane with fewer lanes measured slower
+// on B300: fewer resident warps and a longer per-step chain outweigh the shorter
+// reductions); checkpoint segment length by entries per lane.
+int bwd_lanes(int64_t N) { return N <= 4 ? 4 : N <= 8 ? 8 : N <= 16 ? 16 : 32; }
+int bwd_entries(int64_t N) { return N <= 32 ? 1 : N <= 64 ? 2 : N <= 128 ? 4 : 8; }
+int bwd_seg(int64_t N) { return bwd_entries(N) <= 2 ? 16 : bwd_entries(N) == 4 ? 8 : 4; }
 
 template <typename T>
 struct BwdArgs {
@@ -57,7 +68,8 @@ struct BwdArgs {
     float* ddt_bias;
     float* dinit;
     float* ckpt;  // (b, nseg, dim, N): state entering each segment
-    int64_t L, dim, N, G, cpg;  // L: sequence length
+    int64_t L, dim, N, G, cpg;  // L: sequence length; dim: channels (SSD: heads x P)
+    int64_t P;                  // channels per head (SSD headdim; 1 in diagonal mode)
     int nseg, tiles_per_group;
 };
 
@@ -73,7 +85,7 @@ __device__ __forceinline__ float lane_sum(float v) {
 // The per-step scalars of a channel (Delta, Delta x, dy, the SiLU' factor, sigmoid(v)) are
 // computed once per segment, spread over the channel's lanes (lane j % LPC holds step j),
 // and fetched with shuffles inside the sequential sweeps.
-template <typename T, int LPC, int R, int kSeg>
+template <typename T, int LPC, int R, int kSeg, bool SSD>
 __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> a) {
     constexpr bool PRECISE = sizeof(T) == 4;
     constexpr int CPB = kBwdThreads / LPC;
@@ -92,6 +104,9 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
     const bool c_ok = c < c_end;
     const int64_t b = blockIdx.z;
     const int64_t L = a.L, dim = a.dim, N = a.N, G = a.G;
+    // the index of A's row, Delta, D and dt_bias: the channel, or its head in SSD mode
+    const int64_t hd = SSD ? c / a.P : c;
+    const int64_t H = SSD ? dim / a.P : dim;
 
     float Ar[R];
     int nr[R];
@@ -100,14 +115,15 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
     for (int r = 0; r < R; ++r) {
         nr[r] = lane + r * LPC;
         nok[r] = c_ok && nr[r] < N;
-        Ar[r] = nok[r] ? a.A[c * N + nr[r]] * (PRECISE ? 1.0f : kLog2e) : 0.0f;
+        Ar[r] = nok[r] ? a.A[SSD ? hd : c * N + nr[r]] * (PRECISE ? 1.0f : kLog2e) : 0.0f;
     }
-    const float bias = (c_ok && a.dt_bias) ? a.dt_bias[c] : 0.0f;
-    const float Dc = (c_ok && a.D) ? a.D[c] : 0.0f;
+    const float bias = (c_ok && a.dt_bias) ? a.dt_bias[hd] : 0.0f;
+    const float Dc = (c_ok && a.D) ? a.D[hd] : 0.0f;
     auto decay = [&](float de, int r) { return PRECISE ? expf(de * Ar[r]) : ex2(de * Ar[r]); };
     auto Aval = [&](int r) { return PRECISE ? Ar[r] : Ar[r] * (1.0f / kLog2e); };
 
     auto row = [&](int64_t t) { return (b * L + t) * dim + c; };
+    auto drow = [&](int64_t t) { return (b * L + t) * H + hd; };  // dt and ddt
     auto bc = [&](int64_t t) { return (b * L + t) * G * N + (int64_t)group * N; };
     auto fetch = [&](const float (&v)[SPL], int j) { return __shfl_sync(0xffffffffu, v[j / LPC], j % LPC, LPC); };
 
@@ -127,7 +143,7 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
             const int j = lane + LPC * k;
             pde[k] = pu[k] = 0.0f;
             if (c_ok && j < len) {
-                pde[k] = softplus_t<PRECISE>(to_f32<T>(a.dt[row(t0 + j)]) + bias);
+                pde[k] = softplus_t<PRECISE>(to_f32<T>(a.dt[drow(t0 + j)]) + bias);
                 pu[k] = pde[k] * to_f32<T>(a.x[row(t0 + j)]);
             }
         }
@@ -162,7 +178,7 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
             pde[k] = pu[k] = px[k] = pdy[k] = pdz[k] = psig[k] = 0.0f;
             if (c_ok && j < len) {
                 const int64_t t = t0 + j;
-                const float v = to_f32<T>(a.dt[row(t)]) + bias;
+                const float v = to_f32<T>(a.dt[drow(t)]) + bias;
                 pde[k] = softplus_t<PRECISE>(v);
                 psig[k] = 1.0f / (1.0f + __expf(-v));
                 px[k] = to_f32<T>(a.x[row(t)]);
@@ -225,7 +241,10 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
                 const int k = j / LPC;
                 a.dx[row(t)] = fmaf(dy, Dc, dxp);
                 const float dv = ddp * psig[k];
-                a.ddt[row(t)] = dv;
+                if (SSD)
+                    atomicAdd(&a.ddt[drow(t)], dv);  // the head's channels share Delta_t
+                else
+                    a.ddt[row(t)] = dv;
                 dbias_acc += dv;
                 dD_acc = fmaf(dy, xv, dD_acc);
                 if (a.z) a.dz[row(t)] = pdz[k] * (yp + Dc * xv);
@@ -250,27 +269,35 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
     }
     dD_acc = lane_sum<LPC>(dD_acc);
     dbias_acc = lane_sum<LPC>(dbias_acc);
+    float dA_sum = 0.0f;  // SSD: the head's dA sums every entry of the channel
 #pragma unroll
     for (int r = 0; r < R; ++r)
         if (nok[r]) {
             if (a.dinit) a.dinit[(b * dim + c) * N + nr[r]] = g[r];
-            atomicAdd(&a.dA[c * N + nr[r]], dA_acc[r]);
+            if (SSD)
+                dA_sum += dA_acc[r];
+            else
+                atomicAdd(&a.dA[c * N + nr[r]], dA_acc[r]);
         }
+    if (SSD) dA_sum = lane_sum<LPC>(dA_sum);
     if (c_ok && lane == 0) {
-        if (a.dD) atomicAdd(&a.dD[c], dD_acc);
-        if (a.ddt_bias) atomicAdd(&a.ddt_bias[c], dbias_acc);
+        if (SSD) atomicAdd(&a.dA[hd], dA_sum);
+        if (a.dD) atomicAdd(&a.dD[hd], dD_acc);
+        if (a.ddt_bias) atomicAdd(&a.ddt_bias[hd], dbias_acc);
     }
 }
 
-template <typename T, int LPC, int R, int kSeg>
+template <typename T, int LPC, int R, bool SSD>
 cudaError_t launch_bwd(const BwdArgs<T>& a, int64_t batch, cudaStream_t stream) {
+    constexpr int kSeg = R <= 2 ? 16 : R == 4 ? 8 : 4;  // as bwd_seg
     constexpr int CPB = kBwdThreads / LPC;
     constexpr size_t kSmem = sizeof(float) * 2 * kSeg * CPB * LPC * R;
     BwdArgs<T> k = a;
     k.tiles_per_group = (int)((a.cpg + CPB - 1) / CPB);
     k.nseg = (int)((a.L + kSeg - 1) / kSeg);
+    if (kSeg != bwd_seg(a.N)) return cudaErrorInvalidValue;  // scratch sized by bwd_seg
     const dim3 grid((unsigned)(a.G * k.tiles_per_group), 1, (unsigned)batch);
-    auto kern = scan_bwd_kernel<T, LPC, R, kSeg>;
+    auto kern = scan_bwd_kernel<T, LPC, R, kSeg, SSD>;
     if (kSmem > 48 * 1024) {
         const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
         if (e != cudaSuccess) return e;
@@ -306,39 +333,50 @@ cudaError_t bwd_typed(const ScanBwdArgs& s, void* ws, cudaStream_t stream) {
     a.ddt_bias = s.ddt_bias;
     a.dinit = s.dinit;
     a.ckpt = (float*)ws;
+    const bool ssd = s.ssd;
     a.L = f.seqlen;
-    a.dim = f.nheads;
+    a.dim = f.nheads * f.headdim;
+    a.P = f.headdim;
     a.N = f.dstate;
     a.G = f.ngroups;
-    a.cpg = f.nheads / f.ngroups;
+    a.cpg = a.dim / f.ngroups;
     a.nseg = 0;
     a.tiles_per_group = 0;
-    // lanes per channel: the state width padded to a power of two, at most a warp (four
-    // entries per lane with fewer lanes measured slower on B300: fewer resident warps and
-    // a longer per-step chain outweigh the shorter reductions)
-    const int64_t np = f.dstate <= 4 ? 4 : f.dstate <= 8 ? 8 : f.dstate <= 16 ? 16 : f.dstate <= 32 ? 32 : 64;
-    if (np == 4) return launch_bwd<T, 4, 1, 16>(a, f.batch, stream);
-    if (np == 8) return launch_bwd<T, 8, 1, 16>(a, f.batch, stream);
-    if (np == 16) return launch_bwd<T, 16, 1, 16>(a, f.batch, stream);
-    if (np == 32) return launch_bwd<T, 32, 1, 16>(a, f.batch, stream);
-    return launch_bwd<T, 32, 2, 16>(a, f.batch, stream);
+    const int lpc = bwd_lanes(f.dstate), r = bwd_entries(f.dstate);
+    if (ssd) {
+        if (lpc == 4) return launch_bwd<T, 4, 1, true>(a, f.batch, stream);
+        if (lpc == 8) return launch_bwd<T, 8, 1, true>(a, f.batch, stream);
+        if (lpc == 16) return launch_bwd<T, 16, 1, true>(a, f.batch, stream);
+        if (r == 1) return launch_bwd<T, 32, 1, true>(a, f.batch, stream);
+        if (r == 2) return launch_bwd<T, 32, 2, true>(a, f.batch, stream);
+        if (r == 4) return launch_bwd<T, 32, 4, true>(a, f.batch, stream);
+        return launch_bwd<T, 32, 8, true>(a, f.batch, stream);
+    }
+    if (lpc == 4) return launch_bwd<T, 4, 1, false>(a, f.batch, stream);
+    if (lpc == 8) return launch_bwd<T, 8, 1, false>(a, f.batch, stream);
+    if (lpc == 16) return launch_bwd<T, 16, 1, false>(a, f.batch, stream);
+    if (r == 1) return launch_bwd<T, 32, 1, false>(a, f.batch, stream);
+    return launch_bwd<T, 32, 2, false>(a, f.batch, stream);
 }
 
 }  // namespace
 
 size_t scan_bwd_workspace_bytes(const ScanArgs& a) {
-    const int64_t nseg = (a.seqlen + kMinSeg - 1) / kMinSeg;
-    return align_up((size_t)a.batch * nseg * a.nheads * a.dstate * sizeof(float), 256);
+    const int64_t seg = bwd_seg(a.dstate);
+    const int64_t nseg = (a.seqlen + seg - 1) / seg;
+    return align_up((size_t)a.batch * nseg * a.nheads * a.headdim * a.dstate * sizeof(float), 256);
 }
 
 cudaError_t scan_bwd_launch(const ScanBwdArgs& s, void* ws, cudaStream_t stream) {
     const ScanArgs& f = s.fwd;
-    // accumulated gradients start from zero
-    const size_t acc_bytes[] = {(size_t)f.nheads * f.dstate * 4, (size_t)f.batch * f.seqlen * f.ngroups * f.dstate * 4,
+    // accumulated gradients start from zero (SSD: dA per head, and ddt, a sum over the
+    // head's channels)
+    const size_t acc_bytes[] = {(size_t)f.nheads * (s.ssd ? 1 : f.dstate) * 4,
+                                (size_t)f.batch * f.seqlen * f.ngroups * f.dstate * 4,
                                 (size_t)f.batch * f.seqlen * f.ngroups * f.dstate * 4, (size_t)f.nheads * 4,
-                                (size_t)f.nheads * 4};
-    float* acc[] = {s.dA, s.dB, s.dC, s.dD, s.ddt_bias};
-    for (int i = 0; i < 5; ++i)
+                                (size_t)f.nheads * 4, s.ssd ? (size_t)f.batch * f.seqlen * f.nheads * 4 : 0};
+    float* acc[] = {s.dA, s.dB, s.dC, s.dD, s.ddt_bias, s.ddt};
+    for (int i = 0; i < 6; ++i)
         if (acc[i] && acc_bytes[i]) {
             const cudaError_t e = cudaMemsetAsync(acc[i], 0, acc_bytes[i], stream);
             if (e != cudaSuccess) return e;

@@ -57,10 +57,12 @@ bool ssd_conv_split(const ScanArgs& a);
 // out (batch, nheads, headdim) written; diag_a selects A of shape (nheads, dstate).
 cudaError_t step_launch(const ScanArgs& a, bool diag_a, float* state, cudaStream_t stream);
 
-// Backward pass of the diagonal scan: the forward arguments plus the incoming gradients
-// and the gradient outputs (fp32; dA, dB, dC, dD and ddt_bias are zeroed, then summed).
+// Backward pass of the scan: the forward arguments plus the incoming gradients and the
+// gradient outputs (fp32; dA, dB, dC, dD and ddt_bias, and in SSD mode ddt, are zeroed,
+// then summed).
 struct ScanBwdArgs {
     ScanArgs fwd;
+    bool ssd;  // SSD mode: A, Delta, D and dt_bias per head
     const void* dout;
     const float* dfinal;
     float *dx, *ddt, *dA, *dB, *dC, *dD, *dz, *ddt_bias, *dinit;

@@ -258,9 +258,14 @@ def test_backward_argument_errors():
             args[names.index(k)] = None if v is None else vp(v)
         return lib.ssm_scan_bwd(*args, ctypes.byref(shape), None, 0, None)
 
+    # SSD mode: the state of every (head, p) channel every 8 steps at dstate 128, every 4
+    # at 256
     ssd = _shape(mode=1, nheads=8, headdim=64, dstate=128, chunk=64)
-    assert call(ssd) == _lib.SSM_ERR_UNSUPPORTED
-    assert lib.ssm_scan_bwd_workspace_size(ctypes.byref(ssd)) == BAD
+    assert lib.ssm_scan_bwd_workspace_size(ctypes.byref(ssd)) == 2 * (64 // 8) * 8 * 64 * 128 * 4
+    ssd256 = _shape(mode=1, nheads=2, headdim=64, dstate=256)
+    assert lib.ssm_scan_bwd_workspace_size(ctypes.byref(ssd256)) == 2 * (64 // 4) * 2 * 64 * 256 * 4
+    assert call(ssd, dB=(15 << 12) + 8) == _lib.SSM_ERR_ALIGN
+    assert lib.ssm_scan_bwd_workspace_size(ctypes.byref(_shape(mode=1, dstate=300))) == BAD
     assert call(s, dx=None) == _lib.SSM_ERR_NULL
     assert call(s, dout=None) == _lib.SSM_ERR_NULL
     assert call(s, dA=None) == _lib.SSM_ERR_NULL

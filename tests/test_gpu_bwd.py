@@ -1,5 +1,6 @@
-"""GPU parity of the diagonal-mode backward pass (ssm_scan_bwd) against the fp64 oracle's
-backward, which is pinned by finite differences: every gradient, element by element.
+"""GPU parity of the backward pass (ssm_scan_bwd, diagonal and SSD mode) against the fp64
+oracle's backward, which is pinned by finite differences: every gradient, element by
+element.
 
 Tolerances: max relative error (floor 1e-2 of the largest reference value) 1e-4 for fp32
 inputs, 2e-2 for bf16 inputs; all gradients are fp32.
@@ -50,10 +51,11 @@ def compare(w, inp, dout, dfinal, init):
 
 def extras(w, seed, with_init=True, with_dfinal=True):
     gen = torch.Generator().manual_seed(seed)
-    xs = (w.batch, w.seqlen, w.nheads)
+    ssd = w.mode == "ssd"
+    xs = (w.batch, w.seqlen, w.nheads) + ((w.headdim,) if ssd else ())
     dout = torch.randn(xs, generator=gen)
     dout = dout.to(torch.bfloat16) if w.dtype == "bf16" else dout
-    st = (w.batch, w.nheads, w.dstate)
+    st = (w.batch, w.nheads) + ((w.headdim,) if ssd else ()) + (w.dstate,)
     dfinal = torch.randn(st, generator=gen) if with_dfinal else None
     init = torch.randn(st, generator=gen) if with_init else None
     return dout, dfinal, init
@@ -123,4 +125,34 @@ def test_backward_many_channels(case):
     dtype, b, T, D, N = case
     w, inp = random_inputs("diag", dtype, b, T, D, 1, N, seed=T + N)
     dout, dfinal, h0 = extras(w, seed=T + 1)
+    compare(w, inp, dout, dfinal, h0)
+
+
+# SSD mode: A, Delta, D and dt_bias per head; dstate up to 256 (4 and 8 entries per lane,
+# 8- and 4-step checkpoint segments)
+# (dtype, batch, T, H, P, N, G, gate, bias, skip, init, dfinal)
+SSD_CASES = [
+    ("f32", 1, 37, 2, 8, 16, 1, True, True, True, True, True),
+    ("f32", 2, 50, 4, 4, 64, 2, True, True, True, False, True),
+    ("f32", 1, 30, 2, 4, 256, 1, False, True, False, True, True),
+    ("bf16", 1, 100, 2, 64, 128, 1, True, True, True, True, True),
+    ("bf16", 1, 45, 2, 16, 256, 1, True, False, True, True, True),
+    ("bf16", 2, 64, 4, 32, 32, 2, False, True, False, False, True),
+    ("bf16", 2, 1, 2, 8, 64, 1, True, True, True, True, True),     # one step
+]
+
+
+@pytest.mark.parametrize("case", SSD_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_backward_ssd_shapes(case):
+    dtype, b, T, H, P, N, G, gate, bias, skip, init, dfin = case
+    w, inp = random_inputs("ssd", dtype, b, T, H, P, N, ngroups=G, gate=gate, dt_bias=bias,
+                           d_skip="normal" if skip else "none", seed=T + H + P + N)
+    dout, dfinal, h0 = extras(w, seed=T + 3, with_init=init, with_dfinal=dfin)
+    compare(w, inp, dout, dfinal, h0)
+
+
+def test_backward_ssd_many_channels():
+    """SSD with the channels of many thread blocks per group and head."""
+    w, inp = random_inputs("ssd", "bf16", 2, 24, 16, 64, 128, ngroups=2, seed=11)
+    dout, dfinal, h0 = extras(w, seed=12)
     compare(w, inp, dout, dfinal, h0)
