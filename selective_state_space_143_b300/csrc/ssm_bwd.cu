@@ -120,6 +120,17 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
     const float bias = (c_ok && a.dt_bias) ? a.dt_bias[hd] : 0.0f;
     const float Dc = (c_ok && a.D) ? a.D[hd] : 0.0f;
     auto decay = [&](float de, int r) { return PRECISE ? expf(de * Ar[r]) : ex2(de * Ar[r]); };
+    // the decays of step j for every entry: SSD's scalar A per head makes them one value
+    auto decays = [&](float de, float (&av)[R]) {
+        if (SSD) {
+            const float a0 = decay(de, 0);
+#pragma unroll
+            for (int r = 0; r < R; ++r) av[r] = a0;
+        } else {
+#pragma unroll
+            for (int r = 0; r < R; ++r) av[r] = decay(de, r);
+        }
+    };
     auto Aval = [&](int r) { return PRECISE ? Ar[r] : Ar[r] * (1.0f / kLog2e); };
 
     auto row = [&](int64_t t) { return (b * L + t) * dim + c; };
@@ -151,10 +162,12 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
         for (int j = 0; j < kSeg; ++j) {
             if (j >= len) break;
             const float de = fetch(pde, j), u = fetch(pu, j);
+            float av[R];
+            decays(de, av);
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const float Bv = nok[r] ? to_f32<T>(a.B[bc(t0 + j) + nr[r]]) : 0.0f;
-                h[r] = fmaf(decay(de, r), h[r], u * Bv);
+                h[r] = fmaf(av[r], h[r], u * Bv);
             }
         }
     }
@@ -202,10 +215,12 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
         for (int j = 0; j < kSeg; ++j) {
             if (j < len) {
                 const float de = fetch(pde, j), u = fetch(pu, j);
+                float av[R];
+                decays(de, av);
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     const float Bv = nok[r] ? to_f32<T>(a.B[bc(t0 + j) + nr[r]]) : 0.0f;
-                    hs[j][r] = fmaf(decay(de, r), j == 0 ? h0[r] : hs[j - 1][r], u * Bv);
+                    hs[j][r] = fmaf(av[r], j == 0 ? h0[r] : hs[j - 1][r], u * Bv);
                 }
             }
         }
@@ -215,11 +230,13 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
             const int64_t t = t0 + j;
             const float de = fetch(pde, j), xv = fetch(px, j), dy = fetch(pdy, j);
             float yp = 0.0f, dxp = 0.0f, ddp = 0.0f;
+            float avs[R];
+            decays(de, avs);
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const float Bv = nok[r] ? to_f32<T>(a.B[bc(t) + nr[r]]) : 0.0f;
                 const float Cv = nok[r] ? to_f32<T>(a.C[bc(t) + nr[r]]) : 0.0f;
-                const float av = decay(de, r);
+                const float av = avs[r];
                 const float hp = j == 0 ? h0[r] : hs[j - 1][r];
                 yp = fmaf(Cv, hs[j][r], yp);
                 g[r] = fmaf(dy, Cv, g[r]);
