@@ -63,7 +63,7 @@ typedef enum {
     SSM_ERR_UNSUPPORTED = 5, /* valid but unsupported (dstate too large, flags != 0) */
     SSM_ERR_ALLOC = 6,       /* workspace allocation failed or workspace too small   */
     SSM_ERR_CUDA = 7,        /* a CUDA call failed (launch error, no device)         */
-    SSM_ERR_TIMEOUT = 8      /* reserved: a bounded device-side wait ran out         */
+    SSM_ERR_TIMEOUT = 8      /* a bounded device-side wait ran out (ssm_device_status) */
 } ssm_status;
 
 typedef enum { SSM_MODE_DIAG = 0, SSM_MODE_SSD = 1 } ssm_mode;
@@ -292,6 +292,28 @@ typedef struct ssm_kernel_time {
 } ssm_kernel_time;
 void ssm_timing_enable(int on);
 int ssm_timing_collect(ssm_kernel_time* out, int max_entries);
+
+/*
+ * Device-side wait status (this has no counterpart in the pages: it is how the library's
+ * own kernels report a wait that did not end).  The tensor-core SSD kernels wait on
+ * mbarriers for their MMAs; every such wait is bounded (about one second, or 2^24
+ * polls), and a kernel whose wait ran out records SSM_ERR_TIMEOUT in a per-device status
+ * word, releases its tensor memory and returns, so the context stays usable and its
+ * outputs are not valid.  Launches are asynchronous, so the entry points cannot return
+ * this status themselves: ssm_device_status synchronizes `stream`, then returns SSM_OK
+ * or SSM_ERR_TIMEOUT for the current device (SSM_ERR_CUDA if the read fails), and clears
+ * the word when `clear` is non-zero.
+ */
+int ssm_device_status(int clear, ssm_stream_t stream);
+
+/*
+ * Self-test of the bounded-wait path: one thread block waits on an mbarrier that expects
+ * an arrival nothing makes, gives up after `max_checks` polls (at most one second) and
+ * records SSM_ERR_TIMEOUT in the status word, exactly as the SSD kernels would.  Returns
+ * SSM_OK once launched on `stream` (SSM_ERR_CUDA on a launch error); read the outcome
+ * with ssm_device_status.
+ */
+int ssm_selftest_bounded_wait(uint32_t max_checks, ssm_stream_t stream);
 
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char* ssm_strerror(int status);

@@ -306,6 +306,29 @@ def step(x, dt, A, B, C, D=None, z=None, dt_bias=None, *, state, out=None, strea
     return out
 
 
+def device_status(clear: bool = True, stream=None) -> int:
+    """Status of the library's bounded device-side waits on the current device, after the
+    work queued on ``stream`` (default: the current torch stream): ``_lib.SSM_OK`` or
+    ``_lib.SSM_ERR_TIMEOUT`` (a kernel gave up a wait; its outputs are not valid).
+    ``clear`` resets the status word."""
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    rc = _lib.load().ssm_device_status(1 if clear else 0, ctypes.c_void_p(stream.cuda_stream))
+    if rc not in (_lib.SSM_OK, _lib.SSM_ERR_TIMEOUT):
+        raise SsmError(rc, "ssm_device_status")
+    return rc
+
+
+def selftest_bounded_wait(max_checks: int = 1000, stream=None) -> None:
+    """Launch the bounded-wait self-test (a wait nothing completes; see
+    ``ssm_selftest_bounded_wait``); read the outcome with ``device_status``."""
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    rc = _lib.load().ssm_selftest_bounded_wait(int(max_checks), ctypes.c_void_p(stream.cuda_stream))
+    if rc != _lib.SSM_OK:
+        raise SsmError(rc, "ssm_selftest_bounded_wait")
+
+
 def launch_count() -> int:
     """Kernels launched by libssmscan.so in this process so far."""
     return _lib.launch_count()

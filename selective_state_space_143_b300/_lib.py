@@ -30,7 +30,8 @@ SSM_BF16 = 1
 EXPORTED = ("ssm_scan_fwd", "ssm_scan_fwd_ws", "ssm_scan_workspace_size", "ssm_scan_fwd_noalloc",
             "ssm_scan_fwd_state", "ssm_step", "ssm_scan_fwd_conv", "ssm_scan_conv_workspace_size",
             "ssm_step_conv", "ssm_scan_bwd", "ssm_scan_bwd_workspace_size", "ssm_timing_enable",
-            "ssm_timing_collect", "ssm_strerror", "ssm_kernel_launch_count", "ssm_abi_version")
+            "ssm_timing_collect", "ssm_device_status", "ssm_selftest_bounded_wait", "ssm_strerror",
+            "ssm_kernel_launch_count", "ssm_abi_version")
 
 
 class ssm_shape(ctypes.Structure):
@@ -121,6 +122,10 @@ def load() -> ctypes.CDLL:
         lib.ssm_kernel_launch_count.restype = ctypes.c_uint64
         lib.ssm_abi_version.argtypes = []
         lib.ssm_abi_version.restype = ctypes.c_int
+        lib.ssm_device_status.argtypes = [ctypes.c_int, ctypes.c_void_p]
+        lib.ssm_device_status.restype = ctypes.c_int
+        lib.ssm_selftest_bounded_wait.argtypes = [ctypes.c_uint32, ctypes.c_void_p]
+        lib.ssm_selftest_bounded_wait.restype = ctypes.c_int
         del fp
         _lib = lib
         return lib

@@ -415,7 +415,7 @@ bool force_cuda_cores() {
 
 struct SsdPlan {
     int64_t Q, nchunks;
-    size_t dl_off, cum_off, st_off, status_off, total;
+    size_t dl_off, cum_off, st_off, total;
 };
 
 SsdPlan ssd_plan(const ScanArgs& a) {
@@ -427,8 +427,7 @@ SsdPlan ssd_plan(const ScanArgs& a) {
     p.dl_off = 0;
     p.cum_off = align_up(vec, 256);
     p.st_off = p.cum_off + align_up(vec, 256);
-    p.status_off = p.st_off + align_up(st, 256);
-    p.total = p.status_off + 256;
+    p.total = p.st_off + align_up(st, 256);
     return p;
 }
 
@@ -481,7 +480,6 @@ cudaError_t ssd_launch_typed(const ScanArgs& a, void* ws, cudaStream_t stream) {
         t.dl = s.dl;
         t.cum = s.cum;
         t.states = s.states;
-        t.status = (int*)((char*)ws + pl.status_off);
         t.T = a.seqlen;
         t.H = a.nheads;
         t.N = a.dstate;

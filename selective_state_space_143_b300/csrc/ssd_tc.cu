@@ -118,8 +118,28 @@ __device__ __forceinline__ void mnmajor_item(int i, int MC, int& k, int& mc) {
     mc = (i >> 3) % MC;
 }
 
-__device__ __forceinline__ void report_timeout(int* status) {
-    if (status) atomicExch(status, kStatusTimeout);
+}  // namespace
+
+// Per-device status word: a kernel that gave up a bounded wait records SSM_ERR_TIMEOUT
+// here (and returns instead of hanging); the host reads and clears it through
+// device_status_take (ssm_device_status).
+__device__ int g_device_status = 0;
+
+namespace {
+
+__device__ __forceinline__ void report_timeout() { atomicExch(&g_device_status, kStatusTimeout); }
+
+// One CTA waits on an mbarrier that expects one arrival which nothing makes, giving up
+// after max_checks polls: the bounded-wait path of the kernels above, on demand.
+__global__ void bounded_wait_selftest(uint32_t max_checks) {
+    __shared__ __align__(8) uint64_t mbar;
+    if (threadIdx.x == 0) {
+        tc::mbar_init(&mbar, 1);
+        tc::mbar_fence_init();
+    }
+    __syncthreads();
+    const bool ok = tc::mbar_wait_bounded(&mbar, 0, max_checks);
+    if (!ok && threadIdx.x == 0) report_timeout();
 }
 
 }  // namespace
@@ -339,7 +359,7 @@ __global__ void __launch_bounds__(StateTcCfg<N, XS>::NT) ssd_state_tc(const SsdT
         wait_commit(nsteps - 1);
         epilogue(tmem, hpc / 2 - 1);
     }
-    if (!ok && tid == 0) report_timeout(a.status);
+    if (!ok && tid == 0) report_timeout();
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, kCols);
@@ -699,7 +719,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) ssd_scan_tc(const SsdTcArgs a
         wait_commit(last_commit_prev);
         finish(hbeg + heads_per_cta - 1, (heads_per_cta - 1) & 1, alpha_prev);
     }
-    if (!ok && tid == 0) report_timeout(a.status);
+    if (!ok && tid == 0) report_timeout();
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, 512);
@@ -753,6 +773,28 @@ cudaError_t launch_scan(const SsdTcArgs& s, int64_t batch, cudaStream_t stream) 
 }
 
 }  // namespace
+
+cudaError_t device_status_take(int* status, bool clear, cudaStream_t stream) {
+    int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_device_status, sizeof(int), 0, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return e;
+    if (clear && v != 0) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbolAsync(g_device_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+        if (e != cudaSuccess) return e;
+    }
+    *status = v;
+    return cudaSuccess;
+}
+
+cudaError_t bounded_wait_selftest_launch(uint32_t max_checks, cudaStream_t stream) {
+    cudaEvent_t t0 = timing_begin(stream);
+    bounded_wait_selftest<<<1, 32, 0, stream>>>(max_checks);
+    note_launch("bounded_wait_selftest", stream, t0);
+    return cudaGetLastError();
+}
 
 cudaError_t ssd_tc_chunk_state(const SsdTcArgs& s, int64_t batch, cudaStream_t stream) {
     if (s.x_lo) {

@@ -23,7 +23,6 @@ struct SsdTcArgs {
     float* dl;      // (b, H, nchunks, Q) Delta
     float* cum;     // (b, H, nchunks, Q) inclusive cumsum of Delta*A_h within the chunk
     float* states;  // (b, nchunks, H, P, N): S_c, then (after the carry pass) h_{c-1}
-    int* status;    // device status word (set to SSM_ERR_TIMEOUT if a bounded wait ran out)
     int64_t T, H, N, G, Q, nchunks;
 };
 

@@ -293,7 +293,24 @@ using namespace ssm;
 
 extern "C" {
 
-int ssm_abi_version(void) { return (1 << 16) | 3; }
+int ssm_abi_version(void) { return (1 << 16) | 4; }
+
+int ssm_device_status(int clear, ssm_stream_t stream) {
+    int v = 0;
+    if (ssm::device_status_take(&v, clear != 0, (cudaStream_t)stream) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SSM_ERR_CUDA;
+    }
+    return v == 0 ? SSM_OK : SSM_ERR_TIMEOUT;
+}
+
+int ssm_selftest_bounded_wait(uint32_t max_checks, ssm_stream_t stream) {
+    if (ssm::bounded_wait_selftest_launch(max_checks, (cudaStream_t)stream) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SSM_ERR_CUDA;
+    }
+    return SSM_OK;
+}
 
 uint64_t ssm_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 

@@ -123,14 +123,17 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // between checks (so waiting warps take no issue slots from the working ones), and the
 // wait gives up (returns false) after about one second of wall time or 2^24 checks,
 // whichever comes first.
-__device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t phase) {
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* mbar, uint32_t phase, uint32_t max_checks) {
     if (mbar_try_wait(mbar, phase)) return true;
     const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 0; it < (1u << 24); ++it) {
+    for (uint32_t it = 0; it < max_checks; ++it) {
         if (mbar_try_wait(mbar, phase)) return true;
         if ((it & 255u) == 0 && globaltimer_ns() - t0 > 1000000000ull) return false;
     }
     return false;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t phase) {
+    return mbar_wait_bounded(mbar, phase, 1u << 24);
 }
 
 // Load 16 consecutive fp32 columns of this warp's 32 TMEM lanes (lane = row).
