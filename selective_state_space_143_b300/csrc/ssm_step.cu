@@ -11,9 +11,11 @@
 // x is first replaced by x' = SiLU(bias + sum_k w[k] x_{t-K+1+k}), the K-1 earlier
 // inputs coming from the carried convolution state, which is then shifted by one token.
 // The step reads and writes the whole state once, so it is bound by HBM (or L2 when the
-// state fits there).  LPC lanes share one channel's state row, each lane taking 16-byte
-// pieces of it, so a warp's accesses are contiguous; the C.h partial sums are combined
-// with shuffles inside the LPC-lane group.
+// state fits there).  LPC lanes share one channel's state row, each lane taking PPL
+// 16-byte pieces of it (pieces lane, lane + LPC, ...), so a warp's accesses are
+// contiguous; a lane issues every load of its pieces before its first store, which keeps
+// PPL state pieces per thread in flight; the C.h partial sums are combined with shuffles
+// inside the LPC-lane group.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -60,7 +62,7 @@ __device__ __forceinline__ float decay(float de_times_a) {
     return PRECISE ? expf(de_times_a) : ex2(de_times_a * kLog2e);
 }
 
-template <typename T, int LPC, bool CONV>
+template <typename T, int LPC, int PPL, bool CONV>
 __global__ void __launch_bounds__(kStepThreads) ssm_step_kernel(const StepArgs a) {
     constexpr bool PRECISE = sizeof(T) == 4;
     constexpr int CPB = kStepThreads / LPC;  // channels per block
@@ -97,25 +99,35 @@ __global__ void __launch_bounds__(kStepThreads) ssm_step_kernel(const StepArgs a
         float* st = a.state + ch * a.N;
         const float* Arow = a.A + h * a.N;
         const float ah = a.diag ? 0.0f : decay<PRECISE>(de * a.A[h]);
-        for (int64_t n = 4 * lane; n < a.N; n += 4 * LPC) {
-            float4 hv = *reinterpret_cast<const float4*>(st + n);
-            const float4 Bv = load4(Bs + n);
-            const float4 Cv = load4(Cs + n);
-            float4 av = make_float4(ah, ah, ah, ah);
-            if (a.diag) {
-                const float4 Av = load4(Arow + n);
-                av = make_float4(decay<PRECISE>(de * Av.x), decay<PRECISE>(de * Av.y),
-                                 decay<PRECISE>(de * Av.z), decay<PRECISE>(de * Av.w));
+        float4 hv[PPL], Bv[PPL], Cv[PPL], Av[PPL];
+#pragma unroll
+        for (int q = 0; q < PPL; ++q) {  // every load first
+            const int n = 4 * (lane + q * LPC);
+            if (n < a.N) {
+                hv[q] = *reinterpret_cast<const float4*>(st + n);
+                Bv[q] = load4(Bs + n);
+                Cv[q] = load4(Cs + n);
+                if (a.diag) Av[q] = load4(Arow + n);
             }
-            hv.x = fmaf(av.x, hv.x, u * Bv.x);
-            hv.y = fmaf(av.y, hv.y, u * Bv.y);
-            hv.z = fmaf(av.z, hv.z, u * Bv.z);
-            hv.w = fmaf(av.w, hv.w, u * Bv.w);
-            *reinterpret_cast<float4*>(st + n) = hv;
-            y = fmaf(Cv.x, hv.x, y);
-            y = fmaf(Cv.y, hv.y, y);
-            y = fmaf(Cv.z, hv.z, y);
-            y = fmaf(Cv.w, hv.w, y);
+        }
+#pragma unroll
+        for (int q = 0; q < PPL; ++q) {
+            const int n = 4 * (lane + q * LPC);
+            if (n >= a.N) break;
+            float4 av = make_float4(ah, ah, ah, ah);
+            if (a.diag)
+                av = make_float4(decay<PRECISE>(de * Av[q].x), decay<PRECISE>(de * Av[q].y),
+                                 decay<PRECISE>(de * Av[q].z), decay<PRECISE>(de * Av[q].w));
+            float4 hn = hv[q];
+            hn.x = fmaf(av.x, hn.x, u * Bv[q].x);
+            hn.y = fmaf(av.y, hn.y, u * Bv[q].y);
+            hn.z = fmaf(av.z, hn.z, u * Bv[q].z);
+            hn.w = fmaf(av.w, hn.w, u * Bv[q].w);
+            *reinterpret_cast<float4*>(st + n) = hn;
+            y = fmaf(Cv[q].x, hn.x, y);
+            y = fmaf(Cv[q].y, hn.y, y);
+            y = fmaf(Cv[q].z, hn.z, y);
+            y = fmaf(Cv[q].w, hn.w, y);
         }
     }
     // every lane of the warp takes part; an LPC group never straddles the ok boundary
@@ -135,27 +147,29 @@ __global__ void __launch_bounds__(kStepThreads) ssm_step_kernel(const StepArgs a
     static_cast<T*>(a.out)[ch] = from_f32<T>(y);
 }
 
-template <typename T, int LPC>
+template <typename T, int LPC, int PPL>
 void launch_lpc(const StepArgs& s, int64_t nch, cudaStream_t stream) {
     constexpr int CPB = kStepThreads / LPC;
     (void)nch;
     const dim3 blocks((unsigned)((s.H * s.P + CPB - 1) / CPB), (unsigned)s.batch);
     if (s.conv_k > 0)
-        ssm_step_kernel<T, LPC, true><<<blocks, kStepThreads, 0, stream>>>(s);
+        ssm_step_kernel<T, LPC, PPL, true><<<blocks, kStepThreads, 0, stream>>>(s);
     else
-        ssm_step_kernel<T, LPC, false><<<blocks, kStepThreads, 0, stream>>>(s);
+        ssm_step_kernel<T, LPC, PPL, false><<<blocks, kStepThreads, 0, stream>>>(s);
 }
 
 template <typename T>
 void launch_typed(const StepArgs& s, int64_t nch, cudaStream_t stream) {
-    // lanes per channel: one 16-byte piece of the state row each, at most a warp
+    // 16-byte pieces of a state row: two per lane (the smallest power-of-two lane count
+    // that covers the row), one when the row is a single piece; N <= 256 is at most 64
     const int64_t pieces = s.N / 4;
-    if (pieces >= 32) return launch_lpc<T, 32>(s, nch, stream);
-    if (pieces >= 16) return launch_lpc<T, 16>(s, nch, stream);
-    if (pieces >= 8) return launch_lpc<T, 8>(s, nch, stream);
-    if (pieces >= 4) return launch_lpc<T, 4>(s, nch, stream);
-    if (pieces >= 2) return launch_lpc<T, 2>(s, nch, stream);
-    return launch_lpc<T, 1>(s, nch, stream);
+    if (pieces > 32) return launch_lpc<T, 32, 2>(s, nch, stream);
+    if (pieces > 16) return launch_lpc<T, 16, 2>(s, nch, stream);
+    if (pieces > 8) return launch_lpc<T, 8, 2>(s, nch, stream);
+    if (pieces > 4) return launch_lpc<T, 4, 2>(s, nch, stream);
+    if (pieces > 2) return launch_lpc<T, 2, 2>(s, nch, stream);
+    if (pieces == 2) return launch_lpc<T, 1, 2>(s, nch, stream);
+    return launch_lpc<T, 1, 1>(s, nch, stream);
 }
 
 }  // namespace
