@@ -10,9 +10,9 @@
 // bf16 planes x_hi = bf16(x'), x_lo = bf16(x' - x_hi) (read by the tensor-core SSD
 // kernels, which multiply both planes against exact bf16 operands).
 //
-// One thread per 16-byte channel vector and 16 consecutive steps: the three inputs before
+// One thread per 4 channels and 16 consecutive steps: the three inputs before
 // its current step slide through registers, so each input row is read once per thread
-// (plus a three-row halo per 16 steps); a warp's loads and stores are 512-byte rows.
+// (plus a three-row halo per 16 steps); a warp's loads and stores are contiguous rows.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -40,8 +40,8 @@ struct ConvArgs {
     int K;
 };
 
-// One 16-byte vector of inputs (VW channels from c0) at step s, fp32; rows before t = 0
-// come from x_prev, else zero.
+// One vector of inputs (VW channels from c0: 8 bytes of bf16 or 16 of fp32) at step s,
+// as fp32; rows before t = 0 come from x_prev, else zero.
 template <typename T, int VW>
 __device__ __forceinline__ void load_vec(const ConvArgs& a, int64_t b, int64_t s, int64_t c0, float (&v)[VW]) {
     const T* src = nullptr;
@@ -54,7 +54,13 @@ __device__ __forceinline__ void load_vec(const ConvArgs& a, int64_t b, int64_t s
         for (int j = 0; j < VW; ++j) v[j] = 0.0f;
         return;
     }
-    const uint4 r = *reinterpret_cast<const uint4*>(src);
+    uint4 r;
+    if constexpr (VW * sizeof(T) == 16) {
+        r = *reinterpret_cast<const uint4*>(src);
+    } else {
+        const uint2 h = *reinterpret_cast<const uint2*>(src);
+        r = make_uint4(h.x, h.y, 0u, 0u);
+    }
     if constexpr (sizeof(T) == 2) {
         const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&r);
 #pragma unroll
@@ -73,7 +79,7 @@ __device__ __forceinline__ void load_vec(const ConvArgs& a, int64_t b, int64_t s
 // SPLIT: xc holds the bf16 planes x_hi (first batch*T*ch elements) and x_lo; else fp32.
 template <typename T, bool SPLIT>
 __global__ void __launch_bounds__(kConvThreads) conv_silu_kernel(const ConvArgs a) {
-    constexpr int VW = 16 / (int)sizeof(T);  // channels per thread
+    constexpr int VW = 4;  // channels per thread (8-byte bf16 vectors, 16-byte fp32 vectors)
     constexpr bool PRECISE = sizeof(T) == 4;
     const int64_t c0 = ((int64_t)blockIdx.x * kConvVX + threadIdx.x) * VW;
     const int64_t b = blockIdx.z;
@@ -136,8 +142,8 @@ __global__ void __launch_bounds__(kConvThreads) conv_silu_kernel(const ConvArgs 
                         lo[j] = *reinterpret_cast<const uint32_t*>(&l2);
                     }
                     __nv_bfloat16* xh = static_cast<__nv_bfloat16*>(a.xc);
-                    *reinterpret_cast<uint4*>(xh + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                    *reinterpret_cast<uint4*>(xh + plane + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    *reinterpret_cast<uint2*>(xh + o) = make_uint2(hi[0], hi[1]);
+                    *reinterpret_cast<uint2*>(xh + plane + o) = make_uint2(lo[0], lo[1]);
                 } else {
                     float* xf = static_cast<float*>(a.xc) + o;
 #pragma unroll
@@ -188,7 +194,7 @@ cudaError_t conv_prepass_launch(const ScanArgs& a, void* xc, bool split, cudaStr
     const ConvArgs c = conv_args(a, xc);
     if (c.batch * c.T * c.ch == 0) return cudaSuccess;
     if (split && a.dtype != 1) return cudaErrorInvalidValue;  // planes are for bf16 inputs
-    const int vw = a.dtype == 1 ? 8 : 4;  // channels per 16-byte vector (ch is a multiple)
+    const int vw = 4;  // channels per thread (ch is a multiple of 4 for either dtype)
     const int64_t nvec = c.ch / vw;
     const int64_t tblocks = (c.T + kConvTT * kConvTY - 1) / (kConvTT * kConvTY);
     const dim3 grid((unsigned)((nvec + kConvVX - 1) / kConvVX), (unsigned)std::min<int64_t>(tblocks, 65535),
