@@ -107,6 +107,7 @@ struct DiagKernelArgs {
     int64_t T, dim, N, G, cpg;
     int64_t seg_len;
     int nseg, tiles_per_group;
+    int nsub_launched;   // host side: a state-only pass was launched ahead of this pass
 };
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
@@ -238,9 +239,9 @@ __global__ void __launch_bounds__(32 * WARPS) diag_scan_kernel(const DiagKernelA
         A2[k].y = (c_ok && n + 1 < a.N) ? a.A[c * a.N + n + 1] * kLog2e : 0.0f;
         h[k] = make_float2(0.0f, 0.0f);
     }
-    if (!STATE_ONLY) {
-        // state entering this segment: the initial state decayed through the earlier
-        // segments plus their local end states
+    // state entering this segment: the initial state decayed through the earlier segments
+    // plus their local end states (the state-only pass's results)
+    auto fold_initial_state = [&]() {
         if (c_ok && a.init) {
             const float* hi = a.init + (b * a.dim + c) * a.N;
 #pragma unroll
@@ -260,7 +261,7 @@ __global__ void __launch_bounds__(32 * WARPS) diag_scan_kernel(const DiagKernelA
                 if (n + 1 < a.N) h[k].y = ex2(A2[k].y * dsum) * h[k].y + Hs[n + 1];
             }
         }
-    }
+    };
 
     const int64_t row_stride = a.dim * E;     // bytes between consecutive time rows
     const int64_t bc_stride = a.G * a.N * E;  // bytes between consecutive B/C rows
@@ -361,10 +362,18 @@ __global__ void __launch_bounds__(32 * WARPS) diag_scan_kernel(const DiagKernelA
         store_pair<T>(a.out + (b * a.T + t) * row_stride + cA * E, y);
     };
 
+    // The output pass may start while the state-only pass is finishing (programmatic
+    // dependent launch): inputs only until griddepcontrol.wait, which returns once that
+    // grid has completed and its writes are visible; before it, nothing is written.
+    if (STATE_ONLY) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // prologue: tiles 0..2 in flight, tile 0 prepared
     issue_tile(0);
     issue_tile(1);
     issue_tile(2);
+    if (!STATE_ONLY) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        fold_initial_state();
+    }
     if (CONV) {
         // the three inputs before the segment: earlier rows of x, else the previous
         // call's last inputs, else zero
@@ -601,7 +610,23 @@ cudaError_t launch_one(const DiagKernelArgs& ka, dim3 grid, cudaStream_t stream)
         attr_done.fetch_or(bit, std::memory_order_relaxed);
     }
     cudaEvent_t t0 = timing_begin(stream);
-    kern<<<grid, Cfg::NT, Cfg::kSmemBytes, stream>>>(ka);
+    if (!STATE_ONLY && ka.nsub_launched) {
+        // after a state-only pass: programmatic dependent launch (see the kernel)
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr.val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(Cfg::NT);
+        cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+        cfg.stream = stream;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kern, ka);
+        if (e != cudaSuccess) return e;
+    } else {
+        kern<<<grid, Cfg::NT, Cfg::kSmemBytes, stream>>>(ka);
+    }
     note_launch(STATE_ONLY ? "diag_scan_kernel (segment state pass)" : "diag_scan_kernel (output pass)", stream, t0);
     return cudaGetLastError();
 }
@@ -635,6 +660,7 @@ cudaError_t launch_typed(const ScanArgs& a, const Plan& p, void* ws, cudaStream_
     ka.tiles_per_group = p.tiles_per_group;
     ka.seg_h = nullptr;
     ka.seg_dsum = nullptr;
+    ka.nsub_launched = 0;
     if (p.nseg > 1) {
         const size_t hbytes = (size_t)(p.nseg - 1) * a.batch * a.nheads * a.dstate * sizeof(float);
         ka.seg_h = (float*)ws;
@@ -643,6 +669,7 @@ cudaError_t launch_typed(const ScanArgs& a, const Plan& p, void* ws, cudaStream_
         cudaError_t e = CONV ? launch_one<T, NK, LPC, true, false, true>(ka, g1, stream)
                              : launch_one<T, NK, LPC, true, false, false>(ka, g1, stream);
         if (e != cudaSuccess) return e;
+        ka.nsub_launched = 1;
     }
     const dim3 g2(p.blocks_x, p.nseg, (unsigned)a.batch);
     if (a.z) return launch_one<T, NK, LPC, false, true, CONV>(ka, g2, stream);
