@@ -220,7 +220,6 @@ def kernel_roofline(kt, nbytes, calls, peak_gbs, peak_kind, whole):
 NCU_TRAFFIC = {
     ("scan", "c1", "diag_scan_kernel (output pass)"): 26_596_352 + 1_536,
     ("decode", "c1/8192", "ssm_step_kernel"): 294_216_448 + 221_896_960,
-    ("backward", "c1", "scan_bwd_kernel"): 38_175_744 + 19_325_440,
 }
 
 

@@ -29,6 +29,9 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <cstdlib>
+
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
 
@@ -44,6 +47,43 @@ constexpr int kBwdThreads = 256;
 int bwd_lanes(int64_t N) { return N <= 4 ? 4 : N <= 8 ? 8 : N <= 16 ? 16 : 32; }
 int bwd_entries(int64_t N) { return N <= 32 ? 1 : N <= 64 ? 2 : N <= 128 ? 4 : 8; }
 int bwd_seg(int64_t N) { return bwd_entries(N) <= 2 ? 16 : bwd_entries(N) == 4 ? 8 : 4; }
+
+// Time parts: SSM_BWD_PARTS when set (tuning knob).  Otherwise one part when the channels
+// give at least 8 warps per SM sub-partition (measured on B300: more parts only add the
+// summary pass), else enough parts for ~32 warps per sub-partition, at most 16 and at
+// least two checkpoint segments each (c1 backward: 1 part 1.15 ms, 4 parts 0.78 ms, 8-16
+// parts 0.72 ms).  Each part is a whole number of checkpoint segments; the part count is
+// recomputed from that length.
+struct BwdPlan {
+    int64_t nseg, subs_per_part;
+    int parts;
+    size_t ckpt_bytes, h_off, q_off, d_off, total;
+};
+BwdPlan bwd_plan(const ScanArgs& a) {
+    static const int knob = [] {
+        const char* e = getenv("SSM_BWD_PARTS");
+        return e ? atoi(e) : 0;
+    }();
+    BwdPlan p;
+    const int64_t seg = bwd_seg(a.dstate);
+    p.nseg = (a.seqlen + seg - 1) / seg;
+    const int64_t smsp = 148 * 4;  // B300 SM sub-partitions
+    const int64_t warps = (int64_t)a.batch * a.nheads * a.headdim * bwd_lanes(a.dstate) / 32;
+    int64_t rule = 1;
+    if (warps > 0 && warps < 8 * smsp)
+        rule = std::min<int64_t>({16, (32 * smsp + warps - 1) / warps, std::max<int64_t>(1, p.nseg / 2)});
+    const int64_t want = std::max<int64_t>(1, std::min<int64_t>(knob > 0 ? knob : rule, std::max<int64_t>(p.nseg, 1)));
+    p.subs_per_part = std::max<int64_t>(1, (p.nseg + want - 1) / want);
+    p.parts = (int)std::max<int64_t>(1, (p.nseg + p.subs_per_part - 1) / p.subs_per_part);
+    const size_t ch = (size_t)a.batch * a.nheads * a.headdim;
+    p.ckpt_bytes = align_up(ch * p.nseg * a.dstate * sizeof(float), 256);
+    const size_t hq = p.parts > 1 ? align_up(ch * p.parts * a.dstate * sizeof(float), 256) : 0;
+    p.h_off = p.ckpt_bytes;
+    p.q_off = p.h_off + hq;
+    p.d_off = p.q_off + hq;
+    p.total = p.d_off + (p.parts > 1 ? align_up(ch * p.parts * sizeof(float), 256) : 0);
+    return p;
+}
 
 template <typename T>
 struct BwdArgs {
@@ -68,9 +108,14 @@ struct BwdArgs {
     float* ddt_bias;
     float* dinit;
     float* ckpt;  // (b, nseg, dim, N): state entering each segment
+    // time parts (blockIdx.y), each subs_per_part segments: the parts pass writes, per
+    // part k, the local end state Hloc (from zero), the local adjoint Qloc carried out of
+    // its first step (from zero at its end), both (b, parts, dim, N), and Dsum (b, parts,
+    // dim), the sum of Delta over the part
+    float *Hloc, *Qloc, *Dsum;
     int64_t L, dim, N, G, cpg;  // L: sequence length; dim: channels (SSD: heads x P)
     int64_t P;                  // channels per head (SSD headdim; 1 in diagonal mode)
-    int nseg, tiles_per_group;
+    int nseg, tiles_per_group, subs_per_part;
 };
 
 template <int LPC>
@@ -80,12 +125,18 @@ __device__ __forceinline__ float lane_sum(float v) {
     return v;
 }
 
-// grid (G * tiles_per_group, 1, batch); LPC lanes x R entries per channel, CPB channels,
-// checkpoints every kSeg steps.
+// grid (G * tiles_per_group, parts, batch); LPC lanes x R entries per channel, CPB
+// channels, checkpoints every kSeg steps.
+// PARTS: the summaries of every time part (forward sweep from zero, adjoint-only reverse
+// sweep from zero).  Otherwise the gradients over one part, its entering state folded from
+// the earlier parts' summaries, h <- exp(A Dsum_k) h + Hloc_k, and its entering adjoint
+// from the later parts', q <- Qloc_k + exp(A Dsum_k) q (the affine combine of the
+// parallel-scan formulation, "引言：Attention的天花板" article, 硬件感知算法, run in both
+// directions).
 // The per-step scalars of a channel (Delta, Delta x, dy, the SiLU' factor, sigmoid(v)) are
 // computed once per segment, spread over the channel's lanes (lane j % LPC holds step j),
 // and fetched with shuffles inside the sequential sweeps.
-template <typename T, int LPC, int R, int kSeg, bool SSD>
+template <typename T, int LPC, int R, int kSeg, bool SSD, bool PARTS>
 __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> a) {
     constexpr bool PRECISE = sizeof(T) == 4;
     constexpr int CPB = kBwdThreads / LPC;
@@ -138,15 +189,30 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
     auto bc = [&](int64_t t) { return (b * L + t) * G * N + (int64_t)group * N; };
     auto fetch = [&](const float (&v)[SPL], int j) { return __shfl_sync(0xffffffffu, v[j / LPC], j % LPC, LPC); };
 
-    // forward sweep: checkpoints of the state entering every segment
+    const int part = blockIdx.y, nparts = gridDim.y;
+    const int sub0 = part * a.subs_per_part, sub1 = min(a.nseg, sub0 + a.subs_per_part);
+    auto sidx = [&](int k) { return (b * nparts + k) * dim + c; };  // summary of part k
+
+    // forward sweep: checkpoints of the state entering every segment of the part
     float h[R];
 #pragma unroll
-    for (int r = 0; r < R; ++r) h[r] = (nok[r] && a.init) ? a.init[(b * dim + c) * N + nr[r]] : 0.0f;
-    for (int seg = 0; seg < a.nseg; ++seg) {
-        const int64_t t0 = (int64_t)seg * kSeg;
+    for (int r = 0; r < R; ++r) h[r] = (!PARTS && nok[r] && a.init) ? a.init[(b * dim + c) * N + nr[r]] : 0.0f;
+    if (!PARTS) {
+        for (int k = 0; k < part && c_ok; ++k) {
+            const float ds = a.Dsum[sidx(k)];
 #pragma unroll
-        for (int r = 0; r < R; ++r)
-            if (nok[r]) a.ckpt[((b * a.nseg + seg) * dim + c) * N + nr[r]] = h[r];
+            for (int r = 0; r < R; ++r)
+                if (nok[r]) h[r] = fmaf(decay(ds, r), h[r], a.Hloc[sidx(k) * N + nr[r]]);
+        }
+    }
+    float dsum_lane = 0.0f;  // PARTS: this lane's steps of Delta
+    for (int seg = sub0; seg < sub1; ++seg) {
+        const int64_t t0 = (int64_t)seg * kSeg;
+        if (!PARTS) {
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+                if (nok[r]) a.ckpt[((b * a.nseg + seg) * dim + c) * N + nr[r]] = h[r];
+        }
         const int len = (int)min((int64_t)kSeg, L - t0);
         float pde[SPL], pu[SPL];
 #pragma unroll
@@ -156,6 +222,7 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
             if (c_ok && j < len) {
                 pde[k] = softplus_t<PRECISE>(to_f32<T>(a.dt[drow(t0 + j)]) + bias);
                 pu[k] = pde[k] * to_f32<T>(a.x[row(t0 + j)]);
+                dsum_lane += pde[k];
             }
         }
 #pragma unroll
@@ -172,151 +239,217 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
         }
     }
 
-    // reverse sweep
-    float g[R], dA_acc[R];
+    if (PARTS) {
+        // the part's Delta sum and local end state; then its local adjoint, from zero at
+        // its end, carried out of its first step (g_t = dy_t C_t + a_{t+1} g_{t+1})
+        const float dsum = lane_sum<LPC>(dsum_lane);
+        if (c_ok && lane == 0) a.Dsum[sidx(part)] = dsum;
+        if (part < nparts - 1) {
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-        g[r] = (nok[r] && a.dfinal) ? a.dfinal[(b * dim + c) * N + nr[r]] : 0.0f;
-        dA_acc[r] = 0.0f;
-    }
-    float dD_acc = 0.0f, dbias_acc = 0.0f;  // this lane's steps
-    for (int seg = a.nseg - 1; seg >= 0; --seg) {
-        const int64_t t0 = (int64_t)seg * kSeg;
-        const int len = (int)min((int64_t)kSeg, L - t0);
-        // per-step scalars of the segment
-        float pde[SPL], pu[SPL], px[SPL], pdy[SPL], pdz[SPL], psig[SPL];
+            for (int r = 0; r < R; ++r)
+                if (nok[r]) a.Hloc[sidx(part) * N + nr[r]] = h[r];
+        }
+        if (part == 0) return;
+        float q[R];
 #pragma unroll
-        for (int k = 0; k < SPL; ++k) {
-            const int j = lane + LPC * k;
-            pde[k] = pu[k] = px[k] = pdy[k] = pdz[k] = psig[k] = 0.0f;
-            if (c_ok && j < len) {
-                const int64_t t = t0 + j;
-                const float v = to_f32<T>(a.dt[drow(t)]) + bias;
-                pde[k] = softplus_t<PRECISE>(v);
-                psig[k] = 1.0f / (1.0f + __expf(-v));
-                px[k] = to_f32<T>(a.x[row(t)]);
-                pu[k] = pde[k] * px[k];
-                const float dov = to_f32<T>(a.dout[row(t)]);
-                if (a.z) {
-                    const float zv = to_f32<T>(a.z[row(t)]);
-                    const float sz = 1.0f / (1.0f + __expf(-zv));
-                    pdy[k] = dov * zv * sz;
-                    pdz[k] = dov * sz * (1.0f + zv * (1.0f - sz));
-                } else {
-                    pdy[k] = dov;
+        for (int r = 0; r < R; ++r) q[r] = 0.0f;
+        for (int seg = sub1 - 1; seg >= sub0; --seg) {
+            const int64_t t0 = (int64_t)seg * kSeg;
+            const int len = (int)min((int64_t)kSeg, L - t0);
+            float pde[SPL], pdy[SPL];
+#pragma unroll
+            for (int k = 0; k < SPL; ++k) {
+                const int j = lane + LPC * k;
+                pde[k] = pdy[k] = 0.0f;
+                if (c_ok && j < len) {
+                    const int64_t t = t0 + j;
+                    pde[k] = softplus_t<PRECISE>(to_f32<T>(a.dt[drow(t)]) + bias);
+                    const float dov = to_f32<T>(a.dout[row(t)]);
+                    if (a.z) {
+                        const float zv = to_f32<T>(a.z[row(t)]);
+                        pdy[k] = dov * zv / (1.0f + __expf(-zv));
+                    } else {
+                        pdy[k] = dov;
+                    }
                 }
             }
-        }
-        // the segment's states h_t (after step t), recomputed from the checkpoint
-        float hs[kSeg][R], h0[R];
 #pragma unroll
-        for (int r = 0; r < R; ++r) h0[r] = nok[r] ? a.ckpt[((b * a.nseg + seg) * dim + c) * N + nr[r]] : 0.0f;
-#pragma unroll
-        for (int j = 0; j < kSeg; ++j) {
-            if (j < len) {
-                const float de = fetch(pde, j), u = fetch(pu, j);
+            for (int j = kSeg - 1; j >= 0; --j) {
+                if (j >= len) continue;
+                const float de = fetch(pde, j), dy = fetch(pdy, j);
                 float av[R];
                 decays(de, av);
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    const float Bv = nok[r] ? to_f32<T>(a.B[bc(t0 + j) + nr[r]]) : 0.0f;
-                    hs[j][r] = fmaf(av[r], j == 0 ? h0[r] : hs[j - 1][r], u * Bv);
+                    const float Cv = nok[r] ? to_f32<T>(a.C[bc(t0 + j) + nr[r]]) : 0.0f;
+                    q[r] = av[r] * fmaf(dy, Cv, q[r]);
                 }
             }
         }
 #pragma unroll
-        for (int j = kSeg - 1; j >= 0; --j) {
-            if (j >= len) continue;
-            const int64_t t = t0 + j;
-            const float de = fetch(pde, j), xv = fetch(px, j), dy = fetch(pdy, j);
-            float yp = 0.0f, dxp = 0.0f, ddp = 0.0f;
-            float avs[R];
-            decays(de, avs);
+        for (int r = 0; r < R; ++r)
+            if (nok[r]) a.Qloc[sidx(part) * N + nr[r]] = q[r];
+    } else {
+        // reverse sweep: the adjoint entering the part's last step, folded from the later
+        // parts
+        float g[R], dA_acc[R];
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const float Bv = nok[r] ? to_f32<T>(a.B[bc(t) + nr[r]]) : 0.0f;
-                const float Cv = nok[r] ? to_f32<T>(a.C[bc(t) + nr[r]]) : 0.0f;
-                const float av = avs[r];
-                const float hp = j == 0 ? h0[r] : hs[j - 1][r];
-                yp = fmaf(Cv, hs[j][r], yp);
-                g[r] = fmaf(dy, Cv, g[r]);
-                dxp = fmaf(g[r] * de, Bv, dxp);
-                ddp = fmaf(g[r], fmaf(av * Aval(r), hp, Bv * xv), ddp);
-                dA_acc[r] = fmaf(g[r] * av * de, hp, dA_acc[r]);
-                s_dB[(j * CPB + cc) * NP + r * LPC + lane] = g[r] * de * xv;
-                s_dC[(j * CPB + cc) * NP + r * LPC + lane] = dy * hs[j][r];
-                g[r] *= av;  // dL/dh_{t-1}
-            }
-            // three independent reductions over the channel's lanes
+        for (int r = 0; r < R; ++r) {
+            g[r] = (nok[r] && a.dfinal) ? a.dfinal[(b * dim + c) * N + nr[r]] : 0.0f;
+            dA_acc[r] = 0.0f;
+        }
+        for (int k = nparts - 1; k > part && c_ok; --k) {
+            const float ds = a.Dsum[sidx(k)];
 #pragma unroll
-            for (int o = LPC / 2; o > 0; o >>= 1) {
-                yp += __shfl_xor_sync(0xffffffffu, yp, o, LPC);
-                dxp += __shfl_xor_sync(0xffffffffu, dxp, o, LPC);
-                ddp += __shfl_xor_sync(0xffffffffu, ddp, o, LPC);
+            for (int r = 0; r < R; ++r)
+                if (nok[r]) g[r] = fmaf(decay(ds, r), g[r], a.Qloc[sidx(k) * N + nr[r]]);
+        }
+        float dD_acc = 0.0f, dbias_acc = 0.0f;  // this lane's steps
+        for (int seg = sub1 - 1; seg >= sub0; --seg) {
+            const int64_t t0 = (int64_t)seg * kSeg;
+            const int len = (int)min((int64_t)kSeg, L - t0);
+            // per-step scalars of the segment
+            float pde[SPL], pu[SPL], px[SPL], pdy[SPL], pdz[SPL], psig[SPL];
+#pragma unroll
+            for (int k = 0; k < SPL; ++k) {
+                const int j = lane + LPC * k;
+                pde[k] = pu[k] = px[k] = pdy[k] = pdz[k] = psig[k] = 0.0f;
+                if (c_ok && j < len) {
+                    const int64_t t = t0 + j;
+                    const float v = to_f32<T>(a.dt[drow(t)]) + bias;
+                    pde[k] = softplus_t<PRECISE>(v);
+                    psig[k] = 1.0f / (1.0f + __expf(-v));
+                    px[k] = to_f32<T>(a.x[row(t)]);
+                    pu[k] = pde[k] * px[k];
+                    const float dov = to_f32<T>(a.dout[row(t)]);
+                    if (a.z) {
+                        const float zv = to_f32<T>(a.z[row(t)]);
+                        const float sz = 1.0f / (1.0f + __expf(-zv));
+                        pdy[k] = dov * zv * sz;
+                        pdz[k] = dov * sz * (1.0f + zv * (1.0f - sz));
+                    } else {
+                        pdy[k] = dov;
+                    }
+                }
             }
-            if (c_ok && lane == j % LPC) {  // the lane that holds step j's scalars
-                const int k = j / LPC;
-                a.dx[row(t)] = fmaf(dy, Dc, dxp);
-                const float dv = ddp * psig[k];
+            // the segment's states h_t (after step t), recomputed from the checkpoint
+            float hs[kSeg][R], h0[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) h0[r] = nok[r] ? a.ckpt[((b * a.nseg + seg) * dim + c) * N + nr[r]] : 0.0f;
+#pragma unroll
+            for (int j = 0; j < kSeg; ++j) {
+                if (j < len) {
+                    const float de = fetch(pde, j), u = fetch(pu, j);
+                    float av[R];
+                    decays(de, av);
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const float Bv = nok[r] ? to_f32<T>(a.B[bc(t0 + j) + nr[r]]) : 0.0f;
+                        hs[j][r] = fmaf(av[r], j == 0 ? h0[r] : hs[j - 1][r], u * Bv);
+                    }
+                }
+            }
+#pragma unroll
+            for (int j = kSeg - 1; j >= 0; --j) {
+                if (j >= len) continue;
+                const int64_t t = t0 + j;
+                const float de = fetch(pde, j), xv = fetch(px, j), dy = fetch(pdy, j);
+                float yp = 0.0f, dxp = 0.0f, ddp = 0.0f;
+                float avs[R];
+                decays(de, avs);
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const float Bv = nok[r] ? to_f32<T>(a.B[bc(t) + nr[r]]) : 0.0f;
+                    const float Cv = nok[r] ? to_f32<T>(a.C[bc(t) + nr[r]]) : 0.0f;
+                    const float av = avs[r];
+                    const float hp = j == 0 ? h0[r] : hs[j - 1][r];
+                    yp = fmaf(Cv, hs[j][r], yp);
+                    g[r] = fmaf(dy, Cv, g[r]);
+                    dxp = fmaf(g[r] * de, Bv, dxp);
+                    ddp = fmaf(g[r], fmaf(av * Aval(r), hp, Bv * xv), ddp);
+                    dA_acc[r] = fmaf(g[r] * av * de, hp, dA_acc[r]);
+                    s_dB[(j * CPB + cc) * NP + r * LPC + lane] = g[r] * de * xv;
+                    s_dC[(j * CPB + cc) * NP + r * LPC + lane] = dy * hs[j][r];
+                    g[r] *= av;  // dL/dh_{t-1}
+                }
+                // three independent reductions over the channel's lanes
+#pragma unroll
+                for (int o = LPC / 2; o > 0; o >>= 1) {
+                    yp += __shfl_xor_sync(0xffffffffu, yp, o, LPC);
+                    dxp += __shfl_xor_sync(0xffffffffu, dxp, o, LPC);
+                    ddp += __shfl_xor_sync(0xffffffffu, ddp, o, LPC);
+                }
+                if (c_ok && lane == j % LPC) {  // the lane that holds step j's scalars
+                    const int k = j / LPC;
+                    a.dx[row(t)] = fmaf(dy, Dc, dxp);
+                    const float dv = ddp * psig[k];
+                    if (SSD)
+                        atomicAdd(&a.ddt[drow(t)], dv);  // the head's channels share Delta_t
+                    else
+                        a.ddt[row(t)] = dv;
+                    dbias_acc += dv;
+                    dD_acc = fmaf(dy, xv, dD_acc);
+                    if (a.z) a.dz[row(t)] = pdz[k] * (yp + Dc * xv);
+                }
+            }
+            __syncthreads();  // the segment's dB / dC terms are in shared memory
+            for (int i = tid; i < len * NP; i += kBwdThreads) {
+                const int j = i / NP, n = i % NP;
+                if (n < N) {
+                    float sb = 0.0f, sc = 0.0f;
+                    const int cmax = (int)min((int64_t)CPB, c_end - c_begin);
+                    for (int q = 0; q < cmax; ++q) {
+                        sb += s_dB[(j * CPB + q) * NP + n];
+                        sc += s_dC[(j * CPB + q) * NP + n];
+                    }
+                    const int64_t o = bc(t0 + j) + n;
+                    atomicAdd(&a.dB[o], sb);
+                    atomicAdd(&a.dC[o], sc);
+                }
+            }
+            __syncthreads();  // read before the next segment overwrites them
+        }
+        dD_acc = lane_sum<LPC>(dD_acc);
+        dbias_acc = lane_sum<LPC>(dbias_acc);
+        float dA_sum = 0.0f;  // SSD: the head's dA sums every entry of the channel
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+            if (nok[r]) {
+                if (a.dinit && part == 0) a.dinit[(b * dim + c) * N + nr[r]] = g[r];
                 if (SSD)
-                    atomicAdd(&a.ddt[drow(t)], dv);  // the head's channels share Delta_t
+                    dA_sum += dA_acc[r];
                 else
-                    a.ddt[row(t)] = dv;
-                dbias_acc += dv;
-                dD_acc = fmaf(dy, xv, dD_acc);
-                if (a.z) a.dz[row(t)] = pdz[k] * (yp + Dc * xv);
+                    atomicAdd(&a.dA[c * N + nr[r]], dA_acc[r]);
             }
+        if (SSD) dA_sum = lane_sum<LPC>(dA_sum);
+        if (c_ok && lane == 0) {
+            if (SSD) atomicAdd(&a.dA[hd], dA_sum);
+            if (a.dD) atomicAdd(&a.dD[hd], dD_acc);
+            if (a.ddt_bias) atomicAdd(&a.ddt_bias[hd], dbias_acc);
         }
-        __syncthreads();  // the segment's dB / dC terms are in shared memory
-        for (int i = tid; i < len * NP; i += kBwdThreads) {
-            const int j = i / NP, n = i % NP;
-            if (n < N) {
-                float sb = 0.0f, sc = 0.0f;
-                const int cmax = (int)min((int64_t)CPB, c_end - c_begin);
-                for (int q = 0; q < cmax; ++q) {
-                    sb += s_dB[(j * CPB + q) * NP + n];
-                    sc += s_dC[(j * CPB + q) * NP + n];
-                }
-                const int64_t o = bc(t0 + j) + n;
-                atomicAdd(&a.dB[o], sb);
-                atomicAdd(&a.dC[o], sc);
-            }
-        }
-        __syncthreads();  // read before the next segment overwrites them
-    }
-    dD_acc = lane_sum<LPC>(dD_acc);
-    dbias_acc = lane_sum<LPC>(dbias_acc);
-    float dA_sum = 0.0f;  // SSD: the head's dA sums every entry of the channel
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-        if (nok[r]) {
-            if (a.dinit) a.dinit[(b * dim + c) * N + nr[r]] = g[r];
-            if (SSD)
-                dA_sum += dA_acc[r];
-            else
-                atomicAdd(&a.dA[c * N + nr[r]], dA_acc[r]);
-        }
-    if (SSD) dA_sum = lane_sum<LPC>(dA_sum);
-    if (c_ok && lane == 0) {
-        if (SSD) atomicAdd(&a.dA[hd], dA_sum);
-        if (a.dD) atomicAdd(&a.dD[hd], dD_acc);
-        if (a.ddt_bias) atomicAdd(&a.ddt_bias[hd], dbias_acc);
     }
 }
 
 template <typename T, int LPC, int R, bool SSD>
-cudaError_t launch_bwd(const BwdArgs<T>& a, int64_t batch, cudaStream_t stream) {
+cudaError_t launch_bwd(const BwdArgs<T>& a, int parts, int64_t batch, cudaStream_t stream) {
     constexpr int kSeg = R <= 2 ? 16 : R == 4 ? 8 : 4;  // as bwd_seg
     constexpr int CPB = kBwdThreads / LPC;
     constexpr size_t kSmem = sizeof(float) * 2 * kSeg * CPB * LPC * R;
     BwdArgs<T> k = a;
     k.tiles_per_group = (int)((a.cpg + CPB - 1) / CPB);
-    k.nseg = (int)((a.L + kSeg - 1) / kSeg);
-    if (kSeg != bwd_seg(a.N)) return cudaErrorInvalidValue;  // scratch sized by bwd_seg
-    const dim3 grid((unsigned)(a.G * k.tiles_per_group), 1, (unsigned)batch);
-    auto kern = scan_bwd_kernel<T, LPC, R, kSeg, SSD>;
+    if (kSeg != bwd_seg(a.N) || k.nseg != (int)((a.L + kSeg - 1) / kSeg))
+        return cudaErrorInvalidValue;  // scratch sized by bwd_plan
+    const dim3 grid((unsigned)(a.G * k.tiles_per_group), (unsigned)parts, (unsigned)batch);
+    auto kern = scan_bwd_kernel<T, LPC, R, kSeg, SSD, false>;
     if (kSmem > 48 * 1024) {
         const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+        if (e != cudaSuccess) return e;
+    }
+    if (parts > 1) {
+        cudaEvent_t t1 = timing_begin(stream);
+        scan_bwd_kernel<T, LPC, R, kSeg, SSD, true><<<grid, kBwdThreads, 0, stream>>>(k);
+        note_launch("scan_bwd_kernel (part summaries)", stream, t1);
+        const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     cudaEvent_t t0 = timing_begin(stream);
@@ -349,7 +482,13 @@ cudaError_t bwd_typed(const ScanBwdArgs& s, void* ws, cudaStream_t stream) {
     a.dz = s.dz;
     a.ddt_bias = s.ddt_bias;
     a.dinit = s.dinit;
+    const BwdPlan pl = bwd_plan(f);
     a.ckpt = (float*)ws;
+    a.Hloc = (float*)((char*)ws + pl.h_off);
+    a.Qloc = (float*)((char*)ws + pl.q_off);
+    a.Dsum = (float*)((char*)ws + pl.d_off);
+    a.nseg = (int)pl.nseg;
+    a.subs_per_part = (int)pl.subs_per_part;
     const bool ssd = s.ssd;
     a.L = f.seqlen;
     a.dim = f.nheads * f.headdim;
@@ -357,32 +496,27 @@ cudaError_t bwd_typed(const ScanBwdArgs& s, void* ws, cudaStream_t stream) {
     a.N = f.dstate;
     a.G = f.ngroups;
     a.cpg = a.dim / f.ngroups;
-    a.nseg = 0;
     a.tiles_per_group = 0;
     const int lpc = bwd_lanes(f.dstate), r = bwd_entries(f.dstate);
     if (ssd) {
-        if (lpc == 4) return launch_bwd<T, 4, 1, true>(a, f.batch, stream);
-        if (lpc == 8) return launch_bwd<T, 8, 1, true>(a, f.batch, stream);
-        if (lpc == 16) return launch_bwd<T, 16, 1, true>(a, f.batch, stream);
-        if (r == 1) return launch_bwd<T, 32, 1, true>(a, f.batch, stream);
-        if (r == 2) return launch_bwd<T, 32, 2, true>(a, f.batch, stream);
-        if (r == 4) return launch_bwd<T, 32, 4, true>(a, f.batch, stream);
-        return launch_bwd<T, 32, 8, true>(a, f.batch, stream);
+        if (lpc == 4) return launch_bwd<T, 4, 1, true>(a, pl.parts, f.batch, stream);
+        if (lpc == 8) return launch_bwd<T, 8, 1, true>(a, pl.parts, f.batch, stream);
+        if (lpc == 16) return launch_bwd<T, 16, 1, true>(a, pl.parts, f.batch, stream);
+        if (r == 1) return launch_bwd<T, 32, 1, true>(a, pl.parts, f.batch, stream);
+        if (r == 2) return launch_bwd<T, 32, 2, true>(a, pl.parts, f.batch, stream);
+        if (r == 4) return launch_bwd<T, 32, 4, true>(a, pl.parts, f.batch, stream);
+        return launch_bwd<T, 32, 8, true>(a, pl.parts, f.batch, stream);
     }
-    if (lpc == 4) return launch_bwd<T, 4, 1, false>(a, f.batch, stream);
-    if (lpc == 8) return launch_bwd<T, 8, 1, false>(a, f.batch, stream);
-    if (lpc == 16) return launch_bwd<T, 16, 1, false>(a, f.batch, stream);
-    if (r == 1) return launch_bwd<T, 32, 1, false>(a, f.batch, stream);
-    return launch_bwd<T, 32, 2, false>(a, f.batch, stream);
+    if (lpc == 4) return launch_bwd<T, 4, 1, false>(a, pl.parts, f.batch, stream);
+    if (lpc == 8) return launch_bwd<T, 8, 1, false>(a, pl.parts, f.batch, stream);
+    if (lpc == 16) return launch_bwd<T, 16, 1, false>(a, pl.parts, f.batch, stream);
+    if (r == 1) return launch_bwd<T, 32, 1, false>(a, pl.parts, f.batch, stream);
+    return launch_bwd<T, 32, 2, false>(a, pl.parts, f.batch, stream);
 }
 
 }  // namespace
 
-size_t scan_bwd_workspace_bytes(const ScanArgs& a) {
-    const int64_t seg = bwd_seg(a.dstate);
-    const int64_t nseg = (a.seqlen + seg - 1) / seg;
-    return align_up((size_t)a.batch * nseg * a.nheads * a.headdim * a.dstate * sizeof(float), 256);
-}
+size_t scan_bwd_workspace_bytes(const ScanArgs& a) { return bwd_plan(a).total; }
 
 cudaError_t scan_bwd_launch(const ScanBwdArgs& s, void* ws, cudaStream_t stream) {
     const ScanArgs& f = s.fwd;

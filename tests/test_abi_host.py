@@ -258,20 +258,36 @@ def test_backward_argument_errors():
             args[names.index(k)] = None if v is None else vp(v)
         return lib.ssm_scan_bwd(*args, ctypes.byref(shape), None, 0, None)
 
+    def parts_extra(n, ch, N):
+        """The scratch beyond the checkpoints: per time part a local end state, a local
+        adjoint (ch x N fp32 each) and a Delta sum per channel (256-byte aligned)."""
+        for p in range(1, 17):
+            hq = 0 if p == 1 else -(-(ch * p * N * 4) // 256) * 256
+            d = 0 if p == 1 else -(-(ch * p * 4) // 256) * 256
+            if n == 2 * hq + d:
+                return p
+        return None
+
     # SSD mode: the state of every (head, p) channel every 8 steps at dstate 128, every 4
-    # at 256
-    ssd = _shape(mode=1, nheads=8, headdim=64, dstate=128, chunk=64)
-    assert lib.ssm_scan_bwd_workspace_size(ctypes.byref(ssd)) == 2 * (64 // 8) * 8 * 64 * 128 * 4
-    ssd256 = _shape(mode=1, nheads=2, headdim=64, dstate=256)
-    assert lib.ssm_scan_bwd_workspace_size(ctypes.byref(ssd256)) == 2 * (64 // 4) * 2 * 64 * 256 * 4
-    assert call(ssd, dB=(15 << 12) + 8) == _lib.SSM_ERR_ALIGN
+    # at 256; with this many channels the sequence is not split into time parts
+    ssd = _shape(mode=1, batch=16, nheads=64, headdim=64, dstate=128, chunk=64)
+    assert lib.ssm_scan_bwd_workspace_size(ctypes.byref(ssd)) == 16 * (64 // 8) * 64 * 64 * 128 * 4
+    ssd256 = _shape(mode=1, batch=16, nheads=64, headdim=64, dstate=256)
+    assert lib.ssm_scan_bwd_workspace_size(ctypes.byref(ssd256)) == 16 * (64 // 4) * 64 * 64 * 256 * 4
+    # few channels: the checkpoints plus the summaries of several time parts
+    small = _shape(mode=1, nheads=8, headdim=64, dstate=128, chunk=64)
+    ckpt = 2 * (64 // 8) * 8 * 64 * 128 * 4
+    n = lib.ssm_scan_bwd_workspace_size(ctypes.byref(small))
+    assert n > ckpt and (parts_extra(n - ckpt, 2 * 8 * 64, 128) or 0) > 1
+    assert call(small, dB=(15 << 12) + 8) == _lib.SSM_ERR_ALIGN
     assert lib.ssm_scan_bwd_workspace_size(ctypes.byref(_shape(mode=1, dstate=300))) == BAD
     assert call(s, dx=None) == _lib.SSM_ERR_NULL
     assert call(s, dout=None) == _lib.SSM_ERR_NULL
     assert call(s, dA=None) == _lib.SSM_ERR_NULL
     assert call(s, dB=(15 << 12) + 8) == _lib.SSM_ERR_ALIGN
     n = lib.ssm_scan_bwd_workspace_size(ctypes.byref(s))
-    assert n == 2 * (64 // 16) * 64 * 16 * 4   # the state every 16 steps
+    ckpt = 2 * (64 // 16) * 64 * 16 * 4   # the state every 16 steps
+    assert n >= ckpt and parts_extra(n - ckpt, 2 * 64, 16) is not None
 
 
 def test_timing_collect_without_launches():
