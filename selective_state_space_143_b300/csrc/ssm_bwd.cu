@@ -46,7 +46,6 @@ constexpr int kBwdThreads = 256;
 // reductions); checkpoint segment length by entries per lane.
 int bwd_lanes(int64_t N) { return N <= 4 ? 4 : N <= 8 ? 8 : N <= 16 ? 16 : 32; }
 int bwd_entries(int64_t N) { return N <= 32 ? 1 : N <= 64 ? 2 : N <= 128 ? 4 : 8; }
-int bwd_seg(int64_t N) { return bwd_entries(N) <= 2 ? 16 : bwd_entries(N) == 4 ? 8 : 4; }
 
 // Time parts: SSM_BWD_PARTS when set (tuning knob).  Otherwise one part when the channels
 // give at least 8 warps per SM sub-partition (measured on B300: more parts only add the
@@ -55,6 +54,7 @@ int bwd_seg(int64_t N) { return bwd_entries(N) <= 2 ? 16 : bwd_entries(N) == 4 ?
 // parts 0.72 ms).  Each part is a whole number of checkpoint segments; the part count is
 // recomputed from that length.
 struct BwdPlan {
+    int lpc, r, seg;  // lanes per channel, entries per lane, checkpoint segment length
     int64_t nseg, subs_per_part;
     int parts;
     size_t ckpt_bytes, h_off, q_off, d_off, total;
@@ -64,11 +64,35 @@ BwdPlan bwd_plan(const ScanArgs& a) {
         const char* e = getenv("SSM_BWD_PARTS");
         return e ? atoi(e) : 0;
     }();
+    // SSM_BWD_LPC (4, 8, 16 or 32): lanes per channel in diagonal mode (tuning knob)
+    static const int knob_lpc = [] {
+        const char* e = getenv("SSM_BWD_LPC");
+        return e ? atoi(e) : 0;
+    }();
     BwdPlan p;
-    const int64_t seg = bwd_seg(a.dstate);
+    p.lpc = bwd_lanes(a.dstate);
+    p.r = bwd_entries(a.dstate);
+    if (a.headdim == 1 && a.dstate <= 64) {
+        // diagonal mode: four entries per lane (fewer per-step reductions; the time parts
+        // supply the parallelism): c1 0.49 ms against 0.73 ms with one entry per lane,
+        // c2 19.6 ms against 22.2 ms
+        p.lpc = a.dstate <= 16 ? 4 : a.dstate <= 32 ? 8 : 16;
+        p.r = 1;
+        while (p.r * p.lpc < a.dstate) p.r *= 2;
+    }
+    if (a.headdim == 1 && a.dstate <= 64 && (knob_lpc == 4 || knob_lpc == 8 || knob_lpc == 16 || knob_lpc == 32)) {
+        int r = 1;
+        while (r * knob_lpc < a.dstate) r *= 2;
+        if (r <= 4) {
+            p.lpc = knob_lpc;
+            p.r = r;
+        }
+    }
+    p.seg = p.r <= 2 ? 16 : p.r == 4 ? 8 : 4;
+    const int64_t seg = p.seg;
     p.nseg = (a.seqlen + seg - 1) / seg;
     const int64_t smsp = 148 * 4;  // B300 SM sub-partitions
-    const int64_t warps = (int64_t)a.batch * a.nheads * a.headdim * bwd_lanes(a.dstate) / 32;
+    const int64_t warps = (int64_t)a.batch * a.nheads * a.headdim * p.lpc / 32;
     int64_t rule = 1;
     if (warps > 0 && warps < 8 * smsp)
         rule = std::min<int64_t>({16, (32 * smsp + warps - 1) / warps, std::max<int64_t>(1, p.nseg / 2)});
@@ -432,12 +456,12 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
 
 template <typename T, int LPC, int R, bool SSD>
 cudaError_t launch_bwd(const BwdArgs<T>& a, int parts, int64_t batch, cudaStream_t stream) {
-    constexpr int kSeg = R <= 2 ? 16 : R == 4 ? 8 : 4;  // as bwd_seg
+    constexpr int kSeg = R <= 2 ? 16 : R == 4 ? 8 : 4;  // as bwd_plan
     constexpr int CPB = kBwdThreads / LPC;
     constexpr size_t kSmem = sizeof(float) * 2 * kSeg * CPB * LPC * R;
     BwdArgs<T> k = a;
     k.tiles_per_group = (int)((a.cpg + CPB - 1) / CPB);
-    if (kSeg != bwd_seg(a.N) || k.nseg != (int)((a.L + kSeg - 1) / kSeg))
+    if (k.nseg != (int)((a.L + kSeg - 1) / kSeg))
         return cudaErrorInvalidValue;  // scratch sized by bwd_plan
     const dim3 grid((unsigned)(a.G * k.tiles_per_group), (unsigned)parts, (unsigned)batch);
     auto kern = scan_bwd_kernel<T, LPC, R, kSeg, SSD, false>;
@@ -456,6 +480,34 @@ cudaError_t launch_bwd(const BwdArgs<T>& a, int parts, int64_t batch, cudaStream
     kern<<<grid, kBwdThreads, kSmem, stream>>>(k);
     note_launch("scan_bwd_kernel", stream, t0);
     return cudaGetLastError();
+}
+
+// Every (lanes, entries) pair the plans choose: the defaults (one entry per lane up to
+// 32 lanes, then 2, 4, 8 entries) and the diagonal-mode tuning knob's (2 or 4 entries
+// with 4 to 16 lanes).
+template <typename T, bool SSD>
+cudaError_t launch_mode(int lpc, int r, const BwdArgs<T>& a, int parts, int64_t batch, cudaStream_t stream) {
+    switch (lpc * 10 + r) {
+        case 41: return launch_bwd<T, 4, 1, SSD>(a, parts, batch, stream);
+        case 42: return launch_bwd<T, 4, 2, SSD>(a, parts, batch, stream);
+        case 44: return launch_bwd<T, 4, 4, SSD>(a, parts, batch, stream);
+        case 81: return launch_bwd<T, 8, 1, SSD>(a, parts, batch, stream);
+        case 82: return launch_bwd<T, 8, 2, SSD>(a, parts, batch, stream);
+        case 84: return launch_bwd<T, 8, 4, SSD>(a, parts, batch, stream);
+        case 161: return launch_bwd<T, 16, 1, SSD>(a, parts, batch, stream);
+        case 162: return launch_bwd<T, 16, 2, SSD>(a, parts, batch, stream);
+        case 164: return launch_bwd<T, 16, 4, SSD>(a, parts, batch, stream);
+        case 321: return launch_bwd<T, 32, 1, SSD>(a, parts, batch, stream);
+        case 322: return launch_bwd<T, 32, 2, SSD>(a, parts, batch, stream);
+        case 324: return launch_bwd<T, 32, 4, SSD>(a, parts, batch, stream);
+        case 328: return launch_bwd<T, 32, 8, SSD>(a, parts, batch, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+template <typename T>
+cudaError_t launch_any(bool ssd, int lpc, int r, const BwdArgs<T>& a, int parts, int64_t batch, cudaStream_t stream) {
+    return ssd ? launch_mode<T, true>(lpc, r, a, parts, batch, stream)
+               : launch_mode<T, false>(lpc, r, a, parts, batch, stream);
 }
 
 template <typename T>
@@ -497,21 +549,7 @@ cudaError_t bwd_typed(const ScanBwdArgs& s, void* ws, cudaStream_t stream) {
     a.G = f.ngroups;
     a.cpg = a.dim / f.ngroups;
     a.tiles_per_group = 0;
-    const int lpc = bwd_lanes(f.dstate), r = bwd_entries(f.dstate);
-    if (ssd) {
-        if (lpc == 4) return launch_bwd<T, 4, 1, true>(a, pl.parts, f.batch, stream);
-        if (lpc == 8) return launch_bwd<T, 8, 1, true>(a, pl.parts, f.batch, stream);
-        if (lpc == 16) return launch_bwd<T, 16, 1, true>(a, pl.parts, f.batch, stream);
-        if (r == 1) return launch_bwd<T, 32, 1, true>(a, pl.parts, f.batch, stream);
-        if (r == 2) return launch_bwd<T, 32, 2, true>(a, pl.parts, f.batch, stream);
-        if (r == 4) return launch_bwd<T, 32, 4, true>(a, pl.parts, f.batch, stream);
-        return launch_bwd<T, 32, 8, true>(a, pl.parts, f.batch, stream);
-    }
-    if (lpc == 4) return launch_bwd<T, 4, 1, false>(a, pl.parts, f.batch, stream);
-    if (lpc == 8) return launch_bwd<T, 8, 1, false>(a, pl.parts, f.batch, stream);
-    if (lpc == 16) return launch_bwd<T, 16, 1, false>(a, pl.parts, f.batch, stream);
-    if (r == 1) return launch_bwd<T, 32, 1, false>(a, pl.parts, f.batch, stream);
-    return launch_bwd<T, 32, 2, false>(a, pl.parts, f.batch, stream);
+    return launch_any<T>(ssd, pl.lpc, pl.r, a, pl.parts, f.batch, stream);
 }
 
 }  // namespace

@@ -286,7 +286,7 @@ def test_backward_argument_errors():
     assert call(s, dA=None) == _lib.SSM_ERR_NULL
     assert call(s, dB=(15 << 12) + 8) == _lib.SSM_ERR_ALIGN
     n = lib.ssm_scan_bwd_workspace_size(ctypes.byref(s))
-    ckpt = 2 * (64 // 16) * 64 * 16 * 4   # the state every 16 steps
+    ckpt = 2 * (64 // 8) * 64 * 16 * 4   # the state every 8 steps (4 entries per lane)
     assert n >= ckpt and parts_extra(n - ckpt, 2 * 64, 16) is not None
 
 
