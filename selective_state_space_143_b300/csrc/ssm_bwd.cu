@@ -165,10 +165,13 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
     constexpr bool PRECISE = sizeof(T) == 4;
     constexpr int CPB = kBwdThreads / LPC;
     constexpr int NP = LPC * R;                    // padded state width
+    // row stride of the dB/dC terms: an odd multiple of LPC, so that the channels of a
+    // warp store to distinct banks
+    constexpr int SNP = NP + (R > 1 ? LPC : 0);
     constexpr int SPL = (kSeg + LPC - 1) / LPC;    // steps per lane in the per-step pass
-    extern __shared__ float s_acc[];               // [2][kSeg][CPB][NP]: dB and dC terms
+    extern __shared__ float s_acc[];               // [2][kSeg][CPB][SNP]: dB and dC terms
     float* s_dB = s_acc;
-    float* s_dC = s_acc + kSeg * CPB * NP;
+    float* s_dC = s_acc + kSeg * CPB * SNP;
     const int tid = threadIdx.x;
     const int lane = tid % LPC;
     const int cc = tid / LPC;  // channel within the block
@@ -392,8 +395,8 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
                     dxp = fmaf(g[r] * de, Bv, dxp);
                     ddp = fmaf(g[r], fmaf(av * Aval(r), hp, Bv * xv), ddp);
                     dA_acc[r] = fmaf(g[r] * av * de, hp, dA_acc[r]);
-                    s_dB[(j * CPB + cc) * NP + r * LPC + lane] = g[r] * de * xv;
-                    s_dC[(j * CPB + cc) * NP + r * LPC + lane] = dy * hs[j][r];
+                    s_dB[(j * CPB + cc) * SNP + r * LPC + lane] = g[r] * de * xv;
+                    s_dC[(j * CPB + cc) * SNP + r * LPC + lane] = dy * hs[j][r];
                     g[r] *= av;  // dL/dh_{t-1}
                 }
                 // three independent reductions over the channel's lanes
@@ -423,8 +426,8 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
                     float sb = 0.0f, sc = 0.0f;
                     const int cmax = (int)min((int64_t)CPB, c_end - c_begin);
                     for (int q = 0; q < cmax; ++q) {
-                        sb += s_dB[(j * CPB + q) * NP + n];
-                        sc += s_dC[(j * CPB + q) * NP + n];
+                        sb += s_dB[(j * CPB + q) * SNP + n];
+                        sc += s_dC[(j * CPB + q) * SNP + n];
                     }
                     const int64_t o = bc(t0 + j) + n;
                     atomicAdd(&a.dB[o], sb);
@@ -458,7 +461,7 @@ template <typename T, int LPC, int R, bool SSD>
 cudaError_t launch_bwd(const BwdArgs<T>& a, int parts, int64_t batch, cudaStream_t stream) {
     constexpr int kSeg = R <= 2 ? 16 : R == 4 ? 8 : 4;  // as bwd_plan
     constexpr int CPB = kBwdThreads / LPC;
-    constexpr size_t kSmem = sizeof(float) * 2 * kSeg * CPB * LPC * R;
+    constexpr size_t kSmem = sizeof(float) * 2 * kSeg * CPB * (LPC * R + (R > 1 ? LPC : 0));
     BwdArgs<T> k = a;
     k.tiles_per_group = (int)((a.cpg + CPB - 1) / CPB);
     if (k.nseg != (int)((a.L + kSeg - 1) / kSeg))
