@@ -259,8 +259,8 @@ int ssm_step_conv(const void* x, const void* dt, const float* A, const void* B, 
  * dA, dB, dC, dD and ddt_bias (and, in SSD mode, ddt) are sums over channels and batch:
  * the call zeroes them first.  No output may overlap an input or another output.
  * Scratch: ssm_scan_bwd_workspace_size(shape) bytes: the state every 8 steps in diagonal
- * mode (16 for dstate 8 or less), every 16 in SSD mode (8 or 4 for dstate above 64 or
- * 128); with few channels the sequence is also cut into up to 16 time parts, each with
+ * mode (16 for dstate 8 or less), every 16 in SSD mode (4 for dstate above 64); with few
+ * channels the sequence is also cut into up to 16 time parts, each with
  * a local end state, a local adjoint and a Delta sum.  Workspace NULL/0 draws it from
  * the stream-ordered allocator, as ssm_scan_fwd does.
  * The sums over channels use floating-point atomics, so dA, dB, dC, dD and ddt_bias (and

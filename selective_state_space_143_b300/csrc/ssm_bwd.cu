@@ -64,7 +64,8 @@ BwdPlan bwd_plan(const ScanArgs& a) {
         const char* e = getenv("SSM_BWD_PARTS");
         return e ? atoi(e) : 0;
     }();
-    // SSM_BWD_LPC (4, 8, 16 or 32): lanes per channel in diagonal mode (tuning knob)
+    // SSM_BWD_LPC (4, 8, 16 or 32): lanes per channel (tuning knob; entries per lane follow,
+// at most 4, or 8 with 16 or more lanes)
     static const int knob_lpc = [] {
         const char* e = getenv("SSM_BWD_LPC");
         return e ? atoi(e) : 0;
@@ -80,10 +81,16 @@ BwdPlan bwd_plan(const ScanArgs& a) {
         p.r = 1;
         while (p.r * p.lpc < a.dstate) p.r *= 2;
     }
-    if (a.headdim == 1 && a.dstate <= 64 && (knob_lpc == 4 || knob_lpc == 8 || knob_lpc == 16 || knob_lpc == 32)) {
+    if (a.dstate > 64 && a.dstate <= 128) {
+        // SSD widths: 16 lanes of 8 entries (one shuffle level and half the reductions
+        // per entry fewer than 32 x 4): c3 backward 96 ms against 150 ms
+        p.lpc = 16;
+        p.r = 8;
+    }
+    if (knob_lpc == 4 || knob_lpc == 8 || knob_lpc == 16 || knob_lpc == 32) {
         int r = 1;
         while (r * knob_lpc < a.dstate) r *= 2;
-        if (r <= 4) {
+        if (r <= (knob_lpc >= 16 ? 8 : 4)) {
             p.lpc = knob_lpc;
             p.r = r;
         }
@@ -500,6 +507,7 @@ cudaError_t launch_mode(int lpc, int r, const BwdArgs<T>& a, int parts, int64_t 
         case 161: return launch_bwd<T, 16, 1, SSD>(a, parts, batch, stream);
         case 162: return launch_bwd<T, 16, 2, SSD>(a, parts, batch, stream);
         case 164: return launch_bwd<T, 16, 4, SSD>(a, parts, batch, stream);
+        case 168: return launch_bwd<T, 16, 8, SSD>(a, parts, batch, stream);
         case 321: return launch_bwd<T, 32, 1, SSD>(a, parts, batch, stream);
         case 322: return launch_bwd<T, 32, 2, SSD>(a, parts, batch, stream);
         case 324: return launch_bwd<T, 32, 4, SSD>(a, parts, batch, stream);

@@ -268,15 +268,15 @@ def test_backward_argument_errors():
                 return p
         return None
 
-    # SSD mode: the state of every (head, p) channel every 8 steps at dstate 128, every 4
-    # at 256; with this many channels the sequence is not split into time parts
+    # SSD mode: the state of every (head, p) channel every 4 steps at dstate 128 and 256;
+    # with this many channels the sequence is not split into time parts
     ssd = _shape(mode=1, batch=16, nheads=64, headdim=64, dstate=128, chunk=64)
-    assert lib.ssm_scan_bwd_workspace_size(ctypes.byref(ssd)) == 16 * (64 // 8) * 64 * 64 * 128 * 4
+    assert lib.ssm_scan_bwd_workspace_size(ctypes.byref(ssd)) == 16 * (64 // 4) * 64 * 64 * 128 * 4
     ssd256 = _shape(mode=1, batch=16, nheads=64, headdim=64, dstate=256)
     assert lib.ssm_scan_bwd_workspace_size(ctypes.byref(ssd256)) == 16 * (64 // 4) * 64 * 64 * 256 * 4
     # few channels: the checkpoints plus the summaries of several time parts
     small = _shape(mode=1, nheads=8, headdim=64, dstate=128, chunk=64)
-    ckpt = 2 * (64 // 8) * 8 * 64 * 128 * 4
+    ckpt = 2 * (64 // 4) * 8 * 64 * 128 * 4
     n = lib.ssm_scan_bwd_workspace_size(ctypes.byref(small))
     assert n > ckpt and (parts_extra(n - ckpt, 2 * 8 * 64, 128) or 0) > 1
     assert call(small, dB=(15 << 12) + 8) == _lib.SSM_ERR_ALIGN
