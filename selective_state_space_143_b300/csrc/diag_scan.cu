@@ -268,19 +268,24 @@ __global__ void __launch_bounds__(32 * WARPS) diag_scan_kernel(const DiagKernelA
     const char* bc_off_B = a.B + (int64_t)group * a.N * E;
     const char* bc_off_C = a.C + (int64_t)group * a.N * E;
 
-    auto tile_rows = [&](int k) { return (int)min((int64_t)kTT, t_end - (t_begin + (int64_t)k * kTT)); };
+    // 32-bit tile arithmetic and 64-bit bases computed once (a segment holds < 2^31
+    // steps): byte offsets of the segment's first x and B/C rows, this pair's output column
+    const int seg_rows = (int)(t_end - t_begin);
+    const int chans = (int)(c_end - c_begin);  // channels of the group from c_begin
+    const int64_t row_base = (b * a.T + t_begin) * row_stride;
+    const int64_t bc_base = (b * a.T + t_begin) * bc_stride;
+    char* const out_base = a.out + row_base + cA * E;
+    auto tile_rows = [&](int k) { return min(kTT, seg_rows - k * kTT); };
     auto stage = [&](int k) { return stage0 + (k % kStages) * Cfg::kStageBytes; };
 
     auto issue_tile = [&](int k) {
         if (k < ntiles) {
             unsigned char* st = stage(k);
-            const int64_t t0 = t_begin + (int64_t)k * kTT;
             const int rows = tile_rows(k);
             for (int i = tid; i < kTT * Cfg::kRowChunks; i += NT) {
                 const int r = i / Cfg::kRowChunks, q = i % Cfg::kRowChunks;
-                const int64_t ch = c_begin + q * (16 / E);
-                const bool ok = r < rows && ch < c_end;
-                const int64_t off = ok ? ((b * a.T + t0 + r) * row_stride + ch * E) : 0;
+                const bool ok = r < rows && q * (16 / E) < chans;
+                const int64_t off = ok ? (row_base + (int64_t)(k * kTT + r) * row_stride + (c_begin * E + q * 16)) : 0;
                 cp_async16(st + r * Cfg::kRowBytes + q * 16, a.x + off, ok);
                 cp_async16(st + Cfg::kXBytes + r * Cfg::kRowBytes + q * 16, a.dt + off, ok);
                 if (GATE && !STATE_ONLY)
@@ -289,7 +294,7 @@ __global__ void __launch_bounds__(32 * WARPS) diag_scan_kernel(const DiagKernelA
             for (int i = tid; i < kTT * Cfg::kBCRowChunks; i += NT) {
                 const int r = i / Cfg::kBCRowChunks, q = i % Cfg::kBCRowChunks;
                 const bool ok = r < rows && q * (16 / E) < a.N;
-                const int64_t off = ok ? ((b * a.T + t0 + r) * bc_stride + q * 16) : 0;
+                const int64_t off = ok ? (bc_base + (int64_t)(k * kTT + r) * bc_stride + q * 16) : 0;
                 unsigned char* dB = st + 3 * Cfg::kXBytes + r * Cfg::kBCRowBytes + q * 16;
                 cp_async16(dB, bc_off_B + off, ok);
                 if (!STATE_ONLY) cp_async16(dB + Cfg::kBCBytes, bc_off_C + off, ok);
@@ -358,8 +363,7 @@ __global__ void __launch_bounds__(32 * WARPS) diag_scan_kernel(const DiagKernelA
                                : load_pair<T>(st + r * Cfg::kRowBytes + 2 * pp * E);
         y = __ffma2_rn(d2, xv, y);
         if (GATE) y = __fmul2_rn(y, silu_pair<PRECISE>(load_pair<T>(st + 2 * Cfg::kXBytes + r * Cfg::kRowBytes + 2 * pp * E)));
-        const int64_t t = t_begin + (int64_t)k * kTT + r;
-        store_pair<T>(a.out + (b * a.T + t) * row_stride + cA * E, y);
+        store_pair<T>(out_base + (int64_t)(k * kTT + r) * row_stride, y);
     };
 
     // The output pass may start while the state-only pass is finishing (programmatic
