@@ -218,7 +218,7 @@ def kernel_roofline(kt, nbytes, calls, peak_gbs, peak_kind, whole):
 # kernel source as it stands: {(bench mode, workload, kernel name): bytes}.  Anything
 # not listed (no capture of the current kernel) reports null.
 NCU_TRAFFIC = {
-    ("scan", "c1", "diag_scan_kernel (output pass)"): 26_592_000 + 0,
+    ("scan", "c1", "diag_scan_kernel (output pass)"): 26_591_488 + 768,
     ("decode", "c1/8192", "ssm_step_kernel"): 294_216_448 + 221_896_960,
     ("backward", "c1", "scan_bwd_kernel"): 43_649_792 + 37_010_432,
 }
