@@ -31,7 +31,9 @@
 //    sum of Delta; the output pass folds those summaries into the segment's initial
 //    state, h <- exp(A sum Delta_j) h + H_j, which is the affine combine
 //    (a1, b1) o (a2, b2) = (a1 a2, a2 b1 + b2) of the parallel-scan formulation
-//    ("引言：Attention的天花板" article, 硬件感知算法).
+//    ("引言：Attention的天花板" article, 硬件感知算法).  The output pass is launched as a
+//    programmatic dependent of the state-only pass, so its blocks stage their first tiles
+//    while that pass finishes.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 

@@ -15,11 +15,16 @@
 // shared by the head's channels (Mamba-2 explainer, 第二步: a scalar A per head), so
 // dA, ddt, dD and ddt_bias of a head are sums over its channels (and, for dA, over n).
 //
-// Design: LPC lanes of a warp share one channel, each lane R state entries (N up to 64
-// in diagonal mode, 256 in SSD mode; segments shorten as R grows so that a segment's
-// recomputed states stay in registers).  A forward sweep stores the state entering every
-// segment of kSeg steps (the only scratch); the reverse sweep walks the segments backwards, recomputes the segment's
-// states into registers from its checkpoint and runs the adjoint recurrence over them.
+// Design: LPC lanes of a warp share one channel, each lane R state entries (diagonal
+// mode: 4 entries per lane; SSD mode: 8 per lane for dstate above 64; checkpoint
+// segments shorten as R grows so that a segment's recomputed states stay in registers).
+// A forward sweep stores the state entering every segment of kSeg steps; the reverse
+// sweep walks the segments backwards, recomputes each segment's states into registers
+// from its checkpoint and runs the adjoint recurrence over them.  With few channels the
+// sequence is also cut into time parts: a summary pass gives every part its local end
+// state, its local adjoint and its sum of Delta, and the main pass over each part folds
+// the earlier parts' states and the later parts' adjoints into its entering state and
+// adjoint (see the kernel).
 // The per-step scalars of a channel are computed once per segment, spread over its
 // lanes, and shuffled to the sweeps; sums over n use shuffles inside the LPC lanes; the
 // dB and dC terms of the block's channels (one group) go to shared memory and are summed
