@@ -7,6 +7,7 @@ with the CUDA runtime linked statically, so the library loads without a GPU.
 from __future__ import annotations
 
 import argparse
+import concurrent.futures
 import os
 import shutil
 import subprocess
@@ -54,15 +55,20 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
         return OUT
     os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
-    objs = []
+    objs, cmds = [], []
     for src in sources():
         obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [cc, *ARCH, *FLAGS, *(extra or []), "-c", src, "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
             print(" ".join(cmd), flush=True)
-        subprocess.run(cmd, check=True)
+        cmds.append(cmd)
         objs.append(obj)
+    # the translation units are independent: compile them concurrently
+    workers = max(1, min(len(cmds), os.cpu_count() or 1))
+    with concurrent.futures.ThreadPoolExecutor(workers) as pool:
+        for f in [pool.submit(subprocess.run, c, check=True) for c in cmds]:
+            f.result()
     tmp = out + ".tmp"
     cmd = [cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     subprocess.run(cmd, check=True)
