@@ -55,7 +55,10 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="c1", choices=sorted(DESCRIPTIONS))
+    ap.add_argument("--workload", default="c4", choices=sorted(DESCRIPTIONS),
+                    help="the timed workload (default c4, the largest by token-channels)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-workload block (c0..c4) of the forward scan line")
     ap.add_argument("--chunk", type=int, default=None, help="override the workload's chunk")
     ap.add_argument("--quick", action="store_true",
                     help="skip the clock soak, CPU baseline and end-to-end legs (profiling runs)")
@@ -213,22 +216,45 @@ def kernel_roofline(kt, nbytes, calls, peak_gbs, peak_kind, whole):
     return roof
 
 
-# DRAM traffic per launch of the dominant kernel (dram__bytes_read.sum +
-# dram__bytes_write.sum) from an ncu capture of the same bench command, taken with the
-# kernel source as it stands: {(bench mode, workload, kernel name): bytes}.  Anything
-# not listed (no capture of the current kernel) reports null.
-NCU_TRAFFIC = {
-    ("scan", "c1", "diag_scan_kernel (output pass)"): 26_591_488 + 768,
-    ("decode", "c1/8192", "ssm_step_kernel"): 294_216_448 + 221_896_960,
-    ("backward", "c1", "scan_bwd_kernel"): 43_649_792 + 37_010_432,
-}
+# DRAM traffic per launch of a kernel (dram__bytes_read.sum + dram__bytes_write.sum) comes
+# from profiles/dram_traffic.json: one entry per (bench mode, workload, kernel) with the
+# ncu command it was read from and a digest of the library sources at capture time.  An
+# entry counts only while the sources are unchanged; otherwise the traffic is null.
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
+CSRC = os.path.join(ROOT, "selective_state_space_143_b300", "csrc")
+
+
+def sources_digest() -> str:
+    """sha256 over the library's kernel sources (every file under csrc/, sorted)."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(CSRC)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(f.encode())
+            with open(os.path.join(CSRC, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()
+
+
+def traffic_entry(key):
+    try:
+        with open(TRAFFIC_FILE) as f:
+            entries = json.load(f)
+    except (OSError, ValueError):
+        return None, "no capture file"
+    digest = sources_digest()
+    for e in entries:
+        if (e.get("mode"), e.get("workload"), e.get("kernel")) == key:
+            if e.get("sources_sha256") != digest:
+                return None, "the kernel sources changed since the capture"
+            return int(e["bytes_per_launch"]), e.get("command", "")
+    return None, "no capture of this kernel and workload"
 
 
 def with_traffic(roof, key):
-    t = NCU_TRAFFIC.get(key + (roof.get("kernel"),))
+    t, how = traffic_entry(key + (roof.get("kernel"),))
     roof["traffic"] = t
-    roof["traffic_source"] = ("ncu capture of this command (bytes per launch)" if t is not None
-                              else "no capture of the current kernel")
+    roof["traffic_source"] = (f"ncu capture (bytes per launch): {how}" if t is not None else how)
     return roof
 
 
@@ -326,8 +352,10 @@ def max_over_ranks(dist, value: float) -> float:
 
 def oracle_sample(w, inp, seconds: float, max_reps: int = 1000, conv=None):
     """Time the oracle on whole channels of the workload until ``seconds`` pass.
-    Returns (token-channels processed, elapsed seconds, threads, description).  With
-    ``conv`` (weight, bias) each call also runs the oracle's convolution over the input."""
+    Returns (token-channels processed, elapsed seconds, threads, description, last) with
+    ``last`` = (selected flat channels, oracle out of the last call) for a parity check.
+    With ``conv`` (weight, bias) each call also runs the oracle's convolution over the
+    input."""
     import oracle
     nch = w.batch * w.d_inner
     per_channel = w.seqlen
@@ -336,27 +364,50 @@ def oracle_sample(w, inp, seconds: float, max_reps: int = 1000, conv=None):
         x = inp["x"]
         if conv is not None:
             x, _ = oracle.conv_silu(x, conv["weight"], conv["bias"])
-        oracle.scan(x, inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
-                    inp["dt_bias"], select=sel)
+        out, _ = oracle.scan(x, inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
+                             inp["dt_bias"], select=sel)
+        return out
 
-    # pick a channel block sized to ~1 s per call
+    # pick a channel block sized to ~1 s per call (at most the time budget)
     t0 = time.perf_counter()
-    probe = np.arange(min(nch, 64))
+    probe = np.arange(min(nch, 16))
     run(probe)
     dt_probe = max(time.perf_counter() - t0, 1e-4)
-    per_call = int(min(nch, max(64, probe.size * 1.0 / dt_probe)))
+    per_call = int(min(nch, max(16, probe.size * min(1.0, seconds) / dt_probe)))
     done, elapsed, reps = 0, 0.0, 0
     rng = np.random.default_rng(0)
-    while elapsed < seconds and reps < max_reps:
+    last = None
+    while (elapsed < seconds and reps < max_reps) or reps == 0:
         sel = np.sort(rng.choice(nch, per_call, replace=False)) if per_call < nch else np.arange(nch)
         t0 = time.perf_counter()
-        run(sel)
+        out = run(sel)
         elapsed += time.perf_counter() - t0
         done += sel.size * per_channel
         reps += 1
+        last = (sel, out)
     desc = (f"{reps} oracle calls of {per_call} whole channels (of {nch}) x L {w.seqlen}, "
             f"fp64, OpenMP over channels")
-    return done, elapsed, oracle.max_threads(), desc
+    return done, elapsed, oracle.max_threads(), desc, last
+
+
+def channel_view(a, mode):
+    """(b, T, H[, P]) -> (b*H*P, T), the oracle's flat channel order."""
+    if mode == "diag":
+        return a.transpose(0, 2, 1).reshape(-1, a.shape[1])
+    return a.transpose(0, 2, 3, 1).reshape(-1, a.shape[1])
+
+
+def parity_of(w, gpu_out, last):
+    """Error measures of the GPU output against the oracle on the sampled channels."""
+    import oracle
+    sel, ref = last
+    y = channel_view(gpu_out, w.mode)[sel]
+    r = channel_view(ref, w.mode)[sel]
+    rep = oracle.error_report(y, r)
+    tol = 1e-4 if w.dtype == "f32" else 2e-2
+    return {**{k: float(f"{v:.4g}") for k, v in rep.items()}, "tolerance": tol,
+            "pass": bool(rep["gated"] <= tol), "channels": int(len(sel)),
+            "what": "out on the oracle sample's channels, whole sequences"}
 
 
 # ---------------------------------------------------------------------------- arms
@@ -375,7 +426,7 @@ def run_reference(args, w):
     import oracle
     nch = w.batch * w.d_inner
     # per step: a bounded sample of whole channels (about 1 s of CPU work)
-    done_probe, el_probe, threads, _ = oracle_sample(w, inp, seconds=0.5, max_reps=1)
+    done_probe, el_probe, threads, _, _ = oracle_sample(w, inp, seconds=0.5, max_reps=1)
     per_sec = done_probe / el_probe / w.seqlen  # channels per second
     per_step = int(max(1, min(nch, per_sec * 1.0)))
     rng = np.random.default_rng(1)
@@ -407,14 +458,14 @@ def run_reference(args, w):
     return 0
 
 
-def run_ours(args, w):
+def measure_forward(args, w, dev, dist, rank, world, K, warmup, headline, cpu_seconds):
+    """Time ssm_scan_fwd on workload ``w``: K steps after ``warmup``, L2 flushed before
+    each; the library's per-kernel event times from a second pass; roofline of the
+    dominant kernel and of the whole call.  With ``headline`` also the clock record
+    during a load soak and the end-to-end leg.  On rank 0 the oracle baseline on a
+    bounded sample, and the parity of the GPU output on that sample."""
     import selective_state_space_143_b300 as ssm
-    dist, world, rank, local = dist_setup()
-    if not torch.cuda.is_available():
-        raise SystemExit("bench.py needs a CUDA device (there is no CPU path)")
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    chunk = w.chunk if args.chunk is None else args.chunk
+    chunk = w.chunk if args.chunk is None or not headline else args.chunk
     inp = host_inputs(w)
     d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
     out = torch.empty_like(d["x"])
@@ -422,7 +473,7 @@ def run_ours(args, w):
     fs = torch.empty(st_shape, device=dev, dtype=torch.float32) if w.final_state else None
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    conv = {}
+    conv, cp = {}, None
     if args.conv:
         from selective_state_space_143_b300.inputs import conv_params
         cp = conv_params(w.d_inner, 4, seed=w.seed)
@@ -432,22 +483,22 @@ def run_ours(args, w):
         ssm.scan_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["z"], d["dt_bias"],
                      out=out, final_state=fs, chunk=chunk, stream=stream, **conv)
 
-    for _ in range(max(args.warmup, 3)):
+    for _ in range(max(warmup, 3)):
         flush.zero_()
         step()
     torch.cuda.synchronize()
 
-    clocks = ClockSampler(local)
-    if not args.quick:
+    clocks = ClockSampler(torch.cuda.current_device())
+    soak = headline and not args.quick
+    if soak:
         clocks.start()
         # keep the GPU busy for about a second so that the clock samples see load
         t_end = time.perf_counter() + 1.0
         while time.perf_counter() < t_end:
-            for _ in range(50):
+            for _ in range(20):
                 step()
             torch.cuda.synchronize()
 
-    K = args.steps
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     barrier(dist)
@@ -465,11 +516,10 @@ def run_ours(args, w):
     launches = ssm.launch_count() - n0
     kt = kernel_times(ssm, K, lambda i: step(), flush)
     barrier(dist)
-    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
     ms_step = max_over_ranks(dist, sum(ms) / K)
-    clk = clocks.stop() if not args.quick else {"sm_mhz": None, "sm_max_mhz": None,
-                                               "reasons": ["not sampled (--quick)"]}
-
+    clk = clocks.stop() if soak else {"sm_mhz": None, "sm_max_mhz": None,
+                                     "reasons": ["not sampled (--quick)"]}
     units = w.token_channels * world
     value = units / (ms_step * 1e-3) / 1e9
 
@@ -482,27 +532,29 @@ def run_ours(args, w):
              "what": "all kernels of one ssm_scan_fwd call"}
     roof = kernel_roofline(kt, nbytes, K, peaks["hbm_gbs"], peak_kind, whole)
     roof = with_traffic(roof, ("conv" if args.conv else "scan", w.name))
+    sm_mhz = float(peaks.get("sm_max_mhz", 2032.0))
     if w.mode == "ssd":
         fl = algorithmic_flops(w)
         roof["tensor_tflops"] = fl / (ms_step * 1e-3) / 1e12
         roof["tensor_frac"] = roof["tensor_tflops"] / peaks["bf16_tflops"]
+        roof["tensor_note"] = ("algorithmic FLOPs of the chunk form over the whole call's time, "
+                               "against the measured bf16 dense peak")
     else:
         # The diagonal scan needs one exponential per state entry and step; B300's SFU
         # retires 32 ex2 per clock per SM (measured), so its ceiling is
-        # 148 x 32 x SM clock.
-        sm_mhz = float(peaks.get("sm_max_mhz", 2032.0))
-        sfu_peak = 148 * 32 * sm_mhz * 1e6
+        # SMs x 32 x SM clock.
+        nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+        sfu_peak = nsm * 32 * sm_mhz * 1e6
         exps = float(w.token_channels * w.dstate)
         t_sfu = roof.get("kernel_avg_us", ms_step * 1e3) * 1e-6
         roof["sfu"] = {"achieved": exps / t_sfu, "peak": sfu_peak, "unit": "exp/s",
                        "frac": exps / t_sfu / sfu_peak,
-                       "note": "one ex2 per state entry and step in the output pass; "
-                               "peak = 148 SMs x 32/clk x max SM clock"}
+                       "note": f"one ex2 per state entry and step in the output pass; peak = "
+                               f"{nsm} SMs x 32/clk x max SM clock"}
 
     # ---- end to end through the public API from pinned host buffers
     e2e = None
-    cpu = None
-    if not args.quick:
+    if headline and not args.quick:
         specs = {"out": (tuple(out.shape), out.dtype)}
         if fs is not None:
             specs["final_state"] = (tuple(fs.shape), torch.float32)
@@ -515,24 +567,74 @@ def run_ours(args, w):
         e2e_ms, h2d, d2h = pipelined_e2e(dev, inp, run, specs, K, dist)
         e2e = {"value": units / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "how": E2E_NOTE}
-        if rank == 0:
-            done, el, threads, desc = oracle_sample(w, inp, args.cpu_seconds,
-                                                    conv=cp if args.conv else None)
-            cpu = {"value": done / el / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
-                   "sample": desc, "seconds": el}
 
+    cpu = parity = None
+    if rank == 0 and not args.quick:
+        done, el, threads, desc, last = oracle_sample(w, inp, cpu_seconds,
+                                                      conv=cp if args.conv else None)
+        cpu = {"value": done / el / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": desc, "seconds": el}
+        step()
+        torch.cuda.synchronize()
+        parity = parity_of(w, out.float().cpu().numpy(), last)
+    res = {"value": value, "ms_per_step": ms_step, "launches": int(launches), "roofline": roof,
+           "cpu_baseline": cpu, "parity": parity, "e2e": e2e, "clocks": clk, "chunk": chunk}
+    del d, out, fs, flush
+    torch.cuda.empty_cache()
+    return res
+
+
+def config_summary(w, r):
+    roof = r["roofline"]
+    item = {"workload": f"{w.name}: {DESCRIPTIONS[w.name]}", "value": r["value"], "unit": UNIT,
+            "ms_per_step": r["ms_per_step"],
+            "kernel": roof.get("kernel"), "kernel_avg_us": roof.get("kernel_avg_us"),
+            "frac": roof.get("frac"), "achieved_gbs": roof.get("achieved"),
+            "traffic": roof.get("traffic"), "call_frac": roof.get("call", {}).get("frac"),
+            "cpu_baseline": r["cpu_baseline"], "parity": r["parity"],
+            "gpu_launches": r["launches"]}
+    if "tensor_frac" in roof:
+        item["tensor_frac"] = roof["tensor_frac"]
+    if "sfu" in roof:
+        item["sfu_frac"] = roof["sfu"]["frac"]
+    return item
+
+
+def run_ours(args, w):
+    from selective_state_space_143_b300.inputs import WORKLOADS
+    dist, world, rank, local = dist_setup()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (there is no CPU path)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    head = measure_forward(args, w, dev, dist, rank, world, args.steps, args.warmup, True,
+                           args.cpu_seconds)
+    configs = None
+    if not args.no_configs and not args.quick and not args.conv:
+        configs = {}
+        for name in sorted(WORKLOADS):
+            if name == w.name:
+                configs[name] = config_summary(w, head)
+                continue
+            wn = WORKLOADS[name]
+            r = measure_forward(args, wn, dev, dist, rank, world, 10, 3, False, 3.0)
+            configs[name] = config_summary(wn, r)
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
-            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic",
             "config": {"workload": f"{w.name}: {DESCRIPTIONS[w.name]}" +
                                    (", width-4 causal conv1d + SiLU ahead of the scan" if args.conv else ""),
                        "l2": "flushed before every timed step (256 MB write)",
-                       "chunk": chunk, "parallelism": f"replicas x{world} (independent batches)"},
-            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
-            "gpu_launches": int(launches),
+                       "chunk": head["chunk"], "parallelism": f"replicas x{world} (independent batches)"},
+            "roofline": head["roofline"], "cpu_baseline": head["cpu_baseline"],
+            "parity": head["parity"], "e2e": head["e2e"], "clocks": head["clocks"],
+            "gpu_launches": head["launches"],
         }
+        if configs is not None:
+            line["configs"] = configs
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

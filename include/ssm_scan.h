@@ -106,7 +106,9 @@ int ssm_scan_fwd(const void* x, const void* dt, const float* A, const void* B, c
                  float* final_state, const ssm_shape* shape, ssm_stream_t stream);
 
 /* Bytes of device scratch the call needs for `shape` (0 when none; (size_t)-1 when the
- * shape is invalid).  Depends only on the shape. */
+ * shape is invalid).  Depends on the shape, the current device's SM count (the
+ * schedule fills the GPU; 148 is assumed when no device is visible) and the plan
+ * overrides of ssm_tuning_set. */
 size_t ssm_scan_workspace_size(const ssm_shape* shape);
 
 /*
@@ -316,6 +318,38 @@ int ssm_device_status(int clear, ssm_stream_t stream);
  * with ssm_device_status.
  */
 int ssm_selftest_bounded_wait(uint32_t max_checks, ssm_stream_t stream);
+
+/*
+ * Plan overrides for measurement sweeps (this has no counterpart in the pages: it
+ * selects among the library's own kernel schedules; results agree within rounding for
+ * every setting).  Process-wide, thread-safe; 0 restores the library's own choice.
+ * A setting changes the scratch size that the *_workspace_size queries report, so query
+ * after setting it.  Values out of a knob's range are ignored by the planner.
+ *   SSM_TUNE_DIAG_NPT       state entries per lane of the diagonal scan: 4 or 8
+ *   SSM_TUNE_SSD_CUDA_CORES 1: run SSD on the CUDA-core kernels (a cross-check of the
+ *                           tensor-core ones)
+ *   SSM_TUNE_BWD_PARTS      time parts of the backward pass, 1..16
+ *   SSM_TUNE_BWD_LPC        lanes per channel of the backward pass: 4, 8, 16 or 32
+ * ssm_tuning_set returns SSM_ERR_UNSUPPORTED for an unknown knob and SSM_ERR_SHAPE for a
+ * negative value; ssm_tuning_get returns the current setting (0 for an unknown knob).
+ */
+typedef enum {
+    SSM_TUNE_DIAG_NPT = 0,
+    SSM_TUNE_SSD_CUDA_CORES = 1,
+    SSM_TUNE_BWD_PARTS = 2,
+    SSM_TUNE_BWD_LPC = 3
+} ssm_tuning_knob;
+int ssm_tuning_set(int knob, int64_t value);
+int64_t ssm_tuning_get(int knob);
+
+/*
+ * Host-side fault injection for tests (this has no counterpart in the pages): the next
+ * `count` device-scratch allocations made by the entry points that allocate
+ * (ssm_scan_fwd, ssm_scan_fwd_state/_conv and ssm_scan_bwd with no workspace) report
+ * failure without allocating, so those calls return SSM_ERR_ALLOC with nothing queued.
+ * 0 clears pending failures.  Process-wide.
+ */
+void ssm_inject_alloc_failures(int count);
 
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char* ssm_strerror(int status);

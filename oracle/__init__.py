@@ -285,3 +285,21 @@ def max_rel_error(y, ref, floor_frac: float = 1e-2) -> float:
     denom = np.maximum(np.abs(ref), floor_frac * scale)
     denom = np.where(denom == 0, 1.0, denom)
     return float(np.max(np.abs(y - ref) / denom))
+
+
+def error_report(y, ref) -> dict:
+    """Every error measure recorded next to the gated one, for information:
+    ``gated`` (the measure the tolerances apply to, floor 1e-2), ``floor_1e-3`` (the same
+    with a floor of 1e-3 of the largest reference magnitude), ``unfloored``
+    (max_i |y_i - r_i| / |r_i| over the nonzero r_i) and ``normwise``
+    (max_i |y_i - r_i| / max_i |r_i|)."""
+    y = np.asarray(y, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    if ref.size == 0:
+        return {"gated": 0.0, "floor_1e-3": 0.0, "unfloored": 0.0, "normwise": 0.0}
+    diff = np.abs(y - ref)
+    nz = ref != 0
+    scale = float(np.max(np.abs(ref)))
+    return {"gated": max_rel_error(y, ref), "floor_1e-3": max_rel_error(y, ref, 1e-3),
+            "unfloored": float(np.max(diff[nz] / np.abs(ref[nz]))) if nz.any() else 0.0,
+            "normwise": float(np.max(diff) / scale) if scale > 0 else float(np.max(diff))}

@@ -31,7 +31,13 @@ EXPORTED = ("ssm_scan_fwd", "ssm_scan_fwd_ws", "ssm_scan_workspace_size", "ssm_s
             "ssm_scan_fwd_state", "ssm_step", "ssm_scan_fwd_conv", "ssm_scan_conv_workspace_size",
             "ssm_step_conv", "ssm_scan_bwd", "ssm_scan_bwd_workspace_size", "ssm_timing_enable",
             "ssm_timing_collect", "ssm_device_status", "ssm_selftest_bounded_wait", "ssm_strerror",
-            "ssm_kernel_launch_count", "ssm_abi_version")
+            "ssm_kernel_launch_count", "ssm_abi_version", "ssm_tuning_set", "ssm_tuning_get",
+            "ssm_inject_alloc_failures")
+
+SSM_TUNE_DIAG_NPT = 0
+SSM_TUNE_SSD_CUDA_CORES = 1
+SSM_TUNE_BWD_PARTS = 2
+SSM_TUNE_BWD_LPC = 3
 
 
 class ssm_shape(ctypes.Structure):
@@ -126,9 +132,43 @@ def load() -> ctypes.CDLL:
         lib.ssm_device_status.restype = ctypes.c_int
         lib.ssm_selftest_bounded_wait.argtypes = [ctypes.c_uint32, ctypes.c_void_p]
         lib.ssm_selftest_bounded_wait.restype = ctypes.c_int
+        lib.ssm_tuning_set.argtypes = [ctypes.c_int, ctypes.c_int64]
+        lib.ssm_tuning_set.restype = ctypes.c_int
+        lib.ssm_tuning_get.argtypes = [ctypes.c_int]
+        lib.ssm_tuning_get.restype = ctypes.c_int64
+        lib.ssm_inject_alloc_failures.argtypes = [ctypes.c_int]
+        lib.ssm_inject_alloc_failures.restype = None
         del fp
         _lib = lib
         return lib
+
+
+def tuning_set(knob: int, value: int) -> None:
+    """Set a plan override (ssm_tuning_set); 0 restores the library's own choice."""
+    rc = load().ssm_tuning_set(int(knob), int(value))
+    if rc != SSM_OK:
+        raise SsmError(rc, "ssm_tuning_set")
+
+
+def tuning_get(knob: int) -> int:
+    return int(load().ssm_tuning_get(int(knob)))
+
+
+class tuned:
+    """Context manager: ``with tuned(SSM_TUNE_BWD_PARTS, 8): ...`` sets a plan override
+    for the block and restores the previous setting afterwards."""
+
+    def __init__(self, knob: int, value: int):
+        self.knob, self.value, self.prev = knob, value, 0
+
+    def __enter__(self):
+        self.prev = tuning_get(self.knob)
+        tuning_set(self.knob, self.value)
+        return self
+
+    def __exit__(self, *exc):
+        tuning_set(self.knob, self.prev)
+        return False
 
 
 def strerror(status: int) -> str:

@@ -39,7 +39,6 @@
 
 #include <algorithm>
 #include <atomic>
-#include <cstdlib>
 
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
@@ -554,20 +553,17 @@ int pick_nk(int64_t N) {
     return 64;
 }
 
-// State entries per lane: SSM_DIAG_NPT (4 or 8) when set (tuning knob), else 8 when
+// State entries per lane: the SSM_TUNE_DIAG_NPT override (4 or 8) when set, else 8 when
 // the channels alone fill the GPU and 4 when the sequence has to be split.
 int npt_override() {
-    static const int v = [] {
-        const char* e = getenv("SSM_DIAG_NPT");
-        return e ? atoi(e) : 0;
-    }();
-    return v == 4 || v == 8 ? v : 0;
+    const int64_t v = tuning(0);
+    return v == 4 || v == 8 ? (int)v : 0;
 }
 
 Plan make_plan(const ScanArgs& a) {
     Plan p;
     p.NK = pick_nk(a.dstate);
-    const int64_t smsp = 148 * 4;  // B300 SM sub-partitions
+    const int64_t smsp = (int64_t)sm_count() * 4;  // SM sub-partitions
     auto fill = [&](int npt) {
         p.LPC = std::max(1, std::min(8, p.NK / npt));
         p.cpb = p.LPC == 1 ? 32 : 16;

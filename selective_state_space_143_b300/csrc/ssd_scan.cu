@@ -22,7 +22,6 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
-#include <cstdlib>
 
 #include "ssm_device.cuh"
 #include "ssd_tc.h"
@@ -403,15 +402,9 @@ __global__ void __launch_bounds__(kThreads) ssd_chunk_scan(const SsdArgs a) {
     }
 }
 
-// SSM_SSD_CUDA_CORES=1 keeps every shape on the CUDA-core kernels (a cross-check of the
-// tensor-core kernels; both compute the same chunk algebra).
-bool force_cuda_cores() {
-    static const bool v = [] {
-        const char* e = getenv("SSM_SSD_CUDA_CORES");
-        return e && e[0] == '1';
-    }();
-    return v;
-}
+// The SSM_TUNE_SSD_CUDA_CORES override (1) keeps every shape on the CUDA-core kernels (a
+// cross-check of the tensor-core kernels; both compute the same chunk algebra).
+bool force_cuda_cores() { return tuning(1) == 1; }
 
 struct SsdPlan {
     int64_t Q, nchunks;

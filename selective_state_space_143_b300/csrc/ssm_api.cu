@@ -67,6 +67,44 @@ void note_launch(const char* name, cudaStream_t stream, cudaEvent_t start) {
     g_timed.push_back({name, start, end});
 }
 
+// Plan overrides (ssm_tuning_set), one slot per ssm_tuning_knob.
+namespace {
+constexpr int kKnobs = 4;
+std::atomic<int64_t> g_tuning[kKnobs] = {};
+std::atomic<int> g_alloc_failures{0};
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices] = {};
+}  // namespace
+
+int64_t tuning(int knob) { return knob >= 0 && knob < kKnobs ? g_tuning[knob].load(std::memory_order_relaxed) : 0; }
+
+int sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        (void)cudaGetLastError();
+        return 148;
+    }
+    int n = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (n > 0) return n;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        (void)cudaGetLastError();
+        return 148;
+    }
+    g_sm_count[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+cudaError_t scratch_alloc(void** p, size_t bytes, cudaStream_t stream) {
+    int pending = g_alloc_failures.load(std::memory_order_relaxed);
+    while (pending > 0) {
+        if (g_alloc_failures.compare_exchange_weak(pending, pending - 1, std::memory_order_relaxed)) {
+            *p = nullptr;
+            return cudaErrorMemoryAllocation;
+        }
+    }
+    return cudaMallocAsync(p, bytes, stream);
+}
+
 namespace {
 
 constexpr int64_t kMaxGridYZ = 65535;
@@ -242,7 +280,7 @@ int run_allocating(const ScanArgs& a, int mode, cudaStream_t st) {
     const size_t need = workspace_for(a, mode);
     void* ws = nullptr;
     if (need > 0 && a.batch > 0) {
-        if (cudaMallocAsync(&ws, need, st) != cudaSuccess) {
+        if (scratch_alloc(&ws, need, st) != cudaSuccess) {
             (void)cudaGetLastError();
             return SSM_ERR_ALLOC;
         }
@@ -293,7 +331,20 @@ using namespace ssm;
 
 extern "C" {
 
-int ssm_abi_version(void) { return (1 << 16) | 4; }
+int ssm_abi_version(void) { return (1 << 16) | 5; }
+
+int ssm_tuning_set(int knob, int64_t value) {
+    if (knob < 0 || knob >= ssm::kKnobs) return SSM_ERR_UNSUPPORTED;
+    if (value < 0) return SSM_ERR_SHAPE;
+    ssm::g_tuning[knob].store(value, std::memory_order_relaxed);
+    return SSM_OK;
+}
+
+int64_t ssm_tuning_get(int knob) { return ssm::tuning(knob); }
+
+void ssm_inject_alloc_failures(int count) {
+    ssm::g_alloc_failures.store(count > 0 ? count : 0, std::memory_order_relaxed);
+}
 
 int ssm_device_status(int clear, ssm_stream_t stream) {
     int v = 0;
@@ -483,7 +534,7 @@ int ssm_scan_bwd(const void* x, const void* dt, const float* A, const void* B, c
     bool owned = false;
     if (need > 0 && !empty) {
         if (workspace == nullptr && workspace_bytes == 0) {
-            if (cudaMallocAsync(&ws, need, st) != cudaSuccess) {
+            if (scratch_alloc(&ws, need, st) != cudaSuccess) {
                 (void)cudaGetLastError();
                 return SSM_ERR_ALLOC;
             }

@@ -52,7 +52,7 @@ constexpr int kBwdThreads = 256;
 int bwd_lanes(int64_t N) { return N <= 4 ? 4 : N <= 8 ? 8 : N <= 16 ? 16 : 32; }
 int bwd_entries(int64_t N) { return N <= 32 ? 1 : N <= 64 ? 2 : N <= 128 ? 4 : 8; }
 
-// Time parts: SSM_BWD_PARTS when set (tuning knob).  Otherwise one part when the channels
+// Time parts: the SSM_TUNE_BWD_PARTS override when set.  Otherwise one part when the channels
 // give at least 8 warps per SM sub-partition (measured on B300: more parts only add the
 // summary pass), else enough parts for ~32 warps per sub-partition, at most 16 and at
 // least two checkpoint segments each (c1 backward: 1 part 1.15 ms, 4 parts 0.78 ms, 8-16
@@ -65,16 +65,10 @@ struct BwdPlan {
     size_t ckpt_bytes, h_off, q_off, d_off, total;
 };
 BwdPlan bwd_plan(const ScanArgs& a) {
-    static const int knob = [] {
-        const char* e = getenv("SSM_BWD_PARTS");
-        return e ? atoi(e) : 0;
-    }();
-    // SSM_BWD_LPC (4, 8, 16 or 32): lanes per channel (tuning knob; entries per lane follow,
-// at most 4, or 8 with 16 or more lanes)
-    static const int knob_lpc = [] {
-        const char* e = getenv("SSM_BWD_LPC");
-        return e ? atoi(e) : 0;
-    }();
+    const int64_t knob = tuning(2);
+    // the SSM_TUNE_BWD_LPC override (4, 8, 16 or 32): lanes per channel (entries per lane
+    // follow, at most 4, or 8 with 16 or more lanes)
+    const int64_t knob_lpc = tuning(3);
     BwdPlan p;
     p.lpc = bwd_lanes(a.dstate);
     p.r = bwd_entries(a.dstate);
@@ -96,14 +90,14 @@ BwdPlan bwd_plan(const ScanArgs& a) {
         int r = 1;
         while (r * knob_lpc < a.dstate) r *= 2;
         if (r <= (knob_lpc >= 16 ? 8 : 4)) {
-            p.lpc = knob_lpc;
+            p.lpc = (int)knob_lpc;
             p.r = r;
         }
     }
     p.seg = p.r <= 2 ? 16 : p.r == 4 ? 8 : 4;
     const int64_t seg = p.seg;
     p.nseg = (a.seqlen + seg - 1) / seg;
-    const int64_t smsp = 148 * 4;  // B300 SM sub-partitions
+    const int64_t smsp = (int64_t)sm_count() * 4;  // SM sub-partitions
     const int64_t warps = (int64_t)a.batch * a.nheads * a.headdim * p.lpc / 32;
     int64_t rule = 1;
     if (warps > 0 && warps < 8 * smsp)

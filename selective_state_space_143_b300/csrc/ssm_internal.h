@@ -87,4 +87,18 @@ cudaError_t bounded_wait_selftest_launch(uint32_t max_checks, cudaStream_t strea
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Streaming multiprocessors of the current device, read once per device and cached
+// (148 when no device is visible, so that workspace queries still answer on a host
+// without a GPU).  Schedules that size their grids to fill the GPU use this.
+int sm_count();
+
+// Plan overrides set through ssm_tuning_set (0 = the library's own choice).  Indexed by
+// the ssm_tuning_knob values of include/ssm_scan.h.
+int64_t tuning(int knob);
+
+// Stream-ordered scratch allocation for the entry points that allocate.  Reports
+// failure (and allocates nothing) while an injected failure is pending
+// (ssm_inject_alloc_failures).
+cudaError_t scratch_alloc(void** p, size_t bytes, cudaStream_t stream);
+
 }  // namespace ssm

@@ -24,3 +24,15 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def record_errors(name, reports):
+    """Print the error measures of a parity comparison ({quantity: oracle.error_report})
+    and, when SSM_PARITY_REPORT names a file, append them to it as one JSON line."""
+    import json
+    line = {"case": name, **{k: {m: float(f"{v:.4g}") for m, v in r.items()} for k, r in reports.items()}}
+    print(json.dumps(line))
+    path = os.environ.get("SSM_PARITY_REPORT")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(line) + "\n")

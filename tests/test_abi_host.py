@@ -1,12 +1,23 @@
 """Host-side checks of the C ABI that need no GPU: the library loads, exports every
 function include/ssm_scan.h declares, and rejects bad arguments with the documented
-status before touching the device."""
+status before touching the device.
+
+Many of these tests pass made-up device addresses that the host checks must reject
+before anything is launched.  They never run in a process that sees a GPU: where one
+is visible, this module is skipped and tests/test_host_checks_child.py runs it in a
+child process with CUDA_VISIBLE_DEVICES empty, so that a regression in a host check
+fails a test (SSM_ERR_CUDA instead of the expected status) rather than launching a
+kernel on invalid addresses."""
 import ctypes
 import os
 import re
 
 import pytest
 import torch
+
+pytestmark = pytest.mark.skipif(torch.cuda.is_available(),
+                                reason="made-up device addresses: run without a visible GPU "
+                                       "(tests/test_host_checks_child.py)")
 
 import selective_state_space_143_b300 as ssm
 from selective_state_space_143_b300 import _lib
@@ -296,3 +307,52 @@ def test_timing_collect_without_launches():
     assert lib.ssm_timing_collect(None, 0) == 0   # nothing launched, nothing recorded
     lib.ssm_timing_enable(0)
     assert _lib.timing_collect() == {}
+
+
+def test_noalloc_rejects_shapes_beyond_its_scratch():
+    # an SSD shape whose chunk states need far more than the 64 MiB fixed scratch
+    shape = _shape(mode=1, batch=1, seqlen=131072, nheads=32, headdim=64, dstate=256, chunk=256)
+    assert _ws(shape) > (64 << 20)
+    vp = ctypes.c_void_p
+    rc = _lib.load().ssm_scan_fwd_noalloc(vp(1 << 12), vp(2 << 12), vp(3 << 12), vp(4 << 12),
+                                          vp(5 << 12), None, None, None, vp(6 << 12), None,
+                                          ctypes.byref(shape), None)
+    assert rc == _lib.SSM_ERR_ALLOC
+
+
+def test_injected_allocation_failure_is_reported():
+    """A failing stream-ordered allocation (injected on the host) surfaces as
+    SSM_ERR_ALLOC with nothing queued, for the forward and the backward entry points."""
+    lib = _lib.load()
+    vp = ctypes.c_void_p
+    s = _shape(mode=1, nheads=8, headdim=64, dstate=128, chunk=64, seqlen=256)
+    assert _ws(s) > 0
+    lib.ssm_inject_alloc_failures(1)
+    try:
+        assert _call(s) == _lib.SSM_ERR_ALLOC
+    finally:
+        lib.ssm_inject_alloc_failures(0)
+    assert lib.ssm_scan_bwd_workspace_size(ctypes.byref(s)) > 0
+    ptrs = [vp((i + 1) << 12) for i in range(20)]
+    lib.ssm_inject_alloc_failures(1)
+    try:
+        assert lib.ssm_scan_bwd(*ptrs, ctypes.byref(s), None, 0, None) == _lib.SSM_ERR_ALLOC
+    finally:
+        lib.ssm_inject_alloc_failures(0)
+
+
+def test_tuning_knobs():
+    lib = _lib.load()
+    assert lib.ssm_tuning_set(99, 1) == _lib.SSM_ERR_UNSUPPORTED
+    assert lib.ssm_tuning_set(_lib.SSM_TUNE_BWD_PARTS, -1) == _lib.SSM_ERR_SHAPE
+    assert lib.ssm_tuning_get(99) == 0
+    s = _shape(mode=1, nheads=8, headdim=64, dstate=128, chunk=64)
+    default = lib.ssm_scan_bwd_workspace_size(ctypes.byref(s))
+    with _lib.tuned(_lib.SSM_TUNE_BWD_PARTS, 1):
+        assert _lib.tuning_get(_lib.SSM_TUNE_BWD_PARTS) == 1
+        one_part = lib.ssm_scan_bwd_workspace_size(ctypes.byref(s))
+    assert _lib.tuning_get(_lib.SSM_TUNE_BWD_PARTS) == 0
+    # one time part needs only the checkpoints; the default plan splits this few-channel
+    # shape into several parts, each with its own summaries
+    assert one_part < default
+    assert lib.ssm_scan_bwd_workspace_size(ctypes.byref(s)) == default

@@ -380,6 +380,21 @@ def _fp32_recurrence(arr, diag):
     return (y[..., 0] if diag else y), h.reshape((b, H, N) if diag else (b, H, P, N))
 
 
+def test_error_report_definitions():
+    """The informational measures, on values worked by hand."""
+    ref = np.array([10.0, -0.5, 0.0, 0.02])
+    y = np.array([10.01, -0.5, 0.001, 0.021])
+    r = oracle.error_report(y, ref)
+    # gated: floors at 0.1 (1% of 10): errors 0.01/10, 0, 0.001/0.1, 0.001/0.1
+    assert abs(r["gated"] - 0.01) < 1e-12
+    # floor 1e-3 of 10 = 0.01: 0.001/0.01 (the zero), 0.001/0.02
+    assert abs(r["floor_1e-3"] - 0.1) < 1e-12
+    # unfloored over nonzero references: 0.001/0.02 = 0.05 (the zero is left out)
+    assert abs(r["unfloored"] - 0.05) < 1e-12
+    # normwise: max error 0.01 over max |ref| 10
+    assert abs(r["normwise"] - 0.001) < 1e-12
+
+
 @pytest.mark.parametrize("mode", ["diag", "ssd"])
 def test_error_measure_leaves_margin_for_exact_fp32(mode):
     """The fp32 bound (1e-4) must be met with margin by an exactly rounded fp32
