@@ -16,7 +16,9 @@ What it computes (cited by page title and section):
   * "论文解读：Mamba — 线性时间的序列建模革命", 五 Mamba块架构: the SiLU(z) gate
 with Abar = exp(Delta A), Bbar = Delta B.  ``scan(..., chunk=Q)`` evaluates the
 same operator through its semiseparable block form (Mamba-2 explainer, 第二步 and
-关键技术点 1) and serves to pin chunk-size invariance.
+关键技术点 1) and serves to pin chunk-size invariance.  ``scan_complex`` is the
+complex-valued, rotating state update read for Mamba-3 ("状态空间模型与 Mamba：不用注意力
+读取长序列的方法", the Mamba-3 paragraph; "基础知识：Mamba 与混合 SSM 架构", section 6).
 """
 from __future__ import annotations
 
@@ -66,6 +68,8 @@ class OracleLib:
         lib.oracle_scan_bwd.restype = ctypes.c_int
         lib.oracle_conv_silu.argtypes = [i64] * 4 + [dp] * 6
         lib.oracle_conv_silu.restype = ctypes.c_int
+        lib.oracle_scan_complex.argtypes = [i64] * 5 + [dp] * 11 + [ip, i64, ctypes.c_int]
+        lib.oracle_scan_complex.restype = ctypes.c_int
         self.lib = lib
         self.path = path
 
@@ -77,6 +81,9 @@ class OracleLib:
 
     def scan_bwd(self, *args, **kw):
         return _scan_bwd(self.lib, *args, **kw)
+
+    def scan_complex(self, *args, **kw):
+        return _scan_complex(self.lib, *args, **kw)
 
 
 def _load():
@@ -303,3 +310,50 @@ def error_report(y, ref) -> dict:
     return {"gated": max_rel_error(y, ref), "floor_1e-3": max_rel_error(y, ref, 1e-3),
             "unfloored": float(np.max(diff[nz] / np.abs(ref[nz]))) if nz.any() else 0.0,
             "normwise": float(np.max(diff) / scale) if scale > 0 else float(np.max(diff))}
+
+
+def scan_complex(*args, **kw):
+    """Run the oracle's complex diagonal scan; see ``_scan_complex``."""
+    return _scan_complex(_load(), *args, **kw)
+
+
+def _scan_complex(lib, x, dt, A, B, C, D=None, z=None, dt_bias=None, initial_state=None,
+                  select=None, nthreads: int = 0):
+    """Complex diagonal scan (the rotating state update read for Mamba-3), fp64.
+
+    x, z, dt (b, T, D); A (D, N, 2); B, C (b, T, N, 2) or (b, T, G, N, 2), each complex
+    number an (re, im) pair; D, dt_bias (D,); initial_state (b, D, N, 2).  Returns
+    ``(out (b, T, D), final_state (b, D, N, 2))``; ``select`` as for ``scan`` with flat
+    channels b*D + c (unselected channels stay NaN).
+    """
+    x, dt, A, B, C = (_f64(v) for v in (x, dt, A, B, C))
+    D, z, dt_bias, initial_state = (_f64(v) for v in (D, z, dt_bias, initial_state))
+    if x.ndim != 3 or A.ndim != 3 or A.shape[2] != 2:
+        raise ValueError("complex scan expects x (b, T, D) and A (D, N, 2)")
+    b, T, H = x.shape
+    N = A.shape[1]
+    if A.shape[0] != H:
+        raise ValueError("A must be (d_inner, dstate, 2)")
+    if B.ndim == 4:
+        G = 1
+    elif B.ndim == 5:
+        G = B.shape[2]
+    else:
+        raise ValueError("B must be (b, T, N, 2) or (b, T, G, N, 2)")
+    if B.shape[-2:] != (N, 2) or C.shape != B.shape or B.shape[:2] != (b, T):
+        raise ValueError("B and C must be (b, T[, G], N, 2)")
+    if dt.shape != x.shape or (z is not None and z.shape != x.shape):
+        raise ValueError("dt and z must have x's shape")
+    if initial_state is not None and initial_state.size != b * H * N * 2:
+        raise ValueError("initial_state must be (b, D, N, 2)")
+    out = np.full(x.shape, np.nan)
+    fs = np.full((b, H, N, 2), np.nan)
+    sel = None if select is None else np.ascontiguousarray(np.asarray(select, dtype=np.int64))
+    selp = sel.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)) if sel is not None else \
+        ctypes.POINTER(ctypes.c_int64)()
+    rc = lib.oracle_scan_complex(b, T, H, N, G, *(_ptr(v) for v in (x, dt, A, B, C, D, z, dt_bias,
+                                                                     initial_state, out, fs)),
+                                 selp, 0 if sel is None else sel.size, int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle returned status {rc}")
+    return out, fs

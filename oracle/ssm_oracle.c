@@ -48,8 +48,11 @@
  * Parity status: pinned (brute-force semiseparable matrix, closed-form LTI responses,
  * masked linear attention at A = 0, hand-worked golden values, invariants; the
  * convolution against numpy's convolution; the backward pass against central finite
- * differences of the forward).
+ * differences of the forward; the complex scan against the real scan with zero
+ * imaginary parts, its own materialised matrix, closed-form damped-oscillator
+ * responses and pure-rotation invariants).
  */
+#include <complex.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -423,6 +426,99 @@ int oracle_scan_bwd(int mode, int64_t batch, int64_t seqlen, int64_t nheads, int
     free(hist);
     free(g);
     return 0;
+}
+
+/*
+ * Complex diagonal scan: the state update of Mamba-3 read as a complex-valued, rotating
+ * recurrence.  Sources: [SSM/Mamba primer] "状态空间模型与 Mamba：不用注意力读取长序列的方法",
+ * the paragraph on Mamba-3's oscillatory dynamics (an input-dependent rotation in the
+ * state update, read as underdamped oscillation); [Mamba / hybrid overview] section 6
+ * Mamba-3：新的推理优先视角 (keywords: complex-valued state update, SSM discretization).
+ * The pages print no formula.  Reading (listed in the design notes): A[c,n] is complex,
+ * Re A the decay rate and Im A the angular frequency; the same discretisation as the
+ * real scan, Abar = exp(Delta A) = e^{Delta Re A} (cos(Delta Im A) + i sin(Delta Im A)),
+ * so the rotation angle Delta_t Im A follows the input through Delta_t; B and C are
+ * complex; the output reads the real part of the plain (unconjugated) product:
+ *   h_t[n] = exp(Delta_t A[c,n]) h_{t-1}[n] + Delta_t B_t[n] x_t          (complex)
+ *   y_t    = (Re(sum_n C_t[n] h_t[n]) + D x_t) * SiLU(z_t)
+ * Layouts (complex numbers as (re, im) pairs of doubles):
+ *   x, z, out, dt (batch, seqlen, nheads); A (nheads, dstate, 2); B, C (batch, seqlen,
+ *   ngroups, dstate, 2); D, dt_bias (nheads,) nullable; initial_state, final_state
+ *   (batch, nheads, dstate, 2) nullable.  sel/nsel: flat channels b*nheads + c.
+ */
+static void oracle_channel_complex(int64_t T, int64_t H, int64_t N, int64_t G, int64_t b,
+                                   int64_t c, const double* x, const double* dt, const double* A,
+                                   const double* B, const double* C, const double* D,
+                                   const double* z, const double* dt_bias,
+                                   const double* initial_state, double* out, double* final_state,
+                                   double complex* state) {
+    const int64_t g = c / (H / G);
+    const int64_t sidx = (b * H + c) * N;
+    for (int64_t n = 0; n < N; ++n)
+        state[n] = initial_state ? initial_state[2 * (sidx + n)] + I * initial_state[2 * (sidx + n) + 1] : 0.0;
+    for (int64_t t = 0; t < T; ++t) {
+        const int64_t bt = b * T + t;
+        const double delta = oracle_softplus(dt[bt * H + c] + (dt_bias ? dt_bias[c] : 0.0));
+        const double xv = x[bt * H + c];
+        const double* Bt = B + 2 * (bt * G + g) * N;
+        const double* Ct = C + 2 * (bt * G + g) * N;
+        double complex acc = 0.0;
+        for (int64_t n = 0; n < N; ++n) {
+            const double complex an = A[2 * (c * N + n)] + I * A[2 * (c * N + n) + 1];
+            const double complex bn = Bt[2 * n] + I * Bt[2 * n + 1];
+            const double complex cn = Ct[2 * n] + I * Ct[2 * n + 1];
+            state[n] = cexp(delta * an) * state[n] + delta * bn * xv;
+            acc += cn * state[n];
+        }
+        double y = creal(acc);
+        if (D) y += D[c] * xv;
+        if (z) y *= oracle_silu(z[bt * H + c]);
+        out[bt * H + c] = y;
+    }
+    if (final_state)
+        for (int64_t n = 0; n < N; ++n) {
+            final_state[2 * (sidx + n)] = creal(state[n]);
+            final_state[2 * (sidx + n) + 1] = cimag(state[n]);
+        }
+}
+
+int oracle_scan_complex(int64_t batch, int64_t seqlen, int64_t nheads, int64_t dstate,
+                        int64_t ngroups, const double* x, const double* dt, const double* A,
+                        const double* B, const double* C, const double* D, const double* z,
+                        const double* dt_bias, const double* initial_state, double* out,
+                        double* final_state, const int64_t* sel, int64_t nsel, int nthreads) {
+    if (!x || !dt || !A || !B || !C || !out) return 1;
+    if (batch < 0 || seqlen < 0 || nheads <= 0 || dstate <= 0 || ngroups <= 0 || nheads % ngroups) return 2;
+    const int64_t nchan = batch * nheads;
+    const int64_t count = sel ? nsel : nchan;
+    if (sel)
+        for (int64_t i = 0; i < nsel; ++i)
+            if (sel[i] < 0 || sel[i] >= nchan) return 2;
+    int failed = 0;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel
+#endif
+    {
+        double complex* state = (double complex*)malloc(sizeof(double complex) * (size_t)dstate);
+        if (!state) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            failed = 1;
+        }
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int64_t i = 0; i < count; ++i) {
+            if (!state) continue;
+            const int64_t ch = sel ? sel[i] : i;
+            oracle_channel_complex(seqlen, nheads, dstate, ngroups, ch / nheads, ch % nheads, x, dt,
+                                   A, B, C, D, z, dt_bias, initial_state, out, final_state, state);
+        }
+        free(state);
+    }
+    return failed ? 6 : 0;
 }
 
 int oracle_max_threads(void) {
