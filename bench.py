@@ -46,6 +46,10 @@ DESCRIPTIONS = {
           "1 group, chunk 256, D",
     "c4": "Mamba-2 SSD long sequence, bf16, batch 1 x L 131072, 32 heads x 64, N 256, 1 group, "
           "chunk 256, D, final_state",
+    "cx1": "complex diagonal A (the rotating state update read for Mamba-3) at c1's shape, bf16, "
+           "batch 8 x L 1024 x d_inner 512, N 16 complex, dt_bias, D, SiLU(z) gate",
+    "cx2": "complex diagonal A at c2's shape, bf16, batch 4 x L 8192 x d_inner 5120, N 16 complex, "
+           "dt_bias, D, SiLU(z) gate, final_state",
 }
 
 
@@ -84,11 +88,12 @@ def algorithmic_bytes(w) -> int:
     per_tok_ch = (2 + (1 if w.gate else 0)) * E  # x, out, z (dt below)
     nbytes = b * T * H * P * per_tok_ch
     nbytes += b * T * H * E                      # dt: per channel (diag) or per head (ssd)
-    nbytes += 2 * b * T * G * N * E              # B, C
-    nbytes += (H * N if w.mode == "diag" else H) * 4   # A
+    cpl = 2 if w.mode == "cdiag" else 1           # complex: (re, im) pairs
+    nbytes += 2 * b * T * G * N * E * cpl        # B, C
+    nbytes += (H * N * cpl if w.mode != "ssd" else H) * 4   # A
     nbytes += H * 4 * ((1 if w.d_skip != "none" else 0) + (1 if w.dt_bias else 0))
     if w.final_state:
-        nbytes += b * H * P * N * 4
+        nbytes += b * H * P * N * 4 * cpl
     return int(nbytes)
 
 
@@ -364,8 +369,9 @@ def oracle_sample(w, inp, seconds: float, max_reps: int = 1000, conv=None):
         x = inp["x"]
         if conv is not None:
             x, _ = oracle.conv_silu(x, conv["weight"], conv["bias"])
-        out, _ = oracle.scan(x, inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
-                             inp["dt_bias"], select=sel)
+        fn = oracle.scan_complex if w.mode == "cdiag" else oracle.scan
+        out, _ = fn(x, inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
+                    inp["dt_bias"], select=sel)
         return out
 
     # pick a channel block sized to ~1 s per call (at most the time budget)
@@ -392,7 +398,7 @@ def oracle_sample(w, inp, seconds: float, max_reps: int = 1000, conv=None):
 
 def channel_view(a, mode):
     """(b, T, H[, P]) -> (b*H*P, T), the oracle's flat channel order."""
-    if mode == "diag":
+    if mode != "ssd":
         return a.transpose(0, 2, 1).reshape(-1, a.shape[1])
     return a.transpose(0, 2, 3, 1).reshape(-1, a.shape[1])
 
@@ -434,8 +440,9 @@ def run_reference(args, w):
     for i in range(args.warmup + args.steps):
         sel = np.sort(rng.choice(nch, per_step, replace=False))
         t0 = time.perf_counter()
-        oracle.scan(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
-                    inp["dt_bias"], select=sel)
+        fn = oracle.scan_complex if w.mode == "cdiag" else oracle.scan
+        fn(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"], inp["dt_bias"],
+           select=sel)
         el = time.perf_counter() - t0
         if i >= args.warmup:
             times.append(el)
@@ -469,7 +476,8 @@ def measure_forward(args, w, dev, dist, rank, world, K, warmup, headline, cpu_se
     inp = host_inputs(w)
     d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
     out = torch.empty_like(d["x"])
-    st_shape = (w.batch, w.nheads, w.dstate) if w.mode == "diag" else (w.batch, w.nheads, w.headdim, w.dstate)
+    st_shape = {"diag": (w.batch, w.nheads, w.dstate), "cdiag": (w.batch, w.nheads, w.dstate, 2)}.get(
+        w.mode, (w.batch, w.nheads, w.headdim, w.dstate))
     fs = torch.empty(st_shape, device=dev, dtype=torch.float32) if w.final_state else None
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -539,7 +547,7 @@ def measure_forward(args, w, dev, dist, rank, world, K, warmup, headline, cpu_se
         roof["tensor_frac"] = roof["tensor_tflops"] / peaks["bf16_tflops"]
         roof["tensor_note"] = ("algorithmic FLOPs of the chunk form over the whole call's time, "
                                "against the measured bf16 dense peak")
-    else:
+    elif w.mode == "diag":
         # The diagonal scan needs one exponential per state entry and step; B300's SFU
         # retires 32 ex2 per clock per SM (measured), so its ceiling is
         # SMs x 32 x SM clock.

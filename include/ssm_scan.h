@@ -29,7 +29,24 @@
  *     dt        : (batch, seqlen, nheads)
  *     A, D, dt_bias: (nheads,) fp32
  *     final_state: (batch, nheads, headdim, dstate) fp32
- *   both: B, C : (batch, seqlen, ngroups, dstate); head h reads group h / (nheads/ngroups).
+ *   mode CDIAG (complex diagonal A: the rotating, complex-valued state update read for
+ *   Mamba-3 -- "状态空间模型与 Mamba：不用注意力读取长序列的方法", the Mamba-3 paragraph: an
+ *   input-dependent rotation in the state update, read as underdamped oscillation;
+ *   "基础知识：Mamba 与混合 SSM 架构", 6 Mamba-3: complex-valued state update):
+ *     h_t[n] = exp(Delta_t A[c,n]) h_{t-1}[n] + Delta_t B_t[g,n] x_t[c]   (complex)
+ *     out_t[c] = (Re(sum_n C_t[g,n] h_t[n]) + D[c] x_t[c]) * SiLU(z_t[c])
+ *     with exp(Delta A) = e^{Delta Re A} (cos(Delta Im A) + i sin(Delta Im A)); every
+ *     complex number is stored as an (re, im) pair:
+ *     x, z, out, dt, D, dt_bias as DIAG (headdim must be 1);
+ *     A          : (nheads, dstate, 2) fp32
+ *     B, C       : (batch, seqlen, ngroups, dstate, 2) in the input dtype
+ *     final_state, initial_state: (batch, nheads, dstate, 2) fp32
+ *     dstate (complex entries) 1..32, dstate*2 elements a multiple of 16 bytes; chunk: 0
+ *     or the time-segment length (multiple of 16).  Supported by ssm_scan_fwd, _ws,
+ *     _noalloc and _state; the convolution, step and backward entry points return
+ *     SSM_ERR_UNSUPPORTED for it.
+ *   DIAG and SSD: B, C : (batch, seqlen, ngroups, dstate); head h reads group
+ *   h / (nheads/ngroups).
  *   SSD also needs headdim * dstate to be a multiple of 4 (the state moves in 16-byte
  *   pieces).
  *   x, dt, B, C, z and out share the element type `dtype` (fp32 or bf16; bf16 output
@@ -66,7 +83,7 @@ typedef enum {
     SSM_ERR_TIMEOUT = 8      /* a bounded device-side wait ran out (ssm_device_status) */
 } ssm_status;
 
-typedef enum { SSM_MODE_DIAG = 0, SSM_MODE_SSD = 1 } ssm_mode;
+typedef enum { SSM_MODE_DIAG = 0, SSM_MODE_SSD = 1, SSM_MODE_CDIAG = 2 } ssm_mode;
 typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
 
 typedef struct ssm_shape {
@@ -76,7 +93,7 @@ typedef struct ssm_shape {
     int64_t seqlen;   /* >= 0                                                            */
     int64_t nheads;   /* DIAG: d_inner; SSD: heads; >= 1                                 */
     int64_t headdim;  /* DIAG: 1; SSD: channels per head, 1..256                         */
-    int64_t dstate;   /* N: DIAG 1..64; SSD 1..256                                       */
+    int64_t dstate;   /* N: DIAG 1..64; SSD 1..256; CDIAG 1..32 complex entries          */
     int64_t ngroups;  /* >= 1, divides nheads                                            */
     int64_t chunk;    /* 0 = default.  DIAG: time-segment length (multiple of 32) used to
                          split the sequence across thread blocks; SSD: chunk length Q

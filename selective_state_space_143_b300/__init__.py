@@ -28,12 +28,30 @@ def make_shape(x: torch.Tensor, A: torch.Tensor, B: torch.Tensor, chunk: int = 0
     """Build the ``ssm_shape`` descriptor from tensor shapes.
 
     DIAG (Mamba-1): x (b, T, D), A (D, N).  SSD (Mamba-2): x (b, T, H, P), A (H,).
-    B: (b, T, N) or (b, T, G, N).
+    B: (b, T, N) or (b, T, G, N).  CDIAG (complex A, the rotating state update read for
+    Mamba-3): x (b, T, D), A (D, N, 2), B (b, T, N, 2) or (b, T, G, N, 2), every complex
+    number an (re, im) pair.
     """
     if x.dtype not in _DTYPES:
         raise TypeError(f"x must be float32 or bfloat16, got {x.dtype}")
     s = ssm_shape()
     s.dtype = _DTYPES[x.dtype]
+    if A.dim() == 3:
+        if x.dim() != 3 or A.shape[2] != 2:
+            raise ValueError("complex mode: x must be (batch, seqlen, d_inner), A (d_inner, dstate, 2)")
+        s.mode = _lib.SSM_MODE_CDIAG
+        s.batch, s.seqlen, s.nheads = x.shape
+        s.headdim = 1
+        if B.dim() == 4:
+            s.ngroups, s.dstate = 1, B.shape[2]
+        elif B.dim() == 5:
+            s.ngroups, s.dstate = B.shape[2], B.shape[3]
+        else:
+            raise ValueError("complex mode: B must be (batch, seqlen, dstate, 2) or "
+                             "(batch, seqlen, ngroups, dstate, 2)")
+        s.chunk = int(chunk)
+        s.flags = 0
+        return s
     if A.dim() == 2:
         if x.dim() != 3:
             raise ValueError("diagonal mode: x must be (batch, seqlen, d_inner)")
@@ -127,9 +145,10 @@ def scan_fwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, *, out=None, final_st
         raise ValueError("scan_fwd runs on CUDA tensors only")
     b, T, H, P, N, G = s.batch, s.seqlen, s.nheads, s.headdim, s.dstate, s.ngroups
     diag = s.mode == _lib.SSM_MODE_DIAG
+    cplx = s.mode == _lib.SSM_MODE_CDIAG
     _check("x", x, x.shape, x.dtype, dev)
     _check("dt", dt, (b, T, H), x.dtype, dev)
-    _check("A", A, (H, N) if diag else (H,), torch.float32, dev)
+    _check("A", A, (H, N, 2) if cplx else (H, N) if diag else (H,), torch.float32, dev)
     _check("B", B, B.shape, x.dtype, dev)
     _check("C", C, B.shape, x.dtype, dev)
     _check("D", D, (H,), torch.float32, dev)
@@ -139,7 +158,7 @@ def scan_fwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, *, out=None, final_st
         out = torch.empty_like(x)
     _check("out", out, x.shape, x.dtype, dev)
     want_state = return_final_state or final_state is not None
-    st_shape = (b, H, N) if diag else (b, H, P, N)
+    st_shape = (b, H, N, 2) if cplx else (b, H, N) if diag else (b, H, P, N)
     if want_state and final_state is None:
         final_state = torch.empty(st_shape, device=dev, dtype=torch.float32)
     _check("final_state", final_state, st_shape, torch.float32, dev)

@@ -23,6 +23,7 @@ SSM_ERR_TIMEOUT = 8
 
 SSM_MODE_DIAG = 0
 SSM_MODE_SSD = 1
+SSM_MODE_CDIAG = 2
 SSM_F32 = 0
 SSM_BF16 = 1
 

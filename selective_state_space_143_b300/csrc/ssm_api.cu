@@ -116,7 +116,7 @@ int elem_size(int32_t dtype) { return dtype == SSM_BF16 ? 2 : 4; }
 // Shape checks shared by every entry point.  Returns SSM_OK or the status to report.
 int check_shape(const ssm_shape* s) {
     if (!s) return SSM_ERR_NULL;
-    if (s->mode != SSM_MODE_DIAG && s->mode != SSM_MODE_SSD) return SSM_ERR_DTYPE;
+    if (s->mode != SSM_MODE_DIAG && s->mode != SSM_MODE_SSD && s->mode != SSM_MODE_CDIAG) return SSM_ERR_DTYPE;
     if (s->dtype != SSM_F32 && s->dtype != SSM_BF16) return SSM_ERR_DTYPE;
     if (s->flags != 0) return SSM_ERR_UNSUPPORTED;
     if (s->batch < 0 || s->seqlen < 0 || s->nheads < 1 || s->headdim < 1 || s->dstate < 1 ||
@@ -126,7 +126,15 @@ int check_shape(const ssm_shape* s) {
     if (s->batch > kMaxGridYZ / 4) return SSM_ERR_UNSUPPORTED;
     if (s->seqlen > (int64_t(1) << 40) || s->nheads > (int64_t(1) << 24)) return SSM_ERR_UNSUPPORTED;
     const int E = elem_size(s->dtype);
-    if (s->mode == SSM_MODE_DIAG) {
+    if (s->mode == SSM_MODE_CDIAG) {
+        if (s->headdim != 1) return SSM_ERR_SHAPE;
+        if (s->dstate > 32) return SSM_ERR_UNSUPPORTED;
+        if (s->chunk != 0 && s->chunk % 16 != 0) return SSM_ERR_SHAPE;
+        // each group's channel run and each complex B/C row are whole 16-byte chunks
+        if (((s->nheads / s->ngroups) * E) % 16 != 0) return SSM_ERR_ALIGN;
+        if ((s->dstate * 2 * E) % 16 != 0) return SSM_ERR_ALIGN;
+        if (s->chunk > 0 && (s->seqlen + s->chunk - 1) / s->chunk > kMaxGridYZ) return SSM_ERR_UNSUPPORTED;
+    } else if (s->mode == SSM_MODE_DIAG) {
         if (s->headdim != 1) return SSM_ERR_SHAPE;
         if (s->dstate > 64) return SSM_ERR_UNSUPPORTED;
         if (s->chunk != 0 && s->chunk % 32 != 0) return SSM_ERR_SHAPE;
@@ -161,9 +169,11 @@ int check_args(const void* x, const void* dt, const float* A, const void* B, con
     return SSM_OK;
 }
 
-// Bytes of the fp32 state of all sequences: (batch, nheads, headdim, dstate).
+// Bytes of the fp32 state of all sequences: (batch, nheads, headdim, dstate), times two
+// (re, im) in the complex mode.
 size_t state_bytes(const ssm_shape* s) {
-    return (size_t)s->batch * s->nheads * s->headdim * s->dstate * sizeof(float);
+    return (size_t)s->batch * s->nheads * s->headdim * s->dstate * sizeof(float) *
+           (s->mode == SSM_MODE_CDIAG ? 2 : 1);
 }
 
 bool overlaps(const void* p, size_t pn, const void* q, size_t qn) {
@@ -213,7 +223,9 @@ size_t conv_buffer_bytes(const ScanArgs& a, int mode) {
 }
 
 size_t workspace_for(const ScanArgs& a, int mode) {
-    const size_t base = mode == SSM_MODE_DIAG ? diag_workspace_bytes(a) : ssd_workspace_bytes(a);
+    const size_t base = mode == SSM_MODE_DIAG    ? diag_workspace_bytes(a)
+                        : mode == SSM_MODE_CDIAG ? cdiag_workspace_bytes(a)
+                                                 : ssd_workspace_bytes(a);
     const size_t conv = conv_buffer_bytes(a, mode);
     return conv ? align_up(base, 256) + conv : base;
 }
@@ -223,6 +235,8 @@ int run(const ScanArgs& a, int mode, void* ws, cudaStream_t stream) {
     cudaError_t e;
     if (mode == SSM_MODE_DIAG) {
         e = diag_launch(a, ws, stream);
+    } else if (mode == SSM_MODE_CDIAG) {
+        e = cdiag_launch(a, ws, stream);
     } else if (a.conv_k > 0) {
         // convolution pass into scratch, then the SSD kernels on the convolved input
         void* xc = (char*)ws + align_up(ssd_workspace_bytes(a), 256);
@@ -297,6 +311,7 @@ int step_common(const void* x, const void* dt, const float* A, const void* B, co
                 float* state, void* out, const ssm_shape* shape, cudaStream_t stream) {
     const int rc = check_shape(shape);
     if (rc != SSM_OK) return rc;
+    if (shape->mode == SSM_MODE_CDIAG) return SSM_ERR_UNSUPPORTED;
     if (shape->seqlen != 1) return SSM_ERR_SHAPE;
     if (shape->dstate % 4 != 0) return SSM_ERR_ALIGN;  // state rows move in 16-byte pieces
     // one grid row per sequence, 32-bit channel indices within a sequence
@@ -463,7 +478,7 @@ int ssm_scan_fwd_state(const void* x, const void* dt, const float* A, const void
 }
 
 size_t ssm_scan_conv_workspace_size(const ssm_shape* shape) {
-    if (check_shape(shape) != SSM_OK) return (size_t)-1;
+    if (check_shape(shape) != SSM_OK || shape->mode == SSM_MODE_CDIAG) return (size_t)-1;
     ScanArgs a = make_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
                            nullptr, nullptr, shape);
     a.conv_k = 4;  // any width: the scratch does not depend on it
@@ -479,6 +494,7 @@ int ssm_scan_fwd_conv(const void* x, const void* dt, const float* A, const void*
     if (rc != SSM_OK) return rc;
     rc = check_conv(conv);
     if (rc != SSM_OK) return rc;
+    if (shape->mode == SSM_MODE_CDIAG) return SSM_ERR_UNSUPPORTED;
     const size_t sb = state_bytes(shape);
     const size_t cb = conv_state_bytes(shape, conv->width);
     const size_t xb = (size_t)shape->batch * shape->seqlen * shape->nheads * shape->headdim * elem_size(shape->dtype);
@@ -494,7 +510,7 @@ int ssm_scan_fwd_conv(const void* x, const void* dt, const float* A, const void*
 }
 
 size_t ssm_scan_bwd_workspace_size(const ssm_shape* shape) {
-    if (check_shape(shape) != SSM_OK) return (size_t)-1;
+    if (check_shape(shape) != SSM_OK || shape->mode == SSM_MODE_CDIAG) return (size_t)-1;
     const ScanArgs a = make_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
                                  nullptr, nullptr, nullptr, shape);
     return scan_bwd_workspace_bytes(a);
@@ -508,6 +524,7 @@ int ssm_scan_bwd(const void* x, const void* dt, const float* A, const void* B, c
                  size_t workspace_bytes, ssm_stream_t stream) {
     int rc = check_args(x, dt, A, B, C, D, z, dt_bias, dx, nullptr, shape, initial_state);
     if (rc != SSM_OK) return rc;
+    if (shape->mode == SSM_MODE_CDIAG) return SSM_ERR_UNSUPPORTED;
     const bool empty = shape->batch == 0 || shape->seqlen == 0;
     if (!dA || (!empty && (!dout || !dx || !ddt || !dB || !dC))) return SSM_ERR_NULL;
     const void* outs[] = {dout, dfinal_state, dx, ddt, dA, dB, dC, dD, dz, ddt_bias, dinitial_state};

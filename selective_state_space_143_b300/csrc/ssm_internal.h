@@ -46,6 +46,11 @@ void note_launch(const char* name, cudaStream_t stream, cudaEvent_t start);
 size_t diag_workspace_bytes(const ScanArgs& a);
 cudaError_t diag_launch(const ScanArgs& a, void* ws, cudaStream_t stream);
 
+// Complex diagonal path (the rotating state update read for Mamba-3): A (nheads, dstate, 2),
+// B/C (batch, seqlen, ngroups, dstate, 2), states (batch, nheads, dstate, 2).
+size_t cdiag_workspace_bytes(const ScanArgs& a);
+cudaError_t cdiag_launch(const ScanArgs& a, void* ws, cudaStream_t stream);
+
 // SSD (Mamba-2) path.
 size_t ssd_workspace_bytes(const ScanArgs& a);
 cudaError_t ssd_launch(const ScanArgs& a, void* ws, cudaStream_t stream);

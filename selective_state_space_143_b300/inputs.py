@@ -13,11 +13,15 @@ the larger ones are a 3B-width Mamba-1 layer and two Mamba-2/SSD layers):
   c2  diagonal A, bf16:  batch 4,  L 8192,   d_inner 5120,  N 16, gate, dt_bias, D, final state
   c3  SSD, bf16:         batch 4,  L 8192,   64 heads x 64, N 128, chunk 256, D
   c4  SSD, bf16:         batch 1,  L 131072, 32 heads x 64, N 256, chunk 256, D, final state
+  cx1 complex diagonal A (the rotating state update read for Mamba-3) at c1's shape
+  cx2 complex diagonal A at c2's shape, final state
 
 Distributions: x, z, B, C ~ N(0, 1); dt = 0.5 N(0, 1) - 2 (the kernel applies
 softplus(dt + dt_bias)); dt_bias ~ U(-4, -2) per channel; D ~ N(1, 0.1) (c0: D = 1);
-diagonal A[c, n] = -(n + 1); SSD A_h = -U(1, 16).  Values are drawn in float32 from
-numpy's PCG64 stream in the fixed order x, dt, B, C, z, D, dt_bias, A and then
+diagonal A[c, n] = -(n + 1); SSD A_h = -U(1, 16); complex diagonal A[c, n] =
+-(n + 1) + i U(-pi, pi) (the real part as the diagonal workloads, an angular frequency
+per entry), B and C with N(0, 1) real and imaginary parts.  Values are drawn in float32
+from numpy's PCG64 stream in the fixed order x, dt, B, C, z, D, dt_bias, A and then
 rounded (round-to-nearest-even) to the workload's dtype; both the CUDA path and
 the oracle read the rounded values.
 """
@@ -32,7 +36,7 @@ import torch
 @dataclasses.dataclass(frozen=True)
 class Workload:
     name: str
-    mode: str            # "diag" (Mamba-1) or "ssd" (Mamba-2)
+    mode: str            # "diag" (Mamba-1), "ssd" (Mamba-2) or "cdiag" (complex diagonal A)
     dtype: str           # "f32" or "bf16": storage type of x, dt, B, C, z and out
     batch: int
     seqlen: int
@@ -69,6 +73,10 @@ WORKLOADS = {
     "c3": Workload("c3", "ssd", "bf16", 4, 8192, 64, 64, 128, chunk=256, seed=3),
     "c4": Workload("c4", "ssd", "bf16", 1, 131072, 32, 64, 256, chunk=256,
                    final_state=True, seed=4),
+    "cx1": Workload("cx1", "cdiag", "bf16", 8, 1024, 512, 1, 16, gate=True, dt_bias=True,
+                    seed=11),
+    "cx2": Workload("cx2", "cdiag", "bf16", 4, 8192, 5120, 1, 16, gate=True, dt_bias=True,
+                    final_state=True, seed=12),
 }
 
 _TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
@@ -83,6 +91,9 @@ def shapes(w: Workload) -> dict:
     if w.mode == "diag":
         s = dict(x=(b, T, H), dt=(b, T, H), A=(H, N), B=(b, T, G, N), C=(b, T, G, N),
                  state=(b, H, N))
+    elif w.mode == "cdiag":
+        s = dict(x=(b, T, H), dt=(b, T, H), A=(H, N, 2), B=(b, T, G, N, 2), C=(b, T, G, N, 2),
+                 state=(b, H, N, 2))
     else:
         s = dict(x=(b, T, H, P), dt=(b, T, H), A=(H,), B=(b, T, G, N), C=(b, T, G, N),
                  state=(b, H, P, N))
@@ -121,6 +132,10 @@ def make_inputs(w: Workload, seed: int | None = None) -> dict:
     dt_bias = rng.uniform(-4.0, -2.0, s["dt_bias"]).astype(f32) if w.dt_bias else None
     if w.mode == "diag":
         A = -np.broadcast_to(np.arange(1, w.dstate + 1, dtype=f32), s["A"]).copy()
+    elif w.mode == "cdiag":
+        A = np.empty(s["A"], dtype=f32)
+        A[..., 0] = -np.arange(1, w.dstate + 1, dtype=f32)
+        A[..., 1] = rng.uniform(-np.pi, np.pi, s["A"][:2]).astype(f32)
     else:
         A = (-rng.uniform(1.0, 16.0, s["A"])).astype(f32)
     return dict(

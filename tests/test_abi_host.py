@@ -356,3 +356,28 @@ def test_tuning_knobs():
     # shape into several parts, each with its own summaries
     assert one_part < default
     assert lib.ssm_scan_bwd_workspace_size(ctypes.byref(s)) == default
+
+
+def test_complex_mode_shapes_and_unsupported_entry_points():
+    lib = _lib.load()
+    vp = ctypes.c_void_p
+    cd = dict(mode=2, nheads=64, dstate=16)
+    assert _ws(_shape(**cd)) != BAD
+    assert _ws(_shape(mode=2, nheads=64, dstate=33)) == BAD          # at most 32 complex entries
+    assert _ws(_shape(mode=2, nheads=64, dstate=2)) == BAD           # bf16 rows: 16-byte multiples
+    assert _ws(_shape(mode=2, dtype=0, nheads=64, dstate=2)) != BAD  # fp32: 2 x 2 x 4 bytes
+    assert _ws(_shape(mode=2, nheads=64, dstate=16, headdim=2)) == BAD
+    assert _call(_shape(mode=2, nheads=64, dstate=40)) == _lib.SSM_ERR_UNSUPPORTED
+    # few channels: the sequence is split into segments, with their summaries as scratch
+    assert _ws(_shape(mode=2, nheads=64, dstate=16, seqlen=4096)) > 0
+    s = _shape(**cd)
+    assert lib.ssm_scan_conv_workspace_size(ctypes.byref(s)) == BAD
+    assert lib.ssm_scan_bwd_workspace_size(ctypes.byref(s)) == BAD
+    assert _step(_shape(seqlen=1, **cd)) == _lib.SSM_ERR_UNSUPPORTED
+    ptrs = [vp((i + 1) << 12) for i in range(20)]
+    assert lib.ssm_scan_bwd(*ptrs, ctypes.byref(s), None, 0, None) == _lib.SSM_ERR_UNSUPPORTED
+    c = _lib.ssm_conv()
+    c.weight, c.bias, c.x_prev, c.x_last, c.width = 9 << 20, None, None, None, 4
+    assert lib.ssm_scan_fwd_conv(vp(1 << 12), vp(2 << 12), vp(3 << 12), vp(4 << 12), vp(5 << 12),
+                                 None, None, None, ctypes.byref(c), None, vp(6 << 20), None,
+                                 ctypes.byref(s), None, 0, None) == _lib.SSM_ERR_UNSUPPORTED
