@@ -1,0 +1,493 @@
+// SSD chunk scan on the B300 tensor cores: the output of every chunk from the chunk's
+// own inputs and the state carried into it ("Mamba-2：把状态空间模型和 Attention 统一到一个
+// 数学框架里", 第二步 and 关键技术点 1-3: y = (L o M) x, dense diagonal blocks, low-rank
+// off-diagonal blocks through the carried state).  Per (chunk, 128-row half, up to 8
+// heads of one group), with s_t the in-chunk cumulative sum of Delta_t A_h:
+//   G        = C_rows B^T                                   (M = 128, N = rows s of the half's causal range, K = dstate)
+//   M'[t, s] = G[t, s] exp(s_t - s_s) Delta_s  (s < t),  G[t, t] Delta_t + D  (s = t),  0  (s > t)
+//   Y_diag   = M' X_h                                       (M = 128, N = 64, K = s)
+//   Y_off    = C_rows h_{c-1}^T                              (M = 128, N = 64, K = dstate)
+//   out      = (Y_diag + exp(s_t) Y_off) SiLU(z)
+// The skip term D x rides on M's diagonal, so the epilogue reads only the accumulators
+// (and z).  M' is the one operand built by threads: scaled, masked and split into bf16
+// hi + lo halves, both multiplied against the exact bf16 X, so that the scaled operand
+// keeps ~16 significant bits.  Every other operand arrives by TMA / bulk copies: C and
+// B rows and x tiles through 3-D tensor maps whose 8-element boxes write the no-swizzle
+// canonical layout directly, h_{c-1} (already split hi/lo by the carry pass) as one
+// contiguous bulk copy.  Copies complete on mbarriers; every wait is bounded.
+//
+// One CTA of 16 warps per SM (512 TMEM columns: G, and two sets of Y accumulators so
+// that a head's epilogue overlaps the next head's MMAs).  Warp w owns TMEM lanes
+// 32*(w%4).. (rows) and the column quarter w/4 of each M' part.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+#include "ssm_device.cuh"
+#include "ssm_internal.h"
+#include "ssd_tc.h"
+#include "tc_util.cuh"
+
+namespace ssm {
+
+namespace {
+
+constexpr int kP = 64;            // headdim handled here
+constexpr int kThreads = 512;     // 16 warps
+constexpr int kStatusTimeout = 8;
+
+template <int N, bool XS>
+struct ScanCfg {
+    static_assert(N % 64 == 0, "C and B rows are 128-byte swizzle rows of 64 elements");
+    static constexpr int KPC = N > 128 ? 32 : 64;           // columns of M' per K-part
+    static constexpr int BC = KPC / 4;                       // columns of a part per warp
+    static constexpr uint32_t kC = 128u * N * 2;             // C rows of the half
+    static constexpr uint32_t kB = 256u * N * 2;             // B rows [0, SW), prologue only
+    static constexpr uint32_t kMPart = 128u * KPC * 2;       // one M' part, hi or lo
+    static constexpr uint32_t kX = 256u * kP * 2;            // one x buffer (256 rows)
+    static constexpr uint32_t kH = (uint32_t)kP * N * 2;     // one h_{c-1} tile, hi or lo
+    static constexpr int kHBufs = N <= 128 ? 2 : 1;          // (hi, lo) tile sets
+    static constexpr uint32_t kPhase2 = 4 * kMPart + 2 * kX + kHBufs * 2 * kH;
+    static constexpr uint32_t kRegion = kB > kPhase2 ? kB : kPhase2;
+    static constexpr uint32_t kSmem = kC + kRegion;   // operands; the pipeline state follows
+    static constexpr uint32_t kSmemTotal = kSmem + 2304;
+    static_assert(kSmemTotal <= 232448, "shared memory");
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// v = hi + lo with hi = bf16(v) and lo = bf16(v - hi), two values at a time.
+__device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    const float2 hf = __bfloat1622float2(h);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    const float2 l = __ffma2_rn(hf, make_float2(-1.0f, -1.0f), make_float2(a, b));
+    lo = pack_bf16x2(l.x, l.y);
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d));
+}
+
+// Shared state of one CTA's pipeline.
+struct __align__(16) ScanShared {
+    float cum[256];
+    float beta[256];   // log2(Delta_s) - cum_s log2(e): exp(cum_t - cum_s) Delta_s = 2^(alpha_t + beta_s)
+    uint64_t mb_load;  // C and B rows (prologue)
+    uint64_t mb_g;     // G's MMAs
+    uint64_t mb_mma[2];  // M' parts' MMAs: commit n on [n & 1], phase (n >> 1) & 1
+    uint64_t mb_x[2];  // x tiles (buffer i)
+    uint64_t mb_h[2];  // h_{c-1} tiles (set i)
+    uint32_t tmem;
+    int abort;         // a bounded wait gave up: every thread leaves at the next check
+};
+
+// grid (nchunks * Q/128, H / heads_per_cta, batch); 512 threads; one CTA per SM.
+template <int N, bool GATE, bool XS>
+__global__ void __launch_bounds__(kThreads, 1)
+    ssd_scan_tc(const SsdTcArgs a, const int heads_per_cta, int* status, const __grid_constant__ CUtensorMap tm_x,
+                const __grid_constant__ CUtensorMap tm_xlo, const __grid_constant__ CUtensorMap tm_c,
+                const __grid_constant__ CUtensorMap tm_b) {
+    using Cfg = ScanCfg<N, XS>;
+    constexpr int KPC = Cfg::KPC, BC = Cfg::BC;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    ScanShared& sh = *reinterpret_cast<ScanShared*>(smem + Cfg::kSmem);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int Q = (int)a.Q;
+    const int halves = Q / 128;
+    const int64_t c = blockIdx.x / halves;
+    const int rh = blockIdx.x % halves;
+    const int b = blockIdx.z;
+    const int len = (int)min((int64_t)Q, a.T - c * a.Q);
+    const int t0 = 128 * rh;
+    if (t0 >= len) return;      // no valid rows in this half (uniform over the CTA)
+    const int SW = t0 + 128;    // columns s of G this half needs (causal)
+    const int nparts = SW / KPC;
+    const int hbeg = blockIdx.y * heads_per_cta;
+    const int g = hbeg / (int)(a.H / a.G);
+    const int row0 = (int)(c * a.Q);  // first token of the chunk within its sequence
+    // XS with 256 rows: a head's two x planes take both x buffers (serial heads)
+    const bool xser = XS && SW > 128;
+
+    // TMA-written operands use the 128-byte swizzle layout (rows of 64 elements):
+    unsigned char* sC = smem;                               // [n/64][t 128][64], K-major A
+    unsigned char* region = smem + Cfg::kC;
+    unsigned char* sB = region;                             // [n/64][s SW][64], K-major B (prologue)
+    // thread- and carry-written operands use the no-swizzle core-matrix layout:
+    unsigned char* sM = region;                             // [part 2][hi, lo] [t/8][s/8 of KPC][8][8]
+    unsigned char* sX = region + 4 * Cfg::kMPart;           // [buffer 2] [s SW][64] (+ lo plane), MN-major B
+    unsigned char* sH = sX + 2 * Cfg::kX;                   // [set kHBufs][hi, lo] [p/8][n/8][8][8]
+
+    if (tid == 0) {
+        tc::mbar_init(&sh.mb_load, 1);
+        tc::mbar_init(&sh.mb_g, 1);
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&sh.mb_mma[i], 1);
+            tc::mbar_init(&sh.mb_x[i], 1);
+            tc::mbar_init(&sh.mb_h[i], 1);
+        }
+        sh.abort = 0;
+        tc::mbar_fence_init();
+    }
+    if (warp == 0) tc::tmem_alloc(&sh.tmem, 512);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = sh.tmem;
+    const uint32_t tG = tmem;
+
+    // ---- prologue: C rows of the half and B rows [0, SW) by TMA, then G = C B^T
+    if (tid == 0) {
+        tc::mbar_arrive_expect_tx(&sh.mb_load, Cfg::kC + (uint32_t)SW * N * 2);
+        for (int j = 0; j < N / 64; ++j) {
+            tc::tma_load_3d(sC + j * 128 * 128, &tm_c, g * N + 64 * j, row0 + t0, b, &sh.mb_load);
+            for (int rb = 0; rb < SW / 128; ++rb)
+                tc::tma_load_3d(sB + (j * SW + rb * 128) * 128, &tm_b, g * N + 64 * j, row0 + 128 * rb, b, &sh.mb_load);
+        }
+        bool ok = tc::mbar_wait(&sh.mb_load, 0);
+        tc::fence_after_sync();
+        if (ok) {
+            const uint32_t idesc = tc::idesc_bf16(128, SW, 0, 0);
+#pragma unroll 1
+            for (int ks = 0; ks < N / 16; ++ks) {
+                const uint32_t in_row = (uint32_t)(ks & 3) * 32;  // K offset inside a 128-byte row
+                const uint64_t da = tc::desc_sw128(tc::smem_u32(sC + (ks >> 2) * 128 * 128) + in_row, 16, 1024);
+                const uint64_t db = tc::desc_sw128(tc::smem_u32(sB + (ks >> 2) * SW * 128) + in_row, 16, 1024);
+                tc::mma_bf16(tG, da, db, idesc, ks > 0);
+            }
+            tc::mma_commit(&sh.mb_g);
+        } else {
+            sh.abort = 1;
+        }
+    }
+    __syncthreads();
+    if (sh.abort) goto teardown;
+    if (!tc::mbar_wait(&sh.mb_g, 0)) sh.abort = 1;  // every thread: G is in TMEM, B's region is free
+    tc::fence_after_sync();
+    __syncthreads();
+    if (sh.abort) goto teardown;
+    {
+        const int q = warp & 3;             // TMEM lane quarter
+        const int cq = warp >> 2;           // column quarter of a part
+        const int r = q * 32 + lane;        // row (TMEM lane) within the half
+        const int t = t0 + r;               // row within the chunk
+        const bool row_ok = t < len;
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+        const int t_warp_min = t0 + q * 32;  // tcgen05.ld and the part blocks are per warp
+        const int t_warp_max = t_warp_min + 31;
+
+        // x tile of head hn -> buffer xb (xser: hi in buffer 0, lo in buffer 1)
+        auto load_x = [&](int hn, int xb) {
+            const uint32_t planes = XS ? 2 : 1;
+            uint64_t* mb = &sh.mb_x[xser ? 0 : xb];
+            tc::mbar_arrive_expect_tx(mb, planes * (uint32_t)SW * kP * 2);
+            for (int pl = 0; pl < (int)planes; ++pl) {
+                unsigned char* base = xser ? sX + pl * Cfg::kX : sX + xb * Cfg::kX + pl * (uint32_t)SW * kP * 2;
+                const CUtensorMap* tm = pl ? &tm_xlo : &tm_x;
+                for (int rb = 0; rb < SW / 128; ++rb)
+                    tc::tma_load_3d(base + rb * 128 * 128, tm, hn * kP, row0 + 128 * rb, b, mb);
+            }
+        };
+        // h_{c-1} of head hn (hi and lo tiles, contiguous) -> set hs
+        auto load_h = [&](int hn, int hs) {
+            const unsigned char* src = reinterpret_cast<const unsigned char*>(
+                a.states + (((int64_t)b * a.nchunks + c) * a.H + hn) * (int64_t)kP * N);
+            tc::mbar_arrive_expect_tx(&sh.mb_h[hs], 2 * Cfg::kH);
+            tc::bulk_load(sH + hs * 2 * Cfg::kH, src, 2 * Cfg::kH, &sh.mb_h[hs]);
+        };
+        auto x_tile = [&](int hi_, int plane) -> uint32_t {
+            if (xser) return tc::smem_u32(sX + plane * Cfg::kX);
+            return tc::smem_u32(sX + (hi_ & 1) * Cfg::kX + plane * (uint32_t)SW * kP * 2);
+        };
+
+        if (tid == 0) {
+            load_x(hbeg, 0);
+            load_h(hbeg, 0);
+        }
+
+        // MMA commits are numbered; commit n arrives on mb_mma[n & 1], phase (n >> 1) & 1.
+        // A wait is only ever on one of the latest two commits.
+        uint32_t ncommit = 0;
+        auto wait_commit = [&](uint32_t n) {
+            if (!tc::mbar_wait(&sh.mb_mma[n & 1], (n >> 1) & 1)) sh.abort = 1;
+            tc::fence_after_sync();
+        };
+        // epilogue of head hh from accumulator set acc: out = Y_diag + exp(cum_t) Y_off, gate
+        auto finish = [&](int hh, int acc, float alpha_h) {
+            const uint32_t tYd = tmem + 256 + 128 * acc, tYo = tYd + 64;
+            const int p0 = 16 * cq;
+            uint32_t yd[16], yo[16];
+            tc::tmem_ld16_async(tYd + lane_base + (uint32_t)p0, yd);
+            tc::tmem_ld16_async(tYo + lane_base + (uint32_t)p0, yo);
+            tc::tmem_wait_ld();
+            if (!row_ok) return;
+            const float e = ex2(alpha_h);
+            const int64_t row = (((int64_t)b * a.T + row0 + t) * a.H + hh) * kP + p0;
+            uint4 zr[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+            if (GATE) {
+                zr[0] = *reinterpret_cast<const uint4*>(a.z + row);
+                zr[1] = *reinterpret_cast<const uint4*>(a.z + row + 8);
+            }
+            const __nv_bfloat162* z2 = reinterpret_cast<const __nv_bfloat162*>(zr);
+            uint32_t pk[8];
+#pragma unroll
+            for (int j = 0; j < 16; j += 2) {
+                float2 y = __ffma2_rn(make_float2(e, e), make_float2(__uint_as_float(yo[j]), __uint_as_float(yo[j + 1])),
+                                      make_float2(__uint_as_float(yd[j]), __uint_as_float(yd[j + 1])));
+                if (GATE) y = __fmul2_rn(y, silu2_fma(__bfloat1622float2(z2[j / 2])));
+                pk[j / 2] = pack_bf16x2(y.x, y.y);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(a.out + row);
+            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        };
+
+        // Build this thread's BC columns of M' part kp for head hh into part buffer pb:
+        // row t, columns s0 .. s0 + BC - 1.  Blocks wholly above the diagonal are zero;
+        // blocks that reach it are masked and take D on the diagonal.
+        const uint32_t row_off = (uint32_t)((r >> 3) * (KPC / 8) * 128 + (r & 7) * 16);
+        auto build = [&](int kp, int pb, float alpha, float Dh) {
+            const int s0 = KPC * kp + BC * cq;
+            uint32_t hw[BC / 2], lw[BC / 2];
+            if (s0 > t_warp_max) {
+#pragma unroll
+                for (int j = 0; j < BC / 2; ++j) hw[j] = lw[j] = 0u;
+            } else {
+                uint32_t gv[BC];
+                tc::tmem_ld_async(tG + lane_base + (uint32_t)s0, gv);
+                float bt[BC];
+#pragma unroll
+                for (int j = 0; j < BC; j += 4) *reinterpret_cast<float4*>(&bt[j]) = *reinterpret_cast<const float4*>(&sh.beta[s0 + j]);
+                tc::tmem_wait_ld();
+                const bool diag = s0 + BC - 1 >= t_warp_min;  // some column reaches some row of the warp
+                const float2 al = make_float2(alpha, alpha);
+#pragma unroll
+                for (int j = 0; j < BC; j += 2) {
+                    const float2 ar = __fadd2_rn(al, make_float2(bt[j], bt[j + 1]));
+                    float2 v = __fmul2_rn(make_float2(ex2(ar.x), ex2(ar.y)),
+                                          make_float2(__uint_as_float(gv[j]), __uint_as_float(gv[j + 1])));
+                    if (diag) {
+                        const int s = s0 + j;
+                        v.x = s < t ? v.x : (s == t ? v.x + Dh : 0.0f);
+                        v.y = s + 1 < t ? v.y : (s + 1 == t ? v.y + Dh : 0.0f);
+                    }
+                    split_pair(v.x, v.y, hw[j / 2], lw[j / 2]);
+                }
+            }
+            const uint32_t ph = tc::smem_u32(sM + pb * 2 * Cfg::kMPart) + row_off + (uint32_t)(cq * BC / 8) * 128;
+            const uint32_t pl = ph + Cfg::kMPart;
+#pragma unroll
+            for (int j = 0; j < BC / 8; ++j) {
+                sts128(ph + j * 128, hw[4 * j], hw[4 * j + 1], hw[4 * j + 2], hw[4 * j + 3]);
+                sts128(pl + j * 128, lw[4 * j], lw[4 * j + 1], lw[4 * j + 2], lw[4 * j + 3]);
+            }
+        };
+
+        // Delta, cumulative sum and D of the next head, fetched a head ahead
+        float pf_dl = 0.0f, pf_cum = 0.0f, pf_D = 0.0f;
+        auto prefetch = [&](int hn) {
+            if (tid < Q) {
+                const int64_t o = (((int64_t)b * a.H + hn) * a.nchunks + c) * a.Q + tid;
+                pf_dl = a.dl[o];
+                pf_cum = a.cum[o];
+            }
+            pf_D = a.D ? a.D[hn] : 0.0f;
+        };
+        prefetch(hbeg);
+
+        uint32_t last_commit_prev = 0;  // the previous head's last commit
+        float alpha_prev = 0.0f;
+        for (int hi = 0; hi < heads_per_cta; ++hi) {
+            const int h = hbeg + hi;
+            // every thread is past the previous head's builds before cum / beta change
+            __syncthreads();
+            if (sh.abort) break;
+            if (tid < Q) {
+                sh.cum[tid] = pf_cum;
+                sh.beta[tid] = (pf_dl > 0.0f ? lg2(pf_dl) : -INFINITY) - pf_cum * kLog2e;
+            }
+            const float Dh = pf_D;
+            if (hi + 1 < heads_per_cta) prefetch(h + 1);
+            __syncthreads();
+            const float alpha = sh.cum[min(t, Q - 1)] * kLog2e;
+            for (int kp = 0; kp < nparts; ++kp) {
+                // this part's buffer was last used by commit ncommit - 2
+                if (ncommit >= 2) wait_commit(ncommit - 2);
+                // one h set: part 0's MMAs (the last readers of this head's h tiles) are
+                // done once commit ncommit - 2 has arrived at part 2
+                if (Cfg::kHBufs == 1 && kp == 2 && hi + 1 < heads_per_cta && tid == 0) load_h(h + 1, 0);
+                build(kp, ncommit & 1, alpha, Dh);
+                tc::fence_async_smem();
+                tc::fence_before_sync();
+                __syncthreads();
+                if (sh.abort) break;
+                tc::fence_after_sync();
+                if (tid == 0) {
+                    bool ok = true;
+                    if (kp == 0) {
+                        // this head's x and h tiles have landed
+                        ok = tc::mbar_wait(&sh.mb_x[xser ? 0 : (hi & 1)], xser ? (hi & 1) : ((hi >> 1) & 1));
+                        ok = ok && tc::mbar_wait(&sh.mb_h[Cfg::kHBufs == 2 ? (hi & 1) : 0],
+                                                 Cfg::kHBufs == 2 ? ((hi >> 1) & 1) : (hi & 1));
+                        tc::fence_after_sync();
+                    }
+                    if (ok) {
+                        const uint32_t pb = ncommit & 1;
+                        const uint32_t tYd = tmem + 256 + 128 * (hi & 1), tYo = tYd + 64;
+                        constexpr uint32_t id_diag = tc::idesc_bf16(128, kP, 0, 1);
+                        const uint32_t mh = tc::smem_u32(sM + pb * 2 * Cfg::kMPart);
+                        const uint64_t dmh = tc::desc_strided(mh, 128, (KPC / 8) * 128);
+                        const uint64_t dml = tc::desc_strided(mh + Cfg::kMPart, 128, (KPC / 8) * 128);
+                        // x: rows s of this part, 128 bytes each; K steps of 16 rows are 2048
+                        // bytes (128 in descriptor units) apart
+                        const uint64_t dx = tc::desc_sw128(x_tile(hi, 0) + (uint32_t)(kp * KPC) * 128, 1024, 1024);
+#pragma unroll
+                        for (int ks = 0; ks < KPC / 16; ++ks)
+                            tc::mma_bf16(tYd, dmh + ks * 16u, dx + ks * 128u, id_diag, (kp > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
+                        for (int ks = 0; ks < KPC / 16; ++ks) tc::mma_bf16(tYd, dml + ks * 16u, dx + ks * 128u, id_diag, 1u);
+                        if (XS) {
+                            const uint64_t dxl = tc::desc_sw128(x_tile(hi, 1) + (uint32_t)(kp * KPC) * 128, 1024, 1024);
+#pragma unroll
+                            for (int ks = 0; ks < KPC / 16; ++ks) tc::mma_bf16(tYd, dmh + ks * 16u, dxl + ks * 128u, id_diag, 1u);
+                        }
+                        if (kp == 0) {
+                            constexpr uint32_t id_off = tc::idesc_bf16(128, kP, 0, 0);
+                            const uint32_t cb = tc::smem_u32(sC);
+                            const uint32_t hs = tc::smem_u32(sH + (Cfg::kHBufs == 2 ? (hi & 1) : 0) * 2 * Cfg::kH);
+                            const uint64_t dhh = tc::desc_strided(hs, 128, (N / 8) * 128);
+                            const uint64_t dhl = tc::desc_strided(hs + Cfg::kH, 128, (N / 8) * 128);
+#pragma unroll
+                            for (int ks = 0; ks < N / 16; ++ks) {
+                                const uint64_t dc = tc::desc_sw128(cb + (uint32_t)(ks >> 2) * 128 * 128 + (uint32_t)(ks & 3) * 32, 16, 1024);
+                                tc::mma_bf16(tYo, dc, dhh + ks * 16u, id_off, ks > 0 ? 1u : 0u);
+                                tc::mma_bf16(tYo, dc, dhl + ks * 16u, id_off, 1u);
+                            }
+                        }
+                        tc::mma_commit(&sh.mb_mma[ncommit & 1]);
+                    } else {
+                        sh.abort = 1;
+                    }
+                }
+                ++ncommit;
+                if (kp == 0) {
+                    // the previous head's epilogue, once this head's first MMAs are queued;
+                    // then its buffers take the next head's tiles
+                    if (hi > 0) {
+                        wait_commit(last_commit_prev);
+                        finish(h - 1, (hi - 1) & 1, alpha_prev);
+                        tc::fence_before_sync();
+                    }
+                    if (hi + 1 < heads_per_cta && tid == 0 && !sh.abort) {
+                        if (!xser) load_x(h + 1, (hi + 1) & 1);
+                        if (Cfg::kHBufs == 2) load_h(h + 1, (hi + 1) & 1);
+                    }
+                }
+                // serial planes: both x buffers are free once this head's last MMAs are done
+                if (xser && kp == nparts - 1 && hi + 1 < heads_per_cta && tid == 0) {
+                    wait_commit(ncommit - 1);
+                    if (!sh.abort) load_x(h + 1, 0);
+                }
+            }
+            last_commit_prev = ncommit - 1;
+            alpha_prev = alpha;
+        }
+        __syncthreads();
+        if (!sh.abort && heads_per_cta > 0) {
+            wait_commit(last_commit_prev);
+            finish(hbeg + heads_per_cta - 1, (heads_per_cta - 1) & 1, alpha_prev);
+        }
+    }
+teardown:
+    if (sh.abort && tid == 0) atomicExch(status, kStatusTimeout);
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, 512);
+}
+
+// ---- host side -----------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            (void)cudaGetLastError();
+            return (PFN_cuTensorMapEncodeTiled_v12000) nullptr;
+        }
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+// 3-D map over a bf16 tensor (inner, T, batch), row-major and contiguous, with boxes of
+// 64 inner elements x 128 rows x 1 in the 128-byte swizzle layout: each box lands as 128
+// rows of 128 bytes, the operand layout of desc_sw128.  Rows past T read as zero.
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t T, uint64_t batch) {
+    const PFN_cuTensorMapEncodeTiled_v12000 fn = encode_tiled();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {inner, T, batch};
+    const cuuint64_t strides[2] = {inner * 2, inner * 2 * T};
+    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Heads per CTA: the largest of 8, 4, 2 that divides the heads of a group (G = C B^T is
+// shared by the CTA's heads).
+int scan_heads_per_cta(const SsdTcArgs& s) {
+    const int hpg = (int)(s.H / s.G);
+    for (int cand : {8, 4, 2, 1})
+        if (hpg % cand == 0) return cand;
+    return 1;
+}
+
+template <int N, bool GATE, bool XS>
+cudaError_t launch_scan(const SsdTcArgs& s, int64_t batch, cudaStream_t stream) {
+    using Cfg = ScanCfg<N, XS>;
+    CUtensorMap tx, txl, tmc, tmb;
+    const uint64_t T = (uint64_t)s.T, nb = (uint64_t)batch;
+    if (!make_map(&tx, s.x, (uint64_t)s.H * kP, T, nb) || !make_map(&txl, XS ? s.x_lo : s.x, (uint64_t)s.H * kP, T, nb) ||
+        !make_map(&tmc, s.C, (uint64_t)s.G * N, T, nb) || !make_map(&tmb, s.B, (uint64_t)s.G * N, T, nb))
+        return cudaErrorInvalidValue;
+    int* status = nullptr;
+    cudaError_t e = device_status_address(&status);
+    if (e != cudaSuccess) return e;
+    auto kern = ssd_scan_tc<N, GATE, XS>;
+    static_assert(sizeof(ScanShared) <= 2304, "pipeline state");
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmemTotal);
+    if (e != cudaSuccess) return e;
+    const int hpc = scan_heads_per_cta(s);
+    const dim3 grid((unsigned)(s.nchunks * (s.Q / 128)), (unsigned)(s.H / hpc), (unsigned)batch);
+    cudaEvent_t t0 = timing_begin(stream);
+    kern<<<grid, kThreads, Cfg::kSmemTotal, stream>>>(s, hpc, status, tx, txl, tmc, tmb);
+    note_launch("ssd_scan_tc", stream, t0);
+    return cudaGetLastError();
+}
+
+template <bool GATE, bool XS>
+cudaError_t launch_scan_n(const SsdTcArgs& s, int64_t batch, cudaStream_t stream) {
+    switch (s.N) {
+        case 64: return launch_scan<64, GATE, XS>(s, batch, stream);
+        case 128: return launch_scan<128, GATE, XS>(s, batch, stream);
+        default: return launch_scan<256, GATE, XS>(s, batch, stream);
+    }
+}
+
+}  // namespace
+
+cudaError_t ssd_tc_chunk_scan(const SsdTcArgs& s, int64_t batch, bool gate, cudaStream_t stream) {
+    if (s.x_lo) return gate ? launch_scan_n<true, true>(s, batch, stream) : launch_scan_n<false, true>(s, batch, stream);
+    return gate ? launch_scan_n<true, false>(s, batch, stream) : launch_scan_n<false, false>(s, batch, stream);
+}
+
+}  // namespace ssm

@@ -27,7 +27,7 @@ struct SsdTcArgs {
 };
 
 // True when the shape is one the tensor-core kernels take (bf16, headdim 64,
-// dstate in {32, 64, 128, 256}, chunk 128 or 256, even heads per group).
+// dstate 64, 128 or 256, chunk 128 or 256, even heads per group).
 bool ssd_tc_supported(const ScanArgs& a, int64_t Q);
 
 // S_c for every (chunk, head) into states; also writes dl and cum.

@@ -87,6 +87,9 @@ cudaError_t conv_tail_launch(const ScanArgs& a, cudaStream_t stream);
 // Per-device status word of bounded device-side waits: read into *status (0 or
 // SSM_ERR_TIMEOUT) after the stream's work, cleared when `clear`.
 cudaError_t device_status_take(int* status, bool clear, cudaStream_t stream);
+// Device address of that status word for the current device (looked up once per device),
+// for kernels in other translation units, which record SSM_ERR_TIMEOUT through it.
+cudaError_t device_status_address(int** p);
 // One CTA waiting on an mbarrier that nothing completes, giving up after max_checks polls.
 cudaError_t bounded_wait_selftest_launch(uint32_t max_checks, cudaStream_t stream);
 

@@ -167,6 +167,52 @@ __device__ __forceinline__ void tmem_ld_async(uint32_t taddr, uint32_t (&r)[16])
 __device__ __forceinline__ void tmem_ld_async(uint32_t taddr, uint32_t (&r)[8]) { tmem_ld8_async(taddr, r); }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// ---- TMA (bulk asynchronous copies into shared memory, completion on an mbarrier)
+
+// Expect `bytes` more transaction bytes on `mbar` and arrive once (one thread).
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* mbar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(mbar)), "r"(bytes)
+                 : "memory");
+}
+
+// Tiled 3-D tensor copy global -> shared: the box of the tensor map at coordinates
+// (c0 innermost, c1, c2); elements outside the tensor are filled with zeros.  c0 times
+// the element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int c0, int c1, int c2, uint64_t* mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(mbar))
+        : "memory");
+}
+
+// Contiguous bulk copy global -> shared of `bytes` (16-byte aligned addresses, a
+// multiple of 16 bytes).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* mbar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(mbar))
+                 : "memory");
+}
+
+// Descriptor of a no-swizzle operand with explicit strides: lbo = bytes between core
+// matrices adjacent along K, sbo = along M/N (the layouts written by TMA boxes that are
+// 8 elements wide, one 16-byte core-matrix row per box row).
+__device__ __forceinline__ uint64_t desc_strided(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return make_desc(saddr, lbo, sbo);
+}
+
+// Descriptor of an operand in the 128-byte swizzle layout that TMA writes with
+// CU_TENSOR_MAP_SWIZZLE_128B (rows of 128 bytes, the 16-byte chunks of row r stored at
+// chunk ^ (r % 8), groups of 8 rows 1024 bytes apart; the region 1024-byte aligned).
+// K-major: 64 K-elements per row, K steps of 16 advance the start by 32 bytes inside a
+// row; sbo = 1024.  MN-major with 64 MN-elements per row: K steps of 16 rows advance
+// the start by 2048 bytes; the 8-row groups are 1024 bytes apart (lbo and sbo both 1024
+// here, since one 64-element row covers the whole MN extent).
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return make_desc(saddr, lbo, sbo) | ((uint64_t)2 << 61);
+}
+
 // TMEM address of (lane, column).
 __device__ __forceinline__ uint32_t taddr(uint32_t base, uint32_t lane, uint32_t col) {
     return base + (lane << 16) + col;
