@@ -16,9 +16,12 @@
 // canonical layout directly, h_{c-1} (already split hi/lo by the carry pass) as one
 // contiguous bulk copy.  Copies complete on mbarriers; every wait is bounded.
 //
-// One CTA of 16 warps per SM (512 TMEM columns: G, and two sets of Y accumulators so
-// that a head's epilogue overlaps the next head's MMAs).  Warp w owns TMEM lanes
-// 32*(w%4).. (rows) and the column quarter w/4 of each M' part.
+// One CTA per SM, warp-specialised: a TMA warp, an MMA warp and 16 compute warps that
+// build M' and run the epilogues, handing work over on mbarriers (M' parts double
+// buffered, x tiles and h tiles double buffered where they fit, two sets of Y
+// accumulators so that a head's epilogue overlaps the next head's MMAs).  512 TMEM
+// columns: G, and the two accumulator sets.  Compute warp w owns TMEM lanes 32*(w%4)..
+// (rows) and the column quarter w/4 of each M' part.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -36,7 +39,6 @@ namespace ssm {
 namespace {
 
 constexpr int kP = 64;            // headdim handled here
-constexpr int kThreads = 512;     // 16 warps
 constexpr int kStatusTimeout = 8;
 
 template <int N, bool XS>
@@ -75,22 +77,43 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
     asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d));
 }
 
-// Shared state of one CTA's pipeline.
+// Shared state of one CTA's pipeline (after the operand buffers in dynamic shared memory).
 struct __align__(16) ScanShared {
-    float cum[256];
-    float beta[256];   // log2(Delta_s) - cum_s log2(e): exp(cum_t - cum_s) Delta_s = 2^(alpha_t + beta_s)
-    uint64_t mb_load;  // C and B rows (prologue)
-    uint64_t mb_g;     // G's MMAs
-    uint64_t mb_mma[2];  // M' parts' MMAs: commit n on [n & 1], phase (n >> 1) & 1
-    uint64_t mb_x[2];  // x tiles (buffer i)
-    uint64_t mb_h[2];  // h_{c-1} tiles (set i)
+    float beta[2][256];     // per head parity: log2(Delta_s) - cum_s log2(e), so that
+                            // exp(cum_t - cum_s) Delta_s = 2^(alpha_t + beta_s)
+    uint64_t mb_load;       // C and B rows (prologue TMA)
+    uint64_t mb_g;          // G = C B^T in TMEM
+    uint64_t full_part[2];  // M' part built (one arrival per compute warp)
+    uint64_t empty_part[2]; // M' part consumed by its MMAs
+    uint64_t acc_full[2];   // a head's Y accumulators complete
+    uint64_t acc_empty[2];  // a head's Y accumulators read by the epilogue (one arrival per compute warp)
+    uint64_t x_full[2], x_empty[2];
+    uint64_t h_full[2], h_empty[2];
     uint32_t tmem;
-    int abort;         // a bounded wait gave up: every thread leaves at the next check
+    volatile int abort;     // a bounded wait gave up: every later wait returns at once
 };
 
-// grid (nchunks * Q/128, H / heads_per_cta, batch); 512 threads; one CTA per SM.
+constexpr int kComputeWarps = 16;
+constexpr int kMmaWarp = 16;
+constexpr int kLoadWarp = 17;
+constexpr int kCtaThreads = 32 * 18;
+
+// Bounded wait that gives up at once when another wait of the CTA already gave up.
+__device__ __forceinline__ void pipe_wait(ScanShared& sh, uint64_t* mb, uint32_t phase) {
+    if (sh.abort) return;
+    if (!tc::mbar_wait(mb, phase)) sh.abort = 1;
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* mb) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(mb)) : "memory");
+}
+// Named barrier of the compute warps only.
+__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
+
+// grid (nchunks * Q/128, H / heads_per_cta, batch); 18 warps; one CTA per SM.
+// Warps 0-15 build M' and run the epilogues (warp w: TMEM lanes 32*(w%4).., column
+// quarter w/4 of each part); warp 16 issues the MMAs; warp 17 issues the TMA copies.
 template <int N, bool GATE, bool XS>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kCtaThreads, 1)
     ssd_scan_tc(const SsdTcArgs a, const int heads_per_cta, int* status, const __grid_constant__ CUtensorMap tm_x,
                 const __grid_constant__ CUtensorMap tm_xlo, const __grid_constant__ CUtensorMap tm_c,
                 const __grid_constant__ CUtensorMap tm_b) {
@@ -110,9 +133,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int SW = t0 + 128;    // columns s of G this half needs (causal)
     const int nparts = SW / KPC;
     const int hbeg = blockIdx.y * heads_per_cta;
+    const int nh = heads_per_cta;
     const int g = hbeg / (int)(a.H / a.G);
     const int row0 = (int)(c * a.Q);  // first token of the chunk within its sequence
-    // XS with 256 rows: a head's two x planes take both x buffers (serial heads)
+    // XS with 256 rows: a head's two x planes take both x buffers (one head at a time)
     const bool xser = XS && SW > 128;
 
     // TMA-written operands use the 128-byte swizzle layout (rows of 64 elements):
@@ -128,9 +152,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mbar_init(&sh.mb_load, 1);
         tc::mbar_init(&sh.mb_g, 1);
         for (int i = 0; i < 2; ++i) {
-            tc::mbar_init(&sh.mb_mma[i], 1);
-            tc::mbar_init(&sh.mb_x[i], 1);
-            tc::mbar_init(&sh.mb_h[i], 1);
+            tc::mbar_init(&sh.full_part[i], kComputeWarps);
+            tc::mbar_init(&sh.empty_part[i], 1);
+            tc::mbar_init(&sh.acc_full[i], 1);
+            tc::mbar_init(&sh.acc_empty[i], kComputeWarps);
+            tc::mbar_init(&sh.x_full[i], 1);
+            tc::mbar_init(&sh.x_empty[i], 1);
+            tc::mbar_init(&sh.h_full[i], 1);
+            tc::mbar_init(&sh.h_empty[i], 1);
         }
         sh.abort = 0;
         tc::mbar_fence_init();
@@ -142,37 +171,115 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = sh.tmem;
     const uint32_t tG = tmem;
 
-    // ---- prologue: C rows of the half and B rows [0, SW) by TMA, then G = C B^T
-    if (tid == 0) {
-        tc::mbar_arrive_expect_tx(&sh.mb_load, Cfg::kC + (uint32_t)SW * N * 2);
-        for (int j = 0; j < N / 64; ++j) {
-            tc::tma_load_3d(sC + j * 128 * 128, &tm_c, g * N + 64 * j, row0 + t0, b, &sh.mb_load);
-            for (int rb = 0; rb < SW / 128; ++rb)
-                tc::tma_load_3d(sB + (j * SW + rb * 128) * 128, &tm_b, g * N + 64 * j, row0 + 128 * rb, b, &sh.mb_load);
-        }
-        bool ok = tc::mbar_wait(&sh.mb_load, 0);
-        tc::fence_after_sync();
-        if (ok) {
-            const uint32_t idesc = tc::idesc_bf16(128, SW, 0, 0);
-#pragma unroll 1
-            for (int ks = 0; ks < N / 16; ++ks) {
-                const uint32_t in_row = (uint32_t)(ks & 3) * 32;  // K offset inside a 128-byte row
-                const uint64_t da = tc::desc_sw128(tc::smem_u32(sC + (ks >> 2) * 128 * 128) + in_row, 16, 1024);
-                const uint64_t db = tc::desc_sw128(tc::smem_u32(sB + (ks >> 2) * SW * 128) + in_row, 16, 1024);
-                tc::mma_bf16(tG, da, db, idesc, ks > 0);
+    // Buffer schedule: x buffer and its use count for head hi (serial planes: buffer 0 every
+    // head); h set likewise.
+    auto xbuf = [&](int hi) { return xser ? 0 : (hi & 1); };
+    auto xuse = [&](int hi) { return xser ? hi : (hi >> 1); };
+    auto hbuf = [&](int hi) { return Cfg::kHBufs == 2 ? (hi & 1) : 0; };
+    auto huse = [&](int hi) { return Cfg::kHBufs == 2 ? (hi >> 1) : hi; };
+    auto x_tile = [&](int hi, int plane) -> uint32_t {
+        if (xser) return tc::smem_u32(sX + plane * Cfg::kX);
+        return tc::smem_u32(sX + (hi & 1) * Cfg::kX + plane * (uint32_t)SW * kP * 2);
+    };
+
+    if (warp == kLoadWarp) {
+        // ---- TMA producer (one thread)
+        if (lane == 0) {
+            tc::mbar_arrive_expect_tx(&sh.mb_load, Cfg::kC + (uint32_t)SW * N * 2);
+            for (int j = 0; j < N / 64; ++j) {
+                tc::tma_load_3d(sC + j * 128 * 128, &tm_c, g * N + 64 * j, row0 + t0, b, &sh.mb_load);
+                for (int rb = 0; rb < SW / 128; ++rb)
+                    tc::tma_load_3d(sB + (j * SW + rb * 128) * 128, &tm_b, g * N + 64 * j, row0 + 128 * rb, b, &sh.mb_load);
             }
-            tc::mma_commit(&sh.mb_g);
-        } else {
-            sh.abort = 1;
+            pipe_wait(sh, &sh.mb_g, 0);  // G's MMAs are done: B's region takes the head tiles
+            for (int hi = 0; hi < nh && !sh.abort; ++hi) {
+                const int hn = hbeg + hi;
+                const int xb = xbuf(hi), ux = xuse(hi);
+                if (ux > 0) pipe_wait(sh, &sh.x_empty[xb], (ux - 1) & 1);
+                const uint32_t planes = XS ? 2 : 1;
+                tc::mbar_arrive_expect_tx(&sh.x_full[xb], planes * (uint32_t)SW * kP * 2);
+                for (int pl = 0; pl < (int)planes; ++pl) {
+                    unsigned char* base = xser ? sX + pl * Cfg::kX : sX + xb * Cfg::kX + pl * (uint32_t)SW * kP * 2;
+                    const CUtensorMap* tm = pl ? &tm_xlo : &tm_x;
+                    for (int rb = 0; rb < SW / 128; ++rb)
+                        tc::tma_load_3d(base + rb * 128 * 128, tm, hn * kP, row0 + 128 * rb, b, &sh.x_full[xb]);
+                }
+                const int hs = hbuf(hi), uh = huse(hi);
+                if (uh > 0) pipe_wait(sh, &sh.h_empty[hs], (uh - 1) & 1);
+                const unsigned char* src = reinterpret_cast<const unsigned char*>(
+                    a.states + (((int64_t)b * a.nchunks + c) * a.H + hn) * (int64_t)kP * N);
+                tc::mbar_arrive_expect_tx(&sh.h_full[hs], 2 * Cfg::kH);
+                tc::bulk_load(sH + hs * 2 * Cfg::kH, src, 2 * Cfg::kH, &sh.h_full[hs]);
+            }
         }
-    }
-    __syncthreads();
-    if (sh.abort) goto teardown;
-    if (!tc::mbar_wait(&sh.mb_g, 0)) sh.abort = 1;  // every thread: G is in TMEM, B's region is free
-    tc::fence_after_sync();
-    __syncthreads();
-    if (sh.abort) goto teardown;
-    {
+    } else if (warp == kMmaWarp) {
+        // ---- MMA issuer (one thread)
+        if (lane == 0) {
+            pipe_wait(sh, &sh.mb_load, 0);
+            tc::fence_after_sync();
+            if (!sh.abort) {
+                const uint32_t idesc = tc::idesc_bf16(128, SW, 0, 0);
+#pragma unroll 1
+                for (int ks = 0; ks < N / 16; ++ks) {
+                    const uint32_t in_row = (uint32_t)(ks & 3) * 32;  // K offset inside a 128-byte row
+                    const uint64_t da = tc::desc_sw128(tc::smem_u32(sC + (ks >> 2) * 128 * 128) + in_row, 16, 1024);
+                    const uint64_t db = tc::desc_sw128(tc::smem_u32(sB + (ks >> 2) * SW * 128) + in_row, 16, 1024);
+                    tc::mma_bf16(tG, da, db, idesc, ks > 0);
+                }
+                tc::mma_commit(&sh.mb_g);
+            }
+            constexpr uint32_t id_diag = tc::idesc_bf16(128, kP, 0, 1);
+            constexpr uint32_t id_off = tc::idesc_bf16(128, kP, 0, 0);
+            uint32_t n = 0;  // M' parts consumed so far
+            for (int hi = 0; hi < nh && !sh.abort; ++hi) {
+                const int ab = hi & 1;
+                const uint32_t tYd = tmem + 256 + 128 * ab, tYo = tYd + 64;
+                if (hi >= 2) pipe_wait(sh, &sh.acc_empty[ab], ((hi - 2) >> 1) & 1);  // head hi-2's epilogue read them
+                pipe_wait(sh, &sh.x_full[xbuf(hi)], xuse(hi) & 1);
+                pipe_wait(sh, &sh.h_full[hbuf(hi)], huse(hi) & 1);
+                tc::fence_after_sync();
+                for (int kp = 0; kp < nparts && !sh.abort; ++kp, ++n) {
+                    const uint32_t pb = n & 1;
+                    pipe_wait(sh, &sh.full_part[pb], (n >> 1) & 1);
+                    tc::fence_after_sync();
+                    if (sh.abort) break;
+                    const uint32_t mh = tc::smem_u32(sM + pb * 2 * Cfg::kMPart);
+                    const uint64_t dmh = tc::desc_strided(mh, 128, (KPC / 8) * 128);
+                    const uint64_t dml = tc::desc_strided(mh + Cfg::kMPart, 128, (KPC / 8) * 128);
+                    // x: rows s of this part, 128 bytes each; K steps of 16 rows are 2048
+                    // bytes (128 in descriptor units) apart
+                    const uint64_t dx = tc::desc_sw128(x_tile(hi, 0) + (uint32_t)(kp * KPC) * 128, 1024, 1024);
+#pragma unroll
+                    for (int ks = 0; ks < KPC / 16; ++ks)
+                        tc::mma_bf16(tYd, dmh + ks * 16u, dx + ks * 128u, id_diag, (kp > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
+                    for (int ks = 0; ks < KPC / 16; ++ks) tc::mma_bf16(tYd, dml + ks * 16u, dx + ks * 128u, id_diag, 1u);
+                    if (XS) {
+                        const uint64_t dxl = tc::desc_sw128(x_tile(hi, 1) + (uint32_t)(kp * KPC) * 128, 1024, 1024);
+#pragma unroll
+                        for (int ks = 0; ks < KPC / 16; ++ks) tc::mma_bf16(tYd, dmh + ks * 16u, dxl + ks * 128u, id_diag, 1u);
+                    }
+                    if (kp == 0) {
+                        const uint32_t cb = tc::smem_u32(sC);
+                        const uint32_t hs = tc::smem_u32(sH + hbuf(hi) * 2 * Cfg::kH);
+                        const uint64_t dhh = tc::desc_strided(hs, 128, (N / 8) * 128);
+                        const uint64_t dhl = tc::desc_strided(hs + Cfg::kH, 128, (N / 8) * 128);
+#pragma unroll
+                        for (int ks = 0; ks < N / 16; ++ks) {
+                            const uint64_t dc = tc::desc_sw128(cb + (uint32_t)(ks >> 2) * 128 * 128 + (uint32_t)(ks & 3) * 32, 16, 1024);
+                            tc::mma_bf16(tYo, dc, dhh + ks * 16u, id_off, ks > 0 ? 1u : 0u);
+                            tc::mma_bf16(tYo, dc, dhl + ks * 16u, id_off, 1u);
+                        }
+                        tc::mma_commit(&sh.h_empty[hbuf(hi)]);  // the h tiles may be replaced
+                    }
+                    tc::mma_commit(&sh.empty_part[pb]);         // the part buffer may be rebuilt
+                }
+                tc::mma_commit(&sh.acc_full[ab]);   // the epilogue may read this head's accumulators
+                tc::mma_commit(&sh.x_empty[xbuf(hi)]);
+            }
+        }
+    } else {
+        // ---- compute warps: M' builds and epilogues
         const int q = warp & 3;             // TMEM lane quarter
         const int cq = warp >> 2;           // column quarter of a part
         const int r = q * 32 + lane;        // row (TMEM lane) within the half
@@ -181,78 +288,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         const int t_warp_min = t0 + q * 32;  // tcgen05.ld and the part blocks are per warp
         const int t_warp_max = t_warp_min + 31;
-
-        // x tile of head hn -> buffer xb (xser: hi in buffer 0, lo in buffer 1)
-        auto load_x = [&](int hn, int xb) {
-            const uint32_t planes = XS ? 2 : 1;
-            uint64_t* mb = &sh.mb_x[xser ? 0 : xb];
-            tc::mbar_arrive_expect_tx(mb, planes * (uint32_t)SW * kP * 2);
-            for (int pl = 0; pl < (int)planes; ++pl) {
-                unsigned char* base = xser ? sX + pl * Cfg::kX : sX + xb * Cfg::kX + pl * (uint32_t)SW * kP * 2;
-                const CUtensorMap* tm = pl ? &tm_xlo : &tm_x;
-                for (int rb = 0; rb < SW / 128; ++rb)
-                    tc::tma_load_3d(base + rb * 128 * 128, tm, hn * kP, row0 + 128 * rb, b, mb);
-            }
-        };
-        // h_{c-1} of head hn (hi and lo tiles, contiguous) -> set hs
-        auto load_h = [&](int hn, int hs) {
-            const unsigned char* src = reinterpret_cast<const unsigned char*>(
-                a.states + (((int64_t)b * a.nchunks + c) * a.H + hn) * (int64_t)kP * N);
-            tc::mbar_arrive_expect_tx(&sh.mb_h[hs], 2 * Cfg::kH);
-            tc::bulk_load(sH + hs * 2 * Cfg::kH, src, 2 * Cfg::kH, &sh.mb_h[hs]);
-        };
-        auto x_tile = [&](int hi_, int plane) -> uint32_t {
-            if (xser) return tc::smem_u32(sX + plane * Cfg::kX);
-            return tc::smem_u32(sX + (hi_ & 1) * Cfg::kX + plane * (uint32_t)SW * kP * 2);
-        };
-
-        if (tid == 0) {
-            load_x(hbeg, 0);
-            load_h(hbeg, 0);
-        }
-
-        // MMA commits are numbered; commit n arrives on mb_mma[n & 1], phase (n >> 1) & 1.
-        // A wait is only ever on one of the latest two commits.
-        uint32_t ncommit = 0;
-        auto wait_commit = [&](uint32_t n) {
-            if (!tc::mbar_wait(&sh.mb_mma[n & 1], (n >> 1) & 1)) sh.abort = 1;
-            tc::fence_after_sync();
-        };
-        // epilogue of head hh from accumulator set acc: out = Y_diag + exp(cum_t) Y_off, gate
-        auto finish = [&](int hh, int acc, float alpha_h) {
-            const uint32_t tYd = tmem + 256 + 128 * acc, tYo = tYd + 64;
-            const int p0 = 16 * cq;
-            uint32_t yd[16], yo[16];
-            tc::tmem_ld16_async(tYd + lane_base + (uint32_t)p0, yd);
-            tc::tmem_ld16_async(tYo + lane_base + (uint32_t)p0, yo);
-            tc::tmem_wait_ld();
-            if (!row_ok) return;
-            const float e = ex2(alpha_h);
-            const int64_t row = (((int64_t)b * a.T + row0 + t) * a.H + hh) * kP + p0;
-            uint4 zr[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
-            if (GATE) {
-                zr[0] = *reinterpret_cast<const uint4*>(a.z + row);
-                zr[1] = *reinterpret_cast<const uint4*>(a.z + row + 8);
-            }
-            const __nv_bfloat162* z2 = reinterpret_cast<const __nv_bfloat162*>(zr);
-            uint32_t pk[8];
-#pragma unroll
-            for (int j = 0; j < 16; j += 2) {
-                float2 y = __ffma2_rn(make_float2(e, e), make_float2(__uint_as_float(yo[j]), __uint_as_float(yo[j + 1])),
-                                      make_float2(__uint_as_float(yd[j]), __uint_as_float(yd[j + 1])));
-                if (GATE) y = __fmul2_rn(y, silu2_fma(__bfloat1622float2(z2[j / 2])));
-                pk[j / 2] = pack_bf16x2(y.x, y.y);
-            }
-            uint4* dst = reinterpret_cast<uint4*>(a.out + row);
-            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-        };
-
-        // Build this thread's BC columns of M' part kp for head hh into part buffer pb:
-        // row t, columns s0 .. s0 + BC - 1.  Blocks wholly above the diagonal are zero;
-        // blocks that reach it are masked and take D on the diagonal.
         const uint32_t row_off = (uint32_t)((r >> 3) * (KPC / 8) * 128 + (r & 7) * 16);
-        auto build = [&](int kp, int pb, float alpha, float Dh) {
+        const int tq = min(t, Q - 1);
+
+        // per-head scalars: Delta and the cumulative sum of row tid (for beta), the
+        // cumulative sum of this thread's row (alpha), D; fetched a head ahead
+        float pf_dl = 0.0f, pf_cum = 0.0f, pf_row = 0.0f, pf_D = 0.0f;
+        auto prefetch = [&](int hn) {
+            const int64_t base = (((int64_t)b * a.H + hn) * a.nchunks + c) * a.Q;
+            if (tid < Q) {
+                pf_dl = a.dl[base + tid];
+                pf_cum = a.cum[base + tid];
+            }
+            pf_row = a.cum[base + tq];
+            pf_D = a.D ? a.D[hn] : 0.0f;
+        };
+        auto publish_beta = [&](int parity) {
+            if (tid < Q) sh.beta[parity][tid] = (pf_dl > 0.0f ? lg2(pf_dl) : -INFINITY) - pf_cum * kLog2e;
+        };
+        prefetch(hbeg);
+        publish_beta(0);
+        float cur_alpha = pf_row * kLog2e, cur_D = pf_D;  // head hbeg
+        if (nh > 1) prefetch(hbeg + 1);
+
+        // this thread's BC columns of M' part kp into part buffer pb: row t, columns
+        // s0 .. s0 + BC - 1.  Blocks wholly above the diagonal are zero; blocks that reach
+        // it are masked and take D on the diagonal.
+        auto build = [&](int kp, int pb, const float* beta, float alpha, float Dh) {
             const int s0 = KPC * kp + BC * cq;
             uint32_t hw[BC / 2], lw[BC / 2];
             if (s0 > t_warp_max) {
@@ -263,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::tmem_ld_async(tG + lane_base + (uint32_t)s0, gv);
                 float bt[BC];
 #pragma unroll
-                for (int j = 0; j < BC; j += 4) *reinterpret_cast<float4*>(&bt[j]) = *reinterpret_cast<const float4*>(&sh.beta[s0 + j]);
+                for (int j = 0; j < BC; j += 4) *reinterpret_cast<float4*>(&bt[j]) = *reinterpret_cast<const float4*>(&beta[s0 + j]);
                 tc::tmem_wait_ld();
                 const bool diag = s0 + BC - 1 >= t_warp_min;  // some column reaches some row of the warp
                 const float2 al = make_float2(alpha, alpha);
@@ -289,122 +351,72 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         };
 
-        // Delta, cumulative sum and D of the next head, fetched a head ahead
-        float pf_dl = 0.0f, pf_cum = 0.0f, pf_D = 0.0f;
-        auto prefetch = [&](int hn) {
-            if (tid < Q) {
-                const int64_t o = (((int64_t)b * a.H + hn) * a.nchunks + c) * a.Q + tid;
-                pf_dl = a.dl[o];
-                pf_cum = a.cum[o];
+        // epilogue of head hi (accumulator set hi & 1): out = Y_diag + exp(cum_t) Y_off, gate
+        auto finish = [&](int hi, float alpha_h) {
+            const int ab = hi & 1;
+            pipe_wait(sh, &sh.acc_full[ab], (hi >> 1) & 1);
+            tc::fence_after_sync();
+            const uint32_t tYd = tmem + 256 + 128 * ab, tYo = tYd + 64;
+            const int p0 = 16 * cq;
+            uint32_t yd[16], yo[16];
+            tc::tmem_ld16_async(tYd + lane_base + (uint32_t)p0, yd);
+            tc::tmem_ld16_async(tYo + lane_base + (uint32_t)p0, yo);
+            tc::tmem_wait_ld();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.acc_empty[ab]);  // the MMAs of head hi + 2 may overwrite them
+            if (!row_ok || sh.abort) return;
+            const float e = ex2(alpha_h);
+            const int64_t row = (((int64_t)b * a.T + row0 + t) * a.H + hbeg + hi) * kP + p0;
+            uint4 zr[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+            if (GATE) {
+                zr[0] = *reinterpret_cast<const uint4*>(a.z + row);
+                zr[1] = *reinterpret_cast<const uint4*>(a.z + row + 8);
             }
-            pf_D = a.D ? a.D[hn] : 0.0f;
+            const __nv_bfloat162* z2 = reinterpret_cast<const __nv_bfloat162*>(zr);
+            uint32_t pk[8];
+#pragma unroll
+            for (int j = 0; j < 16; j += 2) {
+                float2 y = __ffma2_rn(make_float2(e, e), make_float2(__uint_as_float(yo[j]), __uint_as_float(yo[j + 1])),
+                                      make_float2(__uint_as_float(yd[j]), __uint_as_float(yd[j + 1])));
+                if (GATE) y = __fmul2_rn(y, silu2_fma(__bfloat1622float2(z2[j / 2])));
+                pk[j / 2] = pack_bf16x2(y.x, y.y);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(a.out + row);
+            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
         };
-        prefetch(hbeg);
 
-        uint32_t last_commit_prev = 0;  // the previous head's last commit
+        pipe_wait(sh, &sh.mb_g, 0);  // G is in TMEM
+        tc::fence_after_sync();
+        uint32_t n = 0;  // M' parts built so far
         float alpha_prev = 0.0f;
-        for (int hi = 0; hi < heads_per_cta; ++hi) {
-            const int h = hbeg + hi;
-            // every thread is past the previous head's builds before cum / beta change
-            __syncthreads();
-            if (sh.abort) break;
-            if (tid < Q) {
-                sh.cum[tid] = pf_cum;
-                sh.beta[tid] = (pf_dl > 0.0f ? lg2(pf_dl) : -INFINITY) - pf_cum * kLog2e;
+        for (int hi = 0; hi < nh; ++hi) {
+            // every compute warp is done with head hi-1's builds (so the beta buffer of
+            // head hi + 1 is free) and head hi's beta is visible
+            compute_sync();
+            const float alpha = cur_alpha, Dh = cur_D;
+            if (hi + 1 < nh) {
+                publish_beta((hi + 1) & 1);
+                cur_alpha = pf_row * kLog2e;
+                cur_D = pf_D;
+                if (hi + 2 < nh) prefetch(hbeg + hi + 2);
             }
-            const float Dh = pf_D;
-            if (hi + 1 < heads_per_cta) prefetch(h + 1);
-            __syncthreads();
-            const float alpha = sh.cum[min(t, Q - 1)] * kLog2e;
-            for (int kp = 0; kp < nparts; ++kp) {
-                // this part's buffer was last used by commit ncommit - 2
-                if (ncommit >= 2) wait_commit(ncommit - 2);
-                // one h set: part 0's MMAs (the last readers of this head's h tiles) are
-                // done once commit ncommit - 2 has arrived at part 2
-                if (Cfg::kHBufs == 1 && kp == 2 && hi + 1 < heads_per_cta && tid == 0) load_h(h + 1, 0);
-                build(kp, ncommit & 1, alpha, Dh);
-                tc::fence_async_smem();
-                tc::fence_before_sync();
-                __syncthreads();
-                if (sh.abort) break;
+            const float* beta = sh.beta[hi & 1];
+            for (int kp = 0; kp < nparts; ++kp, ++n) {
+                const uint32_t pb = n & 1;
+                if (n >= 2) pipe_wait(sh, &sh.empty_part[pb], ((n - 2) >> 1) & 1);
                 tc::fence_after_sync();
-                if (tid == 0) {
-                    bool ok = true;
-                    if (kp == 0) {
-                        // this head's x and h tiles have landed
-                        ok = tc::mbar_wait(&sh.mb_x[xser ? 0 : (hi & 1)], xser ? (hi & 1) : ((hi >> 1) & 1));
-                        ok = ok && tc::mbar_wait(&sh.mb_h[Cfg::kHBufs == 2 ? (hi & 1) : 0],
-                                                 Cfg::kHBufs == 2 ? ((hi >> 1) & 1) : (hi & 1));
-                        tc::fence_after_sync();
-                    }
-                    if (ok) {
-                        const uint32_t pb = ncommit & 1;
-                        const uint32_t tYd = tmem + 256 + 128 * (hi & 1), tYo = tYd + 64;
-                        constexpr uint32_t id_diag = tc::idesc_bf16(128, kP, 0, 1);
-                        const uint32_t mh = tc::smem_u32(sM + pb * 2 * Cfg::kMPart);
-                        const uint64_t dmh = tc::desc_strided(mh, 128, (KPC / 8) * 128);
-                        const uint64_t dml = tc::desc_strided(mh + Cfg::kMPart, 128, (KPC / 8) * 128);
-                        // x: rows s of this part, 128 bytes each; K steps of 16 rows are 2048
-                        // bytes (128 in descriptor units) apart
-                        const uint64_t dx = tc::desc_sw128(x_tile(hi, 0) + (uint32_t)(kp * KPC) * 128, 1024, 1024);
-#pragma unroll
-                        for (int ks = 0; ks < KPC / 16; ++ks)
-                            tc::mma_bf16(tYd, dmh + ks * 16u, dx + ks * 128u, id_diag, (kp > 0 || ks > 0) ? 1u : 0u);
-#pragma unroll
-                        for (int ks = 0; ks < KPC / 16; ++ks) tc::mma_bf16(tYd, dml + ks * 16u, dx + ks * 128u, id_diag, 1u);
-                        if (XS) {
-                            const uint64_t dxl = tc::desc_sw128(x_tile(hi, 1) + (uint32_t)(kp * KPC) * 128, 1024, 1024);
-#pragma unroll
-                            for (int ks = 0; ks < KPC / 16; ++ks) tc::mma_bf16(tYd, dmh + ks * 16u, dxl + ks * 128u, id_diag, 1u);
-                        }
-                        if (kp == 0) {
-                            constexpr uint32_t id_off = tc::idesc_bf16(128, kP, 0, 0);
-                            const uint32_t cb = tc::smem_u32(sC);
-                            const uint32_t hs = tc::smem_u32(sH + (Cfg::kHBufs == 2 ? (hi & 1) : 0) * 2 * Cfg::kH);
-                            const uint64_t dhh = tc::desc_strided(hs, 128, (N / 8) * 128);
-                            const uint64_t dhl = tc::desc_strided(hs + Cfg::kH, 128, (N / 8) * 128);
-#pragma unroll
-                            for (int ks = 0; ks < N / 16; ++ks) {
-                                const uint64_t dc = tc::desc_sw128(cb + (uint32_t)(ks >> 2) * 128 * 128 + (uint32_t)(ks & 3) * 32, 16, 1024);
-                                tc::mma_bf16(tYo, dc, dhh + ks * 16u, id_off, ks > 0 ? 1u : 0u);
-                                tc::mma_bf16(tYo, dc, dhl + ks * 16u, id_off, 1u);
-                            }
-                        }
-                        tc::mma_commit(&sh.mb_mma[ncommit & 1]);
-                    } else {
-                        sh.abort = 1;
-                    }
-                }
-                ++ncommit;
-                if (kp == 0) {
-                    // the previous head's epilogue, once this head's first MMAs are queued;
-                    // then its buffers take the next head's tiles
-                    if (hi > 0) {
-                        wait_commit(last_commit_prev);
-                        finish(h - 1, (hi - 1) & 1, alpha_prev);
-                        tc::fence_before_sync();
-                    }
-                    if (hi + 1 < heads_per_cta && tid == 0 && !sh.abort) {
-                        if (!xser) load_x(h + 1, (hi + 1) & 1);
-                        if (Cfg::kHBufs == 2) load_h(h + 1, (hi + 1) & 1);
-                    }
-                }
-                // serial planes: both x buffers are free once this head's last MMAs are done
-                if (xser && kp == nparts - 1 && hi + 1 < heads_per_cta && tid == 0) {
-                    wait_commit(ncommit - 1);
-                    if (!sh.abort) load_x(h + 1, 0);
-                }
+                build(kp, pb, beta, alpha, Dh);
+                tc::fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.full_part[pb]);
             }
-            last_commit_prev = ncommit - 1;
+            if (hi > 0) finish(hi - 1, alpha_prev);
             alpha_prev = alpha;
         }
-        __syncthreads();
-        if (!sh.abort && heads_per_cta > 0) {
-            wait_commit(last_commit_prev);
-            finish(hbeg + heads_per_cta - 1, (heads_per_cta - 1) & 1, alpha_prev);
-        }
+        if (nh > 0) finish(nh - 1, alpha_prev);
     }
-teardown:
     if (sh.abort && tid == 0) atomicExch(status, kStatusTimeout);
     tc::fence_before_sync();
     __syncthreads();
@@ -469,7 +481,7 @@ cudaError_t launch_scan(const SsdTcArgs& s, int64_t batch, cudaStream_t stream) 
     const int hpc = scan_heads_per_cta(s);
     const dim3 grid((unsigned)(s.nchunks * (s.Q / 128)), (unsigned)(s.H / hpc), (unsigned)batch);
     cudaEvent_t t0 = timing_begin(stream);
-    kern<<<grid, kThreads, Cfg::kSmemTotal, stream>>>(s, hpc, status, tx, txl, tmc, tmb);
+    kern<<<grid, kCtaThreads, Cfg::kSmemTotal, stream>>>(s, hpc, status, tx, txl, tmc, tmb);
     note_launch("ssd_scan_tc", stream, t0);
     return cudaGetLastError();
 }
