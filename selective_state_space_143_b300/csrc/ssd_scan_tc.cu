@@ -327,19 +327,25 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
 #pragma unroll
                 for (int j = 0; j < BC; j += 4) *reinterpret_cast<float4*>(&bt[j]) = *reinterpret_cast<const float4*>(&beta[s0 + j]);
                 tc::tmem_wait_ld();
-                const bool diag = s0 + BC - 1 >= t_warp_min;  // some column reaches some row of the warp
-                const float2 al = make_float2(alpha, alpha);
+                if (s0 + BC - 1 < t_warp_min) {
+                    // every column of the block lies left of every row's diagonal
 #pragma unroll
-                for (int j = 0; j < BC; j += 2) {
-                    const float2 ar = __fadd2_rn(al, make_float2(bt[j], bt[j + 1]));
-                    float2 v = __fmul2_rn(make_float2(ex2(ar.x), ex2(ar.y)),
-                                          make_float2(__uint_as_float(gv[j]), __uint_as_float(gv[j + 1])));
-                    if (diag) {
-                        const int s = s0 + j;
-                        v.x = s < t ? v.x : (s == t ? v.x + Dh : 0.0f);
-                        v.y = s + 1 < t ? v.y : (s + 1 == t ? v.y + Dh : 0.0f);
+                    for (int j = 0; j < BC; j += 2) {
+                        const float v0 = ex2(alpha + bt[j]) * __uint_as_float(gv[j]);
+                        const float v1 = ex2(alpha + bt[j + 1]) * __uint_as_float(gv[j + 1]);
+                        split_pair(v0, v1, hw[j / 2], lw[j / 2]);
                     }
-                    split_pair(v.x, v.y, hw[j / 2], lw[j / 2]);
+                } else {
+                    // the block reaches the diagonal: zero right of it, D on it
+                    const int dg = t - s0;
+#pragma unroll
+                    for (int j = 0; j < BC; j += 2) {
+                        float v0 = ex2(alpha + bt[j]) * __uint_as_float(gv[j]);
+                        float v1 = ex2(alpha + bt[j + 1]) * __uint_as_float(gv[j + 1]);
+                        v0 = j < dg ? v0 : (j == dg ? v0 + Dh : 0.0f);
+                        v1 = j + 1 < dg ? v1 : (j + 1 == dg ? v1 + Dh : 0.0f);
+                        split_pair(v0, v1, hw[j / 2], lw[j / 2]);
+                    }
                 }
             }
             const uint32_t ph = tc::smem_u32(sM + pb * 2 * Cfg::kMPart) + row_off + (uint32_t)(cq * BC / 8) * 128;
@@ -454,13 +460,17 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t T, uint
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Heads per CTA: the largest of 8, 4, 2 that divides the heads of a group (G = C B^T is
-// shared by the CTA's heads).
-int scan_heads_per_cta(const SsdTcArgs& s) {
+// Heads per CTA: G = C B^T and the C and B rows are shared by the CTA's heads, and each
+// CTA pays a prologue (the C and B copies, G's MMAs) that nothing overlaps, so a CTA takes
+// as many heads of its group as keep at least six waves of CTAs on the GPU (up to 32).
+int scan_heads_per_cta(const SsdTcArgs& s, int64_t batch) {
     const int hpg = (int)(s.H / s.G);
-    for (int cand : {8, 4, 2, 1})
-        if (hpg % cand == 0) return cand;
-    return 1;
+    const int64_t halves = s.nchunks * (s.Q / 128) * batch;
+    const int64_t want = 6 * (int64_t)sm_count();
+    int best = 1;
+    for (int cand : {1, 2, 4, 8, 16, 32})
+        if (hpg % cand == 0 && (cand == 1 || halves * (s.H / cand) >= want)) best = cand;
+    return best;
 }
 
 template <int N, bool GATE, bool XS>
@@ -478,7 +488,7 @@ cudaError_t launch_scan(const SsdTcArgs& s, int64_t batch, cudaStream_t stream) 
     static_assert(sizeof(ScanShared) <= 2304, "pipeline state");
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmemTotal);
     if (e != cudaSuccess) return e;
-    const int hpc = scan_heads_per_cta(s);
+    const int hpc = scan_heads_per_cta(s, batch);
     const dim3 grid((unsigned)(s.nchunks * (s.Q / 128)), (unsigned)(s.H / hpc), (unsigned)batch);
     cudaEvent_t t0 = timing_begin(stream);
     kern<<<grid, kCtaThreads, Cfg::kSmemTotal, stream>>>(s, hpc, status, tx, txl, tmc, tmb);
