@@ -21,7 +21,7 @@
 // buffered, x tiles and h tiles double buffered where they fit, two sets of Y
 // accumulators so that a head's epilogue overlaps the next head's MMAs).  512 TMEM
 // columns: G, and the two accumulator sets.  Compute warp w owns TMEM lanes 32*(w%4)..
-// (rows) and the column quarter w/4 of each M' part.
+// (rows) and 16 columns of the M' parts it builds.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -45,14 +45,20 @@ template <int N, bool XS>
 struct ScanCfg {
     static_assert(N % 64 == 0, "C and B rows are 128-byte swizzle rows of 64 elements");
     static constexpr int KPC = N > 128 ? 32 : 64;           // columns of M' per K-part
-    static constexpr int BC = KPC / 4;                       // columns of a part per warp
+    static constexpr int BC = 16;                            // columns of a part per warp
+    static constexpr int NCG = KPC / BC;                     // column groups of a part (4 or 2)
+    static constexpr int NG = 4 / NCG;                       // warp groups taking alternate parts
+    static constexpr int kPartWarps = 4 * NCG;               // warps that build one part
     static constexpr uint32_t kC = 128u * N * 2;             // C rows of the half
     static constexpr uint32_t kB = 256u * N * 2;             // B rows [0, SW), prologue only
     static constexpr uint32_t kMPart = 128u * KPC * 2;       // one M' part, hi or lo
     static constexpr uint32_t kX = 256u * kP * 2;            // one x buffer (256 rows)
     static constexpr uint32_t kH = (uint32_t)kP * N * 2;     // one h_{c-1} tile, hi or lo
-    static constexpr int kHBufs = N <= 128 ? 2 : 1;          // (hi, lo) tile sets
-    static constexpr uint32_t kPhase2 = 4 * kMPart + 2 * kX + kHBufs * 2 * kH;
+    // M' parts in flight (a ring of builds ahead of the MMAs) and h_{c-1} tile sets, as
+    // shared memory allows: three parts and one h set up to dstate 128, two and one at 256
+    static constexpr int kParts = N <= 128 ? 3 : 2;
+    static constexpr int kHBufs = 1;
+    static constexpr uint32_t kPhase2 = kParts * 2 * kMPart + 2 * kX + kHBufs * 2 * kH;
     static constexpr uint32_t kRegion = kB > kPhase2 ? kB : kPhase2;
     static constexpr uint32_t kSmem = kC + kRegion;   // operands; the pipeline state follows
     static constexpr uint32_t kSmemTotal = kSmem + 2304;
@@ -83,8 +89,8 @@ struct __align__(16) ScanShared {
                             // exp(cum_t - cum_s) Delta_s = 2^(alpha_t + beta_s)
     uint64_t mb_load;       // C and B rows (prologue TMA)
     uint64_t mb_g;          // G = C B^T in TMEM
-    uint64_t full_part[2];  // M' part built (one arrival per compute warp)
-    uint64_t empty_part[2]; // M' part consumed by its MMAs
+    uint64_t full_part[3];  // M' part built (one arrival per building warp)
+    uint64_t empty_part[3]; // M' part consumed by its MMAs
     uint64_t acc_full[2];   // a head's Y accumulators complete
     uint64_t acc_empty[2];  // a head's Y accumulators read by the epilogue (one arrival per compute warp)
     uint64_t x_full[2], x_empty[2];
@@ -118,7 +124,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
                 const __grid_constant__ CUtensorMap tm_xlo, const __grid_constant__ CUtensorMap tm_c,
                 const __grid_constant__ CUtensorMap tm_b) {
     using Cfg = ScanCfg<N, XS>;
-    constexpr int KPC = Cfg::KPC, BC = Cfg::BC;
+    constexpr int KPC = Cfg::KPC, BC = Cfg::BC, NCG = Cfg::NCG, NG = Cfg::NG;
     extern __shared__ __align__(1024) unsigned char smem[];
     ScanShared& sh = *reinterpret_cast<ScanShared*>(smem + Cfg::kSmem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -144,16 +150,20 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
     unsigned char* region = smem + Cfg::kC;
     unsigned char* sB = region;                             // [n/64][s SW][64], K-major B (prologue)
     // thread- and carry-written operands use the no-swizzle core-matrix layout:
-    unsigned char* sM = region;                             // [part 2][hi, lo] [t/8][s/8 of KPC][8][8]
-    unsigned char* sX = region + 4 * Cfg::kMPart;           // [buffer 2] [s SW][64] (+ lo plane), MN-major B
+    unsigned char* sM = region;                             // [part kParts][hi, lo] [t/8][s/8 of KPC][8][8]
+    unsigned char* sX = region + Cfg::kParts * 2 * Cfg::kMPart;  // [buffer 2] [s SW][64] (+ lo plane), MN-major B
     unsigned char* sH = sX + 2 * Cfg::kX;                   // [set kHBufs][hi, lo] [p/8][n/8][8][8]
 
     if (tid == 0) {
         tc::mbar_init(&sh.mb_load, 1);
         tc::mbar_init(&sh.mb_g, 1);
         for (int i = 0; i < 2; ++i) {
-            tc::mbar_init(&sh.full_part[i], kComputeWarps);
+            tc::mbar_init(&sh.full_part[i], Cfg::kPartWarps);
             tc::mbar_init(&sh.empty_part[i], 1);
+            if (i == 0 && Cfg::kParts == 3) {
+                tc::mbar_init(&sh.full_part[2], Cfg::kPartWarps);
+                tc::mbar_init(&sh.empty_part[2], 1);
+            }
             tc::mbar_init(&sh.acc_full[i], 1);
             tc::mbar_init(&sh.acc_empty[i], kComputeWarps);
             tc::mbar_init(&sh.x_full[i], 1);
@@ -239,8 +249,8 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
                 pipe_wait(sh, &sh.h_full[hbuf(hi)], huse(hi) & 1);
                 tc::fence_after_sync();
                 for (int kp = 0; kp < nparts && !sh.abort; ++kp, ++n) {
-                    const uint32_t pb = n & 1;
-                    pipe_wait(sh, &sh.full_part[pb], (n >> 1) & 1);
+                    const uint32_t pb = n % Cfg::kParts;
+                    pipe_wait(sh, &sh.full_part[pb], (n / Cfg::kParts) & 1);
                     tc::fence_after_sync();
                     if (sh.abort) break;
                     const uint32_t mh = tc::smem_u32(sM + pb * 2 * Cfg::kMPart);
@@ -281,7 +291,9 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
     } else {
         // ---- compute warps: M' builds and epilogues
         const int q = warp & 3;             // TMEM lane quarter
-        const int cq = warp >> 2;           // column quarter of a part
+        const int cq = warp >> 2;           // column quarter of the epilogue's outputs
+        const int cg = (warp >> 2) % NCG;   // column group of a part
+        const int gi = warp / (4 * NCG);    // warp group: builds the parts kp with kp % NG == gi
         const int r = q * 32 + lane;        // row (TMEM lane) within the half
         const int t = t0 + r;               // row within the chunk
         const bool row_ok = t < len;
@@ -315,7 +327,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
         // s0 .. s0 + BC - 1.  Blocks wholly above the diagonal are zero; blocks that reach
         // it are masked and take D on the diagonal.
         auto build = [&](int kp, int pb, const float* beta, float alpha, float Dh) {
-            const int s0 = KPC * kp + BC * cq;
+            const int s0 = KPC * kp + BC * cg;
             uint32_t hw[BC / 2], lw[BC / 2];
             if (s0 > t_warp_max) {
 #pragma unroll
@@ -348,7 +360,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
                     }
                 }
             }
-            const uint32_t ph = tc::smem_u32(sM + pb * 2 * Cfg::kMPart) + row_off + (uint32_t)(cq * BC / 8) * 128;
+            const uint32_t ph = tc::smem_u32(sM + pb * 2 * Cfg::kMPart) + row_off + (uint32_t)(cg * BC / 8) * 128;
             const uint32_t pl = ph + Cfg::kMPart;
 #pragma unroll
             for (int j = 0; j < BC / 8; ++j) {
@@ -410,8 +422,9 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
             }
             const float* beta = sh.beta[hi & 1];
             for (int kp = 0; kp < nparts; ++kp, ++n) {
-                const uint32_t pb = n & 1;
-                if (n >= 2) pipe_wait(sh, &sh.empty_part[pb], ((n - 2) >> 1) & 1);
+                if (kp % NG != gi) continue;  // the other warp group builds this part
+                const uint32_t pb = n % Cfg::kParts;
+                if (n >= (uint32_t)Cfg::kParts) pipe_wait(sh, &sh.empty_part[pb], ((n - Cfg::kParts) / Cfg::kParts) & 1);
                 tc::fence_after_sync();
                 build(kp, pb, beta, alpha, Dh);
                 tc::fence_async_smem();

@@ -4,7 +4,7 @@
 // with cum_s the in-chunk cumulative sum of Delta_s A_h:
 //   S_c[p, n] = sum_s w_s x_s[p] B_s[n],   w_s = exp(cum_last - cum_s) Delta_s
 // computed as D[(head, p), n] = Xw^T B with two heads (128 accumulator rows) per MMA
-// tile: M = 128, N = 64 per MMA (one 128-byte row of B), K = rows s.  The weighted
+// tile: M = 128, N = dstate per MMA, K = rows s.  The weighted
 // operand Xw is built by threads and split into bf16 hi + lo halves, both multiplied
 // against the exact bf16 B, so it keeps ~16 significant bits.
 //
@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(kCta, 1)
         if (lane == 0) {
             wait_or_abort(sh, &sh.mb_b, 0);
             tc::fence_after_sync();
-            constexpr uint32_t idesc = tc::idesc_bf16(128, 64, 1, 1);
+            constexpr uint32_t idesc = tc::idesc_bf16(128, N, 1, 1);
             uint32_t n = 0;
             for (int pr = 0; pr < npairs && !sh.abort; ++pr) {
                 const int ab = pr & 1;
@@ -175,15 +175,13 @@ __global__ void __launch_bounds__(kCta, 1)
                     // Xw^T: MN-major no-swizzle, M = 128 contiguous in 16-byte rows; K steps
                     // of 16 rows are two core-matrix rows (2 * 16 * 128 bytes) apart
                     const uint64_t dah = tc::desc_mnmajor(ah, 128, 0), dal = tc::desc_mnmajor(ah + Cfg::kXt, 128, 0);
+                    // B: all N columns in one MMA, the 64-column rows of the swizzle layout
+                    // 256 * 128 bytes apart (lbo), 8-row groups 1024 bytes apart (sbo)
+                    const uint64_t db = tc::desc_sw128(tc::smem_u32(sB) + (uint32_t)(kp * KS) * 128, 256 * 128, 1024);
 #pragma unroll
-                    for (int j = 0; j < N / 64; ++j) {
-                        const uint64_t db = tc::desc_sw128(tc::smem_u32(sB + j * 256 * 128) + (uint32_t)(kp * KS) * 128, 1024, 1024);
-#pragma unroll
-                        for (int ks = 0; ks < KS / 16; ++ks) {
-                            tc::mma_bf16(acc + 64 * j, dah + ks * tc::kstep_mnmajor(128), db + ks * 128u, idesc,
-                                         (kp > 0 || ks > 0) ? 1u : 0u);
-                            tc::mma_bf16(acc + 64 * j, dal + ks * tc::kstep_mnmajor(128), db + ks * 128u, idesc, 1u);
-                        }
+                    for (int ks = 0; ks < KS / 16; ++ks) {
+                        tc::mma_bf16(acc, dah + ks * tc::kstep_mnmajor(128), db + ks * 128u, idesc, (kp > 0 || ks > 0) ? 1u : 0u);
+                        tc::mma_bf16(acc, dal + ks * tc::kstep_mnmajor(128), db + ks * 128u, idesc, 1u);
                     }
                     tc::mma_commit(&sh.xt_empty[xb]);
                 }
