@@ -54,11 +54,13 @@ struct ScanCfg {
     static constexpr uint32_t kMPart = 128u * KPC * 2;       // one M' part, hi or lo
     static constexpr uint32_t kX = 256u * kP * 2;            // one x buffer (256 rows)
     static constexpr uint32_t kH = (uint32_t)kP * N * 2;     // one h_{c-1} tile, hi or lo
-    // M' parts in flight (a ring of builds ahead of the MMAs) and h_{c-1} tile sets, as
-    // shared memory allows: three parts and one h set up to dstate 128, two and one at 256
-    static constexpr int kParts = N <= 128 ? 3 : 2;
+    // two M' parts in flight, one h_{c-1} tile set; up to dstate 128 also a staging area
+    // for the output tiles (1 KB per compute warp), written to global memory by TMA
+    static constexpr int kParts = 2;
     static constexpr int kHBufs = 1;
-    static constexpr uint32_t kPhase2 = kParts * 2 * kMPart + 2 * kX + kHBufs * 2 * kH;
+    static constexpr bool kStageOut = N <= 128;
+    static constexpr uint32_t kOut = kStageOut ? 16u * 1024 : 0u;
+    static constexpr uint32_t kPhase2 = kParts * 2 * kMPart + 2 * kX + kHBufs * 2 * kH + kOut;
     static constexpr uint32_t kRegion = kB > kPhase2 ? kB : kPhase2;
     static constexpr uint32_t kSmem = kC + kRegion;   // operands; the pipeline state follows
     static constexpr uint32_t kSmemTotal = kSmem + 2304;
@@ -89,8 +91,8 @@ struct __align__(16) ScanShared {
                             // exp(cum_t - cum_s) Delta_s = 2^(alpha_t + beta_s)
     uint64_t mb_load;       // C and B rows (prologue TMA)
     uint64_t mb_g;          // G = C B^T in TMEM
-    uint64_t full_part[3];  // M' part built (one arrival per building warp)
-    uint64_t empty_part[3]; // M' part consumed by its MMAs
+    uint64_t full_part[2];  // M' part built (one arrival per building warp)
+    uint64_t empty_part[2]; // M' part consumed by its MMAs
     uint64_t acc_full[2];   // a head's Y accumulators complete
     uint64_t acc_empty[2];  // a head's Y accumulators read by the epilogue (one arrival per compute warp)
     uint64_t x_full[2], x_empty[2];
@@ -122,7 +124,7 @@ template <int N, bool GATE, bool XS>
 __global__ void __launch_bounds__(kCtaThreads, 1)
     ssd_scan_tc(const SsdTcArgs a, const int heads_per_cta, int* status, const __grid_constant__ CUtensorMap tm_x,
                 const __grid_constant__ CUtensorMap tm_xlo, const __grid_constant__ CUtensorMap tm_c,
-                const __grid_constant__ CUtensorMap tm_b) {
+                const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_out) {
     using Cfg = ScanCfg<N, XS>;
     constexpr int KPC = Cfg::KPC, BC = Cfg::BC, NCG = Cfg::NCG, NG = Cfg::NG;
     extern __shared__ __align__(1024) unsigned char smem[];
@@ -153,6 +155,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
     unsigned char* sM = region;                             // [part kParts][hi, lo] [t/8][s/8 of KPC][8][8]
     unsigned char* sX = region + Cfg::kParts * 2 * Cfg::kMPart;  // [buffer 2] [s SW][64] (+ lo plane), MN-major B
     unsigned char* sH = sX + 2 * Cfg::kX;                   // [set kHBufs][hi, lo] [p/8][n/8][8][8]
+    unsigned char* sOut = sH + Cfg::kHBufs * 2 * Cfg::kH;   // [compute warp][row 32][16 p] output staging
 
     if (tid == 0) {
         tc::mbar_init(&sh.mb_load, 1);
@@ -160,10 +163,6 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(&sh.full_part[i], Cfg::kPartWarps);
             tc::mbar_init(&sh.empty_part[i], 1);
-            if (i == 0 && Cfg::kParts == 3) {
-                tc::mbar_init(&sh.full_part[2], Cfg::kPartWarps);
-                tc::mbar_init(&sh.empty_part[2], 1);
-            }
             tc::mbar_init(&sh.acc_full[i], 1);
             tc::mbar_init(&sh.acc_empty[i], kComputeWarps);
             tc::mbar_init(&sh.x_full[i], 1);
@@ -383,7 +382,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.acc_empty[ab]);  // the MMAs of head hi + 2 may overwrite them
-            if (!row_ok || sh.abort) return;
+            if (sh.abort || (!Cfg::kStageOut && !row_ok)) return;
             const float e = ex2(alpha_h);
             const int64_t row = (((int64_t)b * a.T + row0 + t) * a.H + hbeg + hi) * kP + p0;
             uint4 zr[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
@@ -400,9 +399,25 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
                 if (GATE) y = __fmul2_rn(y, silu2_fma(__bfloat1622float2(z2[j / 2])));
                 pk[j / 2] = pack_bf16x2(y.x, y.y);
             }
-            uint4* dst = reinterpret_cast<uint4*>(a.out + row);
-            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            if (Cfg::kStageOut) {
+                // this warp's 32 rows x 16 columns through shared memory, one TMA store
+                // (rows past the sequence's end are clipped by the tensor map)
+                unsigned char* st = sOut + warp * 1024;
+                if (lane == 0) tc::bulk_wait_read_all();  // the previous head's store has read it
+                __syncwarp();
+                sts128(tc::smem_u32(st + lane * 32), pk[0], pk[1], pk[2], pk[3]);
+                sts128(tc::smem_u32(st + lane * 32 + 16), pk[4], pk[5], pk[6], pk[7]);
+                tc::fence_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tc::tma_store_3d(&tm_out, st, (hbeg + hi) * kP + p0, row0 + t0 + q * 32, b);
+                    tc::bulk_commit();
+                }
+            } else {
+                uint4* dst = reinterpret_cast<uint4*>(a.out + row);
+                dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            }
         };
 
         pipe_wait(sh, &sh.mb_g, 0);  // G is in TMEM
@@ -435,6 +450,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
             alpha_prev = alpha;
         }
         if (nh > 0) finish(nh - 1, alpha_prev);
+        if (Cfg::kStageOut && lane == 0) tc::bulk_wait_all();  // the output stores are done
     }
     if (sh.abort && tid == 0) atomicExch(status, kStatusTimeout);
     tc::fence_before_sync();
@@ -461,6 +477,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
 // 3-D map over a bf16 tensor (inner, T, batch), row-major and contiguous, with boxes of
 // 64 inner elements x 128 rows x 1 in the 128-byte swizzle layout: each box lands as 128
 // rows of 128 bytes, the operand layout of desc_sw128.  Rows past T read as zero.
+bool make_out_map(CUtensorMap* m, void* base, uint64_t inner, uint64_t T, uint64_t batch) {
+    // boxes of 16 columns x 32 rows (one compute warp's epilogue), no swizzle
+    const PFN_cuTensorMapEncodeTiled_v12000 fn = encode_tiled();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {inner, T, batch};
+    const cuuint64_t strides[2] = {inner * 2, inner * 2 * T};
+    const cuuint32_t box[3] = {16, 32, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t T, uint64_t batch) {
     const PFN_cuTensorMapEncodeTiled_v12000 fn = encode_tiled();
     if (!fn) return false;
@@ -489,10 +517,11 @@ int scan_heads_per_cta(const SsdTcArgs& s, int64_t batch) {
 template <int N, bool GATE, bool XS>
 cudaError_t launch_scan(const SsdTcArgs& s, int64_t batch, cudaStream_t stream) {
     using Cfg = ScanCfg<N, XS>;
-    CUtensorMap tx, txl, tmc, tmb;
+    CUtensorMap tx, txl, tmc, tmb, tmo;
     const uint64_t T = (uint64_t)s.T, nb = (uint64_t)batch;
     if (!make_map(&tx, s.x, (uint64_t)s.H * kP, T, nb) || !make_map(&txl, XS ? s.x_lo : s.x, (uint64_t)s.H * kP, T, nb) ||
-        !make_map(&tmc, s.C, (uint64_t)s.G * N, T, nb) || !make_map(&tmb, s.B, (uint64_t)s.G * N, T, nb))
+        !make_map(&tmc, s.C, (uint64_t)s.G * N, T, nb) || !make_map(&tmb, s.B, (uint64_t)s.G * N, T, nb) ||
+        !make_out_map(&tmo, s.out, (uint64_t)s.H * kP, T, nb))
         return cudaErrorInvalidValue;
     int* status = nullptr;
     cudaError_t e = device_status_address(&status);
@@ -504,7 +533,7 @@ cudaError_t launch_scan(const SsdTcArgs& s, int64_t batch, cudaStream_t stream) 
     const int hpc = scan_heads_per_cta(s, batch);
     const dim3 grid((unsigned)(s.nchunks * (s.Q / 128)), (unsigned)(s.H / hpc), (unsigned)batch);
     cudaEvent_t t0 = timing_begin(stream);
-    kern<<<grid, kCtaThreads, Cfg::kSmemTotal, stream>>>(s, hpc, status, tx, txl, tmc, tmb);
+    kern<<<grid, kCtaThreads, Cfg::kSmemTotal, stream>>>(s, hpc, status, tx, txl, tmc, tmb, tmo);
     note_launch("ssd_scan_tc", stream, t0);
     return cudaGetLastError();
 }
