@@ -64,6 +64,9 @@ def parse():
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the per-workload block (c0..c4) of the forward scan line")
     ap.add_argument("--chunk", type=int, default=None, help="override the workload's chunk")
+    ap.add_argument("--seqlen", type=int, default=None,
+                    help="override the workload's sequence length (reduced cases for profiling; "
+                         "not a bench line of the named workload)")
     ap.add_argument("--quick", action="store_true",
                     help="skip the clock soak, CPU baseline and end-to-end legs (profiling runs)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -539,7 +542,8 @@ def measure_forward(args, w, dev, dist, rank, world, K, warmup, headline, cpu_se
              "ms": ms_step, "algorithmic_bytes": nbytes,
              "what": "all kernels of one ssm_scan_fwd call"}
     roof = kernel_roofline(kt, nbytes, K, peaks["hbm_gbs"], peak_kind, whole)
-    roof = with_traffic(roof, ("conv" if args.conv else "scan", w.name))
+    roof = with_traffic(roof, ("conv" if args.conv else "scan",
+                               w.name if args.seqlen is None else f"{w.name}@L{w.seqlen}"))
     sm_mhz = float(peaks.get("sm_max_mhz", 2032.0))
     if w.mode == "ssd":
         fl = algorithmic_flops(w)
@@ -618,7 +622,7 @@ def run_ours(args, w):
     head = measure_forward(args, w, dev, dist, rank, world, args.steps, args.warmup, True,
                            args.cpu_seconds)
     configs = None
-    if not args.no_configs and not args.quick and not args.conv:
+    if not args.no_configs and not args.quick and not args.conv and args.seqlen is None:
         configs = {}
         for name in sorted(WORKLOADS):
             if name == w.name:
@@ -634,7 +638,9 @@ def run_ours(args, w):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
             "data": "synthetic",
             "config": {"workload": f"{w.name}: {DESCRIPTIONS[w.name]}" +
-                                   (", width-4 causal conv1d + SiLU ahead of the scan" if args.conv else ""),
+                                   (", width-4 causal conv1d + SiLU ahead of the scan" if args.conv else "") +
+                                   (f", sequence length reduced to {w.seqlen} (profiling case)"
+                                    if args.seqlen is not None else ""),
                        "l2": "flushed before every timed step (256 MB write)",
                        "chunk": head["chunk"], "parallelism": f"replicas x{world} (independent batches)"},
             "roofline": head["roofline"], "cpu_baseline": head["cpu_baseline"],
@@ -880,7 +886,7 @@ def run_backward(args, w):
     whole = {"achieved": gbs, "frac": gbs / peaks["hbm_gbs"], "unit": "GB/s", "ms": ms_step,
              "algorithmic_bytes": nbytes, "what": "one ssm_scan_bwd call (zeroing + kernel)"}
     roof = kernel_roofline(kt, nbytes, K, peaks["hbm_gbs"], peak_kind, whole)
-    roof = with_traffic(roof, ("backward", w.name))
+    roof = with_traffic(roof, ("backward", w.name if args.seqlen is None else f"{w.name}@L{w.seqlen}"))
     sm_mhz = float(peaks.get("sm_max_mhz", 2032.0))
     exps = 3.0 * w.token_channels * w.dstate  # the decay is formed in three sweeps
     roof["sfu"] = {"achieved": exps / (ms_step * 1e-3), "peak": 148 * 32 * sm_mhz * 1e6,
@@ -960,6 +966,8 @@ def main():
     args = parse()
     from selective_state_space_143_b300.inputs import WORKLOADS
     w = WORKLOADS[args.workload]
+    if args.seqlen is not None:
+        w = w.replace(seqlen=args.seqlen)
     if args.impl == "reference":
         return run_reference(args, w)
     if args.decode:

@@ -80,7 +80,9 @@ typedef enum {
     SSM_ERR_UNSUPPORTED = 5, /* valid but unsupported (dstate too large, flags != 0) */
     SSM_ERR_ALLOC = 6,       /* workspace allocation failed or workspace too small   */
     SSM_ERR_CUDA = 7,        /* a CUDA call failed (launch error, no device)         */
-    SSM_ERR_TIMEOUT = 8      /* a bounded device-side wait ran out (ssm_device_status) */
+    SSM_ERR_TIMEOUT = 8,     /* a bounded device-side wait ran out (ssm_device_status) */
+    SSM_ERR_BOUNDS = 9       /* a store address fell outside its buffer: builds with
+                                SSM_BOUNDS_CHECK only (ssm_device_status)              */
 } ssm_status;
 
 typedef enum { SSM_MODE_DIAG = 0, SSM_MODE_SSD = 1, SSM_MODE_CDIAG = 2 } ssm_mode;
@@ -321,11 +323,31 @@ int ssm_timing_collect(ssm_kernel_time* out, int max_entries);
  * polls), and a kernel whose wait ran out records SSM_ERR_TIMEOUT in a per-device status
  * word, releases its tensor memory and returns, so the context stays usable and its
  * outputs are not valid.  Launches are asynchronous, so the entry points cannot return
- * this status themselves: ssm_device_status synchronizes `stream`, then returns SSM_OK
- * or SSM_ERR_TIMEOUT for the current device (SSM_ERR_CUDA if the read fails), and clears
- * the word when `clear` is non-zero.
+ * this status themselves: ssm_device_status synchronizes `stream`, then returns SSM_OK,
+ * SSM_ERR_TIMEOUT or SSM_ERR_BOUNDS (below) for the current device (SSM_ERR_CUDA if the
+ * read fails), and clears the word when `clear` is non-zero.  The first code a kernel
+ * records stays until cleared.
+ *
+ * Bounds-checked build (compiled with -DSSM_BOUNDS_CHECK; the debugging stand-in for a
+ * memory checker): every kernel checks the address of each global store against the
+ * byte range of the buffer it writes (derived from the shape); an address outside it is
+ * not written and SSM_ERR_BOUNDS is recorded in the same status word.  The kernels do
+ * not trap.  Normal builds compile the checks away.
  */
 int ssm_device_status(int clear, ssm_stream_t stream);
+
+/* 1 if this library was built with SSM_BOUNDS_CHECK, else 0. */
+int ssm_bounds_check_enabled(void);
+
+/*
+ * Self-test of the bounds-check path: one thread stores to buf[index] through the check
+ * against [buf, buf + bytes); with index * 4 >= bytes the store is skipped and
+ * SSM_ERR_BOUNDS recorded (read it with ssm_device_status).  buf is a device buffer
+ * owned by the caller that must hold element `index` either way, so the address stays
+ * valid whatever the check does.  SSM_ERR_UNSUPPORTED in builds without the checks,
+ * SSM_ERR_NULL for a NULL buf, SSM_ERR_SHAPE for index < 0 or bytes not a multiple of 4.
+ */
+int ssm_selftest_bounds(float* buf, size_t bytes, int64_t index, ssm_stream_t stream);
 
 /*
  * Self-test of the bounded-wait path: one thread block waits on an mbarrier that expects

@@ -326,16 +326,36 @@ def step(x, dt, A, B, C, D=None, z=None, dt_bias=None, *, state, out=None, strea
 
 
 def device_status(clear: bool = True, stream=None) -> int:
-    """Status of the library's bounded device-side waits on the current device, after the
-    work queued on ``stream`` (default: the current torch stream): ``_lib.SSM_OK`` or
-    ``_lib.SSM_ERR_TIMEOUT`` (a kernel gave up a wait; its outputs are not valid).
-    ``clear`` resets the status word."""
+    """Status of the library's bounded device-side waits (and, in a bounds-checked build,
+    its store bounds checks) on the current device, after the work queued on ``stream``
+    (default: the current torch stream): ``_lib.SSM_OK``, ``_lib.SSM_ERR_TIMEOUT`` (a
+    kernel gave up a wait; its outputs are not valid) or ``_lib.SSM_ERR_BOUNDS`` (a store
+    fell outside its buffer and was skipped).  ``clear`` resets the status word."""
     if stream is None:
         stream = torch.cuda.current_stream()
     rc = _lib.load().ssm_device_status(1 if clear else 0, ctypes.c_void_p(stream.cuda_stream))
-    if rc not in (_lib.SSM_OK, _lib.SSM_ERR_TIMEOUT):
+    if rc not in (_lib.SSM_OK, _lib.SSM_ERR_TIMEOUT, _lib.SSM_ERR_BOUNDS):
         raise SsmError(rc, "ssm_device_status")
     return rc
+
+
+def bounds_check_enabled() -> bool:
+    """True when the loaded library was built with SSM_BOUNDS_CHECK."""
+    return bool(_lib.load().ssm_bounds_check_enabled())
+
+
+def selftest_bounds(buf: torch.Tensor, nbytes: int, index: int, stream=None) -> None:
+    """Store to ``buf[index]`` through the bounds check against the first ``nbytes`` of the
+    fp32 device tensor ``buf`` (see ``ssm_selftest_bounds``; ``buf`` must hold ``index``).
+    Bounds-checked builds only; read the outcome with ``device_status``."""
+    if buf.dtype != torch.float32 or not buf.is_cuda or index >= buf.numel():
+        raise ValueError("buf must be a CUDA fp32 tensor that holds element `index`")
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    rc = _lib.load().ssm_selftest_bounds(ctypes.c_void_p(buf.data_ptr()), int(nbytes), int(index),
+                                         ctypes.c_void_p(stream.cuda_stream))
+    if rc != _lib.SSM_OK:
+        raise SsmError(rc, "ssm_selftest_bounds")
 
 
 def selftest_bounded_wait(max_checks: int = 1000, stream=None) -> None:

@@ -20,6 +20,7 @@ SSM_ERR_UNSUPPORTED = 5
 SSM_ERR_ALLOC = 6
 SSM_ERR_CUDA = 7
 SSM_ERR_TIMEOUT = 8
+SSM_ERR_BOUNDS = 9
 
 SSM_MODE_DIAG = 0
 SSM_MODE_SSD = 1
@@ -33,7 +34,7 @@ EXPORTED = ("ssm_scan_fwd", "ssm_scan_fwd_ws", "ssm_scan_workspace_size", "ssm_s
             "ssm_step_conv", "ssm_scan_bwd", "ssm_scan_bwd_workspace_size", "ssm_timing_enable",
             "ssm_timing_collect", "ssm_device_status", "ssm_selftest_bounded_wait", "ssm_strerror",
             "ssm_kernel_launch_count", "ssm_abi_version", "ssm_tuning_set", "ssm_tuning_get",
-            "ssm_inject_alloc_failures")
+            "ssm_inject_alloc_failures", "ssm_bounds_check_enabled", "ssm_selftest_bounds")
 
 SSM_TUNE_DIAG_NPT = 0
 SSM_TUNE_SSD_CUDA_CORES = 1
@@ -139,6 +140,10 @@ def load() -> ctypes.CDLL:
         lib.ssm_tuning_get.restype = ctypes.c_int64
         lib.ssm_inject_alloc_failures.argtypes = [ctypes.c_int]
         lib.ssm_inject_alloc_failures.restype = None
+        lib.ssm_bounds_check_enabled.argtypes = []
+        lib.ssm_bounds_check_enabled.restype = ctypes.c_int
+        lib.ssm_selftest_bounds.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int64, ctypes.c_void_p]
+        lib.ssm_selftest_bounds.restype = ctypes.c_int
         del fp
         _lib = lib
         return lib

@@ -1,8 +1,11 @@
 """Build libssmscan.so in-tree with nvcc for sm_103a.
 
-Usage: ``python -m selective_state_space_143_b300.build [--force] [-v]``.
+Usage: ``python -m selective_state_space_143_b300.build [--force] [-v] [--bounds-check]``.
 Each .cu under csrc/ is compiled to an object, then linked into one shared library
 with the CUDA runtime linked statically, so the library loads without a GPU.
+``--bounds-check`` builds the same sources with -DSSM_BOUNDS_CHECK into
+libssmscan_bc.so: every kernel store checks its address against its buffer and
+records SSM_ERR_BOUNDS instead of writing outside it (load it through SSM_LIB_PATH).
 """
 from __future__ import annotations
 
@@ -18,6 +21,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 OUT = os.path.join(HERE, "libssmscan.so")
 BUILD_DIR = os.path.join(HERE, "_build")
+OUT_BC = os.path.join(HERE, "libssmscan_bc.so")
+BUILD_DIR_BC = os.path.join(HERE, "_build_bc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
@@ -41,18 +46,18 @@ def _deps() -> list[str]:
     return out
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(OUT):
+def up_to_date(out: str = OUT) -> bool:
+    if not os.path.exists(out):
         return False
-    t = os.path.getmtime(OUT)
+    t = os.path.getmtime(out)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
 def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None,
           out: str = OUT, build_dir: str = BUILD_DIR) -> str:
     """Compile every .cu under csrc/ and link ``out``; ``extra`` adds nvcc flags."""
-    if not force and out == OUT and up_to_date():
-        return OUT
+    if not force and up_to_date(out):
+        return out
     os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
     objs, cmds = [], []
@@ -80,9 +85,20 @@ def main(argv=None) -> int:
     ap = argparse.ArgumentParser()
     ap.add_argument("--force", action="store_true")
     ap.add_argument("-v", "--verbose", action="store_true", help="print ptxas register/smem usage")
+    ap.add_argument("--bounds-check", action="store_true",
+                    help="build libssmscan_bc.so with -DSSM_BOUNDS_CHECK")
     args = ap.parse_args(argv)
-    print(build(force=args.force, verbose=args.verbose))
+    if args.bounds_check:
+        print(build_bounds_checked(force=args.force, verbose=args.verbose))
+    else:
+        print(build(force=args.force, verbose=args.verbose))
     return 0
+
+
+def build_bounds_checked(force: bool = False, verbose: bool = False) -> str:
+    """The bounds-checked library (stores checked against their buffers)."""
+    return build(force=force, verbose=verbose, extra=["-DSSM_BOUNDS_CHECK"], out=OUT_BC,
+                 build_dir=BUILD_DIR_BC)
 
 
 if __name__ == "__main__":

@@ -77,6 +77,9 @@ struct CDiagArgs {
     float* seg_dsum;      // (nseg-1, b, dim)
     int64_t T, dim, N, G, cpg, seg_len;
     int nseg, tiles_per_group;
+    // byte ranges of the buffers written (stores checked in SSM_BOUNDS_CHECK builds)
+    int* status;
+    Span out_s, final_s, segh_s, segd_s;
 };
 
 __device__ __forceinline__ void ccp_async16(void* smem, const void* gmem, bool valid) {
@@ -257,7 +260,8 @@ __global__ void __launch_bounds__(kCThreads) cdiag_scan_kernel(const CDiagArgs a
                 const float xv = to_f32<T>(*reinterpret_cast<const T*>(st + r * Cfg::kRowBytes + ch * E));
                 if (a.D) y = fmaf(a.D[c_begin + ch], xv, y);
                 if (GATE) y *= silu_t<PRECISE>(to_f32<T>(*reinterpret_cast<const T*>(st + 2 * Cfg::kXBytes + r * Cfg::kRowBytes + ch * E)));
-                *reinterpret_cast<T*>(a.out + row_base + (int64_t)(k * kCTT + r) * row_stride + (c_begin + ch) * E) = from_f32<T>(y);
+                store_checked(a.out_s, reinterpret_cast<T*>(a.out + row_base + (int64_t)(k * kCTT + r) * row_stride + (c_begin + ch) * E),
+                              from_f32<T>(y), a.status);
             }
         }
     }
@@ -270,8 +274,8 @@ __global__ void __launch_bounds__(kCThreads) cdiag_scan_kernel(const CDiagArgs a
             for (int j = 0; j < kEPL; ++j) {
                 const int n = g * kEPL + j;
                 if (n < a.N) {
-                    Hs[2 * n] = h[j].x;
-                    Hs[2 * n + 1] = h[j].y;
+                    store_checked(a.segh_s, &Hs[2 * n], h[j].x, a.status);
+                    store_checked(a.segh_s, &Hs[2 * n + 1], h[j].y, a.status);
                 }
             }
         }
@@ -284,7 +288,7 @@ __global__ void __launch_bounds__(kCThreads) cdiag_scan_kernel(const CDiagArgs a
         if (tid < chans) {
             float s = 0.0f;
             for (int q = tid; q < kCThreads; q += CPB) s += red[q];
-            a.seg_dsum[((int64_t)seg * gridDim.z + b) * a.dim + c_begin + tid] = s;
+            store_checked(a.segd_s, &a.seg_dsum[((int64_t)seg * gridDim.z + b) * a.dim + c_begin + tid], s, a.status);
         }
     } else if (a.final_state && seg == a.nseg - 1 && c_ok) {
         float* fs = a.final_state + (b * a.dim + c) * a.N * 2;
@@ -292,8 +296,8 @@ __global__ void __launch_bounds__(kCThreads) cdiag_scan_kernel(const CDiagArgs a
         for (int j = 0; j < kEPL; ++j) {
             const int n = g * kEPL + j;
             if (n < a.N) {
-                fs[2 * n] = h[j].x;
-                fs[2 * n + 1] = h[j].y;
+                store_checked(a.final_s, &fs[2 * n], h[j].x, a.status);
+                store_checked(a.final_s, &fs[2 * n + 1], h[j].y, a.status);
             }
         }
     }
@@ -369,10 +373,19 @@ cudaError_t claunch_typed(const ScanArgs& a, const CPlan& p, void* ws, cudaStrea
     ka.tiles_per_group = p.tiles_per_group;
     ka.seg_h = nullptr;
     ka.seg_dsum = nullptr;
+    ka.status = nullptr;
+    if (kBoundsCheck) {
+        cudaError_t e = device_status_address(&ka.status);
+        if (e != cudaSuccess) return e;
+    }
+    ka.out_s = span_of(a.out, (size_t)a.batch * a.seqlen * a.nheads * (a.dtype == 1 ? 2 : 4));
+    ka.final_s = span_of(a.final_state, (size_t)a.batch * a.nheads * a.dstate * 2 * sizeof(float));
     if (p.nseg > 1) {
         const size_t hbytes = (size_t)(p.nseg - 1) * a.batch * a.nheads * a.dstate * 2 * sizeof(float);
         ka.seg_h = (float*)ws;
         ka.seg_dsum = (float*)((char*)ws + align_up(hbytes, 256));
+        ka.segh_s = span_of(ka.seg_h, hbytes);
+        ka.segd_s = span_of(ka.seg_dsum, (size_t)(p.nseg - 1) * a.batch * a.nheads * sizeof(float));
         cudaError_t e = claunch_one<T, NK, true, false>(ka, dim3(p.blocks_x, p.nseg - 1, (unsigned)a.batch), stream);
         if (e != cudaSuccess) return e;
     }

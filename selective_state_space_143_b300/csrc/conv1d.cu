@@ -38,6 +38,9 @@ struct ConvArgs {
     void* x_last;
     int64_t batch, T, ch;
     int K;
+    // byte ranges of the buffers written (stores checked in SSM_BOUNDS_CHECK builds)
+    int* status;
+    Span xc_s, xlast_s;
 };
 
 // One vector of inputs (VW channels from c0: 8 bytes of bf16 or 16 of fp32) at step s,
@@ -142,13 +145,13 @@ __global__ void __launch_bounds__(kConvThreads) conv_silu_kernel(const ConvArgs 
                         lo[j] = *reinterpret_cast<const uint32_t*>(&l2);
                     }
                     __nv_bfloat16* xh = static_cast<__nv_bfloat16*>(a.xc);
-                    *reinterpret_cast<uint2*>(xh + o) = make_uint2(hi[0], hi[1]);
-                    *reinterpret_cast<uint2*>(xh + plane + o) = make_uint2(lo[0], lo[1]);
+                    store_checked(a.xc_s, reinterpret_cast<uint2*>(xh + o), make_uint2(hi[0], hi[1]), a.status);
+                    store_checked(a.xc_s, reinterpret_cast<uint2*>(xh + plane + o), make_uint2(lo[0], lo[1]), a.status);
                 } else {
                     float* xf = static_cast<float*>(a.xc) + o;
 #pragma unroll
                     for (int j = 0; j < VW; j += 4)
-                        *reinterpret_cast<float4*>(xf + j) = make_float4(y[j], y[j + 1], y[j + 2], y[j + 3]);
+                        store_checked(a.xc_s, reinterpret_cast<float4*>(xf + j), make_float4(y[j], y[j + 1], y[j + 2], y[j + 3]), a.status);
                 }
             }
         }
@@ -170,7 +173,7 @@ __global__ void __launch_bounds__(kConvThreads) conv_tail_kernel(const ConvArgs 
         v = static_cast<const T*>(a.x)[(b * a.T + s) * a.ch + c];
     else if (a.x_prev)
         v = static_cast<const T*>(a.x_prev)[(b * km1 + (km1 + s)) * a.ch + c];
-    static_cast<T*>(a.x_last)[i] = v;
+    store_checked(a.xlast_s, &static_cast<T*>(a.x_last)[i], v, a.status);
 }
 
 ConvArgs conv_args(const ScanArgs& a, void* xc) {
@@ -185,13 +188,21 @@ ConvArgs conv_args(const ScanArgs& a, void* xc) {
     c.T = a.seqlen;
     c.ch = a.nheads * a.headdim;
     c.K = a.conv_k;
+    c.status = nullptr;
+    const size_t E = a.dtype == 1 ? 2 : 4;
+    c.xc_s = span_of(xc, (size_t)c.batch * c.T * c.ch * 4);  // fp32, or two bf16 planes
+    c.xlast_s = span_of(a.x_last, (size_t)c.batch * (c.K > 1 ? c.K - 1 : 0) * c.ch * E);
     return c;
 }
 
 }  // namespace
 
 cudaError_t conv_prepass_launch(const ScanArgs& a, void* xc, bool split, cudaStream_t stream) {
-    const ConvArgs c = conv_args(a, xc);
+    ConvArgs c = conv_args(a, xc);
+    if (kBoundsCheck) {
+        const cudaError_t e = device_status_address(&c.status);
+        if (e != cudaSuccess) return e;
+    }
     if (c.batch * c.T * c.ch == 0) return cudaSuccess;
     if (split && a.dtype != 1) return cudaErrorInvalidValue;  // planes are for bf16 inputs
     const int vw = 4;  // channels per thread (ch is a multiple of 4 for either dtype)
@@ -214,7 +225,11 @@ cudaError_t conv_prepass_launch(const ScanArgs& a, void* xc, bool split, cudaStr
 }
 
 cudaError_t conv_tail_launch(const ScanArgs& a, cudaStream_t stream) {
-    const ConvArgs c = conv_args(a, nullptr);
+    ConvArgs c = conv_args(a, nullptr);
+    if (kBoundsCheck) {
+        const cudaError_t e = device_status_address(&c.status);
+        if (e != cudaSuccess) return e;
+    }
     const int64_t total = c.batch * (c.K - 1) * c.ch;
     if (!a.x_last || total == 0) return cudaSuccess;
     const unsigned blocks = (unsigned)((total + kConvThreads - 1) / kConvThreads);

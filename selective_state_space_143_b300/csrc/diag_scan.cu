@@ -109,6 +109,9 @@ struct DiagKernelArgs {
     int64_t seg_len;
     int nseg, tiles_per_group;
     int nsub_launched;   // host side: a state-only pass was launched ahead of this pass
+    // byte ranges of the buffers written (stores checked in SSM_BOUNDS_CHECK builds)
+    int* status;
+    Span out_s, final_s, segh_s, segd_s, xlast_s;
 };
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
@@ -364,7 +367,8 @@ __global__ void __launch_bounds__(32 * WARPS) diag_scan_kernel(const DiagKernelA
                                : load_pair<T>(st + r * Cfg::kRowBytes + 2 * pp * E);
         y = __ffma2_rn(d2, xv, y);
         if (GATE) y = __fmul2_rn(y, silu_pair<PRECISE>(load_pair<T>(st + 2 * Cfg::kXBytes + r * Cfg::kRowBytes + 2 * pp * E)));
-        store_pair<T>(out_base + (int64_t)(k * kTT + r) * row_stride, y);
+        char* dst = out_base + (int64_t)(k * kTT + r) * row_stride;
+        if (span_ok(a.out_s, dst, 2 * E, a.status)) store_pair<T>(dst, y);
     };
 
     // The output pass may start while the state-only pass is finishing (programmatic
@@ -483,8 +487,8 @@ __global__ void __launch_bounds__(32 * WARPS) diag_scan_kernel(const DiagKernelA
 #pragma unroll
             for (int k = 0; k < NPT / 2; ++k) {
                 const int n = g * NPT + 2 * k;
-                if (n < a.N) Hs[n] = h[k].x;
-                if (n + 1 < a.N) Hs[n + 1] = h[k].y;
+                if (n < a.N) store_checked(a.segh_s, &Hs[n], h[k].x, a.status);
+                if (n + 1 < a.N) store_checked(a.segh_s, &Hs[n + 1], h[k].y, a.status);
             }
         }
         // the RS threads of a pair each summed a subset of rows
@@ -498,8 +502,8 @@ __global__ void __launch_bounds__(32 * WARPS) diag_scan_kernel(const DiagKernelA
             const int64_t c0 = c_begin + 2 * tid;
             if (c0 < c_end) {
                 float* dst = a.seg_dsum + ((int64_t)seg * gridDim.z + b) * a.dim + c0;
-                dst[0] = s.x;
-                dst[1] = s.y;
+                store_checked(a.segd_s, dst, s.x, a.status);
+                store_checked(a.segd_s, dst + 1, s.y, a.status);
             }
         }
     }
@@ -519,7 +523,7 @@ __global__ void __launch_bounds__(32 * WARPS) diag_scan_kernel(const DiagKernelA
                 v = xg[(b * a.T + s) * a.dim + ch];
             else if (xp)
                 v = xp[(b * km1 + (km1 + s)) * a.dim + ch];
-            xl[(b * km1 + j) * a.dim + ch] = v;
+            store_checked(a.xlast_s, &xl[(b * km1 + j) * a.dim + ch], v, a.status);
         }
     }
     if (!STATE_ONLY && a.final_state && seg == a.nseg - 1 && c_ok) {
@@ -527,8 +531,8 @@ __global__ void __launch_bounds__(32 * WARPS) diag_scan_kernel(const DiagKernelA
 #pragma unroll
         for (int k = 0; k < NPT / 2; ++k) {
             const int n = g * NPT + 2 * k;
-            if (n < a.N) fs[n] = h[k].x;
-            if (n + 1 < a.N) fs[n + 1] = h[k].y;
+            if (n < a.N) store_checked(a.final_s, &fs[n], h[k].x, a.status);
+            if (n + 1 < a.N) store_checked(a.final_s, &fs[n + 1], h[k].y, a.status);
         }
     }
 }
@@ -663,10 +667,22 @@ cudaError_t launch_typed(const ScanArgs& a, const Plan& p, void* ws, cudaStream_
     ka.seg_h = nullptr;
     ka.seg_dsum = nullptr;
     ka.nsub_launched = 0;
+    ka.status = nullptr;
+    if (kBoundsCheck) {
+        cudaError_t e = device_status_address(&ka.status);
+        if (e != cudaSuccess) return e;
+    }
+    const size_t E = a.dtype == 1 ? 2 : 4;
+    ka.out_s = span_of(a.out, (size_t)a.batch * a.seqlen * a.nheads * E);
+    ka.final_s = span_of(a.final_state, (size_t)a.batch * a.nheads * a.dstate * sizeof(float));
+    ka.xlast_s = span_of(a.x_last, (size_t)a.batch * (a.conv_k > 1 ? a.conv_k - 1 : 0) * a.nheads * E);
     if (p.nseg > 1) {
         const size_t hbytes = (size_t)(p.nseg - 1) * a.batch * a.nheads * a.dstate * sizeof(float);
+        const size_t dbytes = (size_t)(p.nseg - 1) * a.batch * a.nheads * sizeof(float);
         ka.seg_h = (float*)ws;
         ka.seg_dsum = (float*)((char*)ws + align_up(hbytes, 256));
+        ka.segh_s = span_of(ka.seg_h, hbytes);
+        ka.segd_s = span_of(ka.seg_dsum, dbytes);
         const dim3 g1(p.blocks_x, p.nseg - 1, (unsigned)a.batch);
         cudaError_t e = CONV ? launch_one<T, NK, LPC, true, false, true>(ka, g1, stream)
                              : launch_one<T, NK, LPC, true, false, false>(ka, g1, stream);

@@ -52,6 +52,9 @@ struct SsdArgs {
     float* states;  // (b, nchunks, H, P, N)
     int64_t T, H, P, N, G, Q, nchunks;
     int x_f32;      // x is stored as fp32 whatever the dtype (the convolved input)
+    // byte ranges of the buffers written (stores checked in SSM_BOUNDS_CHECK builds)
+    int* status;
+    Span out_s, final_s, dl_s, cum_s, states_s;
 };
 
 template <typename T>
@@ -129,8 +132,8 @@ __global__ void __launch_bounds__(kThreads) ssd_chunk_state(const SsdArgs a) {
     const int len = (int)min(a.Q, a.T - t0);
     if (pt == 0 && nt == 0 && tid < a.Q) {
         const int64_t o = ((b * a.H + h) * a.nchunks + c) * a.Q + tid;
-        a.dl[o] = s_dl[tid];
-        a.cum[o] = s_cum[tid];
+        store_checked(a.dl_s, &a.dl[o], s_dl[tid], a.status);
+        store_checked(a.cum_s, &a.cum[o], s_cum[tid], a.status);
     }
     const float last = s_cum[len - 1];
     const int pi = (tid / 16) * 4, nj = (tid % 16) * 4;
@@ -169,7 +172,7 @@ __global__ void __launch_bounds__(kThreads) ssd_chunk_state(const SsdArgs a) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int64_t p = (int64_t)pt * kTile + pi + i, n = (int64_t)nt * kTile + nj + j;
-            if (p < a.P && n < a.N) S[p * a.N + n] = acc[i][j];
+            if (p < a.P && n < a.N) store_checked(a.states_s, &S[p * a.N + n], acc[i][j], a.status);
         }
 }
 
@@ -204,7 +207,7 @@ __global__ void __launch_bounds__(kThreads) ssd_state_pass(const SsdArgs a) {
         for (int j = 0; j < kPassAhead; ++j) {
             const int64_t c = c0 + j;
             if (c < a.nchunks) {
-                *reinterpret_cast<float4*>(base + c * cstride) = st;
+                store_checked(a.states_s, reinterpret_cast<float4*>(base + c * cstride), st, a.status);
                 st.x = fmaf(dec[j], st.x, S[j].x);
                 st.y = fmaf(dec[j], st.y, S[j].y);
                 st.z = fmaf(dec[j], st.z, S[j].z);
@@ -212,7 +215,7 @@ __global__ void __launch_bounds__(kThreads) ssd_state_pass(const SsdArgs a) {
             }
         }
     }
-    if (a.final_state) *reinterpret_cast<float4*>(a.final_state + (b * a.H + h) * PN + i4 * 4) = st;
+    if (a.final_state) store_checked(a.final_s, reinterpret_cast<float4*>(a.final_state + (b * a.H + h) * PN + i4 * 4), st, a.status);
 }
 
 // The tensor-core path's carry.  S_c arrives in the split-ready layout of the
@@ -267,8 +270,8 @@ __global__ void __launch_bounds__(kThreads) ssd_state_pass_split(const SsdArgs a
                     hi[k] = *reinterpret_cast<const uint32_t*>(&hv);
                     lo[k] = *reinterpret_cast<const uint32_t*>(&lv);
                 }
-                *reinterpret_cast<uint4*>(base + c * cstride + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4*>(base + c * cstride + half + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                store_checked(a.states_s, reinterpret_cast<uint4*>(base + c * cstride + o), make_uint4(hi[0], hi[1], hi[2], hi[3]), a.status);
+                store_checked(a.states_s, reinterpret_cast<uint4*>(base + c * cstride + half + o), make_uint4(lo[0], lo[1], lo[2], lo[3]), a.status);
                 const float s[8] = {S0[j].x, S0[j].y, S0[j].z, S0[j].w, S1[j].x, S1[j].y, S1[j].z, S1[j].w};
 #pragma unroll
                 for (int k = 0; k < 8; ++k) st[k] = fmaf(dec[j], st[k], s[k]);
@@ -277,7 +280,7 @@ __global__ void __launch_bounds__(kThreads) ssd_state_pass_split(const SsdArgs a
     }
     if (a.final_state) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) a.final_state[(b * a.H + h) * PN + p * a.N + n0 + k] = st[k];
+        for (int k = 0; k < 8; ++k) store_checked(a.final_s, &a.final_state[(b * a.H + h) * PN + p * a.N + n0 + k], st[k], a.status);
     }
 }
 
@@ -397,7 +400,7 @@ __global__ void __launch_bounds__(kThreads) ssd_chunk_scan(const SsdArgs a) {
             const float xv = ld_x<T>(a, row + p);
             float y = acc[i][j] + e * off[i][j] + Dh * xv;
             if (GATE) y *= silu_t<sizeof(T) == 4>(ld<T>(a.z, row + p));
-            reinterpret_cast<T*>(a.out)[row + p] = from_f32<T>(y);
+            store_checked(a.out_s, &reinterpret_cast<T*>(a.out)[row + p], from_f32<T>(y), a.status);
         }
     }
 }
@@ -450,6 +453,19 @@ cudaError_t ssd_launch_typed(const ScanArgs& a, void* ws, cudaStream_t stream) {
     s.Q = pl.Q;
     s.nchunks = pl.nchunks;
     s.x_f32 = a.x_f32;
+    s.status = nullptr;
+    if (kBoundsCheck) {
+        cudaError_t e = device_status_address(&s.status);
+        if (e != cudaSuccess) return e;
+    }
+    {
+        const size_t vec = (size_t)a.batch * a.nheads * pl.nchunks * pl.Q * sizeof(float);
+        s.out_s = span_of(a.out, (size_t)a.batch * a.seqlen * a.nheads * a.headdim * sizeof(T));
+        s.final_s = span_of(a.final_state, (size_t)a.batch * a.nheads * a.headdim * a.dstate * sizeof(float));
+        s.dl_s = span_of(s.dl, vec);
+        s.cum_s = span_of(s.cum, vec);
+        s.states_s = span_of(s.states, (size_t)a.batch * pl.nchunks * a.nheads * a.headdim * a.dstate * sizeof(float));
+    }
     const unsigned nP = (unsigned)((a.headdim + kTile - 1) / kTile);
     const unsigned nN = (unsigned)((a.dstate + kTile - 1) / kTile);
     const unsigned nTq = (unsigned)((pl.Q + kTile - 1) / kTile);
@@ -479,6 +495,10 @@ cudaError_t ssd_launch_typed(const ScanArgs& a, void* ws, cudaStream_t stream) {
         t.G = a.ngroups;
         t.Q = pl.Q;
         t.nchunks = pl.nchunks;
+        t.out_s = s.out_s;
+        t.dl_s = s.dl_s;
+        t.cum_s = s.cum_s;
+        t.states_s = s.states_s;
         cudaError_t e = ssd_tc_chunk_state(t, a.batch, stream);
         if (e != cudaSuccess) return e;
         cudaEvent_t t0 = timing_begin(stream);

@@ -1,7 +1,7 @@
 // SSD chunk scan on the B300 tensor cores: the output of every chunk from the chunk's
 // own inputs and the state carried into it ("Mamba-2：把状态空间模型和 Attention 统一到一个
 // 数学框架里", 第二步 and 关键技术点 1-3: y = (L o M) x, dense diagonal blocks, low-rank
-// off-diagonal blocks through the carried state).  Per (chunk, 128-row half, up to 8
+// off-diagonal blocks through the carried state).  Per (chunk, 128-row half, up to 32
 // heads of one group), with s_t the in-chunk cumulative sum of Delta_t A_h:
 //   G        = C_rows B^T                                   (M = 128, N = rows s of the half's causal range, K = dstate)
 //   M'[t, s] = G[t, s] exp(s_t - s_s) Delta_s  (s < t),  G[t, t] Delta_t + D  (s = t),  0  (s > t)
@@ -12,16 +12,17 @@
 // (and z).  M' is the one operand built by threads: scaled, masked and split into bf16
 // hi + lo halves, both multiplied against the exact bf16 X, so that the scaled operand
 // keeps ~16 significant bits.  Every other operand arrives by TMA / bulk copies: C and
-// B rows and x tiles through 3-D tensor maps whose 8-element boxes write the no-swizzle
-// canonical layout directly, h_{c-1} (already split hi/lo by the carry pass) as one
-// contiguous bulk copy.  Copies complete on mbarriers; every wait is bounded.
+// B rows and x tiles through 3-D tensor maps with 128-byte rows in the 128-byte swizzle
+// layout (C, B K-major; x MN-major), h_{c-1} (already split hi/lo by the carry pass) as
+// one contiguous bulk copy.  Up to dstate 128 the output tiles go back by TMA stores
+// from shared memory.  Copies complete on mbarriers; every wait is bounded.
 //
 // One CTA per SM, warp-specialised: a TMA warp, an MMA warp and 16 compute warps that
-// build M' and run the epilogues, handing work over on mbarriers (M' parts double
-// buffered, x tiles and h tiles double buffered where they fit, two sets of Y
-// accumulators so that a head's epilogue overlaps the next head's MMAs).  512 TMEM
-// columns: G, and the two accumulator sets.  Compute warp w owns TMEM lanes 32*(w%4)..
-// (rows) and 16 columns of the M' parts it builds.
+// build M' and run the epilogues, handing work over on mbarriers (two M' parts in
+// flight, x tiles double buffered, one h tile set refilled once a head's Y_off MMAs
+// have read it, two sets of Y accumulators so that a head's epilogue overlaps the next
+// head's MMAs).  512 TMEM columns: G, and the two accumulator sets.  Compute warp w
+// owns TMEM lanes 32*(w%4).. (rows) and 16 columns of the M' parts it builds.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -415,8 +416,8 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
                 }
             } else {
                 uint4* dst = reinterpret_cast<uint4*>(a.out + row);
-                dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                store_checked(a.out_s, dst, make_uint4(pk[0], pk[1], pk[2], pk[3]), status);
+                store_checked(a.out_s, dst + 1, make_uint4(pk[4], pk[5], pk[6], pk[7]), status);
             }
         };
 
@@ -474,11 +475,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
     return fn;
 }
 
-// 3-D map over a bf16 tensor (inner, T, batch), row-major and contiguous, with boxes of
-// 64 inner elements x 128 rows x 1 in the 128-byte swizzle layout: each box lands as 128
-// rows of 128 bytes, the operand layout of desc_sw128.  Rows past T read as zero.
+// 3-D store map over the bf16 output (inner, T, batch): boxes of 16 columns x 32 rows
+// (one compute warp's part of an epilogue), no swizzle; rows past T are not written.
 bool make_out_map(CUtensorMap* m, void* base, uint64_t inner, uint64_t T, uint64_t batch) {
-    // boxes of 16 columns x 32 rows (one compute warp's epilogue), no swizzle
     const PFN_cuTensorMapEncodeTiled_v12000 fn = encode_tiled();
     if (!fn) return false;
     const cuuint64_t dims[3] = {inner, T, batch};
@@ -489,6 +488,9 @@ bool make_out_map(CUtensorMap* m, void* base, uint64_t inner, uint64_t T, uint64
               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D map over a bf16 tensor (inner, T, batch), row-major and contiguous, with boxes of
+// 64 inner elements x 128 rows x 1 in the 128-byte swizzle layout: each box lands as 128
+// rows of 128 bytes, the operand layout of desc_sw128.  Rows past T read as zero.
 bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t T, uint64_t batch) {
     const PFN_cuTensorMapEncodeTiled_v12000 fn = encode_tiled();
     if (!fn) return false;

@@ -236,8 +236,8 @@ __global__ void __launch_bounds__(kCta, 1)
                 for (int k = 0; k < kMaxHeads; ++k) {
                     if (k >= hpc) break;
                     const int64_t o = (((int64_t)b * a.H + hbeg + k) * a.nchunks + c) * a.Q + s;
-                    a.dl[o] = d[k];
-                    a.cum[o] = v[k];
+                    store_checked(a.dl_s, &a.dl[o], d[k], status);
+                    store_checked(a.cum_s, &a.cum[o], v[k], status);
                     sW[k * 256 + s] = s < len ? __expf(last[k] - v[k]) * d[k] : 0.0f;
                 }
             }
@@ -301,8 +301,8 @@ __global__ void __launch_bounds__(kCta, 1)
 #pragma unroll
                 for (int j = 0; j < 16; j += 8) {
                     const uint32_t o = (uint32_t)((p >> 3) * (N / 8) * 128 + ((n0 + j) >> 3) * 128 + (p & 7) * 16);
-                    *reinterpret_cast<uint4*>(tile + o) = make_uint4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-                    *reinterpret_cast<uint4*>(tile + kHalf + o) = make_uint4(v[j + 4], v[j + 5], v[j + 6], v[j + 7]);
+                    store_checked(a.states_s, reinterpret_cast<uint4*>(tile + o), make_uint4(v[j], v[j + 1], v[j + 2], v[j + 3]), status);
+                    store_checked(a.states_s, reinterpret_cast<uint4*>(tile + kHalf + o), make_uint4(v[j + 4], v[j + 5], v[j + 6], v[j + 7]), status);
                 }
             }
             tc::fence_before_sync();

@@ -25,7 +25,8 @@ constexpr int kStatusTimeout = 8;
 }  // namespace
 
 // Per-device status word: a kernel that gave up a bounded wait records SSM_ERR_TIMEOUT
-// here (and returns instead of hanging); the host reads and clears it through
+// here (and returns instead of hanging), a store that failed its bounds check (builds
+// with SSM_BOUNDS_CHECK) SSM_ERR_BOUNDS; the host reads and clears it through
 // device_status_take (ssm_device_status).
 __device__ int g_device_status = 0;
 
@@ -44,6 +45,14 @@ __global__ void bounded_wait_selftest(uint32_t max_checks) {
     __syncthreads();
     const bool ok = tc::mbar_wait_bounded(&mbar, 0, max_checks);
     if (!ok && threadIdx.x == 0) report_timeout();
+}
+
+// One thread stores to buf[index] through the bounds check against [buf, buf + bytes):
+// the check's path (record the status, skip the store) on demand.  The caller's buffer
+// holds index, so the address is valid either way.
+__global__ void bounds_selftest(float* buf, Span s, int64_t index) {
+    float* p = buf + index;
+    if (span_ok(s, p, 4, &g_device_status)) *p = 1.0f;
 }
 
 }  // namespace
@@ -88,6 +97,13 @@ cudaError_t device_status_address(int** p) {
     }
     *p = cache[dev];
     return cudaSuccess;
+}
+
+cudaError_t bounds_selftest_launch(float* buf, size_t bytes, int64_t index, cudaStream_t stream) {
+    cudaEvent_t t0 = timing_begin(stream);
+    bounds_selftest<<<1, 1, 0, stream>>>(buf, span_of(buf, bytes), index);
+    note_launch("bounds_selftest", stream, t0);
+    return cudaGetLastError();
 }
 
 cudaError_t bounded_wait_selftest_launch(uint32_t max_checks, cudaStream_t stream) {

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "ssm_device.cuh"
 #include "ssm_internal.h"
 
 namespace ssm {
@@ -24,6 +25,8 @@ struct SsdTcArgs {
     float* cum;     // (b, H, nchunks, Q) inclusive cumsum of Delta*A_h within the chunk
     float* states;  // (b, nchunks, H, P, N): S_c, then (after the carry pass) h_{c-1}
     int64_t T, H, N, G, Q, nchunks;
+    // byte ranges of the buffers written (stores checked in SSM_BOUNDS_CHECK builds)
+    Span out_s, dl_s, cum_s, states_s;
 };
 
 // True when the shape is one the tensor-core kernels take (bf16, headdim 64,

@@ -11,6 +11,7 @@
 #include <vector>
 
 #include "ssm_scan.h"
+#include "ssm_device.cuh"
 #include "ssm_internal.h"
 
 namespace ssm {
@@ -346,7 +347,7 @@ using namespace ssm;
 
 extern "C" {
 
-int ssm_abi_version(void) { return (1 << 16) | 5; }
+int ssm_abi_version(void) { return (1 << 16) | 6; }
 
 int ssm_tuning_set(int knob, int64_t value) {
     if (knob < 0 || knob >= ssm::kKnobs) return SSM_ERR_UNSUPPORTED;
@@ -367,7 +368,21 @@ int ssm_device_status(int clear, ssm_stream_t stream) {
         (void)cudaGetLastError();
         return SSM_ERR_CUDA;
     }
-    return v == 0 ? SSM_OK : SSM_ERR_TIMEOUT;
+    if (v == 0) return SSM_OK;
+    return v == ssm::kStatusBounds ? SSM_ERR_BOUNDS : SSM_ERR_TIMEOUT;
+}
+
+int ssm_bounds_check_enabled(void) { return ssm::kBoundsCheck ? 1 : 0; }
+
+int ssm_selftest_bounds(float* buf, size_t bytes, int64_t index, ssm_stream_t stream) {
+    if (!ssm::kBoundsCheck) return SSM_ERR_UNSUPPORTED;
+    if (!buf) return SSM_ERR_NULL;
+    if (index < 0 || bytes % 4 != 0) return SSM_ERR_SHAPE;
+    if (ssm::bounds_selftest_launch(buf, bytes, index, (cudaStream_t)stream) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SSM_ERR_CUDA;
+    }
+    return SSM_OK;
 }
 
 int ssm_selftest_bounded_wait(uint32_t max_checks, ssm_stream_t stream) {
@@ -432,6 +447,7 @@ const char* ssm_strerror(int status) {
         case SSM_ERR_ALLOC: return "workspace allocation failed or workspace too small";
         case SSM_ERR_CUDA: return "a CUDA call failed";
         case SSM_ERR_TIMEOUT: return "a bounded device-side wait ran out";
+        case SSM_ERR_BOUNDS: return "a store address fell outside its buffer (bounds-checked build)";
         default: return "unknown status";
     }
 }

@@ -146,6 +146,9 @@ struct BwdArgs {
     int64_t L, dim, N, G, cpg;  // L: sequence length; dim: channels (SSD: heads x P)
     int64_t P;                  // channels per head (SSD headdim; 1 in diagonal mode)
     int nseg, tiles_per_group, subs_per_part;
+    // byte ranges of the buffers written (stores checked in SSM_BOUNDS_CHECK builds)
+    int* status;
+    Span dx_s, ddt_s, dA_s, dB_s, dC_s, dD_s, dz_s, ddtb_s, dinit_s, ckpt_s, hloc_s, qloc_s, dsum_s;
 };
 
 template <int LPC>
@@ -244,7 +247,7 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
         if (!PARTS) {
 #pragma unroll
             for (int r = 0; r < R; ++r)
-                if (nok[r]) a.ckpt[((b * a.nseg + seg) * dim + c) * N + nr[r]] = h[r];
+                if (nok[r]) store_checked(a.ckpt_s, &a.ckpt[((b * a.nseg + seg) * dim + c) * N + nr[r]], h[r], a.status);
         }
         const int len = (int)min((int64_t)kSeg, L - t0);
         float pde[SPL], pu[SPL];
@@ -276,11 +279,11 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
         // the part's Delta sum and local end state; then its local adjoint, from zero at
         // its end, carried out of its first step (g_t = dy_t C_t + a_{t+1} g_{t+1})
         const float dsum = lane_sum<LPC>(dsum_lane);
-        if (c_ok && lane == 0) a.Dsum[sidx(part)] = dsum;
+        if (c_ok && lane == 0) store_checked(a.dsum_s, &a.Dsum[sidx(part)], dsum, a.status);
         if (part < nparts - 1) {
 #pragma unroll
             for (int r = 0; r < R; ++r)
-                if (nok[r]) a.Hloc[sidx(part) * N + nr[r]] = h[r];
+                if (nok[r]) store_checked(a.hloc_s, &a.Hloc[sidx(part) * N + nr[r]], h[r], a.status);
         }
         if (part == 0) return;
         float q[R];
@@ -321,7 +324,7 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
         }
 #pragma unroll
         for (int r = 0; r < R; ++r)
-            if (nok[r]) a.Qloc[sidx(part) * N + nr[r]] = q[r];
+            if (nok[r]) store_checked(a.qloc_s, &a.Qloc[sidx(part) * N + nr[r]], q[r], a.status);
     } else {
         // reverse sweep: the adjoint entering the part's last step, folded from the later
         // parts
@@ -414,15 +417,15 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
                 }
                 if (c_ok && lane == j % LPC) {  // the lane that holds step j's scalars
                     const int k = j / LPC;
-                    a.dx[row(t)] = fmaf(dy, Dc, dxp);
+                    store_checked(a.dx_s, &a.dx[row(t)], fmaf(dy, Dc, dxp), a.status);
                     const float dv = ddp * psig[k];
                     if (SSD)
-                        atomicAdd(&a.ddt[drow(t)], dv);  // the head's channels share Delta_t
+                        atomic_add_checked(a.ddt_s, &a.ddt[drow(t)], dv, a.status);  // the head's channels share Delta_t
                     else
-                        a.ddt[row(t)] = dv;
+                        store_checked(a.ddt_s, &a.ddt[row(t)], dv, a.status);
                     dbias_acc += dv;
                     dD_acc = fmaf(dy, xv, dD_acc);
-                    if (a.z) a.dz[row(t)] = pdz[k] * (yp + Dc * xv);
+                    if (a.z) store_checked(a.dz_s, &a.dz[row(t)], pdz[k] * (yp + Dc * xv), a.status);
                 }
             }
             __syncthreads();  // the segment's dB / dC terms are in shared memory
@@ -436,8 +439,8 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
                         sc += s_dC[(j * CPB + q) * SNP + n];
                     }
                     const int64_t o = bc(t0 + j) + n;
-                    atomicAdd(&a.dB[o], sb);
-                    atomicAdd(&a.dC[o], sc);
+                    atomic_add_checked(a.dB_s, &a.dB[o], sb, a.status);
+                    atomic_add_checked(a.dC_s, &a.dC[o], sc, a.status);
                 }
             }
             __syncthreads();  // read before the next segment overwrites them
@@ -448,17 +451,17 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
 #pragma unroll
         for (int r = 0; r < R; ++r)
             if (nok[r]) {
-                if (a.dinit && part == 0) a.dinit[(b * dim + c) * N + nr[r]] = g[r];
+                if (a.dinit && part == 0) store_checked(a.dinit_s, &a.dinit[(b * dim + c) * N + nr[r]], g[r], a.status);
                 if (SSD)
                     dA_sum += dA_acc[r];
                 else
-                    atomicAdd(&a.dA[c * N + nr[r]], dA_acc[r]);
+                    atomic_add_checked(a.dA_s, &a.dA[c * N + nr[r]], dA_acc[r], a.status);
             }
         if (SSD) dA_sum = lane_sum<LPC>(dA_sum);
         if (c_ok && lane == 0) {
-            if (SSD) atomicAdd(&a.dA[hd], dA_sum);
-            if (a.dD) atomicAdd(&a.dD[hd], dD_acc);
-            if (a.ddt_bias) atomicAdd(&a.ddt_bias[hd], dbias_acc);
+            if (SSD) atomic_add_checked(a.dA_s, &a.dA[hd], dA_sum, a.status);
+            if (a.dD) atomic_add_checked(a.dD_s, &a.dD[hd], dD_acc, a.status);
+            if (a.ddt_bias) atomic_add_checked(a.ddtb_s, &a.ddt_bias[hd], dbias_acc, a.status);
         }
     }
 }
@@ -559,6 +562,27 @@ cudaError_t bwd_typed(const ScanBwdArgs& s, void* ws, cudaStream_t stream) {
     a.G = f.ngroups;
     a.cpg = a.dim / f.ngroups;
     a.tiles_per_group = 0;
+    a.status = nullptr;
+    if (kBoundsCheck) {
+        const cudaError_t e = device_status_address(&a.status);
+        if (e != cudaSuccess) return e;
+    }
+    const size_t tok = (size_t)f.batch * f.seqlen;
+    const size_t ch = (size_t)f.batch * a.dim;
+    a.dx_s = span_of(s.dx, tok * a.dim * 4);
+    a.ddt_s = span_of(s.ddt, tok * (ssd ? f.nheads : a.dim) * 4);
+    a.dA_s = span_of(s.dA, (size_t)f.nheads * (ssd ? 1 : f.dstate) * 4);
+    a.dB_s = span_of(s.dB, tok * f.ngroups * f.dstate * 4);
+    a.dC_s = span_of(s.dC, tok * f.ngroups * f.dstate * 4);
+    a.dD_s = span_of(s.dD, (size_t)f.nheads * 4);
+    a.dz_s = span_of(s.dz, tok * a.dim * 4);
+    a.ddtb_s = span_of(s.ddt_bias, (size_t)f.nheads * 4);
+    a.dinit_s = span_of(s.dinit, ch * f.dstate * 4);
+    a.ckpt_s = span_of(a.ckpt, ch * pl.nseg * f.dstate * 4);
+    const size_t hq = pl.parts > 1 ? ch * pl.parts * f.dstate * 4 : 0;
+    a.hloc_s = span_of(a.Hloc, hq);
+    a.qloc_s = span_of(a.Qloc, hq);
+    a.dsum_s = span_of(a.Dsum, pl.parts > 1 ? ch * pl.parts * 4 : 0);
     return launch_any<T>(ssd, pl.lpc, pl.r, a, pl.parts, f.batch, stream);
 }
 

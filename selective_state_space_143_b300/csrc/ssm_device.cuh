@@ -11,6 +11,50 @@ namespace ssm {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// ---- bounds checks (builds with SSM_BOUNDS_CHECK) ---------------------------------
+// A store site checks its address against the byte range of the buffer it writes.  In a
+// build with SSM_BOUNDS_CHECK an address outside the range is not written: the kernel
+// records status code kStatusBounds in the per-device status word (the first code
+// recorded stays) and skips the store.  Other builds compile the check away.
+constexpr int kStatusBounds = 9;
+
+struct Span {
+    const char* lo = nullptr;  // first byte of the buffer
+    const char* hi = nullptr;  // one past its last byte
+};
+
+inline Span span_of(const void* base, size_t bytes) {
+    Span s;
+    s.lo = static_cast<const char*>(base);
+    s.hi = s.lo + (base ? bytes : 0);
+    return s;
+}
+
+#ifdef SSM_BOUNDS_CHECK
+constexpr bool kBoundsCheck = true;
+#else
+constexpr bool kBoundsCheck = false;
+#endif
+
+__device__ __forceinline__ bool span_ok(const Span& s, const void* p, int bytes, int* status) {
+    if (!kBoundsCheck) return true;
+    const char* q = static_cast<const char*>(p);
+    if (q >= s.lo && q + bytes <= s.hi) return true;
+    if (status) atomicCAS(status, 0, kStatusBounds);
+    return false;
+}
+
+// atomicAdd(p, v) when p lies in the span (always, without SSM_BOUNDS_CHECK).
+__device__ __forceinline__ void atomic_add_checked(const Span& s, float* p, float v, int* status) {
+    if (span_ok(s, p, 4, status)) atomicAdd(p, v);
+}
+
+// *p = v when p lies in the span (always, without SSM_BOUNDS_CHECK).
+template <typename V>
+__device__ __forceinline__ void store_checked(const Span& s, V* p, V v, int* status) {
+    if (span_ok(s, p, (int)sizeof(V), status)) *p = v;
+}
+
 // 2^x on the special-function unit (ex2.approx, flush-to-zero).
 __device__ __forceinline__ float ex2(float x) {
     float y;

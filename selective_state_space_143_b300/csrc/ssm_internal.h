@@ -84,14 +84,17 @@ cudaError_t scan_bwd_launch(const ScanBwdArgs& s, void* ws, cudaStream_t stream)
 cudaError_t conv_prepass_launch(const ScanArgs& a, void* xc, bool split, cudaStream_t stream);
 cudaError_t conv_tail_launch(const ScanArgs& a, cudaStream_t stream);
 
-// Per-device status word of bounded device-side waits: read into *status (0 or
-// SSM_ERR_TIMEOUT) after the stream's work, cleared when `clear`.
+// Per-device status word of bounded device-side waits and bounds checks: read into
+// *status (0, SSM_ERR_TIMEOUT or SSM_ERR_BOUNDS) after the stream's work, cleared when
+// `clear`.
 cudaError_t device_status_take(int* status, bool clear, cudaStream_t stream);
 // Device address of that status word for the current device (looked up once per device),
 // for kernels in other translation units, which record SSM_ERR_TIMEOUT through it.
 cudaError_t device_status_address(int** p);
 // One CTA waiting on an mbarrier that nothing completes, giving up after max_checks polls.
 cudaError_t bounded_wait_selftest_launch(uint32_t max_checks, cudaStream_t stream);
+// One thread storing to buf + index * 4 through the bounds check against [buf, buf + bytes).
+cudaError_t bounds_selftest_launch(float* buf, size_t bytes, int64_t index, cudaStream_t stream);
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 

@@ -45,6 +45,9 @@ struct StepArgs {
     int64_t batch, H, P, N, G;
     int diag;  // A per (channel, n) when set, one scalar per head otherwise
     int conv_k;
+    // byte ranges of the buffers written (stores checked in SSM_BOUNDS_CHECK builds)
+    int* status;
+    Span state_s, out_s, xlast_s;
 };
 
 // Four consecutive elements of a B or C row as fp32 (the row start is 8-byte aligned for
@@ -123,7 +126,7 @@ __global__ void __launch_bounds__(kStepThreads) ssm_step_kernel(const StepArgs a
             hn.y = fmaf(av.y, hn.y, u * Bv[q].y);
             hn.z = fmaf(av.z, hn.z, u * Bv[q].z);
             hn.w = fmaf(av.w, hn.w, u * Bv[q].w);
-            *reinterpret_cast<float4*>(st + n) = hn;
+            store_checked(a.state_s, reinterpret_cast<float4*>(st + n), hn, a.status);
             y = fmaf(Cv[q].x, hn.x, y);
             y = fmaf(Cv[q].y, hn.y, y);
             y = fmaf(Cv[q].z, hn.z, y);
@@ -140,11 +143,12 @@ __global__ void __launch_bounds__(kStepThreads) ssm_step_kernel(const StepArgs a
         const int64_t c = cs;
         const int km1 = a.conv_k - 1;
         T* xl = static_cast<T*>(a.x_last) + b * km1 * nc + c;
-        for (int j = 0; j < km1; ++j) xl[j * nc] = from_f32<T>(j + 1 < km1 ? prev[j + 1] : x_raw);
+        for (int j = 0; j < km1; ++j)
+            store_checked(a.xlast_s, &xl[j * nc], from_f32<T>(j + 1 < km1 ? prev[j + 1] : x_raw), a.status);
     }
     if (a.D) y = fmaf(a.D[h], xv, y);
     if (a.z) y *= silu_t<PRECISE>(to_f32<T>(static_cast<const T*>(a.z)[ch]));
-    static_cast<T*>(a.out)[ch] = from_f32<T>(y);
+    store_checked(a.out_s, &static_cast<T*>(a.out)[ch], from_f32<T>(y), a.status);
 }
 
 template <typename T, int LPC, int PPL>
@@ -198,6 +202,15 @@ cudaError_t step_launch(const ScanArgs& a, bool diag_a, float* state, cudaStream
     s.x_last = a.x_last;
     s.conv_k = a.conv_k;
     const int64_t nch = a.batch * a.nheads * a.headdim;
+    s.status = nullptr;
+    if (kBoundsCheck) {
+        const cudaError_t e = device_status_address(&s.status);
+        if (e != cudaSuccess) return e;
+    }
+    const size_t E = a.dtype == 1 ? 2 : 4;
+    s.state_s = span_of(state, (size_t)nch * a.dstate * sizeof(float));
+    s.out_s = span_of(a.out, (size_t)nch * E);
+    s.xlast_s = span_of(a.x_last, (size_t)a.batch * (a.conv_k > 1 ? a.conv_k - 1 : 0) * a.nheads * a.headdim * E);
     if (nch == 0) return cudaSuccess;
     cudaEvent_t t0 = timing_begin(stream);
     if (a.dtype == 1)

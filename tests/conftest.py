@@ -36,3 +36,19 @@ def record_errors(name, reports):
     if path:
         with open(path, "a") as f:
             f.write(json.dumps(line) + "\n")
+
+
+@pytest.fixture(autouse=True)
+def _bounds_checked_status(request):
+    """Under SSM_EXPECT_BOUNDS_CHECK=1 (the bounds-checked library loaded through
+    SSM_LIB_PATH), every GPU test must leave the device status clean: no store of any
+    kernel it ran fell outside its buffer."""
+    yield
+    if os.environ.get("SSM_EXPECT_BOUNDS_CHECK") != "1" or "gpu" not in request.keywords:
+        return
+    import selective_state_space_143_b300 as ssm
+    from selective_state_space_143_b300 import _lib
+    assert ssm.bounds_check_enabled(), "SSM_EXPECT_BOUNDS_CHECK set but the library has no checks"
+    import torch
+    torch.cuda.synchronize()
+    assert ssm.device_status(clear=True) == _lib.SSM_OK, "a bounds check fired"

@@ -381,3 +381,33 @@ def test_complex_mode_shapes_and_unsupported_entry_points():
     assert lib.ssm_scan_fwd_conv(vp(1 << 12), vp(2 << 12), vp(3 << 12), vp(4 << 12), vp(5 << 12),
                                  None, None, None, ctypes.byref(c), None, vp(6 << 20), None,
                                  ctypes.byref(s), None, 0, None) == _lib.SSM_ERR_UNSUPPORTED
+
+
+def test_bounds_check_entry_points_without_checks():
+    """The normal build has no store checks: it says so, and the bounds self-test is
+    refused before any launch."""
+    lib = _lib.load()
+    if os.environ.get("SSM_LIB_PATH"):
+        pytest.skip("another library is loaded")
+    assert lib.ssm_bounds_check_enabled() == 0
+    assert lib.ssm_selftest_bounds(None, 16, 1, None) == _lib.SSM_ERR_UNSUPPORTED
+    assert lib.ssm_strerror(_lib.SSM_ERR_BOUNDS).decode().startswith("a store address")
+
+
+def test_bounds_checked_library_exports_and_host_checks():
+    """libssmscan_bc.so (built with -DSSM_BOUNDS_CHECK) exports the same symbols, reports
+    its checks, and rejects a NULL or malformed self-test before any launch."""
+    from selective_state_space_143_b300 import build as _build
+    path = _build.OUT_BC
+    if not os.path.exists(path):
+        pytest.skip("bounds-checked library not built (build.py --bounds-check)")
+    bc = ctypes.CDLL(path)
+    for name in _lib.EXPORTED:
+        assert hasattr(bc, name), name
+    bc.ssm_bounds_check_enabled.restype = ctypes.c_int
+    bc.ssm_selftest_bounds.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int64, ctypes.c_void_p]
+    bc.ssm_selftest_bounds.restype = ctypes.c_int
+    assert bc.ssm_bounds_check_enabled() == 1
+    assert bc.ssm_selftest_bounds(None, 16, 1, None) == _lib.SSM_ERR_NULL
+    assert bc.ssm_selftest_bounds(ctypes.c_void_p(0x1000), 16, -1, None) == _lib.SSM_ERR_SHAPE
+    assert bc.ssm_selftest_bounds(ctypes.c_void_p(0x1000), 15, 1, None) == _lib.SSM_ERR_SHAPE
