@@ -537,6 +537,35 @@ cudaError_t ssd_launch_typed(const ScanArgs& a, void* ws, cudaStream_t stream) {
 
 }  // namespace
 
+cudaError_t ssd_tc_forward_carry(const ScanArgs& a, int64_t Q, int64_t nchunks, const float* cum, float* states,
+                                 float* final_state, cudaStream_t stream) {
+    SsdArgs s = {};
+    s.init = a.initial_state;
+    s.final_state = final_state;
+    s.cum = const_cast<float*>(cum);
+    s.states = states;
+    s.T = a.seqlen;
+    s.H = a.nheads;
+    s.P = a.headdim;
+    s.N = a.dstate;
+    s.G = a.ngroups;
+    s.Q = Q;
+    s.nchunks = nchunks;
+    s.status = nullptr;
+    if (kBoundsCheck) {
+        const cudaError_t e = device_status_address(&s.status);
+        if (e != cudaSuccess) return e;
+    }
+    s.final_s = span_of(final_state, (size_t)a.batch * a.nheads * a.headdim * a.dstate * sizeof(float));
+    s.states_s = span_of(states, (size_t)a.batch * nchunks * a.nheads * a.headdim * a.dstate * sizeof(float));
+    cudaEvent_t t0 = timing_begin(stream);
+    ssd_state_pass_split<<<dim3((unsigned)((a.headdim * a.dstate / 8 + kThreads - 1) / kThreads), (unsigned)a.nheads,
+                                (unsigned)a.batch),
+                           kThreads, 0, stream>>>(s);
+    note_launch("ssd_state_pass_split", stream, t0);
+    return cudaGetLastError();
+}
+
 bool ssd_conv_split(const ScanArgs& a) {
     const SsdPlan pl = ssd_plan(a);
     return pl.nchunks > 0 && ssd_tc_supported(a, pl.Q) && !force_cuda_cores();

@@ -88,7 +88,13 @@ __device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint3
 
 // grid (nchunks, H / hpc, batch); 10 warps.  Heads [hpc * blockIdx.y, +hpc) (hpc even,
 // a divisor of the heads of a group) of chunk blockIdx.x.
-template <int N, bool XS>
+//
+// ADJ: the adjoint chunk states of the backward pass instead,
+//   S^g_c[p, n] = sum_t exp(cum_t) dy_t[p] C_t[n]
+// with tm_x / tm_xlo the hi / lo planes of dy, tm_b the C rows, and weights exp(cum_t)
+// (the gradient carried into the chunk from its outputs); Delta and the cumulative sums
+// are recomputed for the weights but not stored (the forward pass stored them).
+template <int N, bool XS, bool ADJ>
 __global__ void __launch_bounds__(kCta, 1)
     ssd_state_tc(const SsdTcArgs a, const int hpc, int* status, const __grid_constant__ CUtensorMap tm_x,
                  const __grid_constant__ CUtensorMap tm_xlo, const __grid_constant__ CUtensorMap tm_b) {
@@ -235,10 +241,14 @@ __global__ void __launch_bounds__(kCta, 1)
 #pragma unroll
                 for (int k = 0; k < kMaxHeads; ++k) {
                     if (k >= hpc) break;
-                    const int64_t o = (((int64_t)b * a.H + hbeg + k) * a.nchunks + c) * a.Q + s;
-                    store_checked(a.dl_s, &a.dl[o], d[k], status);
-                    store_checked(a.cum_s, &a.cum[o], v[k], status);
-                    sW[k * 256 + s] = s < len ? __expf(last[k] - v[k]) * d[k] : 0.0f;
+                    if (ADJ) {
+                        sW[k * 256 + s] = s < len ? __expf(v[k]) : 0.0f;
+                    } else {
+                        const int64_t o = (((int64_t)b * a.H + hbeg + k) * a.nchunks + c) * a.Q + s;
+                        store_checked(a.dl_s, &a.dl[o], d[k], status);
+                        store_checked(a.cum_s, &a.cum[o], v[k], status);
+                        sW[k * 256 + s] = s < len ? __expf(last[k] - v[k]) * d[k] : 0.0f;
+                    }
                 }
             }
             compute_sync();
@@ -374,7 +384,7 @@ int state_heads_per_cta(const SsdTcArgs& s) {
     return 2;
 }
 
-template <int N, bool XS>
+template <int N, bool XS, bool ADJ>
 cudaError_t launch_state(const SsdTcArgs& s, int64_t batch, cudaStream_t stream) {
     using Cfg = StateCfg<N, XS>;
     CUtensorMap tx, txl, tb;
@@ -386,7 +396,7 @@ cudaError_t launch_state(const SsdTcArgs& s, int64_t batch, cudaStream_t stream)
     int* status = nullptr;
     cudaError_t e = device_status_address(&status);
     if (e != cudaSuccess) return e;
-    auto kern = ssd_state_tc<N, XS>;
+    auto kern = ssd_state_tc<N, XS, ADJ>;
     static_assert(sizeof(StateShared) <= 512, "pipeline state");
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmemTotal);
     if (e != cudaSuccess) return e;
@@ -394,16 +404,16 @@ cudaError_t launch_state(const SsdTcArgs& s, int64_t batch, cudaStream_t stream)
     cudaEvent_t t0 = timing_begin(stream);
     kern<<<dim3((unsigned)s.nchunks, (unsigned)(s.H / hpc), (unsigned)batch), kCta, Cfg::kSmemTotal, stream>>>(
         s, hpc, status, tx, txl, tb);
-    note_launch("ssd_state_tc", stream, t0);
+    note_launch(ADJ ? "ssd_state_tc (adjoint)" : "ssd_state_tc", stream, t0);
     return cudaGetLastError();
 }
 
 template <bool XS>
 cudaError_t launch_state_n(const SsdTcArgs& s, int64_t batch, cudaStream_t stream) {
     switch (s.N) {
-        case 64: return launch_state<64, XS>(s, batch, stream);
-        case 128: return launch_state<128, XS>(s, batch, stream);
-        default: return launch_state<256, XS>(s, batch, stream);
+        case 64: return launch_state<64, XS, false>(s, batch, stream);
+        case 128: return launch_state<128, XS, false>(s, batch, stream);
+        default: return launch_state<256, XS, false>(s, batch, stream);
     }
 }
 
@@ -411,6 +421,15 @@ cudaError_t launch_state_n(const SsdTcArgs& s, int64_t batch, cudaStream_t strea
 
 cudaError_t ssd_tc_chunk_state(const SsdTcArgs& s, int64_t batch, cudaStream_t stream) {
     return s.x_lo ? launch_state_n<true>(s, batch, stream) : launch_state_n<false>(s, batch, stream);
+}
+
+cudaError_t ssd_tc_chunk_state_adjoint(const SsdTcArgs& s, int64_t batch, cudaStream_t stream) {
+    if (!s.x_lo) return cudaErrorInvalidValue;
+    switch (s.N) {
+        case 64: return launch_state<64, true, true>(s, batch, stream);
+        case 128: return launch_state<128, true, true>(s, batch, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace ssm

@@ -36,7 +36,27 @@ bool ssd_tc_supported(const ScanArgs& a, int64_t Q);
 // S_c for every (chunk, head) into states; also writes dl and cum.
 cudaError_t ssd_tc_chunk_state(const SsdTcArgs& s, int64_t batch, cudaStream_t stream);
 
+// Adjoint chunk states of the backward pass, S^g_c = sum_t exp(cum_t) dy_t C_t^T for
+// every (chunk, head) into states (split-ready layout), with x / x_lo the hi / lo planes
+// of dy and B the C rows; reads dt for the weights, writes neither dl nor cum.  dstate
+// 64 or 128.
+cudaError_t ssd_tc_chunk_state_adjoint(const SsdTcArgs& s, int64_t batch, cudaStream_t stream);
+
 // out for every chunk, reading h_{c-1} from states (after the carry pass).
 cudaError_t ssd_tc_chunk_scan(const SsdTcArgs& s, int64_t batch, bool gate, cudaStream_t stream);
+
+// The tensor-core path's carry over chunks of length Q (states in the split-ready layout
+// of ssd_tc_chunk_state, rewritten in place as h_{c-1} bf16 hi/lo tiles), from
+// a.initial_state; final_state (b, H, P, N) fp32 or null.
+cudaError_t ssd_tc_forward_carry(const ScanArgs& a, int64_t Q, int64_t nchunks, const float* cum, float* states,
+                                 float* final_state, cudaStream_t stream);
+
+// Backward pass of the SSD scan in chunk form on the tensor cores (ssd_bwd_tc.cu): bf16,
+// headdim 64, dstate 64 or 128, the tensor-core forward's head grouping, no convolution.
+bool ssd_bwd_tc_supported(const ScanArgs& a);
+size_t ssd_bwd_tc_workspace_bytes(const ScanArgs& a);
+// Every gradient of ScanBwdArgs; dA, dB, dC, dD and ddt_bias must be zero on entry (they
+// are accumulated); dx, ddt, dz and dinit are written.
+cudaError_t ssd_bwd_tc_launch(const ScanBwdArgs& s, void* ws, cudaStream_t stream);
 
 }  // namespace ssm

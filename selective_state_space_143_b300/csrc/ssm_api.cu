@@ -529,7 +529,7 @@ size_t ssm_scan_bwd_workspace_size(const ssm_shape* shape) {
     if (check_shape(shape) != SSM_OK || shape->mode == SSM_MODE_CDIAG) return (size_t)-1;
     const ScanArgs a = make_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
                                  nullptr, nullptr, nullptr, shape);
-    return scan_bwd_workspace_bytes(a);
+    return scan_bwd_workspace_bytes(a, shape->mode == SSM_MODE_SSD);
 }
 
 int ssm_scan_bwd(const void* x, const void* dt, const float* A, const void* B, const void* C,
@@ -561,7 +561,7 @@ int ssm_scan_bwd(const void* x, const void* dt, const float* A, const void* B, c
     s.dz = z ? dz : nullptr;
     s.ddt_bias = dt_bias ? ddt_bias : nullptr;
     s.dinit = dinitial_state;
-    const size_t need = scan_bwd_workspace_bytes(s.fwd);
+    const size_t need = scan_bwd_workspace_bytes(s.fwd, s.ssd);
     cudaStream_t st = (cudaStream_t)stream;
     void* ws = workspace;
     bool owned = false;

@@ -38,6 +38,7 @@
 #include <cstdlib>
 
 #include "ssm_device.cuh"
+#include "ssd_tc.h"
 #include "ssm_internal.h"
 
 namespace ssm {
@@ -588,7 +589,16 @@ cudaError_t bwd_typed(const ScanBwdArgs& s, void* ws, cudaStream_t stream) {
 
 }  // namespace
 
-size_t scan_bwd_workspace_bytes(const ScanArgs& a) { return bwd_plan(a).total; }
+// The chunked tensor-core backward takes the SSD shapes it supports (bf16, headdim 64,
+// dstate 64 or 128) unless SSM_TUNE_SSD_CUDA_CORES keeps SSD on the CUDA cores; every
+// other shape runs the recurrence kernel above.
+bool use_ssd_tc_bwd(const ScanArgs& a, bool ssd) {
+    return ssd && a.batch > 0 && ssd_bwd_tc_supported(a) && tuning(1) != 1;
+}
+
+size_t scan_bwd_workspace_bytes(const ScanArgs& a, bool ssd) {
+    return use_ssd_tc_bwd(a, ssd) ? ssd_bwd_tc_workspace_bytes(a) : bwd_plan(a).total;
+}
 
 cudaError_t scan_bwd_launch(const ScanBwdArgs& s, void* ws, cudaStream_t stream) {
     const ScanArgs& f = s.fwd;
@@ -605,6 +615,7 @@ cudaError_t scan_bwd_launch(const ScanBwdArgs& s, void* ws, cudaStream_t stream)
             if (e != cudaSuccess) return e;
         }
     if (f.batch == 0) return cudaSuccess;
+    if (use_ssd_tc_bwd(f, s.ssd)) return ssd_bwd_tc_launch(s, ws, stream);
     if (f.dtype == 1) return bwd_typed<__nv_bfloat16>(s, ws, stream);
     return bwd_typed<float>(s, ws, stream);
 }

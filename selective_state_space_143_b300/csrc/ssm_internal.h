@@ -72,7 +72,7 @@ struct ScanBwdArgs {
     const float* dfinal;
     float *dx, *ddt, *dA, *dB, *dC, *dD, *dz, *ddt_bias, *dinit;
 };
-size_t scan_bwd_workspace_bytes(const ScanArgs& a);
+size_t scan_bwd_workspace_bytes(const ScanArgs& a, bool ssd);
 cudaError_t scan_bwd_launch(const ScanBwdArgs& s, void* ws, cudaStream_t stream);
 
 // Convolution + SiLU of x into xc, and the last conv_k-1 inputs into a.x_last; used

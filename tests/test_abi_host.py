@@ -279,14 +279,25 @@ def test_backward_argument_errors():
                 return p
         return None
 
-    # SSD mode: the state of every (head, p) channel every 4 steps at dstate 128 and 256;
-    # with this many channels the sequence is not split into time parts
-    ssd = _shape(mode=1, batch=16, nheads=64, headdim=64, dstate=128, chunk=64)
+    # SSD mode on the recurrence kernel (fp32, or dstate 256): the state of every (head, p)
+    # channel every 4 steps at dstate 128 and 256; with this many channels the sequence is
+    # not split into time parts
+    ssd = _shape(mode=1, dtype=0, batch=16, nheads=64, headdim=64, dstate=128, chunk=64)
     assert lib.ssm_scan_bwd_workspace_size(ctypes.byref(ssd)) == 16 * (64 // 4) * 64 * 64 * 128 * 4
     ssd256 = _shape(mode=1, batch=16, nheads=64, headdim=64, dstate=256)
     assert lib.ssm_scan_bwd_workspace_size(ctypes.byref(ssd256)) == 16 * (64 // 4) * 64 * 64 * 256 * 4
+    # SSD mode on the chunked tensor-core backward (bf16, headdim 64, dstate 64 or 128):
+    # chunks of 128 steps; Delta and the cumulative sums, the forward and the adjoint chunk
+    # states, <R, h_out> per chunk, the final state, y before the gate and the two dy planes
+    a256 = lambda n: -(-n // 256) * 256
+    for b_, T_, H_, N_ in ((16, 64, 64, 128), (3, 300, 4, 64)):
+        tcs = _shape(mode=1, batch=b_, seqlen=T_, nheads=H_, headdim=64, dstate=N_)
+        nc = -(-T_ // 128)
+        want = (2 * a256(b_ * H_ * nc * 128 * 4) + 2 * a256(b_ * nc * H_ * 64 * N_ * 4) + a256(b_ * H_ * nc * 4)
+                + a256(b_ * H_ * 64 * N_ * 4) + 3 * a256(b_ * T_ * H_ * 64 * 2))
+        assert lib.ssm_scan_bwd_workspace_size(ctypes.byref(tcs)) == want
     # few channels: the checkpoints plus the summaries of several time parts
-    small = _shape(mode=1, nheads=8, headdim=64, dstate=128, chunk=64)
+    small = _shape(mode=1, dtype=0, nheads=8, headdim=64, dstate=128, chunk=64)
     ckpt = 2 * (64 // 4) * 8 * 64 * 128 * 4
     n = lib.ssm_scan_bwd_workspace_size(ctypes.byref(small))
     assert n > ckpt and (parts_extra(n - ckpt, 2 * 8 * 64, 128) or 0) > 1
@@ -346,7 +357,7 @@ def test_tuning_knobs():
     assert lib.ssm_tuning_set(99, 1) == _lib.SSM_ERR_UNSUPPORTED
     assert lib.ssm_tuning_set(_lib.SSM_TUNE_BWD_PARTS, -1) == _lib.SSM_ERR_SHAPE
     assert lib.ssm_tuning_get(99) == 0
-    s = _shape(mode=1, nheads=8, headdim=64, dstate=128, chunk=64)
+    s = _shape(mode=1, dtype=0, nheads=8, headdim=64, dstate=128, chunk=64)  # recurrence kernel
     default = lib.ssm_scan_bwd_workspace_size(ctypes.byref(s))
     with _lib.tuned(_lib.SSM_TUNE_BWD_PARTS, 1):
         assert _lib.tuning_get(_lib.SSM_TUNE_BWD_PARTS) == 1
@@ -356,6 +367,13 @@ def test_tuning_knobs():
     # shape into several parts, each with its own summaries
     assert one_part < default
     assert lib.ssm_scan_bwd_workspace_size(ctypes.byref(s)) == default
+    # the CUDA-core knob moves a bf16 SSD backward from the chunked tensor-core path (its
+    # own scratch) to the recurrence kernel
+    t = _shape(mode=1, nheads=8, headdim=64, dstate=128)
+    tc_ws = lib.ssm_scan_bwd_workspace_size(ctypes.byref(t))
+    with _lib.tuned(_lib.SSM_TUNE_SSD_CUDA_CORES, 1):
+        rec_ws = lib.ssm_scan_bwd_workspace_size(ctypes.byref(t))
+    assert tc_ws != rec_ws and lib.ssm_scan_bwd_workspace_size(ctypes.byref(t)) == tc_ws
 
 
 def test_complex_mode_shapes_and_unsupported_entry_points():

@@ -11,7 +11,10 @@ import torch
 
 import oracle
 import selective_state_space_143_b300 as ssm
+from selective_state_space_143_b300 import _lib
 from selective_state_space_143_b300.inputs import WORKLOADS, make_inputs, random_inputs
+
+from conftest import record_errors
 
 pytestmark = pytest.mark.gpu
 
@@ -156,3 +159,40 @@ def test_backward_ssd_many_channels():
     w, inp = random_inputs("ssd", "bf16", 2, 24, 16, 64, 128, ngroups=2, seed=11)
     dout, dfinal, h0 = extras(w, seed=12)
     compare(w, inp, dout, dfinal, h0)
+
+
+# The chunked tensor-core backward (bf16, headdim 64, dstate 64 or 128, an even number of
+# heads per group): chunks of 128 steps, ragged last chunks, groups, every optional input
+# present or absent.  (dtype, batch, T, H, P, N, G, gate, bias, skip, init, dfinal)
+TC_CASES = [
+    ("bf16", 2, 300, 4, 64, 64, 1, True, True, True, True, True),
+    ("bf16", 1, 128, 2, 64, 128, 1, False, False, False, False, False),
+    ("bf16", 2, 257, 6, 64, 128, 3, True, True, True, False, True),
+    ("bf16", 1, 1, 2, 64, 64, 1, True, True, True, True, True),
+    ("bf16", 3, 129, 8, 64, 64, 2, True, False, True, True, False),
+    ("bf16", 1, 1000, 2, 64, 128, 1, True, True, True, True, True),
+]
+
+
+@pytest.mark.parametrize("case", TC_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_backward_ssd_tensor_core(case):
+    dtype, b, T, H, P, N, G, gate, bias, skip, init, dfin = case
+    w, inp = random_inputs("ssd", dtype, b, T, H, P, N, ngroups=G, gate=gate, dt_bias=bias,
+                           d_skip="normal" if skip else "none", seed=T + H + N + 7)
+    dout, dfinal, h0 = extras(w, seed=T + 5, with_init=init, with_dfinal=dfin)
+    errs = compare(w, inp, dout, dfinal, h0)
+    record_errors(f"ssd backward tc {case}", {k: {"gated": v} for k, v in errs.items()})
+
+
+def test_backward_ssd_tensor_core_matches_recurrence_kernel():
+    """The chunked tensor-core backward and the recurrence kernel (SSM_TUNE_SSD_CUDA_CORES)
+    agree on the same inputs within the bf16 bound."""
+    w, inp = random_inputs("ssd", "bf16", 2, 400, 4, 64, 128, gate=True, dt_bias=True, seed=41)
+    dout, dfinal, h0 = extras(w, seed=42)
+    tc = grads_gpu(inp, dout, dfinal, h0)
+    with _lib.tuned(_lib.SSM_TUNE_SSD_CUDA_CORES, 1):
+        rec = grads_gpu(inp, dout, dfinal, h0)
+    for k in tc:
+        if tc[k] is None:
+            continue
+        assert oracle.max_rel_error(tc[k], rec[k]) <= 2e-2, k
