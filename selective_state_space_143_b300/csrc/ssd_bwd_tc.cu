@@ -235,29 +235,31 @@ __global__ void __launch_bounds__(256) ssd_bwd_reverse_carry(const RevArgs a) {
 //              (TMA).  K-major operands along n (G = C B^T, B R^T), MN-major along t (Z B,
 //              Z^T C).
 //   sDy      : dy hi and lo planes of the head, [t][64] swizzled (TMA): K-major along p
-//              (dY X^T, later e^cum dY h) and MN-major along t (M^T dY).  Rescaled in place
-//              by exp(cum_t) once M^T dY has read it.
+//              (dY X^T) and MN-major along t (M^T dY); the epilogue reads D dy from it.
 //   region A : the head's x rows [s][64] swizzled (TMA) for dY X^T; then M hi/lo (no
 //              swizzle, K-major along s: (t, s) at (t/8)*2048 + (s/8)*128 + (t%8)*16 +
-//              (s%8)*2, the same bytes as M^T MN-major); then w o X hi/lo (swizzled).
-//   region Z : Z hi/lo (same layout as M); then the h_in and R hi/lo tiles (bulk copies of
-//              the split-ready layout: K-major along n, MN-major along p).
+//              (s%8)*2, the same bytes as M^T MN-major); once M^T dY is done, the h_in and
+//              R hi/lo tiles (bulk copies of the split-ready layout: K-major along n,
+//              MN-major along p).
+//   region Z : Z hi/lo (same layout as M); then w o X hi/lo and exp(cum) dY hi/lo
+//              (swizzled, written by threads).
 // TMEM (512 columns): G [0,128), Z' = dY X^T [128,256) while M and Z are built; then dX
 // [0,64), B R^T [64,128); dC [256, 256+N) and dB [256+N, 256+2N) accumulate over the
 // CTA's heads (per-head dot products by differences of running sums).
 template <int N>
 struct BwdCfg {
     static constexpr uint32_t kCB = 128u * N * 2;           // C (or B) rows of the chunk
-    static constexpr uint32_t kDy = 128u * kP * 2;          // one dy plane
+    static constexpr uint32_t kDy = 128u * kP * 2;          // one dy (or x) plane
     static constexpr uint32_t kMat = 128u * 128 * 2;        // one 128 x 128 operand plane
     static constexpr uint32_t kHt = (uint32_t)kP * N * 2;   // one h or R plane
     static constexpr uint32_t oC = 0, oB = kCB, oDy = 2 * kCB, oA = oDy + 2 * kDy, oZ = oA + 2 * kMat;
     static constexpr uint32_t kSmem = oZ + 2 * kMat;
-    static_assert(4 * kHt <= 2 * kMat, "h and R tiles fit region Z");
+    static_assert(4 * kHt <= 2 * kMat, "h and R tiles fit region A");
+    static_assert(4 * kDy <= 2 * kMat, "w o X and exp(cum) dY fit region Z");
 };
 
 struct __align__(16) BwdShared {
-    uint64_t mb_cb, mb_xdy, mb_hr, mb_mma;
+    uint64_t mb_cb, mb_x, mb_dy, mb_hr, mb_mfree, mb_mma;
     float dl[kQ], cum[kQ];
     float part[2][kQ];  // per row: x . dX_pre, dcum
     float wsum[4];
@@ -277,8 +279,6 @@ struct BwdTcArgs {
     const float* fst;    // forward h_in tiles (hi/lo) of every (b, chunk, head)
     const float* ast;    // R tiles (hi/lo)
     const float* rdot;   // (b, H, nchunks)
-    const __nv_bfloat16* dy_hi;
-    const __nv_bfloat16* dy_lo;
     float *dx, *ddt, *dA, *dB, *dC, *ddt_bias;
     int64_t T, H, G, nchunks;
     Span dx_s, ddt_s, dA_s, dB_s, dC_s, ddtb_s;
@@ -291,9 +291,19 @@ __device__ __forceinline__ void bwd_wait(BwdShared& sh, uint64_t* mb, uint32_t p
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
+// 8 bf16 of a 16-byte word, scaled, split into hi / lo words
+__device__ __forceinline__ void scale_split8(const float (&f)[8], float w, uint4& hi, uint4& lo) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) split2(f[2 * k] * w, f[2 * k + 1] * w, h[k], l[k]);
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
 
 // grid (nchunks, H / hpc, batch), 256 threads (8 warps; warp w reads TMEM lanes
-// 32*(w%4).. and takes column half w/4 of the builds).
+// 32*(w%4).. and takes column half w/4 of the M and Z builds).  Warps 0-3 own the rows of
+// the dx epilogue, w o X and the suffix sums (their thread index is the row); warps 4-7
+// those of the dcum epilogue and exp(cum) dY.
 template <int N>
 __global__ void __launch_bounds__(256, 1)
     ssd_bwd_chunk_tc(const BwdTcArgs a, const int hpc, int* status, const __grid_constant__ CUtensorMap tm_c,
@@ -321,8 +331,10 @@ __global__ void __launch_bounds__(256, 1)
 
     if (tid == 0) {
         tc::mbar_init(&sh.mb_cb, 1);
-        tc::mbar_init(&sh.mb_xdy, 1);
+        tc::mbar_init(&sh.mb_x, 1);
+        tc::mbar_init(&sh.mb_dy, 1);
         tc::mbar_init(&sh.mb_hr, 1);
+        tc::mbar_init(&sh.mb_mfree, 1);
         tc::mbar_init(&sh.mb_mma, 1);
         sh.abort = 0;
         tc::mbar_fence_init();
@@ -335,12 +347,14 @@ __global__ void __launch_bounds__(256, 1)
     const uint32_t tG = tmem, tZ = tmem + 128, tX = tmem, tXi = tmem + 64;
     const uint32_t tC = tmem + 256, tB = tmem + 256 + N;
 
-    auto issue_xdy = [&](int hi) {
-        tc::mbar_arrive_expect_tx(&sh.mb_xdy, 3 * Cfg::kDy);
-        const int col = (hbeg + hi) * kP;
-        tc::tma_load_3d(sA, &tm_x, col, row0, b, &sh.mb_xdy);
-        tc::tma_load_3d(sDy, &tm_dyh, col, row0, b, &sh.mb_xdy);
-        tc::tma_load_3d(sDy + Cfg::kDy, &tm_dyl, col, row0, b, &sh.mb_xdy);
+    auto issue_x = [&](int hi) {
+        tc::mbar_arrive_expect_tx(&sh.mb_x, Cfg::kDy);
+        tc::tma_load_3d(sA, &tm_x, (hbeg + hi) * kP, row0, b, &sh.mb_x);
+    };
+    auto issue_dy = [&](int hi) {
+        tc::mbar_arrive_expect_tx(&sh.mb_dy, 2 * Cfg::kDy);
+        tc::tma_load_3d(sDy, &tm_dyh, (hbeg + hi) * kP, row0, b, &sh.mb_dy);
+        tc::tma_load_3d(sDy + Cfg::kDy, &tm_dyl, (hbeg + hi) * kP, row0, b, &sh.mb_dy);
     };
     if (tid == 0) {
         tc::mbar_arrive_expect_tx(&sh.mb_cb, 2 * Cfg::kCB);
@@ -348,10 +362,24 @@ __global__ void __launch_bounds__(256, 1)
             tc::tma_load_3d(sC + j * 128 * 128, &tm_c, g * N + 64 * j, row0, b, &sh.mb_cb);
             tc::tma_load_3d(sB + j * 128 * 128, &tm_b, g * N + 64 * j, row0, b, &sh.mb_cb);
         }
-        issue_xdy(0);
+        issue_x(0);
+        issue_dy(0);
     }
 
-    float prev_c = 0.0f, prev_b = 0.0f;  // running C.dC and B.dB of this thread's row (half 1)
+    // per-head values of row tid (tid < 128), fetched one head ahead: Delta, cum, dt, and
+    // for the chunk's last row <R, h_out>
+    float pdl = 0.0f, pcum = 0.0f, pdt = 0.0f, prd = 0.0f;
+    auto fetch = [&](int hi) {
+        const int h = hbeg + hi;
+        const int64_t o = (((int64_t)b * a.H + h) * a.nchunks + c) * kQ + tid;
+        pdl = a.dl[o];
+        pcum = a.cum[o];
+        pdt = tid < len ? __bfloat162float(a.dt[((int64_t)b * a.T + row0 + tid) * a.H + h]) : 0.0f;
+        prd = tid == kQ - 1 ? a.rdot[((int64_t)b * a.H + h) * a.nchunks + c] : 0.0f;
+    };
+    if (tid < kQ) fetch(0);
+
+    float prev_c = 0.0f, prev_b = 0.0f;  // running C.dC and B.dB of this thread's row (warps 4-7)
     uint32_t mma_uses = 0;
     auto mma_done = [&]() {
         bwd_wait(sh, &sh.mb_mma, mma_uses & 1);
@@ -361,10 +389,17 @@ __global__ void __launch_bounds__(256, 1)
 
     for (int hi = 0; hi < hpc; ++hi) {
         const int h = hbeg + hi;
+        float cdt = 0.0f, crd = 0.0f;
+        uint4 cx[8] = {};  // x row tid of this head (warps 0-3), for w o X and x . dX_pre
         if (tid < kQ) {
-            const int64_t o = (((int64_t)b * a.H + h) * a.nchunks + c) * kQ + tid;
-            sh.dl[tid] = a.dl[o];
-            sh.cum[tid] = a.cum[o];
+            sh.dl[tid] = pdl;
+            sh.cum[tid] = pcum;
+            cdt = pdt;
+            crd = prd;
+            const uint4* xr = reinterpret_cast<const uint4*>(a.x + ((int64_t)b * a.T + row0 + tid) * HP + (int64_t)h * kP);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) cx[k] = tid < len ? xr[k] : make_uint4(0, 0, 0, 0);
+            if (hi + 1 < hpc) fetch(hi + 1);
         }
         __syncthreads();
         if (sh.abort) break;
@@ -373,7 +408,8 @@ __global__ void __launch_bounds__(256, 1)
         // ---- phase 1: G = C B^T, Z' = dY X^T
         if (tid == 0) {
             if (hi == 0) bwd_wait(sh, &sh.mb_cb, 0);
-            bwd_wait(sh, &sh.mb_xdy, hi & 1);
+            bwd_wait(sh, &sh.mb_x, hi & 1);
+            bwd_wait(sh, &sh.mb_dy, hi & 1);
             tc::fence_after_sync();
             if (!sh.abort) {
                 constexpr uint32_t id = tc::idesc_bf16(128, 128, 0, 0);
@@ -394,7 +430,8 @@ __global__ void __launch_bounds__(256, 1)
         }
         mma_done();
 
-        // ---- phase 2: M and Z (hi/lo) from TMEM row t = r, columns s of this half
+        // ---- phase 2: M (region A) and Z (region Z), hi/lo, from TMEM row t = r, columns
+        // s of this warp's half
         {
             const int t = r;
             const float at = sh.cum[t] * kLog2e;
@@ -435,7 +472,8 @@ __global__ void __launch_bounds__(256, 1)
         tc::fence_before_sync();
         __syncthreads();
 
-        // ---- phase 3a: dX = M^T dY; dC += Z B; dB += Z^T C
+        // ---- phase 3a: dX = M^T dY (then region A is free: h_in and R tiles are copied in
+        // while the rest runs); dC += Z B; dB += Z^T C
         if (tid == 0) {
             tc::fence_after_sync();
             if (!sh.abort) {
@@ -449,6 +487,7 @@ __global__ void __launch_bounds__(256, 1)
                         tc::mma_bf16(tX, tc::desc_mnmajor(aM + combo_m[cb] * Cfg::kMat, 128, ks),
                                      tc::desc_sw128(aDy + combo_d[cb] * Cfg::kDy + ks * 2048, 1024, 1024), idX,
                                      (cb | ks) != 0);
+                tc::mma_commit(&sh.mb_mfree);
                 constexpr uint32_t idC = tc::idesc_bf16(128, N, 0, 1);
                 constexpr uint32_t idB = tc::idesc_bf16(128, N, 1, 1);
 #pragma unroll
@@ -461,57 +500,51 @@ __global__ void __launch_bounds__(256, 1)
                         tc::mma_bf16(tB, tc::desc_mnmajor(aZ + pl * Cfg::kMat, 128, ks),
                                      tc::desc_sw128(tc::smem_u32(sC) + ks * 2048, 128 * 128, 1024), idB, acc);
                     }
+            } else {
+                tc::mma_commit(&sh.mb_mfree);
             }
             tc::mma_commit(&sh.mb_mma);
+            bwd_wait(sh, &sh.mb_mfree, hi & 1);
+            if (!sh.abort) {
+                const int64_t tile = (((int64_t)b * a.nchunks + c) * a.H + h) * (int64_t)kP * N;
+                tc::mbar_arrive_expect_tx(&sh.mb_hr, 4 * Cfg::kHt);
+                tc::bulk_load(sA, a.fst + tile, 2 * Cfg::kHt, &sh.mb_hr);
+                tc::bulk_load(sA + 2 * Cfg::kHt, a.ast + tile, 2 * Cfg::kHt, &sh.mb_hr);
+            }
         }
         mma_done();
 
-        // ---- phase 3b prep: dY <- exp(cum_t) dY in place; w o X into region A; h_in, R tiles
-        {
-            const int t = tid & 127, hh = tid >> 7;
+        // ---- phase 3b prep (region Z is free): w o X from the x row in registers
+        // (warps 0-3), exp(cum_t) dY from sDy (warps 4-7), both swizzled like TMA tiles
+        if (half == 0) {
+            const int s = r;  // == tid
+            const float w = s < len ? sh.dl[s] * __expf(cum_last - sh.cum[s]) : 0.0f;
+#pragma unroll
+            for (int pc = 0; pc < 8; ++pc) {
+                float fx[8];
+                unpack8(cx[pc], fx);
+                uint4 vh, vl;
+                scale_split8(fx, w, vh, vl);
+                const uint32_t off = (uint32_t)(s * 128 + ((pc ^ (s & 7)) * 16));
+                *reinterpret_cast<uint4*>(sZ + off) = vh;
+                *reinterpret_cast<uint4*>(sZ + Cfg::kDy + off) = vl;
+            }
+        } else {
+            const int t = r;
             const float e = __expf(sh.cum[t]);
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                const int pc = hh * 4 + cc;
+            for (int pc = 0; pc < 8; ++pc) {
                 const uint32_t off = (uint32_t)(t * 128 + ((pc ^ (t & 7)) * 16));
-                uint4* ph = reinterpret_cast<uint4*>(sDy + off);
-                uint4* pl = reinterpret_cast<uint4*>(sDy + Cfg::kDy + off);
                 float fh[8], fl[8];
-                unpack8(*ph, fh);
-                unpack8(*pl, fl);
-                uint32_t oh[4], ol[4];
+                unpack8(*reinterpret_cast<const uint4*>(sDy + off), fh);
+                unpack8(*reinterpret_cast<const uint4*>(sDy + Cfg::kDy + off), fl);
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    split2((fh[2 * k] + fl[2 * k]) * e, (fh[2 * k + 1] + fl[2 * k + 1]) * e, oh[k], ol[k]);
-                *ph = make_uint4(oh[0], oh[1], oh[2], oh[3]);
-                *pl = make_uint4(ol[0], ol[1], ol[2], ol[3]);
+                for (int k = 0; k < 8; ++k) fh[k] += fl[k];
+                uint4 vh, vl;
+                scale_split8(fh, e, vh, vl);
+                *reinterpret_cast<uint4*>(sZ + 2 * Cfg::kDy + off) = vh;
+                *reinterpret_cast<uint4*>(sZ + 3 * Cfg::kDy + off) = vl;
             }
-            const int s = t;
-            const float w = s < len ? sh.dl[s] * __expf(cum_last - sh.cum[s]) : 0.0f;
-            const __nv_bfloat16* xr = a.x + ((int64_t)b * a.T + row0 + s) * HP + (int64_t)h * kP;
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                const int pc = hh * 4 + cc;
-                float fx[8];
-                if (s < len) {
-                    unpack8(*reinterpret_cast<const uint4*>(xr + pc * 8), fx);
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) fx[k] = 0.0f;
-                }
-                uint32_t oh[4], ol[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) split2(fx[2 * k] * w, fx[2 * k + 1] * w, oh[k], ol[k]);
-                const uint32_t off = (uint32_t)(s * 128 + ((pc ^ (s & 7)) * 16));
-                *reinterpret_cast<uint4*>(sA + off) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
-                *reinterpret_cast<uint4*>(sA + Cfg::kDy + off) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
-            }
-        }
-        if (tid == 0 && !sh.abort) {
-            const int64_t tile = (((int64_t)b * a.nchunks + c) * a.H + h) * (int64_t)kP * N;
-            tc::mbar_arrive_expect_tx(&sh.mb_hr, 4 * Cfg::kHt);
-            tc::bulk_load(sZ, a.fst + tile, 2 * Cfg::kHt, &sh.mb_hr);
-            tc::bulk_load(sZ + 2 * Cfg::kHt, a.ast + tile, 2 * Cfg::kHt, &sh.mb_hr);
         }
         tc::fence_async_smem();
         tc::fence_before_sync();
@@ -522,8 +555,8 @@ __global__ void __launch_bounds__(256, 1)
             bwd_wait(sh, &sh.mb_hr, hi & 1);
             tc::fence_after_sync();
             if (!sh.abort) {
-                const uint32_t aH = tc::smem_u32(sZ), aR = aH + 2 * Cfg::kHt, aDy = tc::smem_u32(sDy),
-                               aW = tc::smem_u32(sA);
+                const uint32_t aH = tc::smem_u32(sA), aR = aH + 2 * Cfg::kHt, aW = tc::smem_u32(sZ),
+                               aE = aW + 2 * Cfg::kDy;
                 constexpr uint32_t idXi = tc::idesc_bf16(128, kP, 0, 0);
 #pragma unroll
                 for (int pl = 0; pl < 2; ++pl)
@@ -540,7 +573,7 @@ __global__ void __launch_bounds__(256, 1)
                 for (int cb = 0; cb < 3; ++cb)
 #pragma unroll
                     for (int ks = 0; ks < kP / 16; ++ks) {
-                        tc::mma_bf16(tC, tc::desc_sw128(aDy + combo_a[cb] * Cfg::kDy + ks * 32, 16, 1024),
+                        tc::mma_bf16(tC, tc::desc_sw128(aE + combo_a[cb] * Cfg::kDy + ks * 32, 16, 1024),
                                      tc::desc_mnmajor(aH + combo_b[cb] * Cfg::kHt, N, ks), idCB, 1u);
                         tc::mma_bf16(tB, tc::desc_sw128(aW + combo_a[cb] * Cfg::kDy + ks * 32, 16, 1024),
                                      tc::desc_mnmajor(aR + combo_b[cb] * Cfg::kHt, N, ks), idCB, 1u);
@@ -551,7 +584,7 @@ __global__ void __launch_bounds__(256, 1)
         mma_done();
         __syncthreads();
         if (sh.abort) break;
-        if (tid == 0 && hi + 1 < hpc) issue_xdy(hi + 1);  // region A and sDy are free again
+        if (tid == 0 && hi + 1 < hpc) issue_x(hi + 1);  // region A is free again
 
         // ---- phase 4: epilogues
         if (half == 0) {
@@ -560,29 +593,33 @@ __global__ void __launch_bounds__(256, 1)
             float ddir = 0.0f;
             const float dec = __expf(cum_last - sh.cum[s]);
             const float Dh = a.D ? a.D[h] : 0.0f;
-            const int64_t row = ((int64_t)b * a.T + row0 + s) * HP + (int64_t)h * kP;
-#pragma unroll 1
+            const float dls = sh.dl[s];
+            float* dxr = a.dx + ((int64_t)b * a.T + row0 + s) * HP + (int64_t)h * kP;
+#pragma unroll
             for (int p0 = 0; p0 < kP; p0 += 16) {
                 uint32_t xv[16], xi[16];
                 tc::tmem_ld16_async(tX + lane_base + (uint32_t)p0, xv);
                 tc::tmem_ld16_async(tXi + lane_base + (uint32_t)p0, xi);
                 tc::tmem_wait_ld();
                 if (s < len) {
-                    float fx[16], fdh[16], fdl[16];
-                    unpack8(*reinterpret_cast<const uint4*>(a.x + row + p0), *reinterpret_cast<float(*)[8]>(fx));
-                    unpack8(*reinterpret_cast<const uint4*>(a.x + row + p0 + 8), *reinterpret_cast<float(*)[8]>(fx + 8));
-                    unpack8(*reinterpret_cast<const uint4*>(a.dy_hi + row + p0), *reinterpret_cast<float(*)[8]>(fdh));
-                    unpack8(*reinterpret_cast<const uint4*>(a.dy_hi + row + p0 + 8), *reinterpret_cast<float(*)[8]>(fdh + 8));
-                    unpack8(*reinterpret_cast<const uint4*>(a.dy_lo + row + p0), *reinterpret_cast<float(*)[8]>(fdl));
-                    unpack8(*reinterpret_cast<const uint4*>(a.dy_lo + row + p0 + 8), *reinterpret_cast<float(*)[8]>(fdl + 8));
                     float out[16];
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        const float pre = fmaf(dec, __uint_as_float(xi[k]), __uint_as_float(xv[k]));
-                        ddir = fmaf(fx[k], pre, ddir);
-                        out[k] = fmaf(sh.dl[s], pre, Dh * (fdh[k] + fdl[k]));
+                    for (int c8 = 0; c8 < 2; ++c8) {
+                        const int pc = (p0 >> 3) + c8;
+                        const uint32_t off = (uint32_t)(s * 128 + ((pc ^ (s & 7)) * 16));
+                        float fx[8], fh[8], fl[8];
+                        unpack8(cx[pc], fx);
+                        unpack8(*reinterpret_cast<const uint4*>(sDy + off), fh);
+                        unpack8(*reinterpret_cast<const uint4*>(sDy + Cfg::kDy + off), fl);
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const int j = c8 * 8 + k;
+                            const float pre = fmaf(dec, __uint_as_float(xi[j]), __uint_as_float(xv[j]));
+                            ddir = fmaf(fx[k], pre, ddir);
+                            out[j] = fmaf(dls, pre, Dh * (fh[k] + fl[k]));
+                        }
                     }
-                    float4* dst = reinterpret_cast<float4*>(a.dx + row + p0);
+                    float4* dst = reinterpret_cast<float4*>(dxr + p0);
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
                         store_checked(a.dx_s, dst + k, make_float4(out[4 * k], out[4 * k + 1], out[4 * k + 2], out[4 * k + 3]), status);
@@ -614,18 +651,18 @@ __global__ void __launch_bounds__(256, 1)
                     }
                 }
             }
-            float dcum = (sc - prev_c) - (sb - prev_b);
+            sh.part[1][t] = (sc - prev_c) - (sb - prev_b);
             prev_c = sc;
             prev_b = sb;
-            if (t == kQ - 1) dcum += a.rdot[((int64_t)b * a.H + h) * a.nchunks + c];
-            sh.part[1][t] = dcum;
         }
         tc::fence_before_sync();
         __syncthreads();
+        if (tid == 0 && hi + 1 < hpc) issue_dy(hi + 1);  // the epilogue has read sDy
         if (half == 0) {
-            // da_t = sum of dcum over t' >= t (suffix sum over the chunk's 128 rows)
+            // da_t = sum of dcum over t' >= t (suffix sum over the chunk's 128 rows; the
+            // last row carries <R, h_out>)
             const int t = r;
-            float v = sh.part[1][t];
+            float v = sh.part[1][t] + crd;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const float u = __shfl_down_sync(0xffffffffu, v, o);
@@ -638,9 +675,8 @@ __global__ void __launch_bounds__(256, 1)
             const float dDelta = fmaf(a.A[h], da, sh.part[0][t]);
             float ddt = 0.0f;
             if (t < len) {
-                const float dtv = __bfloat162float(a.dt[((int64_t)b * a.T + row0 + t) * a.H + h]);
                 const float bias = a.dt_bias ? a.dt_bias[h] : 0.0f;
-                ddt = dDelta * sigmoid_fast(dtv + bias);
+                ddt = dDelta * sigmoid_fast(cdt + bias);
                 store_checked(a.ddt_s, &a.ddt[((int64_t)b * a.T + row0 + t) * a.H + h], ddt, status);
             }
             float pa = sh.dl[t] * da, pb = ddt;
@@ -681,9 +717,13 @@ __global__ void __launch_bounds__(256, 1)
             tc::tmem_wait_ld();
             if (t < len) {
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    atomic_add_checked(a.dC_s, a.dC + o + n0 + k, __uint_as_float(cv[k]), status);
-                    atomic_add_checked(a.dB_s, a.dB + o + n0 + k, __uint_as_float(bv[k]), status);
+                for (int k = 0; k < 16; k += 4) {
+                    atomic_add4_checked(a.dC_s, a.dC + o + n0 + k,
+                                        make_float4(__uint_as_float(cv[k]), __uint_as_float(cv[k + 1]),
+                                                    __uint_as_float(cv[k + 2]), __uint_as_float(cv[k + 3])), status);
+                    atomic_add4_checked(a.dB_s, a.dB + o + n0 + k,
+                                        make_float4(__uint_as_float(bv[k]), __uint_as_float(bv[k + 1]),
+                                                    __uint_as_float(bv[k + 2]), __uint_as_float(bv[k + 3])), status);
                 }
             }
         }
@@ -933,8 +973,6 @@ cudaError_t ssd_bwd_tc_launch(const ScanBwdArgs& s, void* ws, cudaStream_t strea
     k.fst = fst;
     k.ast = ast;
     k.rdot = rdot;
-    k.dy_hi = dyh;
-    k.dy_lo = dyl;
     k.dx = s.dx;
     k.ddt = s.ddt;
     k.dA = s.dA;

@@ -49,6 +49,11 @@ __device__ __forceinline__ void atomic_add_checked(const Span& s, float* p, floa
     if (span_ok(s, p, 4, status)) atomicAdd(p, v);
 }
 
+// Four consecutive fp32 atomic adds as one vector atomic (16-byte aligned p).
+__device__ __forceinline__ void atomic_add4_checked(const Span& s, float* p, float4 v, int* status) {
+    if (span_ok(s, p, 16, status)) atomicAdd(reinterpret_cast<float4*>(p), v);
+}
+
 // *p = v when p lies in the span (always, without SSM_BOUNDS_CHECK).
 template <typename V>
 __device__ __forceinline__ void store_checked(const Span& s, V* p, V v, int* status) {
