@@ -13,6 +13,7 @@
 //   dB     = Z^T C + diag(w) X R,   w_s = Delta_s exp(cum_last - cum_s)
 //   dcum_t = C_t . dC_t - B_t . dB_t  (+ <R, h_out> at the chunk's last step)
 //   da_t   = sum_{t' >= t in the chunk} dcum_t'       dDelta_t = A_h da_t + x_t . dX_pre_t
+//   <R, h_out> = exp(cum_last) <R, h_in> + sum_s w_s x_s . (B R^T)_s
 //   ddt_t  = dDelta_t sigmoid(dt_t + dt_bias_h),  ddt_bias_h = sum ddt,  dA_h = sum Delta_t da_t
 // dcum needs no Q x Q reduction: the row sums of (G o Z) are C_t . (Z B)_t and its column
 // sums B_s . (Z^T C)_s.  R itself follows the adjoint recurrence over chunks,
@@ -25,7 +26,7 @@
 //     hi/lo tiles, final state), and with a gate ssd_scan_tc without it (y before the gate);
 //   ssd_bwd_dy        : dy as bf16 hi/lo planes, dz, dD;
 //   ssd_state_tc (adjoint), ssd_bwd_reverse_carry: R_c of every chunk as hi/lo tiles,
-//     <R_c, h_out_c>, dinitial_state;
+//     dinitial_state;
 //   ssd_bwd_chunk_tc  : one CTA per (chunk, batch, heads of one group): every product above
 //     on tcgen05 (bf16 operands, scaled ones split into hi + lo, fp32 accumulators in
 //     TMEM), then the per-row epilogues; dB and dC summed over the CTA's heads in TMEM and
@@ -140,90 +141,63 @@ __global__ void __launch_bounds__(256) ssd_bwd_dy(const DyArgs a) {
 // ---- reverse carry ---------------------------------------------------------------------
 // R over chunks in reverse, in place over the adjoint chunk states (split-ready layout of
 // the chunk-state kernel): reads S^g_c, writes R_c = dL/dh_out(c) as bf16 hi/lo tiles,
-// R_{c-1} = exp(cum_last(c)) R_c + S^g_c; also <R_c, h_out(c)> into rdot (zeroed before;
-// h_out(c) = h_in(c+1) from the forward tiles, the final state for the last chunk) and
-// dinitial_state = R_{-1}.  grid (ceil(P*N / 8 / 256), H, b); a thread owns the 8 values
+// R_{c-1} = exp(cum_last(c)) R_c + S^g_c, and dinitial_state = R_{-1}.  grid (ceil(P*N / 8 / 256), H, b); a thread owns the 8 values
 // (p, n..n+7) of one 16-byte unit, as the forward carry does.
 constexpr int kRevAhead = 4;
 
 struct RevArgs {
     float* ast;
-    const float* fst;
-    const float* fs;
     const float* cum;
     const float* dfinal;
     float* dinit;
-    float* rdot;
     int64_t T, H, P, N, Q, nchunks;
     int* status;
-    Span ast_s, dinit_s, rdot_s;
+    Span ast_s, dinit_s;
 };
 
 __global__ void __launch_bounds__(256) ssd_bwd_reverse_carry(const RevArgs a) {
     const int64_t u = (int64_t)blockIdx.x * 256 + threadIdx.x;
     const int64_t h = blockIdx.y, b = blockIdx.z;
     const int64_t PN = a.P * a.N;
-    const bool ok = u * 8 < PN;  // P*N/8 is a multiple of 32: whole warps agree
-    const int64_t uu = ok ? u : 0;
-    const int64_t blk = uu >> 3, kb = a.N / 8;
-    const int p = (int)((blk / kb) * 8 + (uu & 7)), n0 = (int)(blk % kb) * 8;
-    const uint32_t o = (uint32_t)(16 * uu);
+    if (u * 8 >= PN) return;
+    const int64_t blk = u >> 3, kb = a.N / 8;
+    const int p = (int)((blk / kb) * 8 + (u & 7)), n0 = (int)(blk % kb) * 8;
+    const uint32_t o = (uint32_t)(16 * u);
     const int64_t half = PN * 2;
     float R[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) R[k] = (ok && a.dfinal) ? a.dfinal[(b * a.H + h) * PN + p * a.N + n0 + k] : 0.0f;
+    for (int k = 0; k < 8; ++k) R[k] = a.dfinal ? a.dfinal[(b * a.H + h) * PN + p * a.N + n0 + k] : 0.0f;
     const int64_t cstride = a.H * PN * 4;
     char* base = reinterpret_cast<char*>(a.ast + (b * a.nchunks * a.H + h) * PN);
-    const char* fbase = reinterpret_cast<const char*>(a.fst + (b * a.nchunks * a.H + h) * PN);
     const float* cum = a.cum + (b * a.H + h) * a.nchunks * a.Q;
-    float* rdot = a.rdot + (b * a.H + h) * a.nchunks;
     for (int64_t c0 = a.nchunks - 1; c0 >= 0; c0 -= kRevAhead) {
         float4 S0[kRevAhead], S1[kRevAhead];
-        float ho[kRevAhead][8];
         float dec[kRevAhead];
 #pragma unroll
         for (int j = 0; j < kRevAhead; ++j) {
             const int64_t c = c0 - j;
-            if (c >= 0 && ok) {
+            if (c >= 0) {
                 S0[j] = *reinterpret_cast<const float4*>(base + c * cstride + o);
                 S1[j] = *reinterpret_cast<const float4*>(base + c * cstride + half + o);
                 const int len = (int)min(a.Q, a.T - c * a.Q);
                 dec[j] = expf(cum[c * a.Q + len - 1]);
-                if (c == a.nchunks - 1) {
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) ho[j][k] = a.fs[(b * a.H + h) * PN + p * a.N + n0 + k];
-                } else {
-                    float hh[8], hl[8];
-                    unpack8(*reinterpret_cast<const uint4*>(fbase + (c + 1) * cstride + o), hh);
-                    unpack8(*reinterpret_cast<const uint4*>(fbase + (c + 1) * cstride + half + o), hl);
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) ho[j][k] = hh[k] + hl[k];
-                }
             }
         }
 #pragma unroll
         for (int j = 0; j < kRevAhead; ++j) {
             const int64_t c = c0 - j;
-            if (c < 0) break;  // uniform over the grid
-            float dot = 0.0f;
-            if (ok) {
+            if (c < 0) break;
+            uint32_t hi[4], lo[4];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) dot = fmaf(R[k], ho[j][k], dot);
-                uint32_t hi[4], lo[4];
+            for (int k = 0; k < 4; ++k) split2(R[2 * k], R[2 * k + 1], hi[k], lo[k]);
+            store_checked(a.ast_s, reinterpret_cast<uint4*>(base + c * cstride + o), make_uint4(hi[0], hi[1], hi[2], hi[3]), a.status);
+            store_checked(a.ast_s, reinterpret_cast<uint4*>(base + c * cstride + half + o), make_uint4(lo[0], lo[1], lo[2], lo[3]), a.status);
+            const float s[8] = {S0[j].x, S0[j].y, S0[j].z, S0[j].w, S1[j].x, S1[j].y, S1[j].z, S1[j].w};
 #pragma unroll
-                for (int k = 0; k < 4; ++k) split2(R[2 * k], R[2 * k + 1], hi[k], lo[k]);
-                store_checked(a.ast_s, reinterpret_cast<uint4*>(base + c * cstride + o), make_uint4(hi[0], hi[1], hi[2], hi[3]), a.status);
-                store_checked(a.ast_s, reinterpret_cast<uint4*>(base + c * cstride + half + o), make_uint4(lo[0], lo[1], lo[2], lo[3]), a.status);
-                const float s[8] = {S0[j].x, S0[j].y, S0[j].z, S0[j].w, S1[j].x, S1[j].y, S1[j].z, S1[j].w};
-#pragma unroll
-                for (int k = 0; k < 8; ++k) R[k] = fmaf(dec[j], R[k], s[k]);
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-            if (ok && (threadIdx.x & 31) == 0) atomic_add_checked(a.rdot_s, rdot + c, dot, a.status);
+            for (int k = 0; k < 8; ++k) R[k] = fmaf(dec[j], R[k], s[k]);
         }
     }
-    if (ok && a.dinit) {
+    if (a.dinit) {
 #pragma unroll
         for (int k = 0; k < 8; ++k) store_checked(a.dinit_s, &a.dinit[(b * a.H + h) * PN + p * a.N + n0 + k], R[k], a.status);
     }
@@ -263,6 +237,7 @@ struct __align__(16) BwdShared {
     float dl[kQ], cum[kQ];
     float part[2][kQ];  // per row: x . dX_pre, dcum
     float wsum[4];
+    float rsum[8];      // warp partials of <R, h_out>
     float red[4][2];
     uint32_t tmem;
     volatile int abort;
@@ -278,7 +253,6 @@ struct BwdTcArgs {
     const float* cum;
     const float* fst;    // forward h_in tiles (hi/lo) of every (b, chunk, head)
     const float* ast;    // R tiles (hi/lo)
-    const float* rdot;   // (b, H, nchunks)
     float *dx, *ddt, *dA, *dB, *dC, *ddt_bias;
     int64_t T, H, G, nchunks;
     Span dx_s, ddt_s, dA_s, dB_s, dC_s, ddtb_s;
@@ -366,16 +340,14 @@ __global__ void __launch_bounds__(256, 1)
         issue_dy(0);
     }
 
-    // per-head values of row tid (tid < 128), fetched one head ahead: Delta, cum, dt, and
-    // for the chunk's last row <R, h_out>
-    float pdl = 0.0f, pcum = 0.0f, pdt = 0.0f, prd = 0.0f;
+    // per-head values of row tid (tid < 128), fetched one head ahead: Delta, cum, dt
+    float pdl = 0.0f, pcum = 0.0f, pdt = 0.0f;
     auto fetch = [&](int hi) {
         const int h = hbeg + hi;
         const int64_t o = (((int64_t)b * a.H + h) * a.nchunks + c) * kQ + tid;
         pdl = a.dl[o];
         pcum = a.cum[o];
         pdt = tid < len ? __bfloat162float(a.dt[((int64_t)b * a.T + row0 + tid) * a.H + h]) : 0.0f;
-        prd = tid == kQ - 1 ? a.rdot[((int64_t)b * a.H + h) * a.nchunks + c] : 0.0f;
     };
     if (tid < kQ) fetch(0);
 
@@ -389,13 +361,12 @@ __global__ void __launch_bounds__(256, 1)
 
     for (int hi = 0; hi < hpc; ++hi) {
         const int h = hbeg + hi;
-        float cdt = 0.0f, crd = 0.0f;
+        float cdt = 0.0f;
         uint4 cx[8] = {};  // x row tid of this head (warps 0-3), for w o X and x . dX_pre
         if (tid < kQ) {
             sh.dl[tid] = pdl;
             sh.cum[tid] = pcum;
             cdt = pdt;
-            crd = prd;
             const uint4* xr = reinterpret_cast<const uint4*>(a.x + ((int64_t)b * a.T + row0 + tid) * HP + (int64_t)h * kP);
 #pragma unroll
             for (int k = 0; k < 8; ++k) cx[k] = tid < len ? xr[k] : make_uint4(0, 0, 0, 0);
@@ -581,10 +552,27 @@ __global__ void __launch_bounds__(256, 1)
             }
             tc::mma_commit(&sh.mb_mma);
         }
+        // meanwhile <R, h_in> over the two tiles in region A (hi + lo of each)
+        float phr = 0.0f;
+        if (tid != 0) bwd_wait(sh, &sh.mb_hr, hi & 1);
+        if (!sh.abort) {
+            constexpr int kWords = (int)(Cfg::kHt / 16);  // 16-byte words per plane
+#pragma unroll
+            for (int i = tid; i < kWords; i += 256) {
+                float hh[8], hl[8], rh[8], rl[8];
+                unpack8(*reinterpret_cast<const uint4*>(sA + i * 16), hh);
+                unpack8(*reinterpret_cast<const uint4*>(sA + Cfg::kHt + i * 16), hl);
+                unpack8(*reinterpret_cast<const uint4*>(sA + 2 * Cfg::kHt + i * 16), rh);
+                unpack8(*reinterpret_cast<const uint4*>(sA + 3 * Cfg::kHt + i * 16), rl);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) phr = fmaf(hh[k] + hl[k], rh[k] + rl[k], phr);
+            }
+        }
         mma_done();
         __syncthreads();
         if (sh.abort) break;
         if (tid == 0 && hi + 1 < hpc) issue_x(hi + 1);  // region A is free again
+        float prd = __expf(cum_last) * phr;  // this thread's part of <R, h_out>
 
         // ---- phase 4: epilogues
         if (half == 0) {
@@ -594,6 +582,7 @@ __global__ void __launch_bounds__(256, 1)
             const float dec = __expf(cum_last - sh.cum[s]);
             const float Dh = a.D ? a.D[h] : 0.0f;
             const float dls = sh.dl[s];
+            float xri = 0.0f;  // x_s . (B R^T)_s
             float* dxr = a.dx + ((int64_t)b * a.T + row0 + s) * HP + (int64_t)h * kP;
 #pragma unroll
             for (int p0 = 0; p0 < kP; p0 += 16) {
@@ -616,6 +605,7 @@ __global__ void __launch_bounds__(256, 1)
                             const int j = c8 * 8 + k;
                             const float pre = fmaf(dec, __uint_as_float(xi[j]), __uint_as_float(xv[j]));
                             ddir = fmaf(fx[k], pre, ddir);
+                            xri = fmaf(fx[k], __uint_as_float(xi[j]), xri);
                             out[j] = fmaf(dls, pre, Dh * (fh[k] + fl[k]));
                         }
                     }
@@ -626,6 +616,7 @@ __global__ void __launch_bounds__(256, 1)
                 }
             }
             sh.part[0][s] = ddir;
+            prd = fmaf(dls * dec, xri, prd);  // w_s x_s . (B R^T)_s: <R, S_c> of row s
         } else {
             // dcum of row t = r: C_t . dC_t - B_t . dB_t for this head (running sums over
             // the CTA's heads, differenced)
@@ -655,14 +646,17 @@ __global__ void __launch_bounds__(256, 1)
             prev_c = sc;
             prev_b = sb;
         }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) prd += __shfl_xor_sync(0xffffffffu, prd, o);
+        if (lane == 0) sh.rsum[warp] = prd;
         tc::fence_before_sync();
         __syncthreads();
         if (tid == 0 && hi + 1 < hpc) issue_dy(hi + 1);  // the epilogue has read sDy
         if (half == 0) {
             // da_t = sum of dcum over t' >= t (suffix sum over the chunk's 128 rows; the
-            // last row carries <R, h_out>)
+            // last row also carries <R, h_out>, which reaches every row)
             const int t = r;
-            float v = sh.part[1][t] + crd;
+            float v = sh.part[1][t];
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const float u = __shfl_down_sync(0xffffffffu, v, o);
@@ -671,7 +665,10 @@ __global__ void __launch_bounds__(256, 1)
             if (lane == 0) sh.wsum[q] = v;
             asm volatile("bar.sync 1, 128;" ::: "memory");
             for (int w = q + 1; w < 4; ++w) v += sh.wsum[w];
-            const float da = v;
+            float rdot = 0.0f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) rdot += sh.rsum[w];
+            const float da = v + rdot;
             const float dDelta = fmaf(a.A[h], da, sh.part[0][t]);
             float ddt = 0.0f;
             if (t < len) {
@@ -766,7 +763,7 @@ bool bwd_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t T, uint6
 
 struct BwdTcPlan {
     int64_t nchunks;
-    size_t o_dl, o_cum, o_fst, o_ast, o_rdot, o_fs, o_y, o_dyh, o_dyl, total;
+    size_t o_dl, o_cum, o_fst, o_ast, o_y, o_dyh, o_dyl, total;
 };
 
 BwdTcPlan bwd_tc_plan(const ScanArgs& a) {
@@ -774,8 +771,6 @@ BwdTcPlan bwd_tc_plan(const ScanArgs& a) {
     p.nchunks = (a.seqlen + kQ - 1) / kQ;
     const size_t vec = (size_t)a.batch * a.nheads * p.nchunks * kQ * sizeof(float);
     const size_t st = (size_t)a.batch * p.nchunks * a.nheads * a.headdim * a.dstate * sizeof(float);
-    const size_t rd = (size_t)a.batch * a.nheads * p.nchunks * sizeof(float);
-    const size_t fs = (size_t)a.batch * a.nheads * a.headdim * a.dstate * sizeof(float);
     const size_t el = (size_t)a.batch * a.seqlen * a.nheads * a.headdim * 2;
     size_t o = 0;
     auto take = [&](size_t bytes) {
@@ -787,8 +782,6 @@ BwdTcPlan bwd_tc_plan(const ScanArgs& a) {
     p.o_cum = take(vec);
     p.o_fst = take(st);
     p.o_ast = take(st);
-    p.o_rdot = take(rd);
-    p.o_fs = take(fs);
     p.o_y = take(el);  // with a gate (the size query does not know whether there is one)
     p.o_dyh = take(el);
     p.o_dyl = take(el);
@@ -847,8 +840,6 @@ cudaError_t ssd_bwd_tc_launch(const ScanBwdArgs& s, void* ws, cudaStream_t strea
     float* cum = reinterpret_cast<float*>(w + pl.o_cum);
     float* fst = reinterpret_cast<float*>(w + pl.o_fst);
     float* ast = reinterpret_cast<float*>(w + pl.o_ast);
-    float* rdot = reinterpret_cast<float*>(w + pl.o_rdot);
-    float* fs = reinterpret_cast<float*>(w + pl.o_fs);
     __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(w + pl.o_y);
     __nv_bfloat16* dyh = reinterpret_cast<__nv_bfloat16*>(w + pl.o_dyh);
     __nv_bfloat16* dyl = reinterpret_cast<__nv_bfloat16*>(w + pl.o_dyl);
@@ -862,8 +853,8 @@ cudaError_t ssd_bwd_tc_launch(const ScanBwdArgs& s, void* ws, cudaStream_t strea
         if (e != cudaSuccess) return e;
     }
 
-    // forward recompute: Delta, cumulative sums, h_in of every chunk, final state, and with
-    // a gate the output before it
+    // forward recompute: Delta, cumulative sums, h_in of every chunk, and with a gate the
+    // output before it
     SsdTcArgs t = {};
     t.x = static_cast<const __nv_bfloat16*>(f.x);
     t.x_lo = nullptr;
@@ -890,7 +881,7 @@ cudaError_t ssd_bwd_tc_launch(const ScanBwdArgs& s, void* ws, cudaStream_t strea
     t.states_s = span_of(fst, stb);
     cudaError_t e = ssd_tc_chunk_state(t, b, stream);
     if (e != cudaSuccess) return e;
-    e = ssd_tc_forward_carry(f, kQ, pl.nchunks, cum, fst, fs, stream);
+    e = ssd_tc_forward_carry(f, kQ, pl.nchunks, cum, fst, nullptr, stream);
     if (e != cudaSuccess) return e;
     if (f.z) {
         e = ssd_tc_chunk_scan(t, b, false, stream);
@@ -932,17 +923,12 @@ cudaError_t ssd_bwd_tc_launch(const ScanBwdArgs& s, void* ws, cudaStream_t strea
     ta.states_s = span_of(ast, stb);
     e = ssd_tc_chunk_state_adjoint(ta, b, stream);
     if (e != cudaSuccess) return e;
-    e = cudaMemsetAsync(rdot, 0, (size_t)b * H * pl.nchunks * sizeof(float), stream);
-    if (e != cudaSuccess) return e;
     {
         RevArgs rv;
         rv.ast = ast;
-        rv.fst = fst;
-        rv.fs = fs;
         rv.cum = cum;
         rv.dfinal = s.dfinal;
         rv.dinit = s.dinit;
-        rv.rdot = rdot;
         rv.T = T;
         rv.H = H;
         rv.P = P;
@@ -952,7 +938,6 @@ cudaError_t ssd_bwd_tc_launch(const ScanBwdArgs& s, void* ws, cudaStream_t strea
         rv.status = status;
         rv.ast_s = span_of(ast, stb);
         rv.dinit_s = span_of(s.dinit, (size_t)b * H * P * N * sizeof(float));
-        rv.rdot_s = span_of(rdot, (size_t)b * H * pl.nchunks * sizeof(float));
         const dim3 grid((unsigned)((P * N / 8 + 255) / 256), (unsigned)H, (unsigned)b);
         cudaEvent_t t0 = timing_begin(stream);
         ssd_bwd_reverse_carry<<<grid, 256, 0, stream>>>(rv);
@@ -972,7 +957,6 @@ cudaError_t ssd_bwd_tc_launch(const ScanBwdArgs& s, void* ws, cudaStream_t strea
     k.cum = cum;
     k.fst = fst;
     k.ast = ast;
-    k.rdot = rdot;
     k.dx = s.dx;
     k.ddt = s.ddt;
     k.dA = s.dA;

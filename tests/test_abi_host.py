@@ -288,13 +288,13 @@ def test_backward_argument_errors():
     assert lib.ssm_scan_bwd_workspace_size(ctypes.byref(ssd256)) == 16 * (64 // 4) * 64 * 64 * 256 * 4
     # SSD mode on the chunked tensor-core backward (bf16, headdim 64, dstate 64 or 128):
     # chunks of 128 steps; Delta and the cumulative sums, the forward and the adjoint chunk
-    # states, <R, h_out> per chunk, the final state, y before the gate and the two dy planes
+    # states, y before the gate and the two dy planes
     a256 = lambda n: -(-n // 256) * 256
     for b_, T_, H_, N_ in ((16, 64, 64, 128), (3, 300, 4, 64)):
         tcs = _shape(mode=1, batch=b_, seqlen=T_, nheads=H_, headdim=64, dstate=N_)
         nc = -(-T_ // 128)
-        want = (2 * a256(b_ * H_ * nc * 128 * 4) + 2 * a256(b_ * nc * H_ * 64 * N_ * 4) + a256(b_ * H_ * nc * 4)
-                + a256(b_ * H_ * 64 * N_ * 4) + 3 * a256(b_ * T_ * H_ * 64 * 2))
+        want = (2 * a256(b_ * H_ * nc * 128 * 4) + 2 * a256(b_ * nc * H_ * 64 * N_ * 4)
+                + 3 * a256(b_ * T_ * H_ * 64 * 2))
         assert lib.ssm_scan_bwd_workspace_size(ctypes.byref(tcs)) == want
     # few channels: the checkpoints plus the summaries of several time parts
     small = _shape(mode=1, dtype=0, nheads=8, headdim=64, dstate=128, chunk=64)
