@@ -269,6 +269,9 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
 #pragma unroll
                         for (int ks = 0; ks < KPC / 16; ++ks) tc::mma_bf16(tYd, dmh + ks * 16u, dxl + ks * 128u, id_diag, 1u);
                     }
+                    // the part buffer may be rebuilt once these MMAs are done, before the
+                    // head's Y_off MMAs below
+                    tc::mma_commit(&sh.empty_part[pb]);
                     if (kp == 0) {
                         const uint32_t cb = tc::smem_u32(sC);
                         const uint32_t hs = tc::smem_u32(sH + hbuf(hi) * 2 * Cfg::kH);
@@ -282,7 +285,6 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
                         }
                         tc::mma_commit(&sh.h_empty[hbuf(hi)]);  // the h tiles may be replaced
                     }
-                    tc::mma_commit(&sh.empty_part[pb]);         // the part buffer may be rebuilt
                 }
                 tc::mma_commit(&sh.acc_full[ab]);   // the epilogue may read this head's accumulators
                 tc::mma_commit(&sh.x_empty[xbuf(hi)]);
