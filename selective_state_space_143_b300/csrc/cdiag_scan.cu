@@ -57,7 +57,8 @@ struct CCfg {
     static constexpr int kStageBytes = 3 * kXBytes + 2 * kBCBytes;
     static constexpr int kDuBytes = kCTT * CPB * 8;      // (Delta, Delta x) per (t, c)
     static constexpr int kYsBytes = kCTT * CPB * LPC * 4;
-    static constexpr int kSmem = kCStages * kStageBytes + kDuBytes + kYsBytes;
+    static constexpr int kBfBytes = kCTT * NK * 8;        // B (or C) of a tile as fp32 (re, im)
+    static constexpr int kSmem = kCStages * kStageBytes + kDuBytes + kYsBytes + 2 * kBfBytes;
     static_assert(kRowBytes % 16 == 0 && kBCRowBytes % 16 == 0, "16-byte rows");
 };
 
@@ -98,23 +99,24 @@ __device__ __forceinline__ float2 cld2<__nv_bfloat16>(const unsigned char* p) {
     return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
 }
 
-// exp(d * A) for A = (re, im): (e^{d re} cos(d im), e^{d re} sin(d im)).  16-bit inputs:
-// ex2 on the SFU and sin/cos of the angle reduced to [-pi, pi] (where the SFU's
-// approximations are accurate); fp32 inputs: CUDA's expf and sincosf.
+// exp(d * A) for A = (re, im): (e^{d re} cos(d im), e^{d re} sin(d im)).  16-bit inputs
+// (a.x holding re * log2 e): ex2 on the SFU and sin/cos of the angle reduced to
+// [-pi, pi] (where the SFU's approximations are accurate), the two products as one
+// packed multiply; fp32 inputs: CUDA's expf and sincosf.
 template <bool PRECISE>
 __device__ __forceinline__ float2 cexp_da(float d, float2 a) {
-    float s, c, r;
+    float s, c;
     if (PRECISE) {
-        r = expf(d * a.x);
+        const float r = expf(d * a.x);
         sincosf(d * a.y, &s, &c);
-    } else {
-        r = ex2(d * a.x * kLog2e);
-        float th = d * a.y;
-        th = fmaf(-kTwoPi, rintf(th * kInvTwoPi), th);
-        asm("sin.approx.ftz.f32 %0, %1;" : "=f"(s) : "f"(th));
-        asm("cos.approx.ftz.f32 %0, %1;" : "=f"(c) : "f"(th));
+        return make_float2(r * c, r * s);
     }
-    return make_float2(r * c, r * s);
+    const float r = ex2(d * a.x);
+    float th = d * a.y;
+    th = fmaf(-kTwoPi, rintf(th * kInvTwoPi), th);
+    asm("sin.approx.ftz.f32 %0, %1;" : "=f"(s) : "f"(th));
+    asm("cos.approx.ftz.f32 %0, %1;" : "=f"(c) : "f"(th));
+    return __fmul2_rn(make_float2(r, r), make_float2(c, s));
 }
 
 // STATE_ONLY: each segment's local end state (from zero) and its sum of Delta, for the
@@ -128,6 +130,8 @@ __global__ void __launch_bounds__(kCThreads) cdiag_scan_kernel(const CDiagArgs a
     extern __shared__ __align__(128) unsigned char smem[];
     float2* du = reinterpret_cast<float2*>(smem + kCStages * Cfg::kStageBytes);  // [kCTT][CPB]
     float* ys = reinterpret_cast<float*>(smem + kCStages * Cfg::kStageBytes + Cfg::kDuBytes);  // [kCTT][CPB][LPC]
+    float2* Bf = reinterpret_cast<float2*>(smem + kCStages * Cfg::kStageBytes + Cfg::kDuBytes + Cfg::kYsBytes);  // [kCTT][NK]
+    float2* Cf = Bf + kCTT * NK;                                                                                // [kCTT][NK]
 
     const int tid = threadIdx.x;
     const int group = blockIdx.x / a.tiles_per_group;
@@ -150,7 +154,9 @@ __global__ void __launch_bounds__(kCThreads) cdiag_scan_kernel(const CDiagArgs a
     for (int j = 0; j < kEPL; ++j) {
         const int n = g * kEPL + j;
         const bool ok = c_ok && n < a.N;
-        Ac[j] = ok ? make_float2(a.A[(c * a.N + n) * 2], a.A[(c * a.N + n) * 2 + 1]) : make_float2(0.0f, 0.0f);
+        // the decay rate pre-scaled by log2 e for the ex2 of 16-bit inputs
+        Ac[j] = ok ? make_float2(a.A[(c * a.N + n) * 2] * (PRECISE ? 1.0f : kLog2e), a.A[(c * a.N + n) * 2 + 1])
+                   : make_float2(0.0f, 0.0f);
         h[j] = make_float2(0.0f, 0.0f);
     }
     if (!STATE_ONLY && c_ok) {
@@ -215,7 +221,8 @@ __global__ void __launch_bounds__(kCThreads) cdiag_scan_kernel(const CDiagArgs a
         issue(k + 2);
         const unsigned char* st = stage(k);
         const int rows = min(kCTT, rows_total - k * kCTT);
-        // (1) Delta and Delta x per (t, c); rows past the tile's end get Delta 0
+        // (1) Delta and Delta x per (t, c); rows past the tile's end get Delta 0.  B and C
+        // of the tile to fp32 (re, im) pairs, once for all the block's channels.
         for (int i = tid; i < kCTT * CPB; i += kCThreads) {
             const int r = i / CPB, ch = i % CPB;
             float dl = 0.0f, u = 0.0f;
@@ -228,25 +235,41 @@ __global__ void __launch_bounds__(kCThreads) cdiag_scan_kernel(const CDiagArgs a
             du[r * CPB + ch] = make_float2(dl, u);
             if (STATE_ONLY) dsum += dl;
         }
+        for (int i = tid; i < kCTT * NK; i += kCThreads) {
+            const unsigned char* src = st + 3 * Cfg::kXBytes + i * 2 * E;  // row i / NK, entry i % NK
+            Bf[i] = cld2<T>(src);
+            if (!STATE_ONLY) Cf[i] = cld2<T>(src + Cfg::kBCBytes);
+        }
         __syncthreads();
         // (2) the recurrence over the tile's rows
-        const unsigned char* Bt = st + 3 * Cfg::kXBytes + g * kEPL * 2 * E;
         for (int r = 0; r < kCTT; ++r) {
             const float2 dv = du[r * CPB + cc];
-            float y = 0.0f;
+            float2 bv[kEPL], cv[kEPL];
+            const float4* bq = reinterpret_cast<const float4*>(Bf + r * NK + g * kEPL);
+            const float4 b0 = bq[0], b1 = bq[1];
+            bv[0] = make_float2(b0.x, b0.y);
+            bv[1] = make_float2(b0.z, b0.w);
+            bv[2] = make_float2(b1.x, b1.y);
+            bv[3] = make_float2(b1.z, b1.w);
+            if (!STATE_ONLY) {
+                const float4* cq = reinterpret_cast<const float4*>(Cf + r * NK + g * kEPL);
+                const float4 c0 = cq[0], c1 = cq[1];
+                cv[0] = make_float2(c0.x, -c0.y);
+                cv[1] = make_float2(c0.z, -c0.w);
+                cv[2] = make_float2(c1.x, -c1.y);
+                cv[3] = make_float2(c1.z, -c1.w);
+            }
+            float2 y2 = make_float2(0.0f, 0.0f);
 #pragma unroll
             for (int j = 0; j < kEPL; ++j) {
                 const float2 e = cexp_da<PRECISE>(dv.x, Ac[j]);
-                const float2 bv = cld2<T>(Bt + r * Cfg::kBCRowBytes + j * 2 * E);
-                const float hr = fmaf(e.x, h[j].x, fmaf(-e.y, h[j].y, dv.y * bv.x));
-                const float hi = fmaf(e.x, h[j].y, fmaf(e.y, h[j].x, dv.y * bv.y));
-                h[j] = make_float2(hr, hi);
-                if (!STATE_ONLY) {
-                    const float2 cv = cld2<T>(Bt + Cfg::kBCBytes + r * Cfg::kBCRowBytes + j * 2 * E);
-                    y = fmaf(cv.x, hr, fmaf(-cv.y, hi, y));
-                }
+                // h <- e h + u B in fp32 pairs: (e.re h.re - e.im h.im, e.re h.im + e.im h.re) + u B
+                float2 hn = __ffma2_rn(make_float2(dv.y, dv.y), bv[j], __fmul2_rn(make_float2(e.x, e.x), h[j]));
+                hn = __ffma2_rn(make_float2(-e.y, e.y), make_float2(h[j].y, h[j].x), hn);
+                h[j] = hn;
+                if (!STATE_ONLY) y2 = __ffma2_rn(cv[j], hn, y2);  // Re(C h) = C.re h.re - C.im h.im
             }
-            if (!STATE_ONLY) ys[(r * CPB + cc) * LPC + g] = y;
+            if (!STATE_ONLY) ys[(r * CPB + cc) * LPC + g] = y2.x + y2.y;
         }
         if (!STATE_ONLY) {
             __syncthreads();
