@@ -111,6 +111,20 @@ def algorithmic_flops(w) -> float:
     return float(w.batch * nchunks * (w.ngroups * per_chunk_group + w.nheads * per_chunk_head))
 
 
+def backward_flops(w) -> float:
+    """Tensor-core FLOPs of the chunked SSD backward (chunk 128): per chunk and head the
+    causal halves of M^T dY (Q^2 P), dY X^T (Q^2 P), Z B and Z^T C (Q^2 N each), the
+    inter-chunk products B R^T, dY h_in, X R and the adjoint chunk state (4 Q P N), the
+    recomputed forward chunk state (Q P N); per chunk and group the causal half of C B^T."""
+    if w.mode != "ssd":
+        return 0.0
+    Q, P, N = 128, w.headdim, w.dstate
+    nchunks = math.ceil(w.seqlen / Q)
+    mac_head = Q * Q * P / 2 * 2 + Q * Q * N / 2 * 2 + 5 * Q * P * N
+    mac_group = Q * Q * N / 2
+    return 2.0 * w.batch * nchunks * (w.nheads * mac_head + w.ngroups * mac_group)
+
+
 def _packed(specs, pinned, dev=None):
     """One contiguous buffer holding tensors of the given {name: (shape, dtype)} at
     256-byte aligned offsets; returns (buffer, {name: view})."""
@@ -888,11 +902,20 @@ def run_backward(args, w):
     roof = kernel_roofline(kt, nbytes, K, peaks["hbm_gbs"], peak_kind, whole)
     roof = with_traffic(roof, ("backward", w.name if args.seqlen is None else f"{w.name}@L{w.seqlen}"))
     sm_mhz = float(peaks.get("sm_max_mhz", 2032.0))
-    exps = 3.0 * w.token_channels * w.dstate  # the decay is formed in three sweeps
-    roof["sfu"] = {"achieved": exps / (ms_step * 1e-3), "peak": 148 * 32 * sm_mhz * 1e6,
-                   "unit": "exp/s", "frac": exps / (ms_step * 1e-3) / (148 * 32 * sm_mhz * 1e6),
-                   "note": "three exponentials per state entry and step (forward sweep, "
-                           "recompute, reverse); peak = 148 SMs x 32/clk x max SM clock"}
+    if "ssd_bwd_chunk_tc" in kt:
+        # the chunked tensor-core backward: algorithmic FLOPs of its products over the call
+        fl = backward_flops(w)
+        roof["tensor_tflops"] = fl / (ms_step * 1e-3) / 1e12
+        roof["tensor_frac"] = roof["tensor_tflops"] / peaks["bf16_tflops"]
+        roof["tensor_note"] = ("algorithmic FLOPs of the chunked backward's products (causal halves, "
+                               "chunk 128) over the whole call's time, against the measured bf16 dense peak")
+    else:
+        nsm = torch.cuda.get_device_properties(0).multi_processor_count
+        exps = 3.0 * w.token_channels * w.dstate  # the decay is formed in three sweeps
+        roof["sfu"] = {"achieved": exps / (ms_step * 1e-3), "peak": nsm * 32 * sm_mhz * 1e6,
+                       "unit": "exp/s", "frac": exps / (ms_step * 1e-3) / (nsm * 32 * sm_mhz * 1e6),
+                       "note": "three exponentials per state entry and step (forward sweep, "
+                               f"recompute, reverse); peak = {nsm} SMs x 32/clk x max SM clock"}
     cpu = e2e = None
     if not args.quick:
         host = dict(inp, dout=dout_h, dfinal=dfin_h)
