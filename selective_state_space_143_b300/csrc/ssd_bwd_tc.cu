@@ -19,12 +19,14 @@
 // sums B_s . (Z^T C)_s.  R itself follows the adjoint recurrence over chunks,
 //   R_{c-1} = exp(cum_last(c)) R_c + sum_t exp(cum_t) dy_t C_t^T,   R_last = dfinal,
 // whose chunk terms are the forward chunk-state kernel run on (dy, C) with weights
-// exp(cum_t) (ssd_state_tc, adjoint variant).  dD and dz are per element (dy pass).
+// exp(cum_t) (ssd_state_tc, adjoint variant).  dD = sum dy x comes from the chunk
+// kernel's epilogue, dz (per element) from the dy pass.  Without a gate dy = dout is exact
+// in bf16: the dy pass is skipped and the kernels read dout as dy's only plane.
 //
 // Kernels, in launch order:
 //   forward recompute: ssd_state_tc, ssd_state_pass_split (h_in of every chunk as bf16
 //     hi/lo tiles, final state), and with a gate ssd_scan_tc without it (y before the gate);
-//   ssd_bwd_dy        : dy as bf16 hi/lo planes, dz, dD;
+//   ssd_bwd_dy        : with a gate, dy as bf16 hi/lo planes and dz;
 //   ssd_state_tc (adjoint), ssd_bwd_reverse_carry: R_c of every chunk as hi/lo tiles,
 //     dinitial_state;
 //   ssd_bwd_chunk_tc  : one CTA per (chunk, batch, heads of one group): every product above
@@ -73,69 +75,51 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t&
 __device__ __forceinline__ float sigmoid_fast(float v) { return __fdividef(1.0f, 1.0f + ex2(-v * kLog2e)); }
 
 // ---- dy pass ------------------------------------------------------------------------
-// dy = dout SiLU(z) (dout without a gate) as bf16 hi/lo planes, dz = dout y SiLU'(z) with
-// y the output before the gate, dD_h = sum dy x.  grid (ceil(HP / 8 / 256), ceil(T /
-// kDyRows), batch); a thread owns one 8-column vector (16 bytes of bf16) over kDyRows rows.
+// With a gate: dy = dout SiLU(z) as bf16 hi/lo planes and dz = dout y SiLU'(z), y the
+// output before the gate.  grid (ceil(HP / 8 / 256), ceil(T / kDyRows), batch); a thread
+// owns one 8-column vector (16 bytes of bf16) over kDyRows rows.
 constexpr int kDyRows = 32;
 
 struct DyArgs {
     const __nv_bfloat16* dout;
-    const __nv_bfloat16* z;  // null: no gate
-    const __nv_bfloat16* y;  // output before the gate (with a gate)
-    const __nv_bfloat16* x;
+    const __nv_bfloat16* z;
+    const __nv_bfloat16* y;  // output before the gate
     __nv_bfloat16* dy_hi;
     __nv_bfloat16* dy_lo;
     float* dz;
-    float* dD;
     int64_t T, HP;
     int* status;
-    Span dyh_s, dyl_s, dz_s, dD_s;
+    Span dyh_s, dyl_s, dz_s;
 };
 
 __global__ void __launch_bounds__(256) ssd_bwd_dy(const DyArgs a) {
     const int64_t v = (int64_t)blockIdx.x * 256 + threadIdx.x;
-    const bool ok = v < a.HP / 8;
+    if (v >= a.HP / 8) return;
     const int64_t b = blockIdx.z;
     const int64_t t0 = (int64_t)blockIdx.y * kDyRows;
-    float dsum = 0.0f;
-    if (ok) {
-        for (int r = 0; r < kDyRows; ++r) {
-            const int64_t t = t0 + r;
-            if (t >= a.T) break;
-            const int64_t o = (b * a.T + t) * a.HP + v * 8;
-            float d[8], xs[8], dyv[8];
-            unpack8(*reinterpret_cast<const uint4*>(a.dout + o), d);
-            unpack8(*reinterpret_cast<const uint4*>(a.x + o), xs);
-            if (a.z) {
-                float zz[8], yy[8], dzv[8];
-                unpack8(*reinterpret_cast<const uint4*>(a.z + o), zz);
-                unpack8(*reinterpret_cast<const uint4*>(a.y + o), yy);
+    for (int r = 0; r < kDyRows; ++r) {
+        const int64_t t = t0 + r;
+        if (t >= a.T) break;
+        const int64_t o = (b * a.T + t) * a.HP + v * 8;
+        float d[8], zz[8], yy[8], dyv[8], dzv[8];
+        unpack8(*reinterpret_cast<const uint4*>(a.dout + o), d);
+        unpack8(*reinterpret_cast<const uint4*>(a.z + o), zz);
+        unpack8(*reinterpret_cast<const uint4*>(a.y + o), yy);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const float sg = sigmoid_fast(zz[k]);
-                    dyv[k] = d[k] * zz[k] * sg;
-                    dzv[k] = d[k] * yy[k] * sg * (1.0f + zz[k] * (1.0f - sg));
-                }
-                float4* dzp = reinterpret_cast<float4*>(a.dz + o);
-                store_checked(a.dz_s, dzp, make_float4(dzv[0], dzv[1], dzv[2], dzv[3]), a.status);
-                store_checked(a.dz_s, dzp + 1, make_float4(dzv[4], dzv[5], dzv[6], dzv[7]), a.status);
-            } else {
-#pragma unroll
-                for (int k = 0; k < 8; ++k) dyv[k] = d[k];
-            }
-            uint32_t hi[4], lo[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) split2(dyv[2 * j], dyv[2 * j + 1], hi[j], lo[j]);
-            store_checked(a.dyh_s, reinterpret_cast<uint4*>(a.dy_hi + o), make_uint4(hi[0], hi[1], hi[2], hi[3]), a.status);
-            store_checked(a.dyl_s, reinterpret_cast<uint4*>(a.dy_lo + o), make_uint4(lo[0], lo[1], lo[2], lo[3]), a.status);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) dsum = fmaf(dyv[k], xs[k], dsum);
+        for (int k = 0; k < 8; ++k) {
+            const float sg = sigmoid_fast(zz[k]);
+            dyv[k] = d[k] * zz[k] * sg;
+            dzv[k] = d[k] * yy[k] * sg * (1.0f + zz[k] * (1.0f - sg));
         }
-    }
-    // the 8 vectors of one head (P = 64) are 8 consecutive lanes
+        float4* dzp = reinterpret_cast<float4*>(a.dz + o);
+        store_checked(a.dz_s, dzp, make_float4(dzv[0], dzv[1], dzv[2], dzv[3]), a.status);
+        store_checked(a.dz_s, dzp + 1, make_float4(dzv[4], dzv[5], dzv[6], dzv[7]), a.status);
+        uint32_t hi[4], lo[4];
 #pragma unroll
-    for (int o = 4; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
-    if (ok && (v & 7) == 0 && a.dD) atomic_add_checked(a.dD_s, a.dD + v / 8, dsum, a.status);
+        for (int j = 0; j < 4; ++j) split2(dyv[2 * j], dyv[2 * j + 1], hi[j], lo[j]);
+        store_checked(a.dyh_s, reinterpret_cast<uint4*>(a.dy_hi + o), make_uint4(hi[0], hi[1], hi[2], hi[3]), a.status);
+        store_checked(a.dyl_s, reinterpret_cast<uint4*>(a.dy_lo + o), make_uint4(lo[0], lo[1], lo[2], lo[3]), a.status);
+    }
 }
 
 // ---- reverse carry ---------------------------------------------------------------------
@@ -238,7 +222,7 @@ struct __align__(16) BwdShared {
     float part[2][kQ];  // per row: x . dX_pre, dcum
     float wsum[4];
     float rsum[8];      // warp partials of <R, h_out>
-    float red[4][2];
+    float red[4][3];
     uint32_t tmem;
     volatile int abort;
 };
@@ -253,9 +237,9 @@ struct BwdTcArgs {
     const float* cum;
     const float* fst;    // forward h_in tiles (hi/lo) of every (b, chunk, head)
     const float* ast;    // R tiles (hi/lo)
-    float *dx, *ddt, *dA, *dB, *dC, *ddt_bias;
+    float *dx, *ddt, *dA, *dB, *dC, *dD, *ddt_bias;
     int64_t T, H, G, nchunks;
-    Span dx_s, ddt_s, dA_s, dB_s, dC_s, ddtb_s;
+    Span dx_s, ddt_s, dA_s, dB_s, dC_s, dD_s, ddtb_s;
 };
 
 __device__ __forceinline__ void bwd_wait(BwdShared& sh, uint64_t* mb, uint32_t phase) {
@@ -277,8 +261,9 @@ __device__ __forceinline__ void scale_split8(const float (&f)[8], float w, uint4
 // grid (nchunks, H / hpc, batch), 256 threads (8 warps; warp w reads TMEM lanes
 // 32*(w%4).. and takes column half w/4 of the M and Z builds).  Warps 0-3 own the rows of
 // the dx epilogue, w o X and the suffix sums (their thread index is the row); warps 4-7
-// those of the dcum epilogue and exp(cum) dY.
-template <int N>
+// those of the dcum epilogue and exp(cum) dY.  DYLO: dy has a lo plane (with a gate);
+// without it dy = dout is exact in bf16 and its lo products are skipped.
+template <int N, bool DYLO>
 __global__ void __launch_bounds__(256, 1)
     ssd_bwd_chunk_tc(const BwdTcArgs a, const int hpc, int* status, const __grid_constant__ CUtensorMap tm_c,
                      const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_x,
@@ -326,9 +311,9 @@ __global__ void __launch_bounds__(256, 1)
         tc::tma_load_3d(sA, &tm_x, (hbeg + hi) * kP, row0, b, &sh.mb_x);
     };
     auto issue_dy = [&](int hi) {
-        tc::mbar_arrive_expect_tx(&sh.mb_dy, 2 * Cfg::kDy);
+        tc::mbar_arrive_expect_tx(&sh.mb_dy, (DYLO ? 2 : 1) * Cfg::kDy);
         tc::tma_load_3d(sDy, &tm_dyh, (hbeg + hi) * kP, row0, b, &sh.mb_dy);
-        tc::tma_load_3d(sDy + Cfg::kDy, &tm_dyl, (hbeg + hi) * kP, row0, b, &sh.mb_dy);
+        if (DYLO) tc::tma_load_3d(sDy + Cfg::kDy, &tm_dyl, (hbeg + hi) * kP, row0, b, &sh.mb_dy);
     };
     if (tid == 0) {
         tc::mbar_arrive_expect_tx(&sh.mb_cb, 2 * Cfg::kCB);
@@ -391,7 +376,7 @@ __global__ void __launch_bounds__(256, 1)
                                  tc::desc_sw128(tc::smem_u32(sB) + o, 16, 1024), id, ks > 0);
                 }
 #pragma unroll
-                for (int pl = 0; pl < 2; ++pl)
+                for (int pl = 0; pl < (DYLO ? 2 : 1); ++pl)
 #pragma unroll
                     for (int ks = 0; ks < kP / 16; ++ks)
                         tc::mma_bf16(tZ, tc::desc_sw128(tc::smem_u32(sDy + pl * Cfg::kDy) + ks * 32, 16, 1024),
@@ -452,7 +437,7 @@ __global__ void __launch_bounds__(256, 1)
                 constexpr uint32_t idX = tc::idesc_bf16(128, kP, 1, 1);
                 const int combo_m[3] = {0, 1, 0}, combo_d[3] = {0, 0, 1};
 #pragma unroll
-                for (int cb = 0; cb < 3; ++cb)
+                for (int cb = 0; cb < (DYLO ? 3 : 2); ++cb)
 #pragma unroll
                     for (int ks = 0; ks < kQ / 16; ++ks)
                         tc::mma_bf16(tX, tc::desc_mnmajor(aM + combo_m[cb] * Cfg::kMat, 128, ks),
@@ -506,11 +491,14 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
             for (int pc = 0; pc < 8; ++pc) {
                 const uint32_t off = (uint32_t)(t * 128 + ((pc ^ (t & 7)) * 16));
-                float fh[8], fl[8];
+                float fh[8];
                 unpack8(*reinterpret_cast<const uint4*>(sDy + off), fh);
-                unpack8(*reinterpret_cast<const uint4*>(sDy + Cfg::kDy + off), fl);
+                if (DYLO) {
+                    float fl[8];
+                    unpack8(*reinterpret_cast<const uint4*>(sDy + Cfg::kDy + off), fl);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) fh[k] += fl[k];
+                    for (int k = 0; k < 8; ++k) fh[k] += fl[k];
+                }
                 uint4 vh, vl;
                 scale_split8(fh, e, vh, vl);
                 *reinterpret_cast<uint4*>(sZ + 2 * Cfg::kDy + off) = vh;
@@ -573,6 +561,7 @@ __global__ void __launch_bounds__(256, 1)
         if (sh.abort) break;
         if (tid == 0 && hi + 1 < hpc) issue_x(hi + 1);  // region A is free again
         float prd = __expf(cum_last) * phr;  // this thread's part of <R, h_out>
+        float pdd = 0.0f;                      // this thread's part of dD (row s, warps 0-3)
 
         // ---- phase 4: epilogues
         if (half == 0) {
@@ -583,6 +572,7 @@ __global__ void __launch_bounds__(256, 1)
             const float Dh = a.D ? a.D[h] : 0.0f;
             const float dls = sh.dl[s];
             float xri = 0.0f;  // x_s . (B R^T)_s
+            float xdy = 0.0f;  // x_s . dy_s (dD)
             float* dxr = a.dx + ((int64_t)b * a.T + row0 + s) * HP + (int64_t)h * kP;
 #pragma unroll
             for (int p0 = 0; p0 < kP; p0 += 16) {
@@ -596,17 +586,19 @@ __global__ void __launch_bounds__(256, 1)
                     for (int c8 = 0; c8 < 2; ++c8) {
                         const int pc = (p0 >> 3) + c8;
                         const uint32_t off = (uint32_t)(s * 128 + ((pc ^ (s & 7)) * 16));
-                        float fx[8], fh[8], fl[8];
+                        float fx[8], fh[8], fl[8] = {};
                         unpack8(cx[pc], fx);
                         unpack8(*reinterpret_cast<const uint4*>(sDy + off), fh);
-                        unpack8(*reinterpret_cast<const uint4*>(sDy + Cfg::kDy + off), fl);
+                        if (DYLO) unpack8(*reinterpret_cast<const uint4*>(sDy + Cfg::kDy + off), fl);
 #pragma unroll
                         for (int k = 0; k < 8; ++k) {
                             const int j = c8 * 8 + k;
                             const float pre = fmaf(dec, __uint_as_float(xi[j]), __uint_as_float(xv[j]));
+                            const float dy = fh[k] + fl[k];
                             ddir = fmaf(fx[k], pre, ddir);
                             xri = fmaf(fx[k], __uint_as_float(xi[j]), xri);
-                            out[j] = fmaf(dls, pre, Dh * (fh[k] + fl[k]));
+                            xdy = fmaf(fx[k], dy, xdy);
+                            out[j] = fmaf(dls, pre, Dh * dy);
                         }
                     }
                     float4* dst = reinterpret_cast<float4*>(dxr + p0);
@@ -617,6 +609,7 @@ __global__ void __launch_bounds__(256, 1)
             }
             sh.part[0][s] = ddir;
             prd = fmaf(dls * dec, xri, prd);  // w_s x_s . (B R^T)_s: <R, S_c> of row s
+            pdd = xdy;
         } else {
             // dcum of row t = r: C_t . dC_t - B_t . dB_t for this head (running sums over
             // the CTA's heads, differenced)
@@ -676,25 +669,29 @@ __global__ void __launch_bounds__(256, 1)
                 ddt = dDelta * sigmoid_fast(cdt + bias);
                 store_checked(a.ddt_s, &a.ddt[((int64_t)b * a.T + row0 + t) * a.H + h], ddt, status);
             }
-            float pa = sh.dl[t] * da, pb = ddt;
+            float pa = sh.dl[t] * da, pb = ddt, pc = pdd;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
                 pa += __shfl_xor_sync(0xffffffffu, pa, o);
                 pb += __shfl_xor_sync(0xffffffffu, pb, o);
+                pc += __shfl_xor_sync(0xffffffffu, pc, o);
             }
             if (lane == 0) {
                 sh.red[q][0] = pa;
                 sh.red[q][1] = pb;
+                sh.red[q][2] = pc;
             }
             asm volatile("bar.sync 1, 128;" ::: "memory");
             if (tid == 0) {
-                float sa = 0.0f, sbias = 0.0f;
+                float sa = 0.0f, sbias = 0.0f, sd = 0.0f;
                 for (int w = 0; w < 4; ++w) {
                     sa += sh.red[w][0];
                     sbias += sh.red[w][1];
+                    sd += sh.red[w][2];
                 }
                 atomic_add_checked(a.dA_s, a.dA + h, sa, status);
                 if (a.ddt_bias) atomic_add_checked(a.ddtb_s, a.ddt_bias + h, sbias, status);
+                if (a.dD) atomic_add_checked(a.dD_s, a.dD + h, sd, status);
             }
         }
         tc::fence_before_sync();
@@ -798,21 +795,21 @@ int bwd_heads_per_cta(const ScanArgs& a, int64_t nchunks) {
     return 1;
 }
 
-template <int N>
+template <int N, bool DYLO>
 cudaError_t launch_chunk(const BwdTcArgs& k, const ScanArgs& f, const BwdTcPlan& pl, const void* dyh, const void* dyl,
                          cudaStream_t stream) {
     using Cfg = BwdCfg<N>;
     CUtensorMap tc_, tb_, tx_, tdh, tdl;
     const uint64_t T = (uint64_t)f.seqlen, nb = (uint64_t)f.batch, HP = (uint64_t)f.nheads * kP;
     if (!bwd_map(&tc_, f.C, (uint64_t)f.ngroups * N, T, nb) || !bwd_map(&tb_, f.B, (uint64_t)f.ngroups * N, T, nb) ||
-        !bwd_map(&tx_, f.x, HP, T, nb) || !bwd_map(&tdh, dyh, HP, T, nb) || !bwd_map(&tdl, dyl, HP, T, nb))
+        !bwd_map(&tx_, f.x, HP, T, nb) || !bwd_map(&tdh, dyh, HP, T, nb) || !bwd_map(&tdl, DYLO ? dyl : dyh, HP, T, nb))
         return cudaErrorInvalidValue;
     int* status = nullptr;
     cudaError_t e = device_status_address(&status);
     if (e != cudaSuccess) return e;
     constexpr uint32_t smem_bytes = Cfg::kSmem + (uint32_t)sizeof(BwdShared);
     static_assert(smem_bytes <= 232448, "shared memory");
-    auto kern = ssd_bwd_chunk_tc<N>;
+    auto kern = ssd_bwd_chunk_tc<N, DYLO>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
     if (e != cudaSuccess) return e;
     const int hpc = bwd_heads_per_cta(f, pl.nchunks);
@@ -888,24 +885,24 @@ cudaError_t ssd_bwd_tc_launch(const ScanBwdArgs& s, void* ws, cudaStream_t strea
         if (e != cudaSuccess) return e;
     }
 
-    // dy planes, dz, dD
-    {
+    // with a gate: dy planes and dz; without one dy = dout, exact in bf16, read in place
+    const bool gate = f.z != nullptr;
+    const __nv_bfloat16* dy_hi = gate ? dyh : static_cast<const __nv_bfloat16*>(s.dout);
+    const __nv_bfloat16* dy_lo = gate ? dyl : nullptr;
+    if (gate) {
         DyArgs d;
         d.dout = static_cast<const __nv_bfloat16*>(s.dout);
         d.z = static_cast<const __nv_bfloat16*>(f.z);
         d.y = y;
-        d.x = static_cast<const __nv_bfloat16*>(f.x);
         d.dy_hi = dyh;
         d.dy_lo = dyl;
         d.dz = s.dz;
-        d.dD = s.dD;
         d.T = T;
         d.HP = H * P;
         d.status = status;
         d.dyh_s = span_of(dyh, el * 2);
         d.dyl_s = span_of(dyl, el * 2);
         d.dz_s = span_of(s.dz, el * 4);
-        d.dD_s = span_of(s.dD, (size_t)H * 4);
         const dim3 grid((unsigned)((H * P / 8 + 255) / 256), (unsigned)((T + kDyRows - 1) / kDyRows), (unsigned)b);
         cudaEvent_t t0 = timing_begin(stream);
         ssd_bwd_dy<<<grid, 256, 0, stream>>>(d);
@@ -916,8 +913,8 @@ cudaError_t ssd_bwd_tc_launch(const ScanBwdArgs& s, void* ws, cudaStream_t strea
 
     // adjoint chunk states, then R over the chunks in reverse
     SsdTcArgs ta = t;
-    ta.x = dyh;
-    ta.x_lo = dyl;
+    ta.x = dy_hi;
+    ta.x_lo = dy_lo;
     ta.B = static_cast<const __nv_bfloat16*>(f.C);
     ta.states = ast;
     ta.states_s = span_of(ast, stb);
@@ -963,6 +960,7 @@ cudaError_t ssd_bwd_tc_launch(const ScanBwdArgs& s, void* ws, cudaStream_t strea
     k.dB = s.dB;
     k.dC = s.dC;
     k.ddt_bias = s.ddt_bias;
+    k.dD = s.dD;
     k.T = T;
     k.H = H;
     k.G = f.ngroups;
@@ -973,7 +971,12 @@ cudaError_t ssd_bwd_tc_launch(const ScanBwdArgs& s, void* ws, cudaStream_t strea
     k.dB_s = span_of(s.dB, (size_t)b * T * f.ngroups * N * 4);
     k.dC_s = span_of(s.dC, (size_t)b * T * f.ngroups * N * 4);
     k.ddtb_s = span_of(s.ddt_bias, (size_t)H * 4);
-    return N == 64 ? launch_chunk<64>(k, f, pl, dyh, dyl, stream) : launch_chunk<128>(k, f, pl, dyh, dyl, stream);
+    k.dD_s = span_of(s.dD, (size_t)H * 4);
+    if (gate)
+        return N == 64 ? launch_chunk<64, true>(k, f, pl, dy_hi, dy_lo, stream)
+                       : launch_chunk<128, true>(k, f, pl, dy_hi, dy_lo, stream);
+    return N == 64 ? launch_chunk<64, false>(k, f, pl, dy_hi, dy_lo, stream)
+                   : launch_chunk<128, false>(k, f, pl, dy_hi, dy_lo, stream);
 }
 
 }  // namespace ssm

@@ -424,10 +424,9 @@ cudaError_t ssd_tc_chunk_state(const SsdTcArgs& s, int64_t batch, cudaStream_t s
 }
 
 cudaError_t ssd_tc_chunk_state_adjoint(const SsdTcArgs& s, int64_t batch, cudaStream_t stream) {
-    if (!s.x_lo) return cudaErrorInvalidValue;
     switch (s.N) {
-        case 64: return launch_state<64, true, true>(s, batch, stream);
-        case 128: return launch_state<128, true, true>(s, batch, stream);
+        case 64: return s.x_lo ? launch_state<64, true, true>(s, batch, stream) : launch_state<64, false, true>(s, batch, stream);
+        case 128: return s.x_lo ? launch_state<128, true, true>(s, batch, stream) : launch_state<128, false, true>(s, batch, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -38,8 +38,8 @@ cudaError_t ssd_tc_chunk_state(const SsdTcArgs& s, int64_t batch, cudaStream_t s
 
 // Adjoint chunk states of the backward pass, S^g_c = sum_t exp(cum_t) dy_t C_t^T for
 // every (chunk, head) into states (split-ready layout), with x / x_lo the hi / lo planes
-// of dy and B the C rows; reads dt for the weights, writes neither dl nor cum.  dstate
-// 64 or 128.
+// of dy (x_lo null when dy is exact in bf16) and B the C rows; reads dt for the weights,
+// writes neither dl nor cum.  dstate 64 or 128.
 cudaError_t ssd_tc_chunk_state_adjoint(const SsdTcArgs& s, int64_t batch, cudaStream_t stream);
 
 // out for every chunk, reading h_{c-1} from states (after the carry pass).
