@@ -48,7 +48,7 @@ def test_slowest_rank_time_over_gloo(tmp_path):
 
 
 def test_reference_arm_under_torchrun_prints_one_line():
-    """Launched as the driver launches it (torchrun, 2 ranks, 127.0.0.1): rank 0 times
+    """Launched the way a multi-GPU bench run is (torchrun, 2 ranks, 127.0.0.1): rank 0 times
     the oracle and prints one line; rank 1 does no work and exits 0."""
     port = free_port()
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
