@@ -182,6 +182,10 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
     extern __shared__ float s_acc[];               // [2][kSeg][CPB][SNP]: dB and dC terms
     float* s_dB = s_acc;
     float* s_dC = s_acc + kSeg * CPB * SNP;
+    // [kSeg][NP]: the segment's B rows (fp32); the part-summary pass has no dB / dC terms
+    // and is launched with room for the two row tiles only
+    float* s_B = PARTS ? s_acc : s_acc + 2 * kSeg * CPB * SNP;
+    float* s_C = s_B + kSeg * NP;                  // [kSeg][NP]: its C rows
     const int tid = threadIdx.x;
     const int lane = tid % LPC;
     const int cc = tid / LPC;  // channel within the block
@@ -225,6 +229,18 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
     auto drow = [&](int64_t t) { return (b * L + t) * H + hd; };  // dt and ddt
     auto bc = [&](int64_t t) { return (b * L + t) * G * N + (int64_t)group * N; };
     auto fetch = [&](const float (&v)[SPL], int j) { return __shfl_sync(0xffffffffu, v[j / LPC], j % LPC, LPC); };
+    // B and / or C rows t0 .. t0 + len - 1 of the block's group into shared memory as fp32
+    // (zero past len and N), read by every channel of the block; the caller's block
+    // barrier before it keeps earlier readers safe, the one inside makes the rows visible
+    auto stage_bc = [&](int64_t t0, int len, bool withB, bool withC) {
+        for (int i = tid; i < kSeg * NP; i += kBwdThreads) {
+            const int j = i / NP, n = i % NP;
+            const bool ok = j < len && n < N;
+            if (withB) s_B[i] = ok ? to_f32<T>(a.B[bc(t0 + j) + n]) : 0.0f;
+            if (withC) s_C[i] = ok ? to_f32<T>(a.C[bc(t0 + j) + n]) : 0.0f;
+        }
+        __syncthreads();
+    };
 
     const int part = blockIdx.y, nparts = gridDim.y;
     const int sub0 = part * a.subs_per_part, sub1 = min(a.nseg, sub0 + a.subs_per_part);
@@ -245,6 +261,8 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
     float dsum_lane = 0.0f;  // PARTS: this lane's steps of Delta
     for (int seg = sub0; seg < sub1; ++seg) {
         const int64_t t0 = (int64_t)seg * kSeg;
+        __syncthreads();  // every thread is done with the previous segment's rows
+        stage_bc(t0, (int)min((int64_t)kSeg, L - t0), true, false);
         if (!PARTS) {
 #pragma unroll
             for (int r = 0; r < R; ++r)
@@ -269,10 +287,7 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
             float av[R];
             decays(de, av);
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const float Bv = nok[r] ? to_f32<T>(a.B[bc(t0 + j) + nr[r]]) : 0.0f;
-                h[r] = fmaf(av[r], h[r], u * Bv);
-            }
+            for (int r = 0; r < R; ++r) h[r] = fmaf(av[r], h[r], u * s_B[j * NP + nr[r]]);
         }
     }
 
@@ -293,6 +308,8 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
         for (int seg = sub1 - 1; seg >= sub0; --seg) {
             const int64_t t0 = (int64_t)seg * kSeg;
             const int len = (int)min((int64_t)kSeg, L - t0);
+            __syncthreads();
+            stage_bc(t0, len, false, true);
             float pde[SPL], pdy[SPL];
 #pragma unroll
             for (int k = 0; k < SPL; ++k) {
@@ -317,10 +334,7 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
                 float av[R];
                 decays(de, av);
 #pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const float Cv = nok[r] ? to_f32<T>(a.C[bc(t0 + j) + nr[r]]) : 0.0f;
-                    q[r] = av[r] * fmaf(dy, Cv, q[r]);
-                }
+                for (int r = 0; r < R; ++r) q[r] = av[r] * fmaf(dy, s_C[j * NP + nr[r]], q[r]);
             }
         }
 #pragma unroll
@@ -342,9 +356,11 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
                 if (nok[r]) g[r] = fmaf(decay(ds, r), g[r], a.Qloc[sidx(k) * N + nr[r]]);
         }
         float dD_acc = 0.0f, dbias_acc = 0.0f;  // this lane's steps
+        __syncthreads();  // every thread is done with the forward sweep's last rows
         for (int seg = sub1 - 1; seg >= sub0; --seg) {
             const int64_t t0 = (int64_t)seg * kSeg;
             const int len = (int)min((int64_t)kSeg, L - t0);
+            stage_bc(t0, len, true, true);  // the previous segment ended with a block barrier
             // per-step scalars of the segment
             float pde[SPL], pu[SPL], px[SPL], pdy[SPL], pdz[SPL], psig[SPL];
 #pragma unroll
@@ -380,10 +396,8 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
                     float av[R];
                     decays(de, av);
 #pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        const float Bv = nok[r] ? to_f32<T>(a.B[bc(t0 + j) + nr[r]]) : 0.0f;
-                        hs[j][r] = fmaf(av[r], j == 0 ? h0[r] : hs[j - 1][r], u * Bv);
-                    }
+                    for (int r = 0; r < R; ++r)
+                        hs[j][r] = fmaf(av[r], j == 0 ? h0[r] : hs[j - 1][r], u * s_B[j * NP + nr[r]]);
                 }
             }
 #pragma unroll
@@ -396,8 +410,8 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
                 decays(de, avs);
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    const float Bv = nok[r] ? to_f32<T>(a.B[bc(t) + nr[r]]) : 0.0f;
-                    const float Cv = nok[r] ? to_f32<T>(a.C[bc(t) + nr[r]]) : 0.0f;
+                    const float Bv = s_B[j * NP + nr[r]];
+                    const float Cv = s_C[j * NP + nr[r]];
                     const float av = avs[r];
                     const float hp = j == 0 ? h0[r] : hs[j - 1][r];
                     yp = fmaf(Cv, hs[j][r], yp);
@@ -471,7 +485,7 @@ template <typename T, int LPC, int R, bool SSD>
 cudaError_t launch_bwd(const BwdArgs<T>& a, int parts, int64_t batch, cudaStream_t stream) {
     constexpr int kSeg = R <= 2 ? 16 : R == 4 ? 8 : 4;  // as bwd_plan
     constexpr int CPB = kBwdThreads / LPC;
-    constexpr size_t kSmem = sizeof(float) * 2 * kSeg * CPB * (LPC * R + (R > 1 ? LPC : 0));
+    constexpr size_t kSmem = sizeof(float) * (2 * kSeg * CPB * (LPC * R + (R > 1 ? LPC : 0)) + 2 * kSeg * LPC * R);
     BwdArgs<T> k = a;
     k.tiles_per_group = (int)((a.cpg + CPB - 1) / CPB);
     if (k.nseg != (int)((a.L + kSeg - 1) / kSeg))
@@ -483,8 +497,10 @@ cudaError_t launch_bwd(const BwdArgs<T>& a, int parts, int64_t batch, cudaStream
         if (e != cudaSuccess) return e;
     }
     if (parts > 1) {
+        constexpr size_t kSmemParts = sizeof(float) * 2 * kSeg * LPC * R;  // B and C rows of a segment
+        static_assert(kSmemParts <= 48 * 1024, "part-summary rows");
         cudaEvent_t t1 = timing_begin(stream);
-        scan_bwd_kernel<T, LPC, R, kSeg, SSD, true><<<grid, kBwdThreads, 0, stream>>>(k);
+        scan_bwd_kernel<T, LPC, R, kSeg, SSD, true><<<grid, kBwdThreads, kSmemParts, stream>>>(k);
         note_launch("scan_bwd_kernel (part summaries)", stream, t1);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
