@@ -259,8 +259,29 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
         }
     }
     float dsum_lane = 0.0f;  // PARTS: this lane's steps of Delta
+    // dt and x of a segment, loaded one segment ahead
+    float fw_dt[SPL], fw_x[SPL];
+    auto prefetch_fw = [&](int sg) {
+        const int64_t t0 = (int64_t)sg * kSeg;
+        const int len = (int)min((int64_t)kSeg, L - t0);
+#pragma unroll
+        for (int k = 0; k < SPL; ++k) {
+            const int j = lane + LPC * k;
+            const bool ok = c_ok && j < len;
+            fw_dt[k] = ok ? to_f32<T>(a.dt[drow(t0 + j)]) : 0.0f;
+            fw_x[k] = ok ? to_f32<T>(a.x[row(t0 + j)]) : 0.0f;
+        }
+    };
+    if (sub1 > sub0) prefetch_fw(sub0);
     for (int seg = sub0; seg < sub1; ++seg) {
         const int64_t t0 = (int64_t)seg * kSeg;
+        float cdt[SPL], cx[SPL];
+#pragma unroll
+        for (int k = 0; k < SPL; ++k) {
+            cdt[k] = fw_dt[k];
+            cx[k] = fw_x[k];
+        }
+        if (seg + 1 < sub1) prefetch_fw(seg + 1);
         __syncthreads();  // every thread is done with the previous segment's rows
         stage_bc(t0, (int)min((int64_t)kSeg, L - t0), true, false);
         if (!PARTS) {
@@ -275,8 +296,8 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
             const int j = lane + LPC * k;
             pde[k] = pu[k] = 0.0f;
             if (c_ok && j < len) {
-                pde[k] = softplus_t<PRECISE>(to_f32<T>(a.dt[drow(t0 + j)]) + bias);
-                pu[k] = pde[k] * to_f32<T>(a.x[row(t0 + j)]);
+                pde[k] = softplus_t<PRECISE>(cdt[k] + bias);
+                pu[k] = pde[k] * cx[k];
                 dsum_lane += pde[k];
             }
         }
@@ -356,10 +377,41 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
                 if (nok[r]) g[r] = fmaf(decay(ds, r), g[r], a.Qloc[sidx(k) * N + nr[r]]);
         }
         float dD_acc = 0.0f, dbias_acc = 0.0f;  // this lane's steps
+        // the raw per-step inputs and the checkpoint of a segment, loaded one segment ahead
+        // so that their latency hides behind the previous segment's sweeps
+        float nx_dt[SPL], nx_x[SPL], nx_do[SPL], nx_z[SPL], nx_h0[R];
+        auto prefetch_seg = [&](int sg) {
+            const int64_t t0 = (int64_t)sg * kSeg;
+            const int len = (int)min((int64_t)kSeg, L - t0);
+#pragma unroll
+            for (int k = 0; k < SPL; ++k) {
+                const int j = lane + LPC * k;
+                const bool ok = c_ok && j < len;
+                const int64_t t = t0 + j;
+                nx_dt[k] = ok ? to_f32<T>(a.dt[drow(t)]) : 0.0f;
+                nx_x[k] = ok ? to_f32<T>(a.x[row(t)]) : 0.0f;
+                nx_do[k] = ok ? to_f32<T>(a.dout[row(t)]) : 0.0f;
+                nx_z[k] = (ok && a.z) ? to_f32<T>(a.z[row(t)]) : 0.0f;
+            }
+#pragma unroll
+            for (int r = 0; r < R; ++r) nx_h0[r] = nok[r] ? a.ckpt[((b * a.nseg + sg) * dim + c) * N + nr[r]] : 0.0f;
+        };
+        if (sub1 > sub0) prefetch_seg(sub1 - 1);
         __syncthreads();  // every thread is done with the forward sweep's last rows
         for (int seg = sub1 - 1; seg >= sub0; --seg) {
             const int64_t t0 = (int64_t)seg * kSeg;
             const int len = (int)min((int64_t)kSeg, L - t0);
+            float rdt[SPL], rx[SPL], rdo[SPL], rz[SPL], h0[R];
+#pragma unroll
+            for (int k = 0; k < SPL; ++k) {
+                rdt[k] = nx_dt[k];
+                rx[k] = nx_x[k];
+                rdo[k] = nx_do[k];
+                rz[k] = nx_z[k];
+            }
+#pragma unroll
+            for (int r = 0; r < R; ++r) h0[r] = nx_h0[r];
+            if (seg > sub0) prefetch_seg(seg - 1);
             stage_bc(t0, len, true, true);  // the previous segment ended with a block barrier
             // per-step scalars of the segment
             float pde[SPL], pu[SPL], px[SPL], pdy[SPL], pdz[SPL], psig[SPL];
@@ -368,15 +420,14 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
                 const int j = lane + LPC * k;
                 pde[k] = pu[k] = px[k] = pdy[k] = pdz[k] = psig[k] = 0.0f;
                 if (c_ok && j < len) {
-                    const int64_t t = t0 + j;
-                    const float v = to_f32<T>(a.dt[drow(t)]) + bias;
+                    const float v = rdt[k] + bias;
                     pde[k] = softplus_t<PRECISE>(v);
                     psig[k] = 1.0f / (1.0f + __expf(-v));
-                    px[k] = to_f32<T>(a.x[row(t)]);
+                    px[k] = rx[k];
                     pu[k] = pde[k] * px[k];
-                    const float dov = to_f32<T>(a.dout[row(t)]);
+                    const float dov = rdo[k];
                     if (a.z) {
-                        const float zv = to_f32<T>(a.z[row(t)]);
+                        const float zv = rz[k];
                         const float sz = 1.0f / (1.0f + __expf(-zv));
                         pdy[k] = dov * zv * sz;
                         pdz[k] = dov * sz * (1.0f + zv * (1.0f - sz));
@@ -386,9 +437,7 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs<T> 
                 }
             }
             // the segment's states h_t (after step t), recomputed from the checkpoint
-            float hs[kSeg][R], h0[R];
-#pragma unroll
-            for (int r = 0; r < R; ++r) h0[r] = nok[r] ? a.ckpt[((b * a.nseg + seg) * dim + c) * N + nr[r]] : 0.0f;
+            float hs[kSeg][R];
 #pragma unroll
             for (int j = 0; j < kSeg; ++j) {
                 if (j < len) {
