@@ -223,11 +223,15 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
             }
         }
     } else if (warp == kMmaWarp) {
-        // ---- MMA issuer (one thread)
+        // ---- MMA issuer (one thread).  A shared-memory access by this thread (a barrier
+        // test, a flag read) waits behind the operand reads of the MMAs it has issued, so
+        // the tensor pipe idles while it completes: the loop makes one barrier wait per
+        // M' part and keeps its own give-up state in a register (a wait given up
+        // elsewhere in the CTA stops the arrivals, and its own bounded waits then end).
         if (lane == 0) {
-            pipe_wait(sh, &sh.mb_load, 0);
+            bool ok = tc::mbar_wait(&sh.mb_load, 0);
             tc::fence_after_sync();
-            if (!sh.abort) {
+            if (ok) {
                 const uint32_t idesc = tc::idesc_bf16(128, SW, 0, 0);
 #pragma unroll 1
                 for (int ks = 0; ks < N / 16; ++ks) {
@@ -241,18 +245,35 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
             constexpr uint32_t id_diag = tc::idesc_bf16(128, kP, 0, 1);
             constexpr uint32_t id_off = tc::idesc_bf16(128, kP, 0, 0);
             uint32_t n = 0;  // M' parts consumed so far
-            for (int hi = 0; hi < nh && !sh.abort; ++hi) {
+            for (int hi = 0; hi < nh && ok; ++hi) {
                 const int ab = hi & 1;
                 const uint32_t tYd = tmem + 256 + 128 * ab, tYo = tYd + 64;
-                if (hi >= 2) pipe_wait(sh, &sh.acc_empty[ab], ((hi - 2) >> 1) & 1);  // head hi-2's epilogue read them
-                pipe_wait(sh, &sh.x_full[xbuf(hi)], xuse(hi) & 1);
-                pipe_wait(sh, &sh.h_full[hbuf(hi)], huse(hi) & 1);
+                if (hi >= 2) ok = tc::mbar_wait(&sh.acc_empty[ab], ((hi - 2) >> 1) & 1);  // head hi-2's epilogue read them
+                ok = ok && tc::mbar_wait(&sh.h_full[hbuf(hi)], huse(hi) & 1);
                 tc::fence_after_sync();
-                for (int kp = 0; kp < nparts && !sh.abort; ++kp, ++n) {
+                if (!ok) break;
+                {
+                    // Y_off = C h_hi + C h_lo first: it needs no M' part, so the tensor pipe
+                    // runs it while the compute warps finish the previous heads and build
+                    // this head's first part
+                    const uint32_t cb = tc::smem_u32(sC);
+                    const uint32_t hs = tc::smem_u32(sH + hbuf(hi) * 2 * Cfg::kH);
+                    const uint64_t dhh = tc::desc_strided(hs, 128, (N / 8) * 128);
+                    const uint64_t dhl = tc::desc_strided(hs + Cfg::kH, 128, (N / 8) * 128);
+#pragma unroll
+                    for (int ks = 0; ks < N / 16; ++ks) {
+                        const uint64_t dc = tc::desc_sw128(cb + (uint32_t)(ks >> 2) * 128 * 128 + (uint32_t)(ks & 3) * 32, 16, 1024);
+                        tc::mma_bf16(tYo, dc, dhh + ks * 16u, id_off, ks > 0 ? 1u : 0u);
+                        tc::mma_bf16(tYo, dc, dhl + ks * 16u, id_off, 1u);
+                    }
+                    tc::mma_commit(&sh.h_empty[hbuf(hi)]);  // the h tiles may be replaced
+                }
+                ok = tc::mbar_wait(&sh.x_full[xbuf(hi)], xuse(hi) & 1);
+                for (int kp = 0; kp < nparts && ok; ++kp, ++n) {
                     const uint32_t pb = n % Cfg::kParts;
-                    pipe_wait(sh, &sh.full_part[pb], (n / Cfg::kParts) & 1);
+                    ok = tc::mbar_wait(&sh.full_part[pb], (n / Cfg::kParts) & 1);
                     tc::fence_after_sync();
-                    if (sh.abort) break;
+                    if (!ok) break;
                     const uint32_t mh = tc::smem_u32(sM + pb * 2 * Cfg::kMPart);
                     const uint64_t dmh = tc::desc_strided(mh, 128, (KPC / 8) * 128);
                     const uint64_t dml = tc::desc_strided(mh + Cfg::kMPart, 128, (KPC / 8) * 128);
@@ -269,26 +290,13 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
 #pragma unroll
                         for (int ks = 0; ks < KPC / 16; ++ks) tc::mma_bf16(tYd, dmh + ks * 16u, dxl + ks * 128u, id_diag, 1u);
                     }
-                    // the part buffer may be rebuilt once these MMAs are done, before the
-                    // head's Y_off MMAs below
-                    tc::mma_commit(&sh.empty_part[pb]);
-                    if (kp == 0) {
-                        const uint32_t cb = tc::smem_u32(sC);
-                        const uint32_t hs = tc::smem_u32(sH + hbuf(hi) * 2 * Cfg::kH);
-                        const uint64_t dhh = tc::desc_strided(hs, 128, (N / 8) * 128);
-                        const uint64_t dhl = tc::desc_strided(hs + Cfg::kH, 128, (N / 8) * 128);
-#pragma unroll
-                        for (int ks = 0; ks < N / 16; ++ks) {
-                            const uint64_t dc = tc::desc_sw128(cb + (uint32_t)(ks >> 2) * 128 * 128 + (uint32_t)(ks & 3) * 32, 16, 1024);
-                            tc::mma_bf16(tYo, dc, dhh + ks * 16u, id_off, ks > 0 ? 1u : 0u);
-                            tc::mma_bf16(tYo, dc, dhl + ks * 16u, id_off, 1u);
-                        }
-                        tc::mma_commit(&sh.h_empty[hbuf(hi)]);  // the h tiles may be replaced
-                    }
+                    tc::mma_commit(&sh.empty_part[pb]);  // the part buffer may be rebuilt
                 }
+                if (!ok) break;
                 tc::mma_commit(&sh.acc_full[ab]);   // the epilogue may read this head's accumulators
                 tc::mma_commit(&sh.x_empty[xbuf(hi)]);
             }
+            if (!ok) sh.abort = 1;
         }
     } else {
         // ---- compute warps: M' builds and epilogues

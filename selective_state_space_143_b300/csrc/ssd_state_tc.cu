@@ -162,21 +162,25 @@ __global__ void __launch_bounds__(kCta, 1)
             }
         }
     } else if (warp == kMma) {
-        // ---- MMA: D[(head, p), n] += Xw^T B per K-part, 64 columns of n per MMA
+        // ---- MMA: D[(head, p), n] += Xw^T B per K-part, all N columns per MMA.  A
+        // shared-memory access by this thread waits behind the operand reads of the MMAs
+        // it has issued (the tensor pipe idles meanwhile), so it makes one barrier wait
+        // per K-part and keeps its give-up state in a register; a wait given up elsewhere
+        // stops the arrivals, and its own bounded waits then end.
         if (lane == 0) {
-            wait_or_abort(sh, &sh.mb_b, 0);
+            bool ok = tc::mbar_wait(&sh.mb_b, 0);
             tc::fence_after_sync();
             constexpr uint32_t idesc = tc::idesc_bf16(128, N, 1, 1);
             uint32_t n = 0;
-            for (int pr = 0; pr < npairs && !sh.abort; ++pr) {
+            for (int pr = 0; pr < npairs && ok; ++pr) {
                 const int ab = pr & 1;
                 const uint32_t acc = tmem + (uint32_t)(ab * N);
-                if (pr >= 2) wait_or_abort(sh, &sh.acc_empty[ab], ((pr - 2) >> 1) & 1);
-                for (int kp = 0; kp < nparts; ++kp, ++n) {
+                if (pr >= 2) ok = tc::mbar_wait(&sh.acc_empty[ab], ((pr - 2) >> 1) & 1);
+                for (int kp = 0; kp < nparts && ok; ++kp, ++n) {
                     const uint32_t xb = n & 1;
-                    wait_or_abort(sh, &sh.xt_full[xb], (n >> 1) & 1);
+                    ok = tc::mbar_wait(&sh.xt_full[xb], (n >> 1) & 1);
                     tc::fence_after_sync();
-                    if (sh.abort) break;
+                    if (!ok) break;
                     const uint32_t ah = tc::smem_u32(sXt + xb * 2 * Cfg::kXt);
                     // Xw^T: MN-major no-swizzle, M = 128 contiguous in 16-byte rows; K steps
                     // of 16 rows are two core-matrix rows (2 * 16 * 128 bytes) apart
@@ -191,8 +195,10 @@ __global__ void __launch_bounds__(kCta, 1)
                     }
                     tc::mma_commit(&sh.xt_empty[xb]);
                 }
+                if (!ok) break;
                 tc::mma_commit(&sh.acc_full[ab]);
             }
+            if (!ok) sh.abort = 1;
         }
     } else {
         // ---- compute warps (256 threads)
