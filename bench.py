@@ -79,7 +79,31 @@ def parse():
                     help="time single-token recurrent steps (ssm_step) at the workload's widths")
     ap.add_argument("--decode-batch", type=int, default=0,
                     help="sequences decoded per step (0: enough for a 256 MB carried state)")
+    ap.add_argument("--tune", action="append", default=[], metavar="KNOB=VALUE",
+                    help="plan override through ssm_tuning_set, e.g. DIAG_EXP_POLY=1 "
+                         "(SSM_TUNE_<KNOB>; recorded in the line's config)")
     return ap.parse_args()
+
+
+TUNING: dict = {}
+
+
+def emit(line: dict) -> None:
+    """Print one JSON result line; plan overrides in force go into its config."""
+    if TUNING and isinstance(line.get("config"), dict):
+        line["config"]["tuning"] = dict(TUNING)
+    print(json.dumps(line), flush=True)
+
+
+def apply_tuning(specs) -> None:
+    from selective_state_space_143_b300 import _lib
+    for spec in specs:
+        name, _, value = spec.partition("=")
+        knob = getattr(_lib, "SSM_TUNE_" + name.strip().upper(), None)
+        if knob is None or not value.strip().lstrip("-").isdigit():
+            raise SystemExit(f"--tune {spec}: expected KNOB=VALUE with KNOB one of the SSM_TUNE_* names")
+        _lib.tuning_set(knob, int(value))
+        TUNING["SSM_TUNE_" + name.strip().upper()] = int(value)
 
 
 # ---------------------------------------------------------------------------- helpers
@@ -477,7 +501,7 @@ def run_reference(args, w):
                          "sample": f"{per_step} whole channels x L {w.seqlen} per step"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
-    print(json.dumps(line), flush=True)
+    emit(line)
     barrier(dist)
     return 0
 
@@ -663,7 +687,7 @@ def run_ours(args, w):
         }
         if configs is not None:
             line["configs"] = configs
-        print(json.dumps(line), flush=True)
+        emit(line)
     if dist is not None:
         dist.destroy_process_group()
     return 0
@@ -813,7 +837,7 @@ def run_decode(args, w0):
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
             "gpu_launches": int(launches),
         }
-        print(json.dumps(line), flush=True)
+        emit(line)
     if dist is not None:
         dist.destroy_process_group()
     return 0
@@ -974,7 +998,7 @@ def run_backward(args, w):
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
             "gpu_launches": int(launches),
         }
-        print(json.dumps(line), flush=True)
+        emit(line)
     if dist is not None:
         dist.destroy_process_group()
     return 0
@@ -993,6 +1017,7 @@ def main():
         w = w.replace(seqlen=args.seqlen)
     if args.impl == "reference":
         return run_reference(args, w)
+    apply_tuning(args.tune)
     if args.decode:
         return run_decode(args, w)
     if args.backward:

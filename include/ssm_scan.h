@@ -361,7 +361,7 @@ int ssm_selftest_bounded_wait(uint32_t max_checks, ssm_stream_t stream);
 /*
  * Plan overrides for measurement sweeps (this has no counterpart in the pages: it
  * selects among the library's own kernel schedules; results agree within rounding for
- * every setting).  Process-wide, thread-safe; 0 restores the library's own choice.
+ * every setting, within the stated error for SSM_TUNE_DIAG_EXP_POLY).  Process-wide, thread-safe; 0 restores the library's own choice.
  * A setting changes the scratch size that the *_workspace_size queries report, so query
  * after setting it.  Values out of a knob's range are ignored by the planner.
  *   SSM_TUNE_DIAG_NPT       state entries per lane of the diagonal scan: 4 or 8
@@ -369,6 +369,10 @@ int ssm_selftest_bounded_wait(uint32_t max_checks, ssm_stream_t stream);
  *                           tensor-core ones)
  *   SSM_TUNE_BWD_PARTS      time parts of the backward pass, 1..16
  *   SSM_TUNE_BWD_LPC        lanes per channel of the backward pass: 4, 8, 16 or 32
+ *   SSM_TUNE_DIAG_EXP_POLY  diagonal scan, bf16 with dstate <= 16 and no convolution: of
+ *                           each 4 state entries per step, the decays of 1 or 2 pairs from
+ *                           a polynomial exp2 on the FMA pipe instead of the SFU (results
+ *                           agree within the polynomial's 2.5e-7 relative error)
  * ssm_tuning_set returns SSM_ERR_UNSUPPORTED for an unknown knob and SSM_ERR_SHAPE for a
  * negative value; ssm_tuning_get returns the current setting (0 for an unknown knob).
  */
@@ -376,7 +380,8 @@ typedef enum {
     SSM_TUNE_DIAG_NPT = 0,
     SSM_TUNE_SSD_CUDA_CORES = 1,
     SSM_TUNE_BWD_PARTS = 2,
-    SSM_TUNE_BWD_LPC = 3
+    SSM_TUNE_BWD_LPC = 3,
+    SSM_TUNE_DIAG_EXP_POLY = 4
 } ssm_tuning_knob;
 int ssm_tuning_set(int knob, int64_t value);
 int64_t ssm_tuning_get(int knob);

@@ -40,6 +40,7 @@ SSM_TUNE_DIAG_NPT = 0
 SSM_TUNE_SSD_CUDA_CORES = 1
 SSM_TUNE_BWD_PARTS = 2
 SSM_TUNE_BWD_LPC = 3
+SSM_TUNE_DIAG_EXP_POLY = 4
 
 
 class ssm_shape(ctypes.Structure):

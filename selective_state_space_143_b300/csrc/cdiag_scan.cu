@@ -366,7 +366,7 @@ cudaError_t claunch_one(const CDiagArgs& ka, dim3 grid, cudaStream_t stream) {
     auto kern = cdiag_scan_kernel<T, NK, STATE_ONLY, GATE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
     if (e != cudaSuccess) return e;
-    cudaEvent_t t0 = timing_begin(stream);
+    cudaEvent_t t0 = timing_begin(stream, STATE_ONLY ? "cdiag_scan_kernel (segment state pass)" : "cdiag_scan_kernel (output pass)");
     kern<<<grid, kCThreads, Cfg::kSmem, stream>>>(ka);
     note_launch(STATE_ONLY ? "cdiag_scan_kernel (segment state pass)" : "cdiag_scan_kernel (output pass)", stream, t0);
     return cudaGetLastError();

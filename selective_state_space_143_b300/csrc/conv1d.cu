@@ -211,7 +211,7 @@ cudaError_t conv_prepass_launch(const ScanArgs& a, void* xc, bool split, cudaStr
     const dim3 grid((unsigned)((nvec + kConvVX - 1) / kConvVX), (unsigned)std::min<int64_t>(tblocks, 65535),
                     (unsigned)c.batch);
     const dim3 block(kConvVX, kConvTY);
-    cudaEvent_t t0 = timing_begin(stream);
+    cudaEvent_t t0 = timing_begin(stream, "conv_silu_kernel");
     if (a.dtype == 1) {
         if (split)
             conv_silu_kernel<__nv_bfloat16, true><<<grid, block, 0, stream>>>(c);
@@ -233,7 +233,7 @@ cudaError_t conv_tail_launch(const ScanArgs& a, cudaStream_t stream) {
     const int64_t total = c.batch * (c.K - 1) * c.ch;
     if (!a.x_last || total == 0) return cudaSuccess;
     const unsigned blocks = (unsigned)((total + kConvThreads - 1) / kConvThreads);
-    cudaEvent_t t0 = timing_begin(stream);
+    cudaEvent_t t0 = timing_begin(stream, "conv_tail_kernel");
     if (a.dtype == 1)
         conv_tail_kernel<__nv_bfloat16><<<blocks, kConvThreads, 0, stream>>>(c);
     else

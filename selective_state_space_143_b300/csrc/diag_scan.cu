@@ -39,6 +39,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <type_traits>
 
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
@@ -160,6 +161,33 @@ __device__ __forceinline__ float2 silu_pair(float2 z) {
     return silu2_fma(z);
 }
 
+// 2^x for x <= 0 on the FMA pipe, two values at a time (the alternative to the SFU's
+// ex2 that the SSM_TUNE_DIAG_EXP_POLY plan override selects): x is clamped at -126 (below
+// it the decay is zero to fp32 precision), n = rint(x) by adding 1.5 * 2^23 (the integer
+// lands in the low mantissa bits), f = x - n in [-1/2, 1/2], 2^f by a degree-5
+// polynomial and 2^n written directly as the exponent field.  The coefficients are the
+// relative-error minimax fit of fit_exp2.py (Lawson's iteration on Chebyshev nodes); the
+// fp32 evaluation stays within 2.5e-7 of 2^f.
+__device__ __forceinline__ float2 exp2_fma2(float2 x) {
+    constexpr float kC0 = 1.000000119e+00f, kC1 = 6.931469440e-01f, kC2 = 2.402212024e-01f;
+    constexpr float kC3 = 5.550713092e-02f, kC4 = 9.675540961e-03f, kC5 = 1.327647129e-03f;
+    constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+    x = make_float2(fmaxf(x.x, -126.0f), fmaxf(x.y, -126.0f));
+    const float2 t = __fadd2_rn(x, make_float2(kRound, kRound));
+    const float2 r = __fadd2_rn(t, make_float2(-kRound, -kRound));  // rint(x), exact
+    const float2 f = __ffma2_rn(r, make_float2(-1.0f, -1.0f), x);   // x - rint(x), exact
+    float2 p = __ffma2_rn(make_float2(kC5, kC5), f, make_float2(kC4, kC4));
+    p = __ffma2_rn(p, f, make_float2(kC3, kC3));
+    p = __ffma2_rn(p, f, make_float2(kC2, kC2));
+    p = __ffma2_rn(p, f, make_float2(kC1, kC1));
+    p = __ffma2_rn(p, f, make_float2(kC0, kC0));
+    // the bits of t are those of 1.5 * 2^23 plus n: shifted left by 23 only n survives,
+    // and adding 127 << 23 gives the exponent field of 2^n (n >= -126: a normal number)
+    const float2 s2 = make_float2(__int_as_float(__float_as_int(t.x) * 8388608 + 0x3F800000),
+                                  __int_as_float(__float_as_int(t.y) * 8388608 + 0x3F800000));
+    return __fmul2_rn(p, s2);
+}
+
 // STATE_ONLY: compute each segment's local end state from zero (segments 0..nseg-2).
 // Otherwise: full output pass over every segment with the folded initial state.
 //
@@ -179,7 +207,10 @@ __device__ __forceinline__ float2 silu_pair(float2 z) {
 // formed in prep from the staged rows of this tile and the three rows before it (the
 // previous tile's stage, or a halo loaded once per segment); the epilogue reads x' for
 // the skip term from a ring of three tile buffers.
-template <typename T, int NK, int LPC, int WARPS, bool STATE_ONLY, bool GATE, bool CONV>
+//
+// PX: of each group of 4 state entries per step, the decays of PX pairs come from
+// exp2_fma2 (FMA pipe) and the rest from the SFU's ex2 (0: all SFU, the default).
+template <typename T, int NK, int LPC, int WARPS, bool STATE_ONLY, bool GATE, bool CONV, int PX = 0>
 __global__ void __launch_bounds__(32 * WARPS) diag_scan_kernel(const DiagKernelArgs a) {
     using Cfg = DiagCfg<T, NK, LPC, WARPS, CONV>;
     constexpr int NT = Cfg::NT, CPB = Cfg::CPB, NPT = Cfg::NPT, P2 = Cfg::P2, E = Cfg::kElem;
@@ -445,8 +476,8 @@ __global__ void __launch_bounds__(32 * WARPS) diag_scan_kernel(const DiagKernelA
                     const float4 bq = *reinterpret_cast<const float4*>(&Bf[(rb + i) * NK + g * NPT + 2 * kk]);
                     const float2 dA0 = __fmul2_rn(dd, A2[kk]);
                     const float2 dA1 = __fmul2_rn(dd, A2[kk + 1]);
-                    av[i][kk] = make_float2(ex2(dA0.x), ex2(dA0.y));
-                    av[i][kk + 1] = make_float2(ex2(dA1.x), ex2(dA1.y));
+                    av[i][kk] = PX >= 2 ? exp2_fma2(dA0) : make_float2(ex2(dA0.x), ex2(dA0.y));
+                    av[i][kk + 1] = PX >= 1 ? exp2_fma2(dA1) : make_float2(ex2(dA1.x), ex2(dA1.y));
                     ub[i][kk] = __fmul2_rn(uu, make_float2(bq.x, bq.y));
                     ub[i][kk + 1] = __fmul2_rn(uu, make_float2(bq.z, bq.w));
                 }
@@ -542,6 +573,7 @@ __global__ void __launch_bounds__(32 * WARPS) diag_scan_kernel(const DiagKernelA
 struct Plan {
     int NK;
     int LPC;
+    int px;  // SSM_TUNE_DIAG_EXP_POLY (bf16, dstate <= 16, no convolution): 0, 1 or 2
     int warps;
     int cpb;
     int64_t seg_len;
@@ -567,6 +599,8 @@ int npt_override() {
 Plan make_plan(const ScanArgs& a) {
     Plan p;
     p.NK = pick_nk(a.dstate);
+    const int64_t px = tuning(4);
+    p.px = px == 1 || px == 2 ? (int)px : 0;
     const int64_t smsp = (int64_t)sm_count() * 4;  // SM sub-partitions
     auto fill = [&](int npt) {
         p.LPC = std::max(1, std::min(8, p.NK / npt));
@@ -599,11 +633,11 @@ Plan make_plan(const ScanArgs& a) {
     return p;
 }
 
-template <typename T, int NK, int LPC, bool STATE_ONLY, bool GATE, bool CONV>
+template <typename T, int NK, int LPC, bool STATE_ONLY, bool GATE, bool CONV, int PX>
 cudaError_t launch_one(const DiagKernelArgs& ka, dim3 grid, cudaStream_t stream) {
     constexpr int WARPS = (LPC == 1 ? 32 : 16) * LPC / 32;
     using Cfg = DiagCfg<T, NK, LPC, WARPS, CONV>;
-    auto kern = diag_scan_kernel<T, NK, LPC, WARPS, STATE_ONLY, GATE, CONV>;
+    auto kern = diag_scan_kernel<T, NK, LPC, WARPS, STATE_ONLY, GATE, CONV, PX>;
     // the shared-memory attribute is set once per instantiation and device
     static std::atomic<uint64_t> attr_done{0};
     int dev = 0;
@@ -615,7 +649,7 @@ cudaError_t launch_one(const DiagKernelArgs& ka, dim3 grid, cudaStream_t stream)
         if (e != cudaSuccess) return e;
         attr_done.fetch_or(bit, std::memory_order_relaxed);
     }
-    cudaEvent_t t0 = timing_begin(stream);
+    cudaEvent_t t0 = timing_begin(stream, STATE_ONLY ? "diag_scan_kernel (segment state pass)" : "diag_scan_kernel (output pass)");
     if (!STATE_ONLY && ka.nsub_launched) {
         // after a state-only pass: programmatic dependent launch (see the kernel)
         cudaLaunchAttribute attr;
@@ -629,7 +663,10 @@ cudaError_t launch_one(const DiagKernelArgs& ka, dim3 grid, cudaStream_t stream)
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
         e = cudaLaunchKernelEx(&cfg, kern, ka);
-        if (e != cudaSuccess) return e;
+        if (e != cudaSuccess) {
+            launch_failed(t0);
+            return e;
+        }
     } else {
         kern<<<grid, Cfg::NT, Cfg::kSmemBytes, stream>>>(ka);
     }
@@ -637,7 +674,7 @@ cudaError_t launch_one(const DiagKernelArgs& ka, dim3 grid, cudaStream_t stream)
     return cudaGetLastError();
 }
 
-template <typename T, int NK, int LPC, bool CONV>
+template <typename T, int NK, int LPC, bool CONV, int PX = 0>
 cudaError_t launch_typed(const ScanArgs& a, const Plan& p, void* ws, cudaStream_t stream) {
     DiagKernelArgs ka;
     ka.x = (const char*)a.x;
@@ -684,21 +721,31 @@ cudaError_t launch_typed(const ScanArgs& a, const Plan& p, void* ws, cudaStream_
         ka.segh_s = span_of(ka.seg_h, hbytes);
         ka.segd_s = span_of(ka.seg_dsum, dbytes);
         const dim3 g1(p.blocks_x, p.nseg - 1, (unsigned)a.batch);
-        cudaError_t e = CONV ? launch_one<T, NK, LPC, true, false, true>(ka, g1, stream)
-                             : launch_one<T, NK, LPC, true, false, false>(ka, g1, stream);
+        cudaError_t e = CONV ? launch_one<T, NK, LPC, true, false, true, PX>(ka, g1, stream)
+                             : launch_one<T, NK, LPC, true, false, false, PX>(ka, g1, stream);
         if (e != cudaSuccess) return e;
         ka.nsub_launched = 1;
     }
     const dim3 g2(p.blocks_x, p.nseg, (unsigned)a.batch);
-    if (a.z) return launch_one<T, NK, LPC, false, true, CONV>(ka, g2, stream);
-    return launch_one<T, NK, LPC, false, false, CONV>(ka, g2, stream);
+    if (a.z) return launch_one<T, NK, LPC, false, true, CONV, PX>(ka, g2, stream);
+    return launch_one<T, NK, LPC, false, false, CONV, PX>(ka, g2, stream);
 }
 
 template <typename T, bool CONV>
 cudaError_t launch_conv(const ScanArgs& a, const Plan& p, void* ws, cudaStream_t stream) {
     switch (p.NK) {
         case 8: return p.LPC == 1 ? launch_typed<T, 8, 1, CONV>(a, p, ws, stream) : launch_typed<T, 8, 2, CONV>(a, p, ws, stream);
-        case 16: return p.LPC == 2 ? launch_typed<T, 16, 2, CONV>(a, p, ws, stream) : launch_typed<T, 16, 4, CONV>(a, p, ws, stream);
+        case 16:
+            // the FMA-pipe exponential variants exist for bf16 without the convolution
+            if constexpr (std::is_same<T, __nv_bfloat16>::value && !CONV) {
+                if (p.px == 1)
+                    return p.LPC == 2 ? launch_typed<T, 16, 2, CONV, 1>(a, p, ws, stream)
+                                      : launch_typed<T, 16, 4, CONV, 1>(a, p, ws, stream);
+                if (p.px == 2)
+                    return p.LPC == 2 ? launch_typed<T, 16, 2, CONV, 2>(a, p, ws, stream)
+                                      : launch_typed<T, 16, 4, CONV, 2>(a, p, ws, stream);
+            }
+            return p.LPC == 2 ? launch_typed<T, 16, 2, CONV>(a, p, ws, stream) : launch_typed<T, 16, 4, CONV>(a, p, ws, stream);
         case 32: return p.LPC == 4 ? launch_typed<T, 32, 4, CONV>(a, p, ws, stream) : launch_typed<T, 32, 8, CONV>(a, p, ws, stream);
         default: return launch_typed<T, 64, 8, CONV>(a, p, ws, stream);
     }

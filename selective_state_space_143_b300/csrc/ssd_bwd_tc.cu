@@ -813,7 +813,7 @@ cudaError_t launch_chunk(const BwdTcArgs& k, const ScanArgs& f, const BwdTcPlan&
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
     if (e != cudaSuccess) return e;
     const int hpc = bwd_heads_per_cta(f, pl.nchunks);
-    cudaEvent_t t0 = timing_begin(stream);
+    cudaEvent_t t0 = timing_begin(stream, "ssd_bwd_chunk_tc");
     kern<<<dim3((unsigned)pl.nchunks, (unsigned)(f.nheads / hpc), (unsigned)f.batch), 256, smem_bytes, stream>>>(
         k, hpc, status, tc_, tb_, tx_, tdh, tdl);
     note_launch("ssd_bwd_chunk_tc", stream, t0);
@@ -904,7 +904,7 @@ cudaError_t ssd_bwd_tc_launch(const ScanBwdArgs& s, void* ws, cudaStream_t strea
         d.dyl_s = span_of(dyl, el * 2);
         d.dz_s = span_of(s.dz, el * 4);
         const dim3 grid((unsigned)((H * P / 8 + 255) / 256), (unsigned)((T + kDyRows - 1) / kDyRows), (unsigned)b);
-        cudaEvent_t t0 = timing_begin(stream);
+        cudaEvent_t t0 = timing_begin(stream, "ssd_bwd_dy");
         ssd_bwd_dy<<<grid, 256, 0, stream>>>(d);
         note_launch("ssd_bwd_dy", stream, t0);
         e = cudaGetLastError();
@@ -936,7 +936,7 @@ cudaError_t ssd_bwd_tc_launch(const ScanBwdArgs& s, void* ws, cudaStream_t strea
         rv.ast_s = span_of(ast, stb);
         rv.dinit_s = span_of(s.dinit, (size_t)b * H * P * N * sizeof(float));
         const dim3 grid((unsigned)((P * N / 8 + 255) / 256), (unsigned)H, (unsigned)b);
-        cudaEvent_t t0 = timing_begin(stream);
+        cudaEvent_t t0 = timing_begin(stream, "ssd_bwd_reverse_carry");
         ssd_bwd_reverse_carry<<<grid, 256, 0, stream>>>(rv);
         note_launch("ssd_bwd_reverse_carry", stream, t0);
         e = cudaGetLastError();

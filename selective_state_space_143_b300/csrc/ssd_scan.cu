@@ -501,7 +501,7 @@ cudaError_t ssd_launch_typed(const ScanArgs& a, void* ws, cudaStream_t stream) {
         t.states_s = s.states_s;
         cudaError_t e = ssd_tc_chunk_state(t, a.batch, stream);
         if (e != cudaSuccess) return e;
-        cudaEvent_t t0 = timing_begin(stream);
+        cudaEvent_t t0 = timing_begin(stream, "ssd_state_pass_split");
         ssd_state_pass_split<<<dim3((unsigned)((a.headdim * a.dstate / 8 + kThreads - 1) / kThreads), (unsigned)a.nheads, (unsigned)a.batch), kThreads, 0, stream>>>(s);
         note_launch("ssd_state_pass_split", stream, t0);
         e = cudaGetLastError();
@@ -509,12 +509,12 @@ cudaError_t ssd_launch_typed(const ScanArgs& a, void* ws, cudaStream_t stream) {
         return ssd_tc_chunk_scan(t, a.batch, a.z != nullptr, stream);
     }
     if (pl.nchunks > 0) {
-        cudaEvent_t t0 = timing_begin(stream);
+        cudaEvent_t t0 = timing_begin(stream, "ssd_chunk_state");
         ssd_chunk_state<T><<<dim3((unsigned)pl.nchunks, (unsigned)a.nheads * nP * nN, (unsigned)a.batch), kThreads, 0, stream>>>(s);
         note_launch("ssd_chunk_state", stream, t0);
     }
     {
-        cudaEvent_t t0 = timing_begin(stream);
+        cudaEvent_t t0 = timing_begin(stream, "ssd_state_pass");
         ssd_state_pass<<<dim3((unsigned)((a.headdim * a.dstate / 4 + kThreads - 1) / kThreads), (unsigned)a.nheads, (unsigned)a.batch), kThreads, 0, stream>>>(s);
         note_launch("ssd_state_pass", stream, t0);
     }
@@ -522,7 +522,7 @@ cudaError_t ssd_launch_typed(const ScanArgs& a, void* ws, cudaStream_t stream) {
         const size_t smem = sizeof(float) * (2 * pl.Q + kTile * (a.dstate + 1) + kSub * (a.dstate + 1) +
                                              kSub * (kTile + 1) + kTile * (kSub + 1));
         const dim3 grid((unsigned)pl.nchunks, (unsigned)a.nheads * nP, (unsigned)a.batch * nTq);
-        cudaEvent_t t0 = timing_begin(stream);
+        cudaEvent_t t0 = timing_begin(stream, "ssd_chunk_scan");
         if (a.z) {
             cudaFuncSetAttribute(ssd_chunk_scan<T, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             ssd_chunk_scan<T, true><<<grid, kThreads, smem, stream>>>(s);
@@ -558,7 +558,7 @@ cudaError_t ssd_tc_forward_carry(const ScanArgs& a, int64_t Q, int64_t nchunks, 
     }
     s.final_s = span_of(final_state, (size_t)a.batch * a.nheads * a.headdim * a.dstate * sizeof(float));
     s.states_s = span_of(states, (size_t)a.batch * nchunks * a.nheads * a.headdim * a.dstate * sizeof(float));
-    cudaEvent_t t0 = timing_begin(stream);
+    cudaEvent_t t0 = timing_begin(stream, "ssd_state_pass_split");
     ssd_state_pass_split<<<dim3((unsigned)((a.headdim * a.dstate / 8 + kThreads - 1) / kThreads), (unsigned)a.nheads,
                                 (unsigned)a.batch),
                            kThreads, 0, stream>>>(s);

@@ -544,7 +544,7 @@ cudaError_t launch_scan(const SsdTcArgs& s, int64_t batch, cudaStream_t stream) 
     if (e != cudaSuccess) return e;
     const int hpc = scan_heads_per_cta(s, batch);
     const dim3 grid((unsigned)(s.nchunks * (s.Q / 128)), (unsigned)(s.H / hpc), (unsigned)batch);
-    cudaEvent_t t0 = timing_begin(stream);
+    cudaEvent_t t0 = timing_begin(stream, "ssd_scan_tc");
     kern<<<grid, kCtaThreads, Cfg::kSmemTotal, stream>>>(s, hpc, status, tx, txl, tmc, tmb, tmo);
     note_launch("ssd_scan_tc", stream, t0);
     return cudaGetLastError();

@@ -407,7 +407,7 @@ cudaError_t launch_state(const SsdTcArgs& s, int64_t batch, cudaStream_t stream)
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmemTotal);
     if (e != cudaSuccess) return e;
     const int hpc = state_heads_per_cta(s);
-    cudaEvent_t t0 = timing_begin(stream);
+    cudaEvent_t t0 = timing_begin(stream, ADJ ? "ssd_state_tc (adjoint)" : "ssd_state_tc");
     kern<<<dim3((unsigned)s.nchunks, (unsigned)(s.H / hpc), (unsigned)batch), kCta, Cfg::kSmemTotal, stream>>>(
         s, hpc, status, tx, txl, tb);
     note_launch(ADJ ? "ssd_state_tc (adjoint)" : "ssd_state_tc", stream, t0);

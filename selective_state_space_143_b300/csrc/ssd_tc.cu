@@ -100,14 +100,14 @@ cudaError_t device_status_address(int** p) {
 }
 
 cudaError_t bounds_selftest_launch(float* buf, size_t bytes, int64_t index, cudaStream_t stream) {
-    cudaEvent_t t0 = timing_begin(stream);
+    cudaEvent_t t0 = timing_begin(stream, "bounds_selftest");
     bounds_selftest<<<1, 1, 0, stream>>>(buf, span_of(buf, bytes), index);
     note_launch("bounds_selftest", stream, t0);
     return cudaGetLastError();
 }
 
 cudaError_t bounded_wait_selftest_launch(uint32_t max_checks, cudaStream_t stream) {
-    cudaEvent_t t0 = timing_begin(stream);
+    cudaEvent_t t0 = timing_begin(stream, "bounded_wait_selftest");
     bounded_wait_selftest<<<1, 32, 0, stream>>>(max_checks);
     note_launch("bounded_wait_selftest", stream, t0);
     return cudaGetLastError();

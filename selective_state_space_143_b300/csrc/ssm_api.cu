@@ -1,6 +1,7 @@
 // C-ABI entry points of libssmscan.so: argument checks, workspace, dispatch.
 // The operation and the argument contract are stated in include/ssm_scan.h.
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <atomic>
 #include <cstdint>
@@ -46,7 +47,8 @@ cudaEvent_t take_event() {
 }
 }  // namespace
 
-cudaEvent_t timing_begin(cudaStream_t stream) {
+cudaEvent_t timing_begin(cudaStream_t stream, const char* name) {
+    nvtxRangePushA(name);
     if (!g_timing.load(std::memory_order_relaxed)) return nullptr;
     cudaEvent_t e = take_event();
     if (e && cudaEventRecord(e, stream) != cudaSuccess) {
@@ -56,7 +58,15 @@ cudaEvent_t timing_begin(cudaStream_t stream) {
     return e;
 }
 
+void launch_failed(cudaEvent_t start) {
+    nvtxRangePop();
+    if (!start) return;
+    std::lock_guard<std::mutex> lock(g_timing_mutex);
+    g_event_pool.push_back(start);
+}
+
 void note_launch(const char* name, cudaStream_t stream, cudaEvent_t start) {
+    nvtxRangePop();
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (!start) return;
     cudaEvent_t end = take_event();
@@ -70,7 +80,7 @@ void note_launch(const char* name, cudaStream_t stream, cudaEvent_t start) {
 
 // Plan overrides (ssm_tuning_set), one slot per ssm_tuning_knob.
 namespace {
-constexpr int kKnobs = 4;
+constexpr int kKnobs = 5;
 std::atomic<int64_t> g_tuning[kKnobs] = {};
 std::atomic<int> g_alloc_failures{0};
 constexpr int kMaxDevices = 64;

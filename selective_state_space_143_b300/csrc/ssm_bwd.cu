@@ -548,13 +548,13 @@ cudaError_t launch_bwd(const BwdArgs<T>& a, int parts, int64_t batch, cudaStream
     if (parts > 1) {
         constexpr size_t kSmemParts = sizeof(float) * 2 * kSeg * LPC * R;  // B and C rows of a segment
         static_assert(kSmemParts <= 48 * 1024, "part-summary rows");
-        cudaEvent_t t1 = timing_begin(stream);
+        cudaEvent_t t1 = timing_begin(stream, "scan_bwd_kernel (part summaries)");
         scan_bwd_kernel<T, LPC, R, kSeg, SSD, true><<<grid, kBwdThreads, kSmemParts, stream>>>(k);
         note_launch("scan_bwd_kernel (part summaries)", stream, t1);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    cudaEvent_t t0 = timing_begin(stream);
+    cudaEvent_t t0 = timing_begin(stream, "scan_bwd_kernel");
     kern<<<grid, kBwdThreads, kSmem, stream>>>(k);
     note_launch("scan_bwd_kernel", stream, t0);
     return cudaGetLastError();

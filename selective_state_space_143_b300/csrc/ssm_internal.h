@@ -35,12 +35,16 @@ struct ScanArgs {
 };
 
 // Launch bookkeeping.  Around every kernel launch:
-//   cudaEvent_t t0 = timing_begin(stream);  kernel<<<...>>>(...);  note_launch("name", stream, t0);
-// note_launch counts the launch; when timing is enabled (ssm_timing_enable) timing_begin
-// records an event before the launch and note_launch one after it, on the same stream,
-// for ssm_timing_collect.
-cudaEvent_t timing_begin(cudaStream_t stream);
+//   cudaEvent_t t0 = timing_begin(stream, "name");  kernel<<<...>>>(...);  note_launch("name", stream, t0);
+// timing_begin opens an NVTX range named after the kernel on the calling thread (so a
+// profiler can select a launch by range, e.g. ncu --nvtx --nvtx-include "ssd_scan_tc/")
+// and note_launch closes it; a launcher that gives up between the two calls
+// launch_failed instead.  note_launch counts the launch; when timing is enabled
+// (ssm_timing_enable) timing_begin records an event before the launch and note_launch one
+// after it, on the same stream, for ssm_timing_collect.
+cudaEvent_t timing_begin(cudaStream_t stream, const char* name);
 void note_launch(const char* name, cudaStream_t stream, cudaEvent_t start);
+void launch_failed(cudaEvent_t start);
 
 // Diagonal (Mamba-1) path.
 size_t diag_workspace_bytes(const ScanArgs& a);

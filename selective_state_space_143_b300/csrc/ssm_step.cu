@@ -212,7 +212,7 @@ cudaError_t step_launch(const ScanArgs& a, bool diag_a, float* state, cudaStream
     s.out_s = span_of(a.out, (size_t)nch * E);
     s.xlast_s = span_of(a.x_last, (size_t)a.batch * (a.conv_k > 1 ? a.conv_k - 1 : 0) * a.nheads * a.headdim * E);
     if (nch == 0) return cudaSuccess;
-    cudaEvent_t t0 = timing_begin(stream);
+    cudaEvent_t t0 = timing_begin(stream, "ssm_step_kernel");
     if (a.dtype == 1)
         launch_typed<__nv_bfloat16>(s, nch, stream);
     else

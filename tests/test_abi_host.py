@@ -374,6 +374,14 @@ def test_tuning_knobs():
     with _lib.tuned(_lib.SSM_TUNE_SSD_CUDA_CORES, 1):
         rec_ws = lib.ssm_scan_bwd_workspace_size(ctypes.byref(t))
     assert tc_ws != rec_ws and lib.ssm_scan_bwd_workspace_size(ctypes.byref(t)) == tc_ws
+    # the FMA-pipe exponential knob exists, round-trips, and leaves the scratch size alone
+    d = _shape(mode=0, dtype=1, nheads=512, headdim=1, dstate=16, batch=8, seqlen=1024)
+    diag_ws = _ws(d)
+    for px in (1, 2):
+        with _lib.tuned(_lib.SSM_TUNE_DIAG_EXP_POLY, px):
+            assert _lib.tuning_get(_lib.SSM_TUNE_DIAG_EXP_POLY) == px
+            assert _ws(d) == diag_ws
+    assert _lib.tuning_get(_lib.SSM_TUNE_DIAG_EXP_POLY) == 0
 
 
 def test_complex_mode_shapes_and_unsupported_entry_points():

@@ -11,6 +11,7 @@ import torch
 
 import oracle
 import selective_state_space_143_b300 as ssm
+from selective_state_space_143_b300 import _lib
 from selective_state_space_143_b300.inputs import WORKLOADS, make_inputs, random_inputs
 
 pytestmark = pytest.mark.gpu
@@ -63,6 +64,19 @@ def test_workload_full(name):
     y, fs = run_gpu(inp, w)
     err, err_fs = compare(w, inp, y, fs)
     print(f"{name}: out {err:.3e} final_state {err_fs:.3e}")
+
+
+@pytest.mark.parametrize("px", [1, 2])
+@pytest.mark.parametrize("shape", [dict(batch=8, seqlen=1024, nheads=512), dict(batch=4, seqlen=512, nheads=5120)],
+                         ids=["c1-shape", "c2-widths"])
+def test_diag_fma_pipe_exp2(px, shape):
+    """SSM_TUNE_DIAG_EXP_POLY: 1 or 2 of every 2 decay pairs from the FMA-pipe polynomial
+    exp2 (both lane layouts: 4 entries per lane with time segments, and 8 per lane)."""
+    w, inp = random_inputs("diag", "bf16", headdim=1, dstate=16, seed=17, **shape)
+    with _lib.tuned(_lib.SSM_TUNE_DIAG_EXP_POLY, px):
+        y, fs = run_gpu(inp, w, chunk=0)
+    err, err_fs = compare(w, inp, y, fs)
+    print(f"px {px}: out {err:.3e} final_state {err_fs:.3e}")
 
 
 @pytest.mark.parametrize("name", ["c2", "c3", "c4"])
