@@ -180,6 +180,16 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
     tc::fence_after_sync();
     const uint32_t tmem = sh.tmem;
     const uint32_t tG = tmem;
+    // TMEM columns: G = C B^T in [0, SW), and two sets of {Y_diag, Y_off} at 256 + 128 *
+    // set.  At dstate 256 a first half (SW = 128) uses its 128 spare columns instead:
+    // Y_diag sets at 128 + 64 * set, and Y_off sets of 128 columns at 256 + 128 * set
+    // holding C h_hi and C h_lo side by side from one N = 128 MMA over the stacked
+    // [h_hi; h_lo] tile (half the MMAs and C reads of two N = 64 products; c4 scan
+    // 1005 -> 899 us).  At dstate 128 the extra epilogue load costs more than the 8
+    // MMAs it saves (c3 scan 348 -> 354 us), so those keep the narrow layout.
+    const bool wide_off = N > 128 && SW == 128;
+    auto t_yd = [&](int set) { return wide_off ? tmem + 128 + 64 * set : tmem + 256 + 128 * set; };
+    auto t_yo = [&](int set) { return wide_off ? tmem + 256 + 128 * set : tmem + 256 + 128 * set + 64; };
 
     // Buffer schedule: x buffer and its use count for head hi (serial planes: buffer 0 every
     // head); h set likewise.
@@ -244,10 +254,11 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
             }
             constexpr uint32_t id_diag = tc::idesc_bf16(128, kP, 0, 1);
             constexpr uint32_t id_off = tc::idesc_bf16(128, kP, 0, 0);
+            constexpr uint32_t id_off_wide = tc::idesc_bf16(128, 2 * kP, 0, 0);
             uint32_t n = 0;  // M' parts consumed so far
             for (int hi = 0; hi < nh && ok; ++hi) {
                 const int ab = hi & 1;
-                const uint32_t tYd = tmem + 256 + 128 * ab, tYo = tYd + 64;
+                const uint32_t tYd = t_yd(ab), tYo = t_yo(ab);
                 if (hi >= 2) ok = tc::mbar_wait(&sh.acc_empty[ab], ((hi - 2) >> 1) & 1);  // head hi-2's epilogue read them
                 ok = ok && tc::mbar_wait(&sh.h_full[hbuf(hi)], huse(hi) & 1);
                 tc::fence_after_sync();
@@ -258,13 +269,23 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
                     // this head's first part
                     const uint32_t cb = tc::smem_u32(sC);
                     const uint32_t hs = tc::smem_u32(sH + hbuf(hi) * 2 * Cfg::kH);
+                    // the lo tile continues the hi tile's 8-row groups (kH = 8 group strides),
+                    // so one descriptor spans both as 128 rows
                     const uint64_t dhh = tc::desc_strided(hs, 128, (N / 8) * 128);
                     const uint64_t dhl = tc::desc_strided(hs + Cfg::kH, 128, (N / 8) * 128);
+                    if (wide_off) {
 #pragma unroll
-                    for (int ks = 0; ks < N / 16; ++ks) {
-                        const uint64_t dc = tc::desc_sw128(cb + (uint32_t)(ks >> 2) * 128 * 128 + (uint32_t)(ks & 3) * 32, 16, 1024);
-                        tc::mma_bf16(tYo, dc, dhh + ks * 16u, id_off, ks > 0 ? 1u : 0u);
-                        tc::mma_bf16(tYo, dc, dhl + ks * 16u, id_off, 1u);
+                        for (int ks = 0; ks < N / 16; ++ks) {
+                            const uint64_t dc = tc::desc_sw128(cb + (uint32_t)(ks >> 2) * 128 * 128 + (uint32_t)(ks & 3) * 32, 16, 1024);
+                            tc::mma_bf16(tYo, dc, dhh + ks * 16u, id_off_wide, ks > 0 ? 1u : 0u);
+                        }
+                    } else {
+#pragma unroll
+                        for (int ks = 0; ks < N / 16; ++ks) {
+                            const uint64_t dc = tc::desc_sw128(cb + (uint32_t)(ks >> 2) * 128 * 128 + (uint32_t)(ks & 3) * 32, 16, 1024);
+                            tc::mma_bf16(tYo, dc, dhh + ks * 16u, id_off, ks > 0 ? 1u : 0u);
+                            tc::mma_bf16(tYo, dc, dhl + ks * 16u, id_off, 1u);
+                        }
                     }
                     tc::mma_commit(&sh.h_empty[hbuf(hi)]);  // the h tiles may be replaced
                 }
@@ -384,12 +405,20 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
             const int ab = hi & 1;
             pipe_wait(sh, &sh.acc_full[ab], (hi >> 1) & 1);
             tc::fence_after_sync();
-            const uint32_t tYd = tmem + 256 + 128 * ab, tYo = tYd + 64;
+            const uint32_t tYd = t_yd(ab), tYo = t_yo(ab);
             const int p0 = 16 * cq;
             uint32_t yd[16], yo[16];
             tc::tmem_ld16_async(tYd + lane_base + (uint32_t)p0, yd);
             tc::tmem_ld16_async(tYo + lane_base + (uint32_t)p0, yo);
             tc::tmem_wait_ld();
+            if (wide_off) {
+                // C h_lo sits 64 columns after C h_hi
+                uint32_t yl[16];
+                tc::tmem_ld16_async(tYo + 64 + lane_base + (uint32_t)p0, yl);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) yo[j] = __float_as_uint(__uint_as_float(yo[j]) + __uint_as_float(yl[j]));
+            }
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.acc_empty[ab]);  // the MMAs of head hi + 2 may overwrite them
