@@ -118,7 +118,8 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* mb) {
 // Named barrier of the compute warps only.
 __device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
 
-// grid (nchunks * Q/128, H / heads_per_cta, batch); 18 warps; one CTA per SM.
+// grid (nchunks * Q/128 * H / heads_per_cta, batch): blockIdx.x = (chunk * Q/128 + half) *
+// (H / heads_per_cta) + head block; 18 warps; one CTA per SM.
 // Warps 0-15 build M' and run the epilogues (warp w: TMEM lanes 32*(w%4).., column
 // quarter w/4 of each part); warp 16 issues the MMAs; warp 17 issues the TMA copies.
 template <int N, bool GATE, bool XS>
@@ -133,15 +134,16 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int Q = (int)a.Q;
     const int halves = Q / 128;
-    const int64_t c = blockIdx.x / halves;
-    const int rh = blockIdx.x % halves;
-    const int b = blockIdx.z;
+    const int nhb = (int)(a.H / heads_per_cta);
+    const int64_t c = (blockIdx.x / nhb) / halves;
+    const int rh = (int)((blockIdx.x / nhb) % halves);
+    const int b = blockIdx.y;
     const int len = (int)min((int64_t)Q, a.T - c * a.Q);
     const int t0 = 128 * rh;
     if (t0 >= len) return;      // no valid rows in this half (uniform over the CTA)
     const int SW = t0 + 128;    // columns s of G this half needs (causal)
     const int nparts = SW / KPC;
-    const int hbeg = blockIdx.y * heads_per_cta;
+    const int hbeg = (int)(blockIdx.x % nhb) * heads_per_cta;
     const int nh = heads_per_cta;
     const int g = hbeg / (int)(a.H / a.G);
     const int row0 = (int)(c * a.Q);  // first token of the chunk within its sequence
@@ -572,7 +574,9 @@ cudaError_t launch_scan(const SsdTcArgs& s, int64_t batch, cudaStream_t stream) 
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmemTotal);
     if (e != cudaSuccess) return e;
     const int hpc = scan_heads_per_cta(s, batch);
-    const dim3 grid((unsigned)(s.nchunks * (s.Q / 128)), (unsigned)(s.H / hpc), (unsigned)batch);
+    // the head blocks of a chunk half are adjacent in launch order: they run together and
+    // read its C and B rows once from DRAM and then from L2
+    const dim3 grid((unsigned)(s.nchunks * (s.Q / 128) * (s.H / hpc)), (unsigned)batch);
     cudaEvent_t t0 = timing_begin(stream, "ssd_scan_tc");
     kern<<<grid, kCtaThreads, Cfg::kSmemTotal, stream>>>(s, hpc, status, tx, txl, tmc, tmb, tmo);
     note_launch("ssd_scan_tc", stream, t0);

@@ -86,8 +86,13 @@ __device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint3
     lo = bf16pair(l.x, l.y);
 }
 
-// grid (nchunks, H / hpc, batch); 10 warps.  Heads [hpc * blockIdx.y, +hpc) (hpc even,
-// a divisor of the heads of a group) of chunk blockIdx.x.
+// grid (nchunks * H / hpc, batch); 10 warps.  Each CTA takes heads [hpc * block, +hpc)
+// (hpc even, a divisor of the heads of a group) of one chunk.  At dstate 256, where a
+// chunk's B rows are half as many bytes as a CTA's x rows, blockIdx.x = chunk * (H / hpc)
+// + head block: the head blocks of a chunk run together and read its B rows once from
+// DRAM, then from L2 (c4 434 us against 453 with chunks adjacent).  Below that, blockIdx.x
+// = head block * nchunks + chunk (consecutive chunks of the same heads adjacent), which
+// measured faster there (c3 152 us against 156).
 //
 // ADJ: the adjoint chunk states of the backward pass instead,
 //   S^g_c[p, n] = sum_t exp(cum_t) dy_t[p] C_t[n]
@@ -108,9 +113,11 @@ __global__ void __launch_bounds__(kCta, 1)
     StateShared& sh = *reinterpret_cast<StateShared*>(smem + Cfg::kSmem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int Q = (int)a.Q;
-    const int64_t c = blockIdx.x;
-    const int hbeg = blockIdx.y * hpc;
-    const int b = blockIdx.z;
+    const int nhb = (int)(a.H / hpc);
+    constexpr bool kHeadsAdjacent = N > 128;
+    const int64_t c = kHeadsAdjacent ? (int64_t)(blockIdx.x / nhb) : (int64_t)blockIdx.x % a.nchunks;
+    const int hbeg = (int)(kHeadsAdjacent ? blockIdx.x % nhb : blockIdx.x / a.nchunks) * hpc;
+    const int b = blockIdx.y;
     const int len = (int)min((int64_t)Q, a.T - c * a.Q);
     const int g = hbeg / (int)(a.H / a.G);
     const int row0 = (int)(c * a.Q);
@@ -408,7 +415,7 @@ cudaError_t launch_state(const SsdTcArgs& s, int64_t batch, cudaStream_t stream)
     if (e != cudaSuccess) return e;
     const int hpc = state_heads_per_cta(s);
     cudaEvent_t t0 = timing_begin(stream, ADJ ? "ssd_state_tc (adjoint)" : "ssd_state_tc");
-    kern<<<dim3((unsigned)s.nchunks, (unsigned)(s.H / hpc), (unsigned)batch), kCta, Cfg::kSmemTotal, stream>>>(
+    kern<<<dim3((unsigned)(s.nchunks * (s.H / hpc)), (unsigned)batch), kCta, Cfg::kSmemTotal, stream>>>(
         s, hpc, status, tx, txl, tb);
     note_launch(ADJ ? "ssd_state_tc (adjoint)" : "ssd_state_tc", stream, t0);
     return cudaGetLastError();
