@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(kThreads) ssd_state_pass(const SsdArgs a) {
 // h_{c-1} back in place as bf16 hi = bf16(h) and lo = bf16(h - hi), so the scan kernel
 // copies the tiles straight into shared memory.  Initial and final states are fp32 in
 // the plain (b, H, P, N) layout.  grid: (ceil(P*N / 8 / 256), H, b).
-constexpr int kPassAheadSplit = 4;
+constexpr int kPassAheadSplit = 2;
 
 __global__ void __launch_bounds__(kThreads) ssd_state_pass_split(const SsdArgs a) {
     // units in memory order: unit u sits at byte 16 u of each half, so consecutive
