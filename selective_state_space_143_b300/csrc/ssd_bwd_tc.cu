@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(256) ssd_bwd_dy(const DyArgs a) {
 // the chunk-state kernel): reads S^g_c, writes R_c = dL/dh_out(c) as bf16 hi/lo tiles,
 // R_{c-1} = exp(cum_last(c)) R_c + S^g_c, and dinitial_state = R_{-1}.  grid (ceil(P*N / 8 / 256), H, b); a thread owns the 8 values
 // (p, n..n+7) of one 16-byte unit, as the forward carry does.
-constexpr int kRevAhead = 4;
+constexpr int kRevAhead = 2;
 
 struct RevArgs {
     float* ast;
