@@ -38,7 +38,7 @@ constexpr int kCompute = 8;                 // compute warps
 constexpr int kMma = 8, kLoad = 9;          // MMA and TMA warps
 constexpr int kCta = 32 * 10;
 constexpr int kMaxHeads = 8;
-constexpr int kXStages = 3;
+constexpr int kXStagesMax = 5;
 
 template <int N, bool XS>
 struct StateCfg {
@@ -49,6 +49,9 @@ struct StateCfg {
     static constexpr uint32_t kXStage = 2 * PL * kXHead;     // two heads, every plane
     static constexpr uint32_t kXt = 128u * KS * 2;           // one Xw part, hi or lo
     static constexpr uint32_t kW = kMaxHeads * 256 * 4;      // weights w[head][s]
+    // x stages in flight: 5 at dstate 256 with one x plane (c4 chunk states 433 -> 410 us
+    // against 3), 3 otherwise (more measured slower at dstate 128: c3 154 -> 160 us)
+    static constexpr int kXStages = N > 128 && PL == 1 ? 5 : 3;
     static constexpr uint32_t kSmem = kB + kXStages * kXStage + 4 * kXt + kW;
     static constexpr uint32_t kSmemTotal = kSmem + 512;      // + pipeline state
     static_assert(kSmemTotal <= 232448, "shared memory");
@@ -56,7 +59,7 @@ struct StateCfg {
 
 struct __align__(16) StateShared {
     uint64_t mb_b;              // B rows
-    uint64_t x_full[kXStages], x_empty[kXStages];
+    uint64_t x_full[kXStagesMax], x_empty[kXStagesMax];
     uint64_t xt_full[2], xt_empty[2];
     uint64_t acc_full[2], acc_empty[2];
     float warp_sum[kCompute][kMaxHeads];
@@ -108,6 +111,7 @@ __global__ void __launch_bounds__(kCta, 1)
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char* sB = smem;                                    // [n/64][s 256][64] swizzled
     unsigned char* sXr = smem + Cfg::kB;                         // [stage][head 2][plane][s KS][64] swizzled
+    constexpr int kXStages = Cfg::kXStages;
     unsigned char* sXt = sXr + kXStages * Cfg::kXStage;          // [buffer 2][hi, lo] MN-major A, no swizzle
     float* sW = reinterpret_cast<float*>(sXt + 4 * Cfg::kXt);    // [head][s]
     StateShared& sh = *reinterpret_cast<StateShared*>(smem + Cfg::kSmem);
