@@ -546,13 +546,14 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t T, uint
 
 // Heads per CTA: G = C B^T and the C and B rows are shared by the CTA's heads, and each
 // CTA pays a prologue (the C and B copies, G's MMAs) that nothing overlaps, so a CTA takes
-// as many heads of its group as keep at least six waves of CTAs on the GPU (up to 32).
+// as many heads of its group as keep at least six waves of CTAs on the GPU, up to 16 (32
+// measured slower: c4 scan 900 us against 882 with 16; c3 353 against 348; 8 on c3 357).
 int scan_heads_per_cta(const SsdTcArgs& s, int64_t batch) {
     const int hpg = (int)(s.H / s.G);
     const int64_t halves = s.nchunks * (s.Q / 128) * batch;
     const int64_t want = 6 * (int64_t)sm_count();
     int best = 1;
-    for (int cand : {1, 2, 4, 8, 16, 32})
+    for (int cand : {1, 2, 4, 8, 16})
         if (hpg % cand == 0 && (cand == 1 || halves * (s.H / cand) >= want)) best = cand;
     return best;
 }
