@@ -55,10 +55,10 @@ int bwd_entries(int64_t N) { return N <= 32 ? 1 : N <= 64 ? 2 : N <= 128 ? 4 : 8
 
 // Time parts: the SSM_TUNE_BWD_PARTS override when set.  Otherwise one part when the channels
 // give at least 8 warps per SM sub-partition (measured on B300: more parts only add the
-// summary pass), else enough parts for ~32 warps per sub-partition, at most 16 and at
-// least two checkpoint segments each (c1 backward: 1 part 1.15 ms, 4 parts 0.78 ms, 8-16
-// parts 0.72 ms).  Each part is a whole number of checkpoint segments; the part count is
-// recomputed from that length.
+// summary pass), else enough parts for ~48 warps per sub-partition, at most 16 and at
+// least two checkpoint segments each (c2 backward: 8 parts 11.6 ms, 12 parts 11.2 ms, 16
+// parts 11.4 ms; c1: 4 parts 0.40 ms, 12-16 parts 0.34 ms).  Each part is a whole number
+// of checkpoint segments; the part count is recomputed from that length.
 struct BwdPlan {
     int lpc, r, seg;  // lanes per channel, entries per lane, checkpoint segment length
     int64_t nseg, subs_per_part;
@@ -102,7 +102,7 @@ BwdPlan bwd_plan(const ScanArgs& a) {
     const int64_t warps = (int64_t)a.batch * a.nheads * a.headdim * p.lpc / 32;
     int64_t rule = 1;
     if (warps > 0 && warps < 8 * smsp)
-        rule = std::min<int64_t>({16, (32 * smsp + warps - 1) / warps, std::max<int64_t>(1, p.nseg / 2)});
+        rule = std::min<int64_t>({16, (48 * smsp + warps - 1) / warps, std::max<int64_t>(1, p.nseg / 2)});
     const int64_t want = std::max<int64_t>(1, std::min<int64_t>(knob > 0 ? knob : rule, std::max<int64_t>(p.nseg, 1)));
     p.subs_per_part = std::max<int64_t>(1, (p.nseg + want - 1) / want);
     p.parts = (int)std::max<int64_t>(1, (p.nseg + p.subs_per_part - 1) / p.subs_per_part);
