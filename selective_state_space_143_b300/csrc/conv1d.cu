@@ -25,7 +25,7 @@ namespace ssm {
 namespace {
 
 constexpr int kConvThreads = 256;
-constexpr int kConvTT = 16;  // steps per thread
+constexpr int kConvTT = 32;  // steps per thread (c3 pass: 16 -> 197 us, 32 -> 177, 64 -> 171; c4: 388, 339, 325)
 constexpr int kConvVX = 32;  // channel vectors per block
 constexpr int kConvTY = kConvThreads / kConvVX;  // step blocks per block
 
