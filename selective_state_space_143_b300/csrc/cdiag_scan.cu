@@ -39,7 +39,9 @@ namespace {
 constexpr int kCTT = 16;       // time steps per tile
 constexpr int kCStages = 3;    // cp.async ring
 constexpr int kCThreads = 128;
-constexpr int kEPL = 4;        // complex entries per lane
+constexpr int kEPL = 4;        // complex entries per lane (the B/C tile reads below take
+                               // exactly four: two float4 of (re, im) pairs)
+static_assert(kEPL == 4, "the recurrence loads a lane's B and C entries as two float4");
 constexpr float kTwoPi = 6.283185307179586f;
 constexpr float kInvTwoPi = 0.15915494309189535f;
 
