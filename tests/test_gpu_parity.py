@@ -129,6 +129,8 @@ SSD_CASES = [
     ("bf16", 1, 150, 1, 256, 16, 1, 64),   # largest head dimension (P = 256)
     ("f32", 1, 70, 2, 16, 256, 1, 32),     # largest state (N = 256), fp32
     ("bf16", 1, 300, 4, 64, 128, 4, 256),  # one group per head
+    ("bf16", 2, 777, 8, 64, 256, 1, 128),  # dstate 256 at chunk 128: every CTA a first half, ragged end
+    ("bf16", 1, 1000, 16, 64, 256, 2, 256),  # dstate 256, two groups of 8 heads, ragged end
 ]
 
 
