@@ -143,6 +143,21 @@ def test_ssd_shapes(case):
     compare(w, inp, y, fs)
 
 
+@pytest.mark.parametrize("N,chunk", [(128, 256), (256, 256), (256, 128)])
+def test_ssd_strong_and_weak_decay_heads(N, chunk):
+    """Heads that barely decay within a chunk beside heads whose cumulative sums fall to
+    the hundreds within a chunk (exp(cum_t - cum_s) spanning the whole fp32 range), in
+    one launch: M' must stay exact where the decay underflows, with no overflow where it
+    does not."""
+    w, inp = random_inputs("ssd", "bf16", 1, 700, 8, 64, N, seed=N + chunk)
+    w = w.replace(chunk=chunk)
+    bias = inp["dt_bias"].clone()
+    bias[::2] = 1.0  # Delta ~ 1.3-2.4: cumulative sums of -100s within a chunk
+    inp["dt_bias"] = bias
+    y, fs = run_gpu(inp, w)
+    compare(w, inp, y, fs)
+
+
 @pytest.mark.parametrize("mode", ["diag", "ssd"])
 def test_delta_zero_gives_skip_only(mode):
     if mode == "diag":
